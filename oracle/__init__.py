@@ -1,0 +1,230 @@
+"""fp64 CPU oracle for vocab-wide logprobs, entropy, KL and fused linear logp.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / ``--impl reference`` leg may import this package.
+The product path (``vocab_wide_logprobs_gb300``) never imports it, and the two
+share no code: this module loads ``vp_oracle.c`` (plain C, fp64, OpenMP over
+rows) through ctypes and passes it numpy float64 arrays.
+
+Every function takes exact fp64 copies of the inputs (bf16 / fp32 values upcast
+without rounding) as C-contiguous ``[N, V]`` arrays and returns fp64 results.
+The definitions each C function writes out, and the readings R1-R5 it takes
+where the pages are silent, are listed at the top of ``vp_oracle.c``.
+
+Parity unpinned: nothing. Every function here is pinned by ``tests/test_oracle_*``
+(Decimal brute force, closed forms, finite differences, invariants, shard
+merges, hand-built special rows).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "vp_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libvp_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+REVERSE = 0  # KL(A || B)
+FORWARD = 1  # KL(B || A)
+ERR_TARGET = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile vp_oracle.c with gcc into oracle/libvp_oracle.so (OpenMP if available)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-Wall", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:4] + ["-fopenmp"] + base[4:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_SIGS = {
+    "vpo_num_threads": ([], ctypes.c_int),
+    "vpo_logprobs_fwd": (["P", "I", "I", "I", "P", "P", "P", "P", "P"], None),
+    "vpo_logprobs_bwd": (["P", "I", "I", "I", "P", "P", "P"], None),
+    "vpo_entropy_fwd": (["P", "I", "I", "P", "P", "P"], None),
+    "vpo_entropy_bwd": (["P", "I", "I", "P", "P"], None),
+    "vpo_kl_fwd": (["P", "P", "I", "I", "i", "P", "P", "P", "P", "P"], None),
+    "vpo_kl_bwd": (["P", "P", "I", "I", "i", "P", "P", "P"], None),
+    "vpo_entropy_sharded": (["P", "I", "I", "P", "i", "P"], None),
+    "vpo_kl_sharded": (["P", "P", "I", "I", "i", "P", "i", "P"], None),
+    "vpo_linear_logits": (["P", "P", "I", "I", "I", "P"], None),
+    "vpo_linear_logp_fwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P", "P"], None),
+    "vpo_linear_logp_bwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P"], None),
+}
+_CT = {"P": ctypes.c_void_p, "I": ctypes.c_int64, "i": ctypes.c_int}
+
+
+def load_library(path: str):
+    """ctypes handle on a compiled oracle library with every signature declared."""
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = [_CT[a] for a in args]
+        fn.restype = res
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def num_threads(lib=None) -> int:
+    """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all host cores)."""
+    return (lib or _load()).vpo_num_threads()
+
+
+def _f64(a) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a
+
+
+def _i64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _shape(x):
+    if x.ndim != 2:
+        raise ValueError("oracle inputs are [N, V] arrays")
+    return x.shape
+
+
+def logprobs_fwd(x, targets, vocab_start=0, lib=None):
+    """Returns (logp, m, logS, err) for rows of x; targets are global ids."""
+    x = _f64(x)
+    N, V = _shape(x)
+    t = _i64(targets)
+    logp, m, logS = (np.empty(N) for _ in range(3))
+    err = np.zeros(1, dtype=np.int32)
+    (lib or _load()).vpo_logprobs_fwd(_p(x), N, V, vocab_start, _p(t), _p(logp), _p(m), _p(logS), _p(err))
+    return logp, m, logS, int(err[0])
+
+
+def logprobs_bwd(x, targets, g, vocab_start=0, lib=None):
+    x = _f64(x)
+    N, V = _shape(x)
+    t, g = _i64(targets), _f64(g)
+    dx = np.empty((N, V))
+    (lib or _load()).vpo_logprobs_bwd(_p(x), N, V, vocab_start, _p(t), _p(g), _p(dx))
+    return dx
+
+
+def entropy_fwd(x, lib=None):
+    """Returns (H, m, logS)."""
+    x = _f64(x)
+    N, V = _shape(x)
+    H, m, logS = (np.empty(N) for _ in range(3))
+    (lib or _load()).vpo_entropy_fwd(_p(x), N, V, _p(H), _p(m), _p(logS))
+    return H, m, logS
+
+
+def entropy_bwd(x, g, lib=None):
+    x = _f64(x)
+    N, V = _shape(x)
+    g = _f64(g)
+    dx = np.empty((N, V))
+    (lib or _load()).vpo_entropy_bwd(_p(x), N, V, _p(g), _p(dx))
+    return dx
+
+
+def kl_fwd(a, b, direction=REVERSE, lib=None):
+    """Returns (kl, ma, logSa, mb, logSb); reverse = KL(A||B), forward = KL(B||A)."""
+    a, b = _f64(a), _f64(b)
+    N, V = _shape(a)
+    if b.shape != a.shape:
+        raise ValueError("a and b differ in shape")
+    kl, ma, lsa, mb, lsb = (np.empty(N) for _ in range(5))
+    (lib or _load()).vpo_kl_fwd(_p(a), _p(b), N, V, int(direction), _p(kl), _p(ma), _p(lsa), _p(mb), _p(lsb))
+    return kl, ma, lsa, mb, lsb
+
+
+def kl_bwd(a, b, g, direction=REVERSE, lib=None):
+    """Returns (dA, dB) of g * KL in the given direction."""
+    a, b = _f64(a), _f64(b)
+    N, V = _shape(a)
+    g = _f64(g)
+    da, db = np.empty((N, V)), np.empty((N, V))
+    (lib or _load()).vpo_kl_bwd(_p(a), _p(b), N, V, int(direction), _p(g), _p(da), _p(db))
+    return da, db
+
+
+def entropy_sharded(x, cuts, lib=None):
+    """Entropy from per-shard (m, S, W) merged by re-centring on the row max."""
+    x = _f64(x)
+    N, V = _shape(x)
+    c = _i64(cuts)
+    if c[0] != 0 or c[-1] != V or len(c) - 1 > 64:
+        raise ValueError("cuts must run from 0 to V with at most 64 shards")
+    H = np.empty(N)
+    (lib or _load()).vpo_entropy_sharded(_p(x), N, V, _p(c), len(c) - 1, _p(H))
+    return H
+
+
+def kl_sharded(a, b, cuts, direction=REVERSE, lib=None):
+    a, b = _f64(a), _f64(b)
+    N, V = _shape(a)
+    c = _i64(cuts)
+    if c[0] != 0 or c[-1] != V or len(c) - 1 > 64:
+        raise ValueError("cuts must run from 0 to V with at most 64 shards")
+    kl = np.empty(N)
+    (lib or _load()).vpo_kl_sharded(_p(a), _p(b), N, V, int(direction), _p(c), len(c) - 1, _p(kl))
+    return kl
+
+
+def linear_logits(h, W, lib=None):
+    """fp64 logits h . W^T (materialised; for small cases only)."""
+    h, W = _f64(h), _f64(W)
+    N, D = h.shape
+    V = W.shape[0]
+    out = np.empty((N, V))
+    (lib or _load()).vpo_linear_logits(_p(h), _p(W), N, V, D, _p(out))
+    return out
+
+
+def linear_logp_fwd(h, W, targets, vocab_start=0, lib=None):
+    """Returns (logp, m, logS, err) of logits h . W^T, one fp64 logits row at a time."""
+    h, W = _f64(h), _f64(W)
+    N, D = h.shape
+    V = W.shape[0]
+    if W.shape[1] != D:
+        raise ValueError("hidden and weight disagree on D")
+    t = _i64(targets)
+    logp, m, logS = (np.empty(N) for _ in range(3))
+    scratch = np.empty((max(1, num_threads(lib)), V))
+    err = np.zeros(1, dtype=np.int32)
+    (lib or _load()).vpo_linear_logp_fwd(_p(h), _p(W), N, V, D, vocab_start, _p(t), _p(logp), _p(m),
+                                _p(logS), _p(scratch), _p(err))
+    return logp, m, logS, int(err[0])
+
+
+def linear_logp_bwd(h, W, targets, g, vocab_start=0, want_dh=True, want_dW=True, lib=None):
+    """Returns (dhidden, dW) of sum_r g_r logp_r; either is None when not wanted."""
+    h, W = _f64(h), _f64(W)
+    N, D = h.shape
+    V = W.shape[0]
+    t, g = _i64(targets), _f64(g)
+    dh = np.empty((N, D)) if want_dh else None
+    dW = np.empty((V, D)) if want_dW else None
+    dz = np.empty((N, V))
+    (lib or _load()).vpo_linear_logp_bwd(_p(h), _p(W), N, V, D, vocab_start, _p(t), _p(g), _p(dh),
+                                _p(dW), _p(dz))
+    return dh, dW

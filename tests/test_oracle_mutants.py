@@ -1,0 +1,83 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Each mutant is a one-place edit of ``oracle/vp_oracle.c`` (a dropped term, a
+flipped sign, a wrong index or operand, a missing guard) compiled into a
+temporary library on the CPU. The real oracle source is never modified.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+from tests import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "vp_oracle.c")
+
+MUTANTS = [
+    ("entropy sign", "if (p > 0.0) H -= p * lp;", "if (p > 0.0) H += p * lp;"),
+    ("entropy zero-weight guard dropped", "if (p > 0.0) H -= p * lp;", "H -= p * lp;"),
+    ("log p adds log S", "return (zj - s->m) - s->logS;", "return (zj - s->m) + s->logS;"),
+    ("sum-exp not centred", "s.S += exp(v - s.m);", "s.S += exp(v);"),
+    ("NaN entries not flagged", "if (isnan(v) || v == INFINITY) s.bad = 1;", "if (v == INFINITY) s.bad = 1;"),
+    ("logprobs ignored target not zero", "if (t < 0) { logp[r] = 0.0; continue; }",
+     "if (t < 0) { logp[r] = NAN; continue; }"),
+    ("vocab_start added", "int64_t loc = t - vocab_start;\n        if (loc < 0 || loc >= V) { logp[r] = NAN;",
+     "int64_t loc = t + vocab_start;\n        if (loc < 0 || loc >= V) { logp[r] = NAN;"),
+    ("logprobs bwd sign", "d[j] = g[r] * (onehot - p);", "d[j] = g[r] * (p - onehot);"),
+    ("logprobs bwd onehot dropped", "d[j] = g[r] * (onehot - p);", "d[j] = g[r] * (0.0 - p);"),
+    ("entropy bwd drops +H", "d[j] = (p > 0.0) ? -g[r] * p * (lp + H) : 0.0;",
+     "d[j] = (p > 0.0) ? -g[r] * p * lp : 0.0;"),
+    ("entropy bwd sign", "d[j] = (p > 0.0) ? -g[r] * p * (lp + H) : 0.0;",
+     "d[j] = (p > 0.0) ? g[r] * p * (lp + H) : 0.0;"),
+    ("KL wrong operand", "if (p > 0.0) kl += p * (lp - log_prob(Q[j], sq));",
+     "if (p > 0.0) kl += p * (lp - log_prob(P[j], sq));"),
+    ("KL direction swapped", "kl[r] = direction == 0 ? kl_row(A, B, V, &sa, &sb)",
+     "kl[r] = direction == 1 ? kl_row(A, B, V, &sa, &sb)"),
+    ("mismatch test swapped", "if (P[j] > -INFINITY && Q[j] == -INFINITY) return 1;",
+     "if (Q[j] > -INFINITY && P[j] == -INFINITY) return 1;"),
+    ("mismatch ignored", "if (mismatch(P, Q, V)) return INFINITY;", ""),
+    ("KL dQ sign", "if (dQ) dQ[j] = g * (q - p);", "if (dQ) dQ[j] = g * (p - q);"),
+    ("KL dP drops -KL", "else dP[j] = (p > 0.0) ? g * p * (lp - lq - kl) : 0.0;",
+     "else dP[j] = (p > 0.0) ? g * p * (lp - lq) : 0.0;"),
+    ("KL bwd direction swapped", "if (direction == 0) kl_bwd_row(A, B, V, g[r], dA, dB);",
+     "if (direction == 1) kl_bwd_row(A, B, V, g[r], dA, dB);"),
+    ("merge drops re-centring", "W += alpha * (parts[s].W - (m - parts[s].m) * parts[s].S);",
+     "W += alpha * parts[s].W;"),
+    ("merge zero-weight skip dropped", "if (w == 0.0) continue;                  /* zero-weight shard skipped */", ""),
+    ("KL merge shift sign", "W += ap * (parts[s].W - (dp - dq) * parts[s].Sp);",
+     "W += ap * (parts[s].W - (dp + dq) * parts[s].Sp);"),
+    ("linear logits transposed", "acc += h[r * D + k] * W[j * D + k];", "acc += h[r * D + k] * W[k * V + j];"),
+    ("linear dW wrong row", "out[k] += c * h[r * D + k];", "out[k] += c * h[((r + 1) % N) * D + k];"),
+    ("linear dh wrong vocab row", "out[k] += c * W[j * D + k];", "out[k] += c * W[((j + 1) % V) * D + k];"),
+    ("linear bwd onehot dropped", "z[j] = g[r] * (((j == loc) ? 1.0 : 0.0) - p);", "z[j] = g[r] * (0.0 - p);"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="gcc not available")
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(source, tmp_path, name, old, new):
+    assert source.count(old) >= 1, f"mutation site not found: {old!r}"
+    mutated = source.replace(old, new, 1)
+    c = tmp_path / "mutant.c"
+    c.write_text(mutated)
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-fPIC", "-shared", "-std=c11", "-fopenmp", str(c), "-o", str(so), "-lm"],
+                   check=True, capture_output=True)
+    lib = oracle.load_library(str(so))
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except (ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"mutant '{name}' passed every pin"
