@@ -1,0 +1,179 @@
+/*
+ * vp.h -- C ABI of libvp: vocab-wide logprobs, entropy and KL on one GB300.
+ *
+ * Sources cited below:
+ *   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL"
+ *        (DeepSpeed pull request 8838).
+ *   [P2] page "[Feat][Kernel] Add TP Fused linear logp Triton" (RL-Kernel pull
+ *        request 208).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every array argument is a DEVICE pointer owned by the caller; the
+ *   library never allocates, frees, copies to the host or synchronises. The
+ *   arrays must stay alive until the work queued on `stream` has finished.
+ *   `stream` is a cudaStream_t (NULL = the legacy default stream); all work is
+ *   queued on it in call order and the call returns without waiting.
+ *
+ * Rows.  An input holds N rows of V logits. Row r (0 <= r < N) starts at
+ *   element offset (r / R) * s_o + (r % R) * s_i from the base pointer and its
+ *   V logits are consecutive (unit stride) [P1, second commit message: "rows
+ *   are addressed with up to two strides, so a slice such as logits[:, :-1]
+ *   is read in place"]. Strides and R are counted in elements. A contiguous
+ *   [N, V] input is R = N, s_i = V (s_o is then unused). For logits[:, :-1]
+ *   of a contiguous [B, T, V] tensor: N = B (T - 1), R = T - 1, s_o = T V,
+ *   s_i = V. Inputs that need more than two strides must be copied by the
+ *   caller.
+ *
+ * Dtypes.  VP_F32 or VP_BF16 logits. Arithmetic is fp32 throughout. Per-row
+ *   outputs and saved statistics are fp32. Gradients are written contiguous,
+ *   [N, V] row-major, in the dtype of the logits, rounded to nearest even
+ *   [P1, second commit message: "gradients are returned contiguous"; the
+ *   reviewer's note that the bf16 gradient equals the round-to-nearest-even
+ *   of the fp32 one].
+ *
+ * Saved statistics.  Forward calls return, per row and input, the row max m
+ *   and logS = log sum_j exp(z_j - m); backward calls take them back. The sum
+ *   lse = m + logS is never formed, so a large common offset does not round
+ *   away the centred logits [P1, second commit message: "centring on the max
+ *   keeps a large common offset from cancelling in fp32"]. For a row whose
+ *   logits are all -inf, m is -FLT_MAX and logS is -inf.
+ *
+ * Per-row special values (the pages state the cases, not all outcomes; these
+ *   are the readings the library implements):
+ *   - a NaN or +inf logit in a used row: output NaN, gradient row NaN;
+ *   - an all -inf row (the P row for KL): output NaN, gradient row NaN;
+ *   - KL(P||Q) with some P_j > -inf where Q_j = -inf ("support mismatch",
+ *     decided on the logits, even when p_j underflows) [P1, reviewer's
+ *     suggested change]: +inf; the dP row is NaN and dQ = g (q - p) stays
+ *     finite;
+ *   - terms whose weight is exactly 0 contribute exactly 0, so a one-hot row
+ *     spanning +-3e38 gives H = 0 and KL(p||p) = 0 with zero gradients [P1,
+ *     Codex thread "Guard zero rescaling before applying infinite shifts"].
+ *
+ * Targets.  int64 global token ids, one per row (contiguous, length N). The
+ *   local column is target - vocab_start. A negative target is ignored: logp
+ *   0 and a zero gradient row. A target >= 0 outside [vocab_start,
+ *   vocab_start + V) is a data error: that row's output (and gradient row) is
+ *   NaN and bit VP_ERRBIT_TARGET is OR-ed into *err_word (a device int32,
+ *   may be NULL) with an atomic; nothing is reported on the host.
+ *
+ * Batch invariance.  The launch shape depends on V and the dtype only, so each
+ *   row's outputs and gradients are bitwise identical for any N and any other
+ *   rows in the batch [P1, maintainer's remark on batch invariance for RL
+ *   rollouts].
+ *
+ * Errors.  Every call returns a vp_status. Argument errors are found on the
+ *   host before anything is queued and leave the outputs untouched. N = 0 is
+ *   valid and queues nothing.
+ */
+#ifndef VP_H
+#define VP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define VP_API __attribute__((visibility("default")))
+#else
+#define VP_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *vp_stream; /* identical to cudaStream_t */
+
+typedef enum vp_status {
+    VP_OK = 0,
+    VP_ERR_NULL = 1,      /* a required pointer is NULL                              */
+    VP_ERR_SHAPE = 2,     /* N < 0, V < 1, V > 2^31 - 1, R < 1, D < 1, ...              */
+    VP_ERR_DTYPE = 3,     /* unknown dtype code                                      */
+    VP_ERR_LAYOUT = 4,    /* a negative stride                                       */
+    VP_ERR_ALIGN = 5,     /* a pointer not aligned to its element size (or 16 B for
+                             the linear-logp operands)                               */
+    VP_ERR_LAUNCH = 6,    /* the CUDA launch failed                                  */
+    VP_ERR_ARG = 7,       /* another invalid argument (direction, both gradients
+                             requested as NULL where one is required, ...)          */
+    VP_ERR_DEVICE = 8     /* no usable device, or not an sm_103 device               */
+} vp_status;
+
+typedef enum vp_dtype { VP_F32 = 0, VP_BF16 = 1 } vp_dtype;
+
+/* KL direction [P1: "reverse KL" / "forward KL"; the pages do not define them.
+ * Reading: A is the first argument (student / policy), reverse = KL(A||B),
+ * forward = KL(B||A).] */
+typedef enum vp_kl_direction { VP_KL_REVERSE = 0, VP_KL_FORWARD = 1 } vp_kl_direction;
+
+#define VP_ERRBIT_TARGET 1
+
+/* ------------------------------------------------------------------------ */
+/* Logprobs [P1, first commit message; P2, "Implementation"]                 */
+/* ------------------------------------------------------------------------ */
+
+/* logp[r] = (z_{r,t} - m_r) - logS_r for t = targets[r] - vocab_start, read in
+ * one pass over each row. Outputs: logp, m, logS (fp32 [N] each, required).
+ * err_word may be NULL. */
+VP_API vp_status vp_logprobs_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
+                          int64_t s_o, int64_t s_i, int64_t vocab_start,
+                          const int64_t *targets, float *logp, float *m, float *logS,
+                          int32_t *err_word, vp_stream stream);
+
+/* dx[r, j] = g[r] (onehot_{j,t} - p_{r,j}), p = exp((z - m) - logS), using
+ * the m / logS of vp_logprobs_fwd [P2, review nitpick on the chunked
+ * backward]. grad_out: fp32 [N]. dx: contiguous [N, V], dtype of x. */
+VP_API vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
+                          int64_t s_o, int64_t s_i, int64_t vocab_start,
+                          const int64_t *targets, const float *m, const float *logS,
+                          const float *grad_out, void *dx, int32_t *err_word,
+                          vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Entropy [P1, second commit message and reviewer's suggested change]      */
+/* ------------------------------------------------------------------------ */
+
+/* H[r] = log S - W / S from one read of the row, with the online max m,
+ * S = sum e^{z-m} and W = sum e^{z-m} (z - m). Outputs fp32 [N]: H, m, logS. */
+VP_API vp_status vp_entropy_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
+                         int64_t s_o, int64_t s_i, float *H, float *m, float *logS,
+                         vp_stream stream);
+
+/* dx[r, j] = -g[r] p_j (log p_j + H_r), exactly 0 where p_j = 0. */
+VP_API vp_status vp_entropy_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
+                         int64_t s_o, int64_t s_i, const float *m, const float *logS,
+                         const float *H, const float *grad_out, void *dx, vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* KL [P1, second commit message and reviewer's suggested change]           */
+/* ------------------------------------------------------------------------ */
+
+/* One read of A and B. With (P, Q) = (A, B) for VP_KL_REVERSE and (B, A) for
+ * VP_KL_FORWARD: KL = W / S_P - log S_P + log S_Q, where
+ * W = sum_j e^{P_j - m_P} ((P_j - m_P) - (Q_j - m_Q)), or +inf on a support
+ * mismatch. A and B share one row layout (R, s_o, s_i) and dtype.
+ * Outputs fp32 [N]: kl, and m / logS of A and of B (all required). */
+VP_API vp_status vp_kl_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R,
+                    int64_t s_o, int64_t s_i, int direction, float *kl, float *ma,
+                    float *logSa, float *mb, float *logSb, vp_stream stream);
+
+/* dP_j = g p_j (log p_j - log q_j - KL), dQ_j = g (q_j - p_j), mapped back to
+ * A and B by the direction. da and db are contiguous [N, V] in the dtype of
+ * the inputs; either may be NULL (that gradient is then neither computed nor
+ * written), not both. */
+VP_API vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R,
+                    int64_t s_o, int64_t s_i, int direction, const float *ma,
+                    const float *logSa, const float *mb, const float *logSb, const float *kl,
+                    const float *grad_out, void *da, void *db, vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Misc                                                                      */
+/* ------------------------------------------------------------------------ */
+VP_API const char *vp_status_string(int status);
+VP_API int vp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VP_H */

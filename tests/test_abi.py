@@ -1,0 +1,94 @@
+"""The C-ABI library: it loads, exports every entry point include/vp.h declares,
+and rejects bad arguments on the host before any device work (CPU-only checks)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from vocab_wide_logprobs_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vp.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_LAYOUT, ERR_ALIGN, ERR_LAUNCH, ERR_ARG, ERR_DEVICE = range(9)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"VP_API\s+[\w\s\*]*?\b(vp_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("vp_logprobs_fwd", "vp_logprobs_bwd", "vp_entropy_fwd", "vp_entropy_bwd", "vp_kl_fwd",
+              "vp_kl_bwd", "vp_status_string", "vp_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (vp_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    assert lib.vp_version() >= 1
+    assert _lib.status_string(ERR_ALIGN) == "misaligned pointer"
+
+
+def test_library_is_built_for_sm_103a():
+    # the fatbinary carries only sm_103a code (checked from the build flags, not by reading the binary)
+    from vocab_wide_logprobs_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+# ---------------------------------------------------------------------------
+# host-side argument checks: these return before any device is touched
+# ---------------------------------------------------------------------------
+FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: every call below fails its host checks
+FAKE_ODD = ctypes.c_void_p(0x100001)
+
+
+def ent_fwd(x=FAKE, dtype=1, N=4, V=16, R=4, s_o=0, s_i=16, H=FAKE, m=FAKE, logS=FAKE):
+    return _lib.lib().vp_entropy_fwd(x, dtype, N, V, R, s_o, s_i, H, m, logS, None)
+
+
+def test_status_codes_for_bad_arguments():
+    assert ent_fwd(dtype=7) == ERR_DTYPE
+    assert ent_fwd(N=-1) == ERR_SHAPE
+    assert ent_fwd(V=0) == ERR_SHAPE
+    assert ent_fwd(V=2**31) == ERR_SHAPE
+    assert ent_fwd(R=0) == ERR_SHAPE
+    assert ent_fwd(s_i=-16) == ERR_LAYOUT
+    assert ent_fwd(s_o=-1) == ERR_LAYOUT
+    assert ent_fwd(x=None) == ERR_NULL
+    assert ent_fwd(H=None) == ERR_NULL
+    assert ent_fwd(x=FAKE_ODD) == ERR_ALIGN
+    assert ent_fwd(m=FAKE_ODD) == ERR_ALIGN
+    assert ent_fwd(N=0, x=None, H=None, m=None, logS=None) == OK  # N = 0 queues nothing
+    L = _lib.lib()
+    args = (FAKE, FAKE, 1, 4, 16, 4, 0, 16)
+    assert L.vp_kl_fwd(*args, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == ERR_ARG
+    assert L.vp_kl_bwd(*args, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == ERR_ARG
+    assert L.vp_logprobs_fwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE_ODD, FAKE, FAKE, FAKE, None, None) == ERR_ALIGN
+    assert L.vp_logprobs_bwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE, FAKE, FAKE, FAKE, None, None, None) == ERR_NULL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device status; needs a machine without a GPU")
+def test_no_device_status_without_gpu():
+    assert ent_fwd() == ERR_DEVICE
+
+
+def test_binding_rejects_bad_layouts_before_calling():
+    from vocab_wide_logprobs_gb300 import VPError, rows_of
+    x = torch.zeros(4, 6, 16)
+    assert rows_of(x) == (24, 16, 6, 96, 16)
+    assert rows_of(x[:, :-1]) == (20, 16, 5, 96, 16)
+    assert rows_of(x[0]) == (6, 16, 6, 0, 16)
+    with pytest.raises(VPError):
+        rows_of(x.transpose(1, 2))
+    with pytest.raises(VPError):
+        rows_of(torch.zeros(3))

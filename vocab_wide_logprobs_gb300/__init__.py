@@ -1,9 +1,13 @@
 """Vocab-wide logprobs, entropy and KL (and fused linear logp) on GB300.
 
 The compute runs in ``libvp.so`` (hand-written CUDA for sm_103a behind a C-ABI,
-declared in ``include/vp.h``). This package is a thin ctypes binding: it turns
-torch tensors into pointers, sizes and strides and calls the C functions of the
-same names. There is no CPU fallback: every call raises if the library is
-missing or no CUDA device is present.
+declared in ``include/vp.h``). ``api`` is a thin ctypes binding with the same
+function names: it turns torch tensors into pointers, sizes and strides and
+calls the C functions. There is no CPU fallback: every call raises if the
+library cannot be built or loaded, or if no sm_103 device is present.
 """
-__all__ = ["workloads"]
+from .api import (KL_FORWARD, KL_REVERSE, VPError, rows_of, vp_entropy_bwd, vp_entropy_fwd, vp_kl_bwd,
+                  vp_kl_fwd, vp_logprobs_bwd, vp_logprobs_fwd)
+
+__all__ = ["KL_FORWARD", "KL_REVERSE", "VPError", "rows_of", "vp_entropy_bwd", "vp_entropy_fwd", "vp_kl_bwd",
+           "vp_kl_fwd", "vp_logprobs_bwd", "vp_logprobs_fwd"]

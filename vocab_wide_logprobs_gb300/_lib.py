@@ -1,0 +1,54 @@
+"""Loader of the in-tree libvp.so (the CUDA library) with every C signature declared.
+
+There is no fallback: if the library is missing it is built from csrc/ with
+nvcc (the same CUDA path), and if that fails the error propagates.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_handle = None
+
+P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+
+# name -> argument types (all return int status unless noted)
+SIGNATURES = {
+    "vp_logprobs_fwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P],
+    "vp_logprobs_bwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P, P],
+    "vp_entropy_fwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P],
+    "vp_entropy_bwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P, P, P],
+    "vp_kl_fwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
+    "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, P, P],
+}
+
+
+def path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libvp (building it first if it is absent or stale)."""
+    global _handle
+    with _lock:
+        if _handle is None:
+            so = _build.build()
+            h = ctypes.CDLL(so, mode=os.RTLD_NOW | getattr(os, "RTLD_LOCAL", 0))
+            for name, args in SIGNATURES.items():
+                fn = getattr(h, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            h.vp_status_string.argtypes = [ctypes.c_int]
+            h.vp_status_string.restype = ctypes.c_char_p
+            h.vp_version.argtypes = []
+            h.vp_version.restype = ctypes.c_int
+            _handle = h
+    return _handle
+
+
+def status_string(status: int) -> str:
+    return lib().vp_status_string(int(status)).decode()

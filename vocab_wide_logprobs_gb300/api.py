@@ -1,0 +1,144 @@
+"""ctypes binding of libvp: one Python function per C entry point, same names.
+
+Argument marshalling only: a function turns torch CUDA tensors into device
+pointers, sizes and the two row strides of ``include/vp.h``, allocates any
+output the caller did not pass (torch owns device memory), calls the C
+function on the current torch stream and raises ``VPError`` on a non-zero
+status. Every step of the computation runs in libvp's CUDA kernels; there is
+no CPU or PyTorch fallback, and a missing library or device raises.
+
+Row layouts accepted for logits (last stride must be 1):
+  * ``[N, V]``: any row stride (R = N, s_i = stride(0));
+  * ``[B, T, V]``: any two outer strides, e.g. ``logits[:, :-1]`` of a
+    contiguous ``[B, T + 1, V]`` tensor (N = B T, R = T, s_o = stride(0),
+    s_i = stride(1)).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+F32, BF16 = 0, 1
+KL_REVERSE, KL_FORWARD = 0, 1
+ERRBIT_TARGET = 1
+
+
+class VPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib.status_string(status)} (status {status})")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise VPError(3, f"dtype {t.dtype}")
+
+
+def rows_of(x: torch.Tensor):
+    """(N, V, R, s_o, s_i) of a [N, V] or [B, T, V] logits view with unit last stride."""
+    if x.dim() == 2:
+        N, V = x.shape
+        if V > 1 and x.stride(1) != 1:
+            raise VPError(4, "logits need a unit stride along V")
+        return N, V, max(N, 1), 0, x.stride(0)
+    if x.dim() == 3:
+        B, T, V = x.shape
+        if V > 1 and x.stride(2) != 1:
+            raise VPError(4, "logits need a unit stride along V")
+        return B * T, V, max(T, 1), x.stride(0), x.stride(1)
+    raise VPError(2, f"logits must be 2-D or 3-D, got {x.dim()}-D")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise VPError(status, where)
+
+
+def _f32(n, like):
+    return torch.empty(n, dtype=torch.float32, device=like.device)
+
+
+def _same_layout(a: torch.Tensor, b: torch.Tensor):
+    if a.shape != b.shape or a.stride() != b.stride() or a.dtype != b.dtype:
+        raise VPError(4, "A and B must share shape, strides and dtype")
+
+
+def vp_logprobs_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=None, m=None, logS=None):
+    """Returns (logp, m, logS), fp32 [N] each."""
+    N, V, R, s_o, s_i = rows_of(x)
+    logp = _f32(N, x) if logp is None else logp
+    m = _f32(N, x) if m is None else m
+    logS = _f32(N, x) if logS is None else logS
+    _check(_lib.lib().vp_logprobs_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
+                                      _ptr(logp), _ptr(m), _ptr(logS), _ptr(err_word), _stream()),
+           "vp_logprobs_fwd")
+    return logp, m, logS
+
+
+def vp_logprobs_bwd(x, targets, m, logS, grad, vocab_start: int = 0, err_word=None, dx=None):
+    """Returns dx, contiguous [N, V] in the dtype of x."""
+    N, V, R, s_o, s_i = rows_of(x)
+    dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
+    _check(_lib.lib().vp_logprobs_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
+                                      _ptr(m), _ptr(logS), _ptr(grad), _ptr(dx), _ptr(err_word), _stream()),
+           "vp_logprobs_bwd")
+    return dx
+
+
+def vp_entropy_fwd(x, H=None, m=None, logS=None):
+    """Returns (H, m, logS), fp32 [N] each."""
+    N, V, R, s_o, s_i = rows_of(x)
+    H = _f32(N, x) if H is None else H
+    m = _f32(N, x) if m is None else m
+    logS = _f32(N, x) if logS is None else logS
+    _check(_lib.lib().vp_entropy_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(H), _ptr(m), _ptr(logS),
+                                     _stream()), "vp_entropy_fwd")
+    return H, m, logS
+
+
+def vp_entropy_bwd(x, m, logS, H, grad, dx=None):
+    N, V, R, s_o, s_i = rows_of(x)
+    dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
+    _check(_lib.lib().vp_entropy_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(m), _ptr(logS), _ptr(H),
+                                     _ptr(grad), _ptr(dx), _stream()), "vp_entropy_bwd")
+    return dx
+
+
+def vp_kl_fwd(a, b, direction: int = KL_REVERSE, kl=None, ma=None, logSa=None, mb=None, logSb=None):
+    """Returns (kl, ma, logSa, mb, logSb); reverse = KL(A||B), forward = KL(B||A)."""
+    _same_layout(a, b)
+    N, V, R, s_o, s_i = rows_of(a)
+    kl, ma, logSa, mb, logSb = (_f32(N, a) if t is None else t for t in (kl, ma, logSa, mb, logSb))
+    _check(_lib.lib().vp_kl_fwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction), _ptr(kl),
+                                _ptr(ma), _ptr(logSa), _ptr(mb), _ptr(logSb), _stream()), "vp_kl_fwd")
+    return kl, ma, logSa, mb, logSb
+
+
+def vp_kl_bwd(a, b, direction, ma, logSa, mb, logSb, kl, grad, want_da=True, want_db=True, da=None, db=None):
+    """Returns (da, db); an unwanted gradient is None and is not computed."""
+    _same_layout(a, b)
+    N, V, R, s_o, s_i = rows_of(a)
+    if want_da and da is None:
+        da = torch.empty((N, V), dtype=a.dtype, device=a.device)
+    if want_db and db is None:
+        db = torch.empty((N, V), dtype=a.dtype, device=a.device)
+    da = da if want_da else None
+    db = db if want_db else None
+    _check(_lib.lib().vp_kl_bwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction), _ptr(ma),
+                                _ptr(logSa), _ptr(mb), _ptr(logSb), _ptr(kl), _ptr(grad), _ptr(da), _ptr(db),
+                                _stream()), "vp_kl_bwd")
+    return da, db

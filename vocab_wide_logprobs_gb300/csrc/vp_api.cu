@@ -1,0 +1,182 @@
+// vp_api.cu -- the extern "C" entry points declared in include/vp.h.
+//
+// Each entry point checks its arguments on the host (no device access, no
+// allocation, no synchronisation), fills a launcher argument block and queues
+// the kernel on the caller's stream. The launch shape is chosen from V and the
+// dtype alone.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "vp.h"
+#include "vp_launch.h"
+
+namespace {
+
+constexpr int64_t kMaxV = 2147483647LL;
+constexpr int64_t kMaxRowsPerLaunch = 2147483647LL;  // one CTA per row in the forward
+
+// 0 = unknown, 1 = sm_103, 2 = other
+std::atomic<int> g_dev_ok[64];
+
+vp_status check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VP_ERR_DEVICE;
+    if (dev < 0 || dev >= 64) return VP_ERR_DEVICE;
+    int known = g_dev_ok[dev].load(std::memory_order_relaxed);
+    if (known == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return VP_ERR_DEVICE;
+        known = (major == 10 && minor == 3) ? 1 : 2;
+        g_dev_ok[dev].store(known, std::memory_order_relaxed);
+    }
+    return known == 1 ? VP_OK : VP_ERR_DEVICE;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t elem_size(int dtype) { return dtype == VP_BF16 ? 2 : 4; }
+
+// Shared checks of the row description.
+vp_status check_rows(int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i) {
+    if (dtype != VP_F32 && dtype != VP_BF16) return VP_ERR_DTYPE;
+    if (N < 0 || N > kMaxRowsPerLaunch || V < 1 || V > kMaxV || R < 1) return VP_ERR_SHAPE;
+    if (s_o < 0 || s_i < 0) return VP_ERR_LAYOUT;
+    return VP_OK;
+}
+
+vp_status launched(cudaError_t e) { return e == cudaSuccess ? VP_OK : VP_ERR_LAUNCH; }
+
+}  // namespace
+
+extern "C" {
+
+vp_status vp_logprobs_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                          int64_t s_i, int64_t vocab_start, const int64_t *targets, float *logp,
+                          float *m, float *logS, int32_t *err_word, vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!x || !targets || !logp || !m || !logS) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(targets, 8) || !aligned(logp, 4) || !aligned(m, 4) ||
+        !aligned(logS, 4) || !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, targets, logp, m, logS, err_word,
+                    (cudaStream_t)stream};
+    return launched(vp::launch_logprobs_fwd(a));
+}
+
+vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                          int64_t s_i, int64_t vocab_start, const int64_t *targets, const float *m,
+                          const float *logS, const float *grad_out, void *dx, int32_t *err_word,
+                          vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!x || !targets || !m || !logS || !grad_out || !dx) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(dx, es) || !aligned(targets, 8) || !aligned(m, 4) || !aligned(logS, 4) ||
+        !aligned(grad_out, 4) || !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, m, logS, nullptr, grad_out, targets,
+                   dx, err_word, (cudaStream_t)stream};
+    return launched(vp::launch_logprobs_bwd(a));
+}
+
+vp_status vp_entropy_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
+                         float *H, float *m, float *logS, vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!x || !H || !m || !logS) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(H, 4) || !aligned(m, 4) || !aligned(logS, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, nullptr, H, m, logS, nullptr,
+                    (cudaStream_t)stream};
+    return launched(vp::launch_entropy_fwd(a));
+}
+
+vp_status vp_entropy_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
+                         const float *m, const float *logS, const float *H, const float *grad_out, void *dx,
+                         vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!x || !m || !logS || !H || !grad_out || !dx) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(dx, es) || !aligned(m, 4) || !aligned(logS, 4) || !aligned(H, 4) ||
+        !aligned(grad_out, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, m, logS, H, grad_out, nullptr, dx, nullptr,
+                   (cudaStream_t)stream};
+    return launched(vp::launch_entropy_bwd(a));
+}
+
+vp_status vp_kl_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                    int64_t s_i, int direction, float *kl, float *ma, float *logSa, float *mb, float *logSb,
+                    vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!a || !b || !kl || !ma || !logSa || !mb || !logSb) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(kl, 4) || !aligned(ma, 4) || !aligned(logSa, 4) ||
+        !aligned(mb, 4) || !aligned(logSb, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    const bool rev = direction == VP_KL_REVERSE;  // reverse: P = A, Q = B
+    vp::KLFwdArgs k{rev ? a : b, rev ? b : a, dtype == VP_BF16, N, V, R, s_o, s_i, kl,
+                    rev ? ma : mb, rev ? logSa : logSb, rev ? mb : ma, rev ? logSb : logSa,
+                    (cudaStream_t)stream};
+    return launched(vp::launch_kl_fwd(k));
+}
+
+vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                    int64_t s_i, int direction, const float *ma, const float *logSa, const float *mb,
+                    const float *logSb, const float *kl, const float *grad_out, void *da, void *db,
+                    vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (!da && !db) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!a || !b || !ma || !logSa || !mb || !logSb || !kl || !grad_out) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(da, es) || !aligned(db, es) || !aligned(ma, 4) ||
+        !aligned(logSa, 4) || !aligned(mb, 4) || !aligned(logSb, 4) || !aligned(kl, 4) ||
+        !aligned(grad_out, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    const bool rev = direction == VP_KL_REVERSE;
+    vp::KLBwdArgs k{rev ? a : b, rev ? b : a, dtype == VP_BF16, N, V, R, s_o, s_i,
+                    rev ? ma : mb, rev ? logSa : logSb, rev ? mb : ma, rev ? logSb : logSa, kl, grad_out,
+                    rev ? da : db, rev ? db : da, (cudaStream_t)stream};
+    return launched(vp::launch_kl_bwd(k));
+}
+
+const char *vp_status_string(int status) {
+    switch (status) {
+        case VP_OK: return "ok";
+        case VP_ERR_NULL: return "a required pointer is NULL";
+        case VP_ERR_SHAPE: return "invalid shape (N, V, R or D)";
+        case VP_ERR_DTYPE: return "unknown dtype";
+        case VP_ERR_LAYOUT: return "invalid row layout (negative stride)";
+        case VP_ERR_ALIGN: return "misaligned pointer";
+        case VP_ERR_LAUNCH: return "CUDA launch failed";
+        case VP_ERR_ARG: return "invalid argument";
+        case VP_ERR_DEVICE: return "no usable sm_103 device";
+        default: return "unknown status";
+    }
+}
+
+int vp_version(void) { return 1; }
+
+}  // extern "C"

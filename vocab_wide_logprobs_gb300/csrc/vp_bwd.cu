@@ -1,0 +1,303 @@
+// vp_bwd.cu -- fused backward kernels: logprobs, entropy and KL gradients.
+//
+// Sources:
+//   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL"
+//        (DeepSpeed pull request 8838): first commit message (fused forward
+//        and backward passes per op), second commit message ("gradients are
+//        returned contiguous"; rows read in place through two strides), and
+//        the Codex thread (positions of zero weight get exactly zero).
+//   [P2] page "[Feat][Kernel] Add TP Fused linear logp Triton", review nitpick
+//        on the chunked backward: dz = onehot - exp(logits - lse), scaled by
+//        the upstream gradient.
+//
+// Gradients, per row with upstream g and p_j = exp((z_j - m) - logS):
+//   logprobs  dz_j = g (onehot_{j,t} - p_j)
+//   entropy   dz_j = -g p_j (log p_j + H)                 (0 where p_j = 0)
+//   KL(P||Q)  dP_j = g p_j (log p_j - log q_j - KL)       (0 where p_j = 0)
+//             dQ_j = g (q_j - p_j)
+// m and logS come from the forward and are never summed into one fp32 lse.
+//
+// Shape: each CTA (256 threads) handles one tile of one row: up to 1024
+// 16-byte vectors of the input (8192 bf16 / 4096 fp32 logits), four loads in
+// flight per thread, and writes the same span of the contiguous gradient with
+// streaming 16-byte stores. Rows whose input and output do not share their
+// address modulo 16 are processed element by element.
+#include "vp_device.cuh"
+#include "vp_launch.h"
+
+namespace vp {
+
+constexpr int kTileVec = kBwdThreads * kBwdVecPerThread;
+
+enum RowMode { kNormal = 0, kZero = 1, kNaN = 2 };
+
+__device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
+
+template <typename T>
+__device__ __forceinline__ uint4 splat(float v) {
+    float f[Elem<T>::kVec];
+#pragma unroll
+    for (int i = 0; i < Elem<T>::kVec; ++i) f[i] = v;
+    return Elem<T>::pack(f);
+}
+
+// --------------------------------------------------------------------------
+// logprobs (kOp = 0) and entropy (kOp = 1)
+// --------------------------------------------------------------------------
+template <int kOp, typename T>
+__device__ __forceinline__ float grad_elem(float z, int64_t j, float m, float logS, float g, float H,
+                                           int64_t loc) {
+    const float lp = (z - m) - logS;
+    const float p = Elem<T>::exp(lp);
+    if (kOp == 0) return (j == loc) ? g * (1.f - p) : -g * p;
+    return (p == 0.f) ? 0.f : -g * p * (lp + H);
+}
+
+template <int kOp, typename T>
+__global__ void __launch_bounds__(kBwdThreads)
+grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__ m_in,
+            const float *__restrict__ logS_in, const float *__restrict__ H_in,
+            const float *__restrict__ g_in, const int64_t *__restrict__ targets, int64_t vocab_start,
+            T *__restrict__ dx, int32_t *__restrict__ err, int tiles_per_row, int64_t total_tiles) {
+    constexpr int kVec = Elem<T>::kVec;
+    const int tid = threadIdx.x;
+    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const int64_t r = tile / tiles_per_row;
+        const int seg = (int)(tile - r * tiles_per_row);
+        const T *in = x + rows.off(r);
+        T *out = dx + r * (int64_t)V;
+        const float m = m_in[r], logS = logS_in[r], g = g_in[r];
+        float H = 0.f;
+        int64_t loc = -1;
+        int mode = kNormal;
+        if (kOp == 0) {
+            const int64_t t = targets[r];
+            if (t < 0) {
+                mode = kZero;
+            } else {
+                loc = t - vocab_start;
+                if (loc < 0 || loc >= V) {
+                    mode = kNaN;
+                    if (err && seg == 0 && tid == 0) atomicOr(err, VP_ERRBIT_TARGET_);
+                } else if (!(fabsf(logS) < INFINITY)) {
+                    mode = kNaN;
+                }
+            }
+        } else {
+            H = H_in[r];
+            if (H != H) mode = kNaN;
+        }
+
+        const int hin = head_count(in, V), hout = head_count(out, V);
+        if (hin == hout) {
+            const int head = hin;
+            const int nv = (V - head) / kVec;
+            const int tail0 = head + nv * kVec;
+            if (seg == 0) {
+                for (int j = tid; j < head; j += kBwdThreads) {
+                    float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
+                              : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, m, logS, g, H, loc);
+                    Elem<T>::store1(out + j, d);
+                }
+                for (int j = tail0 + tid; j < V; j += kBwdThreads) {
+                    float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
+                              : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, m, logS, g, H, loc);
+                    Elem<T>::store1(out + j, d);
+                }
+            }
+            const int v0 = seg * kTileVec;
+            const int v1 = min(nv, v0 + kTileVec);
+            const uint4 *vin = reinterpret_cast<const uint4 *>(in + head);
+            uint4 *vout = reinterpret_cast<uint4 *>(out + head);
+            if (mode != kNormal) {
+                const uint4 c = splat<T>(mode == kZero ? 0.f : qnan());
+                for (int i = v0 + tid; i < v1; i += kBwdThreads) stg_stream(vout + i, c);
+                continue;
+            }
+            uint4 u[kBwdVecPerThread];
+#pragma unroll
+            for (int k = 0; k < kBwdVecPerThread; ++k) {
+                const int i = v0 + tid + k * kBwdThreads;
+                if (i < v1) u[k] = ldg_stream(vin + i);
+            }
+#pragma unroll
+            for (int k = 0; k < kBwdVecPerThread; ++k) {
+                const int i = v0 + tid + k * kBwdThreads;
+                if (i < v1) {
+                    float z[kVec], d[kVec];
+                    Elem<T>::unpack(u[k], z);
+                    const int64_t j0 = head + (int64_t)i * kVec;
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, m, logS, g, H, loc);
+                    stg_stream(vout + i, Elem<T>::pack(d));
+                }
+            }
+        } else {
+            const int64_t e0 = (int64_t)seg * kTileVec * kVec;
+            const int64_t e1 = min((int64_t)V, e0 + (int64_t)kTileVec * kVec);
+            for (int64_t j = e0 + tid; j < e1; j += kBwdThreads) {
+                float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
+                          : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, m, logS, g, H, loc);
+                Elem<T>::store1(out + j, d);
+            }
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// KL(P||Q): dP and / or dQ
+// --------------------------------------------------------------------------
+template <typename T, bool kDP, bool kDQ>
+__device__ __forceinline__ void kl_grad_elem(float zp, float zq, float mp, float lsp, float mq, float lsq,
+                                             float g, float kl, bool p_nan, float &dp, float &dq) {
+    const float lp = (zp - mp) - lsp, lq = (zq - mq) - lsq;
+    const float p = Elem<T>::exp(lp), q = Elem<T>::exp(lq);
+    if (kDQ) dq = g * (q - p);
+    if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * ((lp - lq) - kl);
+}
+
+template <typename T, bool kDP, bool kDQ>
+__global__ void __launch_bounds__(kBwdThreads)
+kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,
+               const float *__restrict__ mp_in, const float *__restrict__ lsp_in,
+               const float *__restrict__ mq_in, const float *__restrict__ lsq_in,
+               const float *__restrict__ kl_in, const float *__restrict__ g_in, T *__restrict__ dP,
+               T *__restrict__ dQ, int tiles_per_row, int64_t total_tiles) {
+    constexpr int kVec = Elem<T>::kVec;
+    const int tid = threadIdx.x;
+    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const int64_t r = tile / tiles_per_row;
+        const int seg = (int)(tile - r * tiles_per_row);
+        const int64_t off = rows.off(r);
+        const T *prow = P + off, *qrow = Q + off;
+        T *dprow = kDP ? dP + r * (int64_t)V : nullptr;
+        T *dqrow = kDQ ? dQ + r * (int64_t)V : nullptr;
+        const float mp = mp_in[r], lsp = lsp_in[r], mq = mq_in[r], lsq = lsq_in[r];
+        const float g = g_in[r], kl = kl_in[r];
+        const bool all_nan = kl != kl;          // NaN row: both gradients NaN
+        const bool p_nan = !(kl < INFINITY);    // NaN or mismatch (+inf): dP is NaN
+
+        uintptr_t ph = (uintptr_t)prow & 15u;
+        bool vec = (((uintptr_t)qrow & 15u) == ph);
+        if (kDP) vec = vec && (((uintptr_t)dprow & 15u) == ph);
+        if (kDQ) vec = vec && (((uintptr_t)dqrow & 15u) == ph);
+
+        auto scalar_range = [&](int64_t j0, int64_t j1) {
+            for (int64_t j = j0 + tid; j < j1; j += kBwdThreads) {
+                float dp = qnan(), dq = qnan();
+                if (!all_nan)
+                    kl_grad_elem<T, kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), mp, lsp, mq,
+                                              lsq, g, kl, p_nan, dp, dq);
+                if (kDP) Elem<T>::store1(dprow + j, dp);
+                if (kDQ) Elem<T>::store1(dqrow + j, dq);
+            }
+        };
+
+        if (vec) {
+            const int head = head_count(prow, V);
+            const int nv = (V - head) / kVec;
+            const int tail0 = head + nv * kVec;
+            if (seg == 0) {
+                scalar_range(0, head);
+                scalar_range(tail0, V);
+            }
+            const int v0 = seg * kTileVec;
+            const int v1 = min(nv, v0 + kTileVec);
+            const uint4 *vp = reinterpret_cast<const uint4 *>(prow + head);
+            const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + head);
+            uint4 *vdp = kDP ? reinterpret_cast<uint4 *>(dprow + head) : nullptr;
+            uint4 *vdq = kDQ ? reinterpret_cast<uint4 *>(dqrow + head) : nullptr;
+            if (all_nan) {
+                const uint4 c = splat<T>(qnan());
+                for (int i = v0 + tid; i < v1; i += kBwdThreads) {
+                    if (kDP) stg_stream(vdp + i, c);
+                    if (kDQ) stg_stream(vdq + i, c);
+                }
+                continue;
+            }
+            if (kDP && !kDQ && p_nan) {
+                const uint4 c = splat<T>(qnan());
+                for (int i = v0 + tid; i < v1; i += kBwdThreads) stg_stream(vdp + i, c);
+                continue;
+            }
+            uint4 up[kBwdVecPerThread], uq[kBwdVecPerThread];
+#pragma unroll
+            for (int k = 0; k < kBwdVecPerThread; ++k) {
+                const int i = v0 + tid + k * kBwdThreads;
+                if (i < v1) { up[k] = ldg_stream(vp + i); uq[k] = ldg_stream(vq + i); }
+            }
+#pragma unroll
+            for (int k = 0; k < kBwdVecPerThread; ++k) {
+                const int i = v0 + tid + k * kBwdThreads;
+                if (i < v1) {
+                    float zp[kVec], zq[kVec], dp[kVec], dq[kVec];
+                    Elem<T>::unpack(up[k], zp);
+                    Elem<T>::unpack(uq[k], zq);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e)
+                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], mp, lsp, mq, lsq, g, kl, p_nan, dp[e], dq[e]);
+                    if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
+                    if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
+                }
+            }
+        } else {
+            const int64_t e0 = (int64_t)seg * kTileVec * kVec;
+            scalar_range(e0, min((int64_t)V, e0 + (int64_t)kTileVec * kVec));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+static inline void tile_grid(int64_t N, int64_t V, int vec, int &tiles_per_row, int64_t &total, unsigned &grid) {
+    const int64_t per_tile = (int64_t)kTileVec * vec;
+    tiles_per_row = (int)((V + per_tile - 1) / per_tile);
+    total = N * tiles_per_row;
+    grid = (unsigned)(total < (int64_t)(1u << 30) ? total : (int64_t)(1u << 30));
+}
+
+template <int kOp, typename T>
+static cudaError_t launch_grad(const GradArgs &a) {
+    int tpr;
+    int64_t total;
+    unsigned grid;
+    tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
+    grad_kernel<kOp, T><<<grid, kBwdThreads, 0, a.stream>>>(
+        static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.m, a.logS, a.H, a.g, a.targets,
+        a.vocab_start, static_cast<T *>(a.dx), a.err, tpr, total);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_logprobs_bwd(const GradArgs &a) {
+    return a.bf16 ? launch_grad<0, __nv_bfloat16>(a) : launch_grad<0, float>(a);
+}
+
+cudaError_t launch_entropy_bwd(const GradArgs &a) {
+    return a.bf16 ? launch_grad<1, __nv_bfloat16>(a) : launch_grad<1, float>(a);
+}
+
+template <typename T, bool kDP, bool kDQ>
+static cudaError_t launch_kl_grad_t(const KLBwdArgs &a) {
+    int tpr;
+    int64_t total;
+    unsigned grid;
+    tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
+    kl_grad_kernel<T, kDP, kDQ><<<grid, kBwdThreads, 0, a.stream>>>(
+        static_cast<const T *>(a.p), static_cast<const T *>(a.q), (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.mp,
+        a.logSp, a.mq, a.logSq, a.kl, a.g, static_cast<T *>(a.dp), static_cast<T *>(a.dq), tpr, total);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_kl_grad_dt(const KLBwdArgs &a) {
+    if (a.dp && a.dq) return launch_kl_grad_t<T, true, true>(a);
+    if (a.dp) return launch_kl_grad_t<T, true, false>(a);
+    return launch_kl_grad_t<T, false, true>(a);
+}
+
+cudaError_t launch_kl_bwd(const KLBwdArgs &a) {
+    return a.bf16 ? launch_kl_grad_dt<__nv_bfloat16>(a) : launch_kl_grad_dt<float>(a);
+}
+
+}  // namespace vp

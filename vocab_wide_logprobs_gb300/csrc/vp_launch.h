@@ -1,0 +1,57 @@
+// vp_launch.h -- internal launcher interface between the C ABI and the kernels.
+// Arguments here are already validated by vp_api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace vp {
+
+constexpr int VP_ERRBIT_TARGET_ = 1;  // same value as VP_ERRBIT_TARGET in include/vp.h
+
+struct StatsArgs {
+    const void *x;
+    bool bf16;
+    int64_t N, V, R, s_o, s_i, vocab_start;
+    const int64_t *targets;
+    float *out, *m, *logS;
+    int32_t *err;
+    cudaStream_t stream;
+};
+
+struct KLFwdArgs {
+    const void *p, *q;
+    bool bf16;
+    int64_t N, V, R, s_o, s_i;
+    float *kl, *mp, *logSp, *mq, *logSq;
+    cudaStream_t stream;
+};
+
+struct GradArgs {
+    const void *x;
+    bool bf16;
+    int64_t N, V, R, s_o, s_i, vocab_start;
+    const float *m, *logS, *H, *g;
+    const int64_t *targets;
+    void *dx;
+    int32_t *err;
+    cudaStream_t stream;
+};
+
+struct KLBwdArgs {
+    const void *p, *q;
+    bool bf16;
+    int64_t N, V, R, s_o, s_i;
+    const float *mp, *logSp, *mq, *logSq, *kl, *g;
+    void *dp, *dq;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_logprobs_fwd(const StatsArgs &a);
+cudaError_t launch_entropy_fwd(const StatsArgs &a);
+cudaError_t launch_kl_fwd(const KLFwdArgs &a);
+cudaError_t launch_logprobs_bwd(const GradArgs &a);
+cudaError_t launch_entropy_bwd(const GradArgs &a);
+cudaError_t launch_kl_bwd(const KLBwdArgs &a);
+
+}  // namespace vp
