@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark: fwd+bwd of logprobs, entropy and KL (both directions) at 8192 x 75968 bf16.
+
+One step = logprobs fwd+bwd, entropy fwd+bwd, reverse KL fwd+bwd (dA and dB)
+and forward KL fwd+bwd (dA and dB) over one batch of synthetic logits of the
+pages' shape (the ``pages_shape`` workload: N = 8192 rows, V = 75968, bf16,
+N(0, 3^2) plus a per-row offset). ``value`` is the step's algorithmic HBM bytes
+divided by its device time (GB/s); ``ms_per_step`` is the device time.
+
+Launch: ``python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference]``;
+for N > 1 under torchrun every rank runs its own 8192-row batch (rows are
+independent: weak scaling, no data-path collective; one all-reduce of the
+elapsed time takes the max over ranks).
+
+``--impl reference`` times the fp64 CPU oracle on the host cores, on a bounded
+sample of rows of the same workload, and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd ms & HBM GB/s vs ~8 TB/s, 8192×75968 bf16 logp/entropy/KL"
+UNIT = "GB/s"
+N_ROWS, VOCAB = 8192, 75968
+WORKLOAD = "pages' shape: 8192x75968 bf16 logits A,B ~ N(0,3^2)+U[-5,5] row offset; logprobs, entropy, " \
+           "KL(A||B) and KL(B||A), each fwd+bwd (both KL gradients)"
+
+
+def algorithmic_bytes(N: int, V: int, s: int = 2) -> dict:
+    """HBM bytes each op must move at least once (logits and gradients; per-row vectors are < 0.01%)."""
+    E = N * V * s
+    return {
+        "logprobs_fwd": E, "logprobs_bwd": 2 * E,
+        "entropy_fwd": E, "entropy_bwd": 2 * E,
+        "kl_rev_fwd": 2 * E, "kl_rev_bwd": 4 * E,
+        "kl_fwd_fwd": 2 * E, "kl_fwd_bwd": 4 * E,
+    }
+
+
+KERNEL_OF = {  # op -> kernel name prefix in profiles (mangled names contain these)
+    "logprobs_fwd": "stats_fwd_kernel<0", "logprobs_bwd": "grad_kernel<0",
+    "entropy_fwd": "stats_fwd_kernel<1", "entropy_bwd": "grad_kernel<1",
+    "kl_rev_fwd": "kl_fwd_kernel", "kl_rev_bwd": "kl_grad_kernel",
+    "kl_fwd_fwd": "kl_fwd_kernel", "kl_fwd_bwd": "kl_grad_kernel",
+}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "src": "measured"}
+    return {"hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "vocab_wide_logprobs_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key: str):
+    """dram read+write bytes per launch from a committed ncu summary, if it matches the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.seek(0)
+        rows = [r.split(",") for r in self.tmp.read().strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        load = [x for x in sm if smax and x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    from vocab_wide_logprobs_gb300 import workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = workloads.pages_shape(seed=1 + rank)
+    a, b = w["a"].to(dev), w["b"].to(dev)
+    t, g = w["targets"].to(dev), w["grad"].to(dev)
+    N, V = a.shape
+    nbytes = algorithmic_bytes(N, V)
+    step_bytes = sum(nbytes.values())
+
+    # outputs, allocated once (the library never allocates)
+    f32 = lambda: torch.empty(N, dtype=torch.float32, device=dev)
+    st = {k: f32() for k in ("lp", "H", "kl")}
+    st.update({k: vp.rowstats(N, dev) for k in ("lp_s", "H_s", "sa", "sb")})
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    dx = torch.empty_like(a)
+    da, db = torch.empty_like(a), torch.empty_like(a)
+
+    R, F = vp.KL_REVERSE, vp.KL_FORWARD
+    calls = {
+        "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a, t, 0, err, st["lp"], st["lp_s"]),
+        "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a, t, st["lp_s"], g, 0, err, dx),
+        "entropy_fwd": lambda: vp.vp_entropy_fwd(a, st["H"], st["H_s"]),
+        "entropy_bwd": lambda: vp.vp_entropy_bwd(a, st["H_s"], g, dx),
+        "kl_rev_fwd": lambda: vp.vp_kl_fwd(a, b, R, st["kl"], st["sa"], st["sb"]),
+        "kl_rev_bwd": lambda: vp.vp_kl_bwd(a, b, R, st["sa"], st["sb"], g, da=da, db=db),
+        "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a, b, F, st["kl"], st["sa"], st["sb"]),
+        "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a, b, F, st["sa"], st["sb"], g, da=da, db=db),
+    }
+
+    def op(name):
+        calls[name]()
+
+    ops = list(nbytes.keys())
+    launches_per_step = len(ops)
+
+    def step(events=None):
+        for i, name in enumerate(ops):
+            if events is not None:
+                events[i][0].record()
+            op(name)
+            if events is not None:
+                events[i][1].record()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(args.steps):
+            step(ev[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_op_ms = {name: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+                 for i, name in enumerate(ops)}
+    ms_per_step = elapsed_ms / args.steps
+    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+    # dominant kernel (largest share of the step) and its roofline
+    dom = max(per_op_ms, key=per_op_ms.get)
+    peaks = measured_peaks()
+    achieved = nbytes[dom] / (per_op_ms[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": KERNEL_OF[dom], "op": dom, "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "peak_src": peaks["src"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for(dom),
+                "algorithmic_bytes": nbytes[dom]}
+
+    # end to end through the public API with host buffers: H2D of the step's inputs,
+    # the step, D2H of its per-row results, every step
+    h_a, h_b = w["a"].pin_memory(), w["b"].pin_memory()
+    h_t, h_g = w["targets"].pin_memory(), w["grad"].pin_memory()
+    h_out = torch.empty(4, N, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (h_a, h_b, h_t, h_g))
+    d2h = h_out.numel() * 4
+
+    def e2e_step():
+        a.copy_(h_a, non_blocking=True)
+        b.copy_(h_b, non_blocking=True)
+        t.copy_(h_t, non_blocking=True)
+        g.copy_(h_g, non_blocking=True)
+        outs = []
+        for name in ops:
+            op(name)
+            if name == "kl_rev_fwd" or name == "kl_fwd_fwd":
+                outs.append(st["kl"].clone())
+        h_out[0].copy_(st["lp"], non_blocking=True)
+        h_out[1].copy_(st["H"], non_blocking=True)
+        h_out[2].copy_(outs[0], non_blocking=True)
+        h_out[3].copy_(outs[1], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "N": N, "V": V, "rows_per_gpu": N, "parallelism": f"dp{world}",
+                       "l2": "inputs larger than L2 (1.245 GB per logits tensor)",
+                       "algorithmic_bytes_per_step": step_bytes},
+            "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
+            "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(), "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+def _oracle_rows(w, rows):
+    import numpy as np
+    import oracle
+    a64 = w["a"][rows].double().numpy()
+    b64 = w["b"][rows].double().numpy()
+    t = w["targets"][rows].numpy()
+    g = w["grad"][rows].double().numpy()
+
+    def run():
+        lp = oracle.logprobs_fwd(a64, t)
+        oracle.logprobs_bwd(a64, t, g)
+        oracle.entropy_fwd(a64)
+        oracle.entropy_bwd(a64, g)
+        for d in (oracle.REVERSE, oracle.FORWARD):
+            oracle.kl_fwd(a64, b64, d)
+            oracle.kl_bwd(a64, b64, g, d)
+        return lp
+    return run, np
+
+
+def cpu_baseline(w, seconds=12.0, batch_rows=64):
+    """The oracle as it stands, all four ops fwd+bwd, on batches of rows until `seconds` pass."""
+    import oracle
+    run, _ = _oracle_rows(w, slice(0, batch_rows))
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        run()
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    rows = reps * batch_rows
+    step_bytes = sum(algorithmic_bytes(rows, VOCAB).values())
+    return {"value": round(step_bytes / dt / 1e9, 4), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{rows} rows ({reps} x {batch_rows}) of the 8192x75968 bf16 workload, all four ops fwd+bwd, "
+                      f"fp64 C oracle with OpenMP over rows; GB/s = the same algorithmic bytes per row as the GPU"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from vocab_wide_logprobs_gb300 import workloads
+    oracle.build()
+    rows = args.reference_rows
+    w = workloads.pages_shape(seed=1, N=rows)
+    run, _ = _oracle_rows(w, slice(0, rows))
+    for _ in range(max(args.warmup, 3)):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    dt = sum(times)
+    step_bytes = sum(algorithmic_bytes(rows, VOCAB).values())
+    value = step_bytes * args.steps / dt / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "N": rows, "V": VOCAB, "note": f"bounded sample: {rows} rows per step"},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": oracle.num_threads(),
+                             "sample": f"{rows} rows of the 8192x75968 bf16 workload per step, all four ops fwd+bwd"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--reference-rows", type=int, default=64)
+    args = p.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

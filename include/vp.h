@@ -32,12 +32,17 @@
  *   reviewer's note that the bf16 gradient equals the round-to-nearest-even
  *   of the fp32 one].
  *
- * Saved statistics.  Forward calls return, per row and input, the row max m
- *   and logS = log sum_j exp(z_j - m); backward calls take them back. The sum
- *   lse = m + logS is never formed, so a large common offset does not round
- *   away the centred logits [P1, second commit message: "centring on the max
- *   keeps a large common offset from cancelling in fp32"]. For a row whose
- *   logits are all -inf, m is -FLT_MAX and logS is -inf.
+ * Saved statistics.  Forward calls also write, per row and per input, a
+ *   32-byte vp_rowstat record that the matching backward call reads back:
+ *   the exact row max m, logS = log sum_j exp(z_j - m) and the centred mean c
+ *   (below), the last two as unevaluated sums of two floats (hi + lo) computed
+ *   in fp64 at the end of the forward. The sum lse = m + logS is never
+ *   formed, so a large common offset does not round away the centred logits
+ *   [P1, second commit message: "centring on the max keeps a large common
+ *   offset from cancelling in fp32"]. The backward evaluates the gradients
+ *   from the centred logits and c, not from the rounded fp32 output, so an
+ *   element whose gradient cancels to near zero keeps its accuracy (see
+ *   vp_rowstat).
  *
  * Per-row special values (the pages state the cases, not all outcomes; these
  *   are the readings the library implements):
@@ -91,8 +96,8 @@ typedef enum vp_status {
     VP_ERR_SHAPE = 2,     /* N < 0, V < 1, V > 2^31 - 1, R < 1, D < 1, ...              */
     VP_ERR_DTYPE = 3,     /* unknown dtype code                                      */
     VP_ERR_LAYOUT = 4,    /* a negative stride                                       */
-    VP_ERR_ALIGN = 5,     /* a pointer not aligned to its element size (or 16 B for
-                             the linear-logp operands)                               */
+    VP_ERR_ALIGN = 5,     /* a pointer not aligned to its element size (16 B for
+                             vp_rowstat arrays)                                      */
     VP_ERR_LAUNCH = 6,    /* the CUDA launch failed                                  */
     VP_ERR_ARG = 7,       /* another invalid argument (direction, both gradients
                              requested as NULL where one is required, ...)          */
@@ -108,41 +113,67 @@ typedef enum vp_kl_direction { VP_KL_REVERSE = 0, VP_KL_FORWARD = 1 } vp_kl_dire
 
 #define VP_ERRBIT_TARGET 1
 
+/* Row flags of vp_rowstat. */
+#define VP_ROW_NANINF   1u  /* the row holds a NaN or a +inf                          */
+#define VP_ROW_EMPTY    2u  /* no finite logit (all -inf): S = 0                      */
+#define VP_ROW_MISMATCH 4u  /* KL(P||Q) record of P: some P_j > -inf has Q_j = -inf  */
+
+/* Per-row statistics saved by a forward call for its backward call.
+ * m      the exact row max; -FLT_MAX when the row has no finite logit.
+ * logS   log sum_j exp(z_j - m) = logS_hi + logS_lo.
+ * c      the probability-weighted mean of the centred logits, c_hi + c_lo:
+ *          entropy:            c = E_p[z - m] = W / S, so H = logS - c;
+ *          KL(P||Q), P record: c = E_p[(P - m_P) - (Q - m_Q)] = W / S_P,
+ *                              so KL = c - logS_P + logS_Q;
+ *          logprobs, and the Q record of KL: 0.
+ *        Gradients use it as dH/dz_j = -p_j ((z_j - m) - c) and
+ *        dKL/dP_j = p_j (((P_j - m_P) - (Q_j - m_Q)) - c).
+ * flags  VP_ROW_* bits. */
+typedef struct vp_rowstat {
+    float m;
+    float logS_hi, logS_lo;
+    float c_hi, c_lo;
+    uint32_t flags;
+    uint32_t reserved[2];
+} vp_rowstat;
+
 /* ------------------------------------------------------------------------ */
 /* Logprobs [P1, first commit message; P2, "Implementation"]                 */
 /* ------------------------------------------------------------------------ */
 
 /* logp[r] = (z_{r,t} - m_r) - logS_r for t = targets[r] - vocab_start, read in
- * one pass over each row. Outputs: logp, m, logS (fp32 [N] each, required).
- * err_word may be NULL. */
+ * one pass over each row. Outputs: logp (fp32 [N]) and stats (vp_rowstat [N],
+ * 16-byte aligned), both required. err_word may be NULL. */
 VP_API vp_status vp_logprobs_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
-                          int64_t s_o, int64_t s_i, int64_t vocab_start,
-                          const int64_t *targets, float *logp, float *m, float *logS,
-                          int32_t *err_word, vp_stream stream);
+                                 int64_t s_o, int64_t s_i, int64_t vocab_start,
+                                 const int64_t *targets, float *logp, vp_rowstat *stats,
+                                 int32_t *err_word, vp_stream stream);
 
 /* dx[r, j] = g[r] (onehot_{j,t} - p_{r,j}), p = exp((z - m) - logS), using
- * the m / logS of vp_logprobs_fwd [P2, review nitpick on the chunked
- * backward]. grad_out: fp32 [N]. dx: contiguous [N, V], dtype of x. */
+ * the stats of vp_logprobs_fwd [P2, review nitpick on the chunked backward].
+ * grad_out: fp32 [N]. dx: contiguous [N, V], dtype of x. */
 VP_API vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
-                          int64_t s_o, int64_t s_i, int64_t vocab_start,
-                          const int64_t *targets, const float *m, const float *logS,
-                          const float *grad_out, void *dx, int32_t *err_word,
-                          vp_stream stream);
+                                 int64_t s_o, int64_t s_i, int64_t vocab_start,
+                                 const int64_t *targets, const vp_rowstat *stats,
+                                 const float *grad_out, void *dx, int32_t *err_word,
+                                 vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Entropy [P1, second commit message and reviewer's suggested change]      */
 /* ------------------------------------------------------------------------ */
 
 /* H[r] = log S - W / S from one read of the row, with the online max m,
- * S = sum e^{z-m} and W = sum e^{z-m} (z - m). Outputs fp32 [N]: H, m, logS. */
+ * S = sum e^{z-m} and W = sum e^{z-m} (z - m). Outputs: H (fp32 [N]) and
+ * stats (vp_rowstat [N]). */
 VP_API vp_status vp_entropy_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
-                         int64_t s_o, int64_t s_i, float *H, float *m, float *logS,
-                         vp_stream stream);
+                                int64_t s_o, int64_t s_i, float *H, vp_rowstat *stats,
+                                vp_stream stream);
 
-/* dx[r, j] = -g[r] p_j (log p_j + H_r), exactly 0 where p_j = 0. */
+/* dx[r, j] = -g[r] p_j (log p_j + H_r) = -g[r] p_j ((z_j - m) - c), exactly 0
+ * where p_j = 0. */
 VP_API vp_status vp_entropy_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
-                         int64_t s_o, int64_t s_i, const float *m, const float *logS,
-                         const float *H, const float *grad_out, void *dx, vp_stream stream);
+                                int64_t s_o, int64_t s_i, const vp_rowstat *stats,
+                                const float *grad_out, void *dx, vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* KL [P1, second commit message and reviewer's suggested change]           */
@@ -152,19 +183,20 @@ VP_API vp_status vp_entropy_bwd(const void *x, int dtype, int64_t N, int64_t V, 
  * VP_KL_FORWARD: KL = W / S_P - log S_P + log S_Q, where
  * W = sum_j e^{P_j - m_P} ((P_j - m_P) - (Q_j - m_Q)), or +inf on a support
  * mismatch. A and B share one row layout (R, s_o, s_i) and dtype.
- * Outputs fp32 [N]: kl, and m / logS of A and of B (all required). */
+ * Outputs: kl (fp32 [N]) and the records of A and of B (vp_rowstat [N] each;
+ * the record of P carries c), all required. */
 VP_API vp_status vp_kl_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R,
-                    int64_t s_o, int64_t s_i, int direction, float *kl, float *ma,
-                    float *logSa, float *mb, float *logSb, vp_stream stream);
+                           int64_t s_o, int64_t s_i, int direction, float *kl, vp_rowstat *stats_a,
+                           vp_rowstat *stats_b, vp_stream stream);
 
 /* dP_j = g p_j (log p_j - log q_j - KL), dQ_j = g (q_j - p_j), mapped back to
- * A and B by the direction. da and db are contiguous [N, V] in the dtype of
- * the inputs; either may be NULL (that gradient is then neither computed nor
- * written), not both. */
+ * A and B by the direction, which must be the one given to vp_kl_fwd. da and
+ * db are contiguous [N, V] in the dtype of the inputs; either may be NULL
+ * (that gradient is then neither computed nor written), not both. */
 VP_API vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R,
-                    int64_t s_o, int64_t s_i, int direction, const float *ma,
-                    const float *logSa, const float *mb, const float *logSb, const float *kl,
-                    const float *grad_out, void *da, void *db, vp_stream stream);
+                           int64_t s_o, int64_t s_i, int direction, const vp_rowstat *stats_a,
+                           const vp_rowstat *stats_b, const float *grad_out, void *da, void *db,
+                           vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                      */

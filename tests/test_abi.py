@@ -52,8 +52,8 @@ FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: every call below fai
 FAKE_ODD = ctypes.c_void_p(0x100001)
 
 
-def ent_fwd(x=FAKE, dtype=1, N=4, V=16, R=4, s_o=0, s_i=16, H=FAKE, m=FAKE, logS=FAKE):
-    return _lib.lib().vp_entropy_fwd(x, dtype, N, V, R, s_o, s_i, H, m, logS, None)
+def ent_fwd(x=FAKE, dtype=1, N=4, V=16, R=4, s_o=0, s_i=16, H=FAKE, stats=FAKE):
+    return _lib.lib().vp_entropy_fwd(x, dtype, N, V, R, s_o, s_i, H, stats, None)
 
 
 def test_status_codes_for_bad_arguments():
@@ -67,14 +67,15 @@ def test_status_codes_for_bad_arguments():
     assert ent_fwd(x=None) == ERR_NULL
     assert ent_fwd(H=None) == ERR_NULL
     assert ent_fwd(x=FAKE_ODD) == ERR_ALIGN
-    assert ent_fwd(m=FAKE_ODD) == ERR_ALIGN
-    assert ent_fwd(N=0, x=None, H=None, m=None, logS=None) == OK  # N = 0 queues nothing
+    assert ent_fwd(stats=FAKE_ODD) == ERR_ALIGN
+    assert ent_fwd(stats=ctypes.c_void_p(0x100008)) == ERR_ALIGN  # records need 16-byte alignment
+    assert ent_fwd(N=0, x=None, H=None, stats=None) == OK  # N = 0 queues nothing
     L = _lib.lib()
     args = (FAKE, FAKE, 1, 4, 16, 4, 0, 16)
-    assert L.vp_kl_fwd(*args, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None) == ERR_ARG
-    assert L.vp_kl_bwd(*args, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None) == ERR_ARG
-    assert L.vp_logprobs_fwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE_ODD, FAKE, FAKE, FAKE, None, None) == ERR_ALIGN
-    assert L.vp_logprobs_bwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE, FAKE, FAKE, FAKE, None, None, None) == ERR_NULL
+    assert L.vp_kl_fwd(*args, 2, FAKE, FAKE, FAKE, None) == ERR_ARG
+    assert L.vp_kl_bwd(*args, 0, FAKE, FAKE, FAKE, None, None, None) == ERR_ARG
+    assert L.vp_logprobs_fwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE_ODD, FAKE, FAKE, None, None) == ERR_ALIGN
+    assert L.vp_logprobs_bwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE, FAKE, FAKE, None, None, None) == ERR_NULL
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device status; needs a machine without a GPU")

@@ -142,13 +142,13 @@ def test_empty_batch_is_a_noop():
     x = torch.empty(0, 128, dtype=torch.bfloat16, device=DEV)
     t = torch.empty(0, dtype=torch.int64, device=DEV)
     g = torch.empty(0, dtype=torch.float32, device=DEV)
-    lp, m, ls = vp.vp_logprobs_fwd(x, t)
+    lp, st = vp.vp_logprobs_fwd(x, t)
     assert lp.numel() == 0
-    assert vp.vp_logprobs_bwd(x, t, m, ls, g).shape == (0, 128)
-    H, m, ls = vp.vp_entropy_fwd(x)
-    vp.vp_entropy_bwd(x, m, ls, H, g)
-    kl, *st = vp.vp_kl_fwd(x, x)
-    vp.vp_kl_bwd(x, x, vp.KL_REVERSE, *st, kl, g)
+    assert vp.vp_logprobs_bwd(x, t, st, g).shape == (0, 128)
+    H, st = vp.vp_entropy_fwd(x)
+    vp.vp_entropy_bwd(x, st, g)
+    kl, sa, sb = vp.vp_kl_fwd(x, x)
+    vp.vp_kl_bwd(x, x, vp.KL_REVERSE, sa, sb, g)
     torch.cuda.synchronize()
 
 
@@ -156,10 +156,10 @@ def test_kl_single_gradient_outputs():
     w = workloads.pages_shape(seed=21, N=12, V=9000, dtype=torch.bfloat16)
     a, b, g = w["a"].to(DEV), w["b"].to(DEV), w["grad"].to(DEV)
     for d in (vp.KL_REVERSE, vp.KL_FORWARD):
-        kl, ma, lsa, mb, lsb = vp.vp_kl_fwd(a, b, d)
-        da_both, db_both = vp.vp_kl_bwd(a, b, d, ma, lsa, mb, lsb, kl, g)
-        da, none_b = vp.vp_kl_bwd(a, b, d, ma, lsa, mb, lsb, kl, g, want_db=False)
-        none_a, db = vp.vp_kl_bwd(a, b, d, ma, lsa, mb, lsb, kl, g, want_da=False)
+        kl, sa, sb = vp.vp_kl_fwd(a, b, d)
+        da_both, db_both = vp.vp_kl_bwd(a, b, d, sa, sb, g)
+        da, none_b = vp.vp_kl_bwd(a, b, d, sa, sb, g, want_db=False)
+        none_a, db = vp.vp_kl_bwd(a, b, d, sa, sb, g, want_da=False)
         torch.cuda.synchronize()
         assert none_a is None and none_b is None
         assert torch.equal(da, da_both) and torch.equal(db, db_both)
@@ -262,6 +262,18 @@ def test_full_strided_sampled():
 
 
 @pytest.mark.slow
-def test_short_rows_full():
+def test_short_rows_sampled():
     w = workloads.short_rows()
-    _run_and_compare(w["a"].to(DEV), w["b"].to(DEV), w["targets"].to(DEV), w["grad"].to(DEV), tag="N=1024 ")
+    a, b, t, g = (w[k].to(DEV) for k in ("a", "b", "targets", "grad"))
+    got = parity.gpu_all(a, b, t, g)
+    _properties(got, a.shape[1])
+    rows = _sampled(96, a.shape[0], 4)
+    ref = parity.oracle_all(parity.to64(w["a"][rows]), parity.to64(w["b"][rows]), w["targets"][rows].numpy(),
+                            w["grad"][rows].numpy())
+    parity.compare_all(got, ref, rows=torch.as_tensor(rows, device=DEV), tag="N=1024 ")
+
+
+def test_zz_report_error_stats():
+    """Prints the worst error / tolerance seen by the parity tests above (informational)."""
+    for k, v in sorted(parity.STATS.items()):
+        print(k, v)

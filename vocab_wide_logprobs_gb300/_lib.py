@@ -18,12 +18,12 @@ P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 
 # name -> argument types (all return int status unless noted)
 SIGNATURES = {
-    "vp_logprobs_fwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P],
-    "vp_logprobs_bwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P, P],
-    "vp_entropy_fwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P],
-    "vp_entropy_bwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P, P, P],
-    "vp_kl_fwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
-    "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, P, P],
+    "vp_logprobs_fwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P],
+    "vp_logprobs_bwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P],
+    "vp_entropy_fwd": [P, I32, I64, I64, I64, I64, I64, P, P, P],
+    "vp_entropy_bwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P],
+    "vp_kl_fwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P],
+    "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
 }
 
 

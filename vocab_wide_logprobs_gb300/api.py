@@ -24,6 +24,20 @@ from . import _lib
 F32, BF16 = 0, 1
 KL_REVERSE, KL_FORWARD = 0, 1
 ERRBIT_TARGET = 1
+ROW_NANINF, ROW_EMPTY, ROW_MISMATCH = 1, 2, 4
+ROWSTAT_FLOATS = 8  # sizeof(vp_rowstat) / 4
+
+
+def rowstats(N: int, device) -> torch.Tensor:
+    """Storage for N vp_rowstat records: a float32 [N, 8] tensor (32 bytes per row)."""
+    return torch.empty((N, ROWSTAT_FLOATS), dtype=torch.float32, device=device)
+
+
+def decode_rowstats(stats: torch.Tensor) -> dict:
+    """Fields of vp_rowstat records as tensors: m, logS (hi + lo in fp64), c (hi + lo in fp64), flags."""
+    s = stats.detach()
+    return {"m": s[:, 0], "logS": s[:, 1].double() + s[:, 2].double(), "c": s[:, 3].double() + s[:, 4].double(),
+            "flags": s[:, 5].view(torch.int32)}
 
 
 class VPError(RuntimeError):
@@ -77,58 +91,57 @@ def _same_layout(a: torch.Tensor, b: torch.Tensor):
         raise VPError(4, "A and B must share shape, strides and dtype")
 
 
-def vp_logprobs_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=None, m=None, logS=None):
-    """Returns (logp, m, logS), fp32 [N] each."""
+def vp_logprobs_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=None, stats=None):
+    """Returns (logp fp32 [N], stats vp_rowstat [N] as float32 [N, 8])."""
     N, V, R, s_o, s_i = rows_of(x)
     logp = _f32(N, x) if logp is None else logp
-    m = _f32(N, x) if m is None else m
-    logS = _f32(N, x) if logS is None else logS
+    stats = rowstats(N, x.device) if stats is None else stats
     _check(_lib.lib().vp_logprobs_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
-                                      _ptr(logp), _ptr(m), _ptr(logS), _ptr(err_word), _stream()),
-           "vp_logprobs_fwd")
-    return logp, m, logS
+                                      _ptr(logp), _ptr(stats), _ptr(err_word), _stream()), "vp_logprobs_fwd")
+    return logp, stats
 
 
-def vp_logprobs_bwd(x, targets, m, logS, grad, vocab_start: int = 0, err_word=None, dx=None):
+def vp_logprobs_bwd(x, targets, stats, grad, vocab_start: int = 0, err_word=None, dx=None):
     """Returns dx, contiguous [N, V] in the dtype of x."""
     N, V, R, s_o, s_i = rows_of(x)
     dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
     _check(_lib.lib().vp_logprobs_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
-                                      _ptr(m), _ptr(logS), _ptr(grad), _ptr(dx), _ptr(err_word), _stream()),
+                                      _ptr(stats), _ptr(grad), _ptr(dx), _ptr(err_word), _stream()),
            "vp_logprobs_bwd")
     return dx
 
 
-def vp_entropy_fwd(x, H=None, m=None, logS=None):
-    """Returns (H, m, logS), fp32 [N] each."""
+def vp_entropy_fwd(x, H=None, stats=None):
+    """Returns (H fp32 [N], stats)."""
     N, V, R, s_o, s_i = rows_of(x)
     H = _f32(N, x) if H is None else H
-    m = _f32(N, x) if m is None else m
-    logS = _f32(N, x) if logS is None else logS
-    _check(_lib.lib().vp_entropy_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(H), _ptr(m), _ptr(logS),
-                                     _stream()), "vp_entropy_fwd")
-    return H, m, logS
+    stats = rowstats(N, x.device) if stats is None else stats
+    _check(_lib.lib().vp_entropy_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(H), _ptr(stats), _stream()),
+           "vp_entropy_fwd")
+    return H, stats
 
 
-def vp_entropy_bwd(x, m, logS, H, grad, dx=None):
+def vp_entropy_bwd(x, stats, grad, dx=None):
     N, V, R, s_o, s_i = rows_of(x)
     dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
-    _check(_lib.lib().vp_entropy_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(m), _ptr(logS), _ptr(H),
-                                     _ptr(grad), _ptr(dx), _stream()), "vp_entropy_bwd")
+    _check(_lib.lib().vp_entropy_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(stats), _ptr(grad),
+                                     _ptr(dx), _stream()), "vp_entropy_bwd")
     return dx
 
 
-def vp_kl_fwd(a, b, direction: int = KL_REVERSE, kl=None, ma=None, logSa=None, mb=None, logSb=None):
-    """Returns (kl, ma, logSa, mb, logSb); reverse = KL(A||B), forward = KL(B||A)."""
+def vp_kl_fwd(a, b, direction: int = KL_REVERSE, kl=None, stats_a=None, stats_b=None):
+    """Returns (kl, stats_a, stats_b); reverse = KL(A||B), forward = KL(B||A)."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
-    kl, ma, logSa, mb, logSb = (_f32(N, a) if t is None else t for t in (kl, ma, logSa, mb, logSb))
+    kl = _f32(N, a) if kl is None else kl
+    stats_a = rowstats(N, a.device) if stats_a is None else stats_a
+    stats_b = rowstats(N, a.device) if stats_b is None else stats_b
     _check(_lib.lib().vp_kl_fwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction), _ptr(kl),
-                                _ptr(ma), _ptr(logSa), _ptr(mb), _ptr(logSb), _stream()), "vp_kl_fwd")
-    return kl, ma, logSa, mb, logSb
+                                _ptr(stats_a), _ptr(stats_b), _stream()), "vp_kl_fwd")
+    return kl, stats_a, stats_b
 
 
-def vp_kl_bwd(a, b, direction, ma, logSa, mb, logSb, kl, grad, want_da=True, want_db=True, da=None, db=None):
+def vp_kl_bwd(a, b, direction, stats_a, stats_b, grad, want_da=True, want_db=True, da=None, db=None):
     """Returns (da, db); an unwanted gradient is None and is not computed."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
@@ -138,7 +151,7 @@ def vp_kl_bwd(a, b, direction, ma, logSa, mb, logSb, kl, grad, want_da=True, wan
         db = torch.empty((N, V), dtype=a.dtype, device=a.device)
     da = da if want_da else None
     db = db if want_db else None
-    _check(_lib.lib().vp_kl_bwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction), _ptr(ma),
-                                _ptr(logSa), _ptr(mb), _ptr(logSb), _ptr(kl), _ptr(grad), _ptr(da), _ptr(db),
-                                _stream()), "vp_kl_bwd")
+    _check(_lib.lib().vp_kl_bwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction),
+                                _ptr(stats_a), _ptr(stats_b), _ptr(grad), _ptr(da), _ptr(db), _stream()),
+           "vp_kl_bwd")
     return da, db

@@ -12,6 +12,8 @@
 #include "vp.h"
 #include "vp_launch.h"
 
+static_assert(sizeof(vp_rowstat) == 32, "vp_rowstat is 32 bytes");
+
 namespace {
 
 constexpr int64_t kMaxV = 2147483647LL;
@@ -56,109 +58,101 @@ extern "C" {
 
 vp_status vp_logprobs_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
                           int64_t s_i, int64_t vocab_start, const int64_t *targets, float *logp,
-                          float *m, float *logS, int32_t *err_word, vp_stream stream) {
+                          vp_rowstat *stats, int32_t *err_word, vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (N == 0) return VP_OK;
-    if (!x || !targets || !logp || !m || !logS) return VP_ERR_NULL;
-    if (!aligned(x, elem_size(dtype)) || !aligned(targets, 8) || !aligned(logp, 4) || !aligned(m, 4) ||
-        !aligned(logS, 4) || !aligned(err_word, 4))
+    if (!x || !targets || !logp || !stats) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(targets, 8) || !aligned(logp, 4) || !aligned(stats, 16) ||
+        !aligned(err_word, 4))
         return VP_ERR_ALIGN;
     if ((st = check_device()) != VP_OK) return st;
-    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, targets, logp, m, logS, err_word,
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, targets, logp, stats, err_word,
                     (cudaStream_t)stream};
     return launched(vp::launch_logprobs_fwd(a));
 }
 
 vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
-                          int64_t s_i, int64_t vocab_start, const int64_t *targets, const float *m,
-                          const float *logS, const float *grad_out, void *dx, int32_t *err_word,
-                          vp_stream stream) {
+                          int64_t s_i, int64_t vocab_start, const int64_t *targets, const vp_rowstat *stats,
+                          const float *grad_out, void *dx, int32_t *err_word, vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (N == 0) return VP_OK;
-    if (!x || !targets || !m || !logS || !grad_out || !dx) return VP_ERR_NULL;
+    if (!x || !targets || !stats || !grad_out || !dx) return VP_ERR_NULL;
     const size_t es = elem_size(dtype);
-    if (!aligned(x, es) || !aligned(dx, es) || !aligned(targets, 8) || !aligned(m, 4) || !aligned(logS, 4) ||
+    if (!aligned(x, es) || !aligned(dx, es) || !aligned(targets, 8) || !aligned(stats, 16) ||
         !aligned(grad_out, 4) || !aligned(err_word, 4))
         return VP_ERR_ALIGN;
     if ((st = check_device()) != VP_OK) return st;
-    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, m, logS, nullptr, grad_out, targets,
-                   dx, err_word, (cudaStream_t)stream};
+    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, stats, grad_out, targets, dx, err_word,
+                   (cudaStream_t)stream};
     return launched(vp::launch_logprobs_bwd(a));
 }
 
 vp_status vp_entropy_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
-                         float *H, float *m, float *logS, vp_stream stream) {
+                         float *H, vp_rowstat *stats, vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (N == 0) return VP_OK;
-    if (!x || !H || !m || !logS) return VP_ERR_NULL;
-    if (!aligned(x, elem_size(dtype)) || !aligned(H, 4) || !aligned(m, 4) || !aligned(logS, 4))
-        return VP_ERR_ALIGN;
+    if (!x || !H || !stats) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(H, 4) || !aligned(stats, 16)) return VP_ERR_ALIGN;
     if ((st = check_device()) != VP_OK) return st;
-    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, nullptr, H, m, logS, nullptr,
-                    (cudaStream_t)stream};
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, nullptr, H, stats, nullptr, (cudaStream_t)stream};
     return launched(vp::launch_entropy_fwd(a));
 }
 
 vp_status vp_entropy_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
-                         const float *m, const float *logS, const float *H, const float *grad_out, void *dx,
-                         vp_stream stream) {
+                         const vp_rowstat *stats, const float *grad_out, void *dx, vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (N == 0) return VP_OK;
-    if (!x || !m || !logS || !H || !grad_out || !dx) return VP_ERR_NULL;
+    if (!x || !stats || !grad_out || !dx) return VP_ERR_NULL;
     const size_t es = elem_size(dtype);
-    if (!aligned(x, es) || !aligned(dx, es) || !aligned(m, 4) || !aligned(logS, 4) || !aligned(H, 4) ||
-        !aligned(grad_out, 4))
-        return VP_ERR_ALIGN;
+    if (!aligned(x, es) || !aligned(dx, es) || !aligned(stats, 16) || !aligned(grad_out, 4)) return VP_ERR_ALIGN;
     if ((st = check_device()) != VP_OK) return st;
-    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, m, logS, H, grad_out, nullptr, dx, nullptr,
+    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, stats, grad_out, nullptr, dx, nullptr,
                    (cudaStream_t)stream};
     return launched(vp::launch_entropy_bwd(a));
 }
 
 vp_status vp_kl_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
-                    int64_t s_i, int direction, float *kl, float *ma, float *logSa, float *mb, float *logSb,
+                    int64_t s_i, int direction, float *kl, vp_rowstat *stats_a, vp_rowstat *stats_b,
                     vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
-    if (!a || !b || !kl || !ma || !logSa || !mb || !logSb) return VP_ERR_NULL;
+    if (!a || !b || !kl || !stats_a || !stats_b) return VP_ERR_NULL;
     const size_t es = elem_size(dtype);
-    if (!aligned(a, es) || !aligned(b, es) || !aligned(kl, 4) || !aligned(ma, 4) || !aligned(logSa, 4) ||
-        !aligned(mb, 4) || !aligned(logSb, 4))
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(kl, 4) || !aligned(stats_a, 16) || !aligned(stats_b, 16))
         return VP_ERR_ALIGN;
     if ((st = check_device()) != VP_OK) return st;
     const bool rev = direction == VP_KL_REVERSE;  // reverse: P = A, Q = B
     vp::KLFwdArgs k{rev ? a : b, rev ? b : a, dtype == VP_BF16, N, V, R, s_o, s_i, kl,
-                    rev ? ma : mb, rev ? logSa : logSb, rev ? mb : ma, rev ? logSb : logSa,
+                    rev ? (void *)stats_a : (void *)stats_b, rev ? (void *)stats_b : (void *)stats_a,
                     (cudaStream_t)stream};
     return launched(vp::launch_kl_fwd(k));
 }
 
 vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
-                    int64_t s_i, int direction, const float *ma, const float *logSa, const float *mb,
-                    const float *logSb, const float *kl, const float *grad_out, void *da, void *db,
-                    vp_stream stream) {
+                    int64_t s_i, int direction, const vp_rowstat *stats_a, const vp_rowstat *stats_b,
+                    const float *grad_out, void *da, void *db, vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
     if (!da && !db) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
-    if (!a || !b || !ma || !logSa || !mb || !logSb || !kl || !grad_out) return VP_ERR_NULL;
+    if (!a || !b || !stats_a || !stats_b || !grad_out) return VP_ERR_NULL;
     const size_t es = elem_size(dtype);
-    if (!aligned(a, es) || !aligned(b, es) || !aligned(da, es) || !aligned(db, es) || !aligned(ma, 4) ||
-        !aligned(logSa, 4) || !aligned(mb, 4) || !aligned(logSb, 4) || !aligned(kl, 4) ||
-        !aligned(grad_out, 4))
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(da, es) || !aligned(db, es) || !aligned(stats_a, 16) ||
+        !aligned(stats_b, 16) || !aligned(grad_out, 4))
         return VP_ERR_ALIGN;
     if ((st = check_device()) != VP_OK) return st;
     const bool rev = direction == VP_KL_REVERSE;
     vp::KLBwdArgs k{rev ? a : b, rev ? b : a, dtype == VP_BF16, N, V, R, s_o, s_i,
-                    rev ? ma : mb, rev ? logSa : logSb, rev ? mb : ma, rev ? logSb : logSa, kl, grad_out,
-                    rev ? da : db, rev ? db : da, (cudaStream_t)stream};
+                    rev ? (const void *)stats_a : (const void *)stats_b,
+                    rev ? (const void *)stats_b : (const void *)stats_a, grad_out, rev ? da : db, rev ? db : da,
+                    (cudaStream_t)stream};
     return launched(vp::launch_kl_bwd(k));
 }
 

@@ -10,12 +10,17 @@
 //        on the chunked backward: dz = onehot - exp(logits - lse), scaled by
 //        the upstream gradient.
 //
-// Gradients, per row with upstream g and p_j = exp((z_j - m) - logS):
+// Gradients, per row with upstream g, t_j = z_j - m and p_j = exp(t_j - logS),
+// written with the centred mean c of the forward's vp_rowstat record:
 //   logprobs  dz_j = g (onehot_{j,t} - p_j)
-//   entropy   dz_j = -g p_j (log p_j + H)                 (0 where p_j = 0)
-//   KL(P||Q)  dP_j = g p_j (log p_j - log q_j - KL)       (0 where p_j = 0)
+//   entropy   dz_j = -g p_j (log p_j + H)  = -g p_j (t_j - c)          (0 where p_j = 0)
+//   KL(P||Q)  dP_j = g p_j (log p_j - log q_j - KL)
+//                  = g p_j ((t^P_j - t^Q_j) - c)                       (0 where p_j = 0)
 //             dQ_j = g (q_j - p_j)
-// m and logS come from the forward and are never summed into one fp32 lse.
+// m is the exact row max, so t_j is exact; logS and c arrive as hi + lo pairs.
+// The fp32 path uses both halves and an error-free difference t^P - t^Q, so a
+// gradient that cancels to near zero keeps its accuracy; the bf16 path uses
+// the hi halves (its gradients are rounded to bf16).
 //
 // Shape: each CTA (256 threads) handles one tile of one row: up to 1024
 // 16-byte vectors of the input (8192 bf16 / 4096 fp32 logits), four loads in
@@ -31,8 +36,6 @@ constexpr int kTileVec = kBwdThreads * kBwdVecPerThread;
 
 enum RowMode { kNormal = 0, kZero = 1, kNaN = 2 };
 
-__device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
-
 template <typename T>
 __device__ __forceinline__ uint4 splat(float v) {
     float f[Elem<T>::kVec];
@@ -42,21 +45,44 @@ __device__ __forceinline__ uint4 splat(float v) {
 }
 
 // --------------------------------------------------------------------------
+// Element formulas
+// --------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float log_prob(float z, const RowStat &s, float &t) {
+    t = z - s.m;
+    return Elem<T>::kPrecise ? __fsub_rn(__fsub_rn(t, s.logS_hi), s.logS_lo) : t - s.logS_hi;
+}
+
+// (x - y) - c for the KL term, with c = c_hi + c_lo
+template <typename T>
+__device__ __forceinline__ float centred_ratio(float x, float y, const RowStat &s) {
+    if (Elem<T>::kPrecise) {
+        const DF d = two_sum(x, -y);  // x - y exactly, as d.hi + d.lo
+        return __fadd_rn(__fsub_rn(__fsub_rn(d.hi, s.c_hi), s.c_lo), d.lo);
+    }
+    return (x - y) - s.c_hi;
+}
+
+template <typename T>
+__device__ __forceinline__ float centred(float t, const RowStat &s) {
+    return Elem<T>::kPrecise ? __fsub_rn(__fsub_rn(t, s.c_hi), s.c_lo) : t - s.c_hi;
+}
+
+// kOp 0: logprobs, 1: entropy
+template <int kOp, typename T>
+__device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s, float g, int64_t loc) {
+    float t;
+    const float p = Elem<T>::exp(log_prob<T>(z, s, t));
+    if (kOp == 0) return (j == loc) ? g * (1.f - p) : -g * p;
+    return (p == 0.f) ? 0.f : -g * p * centred<T>(t, s);
+}
+
+// --------------------------------------------------------------------------
 // logprobs (kOp = 0) and entropy (kOp = 1)
 // --------------------------------------------------------------------------
 template <int kOp, typename T>
-__device__ __forceinline__ float grad_elem(float z, int64_t j, float m, float logS, float g, float H,
-                                           int64_t loc) {
-    const float lp = (z - m) - logS;
-    const float p = Elem<T>::exp(lp);
-    if (kOp == 0) return (j == loc) ? g * (1.f - p) : -g * p;
-    return (p == 0.f) ? 0.f : -g * p * (lp + H);
-}
-
-template <int kOp, typename T>
 __global__ void __launch_bounds__(kBwdThreads)
-grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__ m_in,
-            const float *__restrict__ logS_in, const float *__restrict__ H_in,
+grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict__ stats,
             const float *__restrict__ g_in, const int64_t *__restrict__ targets, int64_t vocab_start,
             T *__restrict__ dx, int32_t *__restrict__ err, int tiles_per_row, int64_t total_tiles) {
     constexpr int kVec = Elem<T>::kVec;
@@ -66,10 +92,10 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__
         const int seg = (int)(tile - r * tiles_per_row);
         const T *in = x + rows.off(r);
         T *out = dx + r * (int64_t)V;
-        const float m = m_in[r], logS = logS_in[r], g = g_in[r];
-        float H = 0.f;
+        const RowStat s = load_rowstat(stats + r);
+        const float g = g_in[r];
         int64_t loc = -1;
-        int mode = kNormal;
+        int mode = (s.flags & (kRowNanInf | kRowEmpty)) ? kNaN : kNormal;
         if (kOp == 0) {
             const int64_t t = targets[r];
             if (t < 0) {
@@ -79,13 +105,8 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__
                 if (loc < 0 || loc >= V) {
                     mode = kNaN;
                     if (err && seg == 0 && tid == 0) atomicOr(err, VP_ERRBIT_TARGET_);
-                } else if (!(fabsf(logS) < INFINITY)) {
-                    mode = kNaN;
                 }
             }
-        } else {
-            H = H_in[r];
-            if (H != H) mode = kNaN;
         }
 
         const int hin = head_count(in, V), hout = head_count(out, V);
@@ -96,12 +117,12 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__
             if (seg == 0) {
                 for (int j = tid; j < head; j += kBwdThreads) {
                     float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
-                              : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, m, logS, g, H, loc);
+                              : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, s, g, loc);
                     Elem<T>::store1(out + j, d);
                 }
                 for (int j = tail0 + tid; j < V; j += kBwdThreads) {
                     float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
-                              : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, m, logS, g, H, loc);
+                              : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, s, g, loc);
                     Elem<T>::store1(out + j, d);
                 }
             }
@@ -128,7 +149,7 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__
                     Elem<T>::unpack(u[k], z);
                     const int64_t j0 = head + (int64_t)i * kVec;
 #pragma unroll
-                    for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, m, logS, g, H, loc);
+                    for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, s, g, loc);
                     stg_stream(vout + i, Elem<T>::pack(d));
                 }
             }
@@ -137,7 +158,7 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__
             const int64_t e1 = min((int64_t)V, e0 + (int64_t)kTileVec * kVec);
             for (int64_t j = e0 + tid; j < e1; j += kBwdThreads) {
                 float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
-                          : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, m, logS, g, H, loc);
+                          : grad_elem<kOp, T>(Elem<T>::load1(in + j), j, s, g, loc);
                 Elem<T>::store1(out + j, d);
             }
         }
@@ -148,21 +169,21 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const float *__restrict__
 // KL(P||Q): dP and / or dQ
 // --------------------------------------------------------------------------
 template <typename T, bool kDP, bool kDQ>
-__device__ __forceinline__ void kl_grad_elem(float zp, float zq, float mp, float lsp, float mq, float lsq,
-                                             float g, float kl, bool p_nan, float &dp, float &dq) {
-    const float lp = (zp - mp) - lsp, lq = (zq - mq) - lsq;
-    const float p = Elem<T>::exp(lp), q = Elem<T>::exp(lq);
+__device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, float g,
+                                             bool p_nan, float &dp, float &dq) {
+    float tp, tq;
+    const float p = Elem<T>::exp(log_prob<T>(zp, sp, tp));
+    const float q = Elem<T>::exp(log_prob<T>(zq, sq, tq));
     if (kDQ) dq = g * (q - p);
-    if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * ((lp - lq) - kl);
+    if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * centred_ratio<T>(tp, tq, sp);
 }
 
 template <typename T, bool kDP, bool kDQ>
 __global__ void __launch_bounds__(kBwdThreads)
 kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,
-               const float *__restrict__ mp_in, const float *__restrict__ lsp_in,
-               const float *__restrict__ mq_in, const float *__restrict__ lsq_in,
-               const float *__restrict__ kl_in, const float *__restrict__ g_in, T *__restrict__ dP,
-               T *__restrict__ dQ, int tiles_per_row, int64_t total_tiles) {
+               const RowStat *__restrict__ stats_p, const RowStat *__restrict__ stats_q,
+               const float *__restrict__ g_in, T *__restrict__ dP, T *__restrict__ dQ, int tiles_per_row,
+               int64_t total_tiles) {
     constexpr int kVec = Elem<T>::kVec;
     const int tid = threadIdx.x;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -172,10 +193,12 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
         const T *prow = P + off, *qrow = Q + off;
         T *dprow = kDP ? dP + r * (int64_t)V : nullptr;
         T *dqrow = kDQ ? dQ + r * (int64_t)V : nullptr;
-        const float mp = mp_in[r], lsp = lsp_in[r], mq = mq_in[r], lsq = lsq_in[r];
-        const float g = g_in[r], kl = kl_in[r];
-        const bool all_nan = kl != kl;          // NaN row: both gradients NaN
-        const bool p_nan = !(kl < INFINITY);    // NaN or mismatch (+inf): dP is NaN
+        const RowStat sp = load_rowstat(stats_p + r), sq = load_rowstat(stats_q + r);
+        const float g = g_in[r];
+        // NaN row (NaN / +inf anywhere, or no finite P logit): both gradients NaN;
+        // support mismatch (KL = +inf): dP is NaN, dQ = g (q - p) stays finite
+        const bool all_nan = (sp.flags & (kRowNanInf | kRowEmpty)) || (sq.flags & kRowNanInf);
+        const bool p_nan = all_nan || (sp.flags & kRowMismatch);
 
         uintptr_t ph = (uintptr_t)prow & 15u;
         bool vec = (((uintptr_t)qrow & 15u) == ph);
@@ -186,8 +209,8 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
             for (int64_t j = j0 + tid; j < j1; j += kBwdThreads) {
                 float dp = qnan(), dq = qnan();
                 if (!all_nan)
-                    kl_grad_elem<T, kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), mp, lsp, mq,
-                                              lsq, g, kl, p_nan, dp, dq);
+                    kl_grad_elem<T, kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), sp, sq, g, p_nan,
+                                              dp, dq);
                 if (kDP) Elem<T>::store1(dprow + j, dp);
                 if (kDQ) Elem<T>::store1(dqrow + j, dq);
             }
@@ -207,17 +230,12 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
             const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + head);
             uint4 *vdp = kDP ? reinterpret_cast<uint4 *>(dprow + head) : nullptr;
             uint4 *vdq = kDQ ? reinterpret_cast<uint4 *>(dqrow + head) : nullptr;
-            if (all_nan) {
+            if (all_nan || (kDP && !kDQ && p_nan)) {
                 const uint4 c = splat<T>(qnan());
                 for (int i = v0 + tid; i < v1; i += kBwdThreads) {
                     if (kDP) stg_stream(vdp + i, c);
                     if (kDQ) stg_stream(vdq + i, c);
                 }
-                continue;
-            }
-            if (kDP && !kDQ && p_nan) {
-                const uint4 c = splat<T>(qnan());
-                for (int i = v0 + tid; i < v1; i += kBwdThreads) stg_stream(vdp + i, c);
                 continue;
             }
             uint4 up[kBwdVecPerThread], uq[kBwdVecPerThread];
@@ -235,7 +253,7 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
                     Elem<T>::unpack(uq[k], zq);
 #pragma unroll
                     for (int e = 0; e < kVec; ++e)
-                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], mp, lsp, mq, lsq, g, kl, p_nan, dp[e], dq[e]);
+                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], sp, sq, g, p_nan, dp[e], dq[e]);
                     if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
                     if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
                 }
@@ -264,8 +282,8 @@ static cudaError_t launch_grad(const GradArgs &a) {
     unsigned grid;
     tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
     grad_kernel<kOp, T><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.m, a.logS, a.H, a.g, a.targets,
-        a.vocab_start, static_cast<T *>(a.dx), a.err, tpr, total);
+        static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i}, static_cast<const RowStat *>(a.stats),
+        a.g, a.targets, a.vocab_start, static_cast<T *>(a.dx), a.err, tpr, total);
     return cudaGetLastError();
 }
 
@@ -284,8 +302,9 @@ static cudaError_t launch_kl_grad_t(const KLBwdArgs &a) {
     unsigned grid;
     tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
     kl_grad_kernel<T, kDP, kDQ><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.p), static_cast<const T *>(a.q), (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.mp,
-        a.logSp, a.mq, a.logSq, a.kl, a.g, static_cast<T *>(a.dp), static_cast<T *>(a.dq), tpr, total);
+        static_cast<const T *>(a.p), static_cast<const T *>(a.q), (int)a.V, Rows{a.R, a.s_o, a.s_i},
+        static_cast<const RowStat *>(a.stats_p), static_cast<const RowStat *>(a.stats_q), a.g,
+        static_cast<T *>(a.dp), static_cast<T *>(a.dq), tpr, total);
     return cudaGetLastError();
 }
 

@@ -2,27 +2,27 @@
 //
 // Sources:
 //   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL"
-//        (DeepSpeed pull request 8838).
+//        (DeepSpeed pull request 8838): second commit message and the
+//        reviewer's "Suggested change" (online max, sum-exp S and centred
+//        weighted sum W in one read; partials re-centred on the max), and the
+//        Codex thread "Guard zero rescaling before applying infinite shifts".
 //
-// Online statistics of one row slice, kept per thread and merged across
-// threads, warps and CTAs [P1, second commit message and the reviewer's
-// "Suggested change"]:
-//   m  running centre. On the fp32 path it is the exact running max. On the
-//      bf16 path it is a stale max that only moves when a value exceeds it by
-//      more than kTau (so the per-element exponent stays <= kTau and the
-//      rescale is rare); each thread also tracks its true max and re-centres
-//      on it before the merge, so the merged m is the exact row max on both
-//      paths,
-//   S  = sum_j e^{z_j - m},
-//   W  = sum_j e^{z_j - m} (z_j - m).
-// When the centre moves from m to m' the partial becomes
-//   S <- a S,  W <- a (W - (m' - m) S),  a = e^{m - m'},
-// and a term whose weight a S is exactly 0 is dropped, so an overflowing shift
-// (a row spanning +-3e38) never meets a zero weight as 0 * inf [P1, Codex
-// thread "Guard zero rescaling before applying infinite shifts"].
-//
-// The empty state has m = -FLT_MAX, S = W = 0: an all -inf slice leaves it
-// unchanged, and e^{-inf - (-FLT_MAX)} = 0 needs no special case.
+// Numerics of the online statistics (one distribution):
+//   Every lane keeps S = sum_j e^{z_j - ref} and W = sum_j e^{z_j - ref} (z_j - ref)
+//   against a centre `ref` that all 32 lanes of a warp share: the max of the
+//   warp's first round of loads. Terms are summed in fp32 over one round of
+//   loads and folded into double-float (hi + lo) accumulators with an
+//   error-free two-sum, so the row sums keep ~2^-40 relative accuracy beyond
+//   the per-term exponentials. Because a warp shares one centre, the warp merge
+//   is a plain double-float sum; the 16 warp partials are re-centred on the
+//   largest centre in fp64 (S <- a S, W <- a (W - d S), a = e^{-d}), terms of
+//   zero weight skipped [P1], and the row is finished in fp64.
+//   A lane moves its own centre only when a value exceeds it by more than
+//   kSpan (so e^{z - ref} cannot overflow); this happens only in rows whose
+//   values span more than kSpan natural-log units, and the warp then merges
+//   in fp64 with explicit re-centring.
+//   The empty state has ref = -FLT_MAX and S = W = 0: an all -inf slice leaves
+//   it unchanged and needs no special case.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -33,9 +33,23 @@ namespace vp {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -3.4028234663852886e38f;  // -FLT_MAX
+constexpr float kSpan = 64.0f;                       // largest exponent a lane accumulates
 constexpr int kFwdThreads = 512;
+constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr int kBwdThreads = 256;
 constexpr int kBwdVecPerThread = 4;
+
+constexpr uint32_t kRowNanInf = 1u, kRowEmpty = 2u, kRowMismatch = 4u;  // = VP_ROW_* of vp.h
+
+// Device-side image of vp_rowstat (32 bytes).
+struct RowStat {
+    float m, logS_hi, logS_lo, c_hi, c_lo;
+    uint32_t flags, r0, r1;
+};
+static_assert(sizeof(RowStat) == 32, "vp_rowstat is 32 bytes");
+
+__device__ __forceinline__ float qnan() { return __int_as_float(0x7fc00000); }
+__device__ __forceinline__ float pinf() { return __int_as_float(0x7f800000); }
 
 // ---------------------------------------------------------------------------
 // Row addressing: row r starts at (r / R) * s_o + (r % R) * s_i elements.
@@ -52,6 +66,7 @@ template <typename T> struct Elem;
 
 template <> struct Elem<float> {
     static constexpr int kVec = 4;
+    static constexpr bool kPrecise = true;   // fp32 gradients are held to 1e-6 absolute
     static __device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
     static __device__ __forceinline__ void unpack(const uint4 &u, float *v) {
         v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
@@ -62,13 +77,12 @@ template <> struct Elem<float> {
                           __float_as_uint(v[3]));
     }
     static __device__ __forceinline__ void store1(float *p, float v) { *p = v; }
-    // Accurate exponential for the fp32 path (gradients are held to 1e-6).
     static __device__ __forceinline__ float exp(float t) { return expf(t); }
-    static constexpr float kTau = 0.0f;  // exact running max
 };
 
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kVec = 8;
+    static constexpr bool kPrecise = false;  // bf16 gradients are held to one bf16 ulp
     static __device__ __forceinline__ float load1(const __nv_bfloat16 *p) {
         unsigned short u = __ldg(reinterpret_cast<const unsigned short *>(p));
         return __uint_as_float(((uint32_t)u) << 16);
@@ -89,8 +103,7 @@ template <> struct Elem<__nv_bfloat16> {
         return make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
     }
     static __device__ __forceinline__ void store1(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
-    static constexpr float kTau = 8.0f;  // allowed staleness of the centre (natural-log units)
-    // Hardware base-2 exponential; bf16 results need far less than fp32 accuracy.
+    // Hardware base-2 exponential (MUFU.EX2); results below 2^-126 flush to 0.
     static __device__ __forceinline__ float exp(float t) {
         float y;
         asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t * kLog2e));
@@ -120,142 +133,72 @@ __device__ __forceinline__ int head_count(const T *p, int V) {
 }
 
 // ---------------------------------------------------------------------------
-// (m, S, W) of one distribution.
+// Double-float accumulation (error-free transformations of Knuth's two-sum).
 // ---------------------------------------------------------------------------
-struct Stat {
-    float m, S, W;
-    __device__ __forceinline__ static Stat empty() { return {kNegBig, 0.f, 0.f}; }
+struct DF {
+    float hi, lo;
 };
 
-// Move the centre of a partial up to m_new (> s.m).
-template <bool kW>
-__device__ __forceinline__ void recentre(Stat &s, float m_new) {
-    float d = m_new - s.m;          // > 0, may overflow to +inf
-    float a = expf(-d);             // 0 when the shift is huge
-    if (kW) s.W = (a == 0.f) ? 0.f : a * (s.W - d * s.S);
-    s.S *= a;                       // keeps a NaN
-    s.m = m_new;
+__device__ __forceinline__ DF two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
 }
 
-// Fold partial b into the running merge o (o.m already the max of both).
-template <bool kW>
-__device__ __forceinline__ void fold(Stat &o, const Stat &b) {
-    float a = (b.m == o.m) ? 1.f : expf(b.m - o.m);
-    float w = a * b.S;
-    if (w != 0.f) {                 // zero-weight partials are skipped; NaN is kept
-        o.S += w;
-        if (kW) o.W += a * (b.W - (o.m - b.m) * b.S);
-    }
+// acc += x
+__device__ __forceinline__ void df_add(DF &acc, float x) {
+    const DF t = two_sum(acc.hi, x);
+    acc.hi = t.hi;
+    acc.lo = __fadd_rn(acc.lo, t.lo);
 }
 
-template <bool kW>
-__device__ __forceinline__ Stat merge(const Stat &x, const Stat &y) {
-    Stat o;
-    o.m = fmaxf(x.m, y.m);
-    o.S = 0.f;
-    o.W = 0.f;
-    fold<kW>(o, x);
-    fold<kW>(o, y);
-    return o;
+// acc += y (both double-float)
+__device__ __forceinline__ void df_add(DF &acc, const DF &y) {
+    const DF t = two_sum(acc.hi, y.hi);
+    acc.hi = t.hi;
+    acc.lo = __fadd_rn(__fadd_rn(acc.lo, y.lo), t.lo);
 }
 
-template <bool kW>
-__device__ __forceinline__ Stat shfl_down(const Stat &s, int off) {
-    Stat o;
-    o.m = __shfl_down_sync(0xffffffffu, s.m, off);
-    o.S = __shfl_down_sync(0xffffffffu, s.S, off);
-    o.W = kW ? __shfl_down_sync(0xffffffffu, s.W, off) : 0.f;
-    return o;
+__device__ __forceinline__ double df_value(const DF &a) { return (double)a.hi + (double)a.lo; }
+
+__device__ __forceinline__ DF df_from(double v) {
+    const float hi = (float)v;
+    // NaN / inf pass through hi; lo is 0 then
+    const float lo = isfinite(v) ? (float)(v - (double)hi) : 0.f;
+    return {hi, lo};
 }
 
-// Block-wide merge in a fixed order; the result is valid in thread 0.
-template <bool kW, int kThreads>
-__device__ __forceinline__ Stat block_merge(Stat s) {
-    __shared__ Stat part[kThreads / 32];
+__device__ __forceinline__ DF shfl_xor(const DF &a, int m) {
+    return {__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
+}
+
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s = merge<kW>(s, shfl_down<kW>(s, off));
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) part[warp] = s;
-    __syncthreads();
-    if (warp == 0) {
-        s = lane < kThreads / 32 ? part[lane] : Stat::empty();
+    for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s = merge<kW>(s, shfl_down<kW>(s, off));
-    }
-    return s;
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
 }
 
-// ---------------------------------------------------------------------------
-// Paired statistics for KL(P||Q): (m_P, S_P, m_Q, S_Q, W, flag) with
-// W = sum_{p_j > 0} e^{P_j - m_P} ((P_j - m_P) - (Q_j - m_Q)) and flag set
-// when some P_j > -inf has Q_j = -inf [P1, reviewer's suggested change].
-// Moving the centres by (dp, dq) turns W into a_P (W - (dp - dq) S_P).
-// ---------------------------------------------------------------------------
-struct KLStat {
-    float mp, Sp, mq, Sq, W;
-    int flag;
-    __device__ __forceinline__ static KLStat empty() { return {kNegBig, 0.f, kNegBig, 0.f, 0.f, 0}; }
-};
-
-__device__ __forceinline__ void kl_recentre(KLStat &s, float mp_new, float mq_new) {
-    float dp = mp_new - s.mp, dq = mq_new - s.mq;   // >= 0
-    float ap = (dp == 0.f) ? 1.f : expf(-dp);
-    float aq = (dq == 0.f) ? 1.f : expf(-dq);
-    s.W = (ap == 0.f) ? 0.f : ap * (s.W - (dp - dq) * s.Sp);
-    s.Sp *= ap;
-    s.Sq *= aq;
-    s.mp = mp_new;
-    s.mq = mq_new;
+__device__ __forceinline__ void store_rowstat(RowStat *dst, float m, double logS, double c, uint32_t flags) {
+    const DF l = df_from(logS), cc = df_from(c);
+    RowStat s{m, l.hi, l.lo, cc.hi, cc.lo, flags, 0u, 0u};
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    const uint4 *src = reinterpret_cast<const uint4 *>(&s);
+    d[0] = src[0];
+    d[1] = src[1];
 }
 
-__device__ __forceinline__ void kl_fold(KLStat &o, const KLStat &b) {
-    float ap = (b.mp == o.mp) ? 1.f : expf(b.mp - o.mp);
-    float aq = (b.mq == o.mq) ? 1.f : expf(b.mq - o.mq);
-    float wq = aq * b.Sq;
-    if (wq != 0.f) o.Sq += wq;
-    float wp = ap * b.Sp;
-    if (wp != 0.f) {
-        o.Sp += wp;
-        o.W += ap * (b.W - ((o.mp - b.mp) - (o.mq - b.mq)) * b.Sp);
-    }
-    o.flag |= b.flag;
-}
-
-__device__ __forceinline__ KLStat kl_merge(const KLStat &x, const KLStat &y) {
-    KLStat o;
-    o.mp = fmaxf(x.mp, y.mp);
-    o.mq = fmaxf(x.mq, y.mq);
-    o.Sp = o.Sq = o.W = 0.f;
-    o.flag = 0;
-    kl_fold(o, x);
-    kl_fold(o, y);
-    return o;
-}
-
-__device__ __forceinline__ KLStat kl_shfl_down(const KLStat &s, int off) {
-    KLStat o;
-    o.mp = __shfl_down_sync(0xffffffffu, s.mp, off);
-    o.Sp = __shfl_down_sync(0xffffffffu, s.Sp, off);
-    o.mq = __shfl_down_sync(0xffffffffu, s.mq, off);
-    o.Sq = __shfl_down_sync(0xffffffffu, s.Sq, off);
-    o.W = __shfl_down_sync(0xffffffffu, s.W, off);
-    o.flag = __shfl_down_sync(0xffffffffu, s.flag, off);
-    return o;
-}
-
-template <int kThreads>
-__device__ __forceinline__ KLStat kl_block_merge(KLStat s) {
-    __shared__ KLStat part[kThreads / 32];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s = kl_merge(s, kl_shfl_down(s, off));
-    int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) part[warp] = s;
-    __syncthreads();
-    if (warp == 0) {
-        s = lane < kThreads / 32 ? part[lane] : KLStat::empty();
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s = kl_merge(s, kl_shfl_down(s, off));
-    }
+__device__ __forceinline__ RowStat load_rowstat(const RowStat *p) {
+    RowStat s;
+    uint4 *d = reinterpret_cast<uint4 *>(&s);
+    d[0] = __ldg(reinterpret_cast<const uint4 *>(p));
+    d[1] = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
     return s;
 }
 

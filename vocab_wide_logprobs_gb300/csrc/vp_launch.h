@@ -14,7 +14,8 @@ struct StatsArgs {
     bool bf16;
     int64_t N, V, R, s_o, s_i, vocab_start;
     const int64_t *targets;
-    float *out, *m, *logS;
+    float *out;
+    void *stats;  // vp_rowstat [N]
     int32_t *err;
     cudaStream_t stream;
 };
@@ -23,7 +24,8 @@ struct KLFwdArgs {
     const void *p, *q;
     bool bf16;
     int64_t N, V, R, s_o, s_i;
-    float *kl, *mp, *logSp, *mq, *logSq;
+    float *kl;
+    void *stats_p, *stats_q;
     cudaStream_t stream;
 };
 
@@ -31,7 +33,8 @@ struct GradArgs {
     const void *x;
     bool bf16;
     int64_t N, V, R, s_o, s_i, vocab_start;
-    const float *m, *logS, *H, *g;
+    const void *stats;
+    const float *g;
     const int64_t *targets;
     void *dx;
     int32_t *err;
@@ -42,7 +45,8 @@ struct KLBwdArgs {
     const void *p, *q;
     bool bf16;
     int64_t N, V, R, s_o, s_i;
-    const float *mp, *logSp, *mq, *logSq, *kl, *g;
+    const void *stats_p, *stats_q;
+    const float *g;
     void *dp, *dq;
     cudaStream_t stream;
 };
