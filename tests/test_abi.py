@@ -74,6 +74,7 @@ def test_status_codes_for_bad_arguments():
     args = (FAKE, FAKE, 1, 4, 16, 4, 0, 16)
     assert L.vp_kl_fwd(*args, 2, FAKE, FAKE, FAKE, None) == ERR_ARG
     assert L.vp_kl_bwd(*args, 0, FAKE, FAKE, FAKE, None, None, None) == ERR_ARG
+    assert L.vp_kl_bwd(FAKE, FAKE, 1, 0, 16, 4, 0, 16, 0, FAKE, FAKE, FAKE, None, None, None) == OK
     assert L.vp_logprobs_fwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE_ODD, FAKE, FAKE, None, None) == ERR_ALIGN
     assert L.vp_logprobs_bwd(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE, FAKE, FAKE, None, None, None) == ERR_NULL
 

@@ -140,8 +140,8 @@ vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t 
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
     if (st != VP_OK) return st;
     if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
-    if (!da && !db) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
+    if (!da && !db) return VP_ERR_ARG;
     if (!a || !b || !stats_a || !stats_b || !grad_out) return VP_ERR_NULL;
     const size_t es = elem_size(dtype);
     if (!aligned(a, es) || !aligned(b, es) || !aligned(da, es) || !aligned(db, es) || !aligned(stats_a, 16) ||

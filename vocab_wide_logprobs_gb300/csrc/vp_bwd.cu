@@ -45,36 +45,56 @@ __device__ __forceinline__ uint4 splat(float v) {
 }
 
 // --------------------------------------------------------------------------
-// Element formulas
+// Element formulas. The fp32 path carries t, log p and the centred factor as
+// double-floats, takes an accurate exponential and rounds each gradient once;
+// the bf16 path uses fp32 arithmetic and the hardware exponential.
 // --------------------------------------------------------------------------
-template <typename T>
-__device__ __forceinline__ float log_prob(float z, const RowStat &s, float &t) {
-    t = z - s.m;
-    return Elem<T>::kPrecise ? __fsub_rn(__fsub_rn(t, s.logS_hi), s.logS_lo) : t - s.logS_hi;
-}
-
-// (x - y) - c for the KL term, with c = c_hi + c_lo
-template <typename T>
-__device__ __forceinline__ float centred_ratio(float x, float y, const RowStat &s) {
-    if (Elem<T>::kPrecise) {
-        const DF d = two_sum(x, -y);  // x - y exactly, as d.hi + d.lo
-        return __fadd_rn(__fsub_rn(__fsub_rn(d.hi, s.c_hi), s.c_lo), d.lo);
-    }
-    return (x - y) - s.c_hi;
-}
-
-template <typename T>
-__device__ __forceinline__ float centred(float t, const RowStat &s) {
-    return Elem<T>::kPrecise ? __fsub_rn(__fsub_rn(t, s.c_hi), s.c_lo) : t - s.c_hi;
-}
-
-// kOp 0: logprobs, 1: entropy
 template <int kOp, typename T>
 __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s, float g, int64_t loc) {
-    float t;
-    const float p = Elem<T>::exp(log_prob<T>(z, s, t));
-    if (kOp == 0) return (j == loc) ? g * (1.f - p) : -g * p;
-    return (p == 0.f) ? 0.f : -g * p * centred<T>(t, s);
+    if constexpr (Elem<T>::kPrecise) {
+        const DF t = df_diff(z, s.m);
+        const DF lp = df_sub(t, s.logS_hi, s.logS_lo);
+        const DF p = exp_df(lp.hi, lp.lo);
+        if (kOp == 0) {                                   // g (onehot - p)
+            const DF d = df_sub(DF{j == loc ? 1.f : 0.f, 0.f}, p.hi, p.lo);
+            return df_mul_round(DF{g, 0.f}, d);
+        }
+        if (p.hi == 0.f) return 0.f;                      // -g p (t - c)
+        const DF r = df_sub(t, s.c_hi, s.c_lo);
+        const float gp = -g * p.hi;
+        const DF gpd{gp, fmaf(-g, p.hi, -gp) - g * p.lo};
+        return df_mul_round(gpd, r);
+    } else {
+        const float t = z - s.m;
+        const float p = Elem<T>::exp(t - s.logS_hi);
+        if (kOp == 0) return (j == loc) ? g * (1.f - p) : -g * p;
+        return (p == 0.f) ? 0.f : -g * p * (t - s.c_hi);
+    }
+}
+
+template <typename T, bool kDP, bool kDQ>
+__device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, float g,
+                                             bool p_nan, float &dp, float &dq) {
+    if constexpr (Elem<T>::kPrecise) {
+        const DF tp = df_diff(zp, sp.m), tq = df_diff(zq, sq.m);
+        const DF lp = df_sub(tp, sp.logS_hi, sp.logS_lo), lq = df_sub(tq, sq.logS_hi, sq.logS_lo);
+        const DF p = exp_df(lp.hi, lp.lo), q = exp_df(lq.hi, lq.lo);
+        if (kDQ) dq = df_mul_round(DF{g, 0.f}, df_sub(q, p.hi, p.lo));   // g (q - p)
+        if (kDP) {                                                     // g p ((tP - tQ) - c)
+            if (p_nan) dp = qnan();
+            else if (p.hi == 0.f) dp = 0.f;
+            else {
+                const DF r = df_sub(df_sub(tp, tq.hi, tq.lo), sp.c_hi, sp.c_lo);
+                const float gp = g * p.hi;
+                dp = df_mul_round(DF{gp, fmaf(g, p.hi, -gp) + g * p.lo}, r);
+            }
+        }
+    } else {
+        const float tp = zp - sp.m, tq = zq - sq.m;
+        const float p = Elem<T>::exp(tp - sp.logS_hi), q = Elem<T>::exp(tq - sq.logS_hi);
+        if (kDQ) dq = g * (q - p);
+        if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * ((tp - tq) - sp.c_hi);
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -168,16 +188,6 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
 // --------------------------------------------------------------------------
 // KL(P||Q): dP and / or dQ
 // --------------------------------------------------------------------------
-template <typename T, bool kDP, bool kDQ>
-__device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, float g,
-                                             bool p_nan, float &dp, float &dq) {
-    float tp, tq;
-    const float p = Elem<T>::exp(log_prob<T>(zp, sp, tp));
-    const float q = Elem<T>::exp(log_prob<T>(zq, sq, tq));
-    if (kDQ) dq = g * (q - p);
-    if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * centred_ratio<T>(tp, tq, sp);
-}
-
 template <typename T, bool kDP, bool kDQ>
 __global__ void __launch_bounds__(kBwdThreads)
 kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,

@@ -169,6 +169,67 @@ __device__ __forceinline__ DF df_from(double v) {
     return {hi, lo};
 }
 
+// hi + lo when |hi| >= |lo| (Dekker's fast two-sum)
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+// a - b as a double-float (exact)
+__device__ __forceinline__ DF df_diff(float a, float b) { return two_sum(a, -b); }
+
+// (x_hi + x_lo) - (y_hi + y_lo) as a double-float, accurate to ~2^-44 relative
+__device__ __forceinline__ DF df_sub(const DF &x, float y_hi, float y_lo) {
+    const DF d = two_sum(x.hi, -y_hi);
+    return {d.hi, __fadd_rn(d.lo, __fsub_rn(x.lo, y_lo))};
+}
+
+// Accurate e^(a_hi + a_lo) as a double-float (relative error ~1e-8).
+// Method (Cody and Waite's argument reduction followed by a Taylor series):
+//   k = nearest integer to a / ln 2, r = a - k ln 2 with ln 2 split into three
+//   parts so that k * part is exact for the first two (|k| < 256), giving r as
+//   a double-float with |r| <= ln 2 / 2; then e^r = 1 + r + sum_{n=2..9} r^n / n!
+//   (truncation error < 3e-10), the tail evaluated in fp32 by Horner's rule;
+//   finally the result is scaled by 2^k. Arguments below -104 give 0 (the
+//   fp32 result underflows); NaN propagates.
+__device__ __forceinline__ DF exp_df(float a_hi, float a_lo) {
+    constexpr float kL1 = 0.693145751953125f;        // ln 2, 16 significant bits
+    constexpr float kL2 = 1.4286197256296873e-06f;   // next 16 bits
+    constexpr float kL3 = -1.2905320041778356e-11f;  // remainder
+    if (!(a_hi > -104.f)) return {a_hi != a_hi ? a_hi : 0.f, 0.f};
+    const float k = rintf(a_hi * kLog2e);
+    const float x1 = fmaf(-k, kL1, a_hi);             // exact
+    DF r = two_sum(x1, -k * kL2);                     // k * kL2 exact
+    r.lo = __fadd_rn(r.lo, fmaf(-k, kL3, a_lo));
+    const float h = r.hi;
+    float t = 2.7557318844628753e-06f;                // 1/9!
+    t = fmaf(t, h, 2.4801587642286904e-05f);          // 1/8!
+    t = fmaf(t, h, 1.9841270113829523e-04f);          // 1/7!
+    t = fmaf(t, h, 1.3888889225199819e-03f);          // 1/6!
+    t = fmaf(t, h, 8.3333337679505350e-03f);          // 1/5!
+    t = fmaf(t, h, 4.1666667908430100e-02f);          // 1/4!
+    t = fmaf(t, h, 1.6666667163372040e-01f);          // 1/3!
+    t = fmaf(t, h, 0.5f);                             // 1/2!
+    const float tail = (h * h) * t;                   // r^2/2! + ... + r^9/9!
+    const DF s = fast_two_sum(1.f, h);                // 1 + r_hi
+    const float lo = __fadd_rn(__fadd_rn(s.lo, r.lo), fmaf(h, r.lo, tail));
+    DF e = fast_two_sum(s.hi, lo);
+    // scale by 2^k in two exact steps (k in [-151, 128])
+    const int ki = (int)k;
+    const int k1 = ki / 2, k2 = ki - k1;
+    const float f1 = __int_as_float((k1 + 127) << 23), f2 = __int_as_float((k2 + 127) << 23);
+    e.hi = (e.hi * f1) * f2;
+    e.lo = (e.lo * f1) * f2;
+    return e;
+}
+
+// Product (x_hi + x_lo) * (y_hi + y_lo) rounded once to fp32.
+__device__ __forceinline__ float df_mul_round(const DF &x, const DF &y) {
+    const float p = x.hi * y.hi;
+    const float pe = fmaf(x.hi, y.hi, -p);
+    return p + fmaf(x.hi, y.lo, fmaf(x.lo, y.hi, pe));
+}
+
 __device__ __forceinline__ DF shfl_xor(const DF &a, int m) {
     return {__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
 }

@@ -58,17 +58,32 @@ struct Lane1 {
         for (int i = 1; i < n; ++i) c = fmaxf(c, v[i]);
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
-        float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
+        if constexpr (Elem<T>::kPrecise) {
+            // fp32 inputs: exact centred value, accurate exponential, double-float sums
 #pragma unroll
-        for (int i = 0; i < n; ++i) {
-            const float t = v[i] - ref;
-            const float e = Elem<T>::exp(t);
-            // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
-            if (i & 1) { s1 += e; if (kW) w1 = fmaf(e, fmaxf(t, -128.f), w1); }
-            else       { s0 += e; if (kW) w0 = fmaf(e, fmaxf(t, -128.f), w0); }
+            for (int i = 0; i < n; ++i) {
+                const DF t = df_diff(v[i], ref);
+                const DF e = exp_df(t.hi, t.lo);
+                df_add(S, e);
+                if (kW && e.hi != 0.f) {
+                    const float p = e.hi * t.hi;
+                    const float pe = fmaf(e.hi, t.lo, fmaf(e.lo, t.hi, fmaf(e.hi, t.hi, -p)));
+                    df_add(W, DF{p, pe});
+                }
+            }
+        } else {
+            float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+                const float t = v[i] - ref;   // exact for bf16 values
+                const float e = Elem<T>::exp(t);
+                // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
+                if (i & 1) { s1 += e; if (kW) w1 = fmaf(e, fmaxf(t, -128.f), w1); }
+                else       { s0 += e; if (kW) w0 = fmaf(e, fmaxf(t, -128.f), w0); }
+            }
+            df_add(S, s0 + s1);
+            if (kW) df_add(W, w0 + w1);
         }
-        df_add(S, s0 + s1);
-        if (kW) df_add(W, w0 + w1);
     }
 };
 
@@ -261,20 +276,37 @@ struct LaneKL {
         mxq = fmaxf(mxq, cq);
         const bool up = cp > rp + kSpan, uq = cq > rq + kSpan;
         if (up || uq) move_centres(up ? cp : rp, uq ? cq : rq);
-        float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
         int fl = 0;
+        if constexpr (Elem<T>::kPrecise) {
 #pragma unroll
-        for (int i = 0; i < n; ++i) {
-            const float tp = p[i] - rp, tq = q[i] - rq;
-            const float ep = Elem<T>::exp(tp), eq = Elem<T>::exp(tq);
-            const float dl = (ep > 0.f) ? (tp - tq) : 0.f;  // zero-weight terms add nothing
-            if (i & 1) { sp1 += ep; sq1 += eq; w1 = fmaf(ep, dl, w1); }
-            else       { sp0 += ep; sq0 += eq; w0 = fmaf(ep, dl, w0); }
-            fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+            for (int i = 0; i < n; ++i) {
+                const DF tp = df_diff(p[i], rp), tq = df_diff(q[i], rq);
+                const DF ep = exp_df(tp.hi, tp.lo), eq = exp_df(tq.hi, tq.lo);
+                df_add(Sp, ep);
+                df_add(Sq, eq);
+                if (ep.hi != 0.f) {              // zero-weight terms add nothing
+                    const DF d = df_sub(tp, tq.hi, tq.lo);
+                    const float pr = ep.hi * d.hi;
+                    const float pe = fmaf(ep.hi, d.lo, fmaf(ep.lo, d.hi, fmaf(ep.hi, d.hi, -pr)));
+                    df_add(W, DF{pr, pe});
+                }
+                fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+            }
+        } else {
+            float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+                const float tp = p[i] - rp, tq = q[i] - rq;
+                const float ep = Elem<T>::exp(tp), eq = Elem<T>::exp(tq);
+                const float dl = (ep > 0.f) ? (tp - tq) : 0.f;  // zero-weight terms add nothing
+                if (i & 1) { sp1 += ep; sq1 += eq; w1 = fmaf(ep, dl, w1); }
+                else       { sp0 += ep; sq0 += eq; w0 = fmaf(ep, dl, w0); }
+                fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+            }
+            df_add(Sp, sp0 + sp1);
+            df_add(Sq, sq0 + sq1);
+            df_add(W, w0 + w1);
         }
-        df_add(Sp, sp0 + sp1);
-        df_add(Sq, sq0 + sq1);
-        df_add(W, w0 + w1);
         flag |= fl;
     }
 };
