@@ -201,6 +201,14 @@ VP_API vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, i
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                      */
 /* ------------------------------------------------------------------------ */
+
+/* Reads the library's device fault word of the current device into *value
+ * and, when `clear` is non-zero, resets it. The word is non-zero only if a
+ * kernel's bounded wait on its copy pipeline gave up (bit 0: producer, bit 1:
+ * consumer); that kernel then skipped its outputs and returned instead of
+ * spinning. Unlike every other call, this one synchronises with the device.
+ * (No counterpart on the pages: a safety net of this implementation.) */
+VP_API vp_status vp_fault_status(uint32_t *value, int clear);
 VP_API const char *vp_status_string(int status);
 VP_API int vp_version(void);
 

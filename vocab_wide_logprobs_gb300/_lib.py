@@ -44,6 +44,8 @@ def lib():
                 fn.restype = ctypes.c_int
             h.vp_status_string.argtypes = [ctypes.c_int]
             h.vp_status_string.restype = ctypes.c_char_p
+            h.vp_fault_status.argtypes = [P, I32]
+            h.vp_fault_status.restype = ctypes.c_int
             h.vp_version.argtypes = []
             h.vp_version.restype = ctypes.c_int
             _handle = h

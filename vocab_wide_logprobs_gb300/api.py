@@ -155,3 +155,10 @@ def vp_kl_bwd(a, b, direction, stats_a, stats_b, grad, want_da=True, want_db=Tru
                                 _ptr(stats_a), _ptr(stats_b), _ptr(grad), _ptr(da), _ptr(db), _stream()),
            "vp_kl_bwd")
     return da, db
+
+
+def vp_fault_status(clear: bool = False) -> int:
+    """The device fault word (non-zero if a kernel's bounded wait gave up); synchronises."""
+    v = ctypes.c_uint32(0)
+    _check(_lib.lib().vp_fault_status(ctypes.byref(v), int(clear)), "vp_fault_status")
+    return int(v.value)

@@ -156,6 +156,13 @@ vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t 
     return launched(vp::launch_kl_bwd(k));
 }
 
+vp_status vp_fault_status(uint32_t *value, int clear) {
+    if (!value) return VP_ERR_NULL;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    return vp::read_fault(value, clear != 0) == cudaSuccess ? VP_OK : VP_ERR_LAUNCH;
+}
+
 const char *vp_status_string(int status) {
     switch (status) {
         case VP_OK: return "ok";

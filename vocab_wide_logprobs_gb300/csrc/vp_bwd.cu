@@ -49,6 +49,27 @@ __device__ __forceinline__ uint4 splat(float v) {
 // double-floats, takes an accurate exponential and rounds each gradient once;
 // the bf16 path uses fp32 arithmetic and the hardware exponential.
 // --------------------------------------------------------------------------
+// e^x - 1 for |x| < 1/2 by its Taylor series to x^8/8! (relative error < 1e-8 there):
+// used where e^x - 1 would cancel.
+__device__ __forceinline__ float expm1_small(float x) {
+    float t = 2.4801587301587302e-05f;      // 1/8!
+    t = fmaf(t, x, 1.9841269841269841e-04f);  // 1/7!
+    t = fmaf(t, x, 1.3888888888888889e-03f);  // 1/6!
+    t = fmaf(t, x, 8.3333333333333333e-03f);  // 1/5!
+    t = fmaf(t, x, 4.1666666666666667e-02f);  // 1/4!
+    t = fmaf(t, x, 1.6666666666666667e-01f);  // 1/3!
+    t = fmaf(t, x, 0.5f);                     // 1/2!
+    return fmaf(t * x, x, x);                 // x + x^2 (1/2 + x/6 + ...)
+}
+
+// q - p from p = e^{lp}, q = e^{lq} and delta = lq - lp: where |delta| < 1/2 the
+// difference is formed as p (e^delta - 1) (or -q (e^-delta - 1)) so it keeps its
+// relative accuracy as q -> p.
+__device__ __forceinline__ float diff_of_probs(float q, float p, float delta) {
+    if (fabsf(delta) < 0.5f) return delta < 0.f ? p * expm1_small(delta) : -q * expm1_small(-delta);
+    return q - p;
+}
+
 template <int kOp, typename T>
 __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s, float g, int64_t loc) {
     if constexpr (Elem<T>::kPrecise) {
@@ -66,15 +87,20 @@ __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s,
         return df_mul_round(gpd, r);
     } else {
         const float t = z - s.m;
-        const float p = Elem<T>::exp(t - s.logS_hi);
-        if (kOp == 0) return (j == loc) ? g * (1.f - p) : -g * p;
-        return (p == 0.f) ? 0.f : -g * p * (t - s.c_hi);
+        const float lp = t - s.logS_hi;
+        const float p = Elem<T>::exp(lp);
+        if (kOp == 0) {
+            if (j != loc) return -g * p;
+            return g * (lp > -0.5f ? -expm1_small(lp) : 1.f - p);   // 1 - p without cancellation
+        }
+        return (p == 0.f) ? 0.f : -g * p * ((t - s.c_hi) - s.c_lo);
     }
 }
 
+// dlq: log S_Q - log S_P as a double-float (a per-row constant of the bf16 path)
 template <typename T, bool kDP, bool kDQ>
 __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, float g,
-                                             bool p_nan, float &dp, float &dq) {
+                                             bool p_nan, const DF &dls, float &dp, float &dq) {
     if constexpr (Elem<T>::kPrecise) {
         const DF tp = df_diff(zp, sp.m), tq = df_diff(zq, sq.m);
         const DF lp = df_sub(tp, sp.logS_hi, sp.logS_lo), lq = df_sub(tq, sq.logS_hi, sq.logS_lo);
@@ -90,10 +116,10 @@ __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &
             }
         }
     } else {
-        const float tp = zp - sp.m, tq = zq - sq.m;
+        const float tp = zp - sp.m, tq = zq - sq.m;          // exact for bf16 values
         const float p = Elem<T>::exp(tp - sp.logS_hi), q = Elem<T>::exp(tq - sq.logS_hi);
-        if (kDQ) dq = g * (q - p);
-        if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * ((tp - tq) - sp.c_hi);
+        if (kDQ) dq = g * diff_of_probs(q, p, ((tq - tp) - dls.hi) - dls.lo);
+        if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * (((tp - tq) - sp.c_hi) - sp.c_lo);
     }
 }
 
@@ -209,6 +235,8 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
         // support mismatch (KL = +inf): dP is NaN, dQ = g (q - p) stays finite
         const bool all_nan = (sp.flags & (kRowNanInf | kRowEmpty)) || (sq.flags & kRowNanInf);
         const bool p_nan = all_nan || (sp.flags & kRowMismatch);
+        DF dls = two_sum(sq.logS_hi, -sp.logS_hi);
+        dls.lo = __fadd_rn(dls.lo, __fsub_rn(sq.logS_lo, sp.logS_lo));
 
         uintptr_t ph = (uintptr_t)prow & 15u;
         bool vec = (((uintptr_t)qrow & 15u) == ph);
@@ -220,7 +248,7 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
                 float dp = qnan(), dq = qnan();
                 if (!all_nan)
                     kl_grad_elem<T, kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), sp, sq, g, p_nan,
-                                              dp, dq);
+                                              dls, dp, dq);
                 if (kDP) Elem<T>::store1(dprow + j, dp);
                 if (kDQ) Elem<T>::store1(dqrow + j, dq);
             }
@@ -263,7 +291,7 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
                     Elem<T>::unpack(uq[k], zq);
 #pragma unroll
                     for (int e = 0; e < kVec; ++e)
-                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], sp, sq, g, p_nan, dp[e], dq[e]);
+                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], sp, sq, g, p_nan, dls, dp[e], dq[e]);
                     if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
                     if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
                 }

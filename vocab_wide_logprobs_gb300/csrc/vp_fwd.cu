@@ -1,4 +1,4 @@
-// vp_fwd.cu -- single-read forward kernels: logprobs, entropy, KL statistics.
+// vp_fwd.cu -- CTA-per-row KL forward, for A and B rows that differ modulo 16 bytes.
 //
 // Sources:
 //   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL"
@@ -11,372 +11,23 @@
 //   [P2] page "[Feat][Kernel] Add TP Fused linear logp Triton", "Implementation"
 //        (logp = target logit - LSE).
 //
-// Shape: one CTA of 512 threads (16 warps) per row. The row is read once with
-// 16-byte non-caching loads, four in flight per thread (two of A and two of B
-// for KL); a scalar head and tail cover rows that do not start on a 16-byte
-// boundary. Each warp accumulates against one shared centre (the max of its
+// The persistent TMA-ring kernels of vp_fwd_tma.cu copy P and Q rows with one
+// shared 16-byte phase; when A and B differ modulo 16 bytes this kernel reads
+// them instead. Shape: one CTA of 512 threads (16 warps) per row, the row read
+// once with 16-byte non-caching loads (two of P and two of Q in flight per
+// thread), or element by element when P and Q cannot both be read as vectors. Each warp accumulates against one shared centre (the max of its
 // first round of loads), so merging its lanes is a double-float sum; the 16
 // warp partials are re-centred and merged in fp64 by warp 0, which also
 // finishes the row in fp64 and writes the fp32 output and the vp_rowstat
 // record. The decomposition depends only on V, the dtype and the row's address
 // modulo 16, so a row's result does not depend on N or on the other rows.
-#include "vp_device.cuh"
-#include "vp_launch.h"
+#include "vp_stats.cuh"
 
 namespace vp {
 
 // ---------------------------------------------------------------------------
-// One distribution, one lane
-// ---------------------------------------------------------------------------
-template <typename T, bool kW>
-struct Lane1 {
-    float ref, mx;
-    DF S, W;
-    int moved;
-
-    __device__ __forceinline__ void init(float r) {
-        ref = r; mx = kNegBig; S = {0.f, 0.f}; W = {0.f, 0.f}; moved = 0;
-    }
-
-    // Rare: a value exceeds the centre by more than kSpan.
-    __device__ __noinline__ void move_centre(float c) {
-        const double d = (double)c - (double)ref;
-        const double a = exp(-d);
-        double s = df_value(S), w = df_value(W);
-        if (kW) w = (a == 0.0) ? 0.0 : a * (w - d * s);
-        s *= a;
-        S = df_from(s);
-        W = df_from(w);
-        ref = c;
-        moved = 1;
-    }
-
-    template <int n>
-    __device__ __forceinline__ void push(const float (&v)[n]) {
-        float c = v[0];
-#pragma unroll
-        for (int i = 1; i < n; ++i) c = fmaxf(c, v[i]);
-        mx = fmaxf(mx, c);
-        if (c > ref + kSpan) move_centre(c);
-        if constexpr (Elem<T>::kPrecise) {
-            // fp32 inputs: exact centred value, accurate exponential, double-float sums
-#pragma unroll
-            for (int i = 0; i < n; ++i) {
-                const DF t = df_diff(v[i], ref);
-                const DF e = exp_df(t.hi, t.lo);
-                df_add(S, e);
-                if (kW && e.hi != 0.f) {
-                    const float p = e.hi * t.hi;
-                    const float pe = fmaf(e.hi, t.lo, fmaf(e.lo, t.hi, fmaf(e.hi, t.hi, -p)));
-                    df_add(W, DF{p, pe});
-                }
-            }
-        } else {
-            float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < n; ++i) {
-                const float t = v[i] - ref;   // exact for bf16 values
-                const float e = Elem<T>::exp(t);
-                // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
-                if (i & 1) { s1 += e; if (kW) w1 = fmaf(e, fmaxf(t, -128.f), w1); }
-                else       { s0 += e; if (kW) w0 = fmaf(e, fmaxf(t, -128.f), w0); }
-            }
-            df_add(S, s0 + s1);
-            if (kW) df_add(W, w0 + w1);
-        }
-    }
-};
-
-struct Part1 {  // a merged partial, centre `ref`
-    float ref, mx;
-    double S, W;
-};
-
-template <typename T, bool kW>
-__device__ __forceinline__ Part1 warp_merge(const Lane1<T, kW> &L) {
-    Part1 o;
-    o.mx = warp_max(L.mx);
-    if (__all_sync(0xffffffffu, L.moved == 0)) {
-        DF S = L.S, W = L.W;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) {
-            df_add(S, shfl_xor(S, m));
-            if (kW) df_add(W, shfl_xor(W, m));
-        }
-        o.ref = L.ref;
-        o.S = df_value(S);
-        o.W = kW ? df_value(W) : 0.0;
-    } else {
-        const float M = warp_max(L.ref);
-        const double s = df_value(L.S), w = df_value(L.W);
-        const double a = (L.ref == M) ? 1.0 : exp((double)L.ref - (double)M);
-        double sc = a * s, wc = 0.0;
-        if (sc != 0.0) { if (kW) wc = a * (w - ((double)M - (double)L.ref) * s); }
-        else sc = 0.0;
-        o.ref = M;
-        o.S = warp_sum(sc);
-        o.W = kW ? warp_sum(wc) : 0.0;
-    }
-    return o;
-}
-
-// Merge the warps' partials in fp64; valid in lane 0 of warp 0.
-template <bool kW>
-__device__ __forceinline__ Part1 block_merge(const Part1 &p) {
-    __shared__ Part1 parts[kFwdWarps];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) parts[warp] = p;
-    __syncthreads();
-    Part1 o{kNegBig, kNegBig, 0.0, 0.0};
-    if (warp == 0) {
-        const Part1 q = lane < kFwdWarps ? parts[lane] : Part1{kNegBig, kNegBig, 0.0, 0.0};
-        const float M = warp_max(q.ref);
-        const double a = (q.ref == M) ? 1.0 : exp((double)q.ref - (double)M);
-        double sc = a * q.S, wc = 0.0;
-        if (sc != 0.0) { if (kW) wc = a * (q.W - ((double)M - (double)q.ref) * q.S); }
-        else sc = 0.0;
-        o.ref = M;
-        o.mx = warp_max(q.mx);
-        o.S = warp_sum(sc);
-        o.W = kW ? warp_sum(wc) : 0.0;
-    }
-    return o;
-}
-
-// The warp's shared centre: the max over its first round of values.
-__device__ __forceinline__ float warp_centre(float c) { return fmaxf(warp_max(c), kNegBig); }
-
-// kOp: 0 = logprobs (S only), 1 = entropy (S and W).
-template <int kOp, typename T>
-__global__ void __launch_bounds__(kFwdThreads)
-stats_fwd_kernel(const T *__restrict__ x, int V, Rows rows, const int64_t *__restrict__ targets,
-                 int64_t vocab_start, float *__restrict__ out, RowStat *__restrict__ stats,
-                 int32_t *__restrict__ err) {
-    constexpr bool kW = kOp == 1;
-    constexpr int kVec = Elem<T>::kVec;
-    constexpr int kRound = 4;
-    const int64_t r = blockIdx.x;
-    const int tid = threadIdx.x;
-    const T *row = x + rows.off(r);
-
-    // logprobs: fetch the target logit early
-    int64_t t = 0, loc = -1;
-    float zt = 0.f;
-    if (kOp == 0 && tid == 0) {
-        t = targets[r];
-        loc = t - vocab_start;
-        if (t >= 0 && loc >= 0 && loc < V) zt = Elem<T>::load1(row + loc);
-    }
-
-    const int head = head_count(row, V);
-    const int nv = (V - head) / kVec;
-    const int tail0 = head + nv * kVec;
-    const uint4 *vrow = reinterpret_cast<const uint4 *>(row + head);
-
-    // first round: sets the warp's centre
-    Lane1<T, kW> acc;
-    {
-        uint4 u[kRound];
-#pragma unroll
-        for (int k = 0; k < kRound; ++k) {
-            const int i = tid + k * kFwdThreads;
-            if (i < nv) u[k] = ldg_stream(vrow + i);
-        }
-        float v[kRound * kVec];
-#pragma unroll
-        for (int k = 0; k < kRound; ++k) {
-            if (tid + k * kFwdThreads < nv) Elem<T>::unpack(u[k], v + k * kVec);
-            else {
-#pragma unroll
-                for (int e = 0; e < kVec; ++e) v[k * kVec + e] = -INFINITY;
-            }
-        }
-        float c = v[0];
-#pragma unroll
-        for (int i = 1; i < kRound * kVec; ++i) c = fmaxf(c, v[i]);
-        acc.init(warp_centre(c));
-        acc.push(v);
-    }
-    int i = tid + kRound * kFwdThreads;
-    for (; i + (kRound - 1) * kFwdThreads < nv; i += kRound * kFwdThreads) {
-        uint4 u[kRound];
-#pragma unroll
-        for (int k = 0; k < kRound; ++k) u[k] = ldg_stream(vrow + i + k * kFwdThreads);
-        float v[kRound * kVec];
-#pragma unroll
-        for (int k = 0; k < kRound; ++k) Elem<T>::unpack(u[k], v + k * kVec);
-        acc.push(v);
-    }
-    for (; i < nv; i += kFwdThreads) {
-        float v[kVec];
-        Elem<T>::unpack(ldg_stream(vrow + i), v);
-        acc.push(v);
-    }
-    if (tid < head) { float v[1] = {Elem<T>::load1(row + tid)}; acc.push(v); }
-    if (tid < V - tail0) { float v[1] = {Elem<T>::load1(row + tail0 + tid)}; acc.push(v); }
-
-    const Part1 p = block_merge<kW>(warp_merge(acc));
-    if (tid != 0) return;
-
-    // finish in fp64, against the exact row max
-    uint32_t flags = 0;
-    if (p.S != p.S) flags |= kRowNanInf;
-    else if (p.S == 0.0) flags |= kRowEmpty;
-    const double sh = (double)p.mx - (double)p.ref;
-    const double logS = log(p.S) - sh;
-    const double c = kW ? p.W / p.S - sh : 0.0;
-    store_rowstat(stats + r, p.mx, logS, c, flags);
-    const bool bad = flags != 0;
-    if (kOp == 1) {
-        out[r] = bad ? qnan() : (float)(logS - c);
-    } else {
-        if (t < 0) { out[r] = 0.f; return; }    // ignored target
-        if (loc < 0 || loc >= V) {
-            out[r] = qnan();
-            if (err) atomicOr(err, VP_ERRBIT_TARGET_);
-            return;
-        }
-        out[r] = bad ? qnan() : (float)(((double)zt - (double)p.mx) - logS);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // KL(P||Q): paired statistics from one read of P and Q
 // ---------------------------------------------------------------------------
-template <typename T>
-struct LaneKL {
-    float rp, rq, mxp, mxq;
-    DF Sp, Sq, W;
-    int flag, moved;
-
-    __device__ __forceinline__ void init(float p, float q) {
-        rp = p; rq = q; mxp = mxq = kNegBig;
-        Sp = Sq = W = DF{0.f, 0.f};
-        flag = 0; moved = 0;
-    }
-
-    __device__ __noinline__ void move_centres(float np, float nq) {
-        const double dp = (double)np - (double)rp, dq = (double)nq - (double)rq;
-        const double ap = exp(-dp), aq = exp(-dq);
-        const double sp = df_value(Sp), sq = df_value(Sq), w = df_value(W);
-        W = df_from(ap == 0.0 ? 0.0 : ap * (w - (dp - dq) * sp));
-        Sp = df_from(sp * ap);
-        Sq = df_from(sq * aq);
-        rp = np;
-        rq = nq;
-        moved = 1;
-    }
-
-    template <int n>
-    __device__ __forceinline__ void push(const float (&p)[n], const float (&q)[n]) {
-        float cp = p[0], cq = q[0];
-#pragma unroll
-        for (int i = 1; i < n; ++i) { cp = fmaxf(cp, p[i]); cq = fmaxf(cq, q[i]); }
-        mxp = fmaxf(mxp, cp);
-        mxq = fmaxf(mxq, cq);
-        const bool up = cp > rp + kSpan, uq = cq > rq + kSpan;
-        if (up || uq) move_centres(up ? cp : rp, uq ? cq : rq);
-        int fl = 0;
-        if constexpr (Elem<T>::kPrecise) {
-#pragma unroll
-            for (int i = 0; i < n; ++i) {
-                const DF tp = df_diff(p[i], rp), tq = df_diff(q[i], rq);
-                const DF ep = exp_df(tp.hi, tp.lo), eq = exp_df(tq.hi, tq.lo);
-                df_add(Sp, ep);
-                df_add(Sq, eq);
-                if (ep.hi != 0.f) {              // zero-weight terms add nothing
-                    const DF d = df_sub(tp, tq.hi, tq.lo);
-                    const float pr = ep.hi * d.hi;
-                    const float pe = fmaf(ep.hi, d.lo, fmaf(ep.lo, d.hi, fmaf(ep.hi, d.hi, -pr)));
-                    df_add(W, DF{pr, pe});
-                }
-                fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
-            }
-        } else {
-            float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
-#pragma unroll
-            for (int i = 0; i < n; ++i) {
-                const float tp = p[i] - rp, tq = q[i] - rq;
-                const float ep = Elem<T>::exp(tp), eq = Elem<T>::exp(tq);
-                const float dl = (ep > 0.f) ? (tp - tq) : 0.f;  // zero-weight terms add nothing
-                if (i & 1) { sp1 += ep; sq1 += eq; w1 = fmaf(ep, dl, w1); }
-                else       { sp0 += ep; sq0 += eq; w0 = fmaf(ep, dl, w0); }
-                fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
-            }
-            df_add(Sp, sp0 + sp1);
-            df_add(Sq, sq0 + sq1);
-            df_add(W, w0 + w1);
-        }
-        flag |= fl;
-    }
-};
-
-struct PartKL {
-    float rp, rq, mxp, mxq;
-    double Sp, Sq, W;
-    int flag;
-};
-
-// Re-centre one partial on (Mp, Mq) in fp64 and return its contributions.
-__device__ __forceinline__ void kl_recentred(float rp, float rq, double sp, double sq, double w, float Mp,
-                                             float Mq, double &osp, double &osq, double &ow) {
-    const double ap = (rp == Mp) ? 1.0 : exp((double)rp - (double)Mp);
-    const double aq = (rq == Mq) ? 1.0 : exp((double)rq - (double)Mq);
-    osq = aq * sq;
-    if (osq == 0.0) osq = 0.0;
-    osp = ap * sp;
-    ow = 0.0;
-    if (osp != 0.0) ow = ap * (w - (((double)Mp - (double)rp) - ((double)Mq - (double)rq)) * sp);
-    else osp = 0.0;
-}
-
-template <typename T>
-__device__ __forceinline__ PartKL kl_warp_merge(const LaneKL<T> &L) {
-    PartKL o;
-    o.mxp = warp_max(L.mxp);
-    o.mxq = warp_max(L.mxq);
-    o.flag = __any_sync(0xffffffffu, L.flag);
-    if (__all_sync(0xffffffffu, L.moved == 0)) {
-        DF Sp = L.Sp, Sq = L.Sq, W = L.W;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) {
-            df_add(Sp, shfl_xor(Sp, m));
-            df_add(Sq, shfl_xor(Sq, m));
-            df_add(W, shfl_xor(W, m));
-        }
-        o.rp = L.rp; o.rq = L.rq;
-        o.Sp = df_value(Sp); o.Sq = df_value(Sq); o.W = df_value(W);
-    } else {
-        const float Mp = warp_max(L.rp), Mq = warp_max(L.rq);
-        double sp, sq, w;
-        kl_recentred(L.rp, L.rq, df_value(L.Sp), df_value(L.Sq), df_value(L.W), Mp, Mq, sp, sq, w);
-        o.rp = Mp; o.rq = Mq;
-        o.Sp = warp_sum(sp); o.Sq = warp_sum(sq); o.W = warp_sum(w);
-    }
-    return o;
-}
-
-__device__ __forceinline__ PartKL kl_block_merge(const PartKL &p) {
-    __shared__ PartKL parts[kFwdWarps];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) parts[warp] = p;
-    __syncthreads();
-    PartKL o{kNegBig, kNegBig, kNegBig, kNegBig, 0.0, 0.0, 0.0, 0};
-    if (warp == 0) {
-        const PartKL e{kNegBig, kNegBig, kNegBig, kNegBig, 0.0, 0.0, 0.0, 0};
-        const PartKL q = lane < kFwdWarps ? parts[lane] : e;
-        const float Mp = warp_max(q.rp), Mq = warp_max(q.rq);
-        double sp, sq, w;
-        kl_recentred(q.rp, q.rq, q.Sp, q.Sq, q.W, Mp, Mq, sp, sq, w);
-        o.rp = Mp; o.rq = Mq;
-        o.mxp = warp_max(q.mxp);
-        o.mxq = warp_max(q.mxq);
-        o.Sp = warp_sum(sp); o.Sq = warp_sum(sq); o.W = warp_sum(w);
-        o.flag = __any_sync(0xffffffffu, q.flag);
-    }
-    return o;
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kFwdThreads)
 kl_fwd_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows, float *__restrict__ kl,
@@ -452,45 +103,18 @@ kl_fwd_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows
         acc.push(p, q);
     }
 
-    const PartKL s = kl_block_merge(kl_warp_merge(acc));
-    if (tid != 0) return;
-    uint32_t fp = 0, fq = 0;
-    if (s.Sp != s.Sp) fp |= kRowNanInf;
-    else if (s.Sp == 0.0) fp |= kRowEmpty;
-    if (s.Sq != s.Sq) fq |= kRowNanInf;
-    else if (s.Sq == 0.0) fq |= kRowEmpty;
-    if (s.flag) fp |= kRowMismatch;
-    const double shp = (double)s.mxp - (double)s.rp, shq = (double)s.mxq - (double)s.rq;
-    const double logSp = log(s.Sp) - shp, logSq = log(s.Sq) - shq;
-    const double c = s.W / s.Sp - shp + shq;   // E_p[(P - m_P) - (Q - m_Q)]
-    store_rowstat(stats_p + r, s.mxp, logSp, c, fp);
-    store_rowstat(stats_q + r, s.mxq, logSq, 0.0, fq);
-    float res;
-    if ((fp & (kRowNanInf | kRowEmpty)) || (fq & kRowNanInf)) res = qnan();
-    else if (fp & kRowMismatch) res = pinf();
-    else res = (float)(c - logSp + logSq);
-    kl[r] = res;
+    __shared__ PartKL parts[kFwdWarps];
+    const PartKL w = kl_warp_merge(acc);
+    if ((tid & 31) == 0) parts[tid >> 5] = w;
+    __syncthreads();
+    if (tid >= 32) return;
+    const PartKL s = kl_merge_parts(parts, kFwdWarps);
+    if (tid == 0) finish_kl(s, r, kl, stats_p, stats_q);
 }
 
 // ---------------------------------------------------------------------------
 // Launchers (called by the C ABI after argument checks).
 // ---------------------------------------------------------------------------
-template <int kOp, typename T>
-static cudaError_t launch_stats(const StatsArgs &a) {
-    stats_fwd_kernel<kOp, T><<<(unsigned)a.N, kFwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.targets, a.vocab_start, a.out,
-        static_cast<RowStat *>(a.stats), a.err);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_logprobs_fwd(const StatsArgs &a) {
-    return a.bf16 ? launch_stats<0, __nv_bfloat16>(a) : launch_stats<0, float>(a);
-}
-
-cudaError_t launch_entropy_fwd(const StatsArgs &a) {
-    return a.bf16 ? launch_stats<1, __nv_bfloat16>(a) : launch_stats<1, float>(a);
-}
-
 template <typename T>
 static cudaError_t launch_kl_t(const KLFwdArgs &a) {
     kl_fwd_kernel<T><<<(unsigned)a.N, kFwdThreads, 0, a.stream>>>(
@@ -499,7 +123,7 @@ static cudaError_t launch_kl_t(const KLFwdArgs &a) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_kl_fwd(const KLFwdArgs &a) {
+cudaError_t launch_kl_fwd_rowwise(const KLFwdArgs &a) {
     return a.bf16 ? launch_kl_t<__nv_bfloat16>(a) : launch_kl_t<float>(a);
 }
 

@@ -1,0 +1,353 @@
+// vp_fwd_tma.cu -- persistent forward kernels fed by a TMA (bulk-copy) ring.
+//
+// Sources:
+//   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL"
+//        (DeepSpeed pull request 8838): second commit message and the
+//        reviewer's "Suggested change" (one read of each logit, online (m, S,
+//        W), re-centring on the max, the support-mismatch flag); the Codex
+//        thread on zero-weight terms.
+//   [P2] page "[Feat][Kernel] Add TP Fused linear logp Triton", "Implementation".
+//
+// Shape: a persistent grid of up to two CTAs per SM; CTA b owns rows b, b + G,
+// b + 2G, ... Each CTA has one producer warp and eight consumer warps. One
+// producer thread walks the CTA's rows and streams each row's 16-byte-aligned
+// body through a ring of kStages shared-memory stages (16 KB each) with 1-D
+// bulk copies (cp.async.bulk, non-multicast, L2 evict-first), each completing
+// on a "full" mbarrier; consumers read the stage with 16-byte shared loads,
+// fold it into their per-lane statistics (vp_stats.cuh) and arrive on the
+// stage's "empty" mbarrier. The producer runs ahead across row boundaries, so
+// HBM keeps streaming while the consumers merge a finished row (warp
+// double-float sums, then one warp's fp64 merge of the 8 warp partials). The
+// unaligned head and tail of a row (< 16 bytes each) are read directly.
+// A row's arithmetic depends only on V, the dtype and its address modulo 16,
+// never on N or on which CTA handles it.
+#include "vp_stats.cuh"
+#include "vp_tma.cuh"
+
+#include <atomic>
+
+namespace vp {
+
+constexpr int kTmaConsumerWarps = 8;
+constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
+constexpr int kTmaThreads = kTmaConsumers + 32;
+constexpr int kStageBytes = 16384;
+constexpr int kStages = 6;
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr uint32_t kRowBarrier = 1;  // named barrier of the consumer warps
+
+// Set (OR) when a bounded wait gave up: 1 = producer, 2 = consumer.
+__device__ uint32_t g_tma_fault;
+
+struct Ring {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+};
+
+__device__ __forceinline__ void ring_init(Ring &ring) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], kTmaConsumers);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+}
+
+// Producer side: stage `it`'s slot, waiting for the consumers to free it.
+__device__ __forceinline__ bool acquire_stage(Ring &ring, uint32_t it, uint32_t &st) {
+    st = it % kStages;
+    const uint32_t use = it / kStages;
+    return use == 0 || mbar_wait(&ring.empty[st], (use - 1) & 1);
+}
+
+// After a failed wait the producer waits (bounded) for its copies in flight
+// before the CTA may exit.
+__device__ __forceinline__ void drain(Ring &ring, uint32_t issued) {
+    atomicOr(&g_tma_fault, 1u);
+    for (uint32_t k = issued > (uint32_t)kStages ? issued - kStages : 0; k < issued; ++k)
+        mbar_wait(&ring.full[k % kStages], (k / kStages) & 1);
+}
+
+// ---------------------------------------------------------------------------
+// logprobs (kOp = 0) and entropy (kOp = 1)
+// ---------------------------------------------------------------------------
+template <int kOp, typename T>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const int64_t *__restrict__ targets,
+                     int64_t vocab_start, float *__restrict__ out, RowStat *__restrict__ stats,
+                     int32_t *__restrict__ err) {
+    constexpr bool kW = kOp == 1;
+    constexpr int kVec = Elem<T>::kVec;
+    constexpr int kChunkVec = kStageBytes / 16;                 // 16-byte vectors per stage
+    constexpr int kPerThread = kChunkVec / kTmaConsumers;       // 4
+    extern __shared__ __align__(128) uint8_t ring_mem[];
+    __shared__ Ring ring;
+    __shared__ Part1 parts[2][kTmaConsumerWarps];
+    ring_init(ring);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == kTmaConsumerWarps) {                            // producer
+        if (lane != 0) return;
+        const uint64_t pol = policy_evict_first();
+        uint32_t it = 0;
+        for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+            const T *row = x + rows.off(r);
+            const int head = head_count(row, V);
+            const int nv = (V - head) / kVec;
+            const uint8_t *body = reinterpret_cast<const uint8_t *>(row + head);
+            for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
+                uint32_t st;
+                if (!acquire_stage(ring, it, st)) { drain(ring, it); return; }
+                const uint32_t bytes = (uint32_t)min(kChunkVec, nv - c0) * 16u;
+                mbar_arrive_expect_tx(&ring.full[st], bytes);
+                bulk_g2s(ring_mem + st * kStageBytes, body + (int64_t)c0 * 16, bytes, &ring.full[st], pol);
+            }
+        }
+        return;
+    }
+
+    // consumers
+    const int ct = threadIdx.x;
+    uint32_t it = 0;
+    bool ok = true;
+    int parity = 0;
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, parity ^= 1) {
+        const T *row = x + rows.off(r);
+        const int head = head_count(row, V);
+        const int nv = (V - head) / kVec;
+        const int tail0 = head + nv * kVec;
+        int64_t t = 0;
+        float zt = 0.f;
+        if (kOp == 0 && ct == 0) {
+            t = targets[r];
+            const int64_t loc = t - vocab_start;
+            if (t >= 0 && loc >= 0 && loc < V) zt = Elem<T>::load1(row + loc);
+        }
+        Lane1<T, kW> acc;
+        acc.init(kNegBig);
+        for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
+            const uint32_t st = it % kStages;
+            if (ok && !mbar_wait(&ring.full[st], (it / kStages) & 1)) {
+                ok = false;
+                atomicOr(&g_tma_fault, 2u);
+            }
+            const int cnt = min(kChunkVec, nv - c0);
+            const uint4 *sv = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes);
+            float v[kPerThread * kVec];
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const int i = ct + k * kTmaConsumers;
+                if (i < cnt) Elem<T>::unpack(sv[i], v + k * kVec);
+                else {
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) v[k * kVec + e] = -INFINITY;
+                }
+            }
+            mbar_arrive(&ring.empty[st]);                       // values are in registers
+            if (c0 == 0) {                                      // the warp's centre for this row
+                float c = v[0];
+#pragma unroll
+                for (int i = 1; i < kPerThread * kVec; ++i) c = fmaxf(c, v[i]);
+                acc.init(warp_centre(c));
+            }
+            acc.push(v);
+        }
+        if (ct < head) { float v[1] = {Elem<T>::load1(row + ct)}; acc.push(v); }
+        if (ct < V - tail0) { float v[1] = {Elem<T>::load1(row + tail0 + ct)}; acc.push(v); }
+
+        const Part1 w = warp_merge(acc);
+        if (lane == 0) parts[parity][warp] = w;
+        named_sync(kRowBarrier, kTmaConsumers);
+        if (warp == 0) {
+            const Part1 p = merge_parts<kW>(parts[parity], kTmaConsumerWarps);
+            if (lane == 0 && ok) finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// KL(P||Q); P and Q share their address modulo 16 (checked by the launcher)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, int V, Rows rows,
+                  float *__restrict__ kl, RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q) {
+    constexpr int kVec = Elem<T>::kVec;
+    constexpr int kHalf = kStageBytes / 2;                      // P and Q halves of a stage
+    constexpr int kChunkVec = kHalf / 16;                       // 512 vectors of each
+    constexpr int kPerThread = kChunkVec / kTmaConsumers;       // 2
+    extern __shared__ __align__(128) uint8_t ring_mem[];
+    __shared__ Ring ring;
+    __shared__ PartKL parts[2][kTmaConsumerWarps];
+    ring_init(ring);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == kTmaConsumerWarps) {
+        if (lane != 0) return;
+        const uint64_t pol = policy_evict_first();
+        uint32_t it = 0;
+        for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+            const int64_t off = rows.off(r);
+            const T *prow = P + off, *qrow = Q + off;
+            const int head = head_count(prow, V);
+            const int nv = (V - head) / kVec;
+            const uint8_t *pb = reinterpret_cast<const uint8_t *>(prow + head);
+            const uint8_t *qb = reinterpret_cast<const uint8_t *>(qrow + head);
+            for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
+                uint32_t st;
+                if (!acquire_stage(ring, it, st)) { drain(ring, it); return; }
+                const uint32_t bytes = (uint32_t)min(kChunkVec, nv - c0) * 16u;
+                mbar_arrive_expect_tx(&ring.full[st], 2u * bytes);
+                uint8_t *dst = ring_mem + st * kStageBytes;
+                bulk_g2s(dst, pb + (int64_t)c0 * 16, bytes, &ring.full[st], pol);
+                bulk_g2s(dst + kHalf, qb + (int64_t)c0 * 16, bytes, &ring.full[st], pol);
+            }
+        }
+        return;
+    }
+
+    const int ct = threadIdx.x;
+    uint32_t it = 0;
+    bool ok = true;
+    int parity = 0;
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, parity ^= 1) {
+        const int64_t off = rows.off(r);
+        const T *prow = P + off, *qrow = Q + off;
+        const int head = head_count(prow, V);
+        const int nv = (V - head) / kVec;
+        const int tail0 = head + nv * kVec;
+        LaneKL<T> acc;
+        acc.init(kNegBig, kNegBig);
+        for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
+            const uint32_t st = it % kStages;
+            if (ok && !mbar_wait(&ring.full[st], (it / kStages) & 1)) {
+                ok = false;
+                atomicOr(&g_tma_fault, 2u);
+            }
+            const int cnt = min(kChunkVec, nv - c0);
+            const uint4 *sp = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes);
+            const uint4 *sq = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes + kHalf);
+            float p[kPerThread * kVec], q[kPerThread * kVec];
+#pragma unroll
+            for (int k = 0; k < kPerThread; ++k) {
+                const int i = ct + k * kTmaConsumers;
+                if (i < cnt) {
+                    Elem<T>::unpack(sp[i], p + k * kVec);
+                    Elem<T>::unpack(sq[i], q + k * kVec);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) p[k * kVec + e] = q[k * kVec + e] = -INFINITY;
+                }
+            }
+            mbar_arrive(&ring.empty[st]);
+            if (c0 == 0) {
+                float cp = p[0], cq = q[0];
+#pragma unroll
+                for (int i = 1; i < kPerThread * kVec; ++i) { cp = fmaxf(cp, p[i]); cq = fmaxf(cq, q[i]); }
+                acc.init(warp_centre(cp), warp_centre(cq));
+            }
+            acc.push(p, q);
+        }
+        if (ct < head) {
+            float p[1] = {Elem<T>::load1(prow + ct)}, q[1] = {Elem<T>::load1(qrow + ct)};
+            acc.push(p, q);
+        }
+        if (ct < V - tail0) {
+            float p[1] = {Elem<T>::load1(prow + tail0 + ct)}, q[1] = {Elem<T>::load1(qrow + tail0 + ct)};
+            acc.push(p, q);
+        }
+
+        const PartKL w = kl_warp_merge(acc);
+        if (lane == 0) parts[parity][warp] = w;
+        named_sync(kRowBarrier, kTmaConsumers);
+        if (warp == 0) {
+            const PartKL s = kl_merge_parts(parts[parity], kTmaConsumerWarps);
+            if (lane == 0 && ok) finish_kl(s, r, kl, stats_p, stats_q);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+static int sm_count() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int n = (dev >= 0 && dev < 64) ? cached[dev].load() : 0;
+    if (n == 0) {
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (dev >= 0 && dev < 64) cached[dev].store(n);
+    }
+    return n > 0 ? n : 1;
+}
+
+// The ring is dynamic shared memory above the 48 KB default: raise the limit
+// once per kernel and device.
+template <typename K>
+static cudaError_t allow_ring(K kernel, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load() & bit) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    if (e == cudaSuccess) done.fetch_or(bit);
+    return e;
+}
+
+static unsigned persistent_grid(int64_t N) {
+    const int64_t g = 2 * (int64_t)sm_count();
+    return (unsigned)(N < g ? N : g);
+}
+
+template <int kOp, typename T>
+static cudaError_t launch_stats_tma(const StatsArgs &a) {
+    static std::atomic<uint64_t> done{0};
+    auto k = stats_fwd_tma_kernel<kOp, T>;
+    cudaError_t e = allow_ring(k, done);
+    if (e != cudaSuccess) return e;
+    k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
+        static_cast<const T *>(a.x), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.targets, a.vocab_start, a.out,
+        static_cast<RowStat *>(a.stats), a.err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_logprobs_fwd(const StatsArgs &a) {
+    return a.bf16 ? launch_stats_tma<0, __nv_bfloat16>(a) : launch_stats_tma<0, float>(a);
+}
+
+cudaError_t launch_entropy_fwd(const StatsArgs &a) {
+    return a.bf16 ? launch_stats_tma<1, __nv_bfloat16>(a) : launch_stats_tma<1, float>(a);
+}
+
+template <typename T>
+static cudaError_t launch_kl_tma(const KLFwdArgs &a) {
+    static std::atomic<uint64_t> done{0};
+    auto k = kl_fwd_tma_kernel<T>;
+    cudaError_t e = allow_ring(k, done);
+    if (e != cudaSuccess) return e;
+    k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
+        static_cast<const T *>(a.p), static_cast<const T *>(a.q), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.kl,
+        static_cast<RowStat *>(a.stats_p), static_cast<RowStat *>(a.stats_q));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kl_fwd(const KLFwdArgs &a) {
+    // the ring copies P and Q rows with one shared 16-byte phase; otherwise the
+    // element-wise CTA-per-row kernel reads them
+    if ((((uintptr_t)a.p ^ (uintptr_t)a.q) & 15u) != 0) return launch_kl_fwd_rowwise(a);
+    return a.bf16 ? launch_kl_tma<__nv_bfloat16>(a) : launch_kl_tma<float>(a);
+}
+
+cudaError_t read_fault(uint32_t *value, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_tma_fault, sizeof(uint32_t));
+    if (e == cudaSuccess && clear && *value) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_tma_fault, &zero, sizeof(uint32_t));
+    }
+    return e;
+}
+
+}  // namespace vp

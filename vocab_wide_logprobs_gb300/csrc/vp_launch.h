@@ -54,6 +54,8 @@ struct KLBwdArgs {
 cudaError_t launch_logprobs_fwd(const StatsArgs &a);
 cudaError_t launch_entropy_fwd(const StatsArgs &a);
 cudaError_t launch_kl_fwd(const KLFwdArgs &a);
+cudaError_t launch_kl_fwd_rowwise(const KLFwdArgs &a);
+cudaError_t read_fault(uint32_t *value, bool clear);
 cudaError_t launch_logprobs_bwd(const GradArgs &a);
 cudaError_t launch_entropy_bwd(const GradArgs &a);
 cudaError_t launch_kl_bwd(const KLBwdArgs &a);
