@@ -157,7 +157,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = workloads.pages_shape(seed=1 + rank)
+    w = workloads.pages_shape(seed=1 + rank, N=args.rows)
     a, b = w["a"].to(dev), w["b"].to(dev)
     t, g = w["targets"].to(dev), w["grad"].to(dev)
     N, V = a.shape
@@ -236,6 +236,35 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for(dom),
                 "algorithmic_bytes": nbytes[dom]}
 
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, seconds=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "N": N, "V": V, "rows_per_gpu": N, "parallelism": f"dp{world}",
+                       "l2": "inputs larger than L2 (1.245 GB per logits tensor)",
+                       "algorithmic_bytes_per_step": step_bytes},
+            "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
+            "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(), "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream, dev):
+    import torch
+    N = a.shape[0]
     # end to end through the public API with host buffers: H2D of the step's inputs,
     # the step, D2H of its per-row results, every step
     h_a, h_b = w["a"].pin_memory(), w["b"].pin_memory()
@@ -273,29 +302,8 @@ def run_ours(args, rank, world, local_rank):
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
-    e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
-           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, seconds=args.cpu_seconds)
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "N": N, "V": V, "rows_per_gpu": N, "parallelism": f"dp{world}",
-                       "l2": "inputs larger than L2 (1.245 GB per logits tensor)",
-                       "algorithmic_bytes_per_step": step_bytes},
-            "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
-            "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
-            "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu,
-        }
-        print(json.dumps(line))
-    if dist:
-        dist.destroy_process_group()
+    return {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 # ---------------------------------------------------------------------------
@@ -379,6 +387,8 @@ def main():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--reference-rows", type=int, default=64)
+    p.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (8192 is the benchmarked workload)")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     args = p.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

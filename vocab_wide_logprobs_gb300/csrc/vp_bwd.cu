@@ -62,14 +62,6 @@ __device__ __forceinline__ float expm1_small(float x) {
     return fmaf(t * x, x, x);                 // x + x^2 (1/2 + x/6 + ...)
 }
 
-// q - p from p = e^{lp}, q = e^{lq} and delta = lq - lp: where |delta| < 1/2 the
-// difference is formed as p (e^delta - 1) (or -q (e^-delta - 1)) so it keeps its
-// relative accuracy as q -> p.
-__device__ __forceinline__ float diff_of_probs(float q, float p, float delta) {
-    if (fabsf(delta) < 0.5f) return delta < 0.f ? p * expm1_small(delta) : -q * expm1_small(-delta);
-    return q - p;
-}
-
 template <int kOp, typename T>
 __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s, float g, int64_t loc) {
     if constexpr (Elem<T>::kPrecise) {
@@ -97,10 +89,9 @@ __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s,
     }
 }
 
-// dlq: log S_Q - log S_P as a double-float (a per-row constant of the bf16 path)
 template <typename T, bool kDP, bool kDQ>
 __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, float g,
-                                             bool p_nan, const DF &dls, float &dp, float &dq) {
+                                             bool p_nan, float &dp, float &dq) {
     if constexpr (Elem<T>::kPrecise) {
         const DF tp = df_diff(zp, sp.m), tq = df_diff(zq, sq.m);
         const DF lp = df_sub(tp, sp.logS_hi, sp.logS_lo), lq = df_sub(tq, sq.logS_hi, sq.logS_lo);
@@ -118,7 +109,7 @@ __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &
     } else {
         const float tp = zp - sp.m, tq = zq - sq.m;          // exact for bf16 values
         const float p = Elem<T>::exp(tp - sp.logS_hi), q = Elem<T>::exp(tq - sq.logS_hi);
-        if (kDQ) dq = g * diff_of_probs(q, p, ((tq - tp) - dls.hi) - dls.lo);
+        if (kDQ) dq = g * (q - p);
         if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * (((tp - tq) - sp.c_hi) - sp.c_lo);
     }
 }
@@ -235,8 +226,6 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
         // support mismatch (KL = +inf): dP is NaN, dQ = g (q - p) stays finite
         const bool all_nan = (sp.flags & (kRowNanInf | kRowEmpty)) || (sq.flags & kRowNanInf);
         const bool p_nan = all_nan || (sp.flags & kRowMismatch);
-        DF dls = two_sum(sq.logS_hi, -sp.logS_hi);
-        dls.lo = __fadd_rn(dls.lo, __fsub_rn(sq.logS_lo, sp.logS_lo));
 
         uintptr_t ph = (uintptr_t)prow & 15u;
         bool vec = (((uintptr_t)qrow & 15u) == ph);
@@ -248,7 +237,7 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
                 float dp = qnan(), dq = qnan();
                 if (!all_nan)
                     kl_grad_elem<T, kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), sp, sq, g, p_nan,
-                                              dls, dp, dq);
+                                              dp, dq);
                 if (kDP) Elem<T>::store1(dprow + j, dp);
                 if (kDQ) Elem<T>::store1(dqrow + j, dq);
             }
@@ -291,7 +280,7 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
                     Elem<T>::unpack(uq[k], zq);
 #pragma unroll
                     for (int e = 0; e < kVec; ++e)
-                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], sp, sq, g, p_nan, dls, dp[e], dq[e]);
+                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], sp, sq, g, p_nan, dp[e], dq[e]);
                     if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
                     if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
                 }

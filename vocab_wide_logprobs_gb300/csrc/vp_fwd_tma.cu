@@ -39,6 +39,27 @@ constexpr uint32_t kRowBarrier = 1;  // named barrier of the consumer warps
 // Set (OR) when a bounded wait gave up: 1 = producer, 2 = consumer.
 __device__ uint32_t g_tma_fault;
 
+// 16-byte word of -inf values (padding of a partial last stage)
+template <typename T>
+__device__ __forceinline__ uint4 splat_neg_inf() {
+    const uint32_t w = sizeof(T) == 2 ? kBf16NegInf2 : 0xff800000u;
+    return make_uint4(w, w, w, w);
+}
+
+template <typename T, int K>
+__device__ __forceinline__ float chunk_max(const uint4 (&u)[K]) {
+    if constexpr (sizeof(T) == 2) {
+        return max_bf16(u);
+    } else {
+        float c = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+            c = fmaxf(fmaxf(c, fmaxf(__uint_as_float(u[k].x), __uint_as_float(u[k].y))),
+                      fmaxf(__uint_as_float(u[k].z), __uint_as_float(u[k].w)));
+        return c;
+    }
+}
+
 struct Ring {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -135,24 +156,23 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
             }
             const int cnt = min(kChunkVec, nv - c0);
             const uint4 *sv = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes);
-            float v[kPerThread * kVec];
+            const uint4 pad = splat_neg_inf<T>();
+            uint4 u[kPerThread];
 #pragma unroll
             for (int k = 0; k < kPerThread; ++k) {
                 const int i = ct + k * kTmaConsumers;
-                if (i < cnt) Elem<T>::unpack(sv[i], v + k * kVec);
-                else {
-#pragma unroll
-                    for (int e = 0; e < kVec; ++e) v[k * kVec + e] = -INFINITY;
-                }
+                u[k] = i < cnt ? sv[i] : pad;
             }
-            mbar_arrive(&ring.empty[st]);                       // values are in registers
-            if (c0 == 0) {                                      // the warp's centre for this row
-                float c = v[0];
+            mbar_arrive(&ring.empty[st]);                       // the words are in registers
+            if (c0 == 0) acc.init(warp_centre(chunk_max<T>(u)));   // the warp's centre for this row
+            if constexpr (Elem<T>::kPrecise) {
+                float v[kPerThread * kVec];
 #pragma unroll
-                for (int i = 1; i < kPerThread * kVec; ++i) c = fmaxf(c, v[i]);
-                acc.init(warp_centre(c));
+                for (int k = 0; k < kPerThread; ++k) Elem<T>::unpack(u[k], v + k * kVec);
+                acc.push(v);
+            } else {
+                acc.push_bf16(u);
             }
-            acc.push(v);
         }
         if (ct < head) { float v[1] = {Elem<T>::load1(row + ct)}; acc.push(v); }
         if (ct < V - tail0) { float v[1] = {Elem<T>::load1(row + tail0 + ct)}; acc.push(v); }
@@ -229,26 +249,27 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
             const int cnt = min(kChunkVec, nv - c0);
             const uint4 *sp = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes);
             const uint4 *sq = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes + kHalf);
-            float p[kPerThread * kVec], q[kPerThread * kVec];
+            const uint4 pad = splat_neg_inf<T>();
+            uint4 up[kPerThread], uq[kPerThread];
 #pragma unroll
             for (int k = 0; k < kPerThread; ++k) {
                 const int i = ct + k * kTmaConsumers;
-                if (i < cnt) {
-                    Elem<T>::unpack(sp[i], p + k * kVec);
-                    Elem<T>::unpack(sq[i], q + k * kVec);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < kVec; ++e) p[k * kVec + e] = q[k * kVec + e] = -INFINITY;
-                }
+                up[k] = i < cnt ? sp[i] : pad;
+                uq[k] = i < cnt ? sq[i] : pad;
             }
             mbar_arrive(&ring.empty[st]);
-            if (c0 == 0) {
-                float cp = p[0], cq = q[0];
+            if (c0 == 0) acc.init(warp_centre(chunk_max<T>(up)), warp_centre(chunk_max<T>(uq)));
+            if constexpr (Elem<T>::kPrecise) {
+                float p[kPerThread * kVec], q[kPerThread * kVec];
 #pragma unroll
-                for (int i = 1; i < kPerThread * kVec; ++i) { cp = fmaxf(cp, p[i]); cq = fmaxf(cq, q[i]); }
-                acc.init(warp_centre(cp), warp_centre(cq));
+                for (int k = 0; k < kPerThread; ++k) {
+                    Elem<T>::unpack(up[k], p + k * kVec);
+                    Elem<T>::unpack(uq[k], q + k * kVec);
+                }
+                acc.push(p, q);
+            } else {
+                acc.push_bf16(up, uq);
             }
-            acc.push(p, q);
         }
         if (ct < head) {
             float p[1] = {Elem<T>::load1(prow + ct)}, q[1] = {Elem<T>::load1(qrow + ct)};

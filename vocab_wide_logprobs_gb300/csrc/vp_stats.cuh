@@ -13,10 +13,53 @@
 //        (logp = target logit - LSE).
 #pragma once
 
+#include <string.h>
+
 #include "vp_device.cuh"
 #include "vp_launch.h"
 
 namespace vp {
+
+// ---------------------------------------------------------------------------
+// Packed bf16 helpers (the fast path of the bf16 inputs)
+// ---------------------------------------------------------------------------
+constexpr uint32_t kBf16NegInf2 = 0xff80ff80u;   // two bf16 -inf
+
+__device__ __forceinline__ __nv_bfloat162 bf162_bits(uint32_t w) {
+    __nv_bfloat162 b;
+    memcpy(&b, &w, 4);
+    return b;
+}
+
+// max over the bf16 values held in K 16-byte words (NaN ignored, like fmaxf)
+template <int K>
+__device__ __forceinline__ float max_bf16(const uint4 (&u)[K]) {
+    __nv_bfloat162 m0 = bf162_bits(u[0].x), m1 = bf162_bits(u[0].y), m2 = bf162_bits(u[0].z),
+                   m3 = bf162_bits(u[0].w);
+#pragma unroll
+    for (int k = 1; k < K; ++k) {
+        m0 = __hmax2(m0, bf162_bits(u[k].x));
+        m1 = __hmax2(m1, bf162_bits(u[k].y));
+        m2 = __hmax2(m2, bf162_bits(u[k].z));
+        m3 = __hmax2(m3, bf162_bits(u[k].w));
+    }
+    const __nv_bfloat162 m = __hmax2(__hmax2(m0, m1), __hmax2(m2, m3));
+    return fmaxf(__low2float(m), __high2float(m));
+}
+
+__device__ __forceinline__ float2 bf16_pair(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ float ex2_fast(float a) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4 &u, int q) {
+    return q == 0 ? u.x : q == 1 ? u.y : q == 2 ? u.z : u.w;
+}
 
 // ---------------------------------------------------------------------------
 // One distribution, one lane
@@ -76,6 +119,36 @@ struct Lane1 {
             }
             df_add(S, s0 + s1);
             if (kW) df_add(W, w0 + w1);
+        }
+    }
+
+    // bf16 fast path on raw 16-byte words (8 values each): packed max, packed
+    // f32x2 arithmetic and four independent accumulator pairs.
+    template <int K>
+    __device__ __forceinline__ void push_bf16(const uint4 (&u)[K]) {
+        const float c = max_bf16(u);
+        mx = fmaxf(mx, c);
+        if (c > ref + kSpan) move_centre(c);
+        const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
+        float2 s[4], w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s[q] = w[q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
+                const float2 a = __fmul2_rn(t, l2e);
+                const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                s[q] = __fadd2_rn(s[q], e);
+                if (kW) w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
+            }
+        }
+        const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
+        df_add(S, ss.x + ss.y);
+        if (kW) {
+            const float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+            df_add(W, ww.x + ww.y);
         }
     }
 };
@@ -201,6 +274,48 @@ struct LaneKL {
             df_add(W, w0 + w1);
         }
         flag |= fl;
+    }
+
+    // bf16 fast path on raw 16-byte words of P and Q (see Lane1::push_bf16); the
+    // mismatch flag is taken on the raw halves: Q = -inf where P is not -inf.
+    template <int K>
+    __device__ __forceinline__ void push_bf16(const uint4 (&up)[K], const uint4 (&uq)[K]) {
+        const float cp = max_bf16(up), cq = max_bf16(uq);
+        mxp = fmaxf(mxp, cp);
+        mxq = fmaxf(mxq, cq);
+        const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
+        if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
+        const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
+        const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
+        float2 sp[4], sq[4], w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sp[q] = sq[q] = w[q] = make_float2(0.f, 0.f);
+        uint32_t fl = 0;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t pw = word(up[k], q), qw = word(uq[k], q);
+                fl |= __vcmpeq2(qw, kBf16NegInf2) & ~__vcmpeq2(pw, kBf16NegInf2);
+                const float2 tp = __fadd2_rn(bf16_pair(pw), nrp), tq = __fadd2_rn(bf16_pair(qw), nrq);
+                const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
+                const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
+                const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
+                sp[q] = __fadd2_rn(sp[q], ep);
+                sq[q] = __fadd2_rn(sq[q], eq);
+                float2 d = __ffma2_rn(tq, m1, tp);                            // tp - tq
+                d.x = ep.x > 0.f ? d.x : 0.f;                                 // zero-weight terms add nothing
+                d.y = ep.y > 0.f ? d.y : 0.f;
+                w[q] = __ffma2_rn(ep, d, w[q]);
+            }
+        }
+        const float2 a = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
+        const float2 b = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
+        const float2 c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+        df_add(Sp, a.x + a.y);
+        df_add(Sq, b.x + b.y);
+        df_add(W, c.x + c.y);
+        flag |= (fl != 0);
     }
 };
 
