@@ -75,6 +75,7 @@
 #ifndef VP_H
 #define VP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -199,13 +200,39 @@ VP_API vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, i
                            vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused linear logp [P2, "Implementation"]                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace vp_linear_logp_fwd needs for N rows and V
+ * vocabulary rows (per-row, per-256-column (max, sum-exp) pairs and the target
+ * logits). 0 for invalid sizes. */
+VP_API size_t vp_linear_logp_workspace_size(int64_t N, int64_t V, int64_t D);
+
+/* logp[r] = h_r . w_t - log sum_j exp(h_r . w_j), t = targets[r] - vocab_start,
+ * over the V rows of W (a vocabulary shard starting at global id vocab_start),
+ * without materialising the logits: tcgen05 tensor-core tiles (bf16 inputs,
+ * fp32 accumulation in TMEM) with an online log-sum-exp epilogue, then an fp64
+ * merge per row [P2, "Implementation": the forward returns (logp, lse)].
+ * hidden: bf16 [N, D] row-major; weight: bf16 [V, D] row-major; both 16-byte
+ * aligned; D a multiple of 64. targets: int64 [N] (negative = ignored, out of
+ * the shard = data error, as for vp_logprobs_fwd). Outputs: logp fp32 [N] and
+ * stats (vp_rowstat [N]: m = max logit, logS, c = 0) for the backward.
+ * workspace: device memory of at least vp_linear_logp_workspace_size(N, V, D)
+ * bytes, 256-byte aligned, owned by the caller; its contents are scratch.
+ * Logits are rounded nowhere: each is an fp32 accumulation of bf16 products. */
+VP_API vp_status vp_linear_logp_fwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                    int64_t vocab_start, const int64_t *targets, float *logp, vp_rowstat *stats,
+                                    void *workspace, size_t workspace_bytes, int32_t *err_word, vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Misc                                                                      */
 /* ------------------------------------------------------------------------ */
 
 /* Reads the library's device fault word of the current device into *value
  * and, when `clear` is non-zero, resets it. The word is non-zero only if a
- * kernel's bounded wait on its copy pipeline gave up (bit 0: producer, bit 1:
- * consumer); that kernel then skipped its outputs and returned instead of
+ * kernel's bounded wait on its copy pipeline gave up (bits 0-1: the forward
+ * scans' producer / consumers; bits 2-4: the linear-logp producer / MMA /
+ * epilogue); that kernel then skipped its outputs and returned instead of
  * spinning. Unlike every other call, this one synchronises with the device.
  * (No counterpart on the pages: a safety net of this implementation.) */
 VP_API vp_status vp_fault_status(uint32_t *value, int clear);

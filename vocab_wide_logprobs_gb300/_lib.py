@@ -24,6 +24,7 @@ SIGNATURES = {
     "vp_entropy_bwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P],
     "vp_kl_fwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P],
     "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
+    "vp_linear_logp_fwd": [P, P, I64, I64, I64, I64, P, P, P, P, ctypes.c_size_t, P, P],
 }
 
 
@@ -44,6 +45,8 @@ def lib():
                 fn.restype = ctypes.c_int
             h.vp_status_string.argtypes = [ctypes.c_int]
             h.vp_status_string.restype = ctypes.c_char_p
+            h.vp_linear_logp_workspace_size.argtypes = [I64, I64, I64]
+            h.vp_linear_logp_workspace_size.restype = ctypes.c_size_t
             h.vp_fault_status.argtypes = [P, I32]
             h.vp_fault_status.restype = ctypes.c_int
             h.vp_version.argtypes = []

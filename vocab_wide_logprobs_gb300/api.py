@@ -157,6 +157,35 @@ def vp_kl_bwd(a, b, direction, stats_a, stats_b, grad, want_da=True, want_db=Tru
     return da, db
 
 
+def vp_linear_logp_workspace_size(N: int, V: int, D: int) -> int:
+    return int(_lib.lib().vp_linear_logp_workspace_size(N, V, D))
+
+
+def vp_linear_logp_fwd(hidden, weight, targets, vocab_start: int = 0, err_word=None, logp=None, stats=None,
+                       workspace=None):
+    """logp of targets under softmax(hidden @ weight^T) without materialising the logits.
+
+    hidden: bf16 [N, D], weight: bf16 [V, D] (contiguous). Returns (logp fp32 [N], stats)."""
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise VPError(3, "vp_linear_logp_fwd takes bf16 hidden and weight")
+    if not (hidden.is_contiguous() and weight.is_contiguous()) or hidden.dim() != 2 or weight.dim() != 2:
+        raise VPError(4, "hidden and weight must be contiguous 2-D tensors")
+    N, D = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != D:
+        raise VPError(2, "hidden and weight disagree on D")
+    logp = _f32(N, hidden) if logp is None else logp
+    stats = rowstats(N, hidden.device) if stats is None else stats
+    need = vp_linear_logp_workspace_size(N, V, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=hidden.device)
+    _check(_lib.lib().vp_linear_logp_fwd(_ptr(hidden), _ptr(weight), N, V, D, vocab_start, _ptr(targets),
+                                         _ptr(logp), _ptr(stats), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _ptr(err_word),
+                                         _stream()), "vp_linear_logp_fwd")
+    return logp, stats
+
+
 def vp_fault_status(clear: bool = False) -> int:
     """The device fault word (non-zero if a kernel's bounded wait gave up); synchronises."""
     v = ctypes.c_uint32(0)

@@ -156,11 +156,39 @@ vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t 
     return launched(vp::launch_kl_bwd(k));
 }
 
+size_t vp_linear_logp_workspace_size(int64_t N, int64_t V, int64_t D) {
+    (void)D;
+    if (N < 0 || V < 1) return 0;
+    return vp::linear_workspace_bytes(N, V);
+}
+
+vp_status vp_linear_logp_fwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                             int64_t vocab_start, const int64_t *targets, float *logp, vp_rowstat *stats,
+                             void *workspace, size_t workspace_bytes, int32_t *err_word, vp_stream stream) {
+    if (N < 0 || N > kMaxRowsPerLaunch || V < 1 || V > kMaxV || D < 64 || D % 64 != 0 || D > (1 << 20))
+        return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !targets || !logp || !stats || !workspace) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8) || !aligned(logp, 4) ||
+        !aligned(stats, 16) || !aligned(workspace, 256) || !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearFwdArgs a{hidden, weight, N, V, D, vocab_start, targets, logp, stats, workspace, err_word,
+                        (cudaStream_t)stream};
+    return launched(vp::launch_linear_logp_fwd(a));
+}
+
 vp_status vp_fault_status(uint32_t *value, int clear) {
     if (!value) return VP_ERR_NULL;
     vp_status st = check_device();
     if (st != VP_OK) return st;
-    return vp::read_fault(value, clear != 0) == cudaSuccess ? VP_OK : VP_ERR_LAUNCH;
+    uint32_t a = 0, b = 0;
+    if (vp::read_fault(&a, clear != 0) != cudaSuccess || vp::read_linear_fault(&b, clear != 0) != cudaSuccess)
+        return VP_ERR_LAUNCH;
+    *value = a | (b << 2);
+    return VP_OK;
 }
 
 const char *vp_status_string(int status) {

@@ -103,12 +103,12 @@ kl_fwd_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows
         acc.push(p, q);
     }
 
-    __shared__ PartKL parts[kFwdWarps];
-    const PartKL w = kl_warp_merge(acc);
+    __shared__ PartKL<AccT<T>> parts[kFwdWarps];
+    const PartKL<AccT<T>> w = kl_warp_merge(acc);
     if ((tid & 31) == 0) parts[tid >> 5] = w;
     __syncthreads();
     if (tid >= 32) return;
-    const PartKL s = kl_merge_parts(parts, kFwdWarps);
+    const PartKL<AccT<T>> s = kl_merge_parts(parts, kFwdWarps);
     if (tid == 0) finish_kl(s, r, kl, stats_p, stats_q);
 }
 

@@ -105,7 +105,7 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
     constexpr int kPerThread = kChunkVec / kTmaConsumers;       // 4
     extern __shared__ __align__(128) uint8_t ring_mem[];
     __shared__ Ring ring;
-    __shared__ Part1 parts[2][kTmaConsumerWarps];
+    __shared__ Part1<AccT<T>> parts[2][kTmaConsumerWarps];
     ring_init(ring);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -177,11 +177,11 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
         if (ct < head) { float v[1] = {Elem<T>::load1(row + ct)}; acc.push(v); }
         if (ct < V - tail0) { float v[1] = {Elem<T>::load1(row + tail0 + ct)}; acc.push(v); }
 
-        const Part1 w = warp_merge(acc);
+        const Part1<AccT<T>> w = warp_merge(acc);
         if (lane == 0) parts[parity][warp] = w;
         named_sync(kRowBarrier, kTmaConsumers);
         if (warp == 0) {
-            const Part1 p = merge_parts<kW>(parts[parity], kTmaConsumerWarps);
+            const Part1<AccT<T>> p = merge_parts<kW>(parts[parity], kTmaConsumerWarps);
             if (lane == 0 && ok) finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
         }
     }
@@ -200,7 +200,7 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
     constexpr int kPerThread = kChunkVec / kTmaConsumers;       // 2
     extern __shared__ __align__(128) uint8_t ring_mem[];
     __shared__ Ring ring;
-    __shared__ PartKL parts[2][kTmaConsumerWarps];
+    __shared__ PartKL<AccT<T>> parts[2][kTmaConsumerWarps];
     ring_init(ring);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -280,11 +280,11 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
             acc.push(p, q);
         }
 
-        const PartKL w = kl_warp_merge(acc);
+        const PartKL<AccT<T>> w = kl_warp_merge(acc);
         if (lane == 0) parts[parity][warp] = w;
         named_sync(kRowBarrier, kTmaConsumers);
         if (warp == 0) {
-            const PartKL s = kl_merge_parts(parts[parity], kTmaConsumerWarps);
+            const PartKL<AccT<T>> s = kl_merge_parts(parts[parity], kTmaConsumerWarps);
             if (lane == 0 && ok) finish_kl(s, r, kl, stats_p, stats_q);
         }
     }

@@ -51,6 +51,21 @@ struct KLBwdArgs {
     cudaStream_t stream;
 };
 
+struct LinearFwdArgs {
+    const void *hidden, *weight;  // bf16 [N, D], [V, D], row-major
+    int64_t N, V, D, vocab_start;
+    const int64_t *targets;
+    float *logp;
+    void *stats;      // vp_rowstat [N]
+    void *workspace;  // linear_workspace_bytes(N, V)
+    int32_t *err;
+    cudaStream_t stream;
+};
+
+size_t linear_workspace_bytes(int64_t N, int64_t V);
+cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a);
+cudaError_t read_linear_fault(uint32_t *value, bool clear);
+
 cudaError_t launch_logprobs_fwd(const StatsArgs &a);
 cudaError_t launch_entropy_fwd(const StatsArgs &a);
 cudaError_t launch_kl_fwd(const KLFwdArgs &a);

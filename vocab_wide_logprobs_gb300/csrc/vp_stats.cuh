@@ -15,6 +15,8 @@
 
 #include <string.h>
 
+#include <type_traits>
+
 #include "vp_device.cuh"
 #include "vp_launch.h"
 
@@ -45,6 +47,22 @@ __device__ __forceinline__ float max_bf16(const uint4 (&u)[K]) {
     }
     const __nv_bfloat162 m = __hmax2(__hmax2(m0, m1), __hmax2(m2, m3));
     return fmaxf(__low2float(m), __high2float(m));
+}
+
+// min over the bf16 values held in K 16-byte words (NaN ignored)
+template <int K>
+__device__ __forceinline__ float min_bf16(const uint4 (&u)[K]) {
+    __nv_bfloat162 m0 = bf162_bits(u[0].x), m1 = bf162_bits(u[0].y), m2 = bf162_bits(u[0].z),
+                   m3 = bf162_bits(u[0].w);
+#pragma unroll
+    for (int k = 1; k < K; ++k) {
+        m0 = __hmin2(m0, bf162_bits(u[k].x));
+        m1 = __hmin2(m1, bf162_bits(u[k].y));
+        m2 = __hmin2(m2, bf162_bits(u[k].z));
+        m3 = __hmin2(m3, bf162_bits(u[k].w));
+    }
+    const __nv_bfloat162 m = __hmin2(__hmin2(m0, m1), __hmin2(m2, m3));
+    return fminf(__low2float(m), __high2float(m));
 }
 
 __device__ __forceinline__ float2 bf16_pair(uint32_t w) {
@@ -129,19 +147,36 @@ struct Lane1 {
         const float c = max_bf16(u);
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
+        // W needs 0 * (-inf) kept out only when the chunk holds a -inf logit
+        const bool masked = kW && !(min_bf16(u) > -INFINITY);
         const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
         float2 s[4], w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) s[q] = w[q] = make_float2(0.f, 0.f);
+        if (!masked) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
+            for (int k = 0; k < K; ++k) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
-                const float2 a = __fmul2_rn(t, l2e);
-                const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
-                s[q] = __fadd2_rn(s[q], e);
-                if (kW) w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
+                    const float2 a = __fmul2_rn(t, l2e);
+                    const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                    s[q] = __fadd2_rn(s[q], e);
+                    if (kW) w[q] = __ffma2_rn(e, t, w[q]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);
+                    const float2 a = __fmul2_rn(t, l2e);
+                    const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                    s[q] = __fadd2_rn(s[q], e);
+                    // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
+                    w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
+                }
             }
         }
         const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
@@ -153,14 +188,35 @@ struct Lane1 {
     }
 };
 
+// Merged partials carry their sums in fp64 on the fp32 path and in fp32 on the
+// bf16 path (whose results are held to bf16 and 2e-5 accuracy); GB300's fp64
+// pipe is narrow, so the bf16 path keeps it for the one-thread row finish only.
+template <typename T>
+using AccT = typename std::conditional<Elem<T>::kPrecise, double, float>::type;
+
+__device__ __forceinline__ double exp_acc(double x) { return exp(x); }
+__device__ __forceinline__ float exp_acc(float x) { return expf(x); }
+
+template <typename V>
+__device__ __forceinline__ V df_to(const DF &a) { return (V)a.hi + (V)a.lo; }
+
+template <typename V>
+__device__ __forceinline__ V warp_sum_t(V v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+template <typename V>
 struct Part1 {  // a merged partial, centre `ref`
     float ref, mx;
-    double S, W;
+    V S, W;
 };
 
 template <typename T, bool kW>
-__device__ __forceinline__ Part1 warp_merge(const Lane1<T, kW> &L) {
-    Part1 o;
+__device__ __forceinline__ Part1<AccT<T>> warp_merge(const Lane1<T, kW> &L) {
+    using V = AccT<T>;
+    Part1<V> o;
     o.mx = warp_max(L.mx);
     if (__all_sync(0xffffffffu, L.moved == 0)) {
         DF S = L.S, W = L.W;
@@ -170,41 +226,40 @@ __device__ __forceinline__ Part1 warp_merge(const Lane1<T, kW> &L) {
             if (kW) df_add(W, shfl_xor(W, m));
         }
         o.ref = L.ref;
-        o.S = df_value(S);
-        o.W = kW ? df_value(W) : 0.0;
+        o.S = df_to<V>(S);
+        o.W = kW ? df_to<V>(W) : V(0);
     } else {
         const float M = warp_max(L.ref);
-        const double s = df_value(L.S), w = df_value(L.W);
-        const double a = (L.ref == M) ? 1.0 : exp((double)L.ref - (double)M);
-        double sc = a * s, wc = 0.0;
-        if (sc != 0.0) { if (kW) wc = a * (w - ((double)M - (double)L.ref) * s); }
-        else sc = 0.0;
+        const V s = df_to<V>(L.S), w = df_to<V>(L.W);
+        const V a = (L.ref == M) ? V(1) : exp_acc((V)L.ref - (V)M);
+        V sc = a * s, wc = V(0);
+        if (sc != V(0)) { if (kW) wc = a * (w - ((V)M - (V)L.ref) * s); }
+        else sc = V(0);
         o.ref = M;
-        o.S = warp_sum(sc);
-        o.W = kW ? warp_sum(wc) : 0.0;
+        o.S = warp_sum_t(sc);
+        o.W = kW ? warp_sum_t(wc) : V(0);
     }
     return o;
 }
 
-// Merge `count` (<= 32) warp partials in fp64, re-centred on the largest centre
-// and in a fixed order; called by one whole warp, the result is valid in all lanes.
-template <bool kW>
-__device__ __forceinline__ Part1 merge_parts(const Part1 *parts, int count) {
+// Merge `count` (<= 32) warp partials, re-centred on the largest centre and in
+// a fixed order; called by one whole warp, the result is valid in all lanes.
+template <bool kW, typename V>
+__device__ __forceinline__ Part1<V> merge_parts(const Part1<V> *parts, int count) {
     const int lane = threadIdx.x & 31;
-    const Part1 q = lane < count ? parts[lane] : Part1{kNegBig, kNegBig, 0.0, 0.0};
+    const Part1<V> q = lane < count ? parts[lane] : Part1<V>{kNegBig, kNegBig, V(0), V(0)};
     const float M = warp_max(q.ref);
-    const double a = (q.ref == M) ? 1.0 : exp((double)q.ref - (double)M);
-    double sc = a * q.S, wc = 0.0;
-    if (sc != 0.0) { if (kW) wc = a * (q.W - ((double)M - (double)q.ref) * q.S); }
-    else sc = 0.0;
-    Part1 o;
+    const V a = (q.ref == M) ? V(1) : exp_acc((V)q.ref - (V)M);
+    V sc = a * q.S, wc = V(0);
+    if (sc != V(0)) { if (kW) wc = a * (q.W - ((V)M - (V)q.ref) * q.S); }
+    else sc = V(0);
+    Part1<V> o;
     o.ref = M;
     o.mx = warp_max(q.mx);
-    o.S = warp_sum(sc);
-    o.W = kW ? warp_sum(wc) : 0.0;
+    o.S = warp_sum_t(sc);
+    o.W = kW ? warp_sum_t(wc) : V(0);
     return o;
 }
-
 
 // ---------------------------------------------------------------------------
 // KL(P||Q): paired statistics from one read of P and Q
@@ -285,29 +340,49 @@ struct LaneKL {
         mxq = fmaxf(mxq, cq);
         const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
         if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
+        // zero-weight guards and the mismatch flag matter only where a -inf logit sits
+        const bool masked = !(min_bf16(up) > -INFINITY) || !(min_bf16(uq) > -INFINITY);
         const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
         const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
         float2 sp[4], sq[4], w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) sp[q] = sq[q] = w[q] = make_float2(0.f, 0.f);
-        uint32_t fl = 0;
+        if (!masked) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
+            for (int k = 0; k < K; ++k) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t pw = word(up[k], q), qw = word(uq[k], q);
-                fl |= __vcmpeq2(qw, kBf16NegInf2) & ~__vcmpeq2(pw, kBf16NegInf2);
-                const float2 tp = __fadd2_rn(bf16_pair(pw), nrp), tq = __fadd2_rn(bf16_pair(qw), nrq);
-                const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
-                const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
-                const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
-                sp[q] = __fadd2_rn(sp[q], ep);
-                sq[q] = __fadd2_rn(sq[q], eq);
-                float2 d = __ffma2_rn(tq, m1, tp);                            // tp - tq
-                d.x = ep.x > 0.f ? d.x : 0.f;                                 // zero-weight terms add nothing
-                d.y = ep.y > 0.f ? d.y : 0.f;
-                w[q] = __ffma2_rn(ep, d, w[q]);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 tp = __fadd2_rn(bf16_pair(word(up[k], q)), nrp);
+                    const float2 tq = __fadd2_rn(bf16_pair(word(uq[k], q)), nrq);
+                    const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
+                    const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
+                    const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
+                    sp[q] = __fadd2_rn(sp[q], ep);
+                    sq[q] = __fadd2_rn(sq[q], eq);
+                    w[q] = __ffma2_rn(ep, __ffma2_rn(tq, m1, tp), w[q]);    // ep (tp - tq)
+                }
             }
+        } else {
+            uint32_t fl = 0;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t pw = word(up[k], q), qw = word(uq[k], q);
+                    fl |= __vcmpeq2(qw, kBf16NegInf2) & ~__vcmpeq2(pw, kBf16NegInf2);
+                    const float2 tp = __fadd2_rn(bf16_pair(pw), nrp), tq = __fadd2_rn(bf16_pair(qw), nrq);
+                    const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
+                    const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
+                    const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
+                    sp[q] = __fadd2_rn(sp[q], ep);
+                    sq[q] = __fadd2_rn(sq[q], eq);
+                    float2 d = __ffma2_rn(tq, m1, tp);                            // tp - tq
+                    d.x = ep.x > 0.f ? d.x : 0.f;                                 // zero-weight terms add nothing
+                    d.y = ep.y > 0.f ? d.y : 0.f;
+                    w[q] = __ffma2_rn(ep, d, w[q]);
+                }
+            }
+            flag |= (fl != 0);
         }
         const float2 a = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
         const float2 b = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
@@ -315,32 +390,34 @@ struct LaneKL {
         df_add(Sp, a.x + a.y);
         df_add(Sq, b.x + b.y);
         df_add(W, c.x + c.y);
-        flag |= (fl != 0);
     }
 };
 
+template <typename V>
 struct PartKL {
     float rp, rq, mxp, mxq;
-    double Sp, Sq, W;
+    V Sp, Sq, W;
     int flag;
 };
 
-// Re-centre one partial on (Mp, Mq) in fp64 and return its contributions.
-__device__ __forceinline__ void kl_recentred(float rp, float rq, double sp, double sq, double w, float Mp,
-                                             float Mq, double &osp, double &osq, double &ow) {
-    const double ap = (rp == Mp) ? 1.0 : exp((double)rp - (double)Mp);
-    const double aq = (rq == Mq) ? 1.0 : exp((double)rq - (double)Mq);
+// Re-centre one partial on (Mp, Mq) and return its contributions.
+template <typename V>
+__device__ __forceinline__ void kl_recentred(float rp, float rq, V sp, V sq, V w, float Mp, float Mq, V &osp, V &osq,
+                                             V &ow) {
+    const V ap = (rp == Mp) ? V(1) : exp_acc((V)rp - (V)Mp);
+    const V aq = (rq == Mq) ? V(1) : exp_acc((V)rq - (V)Mq);
     osq = aq * sq;
-    if (osq == 0.0) osq = 0.0;
+    if (osq == V(0)) osq = V(0);
     osp = ap * sp;
-    ow = 0.0;
-    if (osp != 0.0) ow = ap * (w - (((double)Mp - (double)rp) - ((double)Mq - (double)rq)) * sp);
-    else osp = 0.0;
+    ow = V(0);
+    if (osp != V(0)) ow = ap * (w - (((V)Mp - (V)rp) - ((V)Mq - (V)rq)) * sp);
+    else osp = V(0);
 }
 
 template <typename T>
-__device__ __forceinline__ PartKL kl_warp_merge(const LaneKL<T> &L) {
-    PartKL o;
+__device__ __forceinline__ PartKL<AccT<T>> kl_warp_merge(const LaneKL<T> &L) {
+    using V = AccT<T>;
+    PartKL<V> o;
     o.mxp = warp_max(L.mxp);
     o.mxq = warp_max(L.mxq);
     o.flag = __any_sync(0xffffffffu, L.flag);
@@ -353,30 +430,31 @@ __device__ __forceinline__ PartKL kl_warp_merge(const LaneKL<T> &L) {
             df_add(W, shfl_xor(W, m));
         }
         o.rp = L.rp; o.rq = L.rq;
-        o.Sp = df_value(Sp); o.Sq = df_value(Sq); o.W = df_value(W);
+        o.Sp = df_to<V>(Sp); o.Sq = df_to<V>(Sq); o.W = df_to<V>(W);
     } else {
         const float Mp = warp_max(L.rp), Mq = warp_max(L.rq);
-        double sp, sq, w;
-        kl_recentred(L.rp, L.rq, df_value(L.Sp), df_value(L.Sq), df_value(L.W), Mp, Mq, sp, sq, w);
+        V sp, sq, w;
+        kl_recentred<V>(L.rp, L.rq, df_to<V>(L.Sp), df_to<V>(L.Sq), df_to<V>(L.W), Mp, Mq, sp, sq, w);
         o.rp = Mp; o.rq = Mq;
-        o.Sp = warp_sum(sp); o.Sq = warp_sum(sq); o.W = warp_sum(w);
+        o.Sp = warp_sum_t(sp); o.Sq = warp_sum_t(sq); o.W = warp_sum_t(w);
     }
     return o;
 }
 
 // KL counterpart of merge_parts.
-__device__ __forceinline__ PartKL kl_merge_parts(const PartKL *parts, int count) {
+template <typename V>
+__device__ __forceinline__ PartKL<V> kl_merge_parts(const PartKL<V> *parts, int count) {
     const int lane = threadIdx.x & 31;
-    const PartKL e{kNegBig, kNegBig, kNegBig, kNegBig, 0.0, 0.0, 0.0, 0};
-    const PartKL q = lane < count ? parts[lane] : e;
+    const PartKL<V> e{kNegBig, kNegBig, kNegBig, kNegBig, V(0), V(0), V(0), 0};
+    const PartKL<V> q = lane < count ? parts[lane] : e;
     const float Mp = warp_max(q.rp), Mq = warp_max(q.rq);
-    double sp, sq, w;
-    kl_recentred(q.rp, q.rq, q.Sp, q.Sq, q.W, Mp, Mq, sp, sq, w);
-    PartKL o;
+    V sp, sq, w;
+    kl_recentred<V>(q.rp, q.rq, q.Sp, q.Sq, q.W, Mp, Mq, sp, sq, w);
+    PartKL<V> o;
     o.rp = Mp; o.rq = Mq;
     o.mxp = warp_max(q.mxp);
     o.mxq = warp_max(q.mxq);
-    o.Sp = warp_sum(sp); o.Sq = warp_sum(sq); o.W = warp_sum(w);
+    o.Sp = warp_sum_t(sp); o.Sq = warp_sum_t(sq); o.W = warp_sum_t(w);
     o.flag = __any_sync(0xffffffffu, q.flag);
     return o;
 }
@@ -385,15 +463,16 @@ __device__ __forceinline__ PartKL kl_merge_parts(const PartKL *parts, int count)
 // Row finish in fp64 against the exact row max; writes the output and records.
 // ---------------------------------------------------------------------------
 // kOp 0 (logprobs): t is the target id, zt the target logit (read when in range).
-template <int kOp>
-__device__ __forceinline__ void finish_stats(const Part1 &p, int64_t r, int V, int64_t t, int64_t vocab_start,
+template <int kOp, typename Acc>
+__device__ __forceinline__ void finish_stats(const Part1<Acc> &p, int64_t r, int V, int64_t t, int64_t vocab_start,
                                              float zt, float *out, RowStat *stats, int32_t *err) {
     uint32_t flags = 0;
-    if (p.S != p.S) flags |= kRowNanInf;
-    else if (p.S == 0.0) flags |= kRowEmpty;
+    const double S = p.S;
+    if (S != S) flags |= kRowNanInf;
+    else if (S == 0.0) flags |= kRowEmpty;
     const double sh = (double)p.mx - (double)p.ref;
-    const double logS = log(p.S) - sh;
-    const double c = kOp == 1 ? p.W / p.S - sh : 0.0;
+    const double logS = log(S) - sh;
+    const double c = kOp == 1 ? (double)p.W / S - sh : 0.0;
     store_rowstat(stats + r, p.mx, logS, c, flags);
     const bool bad = flags != 0;
     if (kOp == 1) {
@@ -410,17 +489,19 @@ __device__ __forceinline__ void finish_stats(const Part1 &p, int64_t r, int V, i
     out[r] = bad ? qnan() : (float)(((double)zt - (double)p.mx) - logS);
 }
 
-__device__ __forceinline__ void finish_kl(const PartKL &s, int64_t r, float *kl, RowStat *stats_p,
+template <typename Acc>
+__device__ __forceinline__ void finish_kl(const PartKL<Acc> &s, int64_t r, float *kl, RowStat *stats_p,
                                           RowStat *stats_q) {
     uint32_t fp = 0, fq = 0;
-    if (s.Sp != s.Sp) fp |= kRowNanInf;
-    else if (s.Sp == 0.0) fp |= kRowEmpty;
-    if (s.Sq != s.Sq) fq |= kRowNanInf;
-    else if (s.Sq == 0.0) fq |= kRowEmpty;
+    const double Sp = s.Sp, Sq = s.Sq, W = s.W;
+    if (Sp != Sp) fp |= kRowNanInf;
+    else if (Sp == 0.0) fp |= kRowEmpty;
+    if (Sq != Sq) fq |= kRowNanInf;
+    else if (Sq == 0.0) fq |= kRowEmpty;
     if (s.flag) fp |= kRowMismatch;
     const double shp = (double)s.mxp - (double)s.rp, shq = (double)s.mxq - (double)s.rq;
-    const double logSp = log(s.Sp) - shp, logSq = log(s.Sq) - shq;
-    const double c = s.W / s.Sp - shp + shq;   // E_p[(P - m_P) - (Q - m_Q)]
+    const double logSp = log(Sp) - shp, logSq = log(Sq) - shq;
+    const double c = W / Sp - shp + shq;   // E_p[(P - m_P) - (Q - m_Q)]
     store_rowstat(stats_p + r, s.mxp, logSp, c, fp);
     store_rowstat(stats_q + r, s.mxq, logSq, 0.0, fq);
     float res;

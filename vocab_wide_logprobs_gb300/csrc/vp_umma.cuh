@@ -1,0 +1,107 @@
+// vp_umma.cuh -- tcgen05 (5th-generation tensor core) and tensor-TMA primitives
+// for sm_103a, in inline PTX: TMEM allocation, shared-memory matrix and
+// instruction descriptors, MMA issue and commit, TMEM loads, 2-D tiled TMA.
+//
+// Operand layout used throughout: K-major bf16 tiles of 64 elements (128 bytes)
+// per row, written by TMA with the 128-byte swizzle, 8-row atoms of 1024 bytes.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "vp_tma.cuh"
+
+namespace vp {
+
+// --- TMEM -----------------------------------------------------------------
+// Executed by one whole warp; the column base is written to *dst_smem.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// --- descriptors ----------------------------------------------------------
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 1024-byte
+// stride between 8-row groups (SBO), descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc_sw128(const void *smem) {
+    const uint64_t addr = smem_u32(smem);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3FFFull;            // start address       [0, 14)
+    d |= (uint64_t)1 << 16;                  // leading byte offset [16, 30) (unused when swizzled)
+    d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset  [32, 46)
+    d |= (uint64_t)1 << 46;                  // version             [46, 48)
+    d |= (uint64_t)2 << 61;                  // layout: 128-byte swizzle [61, 64)
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
+// both operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+    return (1u << 4)                        // accumulator format: f32   [4, 6)
+           | (1u << 7)                      // A format: bf16            [7, 10)
+           | (1u << 10)                     // B format: bf16            [10, 13)
+           | ((uint32_t)(N >> 3) << 17)     // N / 8                     [17, 23)
+           | ((uint32_t)(M >> 4) << 24);    // M / 16                    [24, 29)
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one M x N x 16 step, issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
+// 32 (w % 4) .. 32 (w % 4) + 31).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// --- 2-D tiled TMA --------------------------------------------------------
+// Box at element coordinates (x = inner, y = row) into shared memory; the inner
+// coordinate times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+}  // namespace vp
