@@ -147,8 +147,9 @@ struct Lane1 {
         const float c = max_bf16(u);
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
-        // W needs 0 * (-inf) kept out only when the chunk holds a -inf logit
-        const bool masked = kW && !(min_bf16(u) > -INFINITY);
+        // W needs 0 * (-inf) kept out only where some t = v - ref is -inf: a -inf
+        // logit, or a spread beyond FLT_MAX (e.g. a row holding -3e38 and 3e38)
+        const bool masked = kW && !((ref - min_bf16(u)) < INFINITY);
         const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
         float2 s[4], w[4];
 #pragma unroll
@@ -340,8 +341,9 @@ struct LaneKL {
         mxq = fmaxf(mxq, cq);
         const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
         if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
-        // zero-weight guards and the mismatch flag matter only where a -inf logit sits
-        const bool masked = !(min_bf16(up) > -INFINITY) || !(min_bf16(uq) > -INFINITY);
+        // zero-weight guards and the mismatch flag matter only where some centred
+        // value is -inf: a -inf logit, or a spread beyond FLT_MAX
+        const bool masked = !((rp - min_bf16(up)) < INFINITY) || !((rq - min_bf16(uq)) < INFINITY);
         const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
         const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
         float2 sp[4], sq[4], w[4];
