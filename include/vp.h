@@ -102,7 +102,9 @@ typedef enum vp_status {
     VP_ERR_LAUNCH = 6,    /* the CUDA launch failed                                  */
     VP_ERR_ARG = 7,       /* another invalid argument (direction, both gradients
                              requested as NULL where one is required, ...)          */
-    VP_ERR_DEVICE = 8     /* no usable device, or not an sm_103 device               */
+    VP_ERR_DEVICE = 8,    /* no usable device, or not an sm_103 device               */
+    VP_ERR_SCRATCH = 9    /* too large for the fixed scratch of
+                             vp_linear_logp_fwd_noalloc                             */
 } vp_status;
 
 typedef enum vp_dtype { VP_F32 = 0, VP_BF16 = 1 } vp_dtype;
@@ -223,6 +225,37 @@ VP_API size_t vp_linear_logp_workspace_size(int64_t N, int64_t V, int64_t D);
 VP_API vp_status vp_linear_logp_fwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
                                     int64_t vocab_start, const int64_t *targets, float *logp, vp_rowstat *stats,
                                     void *workspace, size_t workspace_bytes, int32_t *err_word, vp_stream stream);
+
+/* The paper has no counterpart of this entry point; it exists for callers that
+ * cannot allocate device memory themselves.
+ *
+ * Same result as vp_linear_logp_fwd (the same kernels, bitwise), but the
+ * scratch lives in one fixed 24 MiB array inside the library instead of a
+ * workspace passed by the caller, so the call allocates nothing. It serves
+ * callers that must not call cudaMalloc or any allocating routine of their own:
+ * for instance a plugin running inside a host framework that owns all device
+ * memory through its own allocator, or a service that fixes its memory
+ * footprint at start-up and forbids later allocations (which could fail or
+ * fragment memory in the middle of a run). The caller still passes every input
+ * and output.
+ *
+ * Limits and behaviour:
+ *  - the array is 24 MiB; every GPU that loads the library holds it until the
+ *    process exits;
+ *  - the scratch needed is about 8 bytes per row and 256-column vocabulary
+ *    tile plus 4 bytes per row (vp_linear_logp_workspace_size(N, V, D));
+ *    problems needing more than 24 MiB return VP_ERR_SCRATCH before any work
+ *    is queued (e.g. V = 75968 allows up to about 10,500 rows);
+ *  - the first call on each device looks up the array's device address once
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture;
+ *  - all calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs clearing (every entry is written before it is read
+ *    within a call), but calls that overlap on the GPU (concurrent streams)
+ *    race on it and must be serialised by the caller. */
+VP_API vp_status vp_linear_logp_fwd_noalloc(const void *hidden, const void *weight, int64_t N, int64_t V,
+                                            int64_t D, int64_t vocab_start, const int64_t *targets, float *logp,
+                                            vp_rowstat *stats, int32_t *err_word, vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                      */

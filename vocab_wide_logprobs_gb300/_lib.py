@@ -25,6 +25,7 @@ SIGNATURES = {
     "vp_kl_fwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P],
     "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
     "vp_linear_logp_fwd": [P, P, I64, I64, I64, I64, P, P, P, P, ctypes.c_size_t, P, P],
+    "vp_linear_logp_fwd_noalloc": [P, P, I64, I64, I64, I64, P, P, P, P, P],
 }
 
 

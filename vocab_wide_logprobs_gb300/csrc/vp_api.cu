@@ -180,6 +180,24 @@ vp_status vp_linear_logp_fwd(const void *hidden, const void *weight, int64_t N, 
     return launched(vp::launch_linear_logp_fwd(a));
 }
 
+vp_status vp_linear_logp_fwd_noalloc(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                     int64_t vocab_start, const int64_t *targets, float *logp, vp_rowstat *stats,
+                                     int32_t *err_word, vp_stream stream) {
+    if (N < 0 || N > kMaxRowsPerLaunch || V < 1 || V > kMaxV || D < 64 || D % 64 != 0 || D > (1 << 20))
+        return VP_ERR_SHAPE;
+    if (vp::linear_workspace_bytes(N, V) > vp::kNoAllocScratchBytes) return VP_ERR_SCRATCH;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !targets || !logp || !stats) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8) || !aligned(logp, 4) ||
+        !aligned(stats, 16) || !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearFwdArgs a{hidden, weight, N, V, D, vocab_start, targets, logp, stats, nullptr, err_word,
+                        (cudaStream_t)stream};
+    return launched(vp::launch_linear_logp_fwd_noalloc(a));
+}
+
 vp_status vp_fault_status(uint32_t *value, int clear) {
     if (!value) return VP_ERR_NULL;
     vp_status st = check_device();
@@ -202,6 +220,7 @@ const char *vp_status_string(int status) {
         case VP_ERR_LAUNCH: return "CUDA launch failed";
         case VP_ERR_ARG: return "invalid argument";
         case VP_ERR_DEVICE: return "no usable sm_103 device";
+        case VP_ERR_SCRATCH: return "problem too large for the fixed 24 MiB scratch of the no-allocation entry point";
         default: return "unknown status";
     }
 }

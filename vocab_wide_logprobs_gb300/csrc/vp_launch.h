@@ -63,6 +63,11 @@ struct LinearFwdArgs {
 };
 
 size_t linear_workspace_bytes(int64_t N, int64_t V);
+
+// Fixed scratch of vp_linear_logp_fwd_noalloc (24 MiB, held by every device
+// that loads the library, for the life of the process).
+constexpr size_t kNoAllocScratchBytes = (size_t)24 << 20;
+cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a);
 cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a);
 cudaError_t read_linear_fault(uint32_t *value, bool clear);
 

@@ -295,6 +295,65 @@ cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// No-allocation variant: the same two kernels with their scratch in a fixed
+// array inside the library instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// symbol's name is only a host-side stand-in, so the address is looked up once
+// per device with that device current, and cached.
+static cudaError_t noalloc_scratch_address(void **out) {
+    static std::atomic<void *> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    void *p = cached[dev].load();
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        cached[dev].store(p);
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
+cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
+    void *scratch = nullptr;
+    cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done.load() & (1ull << (dev & 63)))) {
+        e = cudaFuncSetAttribute(linear_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(1ull << (dev & 63));
+    }
+    CUtensorMap tm_h, tm_w;
+    if (!make_map(&tm_h, a.hidden, a.N, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, kLBN))
+        return cudaErrorInvalidValue;
+    const int64_t n_vt = (a.V + kLBN - 1) / kLBN;
+    // Every partial and every in-shard target logit is written by the first
+    // kernel before the merge reads it, so nothing in the array needs clearing.
+    float2 *partials = static_cast<float2 *>(scratch);
+    float *tgt = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
+                                           (((size_t)a.N * n_vt * sizeof(float2) + 255) & ~(size_t)255));
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t n_tiles = ((a.N + kLBM - 1) / kLBM) * n_vt;
+    const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
+    linear_lse_kernel<<<grid, kLThreads, kLSmemBytes, a.stream>>>(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D,
+                                                                   a.vocab_start, a.targets, partials, tgt);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+        (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
+    return cudaGetLastError();
+}
+
 cudaError_t read_linear_fault(uint32_t *value, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(value, g_linear_fault, sizeof(uint32_t));
     if (e == cudaSuccess && clear && *value) {
