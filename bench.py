@@ -236,6 +236,10 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for(dom),
                 "algorithmic_bytes": nbytes[dom]}
 
+    linear = None
+    if not args.no_linear and rank == 0:
+        linear = linear_bench(args, dev)
+
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream, dev)
@@ -255,11 +259,65 @@ def run_ours(args, rank, world, local_rank):
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu,
+            "clocks": clocks.summary(), "cpu_baseline": cpu, "linear_logp": linear,
         }
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
+
+
+def linear_bench(args, dev, N=8192, V=75968, D=4096):
+    """Fused linear logp forward on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16)."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    from vocab_wide_logprobs_gb300 import workloads
+    w = workloads.linear(N=N, V=V, D=D)
+    h, W, t = w["hidden"].to(dev), w["weight"].to(dev), w["targets"].to(dev)
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    st = vp.rowstats(N, dev)
+    ws = torch.empty(vp.vp_linear_logp_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
+    run = lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    g = w["grad"].to(dev)
+    dh = torch.empty_like(h)
+    dW = torch.empty_like(W)
+    wsb = torch.empty(vp.vp_linear_logp_bwd_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
+    runb = lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb)
+    runb()
+    torch.cuda.synchronize()
+    breps = 3
+    e0.record()
+    for _ in range(breps):
+        runb()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_b = e0.elapsed_time(e1) / breps
+    flops = 2.0 * N * V * D
+    peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            peak = json.load(f).get("bf16_tflops")
+    tf = flops / (ms * 1e-3) / 1e12
+    tfb = 3 * flops / (ms_b * 1e-3) / 1e12
+    return {"workload": f"hidden [{N},{D}] x W [{V},{D}] bf16, logp of uniform targets", "fwd_ms": round(ms, 4),
+            "bwd_ms": round(ms_b, 4),
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
+                         "peak_src": "measured bf16 burst" if peak else None,
+                         "frac": round(tf / peak, 4) if peak else None, "flops": flops},
+            "bwd_roofline": {"bound": "tensor", "achieved": round(tfb, 1), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(tfb / peak, 4) if peak else None, "flops": 3 * flops,
+                             "note": "three GEMMs of 2NVD each (logits recomputed, dhidden, dW)"}}
 
 
 def end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream, dev):
@@ -389,6 +447,7 @@ def main():
     p.add_argument("--reference-rows", type=int, default=64)
     p.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (8192 is the benchmarked workload)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    p.add_argument("--no-linear", action="store_true", help="skip the fused linear-logp measurement")
     args = p.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

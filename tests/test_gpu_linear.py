@@ -58,3 +58,83 @@ def test_linear_logp_full_size_sampled():
     rows = [0, 1, 127, 128, 4095, 8191]
     lp = _check_fwd(w, rows=rows, tag="config 5 ")
     assert torch.isfinite(lp).all() and (lp <= 0).all()
+
+
+# ---------------------------------------------------------------------------
+# Backward: dhidden and dW. dz is rounded to bf16 for the two gradient GEMMs,
+# so each output is held to one bf16 ulp plus the forward error bound of a dot
+# product with bf16-rounded dz and fp32 accumulation: 2^-8 * sum |dz| |operand|.
+# ---------------------------------------------------------------------------
+GEMM_KAPPA = 2.0 ** -8
+
+
+def _check_gemm_grad(got, ref, mag, what):
+    g = parity.to64(got)
+    r = parity.rne_bf16(ref)
+    parity._placement(g, r, what)
+    fin = np.isfinite(r)
+    err = np.abs(g[fin] - r[fin])
+    tol = parity.ulp_bf16(r[fin]) + GEMM_KAPPA * mag[fin]
+    assert (err <= tol).all(), f"{what}: worst err/tol {(err / tol).max():.3f}, {(err > tol).sum()} bad of {err.size}"
+    return float((err / tol).max())
+
+
+def _bwd_case(N, V, D, seed, vocab_start=0, scale=25.0):
+    w = workloads.linear(seed=seed, N=N, V=V, D=D)
+    w["weight"] = (w["weight"].float() * scale).to(torch.bfloat16)
+    w["targets"] = w["targets"] + vocab_start
+    return w
+
+
+def _run_bwd(w, vocab_start=0, **kw):
+    h, W, t, g = (w[k].to(DEV) for k in ("hidden", "weight", "targets", "grad"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lp, st = vp.vp_linear_logp_fwd(h, W, t, vocab_start, err_word=err)
+    dh, dW = vp.vp_linear_logp_bwd(h, W, t, st, g, vocab_start, err_word=err, **kw)
+    torch.cuda.synchronize()
+    return dh, dW, int(err.item())
+
+
+@pytest.mark.parametrize("N,V,D", [(256, 1024, 256), (200, 777, 128), (130, 300, 64), (64, 9000, 128)])
+def test_linear_logp_bwd_small(N, V, D):
+    w = _bwd_case(N, V, D, seed=N + 7 * V + D)
+    dh, dW, _ = _run_bwd(w)
+    h64, W64 = parity.to64(w["hidden"]), parity.to64(w["weight"])
+    t, g = w["targets"].numpy(), w["grad"].double().numpy()
+    ref_dh, ref_dW = oracle.linear_logp_bwd(h64, W64, t, g)
+    dz = np.abs(oracle.logprobs_bwd(oracle.linear_logits(h64, W64), t, g))
+    _check_gemm_grad(dh, ref_dh, dz @ np.abs(W64), f"{N}x{V}x{D} dhidden")
+    _check_gemm_grad(dW, ref_dW, dz.T @ np.abs(h64), f"{N}x{V}x{D} dW")
+
+
+def test_linear_logp_bwd_single_outputs_and_special_targets():
+    w = _bwd_case(136, 1500, 128, seed=3, vocab_start=500)
+    w["targets"][5] = -1            # ignored: contributes nothing
+    full_dh, full_dW, _ = _run_bwd(w, vocab_start=500)
+    dh_only, none_w, _ = _run_bwd(w, vocab_start=500, want_dW=False)
+    none_h, dW_only, _ = _run_bwd(w, vocab_start=500, want_dhidden=False)
+    assert none_w is None and none_h is None
+    assert torch.equal(dh_only, full_dh) and torch.equal(dW_only, full_dW)
+    assert (full_dh[5] == 0).all()
+    w["targets"][7] = 500 + 1500    # past the shard: NaN row of dhidden, NaN dW, error bit
+    dh, dW, err = _run_bwd(w, vocab_start=500)
+    assert err == 1 and torch.isnan(dh[7]).all() and torch.isfinite(dh[8]).all() and torch.isnan(dW).all()
+
+
+@pytest.mark.slow
+def test_linear_logp_bwd_full_size_sampled():
+    w = workloads.linear()
+    h, W, t, g = (w[k].to(DEV) for k in ("hidden", "weight", "targets", "grad"))
+    lp, st = vp.vp_linear_logp_fwd(h, W, t)
+    dh, dW = vp.vp_linear_logp_bwd(h, W, t, st, g)
+    torch.cuda.synchronize()
+    rows = [0, 777, 8191]
+    h64, W64 = parity.to64(w["hidden"][rows]), parity.to64(w["weight"])
+    tt, gg = w["targets"][rows].numpy(), w["grad"][rows].double().numpy()
+    ref_dh, _ = oracle.linear_logp_bwd(h64, W64, tt, gg, want_dW=False)
+    dz = np.abs(oracle.logprobs_bwd(oracle.linear_logits(h64, W64), tt, gg))
+    _check_gemm_grad(dh[rows], ref_dh, dz @ np.abs(W64), "config 5 dhidden")
+    # dW on every row: each column of dW sums to 0 over the vocabulary (every dz row sums to 0)
+    col = dW.double().sum(0).abs()
+    scale = dW.double().abs().sum(0)
+    assert torch.isfinite(dW).all() and (col <= 2.0 ** -7 * scale + 1e-6).all()

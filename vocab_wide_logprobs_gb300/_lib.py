@@ -26,6 +26,7 @@ SIGNATURES = {
     "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
     "vp_linear_logp_fwd": [P, P, I64, I64, I64, I64, P, P, P, P, ctypes.c_size_t, P, P],
     "vp_linear_logp_fwd_noalloc": [P, P, I64, I64, I64, I64, P, P, P, P, P],
+    "vp_linear_logp_bwd": [P, P, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_size_t, P, P],
 }
 
 
@@ -48,6 +49,8 @@ def lib():
             h.vp_status_string.restype = ctypes.c_char_p
             h.vp_linear_logp_workspace_size.argtypes = [I64, I64, I64]
             h.vp_linear_logp_workspace_size.restype = ctypes.c_size_t
+            h.vp_linear_logp_bwd_workspace_size.argtypes = [I64, I64, I64]
+            h.vp_linear_logp_bwd_workspace_size.restype = ctypes.c_size_t
             h.vp_fault_status.argtypes = [P, I32]
             h.vp_fault_status.restype = ctypes.c_int
             h.vp_version.argtypes = []

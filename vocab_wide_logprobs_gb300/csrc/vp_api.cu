@@ -198,6 +198,32 @@ vp_status vp_linear_logp_fwd_noalloc(const void *hidden, const void *weight, int
     return launched(vp::launch_linear_logp_fwd_noalloc(a));
 }
 
+size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D) {
+    if (N < 0 || V < 1 || D < 64) return 0;
+    return vp::linear_bwd_workspace_bytes(N, V, D);
+}
+
+vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                             int64_t vocab_start, const int64_t *targets, const vp_rowstat *stats,
+                             const float *grad_out, void *dhidden, void *dW, void *workspace, size_t workspace_bytes,
+                             int32_t *err_word, vp_stream stream) {
+    if (N < 0 || N > kMaxRowsPerLaunch || V < 1 || V > kMaxV || D < 64 || D % 64 != 0 || D > (1 << 20))
+        return VP_ERR_SHAPE;
+    if (!dhidden && !dW) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !targets || !stats || !grad_out || !workspace) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8) || !aligned(stats, 16) ||
+        !aligned(grad_out, 4) || !aligned(dhidden, 16) || !aligned(dW, 16) || !aligned(workspace, 256) ||
+        !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_bwd_workspace_bytes(N, V, D)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearBwdArgs a{hidden, weight, N, V, D, vocab_start, targets, stats, grad_out, dhidden, dW, workspace,
+                        err_word, (cudaStream_t)stream};
+    return launched(vp::launch_linear_logp_bwd(a));
+}
+
 vp_status vp_fault_status(uint32_t *value, int clear) {
     if (!value) return VP_ERR_NULL;
     vp_status st = check_device();

@@ -9,16 +9,20 @@
 //   [P2] page "[Feat][Kernel] Add TP Fused linear logp Triton", "Implementation".
 //
 // Shape: a persistent grid of up to two CTAs per SM; CTA b owns rows b, b + G,
-// b + 2G, ... Each CTA has one producer warp and eight consumer warps. One
+// b + 2G, ... Each CTA has eight consumer warps, one producer warp and one
+// finisher warp. One
 // producer thread walks the CTA's rows and streams each row's 16-byte-aligned
 // body through a ring of kStages shared-memory stages (16 KB each) with 1-D
 // bulk copies (cp.async.bulk, non-multicast, L2 evict-first), each completing
 // on a "full" mbarrier; consumers read the stage with 16-byte shared loads,
 // fold it into their per-lane statistics (vp_stats.cuh) and arrive on the
 // stage's "empty" mbarrier. The producer runs ahead across row boundaries, so
-// HBM keeps streaming while the consumers merge a finished row (warp
-// double-float sums, then one warp's fp64 merge of the 8 warp partials). The
-// unaligned head and tail of a row (< 16 bytes each) are read directly.
+// HBM keeps streaming across rows. At the end of a row each consumer warp
+// merges its lanes (double-float sums) and hands its partial to the finisher
+// warp through a double-buffered slot (mbarriers, no CTA barrier); the
+// finisher merges the 8 partials in a fixed order and finishes the row in
+// fp64, so the consumers go straight on to the next row. The unaligned head
+// and tail of a row (< 16 bytes each) are read directly.
 // A row's arithmetic depends only on V, the dtype and its address modulo 16,
 // never on N or on which CTA handles it.
 #include "vp_stats.cuh"
@@ -30,13 +34,14 @@ namespace vp {
 
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
-constexpr int kTmaThreads = kTmaConsumers + 32;
+constexpr int kProducerWarp = kTmaConsumerWarps;       // warp 8
+constexpr int kFinisherWarp = kTmaConsumerWarps + 1;   // warp 9
+constexpr int kTmaThreads = kTmaConsumers + 64;
 constexpr int kStageBytes = 16384;
 constexpr int kStages = 6;
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr uint32_t kRowBarrier = 1;  // named barrier of the consumer warps
 
-// Set (OR) when a bounded wait gave up: 1 = producer, 2 = consumer.
+// Set (OR) when a bounded wait gave up: 1 = producer, 2 = consumer or finisher.
 __device__ uint32_t g_tma_fault;
 
 // 16-byte word of -inf values (padding of a partial last stage)
@@ -63,6 +68,8 @@ __device__ __forceinline__ float chunk_max(const uint4 (&u)[K]) {
 struct Ring {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t parts_full[2];   // the 8 consumer warps have written a row's partials
+    uint64_t parts_empty[2];  // the finisher has read them
 };
 
 __device__ __forceinline__ void ring_init(Ring &ring) {
@@ -71,9 +78,28 @@ __device__ __forceinline__ void ring_init(Ring &ring) {
             mbar_init(&ring.full[s], 1);
             mbar_init(&ring.empty[s], kTmaConsumers);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ring.parts_full[b], kTmaConsumerWarps);
+            mbar_init(&ring.parts_empty[b], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
+}
+
+// Consumer warp side of the hand-over of a row's partial to the finisher warp
+// (slot rowi & 1, reused every second row). Returns false on a timeout.
+template <typename P>
+__device__ __forceinline__ bool hand_over(Ring &ring, P (*parts)[kTmaConsumerWarps], int rowi, const P &w,
+                                          int warp, int lane) {
+    bool ok = true;
+    if (lane == 0) {
+        const int slot = rowi & 1, use = rowi >> 1;
+        if (use > 0) ok = mbar_wait(&ring.parts_empty[slot], (use - 1) & 1);
+        parts[slot][warp] = w;
+        mbar_arrive(&ring.parts_full[slot]);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0);
 }
 
 // Producer side: stage `it`'s slot, waiting for the consumers to free it.
@@ -109,7 +135,33 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
     ring_init(ring);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (warp == kTmaConsumerWarps) {                            // producer
+    if (warp == kFinisherWarp) {
+        // merges the 8 warp partials of each row in a fixed order, finishes the
+        // row in fp64 and writes its output, off the consumers' critical path
+        int rowi = 0;
+        for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
+            int64_t t = 0;
+            float zt = 0.f;
+            if (kOp == 0 && lane == 0) {
+                t = targets[r];
+                const int64_t loc = t - vocab_start;
+                if (t >= 0 && loc >= 0 && loc < V) zt = Elem<T>::load1(x + rows.off(r) + loc);
+            }
+            const int slot = rowi & 1;
+            if (!mbar_wait(&ring.parts_full[slot], (rowi >> 1) & 1)) {
+                atomicOr(&g_tma_fault, 2u);
+                return;
+            }
+            const Part1<AccT<T>> p = merge_parts<kW>(parts[slot], kTmaConsumerWarps);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ring.parts_empty[slot]);
+                finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
+            }
+        }
+        return;
+    }
+    if (warp == kProducerWarp) {                                // producer
         if (lane != 0) return;
         const uint64_t pol = policy_evict_first();
         uint32_t it = 0;
@@ -133,19 +185,12 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
     const int ct = threadIdx.x;
     uint32_t it = 0;
     bool ok = true;
-    int parity = 0;
-    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, parity ^= 1) {
+    int rowi = 0;
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
         const T *row = x + rows.off(r);
         const int head = head_count(row, V);
         const int nv = (V - head) / kVec;
         const int tail0 = head + nv * kVec;
-        int64_t t = 0;
-        float zt = 0.f;
-        if (kOp == 0 && ct == 0) {
-            t = targets[r];
-            const int64_t loc = t - vocab_start;
-            if (t >= 0 && loc >= 0 && loc < V) zt = Elem<T>::load1(row + loc);
-        }
         Lane1<T, kW> acc;
         acc.init(kNegBig);
         for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
@@ -177,12 +222,11 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
         if (ct < head) { float v[1] = {Elem<T>::load1(row + ct)}; acc.push(v); }
         if (ct < V - tail0) { float v[1] = {Elem<T>::load1(row + tail0 + ct)}; acc.push(v); }
 
-        const Part1<AccT<T>> w = warp_merge(acc);
-        if (lane == 0) parts[parity][warp] = w;
-        named_sync(kRowBarrier, kTmaConsumers);
-        if (warp == 0) {
-            const Part1<AccT<T>> p = merge_parts<kW>(parts[parity], kTmaConsumerWarps);
-            if (lane == 0 && ok) finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
+        Part1<AccT<T>> w = warp_merge(acc);
+        if (!ok) w.S = AccT<T>(__int_as_float(0x7fc00000));   // a timed-out row finishes as NaN
+        if (!hand_over(ring, parts, rowi, w, warp, lane)) {
+            atomicOr(&g_tma_fault, 2u);
+            return;
         }
     }
 }
@@ -204,7 +248,24 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
     ring_init(ring);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (warp == kTmaConsumerWarps) {
+    if (warp == kFinisherWarp) {
+        int rowi = 0;
+        for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
+            const int slot = rowi & 1;
+            if (!mbar_wait(&ring.parts_full[slot], (rowi >> 1) & 1)) {
+                atomicOr(&g_tma_fault, 2u);
+                return;
+            }
+            const PartKL<AccT<T>> p = kl_merge_parts(parts[slot], kTmaConsumerWarps);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ring.parts_empty[slot]);
+                finish_kl(p, r, kl, stats_p, stats_q);
+            }
+        }
+        return;
+    }
+    if (warp == kProducerWarp) {
         if (lane != 0) return;
         const uint64_t pol = policy_evict_first();
         uint32_t it = 0;
@@ -231,8 +292,8 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
     const int ct = threadIdx.x;
     uint32_t it = 0;
     bool ok = true;
-    int parity = 0;
-    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, parity ^= 1) {
+    int rowi = 0;
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
         const int64_t off = rows.off(r);
         const T *prow = P + off, *qrow = Q + off;
         const int head = head_count(prow, V);
@@ -280,12 +341,11 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
             acc.push(p, q);
         }
 
-        const PartKL<AccT<T>> w = kl_warp_merge(acc);
-        if (lane == 0) parts[parity][warp] = w;
-        named_sync(kRowBarrier, kTmaConsumers);
-        if (warp == 0) {
-            const PartKL<AccT<T>> s = kl_merge_parts(parts[parity], kTmaConsumerWarps);
-            if (lane == 0 && ok) finish_kl(s, r, kl, stats_p, stats_q);
+        PartKL<AccT<T>> w = kl_warp_merge(acc);
+        if (!ok) w.Sp = AccT<T>(__int_as_float(0x7fc00000));  // a timed-out row finishes as NaN
+        if (!hand_over(ring, parts, rowi, w, warp, lane)) {
+            atomicOr(&g_tma_fault, 2u);
+            return;
         }
     }
 }

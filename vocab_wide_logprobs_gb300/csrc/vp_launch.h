@@ -64,6 +64,21 @@ struct LinearFwdArgs {
 
 size_t linear_workspace_bytes(int64_t N, int64_t V);
 
+struct LinearBwdArgs {
+    const void *hidden, *weight;  // bf16 [N, D], [V, D], row-major
+    int64_t N, V, D, vocab_start;
+    const int64_t *targets;
+    const void *stats;            // vp_rowstat [N] of the forward
+    const float *g;               // upstream gradient of logp, fp32 [N]
+    void *dhidden, *dW;           // bf16 [N, D], [V, D]; either may be NULL
+    void *workspace;              // linear_bwd_workspace_bytes(N, V, D)
+    int32_t *err;
+    cudaStream_t stream;
+};
+
+size_t linear_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D);
+cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a);
+
 // Fixed scratch of vp_linear_logp_fwd_noalloc (24 MiB, held by every device
 // that loads the library, for the life of the process).
 constexpr size_t kNoAllocScratchBytes = (size_t)24 << 20;

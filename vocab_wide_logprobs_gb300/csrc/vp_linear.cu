@@ -35,6 +35,7 @@
 
 #include "vp_device.cuh"
 #include "vp_launch.h"
+#include "vp_stats.cuh"
 #include "vp_umma.cuh"
 
 namespace vp {
@@ -56,17 +57,25 @@ struct LinearBars {
     uint32_t tmem_base;
 };
 
+// ---------------------------------------------------------------------------
+// Persistent tcgen05 GEMM C[M, Nn] = A[M, K] . B[Nn, K]^T (bf16 K-major operands
+// through 2-D tensor maps, fp32 accumulation in TMEM) with a pluggable
+// epilogue. Tiles run N-major (consecutive CTAs share one B tile through L2).
+// The epilogue functor is called by each of the 128 epilogue threads for its
+// accumulator row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the
+// row's 256 columns; it reads them with tmem_ld32.
+// ---------------------------------------------------------------------------
+template <class Epi>
 __global__ void __launch_bounds__(kLThreads, 1)
-linear_lse_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w, int N, int V,
-                  int D, int64_t vocab_start, const int64_t *__restrict__ targets, float2 *__restrict__ partials,
-                  float *__restrict__ tgt_logit) {
+umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M, int Nn,
+                 int K, const Epi epi) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ LinearBars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_rb = (N + kLBM - 1) / kLBM, n_vt = (V + kLBN - 1) / kLBN;
-    const int64_t n_tiles = (int64_t)n_rb * n_vt;
-    const int n_k = D / kLBK;
+    const int n_mb = (M + kLBM - 1) / kLBM, n_nb = (Nn + kLBN - 1) / kLBN;
+    const int64_t n_tiles = (int64_t)n_mb * n_nb;
+    const int n_k = (K + kLBK - 1) / kLBK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLStages; ++s) {
@@ -78,8 +87,8 @@ linear_lse_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
             mbar_init(&bars.acc_empty[b], 4 * 32);
         }
         fence_mbar_init();
-        prefetch_tensormap(&tm_h);
-        prefetch_tensormap(&tm_w);
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
     }
     if (warp == 1) tmem_alloc(&bars.tmem_base, kLTmemCols);
     tc_fence_before();
@@ -93,14 +102,14 @@ linear_lse_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
             uint32_t it = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const int rb = (int)(tile % n_rb), vt = (int)(tile / n_rb);
+                const int mb = (int)(tile % n_mb), nb = (int)(tile / n_mb);
                 for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t st = it % kLStages, use = it / kLStages;
                     if (use > 0 && !mbar_wait(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
                     uint8_t *a = smem + st * kLStageBytes;
                     mbar_arrive_expect_tx(&bars.full[st], kLStageBytes);
-                    tma_load_2d(a, &tm_h, kb * kLBK, rb * kLBM, &bars.full[st]);
-                    tma_load_2d(a + kLAStage, &tm_w, kb * kLBK, vt * kLBN, &bars.full[st]);
+                    tma_load_2d(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st]);
+                    tma_load_2d(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st]);
                 }
             }
             if (!ok) atomicOr(&g_linear_fault, 1u);
@@ -132,62 +141,211 @@ linear_lse_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constan
             if (!ok) atomicOr(&g_linear_fault, 2u);
         }
     } else {
-        // ---------------- epilogue: per-row (m, S) of each tile ----------------
+        // ---------------- epilogue ----------------
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const int r_in = q * 32 + lane;
         uint32_t j = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
-            const int rb = (int)(tile % n_rb), vt = (int)(tile / n_rb);
+            const int mb = (int)(tile % n_mb), nb = (int)(tile / n_mb);
             const uint32_t buf = j & 1;
             if (ok && !mbar_wait(&bars.acc_full[buf], (j >> 1) & 1)) {
                 ok = false;
                 atomicOr(&g_linear_fault, 4u);
             }
             tc_fence_after();
-            const int row = rb * kLBM + r_in;
-            const int ncol = min(kLBN, V - vt * kLBN);   // valid vocabulary columns of this tile
-            int tloc = -1;
-            if (row < N) {
-                const int64_t t = targets[row] - vocab_start - (int64_t)vt * kLBN;
-                if (targets[row] >= 0 && t >= 0 && t < ncol) tloc = (int)t;
-            }
-            float m = -INFINITY, S = 0.f, zt = 0.f;
-            const uint32_t base = tmem + buf * kLBN + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-            for (int c = 0; c < kLBN / 32; ++c) {
-                float v[32];
-                tmem_ld32(base + c * 32, v);
-                float cm = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (c * 32 + i >= ncol) v[i] = -INFINITY;   // past the vocabulary
-                    if (c * 32 + i == tloc) zt = v[i];
-                    cm = fmaxf(cm, v[i]);
-                }
-                if (cm > m) {
-                    S *= exp2f((m - cm) * kLog2e);
-                    m = cm;
-                }
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    s0 += exp2f((v[i] - m) * kLog2e);
-                    s1 += exp2f((v[i + 1] - m) * kLog2e);
-                }
-                S += s0 + s1;
-            }
+            if (ok) epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
+                        tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[buf]);           // the MMA warp may reuse the accumulator
-            if (row < N && ok) {
-                partials[(int64_t)row * n_vt + vt] = make_float2(m, S);
-                if (tloc >= 0) tgt_logit[row] = zt;
-            }
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, kLTmemCols);
+}
+
+// Forward epilogue: the tile's per-row max m and sum-exp S (fp32) and the target
+// logit when the row's target falls in the tile.
+struct LseEpi {
+    int N, V, n_vt;
+    int64_t vocab_start;
+    const int64_t *targets;
+    float2 *partials;   // [N][n_vt]
+    float *tgt_logit;   // [N]
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        if (row >= N) return;
+        const int64_t tg = targets[row];
+        const int64_t t = tg - vocab_start - col0;
+        const int tloc = (tg >= 0 && t >= 0 && t < ncol) ? (int)t : -1;
+        float m = -INFINITY, S = 0.f, zt = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kLBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            float cm = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if (c * 32 + i >= ncol) v[i] = -INFINITY;   // past the vocabulary
+                if (c * 32 + i == tloc) zt = v[i];
+                cm = fmaxf(cm, v[i]);
+            }
+            if (cm > m) {
+                S *= exp2f((m - cm) * kLog2e);
+                m = cm;
+            }
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                s0 += exp2f((v[i] - m) * kLog2e);
+                s1 += exp2f((v[i + 1] - m) * kLog2e);
+            }
+            S += s0 + s1;
+        }
+        partials[(int64_t)row * n_vt + col0 / kLBN] = make_float2(m, S);
+        if (tloc >= 0) tgt_logit[row] = zt;
+    }
+};
+
+// Backward K1 epilogue: dz = g (onehot - p), p = exp((z - m) - logS), for a
+// 256-column tile of a vocabulary chunk starting at shard column v0, written
+// as bf16 (round to nearest even) both row-major dz[row][col] (pitch ldz) and
+// transposed dzt[col][row] (pitch ldt). Rows with an ignored target get 0,
+// rows with a data error or without valid statistics get NaN.
+struct DzEpi {
+    int N, V, v0, ldz, ldt;
+    int64_t vocab_start;
+    const int64_t *targets;
+    const RowStat *stats;
+    const float *g;
+    __nv_bfloat16 *dz, *dzt;
+    int32_t *err;
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        if (row >= N) return;
+        const RowStat s = load_rowstat(stats + row);
+        const int64_t tg = targets[row];
+        const int64_t tl = tg - vocab_start;                // target column in the shard
+        int mode = 0;                                      // 0 normal, 1 zero row, 2 NaN row
+        if (tg < 0) mode = 1;
+        else if (tl < 0 || tl >= V) mode = 2;
+        if (s.flags & (kRowNanInf | kRowEmpty)) mode = mode == 1 ? 1 : 2;
+        if (mode == 2 && err && col0 == 0 && v0 == 0 && tg >= 0 && (tl < 0 || tl >= V)) atomicOr(err, VP_ERRBIT_TARGET_);
+        const int64_t tcol = tl - v0 - col0;               // target column within this tile
+        const float gr = g[row];
+#pragma unroll 1
+        for (int c = 0; c < kLBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float d[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = c * 32 + i + e;
+                    const float p = ex2_fast(((v[i + e] - s.m) - s.logS_hi) * kLog2e);
+                    float x = (col == tcol) ? gr * (1.f - p) : -gr * p;
+                    if (mode == 1 || col >= ncol) x = 0.f;
+                    else if (mode == 2) x = __int_as_float(0x7fc00000);
+                    d[e] = x;
+                }
+                __nv_bfloat162 b = __floats2bfloat162_rn(d[0], d[1]);
+                packed[i / 2] = *reinterpret_cast<uint32_t *>(&b);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(dz + (int64_t)row * ldz + col0 + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+            unsigned short *t = reinterpret_cast<unsigned short *>(dzt);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                t[(int64_t)(col0 + c * 32 + i) * ldt + row] = (unsigned short)(packed[i / 2] >> (16 * (i & 1)));
+        }
+    }
+};
+
+// Backward K2 epilogue: acc[row][col] (+)= tile, fp32 (pitch ld).
+struct AccEpi {
+    int M, ld;
+    bool first;
+    float *acc;
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        if (row >= M) return;
+        float *dst = acc + (int64_t)row * ld + col0;
+#pragma unroll 1
+        for (int c = 0; c < kLBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            if (c * 32 >= ncol) continue;
+            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                if (!first) {
+                    const float4 a = d4[k];
+                    o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+                }
+                d4[k] = o;
+            }
+        }
+    }
+};
+
+// Backward K3 epilogue: out[row0 + row][col] = bf16(tile) (pitch ld), rows < M.
+struct StoreBf16Epi {
+    int M, ld;
+    int64_t row0;
+    __nv_bfloat16 *out;
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        if (row >= M) return;
+        __nv_bfloat16 *dst = out + (row0 + row) * (int64_t)ld + col0;
+#pragma unroll 1
+        for (int c = 0; c < kLBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            if (c * 32 >= ncol) continue;
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                packed[i] = *reinterpret_cast<uint32_t *>(&b);
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+        }
+    }
+};
+
+// dst[c][r] = src[r][c] for a rows x cols bf16 block (pitches in elements); 32 x 32
+// tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16 *__restrict__ src, int rows,
+                                                             int cols, int64_t ld_src,
+                                                             __nv_bfloat16 *__restrict__ dst, int64_t ld_dst) {
+    __shared__ unsigned short tile[32][33];
+    const unsigned short *s = reinterpret_cast<const unsigned short *>(src);
+    unsigned short *d = reinterpret_cast<unsigned short *>(dst);
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int r = r0 + ty + k, c = c0 + tx;
+        tile[ty + k][tx] = (r < rows && c < cols) ? s[(int64_t)r * ld_src + c] : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int c = c0 + ty + k, r = r0 + tx;
+        if (c < cols && r < rows) d[(int64_t)c * ld_dst + r] = tile[tx][ty + k];
+    }
+}
+
+// out[i] = bf16(acc[i]) for rows x cols (pitches in elements)
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ acc, int64_t n,
+                                                      __nv_bfloat16 *__restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = __float2bfloat16_rn(acc[i]);
 }
 
 // One warp per row: fp64 merge of the row's per-tile (m, S), in a fixed order.
@@ -246,17 +404,39 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
-// Row-major [rows, D] bf16 matrix, boxes of box_rows x 64 with the 128-byte swizzle.
-static bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t D, int box_rows) {
+// Row-major bf16 matrix of `rows` rows of `cols` valid elements, `pitch`
+// elements apart; boxes of box_rows x 64 with the 128-byte swizzle. Boxes past
+// the extents read as zeros.
+static bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int64_t pitch, int box_rows) {
     auto enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
     cuuint32_t box[2] = {(cuuint32_t)kLBK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Epi>
+static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, const Epi &epi,
+                               cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done.load() & (1ull << (dev & 63)))) {
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kLSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(1ull << (dev & 63));
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t n_tiles = (int64_t)((M + kLBM - 1) / kLBM) * ((Nn + kLBN - 1) / kLBN);
+    const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
+    umma_gemm_kernel<Epi><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, M, Nn, K, epi);
+    return cudaGetLastError();
 }
 
 size_t linear_workspace_bytes(int64_t N, int64_t V) {
@@ -266,29 +446,15 @@ size_t linear_workspace_bytes(int64_t N, int64_t V) {
 }
 
 cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a) {
-    static std::atomic<uint64_t> attr_done{0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        cudaError_t e = cudaFuncSetAttribute(linear_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kLSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done.fetch_or(1ull << (dev & 63));
-    }
     CUtensorMap tm_h, tm_w;
-    if (!make_map(&tm_h, a.hidden, a.N, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, kLBN))
+    if (!make_map(&tm_h, a.hidden, a.N, a.D, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, a.D, kLBN))
         return cudaErrorInvalidValue;
     const int64_t n_vt = (a.V + kLBN - 1) / kLBN;
     float2 *partials = static_cast<float2 *>(a.workspace);
     float *tgt = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) +
                                            (((size_t)a.N * n_vt * sizeof(float2) + 255) & ~(size_t)255));
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t n_tiles = ((a.N + kLBM - 1) / kLBM) * n_vt;
-    const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
-    linear_lse_kernel<<<grid, kLThreads, kLSmemBytes, a.stream>>>(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D,
-                                                                   a.vocab_start, a.targets, partials, tgt);
-    cudaError_t e = cudaGetLastError();
+    const LseEpi epi{(int)a.N, (int)a.V, (int)n_vt, a.vocab_start, a.targets, partials, tgt};
+    cudaError_t e = launch_gemm(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D, epi, a.stream);
     if (e != cudaSuccess) return e;
     linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
         (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
@@ -324,16 +490,8 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
     void *scratch = nullptr;
     cudaError_t e = noalloc_scratch_address(&scratch);
     if (e != cudaSuccess) return e;
-    static std::atomic<uint64_t> attr_done{0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        e = cudaFuncSetAttribute(linear_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_done.fetch_or(1ull << (dev & 63));
-    }
     CUtensorMap tm_h, tm_w;
-    if (!make_map(&tm_h, a.hidden, a.N, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, kLBN))
+    if (!make_map(&tm_h, a.hidden, a.N, a.D, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, a.D, kLBN))
         return cudaErrorInvalidValue;
     const int64_t n_vt = (a.V + kLBN - 1) / kLBN;
     // Every partial and every in-shard target logit is written by the first
@@ -341,17 +499,102 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
     float2 *partials = static_cast<float2 *>(scratch);
     float *tgt = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
                                            (((size_t)a.N * n_vt * sizeof(float2) + 255) & ~(size_t)255));
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t n_tiles = ((a.N + kLBM - 1) / kLBM) * n_vt;
-    const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
-    linear_lse_kernel<<<grid, kLThreads, kLSmemBytes, a.stream>>>(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D,
-                                                                   a.vocab_start, a.targets, partials, tgt);
-    e = cudaGetLastError();
+    const LseEpi epi{(int)a.N, (int)a.V, (int)n_vt, a.vocab_start, a.targets, partials, tgt};
+    e = launch_gemm(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D, epi, a.stream);
     if (e != cudaSuccess) return e;
     linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
         (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Backward: vocabulary chunks of kVc rows of W.
+//   K1  logits tile (h . W_c^T, K = D) -> dz, dz^T            (DzEpi)
+//   K2  dhidden_acc (+)= dz . W_c     (A = dz, B = W_c^T, K = chunk)   (AccEpi)
+//   K3  dW_c = dz^T . h               (A = dz^T, B = h^T, K = N)       (StoreBf16Epi)
+// Every operand is K-major: W_c^T and h^T come from transpose kernels.
+// ---------------------------------------------------------------------------
+constexpr int64_t kVc = 8192;
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct BwdLayout {
+    size_t ht, wt, dz, dzt, acc, total;
+};
+
+// Pitch (elements) of the transposed [., N] buffers: a multiple of 8, so that
+// rows start on 16-byte boundaries as the tensor maps require.
+static int64_t pitch_n(int64_t N) { return (N + 7) & ~(int64_t)7; }
+
+static BwdLayout bwd_layout(int64_t N, int64_t V, int64_t D) {
+    const int64_t vc = V < kVc ? ((V + 255) / 256) * 256 : kVc;
+    const int64_t ldn = pitch_n(N);
+    BwdLayout L;
+    L.ht = 0;
+    L.wt = L.ht + up256((size_t)D * ldn * 2);
+    L.dz = L.wt + up256((size_t)D * vc * 2);
+    L.dzt = L.dz + up256((size_t)N * vc * 2);
+    L.acc = L.dzt + up256((size_t)vc * ldn * 2);
+    L.total = L.acc + up256((size_t)N * D * 4);
+    return L;
+}
+
+size_t linear_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D) { return bwd_layout(N, V, D).total; }
+
+cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
+    const BwdLayout L = bwd_layout(a.N, a.V, a.D);
+    const int64_t vc = a.V < kVc ? ((a.V + 255) / 256) * 256 : kVc;
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    __nv_bfloat16 *ht = reinterpret_cast<__nv_bfloat16 *>(ws + L.ht);
+    __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(ws + L.wt);
+    __nv_bfloat16 *dz = reinterpret_cast<__nv_bfloat16 *>(ws + L.dz);
+    __nv_bfloat16 *dzt = reinterpret_cast<__nv_bfloat16 *>(ws + L.dzt);
+    float *acc = reinterpret_cast<float *>(ws + L.acc);
+    const __nv_bfloat16 *h = static_cast<const __nv_bfloat16 *>(a.hidden);
+    const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(a.weight);
+    const int N = (int)a.N, V = (int)a.V, D = (int)a.D;
+    const int ldn = (int)pitch_n(a.N);
+    cudaError_t e;
+
+    CUtensorMap tm_h, tm_w, tm_dz, tm_wt, tm_dzt, tm_ht;
+    if (!make_map(&tm_h, h, N, D, D, kLBM) || !make_map(&tm_w, W, V, D, D, kLBN)) return cudaErrorInvalidValue;
+    if (a.dW) {
+        dim3 grid((D + 31) / 32, (N + 31) / 32);
+        transpose_bf16_kernel<<<grid, 256, 0, a.stream>>>(h, N, D, D, ht, ldn);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (!make_map(&tm_ht, ht, D, N, ldn, kLBN)) return cudaErrorInvalidValue;
+    }
+    for (int64_t v0 = 0; v0 < V; v0 += vc) {
+        const int nv = (int)(V - v0 < vc ? V - v0 : vc);
+        // K1 over this chunk's rows of W (the map's rows start at v0)
+        CUtensorMap tm_wc;
+        if (!make_map(&tm_wc, W + v0 * D, nv, D, D, kLBN)) return cudaErrorInvalidValue;
+        const DzEpi de{N, V, (int)v0, (int)vc, ldn, a.vocab_start, a.targets,
+                       static_cast<const RowStat *>(a.stats), a.g, dz, dzt, a.err};
+        if ((e = launch_gemm(tm_h, tm_wc, N, nv, D, de, a.stream)) != cudaSuccess) return e;
+        if (a.dhidden) {
+            dim3 grid((D + 31) / 32, (nv + 31) / 32);
+            transpose_bf16_kernel<<<grid, 256, 0, a.stream>>>(W + v0 * D, nv, D, D, wt, vc);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map(&tm_wt, wt, D, nv, vc, kLBN))
+                return cudaErrorInvalidValue;
+            const AccEpi ae{N, D, v0 == 0, acc};
+            if ((e = launch_gemm(tm_dz, tm_wt, N, D, nv, ae, a.stream)) != cudaSuccess) return e;
+        }
+        if (a.dW) {
+            if (!make_map(&tm_dzt, dzt, nv, N, ldn, kLBM)) return cudaErrorInvalidValue;
+            const StoreBf16Epi se{nv, D, v0, static_cast<__nv_bfloat16 *>(a.dW)};
+            if ((e = launch_gemm(tm_dzt, tm_ht, nv, D, N, se, a.stream)) != cudaSuccess) return e;
+        }
+    }
+    (void)tm_w;
+    if (a.dhidden) {
+        const int64_t n = (int64_t)N * D;
+        to_bf16_kernel<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256, 0, a.stream>>>(
+            acc, n, static_cast<__nv_bfloat16 *>(a.dhidden));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t read_linear_fault(uint32_t *value, bool clear) {
