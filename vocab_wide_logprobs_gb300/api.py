@@ -186,6 +186,10 @@ def vp_linear_logp_fwd(hidden, weight, targets, vocab_start: int = 0, err_word=N
     return logp, stats
 
 
+def vp_linear_logp_bwd_workspace_size(N: int, V: int, D: int) -> int:
+    return int(_lib.lib().vp_linear_logp_bwd_workspace_size(N, V, D))
+
+
 def vp_linear_logp_bwd(hidden, weight, targets, stats, grad, vocab_start: int = 0, want_dhidden=True, want_dW=True,
                        err_word=None, dhidden=None, dW=None, workspace=None):
     """Returns (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None)."""
@@ -198,7 +202,7 @@ def vp_linear_logp_bwd(hidden, weight, targets, stats, grad, vocab_start: int = 
     dhidden = dhidden if want_dhidden else None
     dW = dW if want_dW else None
     if workspace is None:
-        need = int(_lib.lib().vp_linear_logp_bwd_workspace_size(N, V, D))
+        need = vp_linear_logp_bwd_workspace_size(N, V, D)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=hidden.device)
     _check(_lib.lib().vp_linear_logp_bwd(_ptr(hidden), _ptr(weight), N, V, D, vocab_start, _ptr(targets),
                                          _ptr(stats), _ptr(grad), _ptr(dhidden), _ptr(dW), _ptr(workspace),

@@ -185,8 +185,19 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
                     float z[kVec], d[kVec];
                     Elem<T>::unpack(u[k], z);
                     const int64_t j0 = head + (int64_t)i * kVec;
+                    if (kOp == 0 && !Elem<T>::kPrecise) {
+                        // every element as a non-target; the vector holding the target fixes it up
 #pragma unroll
-                    for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, s, g, loc);
+                        for (int e = 0; e < kVec; ++e) d[e] = grad_elem<0, T>(z[e], 0, s, g, -1);
+                        if (loc >= j0 && loc < j0 + kVec) {
+#pragma unroll
+                            for (int e = 0; e < kVec; ++e)
+                                if (j0 + e == loc) d[e] = grad_elem<0, T>(z[e], loc, s, g, loc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, s, g, loc);
+                    }
                     stg_stream(vout + i, Elem<T>::pack(d));
                 }
             }

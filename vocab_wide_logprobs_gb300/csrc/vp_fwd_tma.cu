@@ -203,10 +203,15 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
             const uint4 *sv = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes);
             const uint4 pad = splat_neg_inf<T>();
             uint4 u[kPerThread];
+            if (cnt == kChunkVec) {
 #pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const int i = ct + k * kTmaConsumers;
-                u[k] = i < cnt ? sv[i] : pad;
+                for (int k = 0; k < kPerThread; ++k) u[k] = sv[ct + k * kTmaConsumers];
+            } else {
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    const int i = ct + k * kTmaConsumers;
+                    u[k] = i < cnt ? sv[i] : pad;
+                }
             }
             mbar_arrive(&ring.empty[st]);                       // the words are in registers
             if (c0 == 0) acc.init(warp_centre(chunk_max<T>(u)));   // the warp's centre for this row
@@ -312,11 +317,19 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
             const uint4 *sq = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes + kHalf);
             const uint4 pad = splat_neg_inf<T>();
             uint4 up[kPerThread], uq[kPerThread];
+            if (cnt == kChunkVec) {
 #pragma unroll
-            for (int k = 0; k < kPerThread; ++k) {
-                const int i = ct + k * kTmaConsumers;
-                up[k] = i < cnt ? sp[i] : pad;
-                uq[k] = i < cnt ? sq[i] : pad;
+                for (int k = 0; k < kPerThread; ++k) {
+                    up[k] = sp[ct + k * kTmaConsumers];
+                    uq[k] = sq[ct + k * kTmaConsumers];
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    const int i = ct + k * kTmaConsumers;
+                    up[k] = i < cnt ? sp[i] : pad;
+                    uq[k] = i < cnt ? sq[i] : pad;
+                }
             }
             mbar_arrive(&ring.empty[st]);
             if (c0 == 0) acc.init(warp_centre(chunk_max<T>(up)), warp_centre(chunk_max<T>(uq)));

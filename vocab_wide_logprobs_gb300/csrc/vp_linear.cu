@@ -63,7 +63,9 @@ struct LinearBars {
 // epilogue. Tiles run N-major (consecutive CTAs share one B tile through L2).
 // The epilogue functor is called by each of the 128 epilogue threads for its
 // accumulator row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the
-// row's 256 columns; it reads them with tmem_ld32.
+// row's 256 columns; it reads them with tmem_ld32, which is warp-collective, so
+// every lane runs every load (rows past M included) and only the global
+// accesses are guarded.
 // ---------------------------------------------------------------------------
 template <class Epi>
 __global__ void __launch_bounds__(kLThreads, 1)
@@ -154,8 +156,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                 atomicOr(&g_linear_fault, 4u);
             }
             tc_fence_after();
-            if (ok) epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
-                        tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
+            // tcgen05.ld is warp-collective: the whole warp calls the epilogue or
+            // none of it does, and epilogues guard only their global accesses
+            if (__all_sync(0xffffffffu, ok))
+                epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
+                    tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[buf]);           // the MMA warp may reuse the accumulator
         }
@@ -174,8 +179,8 @@ struct LseEpi {
     float2 *partials;   // [N][n_vt]
     float *tgt_logit;   // [N]
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
-        if (row >= N) return;
-        const int64_t tg = targets[row];
+        const bool valid = row < N;
+        const int64_t tg = valid ? targets[row] : -1;
         const int64_t t = tg - vocab_start - col0;
         const int tloc = (tg >= 0 && t >= 0 && t < ncol) ? (int)t : -1;
         float m = -INFINITY, S = 0.f, zt = 0.f;
@@ -202,6 +207,7 @@ struct LseEpi {
             }
             S += s0 + s1;
         }
+        if (!valid) return;
         partials[(int64_t)row * n_vt + col0 / kLBN] = make_float2(m, S);
         if (tloc >= 0) tgt_logit[row] = zt;
     }
@@ -221,17 +227,18 @@ struct DzEpi {
     __nv_bfloat16 *dz, *dzt;
     int32_t *err;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
-        if (row >= N) return;
-        const RowStat s = load_rowstat(stats + row);
-        const int64_t tg = targets[row];
+        const bool valid = row < N;
+        const RowStat s = load_rowstat(stats + (valid ? row : 0));
+        const int64_t tg = valid ? targets[row] : -1;
         const int64_t tl = tg - vocab_start;                // target column in the shard
         int mode = 0;                                      // 0 normal, 1 zero row, 2 NaN row
         if (tg < 0) mode = 1;
         else if (tl < 0 || tl >= V) mode = 2;
         if (s.flags & (kRowNanInf | kRowEmpty)) mode = mode == 1 ? 1 : 2;
-        if (mode == 2 && err && col0 == 0 && v0 == 0 && tg >= 0 && (tl < 0 || tl >= V)) atomicOr(err, VP_ERRBIT_TARGET_);
+        if (valid && mode == 2 && err && col0 == 0 && v0 == 0 && tg >= 0 && (tl < 0 || tl >= V))
+            atomicOr(err, VP_ERRBIT_TARGET_);
         const int64_t tcol = tl - v0 - col0;               // target column within this tile
-        const float gr = g[row];
+        const float gr = valid ? g[row] : 0.f;
 #pragma unroll 1
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
@@ -252,6 +259,7 @@ struct DzEpi {
                 __nv_bfloat162 b = __floats2bfloat162_rn(d[0], d[1]);
                 packed[i / 2] = *reinterpret_cast<uint32_t *>(&b);
             }
+            if (!valid) continue;
             uint4 *dst = reinterpret_cast<uint4 *>(dz + (int64_t)row * ldz + col0 + c * 32);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -270,13 +278,13 @@ struct AccEpi {
     bool first;
     float *acc;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
-        if (row >= M) return;
-        float *dst = acc + (int64_t)row * ld + col0;
+        const bool valid = row < M;
+        float *dst = acc + (int64_t)(valid ? row : 0) * ld + col0;
 #pragma unroll 1
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
-            if (c * 32 >= ncol) continue;
+            if (!valid || c * 32 >= ncol) continue;
             float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -297,13 +305,13 @@ struct StoreBf16Epi {
     int64_t row0;
     __nv_bfloat16 *out;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
-        if (row >= M) return;
-        __nv_bfloat16 *dst = out + (row0 + row) * (int64_t)ld + col0;
+        const bool valid = row < M;
+        __nv_bfloat16 *dst = out + (row0 + (valid ? row : 0)) * (int64_t)ld + col0;
 #pragma unroll 1
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
-            if (c * 32 >= ncol) continue;
+            if (!valid || c * 32 >= ncol) continue;
             uint32_t packed[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {

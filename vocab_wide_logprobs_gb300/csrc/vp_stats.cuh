@@ -93,7 +93,7 @@ struct Lane1 {
     }
 
     // Rare: a value exceeds the centre by more than kSpan.
-    __device__ __noinline__ void move_centre(float c) {
+    __device__ __forceinline__ void move_centre(float c) {
         const double d = (double)c - (double)ref;
         const double a = exp(-d);
         double s = df_value(S), w = df_value(W);
@@ -147,44 +147,45 @@ struct Lane1 {
         const float c = max_bf16(u);
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
-        // W needs 0 * (-inf) kept out only where some t = v - ref is -inf: a -inf
-        // logit, or a spread beyond FLT_MAX (e.g. a row holding -3e38 and 3e38)
-        const bool masked = kW && !((ref - min_bf16(u)) < INFINITY);
         const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
         float2 s[4], w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) s[q] = w[q] = make_float2(0.f, 0.f);
-        if (!masked) {
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
+        for (int k = 0; k < K; ++k) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
-                    const float2 a = __fmul2_rn(t, l2e);
-                    const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
-                    s[q] = __fadd2_rn(s[q], e);
-                    if (kW) w[q] = __ffma2_rn(e, t, w[q]);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < K; ++k) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);
-                    const float2 a = __fmul2_rn(t, l2e);
-                    const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
-                    s[q] = __fadd2_rn(s[q], e);
-                    // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
-                    w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
+                const float2 a = __fmul2_rn(t, l2e);
+                const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                s[q] = __fadd2_rn(s[q], e);
+                if (kW) w[q] = __ffma2_rn(e, t, w[q]);
             }
         }
         const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
         df_add(S, ss.x + ss.y);
         if (kW) {
-            const float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
-            df_add(W, ww.x + ww.y);
+            float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+            float wsum = ww.x + ww.y;
+            // e * t is 0 * (-inf) = NaN where t = -inf (a -inf logit or a spread beyond
+            // FLT_MAX): redo W for this chunk with t clamped (e is exactly 0 below t = -104)
+            if (!(fabsf(wsum) < INFINITY)) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < K; ++k) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);
+                        const float2 a = __fmul2_rn(t, l2e);
+                        const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                        w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
+                    }
+                }
+                ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+                wsum = ww.x + ww.y;
+            }
+            df_add(W, wsum);
         }
     }
 };
@@ -277,7 +278,7 @@ struct LaneKL {
         flag = 0; moved = 0;
     }
 
-    __device__ __noinline__ void move_centres(float np, float nq) {
+    __device__ __forceinline__ void move_centres(float np, float nq) {
         const double dp = (double)np - (double)rp, dq = (double)nq - (double)rq;
         const double ap = exp(-dp), aq = exp(-dq);
         const double sp = df_value(Sp), sq = df_value(Sq), w = df_value(W);
@@ -341,31 +342,34 @@ struct LaneKL {
         mxq = fmaxf(mxq, cq);
         const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
         if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
-        // zero-weight guards and the mismatch flag matter only where some centred
-        // value is -inf: a -inf logit, or a spread beyond FLT_MAX
-        const bool masked = !((rp - min_bf16(up)) < INFINITY) || !((rq - min_bf16(uq)) < INFINITY);
         const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
         const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
         float2 sp[4], sq[4], w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) sp[q] = sq[q] = w[q] = make_float2(0.f, 0.f);
-        if (!masked) {
 #pragma unroll
-            for (int k = 0; k < K; ++k) {
+        for (int k = 0; k < K; ++k) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float2 tp = __fadd2_rn(bf16_pair(word(up[k], q)), nrp);
-                    const float2 tq = __fadd2_rn(bf16_pair(word(uq[k], q)), nrq);
-                    const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
-                    const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
-                    const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
-                    sp[q] = __fadd2_rn(sp[q], ep);
-                    sq[q] = __fadd2_rn(sq[q], eq);
-                    w[q] = __ffma2_rn(ep, __ffma2_rn(tq, m1, tp), w[q]);    // ep (tp - tq)
-                }
+            for (int q = 0; q < 4; ++q) {
+                const float2 tp = __fadd2_rn(bf16_pair(word(up[k], q)), nrp);
+                const float2 tq = __fadd2_rn(bf16_pair(word(uq[k], q)), nrq);
+                const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
+                const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
+                const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
+                sp[q] = __fadd2_rn(sp[q], ep);
+                sq[q] = __fadd2_rn(sq[q], eq);
+                w[q] = __ffma2_rn(ep, __ffma2_rn(tq, m1, tp), w[q]);    // ep (tp - tq)
             }
-        } else {
+        }
+        float2 c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+        float wsum = c.x + c.y;
+        // A -inf logit in P or Q (or a spread beyond FLT_MAX) makes some tp - tq
+        // infinite or NaN and so W non-finite: redo W with zero-weight terms
+        // skipped and take the support-mismatch flag (Q = -inf where P is not).
+        if (!(fabsf(wsum) < INFINITY)) {
             uint32_t fl = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k = 0; k < K; ++k) {
 #pragma unroll
@@ -373,25 +377,23 @@ struct LaneKL {
                     const uint32_t pw = word(up[k], q), qw = word(uq[k], q);
                     fl |= __vcmpeq2(qw, kBf16NegInf2) & ~__vcmpeq2(pw, kBf16NegInf2);
                     const float2 tp = __fadd2_rn(bf16_pair(pw), nrp), tq = __fadd2_rn(bf16_pair(qw), nrq);
-                    const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
+                    const float2 ap = __fmul2_rn(tp, l2e);
                     const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
-                    const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
-                    sp[q] = __fadd2_rn(sp[q], ep);
-                    sq[q] = __fadd2_rn(sq[q], eq);
                     float2 d = __ffma2_rn(tq, m1, tp);                            // tp - tq
                     d.x = ep.x > 0.f ? d.x : 0.f;                                 // zero-weight terms add nothing
                     d.y = ep.y > 0.f ? d.y : 0.f;
                     w[q] = __ffma2_rn(ep, d, w[q]);
                 }
             }
+            c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+            wsum = c.x + c.y;
             flag |= (fl != 0);
         }
         const float2 a = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
         const float2 b = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
-        const float2 c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
         df_add(Sp, a.x + a.y);
         df_add(Sq, b.x + b.y);
-        df_add(W, c.x + c.y);
+        df_add(W, wsum);
     }
 };
 
