@@ -50,10 +50,10 @@ def algorithmic_bytes(N: int, V: int, s: int = 2) -> dict:
 
 
 KERNEL_OF = {  # op -> kernel name prefix in profiles (mangled names contain these)
-    "logprobs_fwd": "stats_fwd_kernel<0", "logprobs_bwd": "grad_kernel<0",
-    "entropy_fwd": "stats_fwd_kernel<1", "entropy_bwd": "grad_kernel<1",
-    "kl_rev_fwd": "kl_fwd_kernel", "kl_rev_bwd": "kl_grad_kernel",
-    "kl_fwd_fwd": "kl_fwd_kernel", "kl_fwd_bwd": "kl_grad_kernel",
+    "logprobs_fwd": "stats_fwd_tma_kernel<0", "logprobs_bwd": "grad_kernel<0",
+    "entropy_fwd": "stats_fwd_tma_kernel<1", "entropy_bwd": "grad_kernel<1",
+    "kl_rev_fwd": "kl_fwd_tma_kernel", "kl_rev_bwd": "kl_grad_kernel",
+    "kl_fwd_fwd": "kl_fwd_tma_kernel", "kl_fwd_bwd": "kl_grad_kernel",
 }
 
 
@@ -66,9 +66,12 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "src": "fallback"}
 
 
-def source_hash() -> str:
+def source_hash(files=None) -> str:
+    """Hash of the given csrc files (all of csrc when None), to tie a recorded ncu figure to the code it measured."""
+    csrc = os.path.join(ROOT, "vocab_wide_logprobs_gb300", "csrc")
+    paths = sorted(glob.glob(os.path.join(csrc, "*"))) if files is None else [os.path.join(csrc, f) for f in files]
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "vocab_wide_logprobs_gb300", "csrc", "*"))):
+    for f in paths:
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -82,7 +85,7 @@ def traffic_for(kernel_key: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel_key)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(e.get("sources")):
         return None
     return e.get("bytes_per_launch")
 
@@ -157,6 +160,13 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
+    if args.linear_only:
+        if rank == 0:
+            print(json.dumps({"linear_logp": linear_bench(args, dev, N=args.linear_rows)}))
+        if dist:
+            dist.destroy_process_group()
+        return
+
     w = workloads.pages_shape(seed=1 + rank, N=args.rows)
     a, b = w["a"].to(dev), w["b"].to(dev)
     t, g = w["targets"].to(dev), w["grad"].to(dev)
@@ -166,23 +176,30 @@ def run_ours(args, rank, world, local_rank):
 
     # outputs, allocated once (the library never allocates)
     f32 = lambda: torch.empty(N, dtype=torch.float32, device=dev)
-    st = {k: f32() for k in ("lp", "H", "kl")}
+    st = {k: f32() for k in ("lp", "H", "kl", "kl2")}
     st.update({k: vp.rowstats(N, dev) for k in ("lp_s", "H_s", "sa", "sb")})
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     dx = torch.empty_like(a)
     da, db = torch.empty_like(a), torch.empty_like(a)
 
     R, F = vp.KL_REVERSE, vp.KL_FORWARD
-    calls = {
-        "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a, t, 0, err, st["lp"], st["lp_s"]),
-        "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a, t, st["lp_s"], g, 0, err, dx),
-        "entropy_fwd": lambda: vp.vp_entropy_fwd(a, st["H"], st["H_s"]),
-        "entropy_bwd": lambda: vp.vp_entropy_bwd(a, st["H_s"], g, dx),
-        "kl_rev_fwd": lambda: vp.vp_kl_fwd(a, b, R, st["kl"], st["sa"], st["sb"]),
-        "kl_rev_bwd": lambda: vp.vp_kl_bwd(a, b, R, st["sa"], st["sb"], g, da=da, db=db),
-        "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a, b, F, st["kl"], st["sa"], st["sb"]),
-        "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a, b, F, st["sa"], st["sb"], g, da=da, db=db),
-    }
+
+    def make_calls(sl):
+        """The step's eight calls on the rows `sl` of every buffer."""
+        a_, b_, t_, g_, dx_, da_, db_ = a[sl], b[sl], t[sl], g[sl], dx[sl], da[sl], db[sl]
+        s_ = {k: v[sl] for k, v in st.items()}
+        return {
+            "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a_, t_, 0, err, s_["lp"], s_["lp_s"]),
+            "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a_, t_, s_["lp_s"], g_, 0, err, dx_),
+            "entropy_fwd": lambda: vp.vp_entropy_fwd(a_, s_["H"], s_["H_s"]),
+            "entropy_bwd": lambda: vp.vp_entropy_bwd(a_, s_["H_s"], g_, dx_),
+            "kl_rev_fwd": lambda: vp.vp_kl_fwd(a_, b_, R, s_["kl"], s_["sa"], s_["sb"]),
+            "kl_rev_bwd": lambda: vp.vp_kl_bwd(a_, b_, R, s_["sa"], s_["sb"], g_, da=da_, db=db_),
+            "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a_, b_, F, s_["kl2"], s_["sa"], s_["sb"]),
+            "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a_, b_, F, s_["sa"], s_["sb"], g_, da=da_, db=db_),
+        }
+
+    calls = make_calls(slice(None))
 
     def op(name):
         calls[name]()
@@ -238,11 +255,11 @@ def run_ours(args, rank, world, local_rank):
 
     linear = None
     if not args.no_linear and rank == 0:
-        linear = linear_bench(args, dev)
+        linear = linear_bench(args, dev, N=args.linear_rows)
 
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream, dev)
+        e2e = end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -320,37 +337,48 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
                              "note": "three GEMMs of 2NVD each (logits recomputed, dhidden, dW)"}}
 
 
-def end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream, dev):
+def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev, chunks=8):
+    """The step end to end through the public API with host buffers.
+
+    Every step copies the step's inputs from pinned host memory, runs the eight
+    calls and reads the per-row results back. Rows are independent, so the step
+    is cut into `chunks` row blocks: block k's host-to-device copy runs on a copy
+    stream while the calls of block k - 1 run on the compute stream."""
     import torch
     N = a.shape[0]
-    # end to end through the public API with host buffers: H2D of the step's inputs,
-    # the step, D2H of its per-row results, every step
     h_a, h_b = w["a"].pin_memory(), w["b"].pin_memory()
     h_t, h_g = w["targets"].pin_memory(), w["grad"].pin_memory()
     h_out = torch.empty(4, N, dtype=torch.float32).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in (h_a, h_b, h_t, h_g))
     d2h = h_out.numel() * 4
+    chunks = max(1, min(chunks, N))
+    bounds = [N * k // chunks for k in range(chunks + 1)]
+    blocks = [slice(bounds[k], bounds[k + 1]) for k in range(chunks)]
+    calls = [make_calls(sl) for sl in blocks]
+    copy = torch.cuda.Stream(dev)
+    landed = [torch.cuda.Event() for _ in blocks]   # block k's inputs are on the device
+    read = [torch.cuda.Event() for _ in blocks]     # block k's calls have read its inputs
 
     def e2e_step():
-        a.copy_(h_a, non_blocking=True)
-        b.copy_(h_b, non_blocking=True)
-        t.copy_(h_t, non_blocking=True)
-        g.copy_(h_g, non_blocking=True)
-        outs = []
-        for name in ops:
-            op(name)
-            if name == "kl_rev_fwd" or name == "kl_fwd_fwd":
-                outs.append(st["kl"].clone())
-        h_out[0].copy_(st["lp"], non_blocking=True)
-        h_out[1].copy_(st["H"], non_blocking=True)
-        h_out[2].copy_(outs[0], non_blocking=True)
-        h_out[3].copy_(outs[1], non_blocking=True)
+        for k, sl in enumerate(blocks):
+            with torch.cuda.stream(copy):
+                copy.wait_event(read[k])            # the previous step is done with these rows
+                for dst, src in ((a, h_a), (b, h_b), (t, h_t), (g, h_g)):
+                    dst[sl].copy_(src[sl], non_blocking=True)
+                landed[k].record(copy)
+            stream.wait_event(landed[k])
+            for name in ops:
+                calls[k][name]()
+            read[k].record(stream)
+            for i, key in enumerate(("lp", "H", "kl", "kl2")):
+                h_out[i, sl].copy_(st[key][sl], non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(args.steps, 10))
     e0.record(stream)
+    copy.wait_event(e0)
     for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
@@ -361,7 +389,8 @@ def end_to_end(args, w, a, b, t, g, st, ops, op, step_bytes, world, dist, stream
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
     return {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
-            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": f"{chunks} row blocks; host-to-device copies on a copy stream overlap the calls"}
 
 
 # ---------------------------------------------------------------------------
@@ -448,6 +477,9 @@ def main():
     p.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (8192 is the benchmarked workload)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     p.add_argument("--no-linear", action="store_true", help="skip the fused linear-logp measurement")
+    p.add_argument("--linear-only", action="store_true",
+                   help="only the fused linear-logp measurement (profiling of the GEMM kernels)")
+    p.add_argument("--linear-rows", type=int, default=8192, help="hidden rows of the linear-logp workload")
     args = p.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

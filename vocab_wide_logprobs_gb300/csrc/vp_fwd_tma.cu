@@ -15,8 +15,8 @@
 // body through a ring of kStages shared-memory stages (16 KB each) with 1-D
 // bulk copies (cp.async.bulk, non-multicast, L2 evict-first), each completing
 // on a "full" mbarrier; consumers read the stage with 16-byte shared loads,
-// fold it into their per-lane statistics (vp_stats.cuh) and arrive on the
-// stage's "empty" mbarrier. The producer runs ahead across row boundaries, so
+// and each warp arrives once on the stage's "empty" mbarrier before folding
+// the words into its per-lane statistics (vp_stats.cuh). The producer runs ahead across row boundaries, so
 // HBM keeps streaming across rows. At the end of a row each consumer warp
 // merges its lanes (double-float sums) and hands its partial to the finisher
 // warp through a double-buffered slot (mbarriers, no CTA barrier); the
@@ -76,7 +76,7 @@ __device__ __forceinline__ void ring_init(Ring &ring) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ring.full[s], 1);
-            mbar_init(&ring.empty[s], kTmaConsumers);
+            mbar_init(&ring.empty[s], kTmaConsumerWarps);   // one arrival per consumer warp
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ring.parts_full[b], kTmaConsumerWarps);
@@ -100,6 +100,14 @@ __device__ __forceinline__ bool hand_over(Ring &ring, P (*parts)[kTmaConsumerWar
         mbar_arrive(&ring.parts_full[slot]);
     }
     return __shfl_sync(0xffffffffu, ok, 0);
+}
+
+// Consumer warp side: the warp's shared loads of stage `st` are done (ordered
+// before lane 0's release-arrive by the warp barrier), so the producer may
+// refill it.
+__device__ __forceinline__ void release_stage(Ring &ring, uint32_t st, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[st]);
 }
 
 // Producer side: stage `it`'s slot, waiting for the consumers to free it.
@@ -213,7 +221,7 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
                     u[k] = i < cnt ? sv[i] : pad;
                 }
             }
-            mbar_arrive(&ring.empty[st]);                       // the words are in registers
+            release_stage(ring, st, lane);                      // the words are in registers
             if (c0 == 0) acc.init(warp_centre(chunk_max<T>(u)));   // the warp's centre for this row
             if constexpr (Elem<T>::kPrecise) {
                 float v[kPerThread * kVec];
@@ -331,7 +339,7 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
                     uq[k] = i < cnt ? sq[i] : pad;
                 }
             }
-            mbar_arrive(&ring.empty[st]);
+            release_stage(ring, st, lane);
             if (c0 == 0) acc.init(warp_centre(chunk_max<T>(up)), warp_centre(chunk_max<T>(uq)));
             if constexpr (Elem<T>::kPrecise) {
                 float p[kPerThread * kVec], q[kPerThread * kVec];

@@ -24,8 +24,8 @@
 //   2 MB slice of W through L2 while the hidden states (here 64 MB) stay
 //   resident in L2.
 // Kernel 2 (linear_merge_kernel): one warp per row re-centres the row's
-//   per-tile (m, S) on their max in fp64, in a fixed order, and writes logp
-//   and the vp_rowstat record.
+//   per-tile (m, S) on their max (fp32 exponentials, double-float sums), in a
+//   fixed order, and writes logp and the vp_rowstat record (fp64 finish).
 // Scratch: float2 partials [N][ceil(V/256)] and the target logits [N] fp32,
 //   in a caller-provided workspace (see vp_linear_logp_workspace_size).
 #include <cuda.h>
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ 
         out[i] = __float2bfloat16_rn(acc[i]);
 }
 
-// One warp per row: fp64 merge of the row's per-tile (m, S), in a fixed order.
+// One warp per row: merge of the row's per-tile (m, S) in a fixed order.
 __global__ void __launch_bounds__(256)
 linear_merge_kernel(int N, int V, int64_t vocab_start, const int64_t *__restrict__ targets,
                     const float2 *__restrict__ partials, const float *__restrict__ tgt_logit,
@@ -369,16 +369,21 @@ linear_merge_kernel(int N, int V, int64_t vocab_start, const int64_t *__restrict
     float M = -INFINITY;
     for (int i = lane; i < n_vt; i += 32) M = fmaxf(M, p[i].x);
     M = warp_max(M);
-    double S = 0.0;
+    // fp32 exponentials summed as double-floats: each term carries a few fp32
+    // roundings and the positive sum adds none, so S keeps ~1e-7 relative
+    // accuracy without the narrow fp64 pipe
+    DF Sdf{0.f, 0.f};
     bool nan = false;
     for (int i = lane; i < n_vt; i += 32) {
         const float2 v = p[i];
         if (v.y != v.y) nan = true;
-        else if (v.y > 0.f) S += (double)v.y * exp((double)v.x - (double)M);
+        else if (v.y > 0.f) df_add(Sdf, v.y * expf(v.x - M));
     }
-    S = warp_sum(S);
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) df_add(Sdf, shfl_xor(Sdf, m));
     nan = __any_sync(0xffffffffu, nan);
     if (lane != 0) return;
+    const double S = df_value(Sdf);
     uint32_t flags = 0;
     if (nan || S != S) flags |= kRowNanInf;
     else if (S == 0.0) flags |= kRowEmpty;
