@@ -59,6 +59,8 @@ _SIGS = {
     "vpo_kl_bwd": (["P", "P", "I", "I", "i", "P", "P", "P"], None),
     "vpo_entropy_sharded": (["P", "I", "I", "P", "i", "P"], None),
     "vpo_kl_sharded": (["P", "P", "I", "I", "i", "P", "i", "P"], None),
+    "vpo_shard_stats": (["P", "I", "I", "I", "I", "P"], None),
+    "vpo_shard_kl_stats": (["P", "P", "I", "I", "i", "I", "I", "P"], None),
     "vpo_linear_logits": (["P", "P", "I", "I", "I", "P"], None),
     "vpo_linear_logp_fwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P", "P"], None),
     "vpo_linear_logp_bwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P"], None),
@@ -188,6 +190,28 @@ def kl_sharded(a, b, cuts, direction=REVERSE, lib=None):
     kl = np.empty(N)
     (lib or _load()).vpo_kl_sharded(_p(a), _p(b), N, V, int(direction), _p(c), len(c) - 1, _p(kl))
     return kl
+
+
+def shard_stats(x, lo, hi, lib=None):
+    """Per-row records of the vocabulary shard [lo, hi): columns m, S, W, bad (see vpo_shard_stats)."""
+    x = _f64(x)
+    N, V = _shape(x)
+    if not 0 <= lo <= hi <= V:
+        raise ValueError("shard outside the row")
+    out = np.empty((N, 4))
+    (lib or _load()).vpo_shard_stats(_p(x), N, V, int(lo), int(hi), _p(out))
+    return out
+
+
+def shard_kl_stats(a, b, lo, hi, direction=REVERSE, lib=None):
+    """Per-row KL(P||Q) records of the shard [lo, hi): m_P, S_P, m_Q, S_Q, W, bad, mismatch."""
+    a, b = _f64(a), _f64(b)
+    N, V = _shape(a)
+    if not 0 <= lo <= hi <= V:
+        raise ValueError("shard outside the row")
+    out = np.empty((N, 7))
+    (lib or _load()).vpo_shard_kl_stats(_p(a), _p(b), N, V, int(direction), int(lo), int(hi), _p(out))
+    return out
 
 
 def linear_logits(h, W, lib=None):

@@ -360,6 +360,34 @@ void vpo_kl_sharded(const double *a, const double *b, int64_t N, int64_t V, int 
     }
 }
 
+/* Per-shard records of the sharded forms: the max, sum-exp and centred     */
+/* weighted sum that each vocabulary shard reduces on its own before the    */
+/* merge above ([P1] second commit message). Exposed so that per-shard      */
+/* records computed elsewhere can be checked against their definition.      */
+/* Entropy / logprobs: out[4r + 0..3] = m, S, W, bad.                       */
+void vpo_shard_stats(const double *x, int64_t N, int64_t V, int64_t lo, int64_t hi, double *out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        shard_ent s = shard_entropy(x + r * V, lo, hi);
+        double *o = out + 4 * r;
+        o[0] = s.m; o[1] = s.S; o[2] = s.W; o[3] = s.bad;
+    }
+}
+
+/* KL(P||Q), direction as in vpo_kl_fwd (R1): out[7r + 0..6] = m_P, S_P,    */
+/* m_Q, S_Q, W, bad, mismatch. W is left 0 on a bad or mismatched shard.    */
+void vpo_shard_kl_stats(const double *a, const double *b, int64_t N, int64_t V, int direction,
+                        int64_t lo, int64_t hi, double *out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        const double *P = (direction == 0 ? a : b) + r * V;
+        const double *Q = (direction == 0 ? b : a) + r * V;
+        shard_kl s = shard_kl_stats(P, Q, lo, hi);
+        double *o = out + 7 * r;
+        o[0] = s.mp; o[1] = s.Sp; o[2] = s.mq; o[3] = s.Sq; o[4] = s.W; o[5] = s.bad; o[6] = s.flag;
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Fused linear logp [P2 "Implementation"; review nitpick on the backward]   */
 /* logits_rj = sum_k h_rk W_jk in fp64, never rounded.                       */

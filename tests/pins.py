@@ -18,6 +18,8 @@ build) and raises AssertionError when the oracle disagrees with:
 * fp64 central differences on V = 64 rows;
 * the re-centring merge over 2, 3 and 7 host shards, with empty and all -inf
   shards, equal to the direct form;
+* the per-shard records (max, sum-exp, centred weighted sum, flags) against
+  Decimal sums over each shard;
 * hand-built rows for every NaN / inf precedence rule and target rule.
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in copies of the
@@ -337,6 +339,66 @@ def pin_shard_merge(lib=None):
                    1e-12, 1e-12, f"KL merge k={k} dir {d}")
 
 
+def pin_shard_records(lib=None):
+    """Per-shard records (m, S, W, flags) against Decimal sums over the shard."""
+    V = 13
+    rng = np.random.default_rng(51)
+    a, b = rng.normal(0, 3, (4, V)), rng.normal(0, 3, (4, V))
+    a[1, 0:4] = -INF      # an all -inf shard [0, 4) in row 1
+    b[2, 6] = -INF        # B masked where A is finite: a mismatch for KL(A||B)
+    a[3, 9] = NAN         # a NaN in row 3
+
+    def dsum(z, m, w=None):
+        with localcontext() as ctx:
+            ctx.prec = 60
+            e = [Decimal(0) if v == -INF else (Decimal(v) - Decimal(m)).exp() for v in z]
+            S = sum(e, Decimal(0))
+            if w is None:
+                return float(S), None
+            W = sum((ei * wi for ei, wi in zip(e, w) if ei > 0), Decimal(0))
+            return float(S), float(W)
+
+    for lo, hi in ((0, 4), (4, 11), (11, 13), (0, 13)):
+        got = oracle.shard_stats(a, lo, hi, lib=lib)
+        for r in range(a.shape[0]):
+            z = [float(v) for v in a[r, lo:hi]]
+            bad = any(math.isnan(v) or v == INF for v in z)
+            assert got[r, 3] == bad, f"shard [{lo},{hi}) row {r} bad flag"
+            if bad:
+                continue
+            m = max(z)
+            assert got[r, 0] == m, f"shard [{lo},{hi}) row {r} max"
+            if m == -INF:
+                assert got[r, 1] == 0 and got[r, 2] == 0, "all -inf shard has S = W = 0"
+                continue
+            S, W = dsum(z, m, [Decimal(v) - Decimal(m) if v != -INF else 0 for v in z])
+            _close(got[r, 1], S, 0, 1e-14, f"shard [{lo},{hi}) row {r} S")
+            _close(got[r, 2], W, 1e-14, 1e-13, f"shard [{lo},{hi}) row {r} W")
+        for d in (oracle.REVERSE, oracle.FORWARD):
+            got = oracle.shard_kl_stats(a, b, lo, hi, d, lib=lib)
+            P, Q = (a, b) if d == oracle.REVERSE else (b, a)
+            for r in range(a.shape[0]):
+                p = [float(v) for v in P[r, lo:hi]]
+                q = [float(v) for v in Q[r, lo:hi]]
+                bad = any(math.isnan(v) or v == INF for v in p + q)
+                flag = any(pj > -INF and qj == -INF for pj, qj in zip(p, q))
+                what = f"KL dir {d} shard [{lo},{hi}) row {r}"
+                assert got[r, 5] == bad and got[r, 6] == flag, what + " flags"
+                if bad:
+                    continue
+                mp, mq = max(p), max(q)
+                assert got[r, 0] == mp and got[r, 2] == mq, what + " maxima"
+                if mp > -INF:
+                    w = None if flag else [(Decimal(pj) - Decimal(mp)) - (Decimal(qj) - Decimal(mq))
+                                           if pj != -INF else 0 for pj, qj in zip(p, q)]
+                    Sp, W = dsum(p, mp, w)
+                    _close(got[r, 1], Sp, 0, 1e-14, what + " S_P")
+                    if W is not None:
+                        _close(got[r, 4], W, 1e-14, 1e-13, what + " W")
+                if mq > -INF:
+                    _close(got[r, 3], dsum(q, mq)[0], 0, 1e-14, what + " S_Q")
+
+
 # ----------------------------------------------------------------------------
 # NaN / inf precedence and target rules (readings R2-R5 of the oracle header)
 # ----------------------------------------------------------------------------
@@ -462,6 +524,7 @@ ALL_PINS = [
     pin_shift_invariance,
     pin_finite_differences,
     pin_shard_merge,
+    pin_shard_records,
     pin_special_rows,
     pin_linear_logp_brute_force,
     pin_linear_logp_finite_differences,

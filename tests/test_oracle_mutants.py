@@ -48,6 +48,11 @@ MUTANTS = [
     ("merge zero-weight skip dropped", "if (w == 0.0) continue;                  /* zero-weight shard skipped */", ""),
     ("KL merge shift sign", "W += ap * (parts[s].W - (dp - dq) * parts[s].Sp);",
      "W += ap * (parts[s].W - (dp + dq) * parts[s].Sp);"),
+    ("shard record W column", "o[0] = s.m; o[1] = s.S; o[2] = s.W; o[3] = s.bad;",
+     "o[0] = s.m; o[1] = s.S; o[2] = s.S; o[3] = s.bad;"),
+    ("shard KL record Q max", "o[2] = s.mq; o[3] = s.Sq;", "o[2] = s.mp; o[3] = s.Sq;"),
+    ("shard KL record direction", "const double *P = (direction == 0 ? a : b) + r * V;\n        const double *Q = (direction == 0 ? b : a) + r * V;\n        shard_kl s",
+     "const double *P = (direction == 1 ? a : b) + r * V;\n        const double *Q = (direction == 1 ? b : a) + r * V;\n        shard_kl s"),
     ("linear logits transposed", "acc += h[r * D + k] * W[j * D + k];", "acc += h[r * D + k] * W[k * V + j];"),
     ("linear dW wrong row", "out[k] += c * h[r * D + k];", "out[k] += c * h[((r + 1) % N) * D + k];"),
     ("linear dh wrong vocab row", "out[k] += c * W[j * D + k];", "out[k] += c * W[((j + 1) % V) * D + k];"),
