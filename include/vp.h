@@ -120,6 +120,10 @@ typedef enum vp_kl_direction { VP_KL_REVERSE = 0, VP_KL_FORWARD = 1 } vp_kl_dire
 #define VP_ROW_NANINF   1u  /* the row holds a NaN or a +inf                          */
 #define VP_ROW_EMPTY    2u  /* no finite logit (all -inf): S = 0                      */
 #define VP_ROW_MISMATCH 4u  /* KL(P||Q) record of P: some P_j > -inf has Q_j = -inf  */
+#define VP_ROW_SHARDED  8u  /* written by vp_logprobs_merge: the target was checked
+                               across all shards (see the sharded forms below)   */
+#define VP_ROW_BADTARGET 16u /* written by vp_logprobs_merge: no shard, or more
+                               than one, holds the row's target >= 0           */
 
 /* Per-row statistics saved by a forward call for its backward call.
  * m      the exact row max; -FLT_MAX when the row has no finite logit.
@@ -154,7 +158,9 @@ VP_API vp_status vp_logprobs_fwd(const void *x, int dtype, int64_t N, int64_t V,
 
 /* dx[r, j] = g[r] (onehot_{j,t} - p_{r,j}), p = exp((z - m) - logS), using
  * the stats of vp_logprobs_fwd [P2, review nitpick on the chunked backward].
- * grad_out: fp32 [N]. dx: contiguous [N, V], dtype of x. */
+ * grad_out: fp32 [N]. dx: contiguous [N, V], dtype of x. With the records of
+ * vp_logprobs_merge (VP_ROW_SHARDED), x is one vocabulary shard starting at
+ * vocab_start: a target outside it only drops the onehot term. */
 VP_API vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R,
                                  int64_t s_o, int64_t s_i, int64_t vocab_start,
                                  const int64_t *targets, const vp_rowstat *stats,
@@ -200,6 +206,94 @@ VP_API vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, i
                            int64_t s_o, int64_t s_i, int direction, const vp_rowstat *stats_a,
                            const vp_rowstat *stats_b, const float *grad_out, void *da, void *db,
                            vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Vocabulary-sharded (tensor-parallel) forms [P1, second commit message and */
+/* the reviewer's suggested change: each rank reduces its own shard's max,   */
+/* sum-exp and centred weighted sum, and the shards are combined by          */
+/* re-centring on the row max; the pages do this with a MAX then a SUM       */
+/* all-reduce]. Here one gather of fixed-size records replaces both.         */
+/*                                                                           */
+/* Flow for K shards of the vocabulary, shard k holding columns              */
+/* [vocab_start_k, vocab_start_k + V_k) of every row (typically one shard    */
+/* per GPU):                                                                 */
+/*  1. each shard calls vp_*_partial on its logits: one vp_partial per row;  */
+/*  2. the caller gathers the K arrays into one array of K * N records,      */
+/*     shard-major (row r of shard k at index k * N + r), e.g. with an       */
+/*     all-gather; the library itself makes no collective call;              */
+/*  3. vp_*_merge turns the gathered records into the outputs and vp_rowstat */
+/*     records that the unsharded forward would write for the whole rows;    */
+/*  4. each shard calls the ordinary backward (vp_logprobs_bwd with its own  */
+/*     vocab_start, vp_entropy_bwd, vp_kl_bwd) on its own logits with the    */
+/*     merged records and gets its columns of the gradient.                  */
+/* The merge reads a row's K records in shard order, so its result does not  */
+/* depend on N or on the other rows.                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Flags of vp_partial. */
+#define VP_PART_NANINF     1u  /* A (P for KL) holds a NaN or +inf in this shard   */
+#define VP_PART_NANINF_B   2u  /* KL: Q holds a NaN or +inf in this shard          */
+#define VP_PART_MISMATCH   4u  /* KL: some P_j > -inf has Q_j = -inf in the shard  */
+#define VP_PART_HAS_TARGET 8u  /* logprobs: the row's target lies in this shard    */
+#define VP_PART_IGNORED   16u  /* logprobs: the row's target is negative (ignored) */
+
+/* One row's statistics over one shard; 40 bytes, 8-byte aligned.
+ * m     the exact max over the shard of A (of P for KL); -FLT_MAX when the
+ *       shard has no finite logit (S is then 0).
+ * S     sum over the shard of exp(z_j - m), fp64.
+ * W     entropy: sum over the shard of exp(z_j - m) (z_j - m);
+ *       KL(P||Q): sum of exp(P_j - m) ((P_j - m) - (Q_j - m_b)) over the terms
+ *       with exp(P_j - m) > 0, meaningful only when no flag is set;
+ *       logprobs: 0.
+ * m_b, S_b  KL only: the max and sum-exp of Q over the shard (else 0).
+ * z_t   logprobs only: the target's logit when VP_PART_HAS_TARGET (else 0).
+ * flags VP_PART_* bits. */
+typedef struct vp_partial {
+    float m, m_b;
+    double S, S_b, W;
+    float z_t;
+    uint32_t flags;
+} vp_partial;
+
+/* Partial records of logprobs over the shard held by x (V columns starting
+ * at global id vocab_start). targets are global ids: one inside the shard
+ * sets VP_PART_HAS_TARGET and z_t, a negative one VP_PART_IGNORED, one in
+ * another shard neither (not an error here). parts: vp_partial [N], 8-byte
+ * aligned. */
+VP_API vp_status vp_logprobs_partial(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                                     int64_t s_i, int64_t vocab_start, const int64_t *targets,
+                                     vp_partial *parts, vp_stream stream);
+
+/* Partial records of entropy over the shard held by x. */
+VP_API vp_status vp_entropy_partial(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                                    int64_t s_i, vp_partial *parts, vp_stream stream);
+
+/* Partial records of KL(P||Q) over the shard held by a and b, with (P, Q) =
+ * (A, B) for VP_KL_REVERSE and (B, A) for VP_KL_FORWARD. */
+VP_API vp_status vp_kl_partial(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R,
+                               int64_t s_o, int64_t s_i, int direction, vp_partial *parts, vp_stream stream);
+
+/* Merges K >= 1 shards' records (K * N, shard-major) into logp (fp32 [N]) and
+ * stats (vp_rowstat [N]) as vp_logprobs_fwd would write them for the whole
+ * rows. A row whose target is ignored gets logp 0. A row whose target is
+ * >= 0 but held by no shard or by several is a data error: logp NaN,
+ * VP_ERRBIT_TARGET in *err_word (may be NULL) and VP_ROW_BADTARGET in its
+ * record. Every record gets VP_ROW_SHARDED, which tells vp_logprobs_bwd that a
+ * target outside the calling shard is valid (its onehot term lies in another
+ * shard) and that VP_ROW_BADTARGET rows have NaN gradient rows. */
+VP_API vp_status vp_logprobs_merge(const vp_partial *parts, int64_t K, int64_t N, float *logp,
+                                   vp_rowstat *stats, int32_t *err_word, vp_stream stream);
+
+/* Merges K shards' entropy records into H (fp32 [N]) and stats, as
+ * vp_entropy_fwd would write them for the whole rows. */
+VP_API vp_status vp_entropy_merge(const vp_partial *parts, int64_t K, int64_t N, float *H, vp_rowstat *stats,
+                                  vp_stream stream);
+
+/* Merges K shards' KL records into kl (fp32 [N]) and the records of A and of
+ * B, as vp_kl_fwd would write them; direction must be the one given to
+ * vp_kl_partial. */
+VP_API vp_status vp_kl_merge(const vp_partial *parts, int64_t K, int64_t N, int direction, float *kl,
+                             vp_rowstat *stats_a, vp_rowstat *stats_b, vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Fused linear logp [P2, "Implementation"]                                  */

@@ -61,6 +61,8 @@ _SIGS = {
     "vpo_kl_sharded": (["P", "P", "I", "I", "i", "P", "i", "P"], None),
     "vpo_shard_stats": (["P", "I", "I", "I", "I", "P"], None),
     "vpo_shard_kl_stats": (["P", "P", "I", "I", "i", "I", "I", "P"], None),
+    "vpo_merge_entropy_records": (["P", "I", "I", "P"], None),
+    "vpo_merge_kl_records": (["P", "I", "I", "P"], None),
     "vpo_linear_logits": (["P", "P", "I", "I", "I", "P"], None),
     "vpo_linear_logp_fwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P", "P"], None),
     "vpo_linear_logp_bwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P"], None),
@@ -212,6 +214,28 @@ def shard_kl_stats(a, b, lo, hi, direction=REVERSE, lib=None):
     out = np.empty((N, 7))
     (lib or _load()).vpo_shard_kl_stats(_p(a), _p(b), N, V, int(direction), int(lo), int(hi), _p(out))
     return out
+
+
+def merge_entropy_records(recs, lib=None):
+    """Entropy per row from gathered shard records [K, N, 4] (as shard_stats returns them)."""
+    recs = _f64(recs)
+    if recs.ndim != 3 or recs.shape[2] != 4 or not 1 <= recs.shape[0] <= 64:
+        raise ValueError("records must be [K <= 64, N, 4]")
+    K, N = recs.shape[:2]
+    H = np.empty(N)
+    (lib or _load()).vpo_merge_entropy_records(_p(recs), K, N, _p(H))
+    return H
+
+
+def merge_kl_records(recs, lib=None):
+    """KL per row from gathered shard records [K, N, 7] (as shard_kl_stats returns them)."""
+    recs = _f64(recs)
+    if recs.ndim != 3 or recs.shape[2] != 7 or not 1 <= recs.shape[0] <= 64:
+        raise ValueError("records must be [K <= 64, N, 7]")
+    K, N = recs.shape[:2]
+    kl = np.empty(N)
+    (lib or _load()).vpo_merge_kl_records(_p(recs), K, N, _p(kl))
+    return kl
 
 
 def linear_logits(h, W, lib=None):

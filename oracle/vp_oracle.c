@@ -284,28 +284,47 @@ static shard_ent shard_entropy(const double *z, int64_t lo, int64_t hi) {
     return s;
 }
 
+/* Entropy of a row from its k shard records: re-centre on the row max. */
+static double merge_entropy(const shard_ent *parts, int k) {
+    double m = -INFINITY;
+    int bad = 0;
+    for (int s = 0; s < k; ++s) {
+        bad |= parts[s].bad;
+        if (parts[s].m > m) m = parts[s].m;
+    }
+    double S = 0.0, W = 0.0;
+    for (int s = 0; s < k; ++s) {
+        double alpha = exp(parts[s].m - m);     /* 0 for an empty / all -inf shard */
+        double w = alpha * parts[s].S;
+        if (w == 0.0) continue;                  /* zero-weight shard skipped */
+        S += w;
+        W += alpha * (parts[s].W - (m - parts[s].m) * parts[s].S);
+    }
+    return (bad || S == 0.0) ? NAN : log(S) - W / S;
+}
+
 void vpo_entropy_sharded(const double *x, int64_t N, int64_t V, const int64_t *cuts,
                          int k, double *H) {
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < N; ++r) {
         const double *z = x + r * V;
         shard_ent parts[64];
-        double m = -INFINITY;
-        int bad = 0;
-        for (int s = 0; s < k; ++s) {
-            parts[s] = shard_entropy(z, cuts[s], cuts[s + 1]);
-            bad |= parts[s].bad;
-            if (parts[s].m > m) m = parts[s].m;
+        for (int s = 0; s < k; ++s) parts[s] = shard_entropy(z, cuts[s], cuts[s + 1]);
+        H[r] = merge_entropy(parts, k);
+    }
+}
+
+/* Entropy from records laid out as vpo_shard_stats writes them, K x N x 4,
+ * shard-major (K <= 64). */
+void vpo_merge_entropy_records(const double *recs, int64_t K, int64_t N, double *H) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        shard_ent parts[64];
+        for (int64_t s = 0; s < K; ++s) {
+            const double *o = recs + 4 * (s * N + r);
+            parts[s].m = o[0]; parts[s].S = o[1]; parts[s].W = o[2]; parts[s].bad = o[3] != 0.0;
         }
-        double S = 0.0, W = 0.0;
-        for (int s = 0; s < k; ++s) {
-            double alpha = exp(parts[s].m - m);     /* 0 for an empty / all -inf shard */
-            double w = alpha * parts[s].S;
-            if (w == 0.0) continue;                  /* zero-weight shard skipped */
-            S += w;
-            W += alpha * (parts[s].W - (m - parts[s].m) * parts[s].S);
-        }
-        H[r] = (bad || S == 0.0) ? NAN : log(S) - W / S;
+        H[r] = merge_entropy(parts, (int)K);
     }
 }
 
@@ -327,6 +346,31 @@ static shard_kl shard_kl_stats(const double *P, const double *Q, int64_t lo, int
     return s;
 }
 
+/* KL of a row from its k shard records: re-centre P and Q on their row maxima. */
+static double merge_kl(const shard_kl *parts, int k) {
+    double mp = -INFINITY, mq = -INFINITY;
+    int bad = 0, flag = 0;
+    for (int s = 0; s < k; ++s) {
+        bad |= parts[s].bad;
+        flag |= parts[s].flag;
+        if (parts[s].mp > mp) mp = parts[s].mp;
+        if (parts[s].mq > mq) mq = parts[s].mq;
+    }
+    double Sp = 0.0, Sq = 0.0, W = 0.0;
+    for (int s = 0; s < k; ++s) {
+        double ap = exp(parts[s].mp - mp), aq = exp(parts[s].mq - mq);
+        if (aq * parts[s].Sq != 0.0) Sq += aq * parts[s].Sq;
+        double w = ap * parts[s].Sp;
+        if (w == 0.0) continue;
+        Sp += w;
+        double dp = mp - parts[s].mp, dq = mq - parts[s].mq;
+        W += ap * (parts[s].W - (dp - dq) * parts[s].Sp);
+    }
+    if (bad || Sp == 0.0) return NAN;
+    if (flag) return INFINITY;
+    return W / Sp - log(Sp) + log(Sq);
+}
+
 /* Same direction convention as vpo_kl_fwd (R1). */
 void vpo_kl_sharded(const double *a, const double *b, int64_t N, int64_t V, int direction,
                     const int64_t *cuts, int k, double *kl) {
@@ -335,28 +379,23 @@ void vpo_kl_sharded(const double *a, const double *b, int64_t N, int64_t V, int 
         const double *P = (direction == 0 ? a : b) + r * V;
         const double *Q = (direction == 0 ? b : a) + r * V;
         shard_kl parts[64];
-        double mp = -INFINITY, mq = -INFINITY;
-        int bad = 0, flag = 0;
-        for (int s = 0; s < k; ++s) {
-            parts[s] = shard_kl_stats(P, Q, cuts[s], cuts[s + 1]);
-            bad |= parts[s].bad;
-            flag |= parts[s].flag;
-            if (parts[s].mp > mp) mp = parts[s].mp;
-            if (parts[s].mq > mq) mq = parts[s].mq;
+        for (int s = 0; s < k; ++s) parts[s] = shard_kl_stats(P, Q, cuts[s], cuts[s + 1]);
+        kl[r] = merge_kl(parts, k);
+    }
+}
+
+/* KL from records laid out as vpo_shard_kl_stats writes them, K x N x 7,
+ * shard-major (K <= 64). */
+void vpo_merge_kl_records(const double *recs, int64_t K, int64_t N, double *kl) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        shard_kl parts[64];
+        for (int64_t s = 0; s < K; ++s) {
+            const double *o = recs + 7 * (s * N + r);
+            parts[s].mp = o[0]; parts[s].Sp = o[1]; parts[s].mq = o[2]; parts[s].Sq = o[3];
+            parts[s].W = o[4]; parts[s].bad = o[5] != 0.0; parts[s].flag = o[6] != 0.0;
         }
-        double Sp = 0.0, Sq = 0.0, W = 0.0;
-        for (int s = 0; s < k; ++s) {
-            double ap = exp(parts[s].mp - mp), aq = exp(parts[s].mq - mq);
-            if (aq * parts[s].Sq != 0.0) Sq += aq * parts[s].Sq;
-            double w = ap * parts[s].Sp;
-            if (w == 0.0) continue;
-            Sp += w;
-            double dp = mp - parts[s].mp, dq = mq - parts[s].mq;
-            W += ap * (parts[s].W - (dp - dq) * parts[s].Sp);
-        }
-        if (bad || Sp == 0.0) kl[r] = NAN;
-        else if (flag) kl[r] = INFINITY;
-        else kl[r] = W / Sp - log(Sp) + log(Sq);
+        kl[r] = merge_kl(parts, (int)K);
     }
 }
 

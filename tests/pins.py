@@ -334,9 +334,15 @@ def pin_shard_merge(lib=None):
             cuts = np.array([0, 100, V])  # row 0: first shard all -inf
         _close(oracle.entropy_sharded(a, cuts, lib=lib), oracle.entropy_fwd(a, lib=lib)[0],
                1e-13, 1e-13, f"entropy merge k={k}")
+        recs = np.stack([oracle.shard_stats(a, cuts[s], cuts[s + 1], lib=lib) for s in range(k)])
+        _close(oracle.merge_entropy_records(recs, lib=lib), oracle.entropy_fwd(a, lib=lib)[0],
+               1e-13, 1e-13, f"entropy merge of gathered records k={k}")
         for d in (oracle.REVERSE, oracle.FORWARD):
             _close(oracle.kl_sharded(a, b, cuts, d, lib=lib), oracle.kl_fwd(a, b, d, lib=lib)[0],
                    1e-12, 1e-12, f"KL merge k={k} dir {d}")
+            recs = np.stack([oracle.shard_kl_stats(a, b, cuts[s], cuts[s + 1], d, lib=lib) for s in range(k)])
+            _close(oracle.merge_kl_records(recs, lib=lib), oracle.kl_fwd(a, b, d, lib=lib)[0],
+                   1e-12, 1e-12, f"KL merge of gathered records k={k} dir {d}")
 
 
 def pin_shard_records(lib=None):

@@ -94,3 +94,22 @@ def test_binding_rejects_bad_layouts_before_calling():
         rows_of(x.transpose(1, 2))
     with pytest.raises(VPError):
         rows_of(torch.zeros(3))
+
+
+def test_sharded_entry_points_check_arguments_on_the_host():
+    lib = _lib.lib()
+    # merges: K >= 1, parts non-NULL and 8-byte aligned, a valid direction
+    assert lib.vp_entropy_merge(FAKE, 0, 4, FAKE, FAKE, None) == ERR_SHAPE
+    assert lib.vp_entropy_merge(None, 2, 4, FAKE, FAKE, None) == ERR_NULL
+    assert lib.vp_entropy_merge(FAKE_ODD, 2, 4, FAKE, FAKE, None) == ERR_ALIGN
+    assert lib.vp_entropy_merge(None, 2, 0, None, None, None) == OK          # N = 0 queues nothing
+    assert lib.vp_logprobs_merge(FAKE, 2, 4, None, FAKE, None, None) == ERR_NULL
+    assert lib.vp_kl_merge(FAKE, 2, 4, 5, FAKE, FAKE, FAKE, None) == ERR_ARG
+    assert lib.vp_kl_merge(FAKE, 2, 4, 0, FAKE, FAKE_ODD, FAKE, None) == ERR_ALIGN
+    # partials: the same row checks as the forward calls
+    assert lib.vp_entropy_partial(FAKE, 9, 4, 16, 4, 0, 16, FAKE, None) == ERR_DTYPE
+    assert lib.vp_entropy_partial(FAKE, 1, 4, 0, 4, 0, 16, FAKE, None) == ERR_SHAPE
+    assert lib.vp_logprobs_partial(FAKE, 1, 4, 16, 4, 0, 16, 0, None, FAKE, None) == ERR_NULL
+    assert lib.vp_logprobs_partial(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE, FAKE_ODD, None) == ERR_ALIGN
+    assert lib.vp_kl_partial(FAKE, FAKE, 1, 4, 16, 4, 0, 16, 3, FAKE, None) == ERR_ARG
+    assert lib.vp_kl_partial(FAKE, FAKE, 1, 4, 16, 4, -1, 16, 0, FAKE, None) == ERR_LAYOUT

@@ -24,8 +24,10 @@ from . import _lib
 F32, BF16 = 0, 1
 KL_REVERSE, KL_FORWARD = 0, 1
 ERRBIT_TARGET = 1
-ROW_NANINF, ROW_EMPTY, ROW_MISMATCH = 1, 2, 4
+ROW_NANINF, ROW_EMPTY, ROW_MISMATCH, ROW_SHARDED, ROW_BADTARGET = 1, 2, 4, 8, 16
 ROWSTAT_FLOATS = 8  # sizeof(vp_rowstat) / 4
+PART_NANINF, PART_NANINF_B, PART_MISMATCH, PART_HAS_TARGET, PART_IGNORED = 1, 2, 4, 8, 16
+PARTIAL_DOUBLES = 5  # sizeof(vp_partial) / 8
 
 
 def rowstats(N: int, device) -> torch.Tensor:
@@ -44,6 +46,20 @@ class VPError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {_lib.status_string(status)} (status {status})")
+
+
+def partials(N: int, device, K: int = None) -> torch.Tensor:
+    """Storage for vp_partial records: float64 [N, 5] (40 bytes per row), or [K, N, 5] for K shards."""
+    shape = (N, PARTIAL_DOUBLES) if K is None else (K, N, PARTIAL_DOUBLES)
+    return torch.empty(shape, dtype=torch.float64, device=device)
+
+
+def decode_partials(parts: torch.Tensor) -> dict:
+    """Fields of vp_partial records ([..., 5] float64) as tensors: m, m_b, S, S_b, W, z_t, flags."""
+    p = parts.detach()
+    f = p.view(torch.float32)
+    return {"m": f[..., 0], "m_b": f[..., 1], "S": p[..., 1], "S_b": p[..., 2], "W": p[..., 3], "z_t": f[..., 8],
+            "flags": p.view(torch.int32)[..., 9]}
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -209,6 +225,91 @@ def vp_linear_logp_bwd(hidden, weight, targets, stats, grad, vocab_start: int = 
                                          workspace.numel() * workspace.element_size(), _ptr(err_word), _stream()),
            "vp_linear_logp_bwd")
     return dhidden, dW
+
+
+def vp_linear_logp_fwd_noalloc(hidden, weight, targets, vocab_start: int = 0, err_word=None, logp=None,
+                               stats=None):
+    """vp_linear_logp_fwd with the library's fixed internal scratch instead of a workspace."""
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise VPError(3, "vp_linear_logp_fwd_noalloc takes bf16 hidden and weight")
+    if not (hidden.is_contiguous() and weight.is_contiguous()) or hidden.dim() != 2 or weight.dim() != 2:
+        raise VPError(4, "hidden and weight must be contiguous 2-D tensors")
+    N, D = hidden.shape
+    V = weight.shape[0]
+    logp = _f32(N, hidden) if logp is None else logp
+    stats = rowstats(N, hidden.device) if stats is None else stats
+    _check(_lib.lib().vp_linear_logp_fwd_noalloc(_ptr(hidden), _ptr(weight), N, V, D, vocab_start, _ptr(targets),
+                                                 _ptr(logp), _ptr(stats), _ptr(err_word), _stream()),
+           "vp_linear_logp_fwd_noalloc")
+    return logp, stats
+
+
+# ---------------------------------------------------------------------------
+# Vocabulary-sharded forms: per-shard records, gathered by the caller, merged
+# ---------------------------------------------------------------------------
+def vp_logprobs_partial(x, targets, vocab_start: int = 0, parts=None):
+    """Per-row records of logprobs over the shard x (columns vocab_start .. vocab_start + V)."""
+    N, V, R, s_o, s_i = rows_of(x)
+    parts = partials(N, x.device) if parts is None else parts
+    _check(_lib.lib().vp_logprobs_partial(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
+                                          _ptr(parts), _stream()), "vp_logprobs_partial")
+    return parts
+
+
+def vp_entropy_partial(x, parts=None):
+    """Per-row records of entropy over the shard x."""
+    N, V, R, s_o, s_i = rows_of(x)
+    parts = partials(N, x.device) if parts is None else parts
+    _check(_lib.lib().vp_entropy_partial(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(parts), _stream()),
+           "vp_entropy_partial")
+    return parts
+
+
+def vp_kl_partial(a, b, direction: int = KL_REVERSE, parts=None):
+    """Per-row records of KL over the shard held by a and b."""
+    _same_layout(a, b)
+    N, V, R, s_o, s_i = rows_of(a)
+    parts = partials(N, a.device) if parts is None else parts
+    _check(_lib.lib().vp_kl_partial(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction),
+                                    _ptr(parts), _stream()), "vp_kl_partial")
+    return parts
+
+
+def _gathered(parts):
+    if parts.dim() != 3 or parts.shape[2] != PARTIAL_DOUBLES or parts.dtype != torch.float64 \
+            or not parts.is_contiguous():
+        raise VPError(2, "gathered records must be a contiguous float64 [K, N, 5] tensor")
+    return parts.shape[0], parts.shape[1]
+
+
+def vp_logprobs_merge(parts, err_word=None, logp=None, stats=None):
+    """Merges [K, N] shard records (shard-major) into (logp fp32 [N], stats) for the whole rows."""
+    K, N = _gathered(parts)
+    logp = _f32(N, parts) if logp is None else logp
+    stats = rowstats(N, parts.device) if stats is None else stats
+    _check(_lib.lib().vp_logprobs_merge(_ptr(parts), K, N, _ptr(logp), _ptr(stats), _ptr(err_word), _stream()),
+           "vp_logprobs_merge")
+    return logp, stats
+
+
+def vp_entropy_merge(parts, H=None, stats=None):
+    """Merges [K, N] shard records into (H fp32 [N], stats)."""
+    K, N = _gathered(parts)
+    H = _f32(N, parts) if H is None else H
+    stats = rowstats(N, parts.device) if stats is None else stats
+    _check(_lib.lib().vp_entropy_merge(_ptr(parts), K, N, _ptr(H), _ptr(stats), _stream()), "vp_entropy_merge")
+    return H, stats
+
+
+def vp_kl_merge(parts, direction: int = KL_REVERSE, kl=None, stats_a=None, stats_b=None):
+    """Merges [K, N] shard records into (kl fp32 [N], stats of A, stats of B)."""
+    K, N = _gathered(parts)
+    kl = _f32(N, parts) if kl is None else kl
+    stats_a = rowstats(N, parts.device) if stats_a is None else stats_a
+    stats_b = rowstats(N, parts.device) if stats_b is None else stats_b
+    _check(_lib.lib().vp_kl_merge(_ptr(parts), K, N, int(direction), _ptr(kl), _ptr(stats_a), _ptr(stats_b),
+                                  _stream()), "vp_kl_merge")
+    return kl, stats_a, stats_b
 
 
 def vp_fault_status(clear: bool = False) -> int:

@@ -13,6 +13,7 @@
 #include "vp_launch.h"
 
 static_assert(sizeof(vp_rowstat) == 32, "vp_rowstat is 32 bytes");
+static_assert(sizeof(vp_partial) == 40, "vp_partial is 40 bytes");
 
 namespace {
 
@@ -132,6 +133,99 @@ vp_status vp_kl_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t 
                     rev ? (void *)stats_a : (void *)stats_b, rev ? (void *)stats_b : (void *)stats_a,
                     (cudaStream_t)stream};
     return launched(vp::launch_kl_fwd(k));
+}
+
+// ---------------------------------------------------------------------------
+// Vocabulary-sharded forms
+// ---------------------------------------------------------------------------
+vp_status vp_logprobs_partial(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
+                              int64_t vocab_start, const int64_t *targets, vp_partial *parts, vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!x || !targets || !parts) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(targets, 8) || !aligned(parts, 8)) return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, targets, nullptr, nullptr, nullptr,
+                    (cudaStream_t)stream, parts};
+    return launched(vp::launch_logprobs_fwd(a));
+}
+
+vp_status vp_entropy_partial(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
+                             vp_partial *parts, vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!x || !parts) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(parts, 8)) return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, 0, nullptr, nullptr, nullptr, nullptr,
+                    (cudaStream_t)stream, parts};
+    return launched(vp::launch_entropy_fwd(a));
+}
+
+vp_status vp_kl_partial(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                        int64_t s_i, int direction, vp_partial *parts, vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!a || !b || !parts) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(parts, 8)) return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    const bool rev = direction == VP_KL_REVERSE;  // reverse: P = A, Q = B
+    vp::KLFwdArgs k{rev ? a : b, rev ? b : a, dtype == VP_BF16, N, V, R, s_o, s_i, nullptr, nullptr, nullptr,
+                    (cudaStream_t)stream, parts};
+    return launched(vp::launch_kl_fwd(k));
+}
+
+namespace {
+vp_status check_merge(const vp_partial *parts, int64_t K, int64_t N) {
+    if (K < 1 || N < 0 || N > kMaxRowsPerLaunch || K > kMaxRowsPerLaunch / (N > 0 ? N : 1)) return VP_ERR_SHAPE;
+    if (N > 0 && !parts) return VP_ERR_NULL;
+    if (!aligned(parts, 8)) return VP_ERR_ALIGN;
+    return VP_OK;
+}
+}  // namespace
+
+vp_status vp_logprobs_merge(const vp_partial *parts, int64_t K, int64_t N, float *logp, vp_rowstat *stats,
+                            int32_t *err_word, vp_stream stream) {
+    vp_status st = check_merge(parts, K, N);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!logp || !stats) return VP_ERR_NULL;
+    if (!aligned(logp, 4) || !aligned(stats, 16) || !aligned(err_word, 4)) return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::MergeArgs a{parts, K, N, logp, stats, nullptr, err_word, (cudaStream_t)stream};
+    return launched(vp::launch_logprobs_merge(a));
+}
+
+vp_status vp_entropy_merge(const vp_partial *parts, int64_t K, int64_t N, float *H, vp_rowstat *stats,
+                           vp_stream stream) {
+    vp_status st = check_merge(parts, K, N);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!H || !stats) return VP_ERR_NULL;
+    if (!aligned(H, 4) || !aligned(stats, 16)) return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::MergeArgs a{parts, K, N, H, stats, nullptr, nullptr, (cudaStream_t)stream};
+    return launched(vp::launch_entropy_merge(a));
+}
+
+vp_status vp_kl_merge(const vp_partial *parts, int64_t K, int64_t N, int direction, float *kl,
+                      vp_rowstat *stats_a, vp_rowstat *stats_b, vp_stream stream) {
+    vp_status st = check_merge(parts, K, N);
+    if (st != VP_OK) return st;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!kl || !stats_a || !stats_b) return VP_ERR_NULL;
+    if (!aligned(kl, 4) || !aligned(stats_a, 16) || !aligned(stats_b, 16)) return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    const bool rev = direction == VP_KL_REVERSE;
+    vp::MergeArgs a{parts, K, N, kl, rev ? (void *)stats_a : (void *)stats_b, rev ? (void *)stats_b : (void *)stats_a,
+                    nullptr, (cudaStream_t)stream};
+    return launched(vp::launch_kl_merge(a));
 }
 
 vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,

@@ -132,7 +132,7 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
         const RowStat s = load_rowstat(stats + r);
         const float g = g_in[r];
         int64_t loc = -1;
-        int mode = (s.flags & (kRowNanInf | kRowEmpty)) ? kNaN : kNormal;
+        int mode = (s.flags & (kRowNanInf | kRowEmpty | kRowBadTarget)) ? kNaN : kNormal;
         if (kOp == 0) {
             const int64_t t = targets[r];
             if (t < 0) {
@@ -140,8 +140,12 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
             } else {
                 loc = t - vocab_start;
                 if (loc < 0 || loc >= V) {
-                    mode = kNaN;
-                    if (err && seg == 0 && tid == 0) atomicOr(err, VP_ERRBIT_TARGET_);
+                    if (s.flags & kRowSharded) {
+                        loc = -1;   // merged record: the target lies in another vocabulary shard
+                    } else {
+                        mode = kNaN;
+                        if (err && seg == 0 && tid == 0) atomicOr(err, VP_ERRBIT_TARGET_);
+                    }
                 }
             }
         }

@@ -40,6 +40,18 @@ constexpr int kBwdThreads = 256;
 constexpr int kBwdVecPerThread = 4;
 
 constexpr uint32_t kRowNanInf = 1u, kRowEmpty = 2u, kRowMismatch = 4u;  // = VP_ROW_* of vp.h
+constexpr uint32_t kRowSharded = 8u, kRowBadTarget = 16u;
+// = VP_PART_* of vp.h
+constexpr uint32_t kPartNanInf = 1u, kPartNanInfB = 2u, kPartMismatch = 4u, kPartHasTarget = 8u, kPartIgnored = 16u;
+
+// Layout of vp_partial (40 bytes): one row's statistics over one vocabulary shard.
+struct PartialRec {
+    float m, m_b;
+    double S, S_b, W;
+    float z_t;
+    uint32_t flags;
+};
+static_assert(sizeof(PartialRec) == 40, "vp_partial is 40 bytes");
 
 // Device-side image of vp_rowstat (32 bytes).
 struct RowStat {

@@ -31,7 +31,7 @@ namespace vp {
 template <typename T>
 __global__ void __launch_bounds__(kFwdThreads)
 kl_fwd_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows, float *__restrict__ kl,
-              RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q) {
+              RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q, PartialRec *__restrict__ shard_parts) {
     constexpr int kVec = Elem<T>::kVec;
     constexpr int kRound = 2;
     const int64_t r = blockIdx.x;
@@ -109,7 +109,10 @@ kl_fwd_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows
     __syncthreads();
     if (tid >= 32) return;
     const PartKL<AccT<T>> s = kl_merge_parts(parts, kFwdWarps);
-    if (tid == 0) finish_kl(s, r, kl, stats_p, stats_q);
+    if (tid == 0) {
+        if (shard_parts) finish_partial_kl(s, r, shard_parts);
+        else finish_kl(s, r, kl, stats_p, stats_q);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -119,7 +122,7 @@ template <typename T>
 static cudaError_t launch_kl_t(const KLFwdArgs &a) {
     kl_fwd_kernel<T><<<(unsigned)a.N, kFwdThreads, 0, a.stream>>>(
         static_cast<const T *>(a.p), static_cast<const T *>(a.q), (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.kl,
-        static_cast<RowStat *>(a.stats_p), static_cast<RowStat *>(a.stats_q));
+        static_cast<RowStat *>(a.stats_p), static_cast<RowStat *>(a.stats_q), static_cast<PartialRec *>(a.parts));
     return cudaGetLastError();
 }
 

@@ -32,14 +32,29 @@
 
 namespace vp {
 
-constexpr int kTmaConsumerWarps = 8;
+// Ring geometry (compile-time; the defaults are the measured best on GB300).
+#ifndef VP_FWD_STAGE_BYTES
+#define VP_FWD_STAGE_BYTES 16384
+#endif
+#ifndef VP_FWD_STAGES
+#define VP_FWD_STAGES 6
+#endif
+#ifndef VP_FWD_CTAS_PER_SM
+#define VP_FWD_CTAS_PER_SM 2
+#endif
+#ifndef VP_FWD_CONSUMER_WARPS
+#define VP_FWD_CONSUMER_WARPS 8
+#endif
+constexpr int kTmaConsumerWarps = VP_FWD_CONSUMER_WARPS;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
 constexpr int kProducerWarp = kTmaConsumerWarps;       // warp 8
 constexpr int kFinisherWarp = kTmaConsumerWarps + 1;   // warp 9
 constexpr int kTmaThreads = kTmaConsumers + 64;
-constexpr int kStageBytes = 16384;
-constexpr int kStages = 6;
+constexpr int kStageBytes = VP_FWD_STAGE_BYTES;
+constexpr int kStages = VP_FWD_STAGES;
+constexpr int kCtasPerSm = VP_FWD_CTAS_PER_SM;
 constexpr int kRingBytes = kStages * kStageBytes;
+static_assert(kStageBytes % (2 * 16 * kTmaConsumers) == 0, "a stage splits evenly over the consumers (P and Q halves)");
 
 // Set (OR) when a bounded wait gave up: 1 = producer, 2 = consumer or finisher.
 __device__ uint32_t g_tma_fault;
@@ -102,6 +117,14 @@ __device__ __forceinline__ bool hand_over(Ring &ring, P (*parts)[kTmaConsumerWar
     return __shfl_sync(0xffffffffu, ok, 0);
 }
 
+// A consumer's position in the ring: stage index and the parity of its use.
+struct RingPos {
+    uint32_t st = 0, ph = 0;
+    __device__ __forceinline__ void next() {
+        if (++st == (uint32_t)kStages) { st = 0; ph ^= 1u; }
+    }
+};
+
 // Consumer warp side: the warp's shared loads of stage `st` are done (ordered
 // before lane 0's release-arrive by the warp barrier), so the producer may
 // refill it.
@@ -129,10 +152,10 @@ __device__ __forceinline__ void drain(Ring &ring, uint32_t issued) {
 // logprobs (kOp = 0) and entropy (kOp = 1)
 // ---------------------------------------------------------------------------
 template <int kOp, typename T>
-__global__ void __launch_bounds__(kTmaThreads, 2)
+__global__ void __launch_bounds__(kTmaThreads, kCtasPerSm)
 stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const int64_t *__restrict__ targets,
                      int64_t vocab_start, float *__restrict__ out, RowStat *__restrict__ stats,
-                     int32_t *__restrict__ err) {
+                     int32_t *__restrict__ err, PartialRec *__restrict__ shard_parts) {
     constexpr bool kW = kOp == 1;
     constexpr int kVec = Elem<T>::kVec;
     constexpr int kChunkVec = kStageBytes / 16;                 // 16-byte vectors per stage
@@ -164,7 +187,8 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&ring.parts_empty[slot]);
-                finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
+                if (shard_parts) finish_partial<kOp>(p, r, V, t, vocab_start, zt, shard_parts);
+                else finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
             }
         }
         return;
@@ -191,7 +215,7 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
 
     // consumers
     const int ct = threadIdx.x;
-    uint32_t it = 0;
+    RingPos pos;
     bool ok = true;
     int rowi = 0;
     for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
@@ -201,9 +225,9 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
         const int tail0 = head + nv * kVec;
         Lane1<T, kW> acc;
         acc.init(kNegBig);
-        for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
-            const uint32_t st = it % kStages;
-            if (ok && !mbar_wait(&ring.full[st], (it / kStages) & 1)) {
+        for (int c0 = 0; c0 < nv; c0 += kChunkVec, pos.next()) {
+            const uint32_t st = pos.st;
+            if (ok && !mbar_wait(&ring.full[st], pos.ph)) {
                 ok = false;
                 atomicOr(&g_tma_fault, 2u);
             }
@@ -248,9 +272,10 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
 // KL(P||Q); P and Q share their address modulo 16 (checked by the launcher)
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kTmaThreads, 2)
+__global__ void __launch_bounds__(kTmaThreads, kCtasPerSm)
 kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, int V, Rows rows,
-                  float *__restrict__ kl, RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q) {
+                  float *__restrict__ kl, RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q,
+                  PartialRec *__restrict__ shard_parts) {
     constexpr int kVec = Elem<T>::kVec;
     constexpr int kHalf = kStageBytes / 2;                      // P and Q halves of a stage
     constexpr int kChunkVec = kHalf / 16;                       // 512 vectors of each
@@ -273,7 +298,8 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&ring.parts_empty[slot]);
-                finish_kl(p, r, kl, stats_p, stats_q);
+                if (shard_parts) finish_partial_kl(p, r, shard_parts);
+                else finish_kl(p, r, kl, stats_p, stats_q);
             }
         }
         return;
@@ -303,7 +329,7 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
     }
 
     const int ct = threadIdx.x;
-    uint32_t it = 0;
+    RingPos pos;
     bool ok = true;
     int rowi = 0;
     for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
@@ -314,9 +340,9 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
         const int tail0 = head + nv * kVec;
         LaneKL<T> acc;
         acc.init(kNegBig, kNegBig);
-        for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
-            const uint32_t st = it % kStages;
-            if (ok && !mbar_wait(&ring.full[st], (it / kStages) & 1)) {
+        for (int c0 = 0; c0 < nv; c0 += kChunkVec, pos.next()) {
+            const uint32_t st = pos.st;
+            if (ok && !mbar_wait(&ring.full[st], pos.ph)) {
                 ok = false;
                 atomicOr(&g_tma_fault, 2u);
             }
@@ -400,7 +426,7 @@ static cudaError_t allow_ring(K kernel, std::atomic<uint64_t> &done) {
 }
 
 static unsigned persistent_grid(int64_t N) {
-    const int64_t g = 2 * (int64_t)sm_count();
+    const int64_t g = kCtasPerSm * (int64_t)sm_count();
     return (unsigned)(N < g ? N : g);
 }
 
@@ -412,7 +438,7 @@ static cudaError_t launch_stats_tma(const StatsArgs &a) {
     if (e != cudaSuccess) return e;
     k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
         static_cast<const T *>(a.x), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.targets, a.vocab_start, a.out,
-        static_cast<RowStat *>(a.stats), a.err);
+        static_cast<RowStat *>(a.stats), a.err, static_cast<PartialRec *>(a.parts));
     return cudaGetLastError();
 }
 
@@ -432,7 +458,7 @@ static cudaError_t launch_kl_tma(const KLFwdArgs &a) {
     if (e != cudaSuccess) return e;
     k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
         static_cast<const T *>(a.p), static_cast<const T *>(a.q), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.kl,
-        static_cast<RowStat *>(a.stats_p), static_cast<RowStat *>(a.stats_q));
+        static_cast<RowStat *>(a.stats_p), static_cast<RowStat *>(a.stats_q), static_cast<PartialRec *>(a.parts));
     return cudaGetLastError();
 }
 

@@ -18,6 +18,7 @@ struct StatsArgs {
     void *stats;  // vp_rowstat [N]
     int32_t *err;
     cudaStream_t stream;
+    void *parts = nullptr;  // vp_partial [N]: per-shard records instead of out / stats
 };
 
 struct KLFwdArgs {
@@ -27,7 +28,22 @@ struct KLFwdArgs {
     float *kl;
     void *stats_p, *stats_q;
     cudaStream_t stream;
+    void *parts = nullptr;  // vp_partial [N]: per-shard records instead of kl / stats
 };
+
+// Merge of K shards' vp_partial records (K * N, shard-major) per row.
+struct MergeArgs {
+    const void *parts;
+    int64_t K, N;
+    float *out;
+    void *stats_p, *stats_q;  // vp_rowstat [N]; stats_q for KL only
+    int32_t *err;
+    cudaStream_t stream;
+};
+
+cudaError_t launch_logprobs_merge(const MergeArgs &a);
+cudaError_t launch_entropy_merge(const MergeArgs &a);
+cudaError_t launch_kl_merge(const MergeArgs &a);
 
 struct GradArgs {
     const void *x;

@@ -141,7 +141,9 @@ struct Lane1 {
     }
 
     // bf16 fast path on raw 16-byte words (8 values each): packed max, packed
-    // f32x2 arithmetic and four independent accumulator pairs.
+    // f32x2 arithmetic and four independent accumulator pairs. The chunk sums
+    // are added to the lane's running sums in plain fp32 (S.hi, W.hi; a lane
+    // takes about ten chunks per row); only the fp32 path carries double-floats.
     template <int K>
     __device__ __forceinline__ void push_bf16(const uint4 (&u)[K]) {
         const float c = max_bf16(u);
@@ -150,20 +152,23 @@ struct Lane1 {
         const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
         float2 s[4], w[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) s[q] = w[q] = make_float2(0.f, 0.f);
-#pragma unroll
         for (int k = 0; k < K; ++k) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
                 const float2 a = __fmul2_rn(t, l2e);
                 const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
-                s[q] = __fadd2_rn(s[q], e);
-                if (kW) w[q] = __ffma2_rn(e, t, w[q]);
+                if (k == 0) {
+                    s[q] = e;
+                    if (kW) w[q] = __fmul2_rn(e, t);
+                } else {
+                    s[q] = __fadd2_rn(s[q], e);
+                    if (kW) w[q] = __ffma2_rn(e, t, w[q]);
+                }
             }
         }
         const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
-        df_add(S, ss.x + ss.y);
+        S.hi += ss.x + ss.y;
         if (kW) {
             float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
             float wsum = ww.x + ww.y;
@@ -185,7 +190,7 @@ struct Lane1 {
                 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
                 wsum = ww.x + ww.y;
             }
-            df_add(W, wsum);
+            W.hi += wsum;
         }
     }
 };
@@ -346,8 +351,6 @@ struct LaneKL {
         const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
         float2 sp[4], sq[4], w[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) sp[q] = sq[q] = w[q] = make_float2(0.f, 0.f);
-#pragma unroll
         for (int k = 0; k < K; ++k) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -356,9 +359,16 @@ struct LaneKL {
                 const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
                 const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
                 const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
-                sp[q] = __fadd2_rn(sp[q], ep);
-                sq[q] = __fadd2_rn(sq[q], eq);
-                w[q] = __ffma2_rn(ep, __ffma2_rn(tq, m1, tp), w[q]);    // ep (tp - tq)
+                const float2 d = __ffma2_rn(tq, m1, tp);                             // tp - tq
+                if (k == 0) {
+                    sp[q] = ep;
+                    sq[q] = eq;
+                    w[q] = __fmul2_rn(ep, d);
+                } else {
+                    sp[q] = __fadd2_rn(sp[q], ep);
+                    sq[q] = __fadd2_rn(sq[q], eq);
+                    w[q] = __ffma2_rn(ep, d, w[q]);
+                }
             }
         }
         float2 c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
@@ -391,9 +401,9 @@ struct LaneKL {
         }
         const float2 a = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
         const float2 b = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
-        df_add(Sp, a.x + a.y);
-        df_add(Sq, b.x + b.y);
-        df_add(W, wsum);
+        Sp.hi += a.x + a.y;   // plain fp32 lane sums on the bf16 path (see Lane1::push_bf16)
+        Sq.hi += b.x + b.y;
+        W.hi += wsum;
     }
 };
 
@@ -513,6 +523,47 @@ __device__ __forceinline__ void finish_kl(const PartKL<Acc> &s, int64_t r, float
     else if (fp & kRowMismatch) res = pinf();
     else res = (float)(c - logSp + logSq);
     kl[r] = res;
+}
+
+// Per-shard record of a row (vocabulary-sharded forms): the merged partial
+// re-centred in fp64 from its centre `ref` onto the shard's exact max.
+template <int kOp, typename Acc>
+__device__ __forceinline__ void finish_partial(const Part1<Acc> &p, int64_t r, int V, int64_t t, int64_t vocab_start,
+                                               float zt, PartialRec *parts) {
+    PartialRec o;
+    const double sh = (double)p.mx - (double)p.ref;   // >= 0
+    const double a = exp(-sh);
+    const double S = (double)p.S;
+    o.m = p.mx;
+    o.m_b = 0.f;
+    o.S = a * S;
+    o.S_b = 0.0;
+    o.W = (kOp == 1 && o.S > 0.0) ? a * ((double)p.W - sh * S) : 0.0;
+    o.z_t = 0.f;
+    uint32_t flags = (S != S) ? kPartNanInf : 0u;
+    if (kOp == 0) {
+        const int64_t loc = t - vocab_start;
+        if (t < 0) flags |= kPartIgnored;
+        else if (loc >= 0 && loc < V) { flags |= kPartHasTarget; o.z_t = zt; }
+    }
+    o.flags = flags;
+    parts[r] = o;
+}
+
+template <typename Acc>
+__device__ __forceinline__ void finish_partial_kl(const PartKL<Acc> &s, int64_t r, PartialRec *parts) {
+    PartialRec o;
+    const double shp = (double)s.mxp - (double)s.rp, shq = (double)s.mxq - (double)s.rq;
+    const double ap = exp(-shp), aq = exp(-shq);
+    const double Sp = (double)s.Sp, Sq = (double)s.Sq;
+    o.m = s.mxp;
+    o.m_b = s.mxq;
+    o.S = ap * Sp;
+    o.S_b = aq * Sq;
+    o.W = (o.S > 0.0) ? ap * ((double)s.W - (shp - shq) * Sp) : 0.0;
+    o.z_t = 0.f;
+    o.flags = ((Sp != Sp) ? kPartNanInf : 0u) | ((Sq != Sq) ? kPartNanInfB : 0u) | (s.flag ? kPartMismatch : 0u);
+    parts[r] = o;
 }
 
 // The warp's shared centre: the max over its first round of values.

@@ -1,0 +1,44 @@
+"""Host plumbing of the vocabulary-sharded forms across ranks (torch.distributed).
+
+Each rank holds one shard of the vocabulary and computes one vp_partial record
+per row with ``vp_*_partial``. ``gather_partials`` collects every rank's
+records into one ``[world, N, 5]`` tensor in rank order, which is the
+shard-major layout ``vp_*_merge`` takes (the records of rank k become shard k;
+the merge does not depend on which columns a shard holds). This is the
+one exchange step of the sharded forms: a single all-gather of 40 bytes per row
+and rank, in place of the pages' MAX then SUM all-reduces ([P1] page "Add
+Triton kernels for vocab-parallel logprobs, entropy and KL", second commit
+message). The library itself calls no collective.
+"""
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+from . import api
+
+
+def gather_partials(parts: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather one rank's ``[N, 5]`` float64 records into ``[world, N, 5]`` (rank order)."""
+    if parts.dim() != 2 or parts.shape[1] != api.PARTIAL_DOUBLES or parts.dtype != torch.float64:
+        raise api.VPError(2, "records must be a float64 [N, 5] tensor")
+    world = dist.get_world_size(group)
+    out = torch.empty((world,) + tuple(parts.shape), dtype=parts.dtype, device=parts.device)
+    dist.all_gather(list(out.unbind(0)), parts.contiguous(), group=group)
+    return out
+
+
+def tp_entropy_fwd(x_shard, group=None):
+    """Entropy of rows whose vocabulary is split across the ranks of `group`: (H, stats) on every rank."""
+    return api.vp_entropy_merge(gather_partials(api.vp_entropy_partial(x_shard), group))
+
+
+def tp_logprobs_fwd(x_shard, targets, vocab_start: int, group=None, err_word=None):
+    """logp of global target ids over rows split across ranks: (logp, stats) on every rank."""
+    parts = api.vp_logprobs_partial(x_shard, targets, vocab_start)
+    return api.vp_logprobs_merge(gather_partials(parts, group), err_word=err_word)
+
+
+def tp_kl_fwd(a_shard, b_shard, direction: int = api.KL_REVERSE, group=None):
+    """KL over rows split across ranks: (kl, stats_a, stats_b) on every rank."""
+    return api.vp_kl_merge(gather_partials(api.vp_kl_partial(a_shard, b_shard, direction), group), direction)
