@@ -1,4 +1,4 @@
-// vp_linear.cu -- fused linear logp forward on tcgen05 tensor cores.
+// vp_linear.cu -- fused linear logp forward and backward on tcgen05 tensor cores.
 //
 // Sources:
 //   [P2] page "[Feat][Kernel] Add TP Fused linear logp Triton", "Implementation":
@@ -10,7 +10,7 @@
 //   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL",
 //        second commit message (partials re-centred on the max).
 //
-// Kernel 1 (linear_lse_kernel), a persistent grid of one CTA per SM:
+// Kernel 1 (umma_gemm_kernel<LseEpi>), a persistent grid of one CTA per SM:
 //   tiles of 128 hidden rows x 256 vocabulary rows of W, K = D in steps of 64;
 //   warp 0 (one thread) streams the bf16 operand tiles with 2-D TMA into a
 //   4-stage ring (48 KB per stage, 128-byte swizzle); warp 1 (one thread)
@@ -58,16 +58,22 @@ struct LinearBars {
 };
 
 // ---------------------------------------------------------------------------
-// Persistent tcgen05 GEMM C[M, Nn] = A[M, K] . B[Nn, K]^T (bf16 K-major operands
-// through 2-D tensor maps, fp32 accumulation in TMEM) with a pluggable
-// epilogue. Tiles run N-major (consecutive CTAs share one B tile through L2).
+// Persistent tcgen05 GEMM C[M, Nn] = A[M, K] . B[Nn, K]^T (bf16 operands through
+// 2-D tensor maps, fp32 accumulation in TMEM) with a pluggable epilogue.
+// Operand layouts: K-major (kAMn / kBMn false: a row of the operand's tensor map
+// holds K-consecutive elements; one box of 64 x rows per stage) or MN-major
+// (true: the map's rows run along K and hold MN-consecutive elements; 64 x 64
+// boxes, 8 KB apart in shared memory), so that a transposed operand is read in
+// place. Tiles run N-major (consecutive CTAs share one B tile through L2).
 // The epilogue functor is called by each of the 128 epilogue threads for its
 // accumulator row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the
 // row's 256 columns; it reads them with tmem_ld32, which is warp-collective, so
 // every lane runs every load (rows past M included) and only the global
 // accesses are guarded.
 // ---------------------------------------------------------------------------
-template <class Epi>
+constexpr uint32_t kLMnAtomBytes = 64 * kLBK * 2;   // one 64 (MN) x 64 (K) box: 8 KB
+
+template <class Epi, bool kAMn = false, bool kBMn = false>
 __global__ void __launch_bounds__(kLThreads, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M, int Nn,
                  int K, const Epi epi) {
@@ -110,8 +116,21 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     if (use > 0 && !mbar_wait(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
                     uint8_t *a = smem + st * kLStageBytes;
                     mbar_arrive_expect_tx(&bars.full[st], kLStageBytes);
-                    tma_load_2d(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st]);
-                    tma_load_2d(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st]);
+                    if (kAMn) {
+#pragma unroll
+                        for (int i = 0; i < kLBM / 64; ++i)
+                            tma_load_2d(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK, &bars.full[st]);
+                    } else {
+                        tma_load_2d(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st]);
+                    }
+                    if (kBMn) {
+#pragma unroll
+                        for (int i = 0; i < kLBN / 64; ++i)
+                            tma_load_2d(a + kLAStage + i * kLMnAtomBytes, &tm_b, nb * kLBN + 64 * i, kb * kLBK,
+                                        &bars.full[st]);
+                    } else {
+                        tma_load_2d(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st]);
+                    }
                 }
             }
             if (!ok) atomicOr(&g_linear_fault, 1u);
@@ -119,7 +138,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(kLBM, kLBN);
+            constexpr uint32_t idesc = umma_idesc_bf16(kLBM, kLBN, kAMn, kBMn);
             uint32_t it = 0, j = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++j) {
@@ -133,9 +152,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     tc_fence_after();
                     const uint8_t *a = smem + st * kLStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kLBK / 16; ++kk)
-                        umma_bf16(d, umma_desc_sw128(a + kk * 32), umma_desc_sw128(a + kLAStage + kk * 32), idesc,
-                                  (kb | kk) != 0);
+                    for (int kk = 0; kk < kLBK / 16; ++kk) {
+                        // a 16-deep K step: 32 bytes along a K-major row, two 8-row groups MN-major
+                        const uint64_t da = kAMn ? umma_desc_sw128_mn(a + kk * 2048, kLMnAtomBytes)
+                                                 : umma_desc_sw128(a + kk * 32);
+                        const uint64_t db = kBMn ? umma_desc_sw128_mn(a + kLAStage + kk * 2048, kLMnAtomBytes)
+                                                 : umma_desc_sw128(a + kLAStage + kk * 32);
+                        umma_bf16(d, da, db, idesc, (kb | kk) != 0);
+                    }
                     umma_commit(&bars.empty[st]);       // frees the stage once these MMAs are done
                 }
                 umma_commit(&bars.acc_full[buf]);       // the accumulator is complete
@@ -215,16 +239,17 @@ struct LseEpi {
 
 // Backward K1 epilogue: dz = g (onehot - p), p = exp((z - m) - logS), for a
 // 256-column tile of a vocabulary chunk starting at shard column v0, written
-// as bf16 (round to nearest even) both row-major dz[row][col] (pitch ldz) and
-// transposed dzt[col][row] (pitch ldt). Rows with an ignored target get 0,
-// rows with a data error or without valid statistics get NaN.
+// as bf16 (round to nearest even) row-major dz[row][col] (pitch ldz); the two
+// gradient GEMMs read it in place, dz^T through an MN-major tensor map. Rows
+// with an ignored target get 0, rows with a data error or without valid
+// statistics get NaN.
 struct DzEpi {
-    int N, V, v0, ldz, ldt;
+    int N, V, v0, ldz;
     int64_t vocab_start;
     const int64_t *targets;
     const RowStat *stats;
     const float *g;
-    __nv_bfloat16 *dz, *dzt;
+    __nv_bfloat16 *dz;
     int32_t *err;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
         const bool valid = row < N;
@@ -264,10 +289,6 @@ struct DzEpi {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-            unsigned short *t = reinterpret_cast<unsigned short *>(dzt);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                t[(int64_t)(col0 + c * 32 + i) * ldt + row] = (unsigned short)(packed[i / 2] >> (16 * (i & 1)));
         }
     }
 };
@@ -325,29 +346,6 @@ struct StoreBf16Epi {
         }
     }
 };
-
-// dst[c][r] = src[r][c] for a rows x cols bf16 block (pitches in elements); 32 x 32
-// tiles through shared memory.
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16 *__restrict__ src, int rows,
-                                                             int cols, int64_t ld_src,
-                                                             __nv_bfloat16 *__restrict__ dst, int64_t ld_dst) {
-    __shared__ unsigned short tile[32][33];
-    const unsigned short *s = reinterpret_cast<const unsigned short *>(src);
-    unsigned short *d = reinterpret_cast<unsigned short *>(dst);
-    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-#pragma unroll
-    for (int k = 0; k < 32; k += 8) {
-        const int r = r0 + ty + k, c = c0 + tx;
-        tile[ty + k][tx] = (r < rows && c < cols) ? s[(int64_t)r * ld_src + c] : 0;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 32; k += 8) {
-        const int c = c0 + ty + k, r = r0 + tx;
-        if (c < cols && r < rows) d[(int64_t)c * ld_dst + r] = tile[tx][ty + k];
-    }
-}
 
 // out[i] = bf16(acc[i]) for rows x cols (pitches in elements)
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ acc, int64_t n,
@@ -432,15 +430,29 @@ static bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t co
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <class Epi>
+// MN-major operand map: `rows` along K, `cols` (the operand's M or N) consecutive,
+// boxes of 64 x 64.
+static bool make_map_mn(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int64_t pitch) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)kLBK};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Epi, bool kAMn = false, bool kBMn = false>
 static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, const Epi &epi,
                                cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kLSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi, kAMn, kBMn>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(1ull << (dev & 63));
     }
@@ -448,7 +460,7 @@ static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t n_tiles = (int64_t)((M + kLBM - 1) / kLBM) * ((Nn + kLBN - 1) / kLBN);
     const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
-    umma_gemm_kernel<Epi><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, M, Nn, K, epi);
+    umma_gemm_kernel<Epi, kAMn, kBMn><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, M, Nn, K, epi);
     return cudaGetLastError();
 }
 
@@ -522,32 +534,26 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
 
 // ---------------------------------------------------------------------------
 // Backward: vocabulary chunks of kVc rows of W.
-//   K1  logits tile (h . W_c^T, K = D) -> dz, dz^T            (DzEpi)
-//   K2  dhidden_acc (+)= dz . W_c     (A = dz, B = W_c^T, K = chunk)   (AccEpi)
-//   K3  dW_c = dz^T . h               (A = dz^T, B = h^T, K = N)       (StoreBf16Epi)
-// Every operand is K-major: W_c^T and h^T come from transpose kernels.
+//   K1  logits tile (h . W_c^T, K = D) -> dz                   (DzEpi)
+//   K2  dhidden_acc (+)= dz . W_c     (A = dz K-major, B = W_c MN-major, K = chunk)   (AccEpi)
+//   K3  dW_c = dz^T . h               (A = dz MN-major, B = h MN-major, K = N)        (StoreBf16Epi)
+// The transposed operands are read in place through MN-major tensor maps.
 // ---------------------------------------------------------------------------
 constexpr int64_t kVc = 8192;
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct BwdLayout {
-    size_t ht, wt, dz, dzt, acc, total;
+    size_t dz, acc, total;
 };
 
-// Pitch (elements) of the transposed [., N] buffers: a multiple of 8, so that
-// rows start on 16-byte boundaries as the tensor maps require.
-static int64_t pitch_n(int64_t N) { return (N + 7) & ~(int64_t)7; }
+static int64_t chunk_cols(int64_t V) { return V < kVc ? ((V + 255) / 256) * 256 : kVc; }
 
 static BwdLayout bwd_layout(int64_t N, int64_t V, int64_t D) {
-    const int64_t vc = V < kVc ? ((V + 255) / 256) * 256 : kVc;
-    const int64_t ldn = pitch_n(N);
+    const int64_t vc = chunk_cols(V);
     BwdLayout L;
-    L.ht = 0;
-    L.wt = L.ht + up256((size_t)D * ldn * 2);
-    L.dz = L.wt + up256((size_t)D * vc * 2);
-    L.dzt = L.dz + up256((size_t)N * vc * 2);
-    L.acc = L.dzt + up256((size_t)vc * ldn * 2);
+    L.dz = 0;
+    L.acc = L.dz + up256((size_t)N * vc * 2);
     L.total = L.acc + up256((size_t)N * D * 4);
     return L;
 }
@@ -556,51 +562,41 @@ size_t linear_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D) { return bwd_
 
 cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
     const BwdLayout L = bwd_layout(a.N, a.V, a.D);
-    const int64_t vc = a.V < kVc ? ((a.V + 255) / 256) * 256 : kVc;
+    const int64_t vc = chunk_cols(a.V);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-    __nv_bfloat16 *ht = reinterpret_cast<__nv_bfloat16 *>(ws + L.ht);
-    __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(ws + L.wt);
     __nv_bfloat16 *dz = reinterpret_cast<__nv_bfloat16 *>(ws + L.dz);
-    __nv_bfloat16 *dzt = reinterpret_cast<__nv_bfloat16 *>(ws + L.dzt);
     float *acc = reinterpret_cast<float *>(ws + L.acc);
     const __nv_bfloat16 *h = static_cast<const __nv_bfloat16 *>(a.hidden);
     const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(a.weight);
     const int N = (int)a.N, V = (int)a.V, D = (int)a.D;
-    const int ldn = (int)pitch_n(a.N);
     cudaError_t e;
 
-    CUtensorMap tm_h, tm_w, tm_dz, tm_wt, tm_dzt, tm_ht;
-    if (!make_map(&tm_h, h, N, D, D, kLBM) || !make_map(&tm_w, W, V, D, D, kLBN)) return cudaErrorInvalidValue;
-    if (a.dW) {
-        dim3 grid((D + 31) / 32, (N + 31) / 32);
-        transpose_bf16_kernel<<<grid, 256, 0, a.stream>>>(h, N, D, D, ht, ldn);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if (!make_map(&tm_ht, ht, D, N, ldn, kLBN)) return cudaErrorInvalidValue;
-    }
+    CUtensorMap tm_h, tm_h_mn;
+    if (!make_map(&tm_h, h, N, D, D, kLBM) || !make_map_mn(&tm_h_mn, h, N, D, D)) return cudaErrorInvalidValue;
     for (int64_t v0 = 0; v0 < V; v0 += vc) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
         // K1 over this chunk's rows of W (the map's rows start at v0)
         CUtensorMap tm_wc;
         if (!make_map(&tm_wc, W + v0 * D, nv, D, D, kLBN)) return cudaErrorInvalidValue;
-        const DzEpi de{N, V, (int)v0, (int)vc, ldn, a.vocab_start, a.targets,
-                       static_cast<const RowStat *>(a.stats), a.g, dz, dzt, a.err};
+        const DzEpi de{N, V, (int)v0, (int)vc, a.vocab_start, a.targets, static_cast<const RowStat *>(a.stats), a.g,
+                       dz, a.err};
         if ((e = launch_gemm(tm_h, tm_wc, N, nv, D, de, a.stream)) != cudaSuccess) return e;
         if (a.dhidden) {
-            dim3 grid((D + 31) / 32, (nv + 31) / 32);
-            transpose_bf16_kernel<<<grid, 256, 0, a.stream>>>(W + v0 * D, nv, D, D, wt, vc);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-            if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map(&tm_wt, wt, D, nv, vc, kLBN))
+            CUtensorMap tm_dz, tm_wc_mn;
+            if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
                 return cudaErrorInvalidValue;
             const AccEpi ae{N, D, v0 == 0, acc};
-            if ((e = launch_gemm(tm_dz, tm_wt, N, D, nv, ae, a.stream)) != cudaSuccess) return e;
+            if ((e = launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, a.stream)) != cudaSuccess)
+                return e;
         }
         if (a.dW) {
-            if (!make_map(&tm_dzt, dzt, nv, N, ldn, kLBM)) return cudaErrorInvalidValue;
+            CUtensorMap tm_dz_mn;
+            if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc)) return cudaErrorInvalidValue;
             const StoreBf16Epi se{nv, D, v0, static_cast<__nv_bfloat16 *>(a.dW)};
-            if ((e = launch_gemm(tm_dzt, tm_ht, nv, D, N, se, a.stream)) != cudaSuccess) return e;
+            if ((e = launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, a.stream)) != cudaSuccess)
+                return e;
         }
     }
-    (void)tm_w;
     if (a.dhidden) {
         const int64_t n = (int64_t)N * D;
         to_bf16_kernel<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256, 0, a.stream>>>(

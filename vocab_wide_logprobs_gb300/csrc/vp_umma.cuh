@@ -2,8 +2,9 @@
 // for sm_103a, in inline PTX: TMEM allocation, shared-memory matrix and
 // instruction descriptors, MMA issue and commit, TMEM loads, 2-D tiled TMA.
 //
-// Operand layout used throughout: K-major bf16 tiles of 64 elements (128 bytes)
-// per row, written by TMA with the 128-byte swizzle, 8-row atoms of 1024 bytes.
+// Operand layouts: K-major bf16 tiles of 64 K-elements (128 bytes) per row, or
+// MN-major tiles of 64 MN-elements per K-row, both written by TMA with the
+// 128-byte swizzle in 8-row atoms of 1024 bytes.
 #pragma once
 
 #include <cuda.h>
@@ -43,12 +44,30 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(const void *smem) {
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand, 128-byte swizzle:
+// each atom is 8 K-rows of 64 consecutive MN elements (128 bytes per row,
+// 1024 bytes per atom); atoms along MN are `mn_stride` bytes apart (LBO) and
+// groups of 8 K-rows are 1024 bytes apart (SBO). A 16-deep K step advances the
+// start address by 2048 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(const void *smem, uint32_t mn_stride) {
+    const uint64_t addr = smem_u32(smem);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3FFFull;                  // start address              [0, 14)
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFF) << 16;   // leading byte offset: MN atoms [16, 30)
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset: K groups    [32, 46)
+    d |= (uint64_t)1 << 46;                        // version                    [46, 48)
+    d |= (uint64_t)2 << 61;                        // layout: 128-byte swizzle   [61, 64)
+    return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+// shape M x N; each operand K-major unless its MN-major flag is set.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn = false, bool b_mn = false) {
     return (1u << 4)                        // accumulator format: f32   [4, 6)
            | (1u << 7)                      // A format: bf16            [7, 10)
            | (1u << 10)                     // B format: bf16            [10, 13)
+           | ((a_mn ? 1u : 0u) << 15)       // A MN-major                [15]
+           | ((b_mn ? 1u : 0u) << 16)       // B MN-major                [16]
            | ((uint32_t)(N >> 3) << 17)     // N / 8                     [17, 23)
            | ((uint32_t)(M >> 4) << 24);    // M / 16                    [24, 29)
 }
