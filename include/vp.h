@@ -320,15 +320,16 @@ VP_API vp_status vp_linear_logp_fwd(const void *hidden, const void *weight, int6
                                     int64_t vocab_start, const int64_t *targets, float *logp, vp_rowstat *stats,
                                     void *workspace, size_t workspace_bytes, int32_t *err_word, vp_stream stream);
 
-/* Bytes of device workspace vp_linear_logp_bwd needs: dz of one 8192-row
- * vocabulary chunk (bf16 [N, 8192]) and an fp32 accumulator of dhidden
+/* Bytes of device workspace vp_linear_logp_bwd needs: dz of one vocabulary
+ * chunk (bf16 [N, vc], vc = 32768 columns for N <= 8192, 16384 for N <= 16384,
+ * else 8192, at most V rounded up to 256) and an fp32 accumulator of dhidden
  * ([N, D]). 0 for invalid sizes. */
 VP_API size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D);
 
 /* Gradients of sum_r g[r] logp[r] for the forward above [P2, review nitpick on
  * the chunked backward: dz = g (onehot - exp(logits - lse)), dhidden = dz . W,
- * dW = dz^T . h]. The logits are recomputed chunk by chunk (8192 vocabulary
- * rows of W at a time) on tcgen05 tensor cores; dz of a chunk is rounded to
+ * dW = dz^T . h]. The logits are recomputed chunk by chunk (vc vocabulary
+ * rows of W at a time, see above) on tcgen05 tensor cores; dz of a chunk is rounded to
  * bf16 for the two gradient GEMMs (fp32 accumulation in TMEM), which read dz,
  * W and h in place (transposed operands as MN-major tiles); dhidden
  * accumulates across chunks in fp32 and is rounded to bf16 at the end; dW is

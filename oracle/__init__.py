@@ -61,13 +61,15 @@ _SIGS = {
     "vpo_kl_sharded": (["P", "P", "I", "I", "i", "P", "i", "P"], None),
     "vpo_shard_stats": (["P", "I", "I", "I", "I", "P"], None),
     "vpo_shard_kl_stats": (["P", "P", "I", "I", "i", "I", "I", "P"], None),
+    "vpo_jsd_fwd": (["P", "P", "I", "I", "d", "P"], None),
+    "vpo_jsd_bwd": (["P", "P", "I", "I", "d", "P", "P", "P"], None),
     "vpo_merge_entropy_records": (["P", "I", "I", "P"], None),
     "vpo_merge_kl_records": (["P", "I", "I", "P"], None),
     "vpo_linear_logits": (["P", "P", "I", "I", "I", "P"], None),
     "vpo_linear_logp_fwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P", "P"], None),
     "vpo_linear_logp_bwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P"], None),
 }
-_CT = {"P": ctypes.c_void_p, "I": ctypes.c_int64, "i": ctypes.c_int}
+_CT = {"P": ctypes.c_void_p, "I": ctypes.c_int64, "i": ctypes.c_int, "d": ctypes.c_double}
 
 
 def load_library(path: str):
@@ -168,6 +170,25 @@ def kl_bwd(a, b, g, direction=REVERSE, lib=None):
     g = _f64(g)
     da, db = np.empty((N, V)), np.empty((N, V))
     (lib or _load()).vpo_kl_bwd(_p(a), _p(b), N, V, int(direction), _p(g), _p(da), _p(db))
+    return da, db
+
+
+def jsd_fwd(a, b, beta, lib=None):
+    """Generalized JSD per row: beta KL(q || mix) + (1 - beta) KL(p || mix), mix = beta q + (1 - beta) p
+    (p = softmax(a), q = softmax(b)); beta = 0 is KL(b || a), beta = 1 is KL(a || b)."""
+    a, b = _f64(a), _f64(b)
+    N, V = _shape(a)
+    out = np.empty(N)
+    (lib or _load()).vpo_jsd_fwd(_p(a), _p(b), N, V, float(beta), _p(out))
+    return out
+
+
+def jsd_bwd(a, b, beta, g, lib=None):
+    """(dA, dB) of sum_r g[r] JSD_r."""
+    a, b, g = _f64(a), _f64(b), _f64(g)
+    N, V = _shape(a)
+    da, db = np.empty((N, V)), np.empty((N, V))
+    (lib or _load()).vpo_jsd_bwd(_p(a), _p(b), N, V, float(beta), _p(g), _p(da), _p(db))
     return da, db
 
 

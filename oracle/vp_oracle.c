@@ -261,6 +261,73 @@ void vpo_kl_bwd(const double *a, const double *b, int64_t N, int64_t V, int dire
 }
 
 /* ------------------------------------------------------------------------ */
+/* Generalized Jensen-Shannon divergence [P1, the commit message that adds  */
+/* vocab_parallel_jsd: "Changes", "Scope and limitations"]. The page fixes  */
+/* beta = 0 as forward KL and beta = 1 as reverse KL (explicit endpoint     */
+/* branches) and, for 0 < beta < 1, a GKD-style divergence made of two      */
+/* KL-to-mixture expectations, but prints no formula. Reading R13: with     */
+/* p = softmax(A) (the student, first argument), q = softmax(B) (the        */
+/* teacher) and the mixture mix = beta q + (1 - beta) p,                    */
+/*   JSD = beta KL(q || mix) + (1 - beta) KL(p || mix).                      */
+/* Gradients through the two softmaxes (R13):                               */
+/*   dJSD/dA_j = (1 - beta) p_j ((log p_j - log mix_j) - KL(p || mix)),      */
+/*   dJSD/dB_j = beta q_j ((log q_j - log mix_j) - KL(q || mix)).            */
+/* A row with a NaN or +inf in A or B, or without a finite logit in A or B, */
+/* gives NaN and NaN gradient rows (R3, R4); terms with p_j = 0 (q_j = 0)    */
+/* contribute 0 to KL(p || mix) (KL(q || mix)).                              */
+/* ------------------------------------------------------------------------ */
+static double jsd_row(const double *A, const double *B, int64_t V, double beta,
+                      const row_stats *sa, const row_stats *sb, double *ka, double *kb) {
+    *ka = *kb = NAN;
+    if (sa->bad || sb->bad || sa->S == 0.0 || sb->S == 0.0) return NAN;
+    double kp = 0.0, kq = 0.0;   /* KL(p || mix), KL(q || mix) */
+    for (int64_t j = 0; j < V; ++j) {
+        double lp = log_prob(A[j], sa), lq = log_prob(B[j], sb);
+        double p = exp(lp), q = exp(lq);
+        double lmix = log(beta * q + (1.0 - beta) * p);
+        if (p > 0.0) kp += p * (lp - lmix);
+        if (q > 0.0) kq += q * (lq - lmix);
+    }
+    *ka = kp;
+    *kb = kq;
+    return beta * kq + (1.0 - beta) * kp;
+}
+
+void vpo_jsd_fwd(const double *a, const double *b, int64_t N, int64_t V, double beta, double *jsd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        const double *A = a + r * V, *B = b + r * V;
+        row_stats sa = scan_row(A, V), sb = scan_row(B, V);
+        double ka, kb;
+        if (beta == 0.0) jsd[r] = kl_row(B, A, V, &sb, &sa);        /* forward KL(B || A) */
+        else if (beta == 1.0) jsd[r] = kl_row(A, B, V, &sa, &sb);   /* reverse KL(A || B) */
+        else jsd[r] = jsd_row(A, B, V, beta, &sa, &sb, &ka, &kb);
+    }
+}
+
+void vpo_jsd_bwd(const double *a, const double *b, int64_t N, int64_t V, double beta,
+                 const double *g, double *da, double *db) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        const double *A = a + r * V, *B = b + r * V;
+        double *dA = da ? da + r * V : NULL, *dB = db ? db + r * V : NULL;
+        if (beta == 0.0) { kl_bwd_row(B, A, V, g[r], dB, dA); continue; }
+        if (beta == 1.0) { kl_bwd_row(A, B, V, g[r], dA, dB); continue; }
+        row_stats sa = scan_row(A, V), sb = scan_row(B, V);
+        double ka, kb;
+        double jsd = jsd_row(A, B, V, beta, &sa, &sb, &ka, &kb);
+        for (int64_t j = 0; j < V; ++j) {
+            if (isnan(jsd)) { if (dA) dA[j] = NAN; if (dB) dB[j] = NAN; continue; }
+            double lp = log_prob(A[j], &sa), lq = log_prob(B[j], &sb);
+            double p = exp(lp), q = exp(lq);
+            double lmix = log(beta * q + (1.0 - beta) * p);
+            if (dA) dA[j] = (p > 0.0) ? g[r] * (1.0 - beta) * p * ((lp - lmix) - ka) : 0.0;
+            if (dB) dB[j] = (q > 0.0) ? g[r] * beta * q * ((lq - lmix) - kb) : 0.0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Sharded forms: the re-centring merge of [P1] (second commit message and  */
 /* the reviewer's suggested change), with zero-weight terms skipped as in   */
 /* the Codex thread "Guard zero rescaling before applying infinite shifts". */

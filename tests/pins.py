@@ -20,7 +20,11 @@ build) and raises AssertionError when the oracle disagrees with:
   shards, equal to the direct form;
 * the per-shard records (max, sum-exp, centred weighted sum, flags) against
   Decimal sums over each shard;
-* hand-built rows for every NaN / inf precedence rule and target rule.
+* hand-built rows for every NaN / inf precedence rule and target rule;
+* the generalized JSD: Decimal brute force of the value and of both gradients,
+  JSD(A, A) = 0, disjoint supports giving the entropy of the mixing weights,
+  symmetry at beta = 1/2, bounds, and the limits JSD_beta / beta -> KL(B||A)
+  and JSD_beta / (1 - beta) -> KL(A||B) that tie it to the KL endpoints.
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in copies of the
 oracle source and checks that at least one pin fails for each.
@@ -312,6 +316,110 @@ def pin_finite_differences(lib=None):
 
 
 # ----------------------------------------------------------------------------
+# Generalized JSD (reading R13: mix = beta q + (1 - beta) p,
+# JSD = beta KL(q || mix) + (1 - beta) KL(p || mix); beta = 0 / 1 are the KL endpoints)
+# ----------------------------------------------------------------------------
+def _djsd(A, B, beta):
+    beta = Decimal(beta)
+    p, q = _dprobs(A), _dprobs(B)
+    out = Decimal(0)
+    for pi, qi in zip(p, q):
+        mix = beta * qi + (1 - beta) * pi
+        if qi > 0:
+            out += beta * qi * (qi / mix).ln()
+        if pi > 0:
+            out += (1 - beta) * pi * (pi / mix).ln()
+    return out
+
+
+def pin_jsd_brute_force(lib=None):
+    """Interior JSD and both gradients against Decimal, on rows with -inf entries."""
+    with localcontext() as ctx:
+        ctx.prec = 80
+        for V in (2, 3, 6, 11):
+            a = _tiny_rows(300 + V, V, 3, mask_frac=0.2 if V > 2 else 0.0)
+            b = _tiny_rows(400 + V, V, 3, mask_frac=0.2 if V > 2 else 0.0)
+            b += 1.5
+            g = np.array([1.0, -0.6, 2.2])
+            for beta in (0.2, 0.5, 0.83):
+                J = oracle.jsd_fwd(a, b, beta, lib=lib)
+                da, db = oracle.jsd_bwd(a, b, beta, g, lib=lib)
+                for r in range(3):
+                    A, B = list(a[r]), list(b[r])
+                    _close(J[r], float(_djsd(A, B, beta)), 1e-14, 1e-13, f"JSD V={V} beta={beta}")
+                    gr = Decimal(g[r])
+                    ref_a = [float(gr * d) for d in _dgrad(lambda z: _djsd(z, B, beta), A)]
+                    ref_b = [float(gr * d) for d in _dgrad(lambda z: _djsd(A, z, beta), B)]
+                    _close(da[r], ref_a, 1e-13, 1e-12, f"dJSD/dA V={V} beta={beta}")
+                    _close(db[r], ref_b, 1e-13, 1e-12, f"dJSD/dB V={V} beta={beta}")
+
+
+def pin_jsd_closed_forms(lib=None):
+    N, V = 6, 300
+    a, b = _rand(61, N, V), _rand(62, N, V)
+    g = np.linspace(-1.0, 1.5, N)
+    for beta in (0.1, 0.5, 0.9):
+        # identical inputs: 0, with zero gradients
+        _close(oracle.jsd_fwd(a, a, beta, lib=lib), np.zeros(N), 1e-14, 0, f"JSD(A, A) beta={beta}")
+        for d in oracle.jsd_bwd(a, a, beta, g, lib=lib):
+            _close(d, np.zeros_like(d), 1e-15, 0, f"dJSD(A, A) beta={beta}")
+        # disjoint supports: the entropy of the mixing weights, with zero gradients
+        p, q = a.copy(), b.copy()
+        p[:, V // 2:] = -INF
+        q[:, :V // 2] = -INF
+        hb = -beta * math.log(beta) - (1 - beta) * math.log(1 - beta)
+        _close(oracle.jsd_fwd(p, q, beta, lib=lib), np.full(N, hb), 1e-14, 1e-14, f"disjoint beta={beta}")
+        for d in oracle.jsd_bwd(p, q, beta, g, lib=lib):
+            _close(d, np.zeros_like(d), 1e-14, 0, f"dJSD disjoint beta={beta}")
+        # bounds and gradient rows summing to zero
+        J = oracle.jsd_fwd(a, b, beta, lib=lib)
+        assert (J >= 0).all() and (J <= hb + 1e-15).all(), "0 <= JSD <= H(beta)"
+        for d in oracle.jsd_bwd(a, b, beta, g, lib=lib):
+            assert (np.abs(d.sum(1)) <= 1e-13 * (1 + np.abs(d).sum(1))).all(), "dJSD rows sum to 0"
+    # beta = 1/2 is symmetric in its arguments
+    _close(oracle.jsd_fwd(a, b, 0.5, lib=lib), oracle.jsd_fwd(b, a, 0.5, lib=lib), 1e-15, 1e-14, "symmetry")
+    da, db = oracle.jsd_bwd(a, b, 0.5, g, lib=lib)
+    db2, da2 = oracle.jsd_bwd(b, a, 0.5, g, lib=lib)
+    _close(da, da2, 1e-15, 1e-13, "symmetric dA")
+    _close(db, db2, 1e-15, 1e-13, "symmetric dB")
+
+
+def pin_jsd_endpoints(lib=None):
+    """beta = 0 / 1 are the KL branches exactly; the interior tends to them at rate beta (1 - beta)."""
+    N, V = 5, 257
+    a, b = _rand(71, N, V, sigma=1.0, offset=0.5), _rand(72, N, V, sigma=1.0, offset=0.5)
+    g = np.array([1.0, -2.0, 0.5, 0.3, -0.7])
+    klf = oracle.kl_fwd(a, b, oracle.FORWARD, lib=lib)[0]      # KL(B || A)
+    klr = oracle.kl_fwd(a, b, oracle.REVERSE, lib=lib)[0]      # KL(A || B)
+    assert np.array_equal(oracle.jsd_fwd(a, b, 0.0, lib=lib), klf)
+    assert np.array_equal(oracle.jsd_fwd(a, b, 1.0, lib=lib), klr)
+    for got, ref in zip(oracle.jsd_bwd(a, b, 0.0, g, lib=lib), oracle.kl_bwd(a, b, g, oracle.FORWARD, lib=lib)):
+        assert np.array_equal(got, ref)
+    for got, ref in zip(oracle.jsd_bwd(a, b, 1.0, g, lib=lib), oracle.kl_bwd(a, b, g, oracle.REVERSE, lib=lib)):
+        assert np.array_equal(got, ref)
+    # the ratio's error is first order in beta (about 4.4 beta on these rows): take two steps
+    for eps in (1e-6, 1e-7):
+        _close(oracle.jsd_fwd(a, b, eps, lib=lib) / eps, klf, 0, 10 * eps, "JSD_beta / beta -> KL(B||A)")
+        _close(oracle.jsd_fwd(a, b, 1 - eps, lib=lib) / eps, klr, 0, 10 * eps, "JSD_beta / (1 - beta) -> KL(A||B)")
+
+
+def pin_jsd_special_rows(lib=None):
+    V = 8
+    base = np.linspace(-2.0, 1.5, V)
+    a = np.tile(base, (4, 1))
+    b = np.tile(base[::-1], (4, 1))
+    a[0, 3] = NAN            # NaN in A
+    b[1, 5] = INF            # +inf in B
+    a[2, :] = -INF           # no finite logit in A
+    b[3, :6] = -INF          # B supported on two entries only: finite JSD
+    J = oracle.jsd_fwd(a, b, 0.4, lib=lib)
+    da, db = oracle.jsd_bwd(a, b, 0.4, np.ones(4), lib=lib)
+    assert np.isnan(J[:3]).all() and np.isfinite(J[3])
+    assert np.isnan(da[:3]).all() and np.isnan(db[:3]).all()
+    assert np.isfinite(da[3]).all() and (db[3, :6] == 0).all()
+
+
+# ----------------------------------------------------------------------------
 # Re-centring merge over host shards
 # ----------------------------------------------------------------------------
 def pin_shard_merge(lib=None):
@@ -532,6 +640,10 @@ ALL_PINS = [
     pin_shard_merge,
     pin_shard_records,
     pin_special_rows,
+    pin_jsd_brute_force,
+    pin_jsd_closed_forms,
+    pin_jsd_endpoints,
+    pin_jsd_special_rows,
     pin_linear_logp_brute_force,
     pin_linear_logp_finite_differences,
 ]

@@ -95,7 +95,8 @@ def _run_bwd(w, vocab_start=0, **kw):
     return dh, dW, int(err.item())
 
 
-@pytest.mark.parametrize("N,V,D", [(256, 1024, 256), (200, 777, 128), (130, 300, 64), (64, 9000, 128)])
+@pytest.mark.parametrize("N,V,D", [(256, 1024, 256), (200, 777, 128), (130, 300, 64), (64, 9000, 128),
+                                   (72, 70000, 64)])   # the last: three vocabulary chunks, a ragged last one
 def test_linear_logp_bwd_small(N, V, D):
     w = _bwd_case(N, V, D, seed=N + 7 * V + D)
     dh, dW, _ = _run_bwd(w)

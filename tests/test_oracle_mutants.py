@@ -53,6 +53,13 @@ MUTANTS = [
     ("shard KL record Q max", "o[2] = s.mq; o[3] = s.Sq;", "o[2] = s.mp; o[3] = s.Sq;"),
     ("shard KL record direction", "const double *P = (direction == 0 ? a : b) + r * V;\n        const double *Q = (direction == 0 ? b : a) + r * V;\n        shard_kl s",
      "const double *P = (direction == 1 ? a : b) + r * V;\n        const double *Q = (direction == 1 ? b : a) + r * V;\n        shard_kl s"),
+    ("JSD mixture weights swapped", "double lmix = log(beta * q + (1.0 - beta) * p);\n        if (p > 0.0) kp",
+     "double lmix = log((1.0 - beta) * q + beta * p);\n        if (p > 0.0) kp"),
+    ("JSD teacher term dropped", "return beta * kq + (1.0 - beta) * kp;", "return (1.0 - beta) * kp;"),
+    ("JSD dA drops -KL(p||mix)", "g[r] * (1.0 - beta) * p * ((lp - lmix) - ka)", "g[r] * (1.0 - beta) * p * (lp - lmix)"),
+    ("JSD dB wrong weight", "g[r] * beta * q * ((lq - lmix) - kb)", "g[r] * (1.0 - beta) * q * ((lq - lmix) - kb)"),
+    ("JSD endpoint directions swapped", "if (beta == 0.0) jsd[r] = kl_row(B, A, V, &sb, &sa);",
+     "if (beta == 0.0) jsd[r] = kl_row(A, B, V, &sa, &sb);"),
     ("linear logits transposed", "acc += h[r * D + k] * W[j * D + k];", "acc += h[r * D + k] * W[k * V + j];"),
     ("linear dW wrong row", "out[k] += c * h[r * D + k];", "out[k] += c * h[((r + 1) % N) * D + k];"),
     ("linear dh wrong vocab row", "out[k] += c * W[j * D + k];", "out[k] += c * W[((j + 1) % V) * D + k];"),

@@ -533,24 +533,27 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward: vocabulary chunks of kVc rows of W.
+// Backward: vocabulary chunks of vc rows of W (32768 for up to 8192 hidden rows,
+// fewer for more rows, so that dz of a chunk stays near 0.5 GB; larger chunks
+// mean fewer launches and fewer read-modify-write passes over dhidden).
 //   K1  logits tile (h . W_c^T, K = D) -> dz                   (DzEpi)
 //   K2  dhidden_acc (+)= dz . W_c     (A = dz K-major, B = W_c MN-major, K = chunk)   (AccEpi)
 //   K3  dW_c = dz^T . h               (A = dz MN-major, B = h MN-major, K = N)        (StoreBf16Epi)
 // The transposed operands are read in place through MN-major tensor maps.
 // ---------------------------------------------------------------------------
-constexpr int64_t kVc = 8192;
-
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct BwdLayout {
     size_t dz, acc, total;
 };
 
-static int64_t chunk_cols(int64_t V) { return V < kVc ? ((V + 255) / 256) * 256 : kVc; }
+static int64_t chunk_cols(int64_t N, int64_t V) {
+    const int64_t vc = N <= 8192 ? 32768 : N <= 16384 ? 16384 : 8192;
+    return V < vc ? ((V + 255) / 256) * 256 : vc;
+}
 
 static BwdLayout bwd_layout(int64_t N, int64_t V, int64_t D) {
-    const int64_t vc = chunk_cols(V);
+    const int64_t vc = chunk_cols(N, V);
     BwdLayout L;
     L.dz = 0;
     L.acc = L.dz + up256((size_t)N * vc * 2);
@@ -562,7 +565,7 @@ size_t linear_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D) { return bwd_
 
 cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
     const BwdLayout L = bwd_layout(a.N, a.V, a.D);
-    const int64_t vc = chunk_cols(a.V);
+    const int64_t vc = chunk_cols(a.N, a.V);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     __nv_bfloat16 *dz = reinterpret_cast<__nv_bfloat16 *>(ws + L.dz);
     float *acc = reinterpret_cast<float *>(ws + L.acc);
