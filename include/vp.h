@@ -208,6 +208,42 @@ VP_API vp_status vp_kl_bwd(const void *a, const void *b, int dtype, int64_t N, i
                            vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* Generalized Jensen-Shannon divergence [P1, the commit message that adds   */
+/* vocab_parallel_jsd: "Changes", "Scope and limitations"]                   */
+/* ------------------------------------------------------------------------ */
+
+/* With p = softmax of a row of A (the student, first argument), q = softmax
+ * of the row of B (the teacher) and mix = beta q + (1 - beta) p:
+ *   0 < beta < 1:  JSD = beta KL(q || mix) + (1 - beta) KL(p || mix)
+ *                  (the page names a GKD-style interior divergence of two
+ *                  KL-to-mixture expectations; this formula is the reading
+ *                  taken where it prints none);
+ *   beta = 0:      KL(B || A), the same call as vp_kl_fwd with VP_KL_FORWARD;
+ *   beta = 1:      KL(A || B), the same call as vp_kl_fwd with VP_KL_REVERSE
+ *                  (explicit endpoint branches, as on the page).
+ * Interior beta reads A and B twice: the first pass takes each row's (m,
+ * logS) of A and of B, the second reduces the two KL-to-mixture expectations
+ * together. beta is used in fp32. Outputs: jsd fp32 [N] and the records of A
+ * and of B (vp_rowstat [N] each, required); for interior beta their c fields
+ * hold KL(p || mix) and KL(q || mix). A row with a NaN or +inf, or without a
+ * finite logit, in A or B gives NaN; otherwise the interior divergence is
+ * finite (there is no support mismatch). beta outside [0, 1] or NaN:
+ * VP_ERR_ARG. A and B share one row layout and dtype. */
+VP_API vp_status vp_jsd_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                            int64_t s_i, double beta, float *jsd, vp_rowstat *stats_a, vp_rowstat *stats_b,
+                            vp_stream stream);
+
+/* Gradients for interior beta, from the records of vp_jsd_fwd with the same beta:
+ *   dA_j = g (1 - beta) p_j ((log p_j - log mix_j) - KL(p || mix)),
+ *   dB_j = g beta q_j ((log q_j - log mix_j) - KL(q || mix)),
+ * exactly 0 where p_j = 0 (q_j = 0); at beta = 0 and 1, vp_kl_bwd with the
+ * matching direction. da and db are contiguous [N, V] in the inputs' dtype;
+ * either may be NULL (a frozen teacher or student), not both. */
+VP_API vp_status vp_jsd_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                            int64_t s_i, double beta, const vp_rowstat *stats_a, const vp_rowstat *stats_b,
+                            const float *grad_out, void *da, void *db, vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Vocabulary-sharded (tensor-parallel) forms [P1, second commit message and */
 /* the reviewer's suggested change: each rank reduces its own shard's max,   */
 /* sum-exp and centred weighted sum, and the shards are combined by          */

@@ -113,3 +113,13 @@ def test_sharded_entry_points_check_arguments_on_the_host():
     assert lib.vp_logprobs_partial(FAKE, 1, 4, 16, 4, 0, 16, 0, FAKE, FAKE_ODD, None) == ERR_ALIGN
     assert lib.vp_kl_partial(FAKE, FAKE, 1, 4, 16, 4, 0, 16, 3, FAKE, None) == ERR_ARG
     assert lib.vp_kl_partial(FAKE, FAKE, 1, 4, 16, 4, -1, 16, 0, FAKE, None) == ERR_LAYOUT
+
+
+def test_jsd_entry_points_check_beta_first():
+    lib = _lib.lib()
+    for beta in (-0.1, 1.5, float("nan")):
+        assert lib.vp_jsd_fwd(FAKE, FAKE, 1, 4, 16, 4, 0, 16, beta, FAKE, FAKE, FAKE, None) == ERR_ARG
+        assert lib.vp_jsd_bwd(FAKE, FAKE, 1, 4, 16, 4, 0, 16, beta, FAKE, FAKE, FAKE, FAKE, FAKE, None) == ERR_ARG
+    assert lib.vp_jsd_fwd(FAKE, FAKE, 7, 4, 16, 4, 0, 16, 0.5, FAKE, FAKE, FAKE, None) == ERR_DTYPE
+    assert lib.vp_jsd_bwd(FAKE, FAKE, 1, 4, 16, 4, 0, 16, 0.5, FAKE, FAKE, FAKE, None, None, None) == ERR_ARG
+    assert lib.vp_jsd_fwd(FAKE, FAKE, 1, 4, 16, 4, 0, 16, 0.5, FAKE_ODD, FAKE, FAKE, None) == ERR_ALIGN

@@ -27,6 +27,8 @@ SIGNATURES = {
     "vp_linear_logp_fwd": [P, P, I64, I64, I64, I64, P, P, P, P, ctypes.c_size_t, P, P],
     "vp_linear_logp_fwd_noalloc": [P, P, I64, I64, I64, I64, P, P, P, P, P],
     "vp_linear_logp_bwd": [P, P, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_size_t, P, P],
+    "vp_jsd_fwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P],
+    "vp_jsd_bwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P],
     "vp_logprobs_partial": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P],
     "vp_entropy_partial": [P, I32, I64, I64, I64, I64, I64, P, P],
     "vp_kl_partial": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P],

@@ -173,6 +173,35 @@ def vp_kl_bwd(a, b, direction, stats_a, stats_b, grad, want_da=True, want_db=Tru
     return da, db
 
 
+def vp_jsd_fwd(a, b, beta: float = 0.5, jsd=None, stats_a=None, stats_b=None):
+    """Generalized JSD per row (a: student, b: teacher); beta = 0 / 1 are KL(b||a) / KL(a||b).
+
+    Returns (jsd fp32 [N], stats of a, stats of b)."""
+    _same_layout(a, b)
+    N, V, R, s_o, s_i = rows_of(a)
+    jsd = _f32(N, a) if jsd is None else jsd
+    stats_a = rowstats(N, a.device) if stats_a is None else stats_a
+    stats_b = rowstats(N, a.device) if stats_b is None else stats_b
+    _check(_lib.lib().vp_jsd_fwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, float(beta), _ptr(jsd),
+                                 _ptr(stats_a), _ptr(stats_b), _stream()), "vp_jsd_fwd")
+    return jsd, stats_a, stats_b
+
+
+def vp_jsd_bwd(a, b, beta, stats_a, stats_b, grad, want_da=True, want_db=True, da=None, db=None):
+    """Returns (da, db); an unwanted gradient (a frozen input) is None and is not computed."""
+    _same_layout(a, b)
+    N, V, R, s_o, s_i = rows_of(a)
+    if want_da and da is None:
+        da = torch.empty((N, V), dtype=a.dtype, device=a.device)
+    if want_db and db is None:
+        db = torch.empty((N, V), dtype=a.dtype, device=a.device)
+    da = da if want_da else None
+    db = db if want_db else None
+    _check(_lib.lib().vp_jsd_bwd(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, float(beta), _ptr(stats_a),
+                                 _ptr(stats_b), _ptr(grad), _ptr(da), _ptr(db), _stream()), "vp_jsd_bwd")
+    return da, db
+
+
 def vp_linear_logp_workspace_size(N: int, V: int, D: int) -> int:
     return int(_lib.lib().vp_linear_logp_workspace_size(N, V, D))
 

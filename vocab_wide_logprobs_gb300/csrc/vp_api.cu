@@ -136,6 +136,50 @@ vp_status vp_kl_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t 
 }
 
 // ---------------------------------------------------------------------------
+// Generalized JSD
+// ---------------------------------------------------------------------------
+vp_status vp_jsd_fwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                     int64_t s_i, double beta, float *jsd, vp_rowstat *stats_a, vp_rowstat *stats_b,
+                     vp_stream stream) {
+    if (!(beta >= 0.0 && beta <= 1.0)) return VP_ERR_ARG;
+    if (beta == 0.0) return vp_kl_fwd(a, b, dtype, N, V, R, s_o, s_i, VP_KL_FORWARD, jsd, stats_a, stats_b, stream);
+    if (beta == 1.0) return vp_kl_fwd(a, b, dtype, N, V, R, s_o, s_i, VP_KL_REVERSE, jsd, stats_a, stats_b, stream);
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!a || !b || !jsd || !stats_a || !stats_b) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(jsd, 4) || !aligned(stats_a, 16) || !aligned(stats_b, 16))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::JsdFwdArgs k{a, b, dtype == VP_BF16, N, V, R, s_o, s_i, beta, jsd, stats_a, stats_b, (cudaStream_t)stream};
+    return launched(vp::launch_jsd_fwd(k));
+}
+
+vp_status vp_jsd_bwd(const void *a, const void *b, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                     int64_t s_i, double beta, const vp_rowstat *stats_a, const vp_rowstat *stats_b,
+                     const float *grad_out, void *da, void *db, vp_stream stream) {
+    if (!(beta >= 0.0 && beta <= 1.0)) return VP_ERR_ARG;
+    if (beta == 0.0)
+        return vp_kl_bwd(a, b, dtype, N, V, R, s_o, s_i, VP_KL_FORWARD, stats_a, stats_b, grad_out, da, db, stream);
+    if (beta == 1.0)
+        return vp_kl_bwd(a, b, dtype, N, V, R, s_o, s_i, VP_KL_REVERSE, stats_a, stats_b, grad_out, da, db, stream);
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (N == 0) return VP_OK;
+    if (!da && !db) return VP_ERR_ARG;
+    if (!a || !b || !stats_a || !stats_b || !grad_out) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(a, es) || !aligned(b, es) || !aligned(da, es) || !aligned(db, es) || !aligned(stats_a, 16) ||
+        !aligned(stats_b, 16) || !aligned(grad_out, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::JsdBwdArgs k{a, b, dtype == VP_BF16, N, V, R, s_o, s_i, beta, stats_a, stats_b, grad_out, da, db,
+                     (cudaStream_t)stream};
+    return launched(vp::launch_jsd_bwd(k));
+}
+
+// ---------------------------------------------------------------------------
 // Vocabulary-sharded forms
 // ---------------------------------------------------------------------------
 vp_status vp_logprobs_partial(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,

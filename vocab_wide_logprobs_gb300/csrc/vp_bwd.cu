@@ -17,6 +17,8 @@
 //   KL(P||Q)  dP_j = g p_j (log p_j - log q_j - KL)
 //                  = g p_j ((t^P_j - t^Q_j) - c)                       (0 where p_j = 0)
 //             dQ_j = g (q_j - p_j)
+//   JSD       dA_j = g (1 - beta) p_j ((log p_j - log mix_j) - KL(p || mix))
+//             dB_j = g beta q_j ((log q_j - log mix_j) - KL(q || mix)), mix = beta q + (1 - beta) p
 // m is the exact row max, so t_j is exact; logS and c arrive as hi + lo pairs.
 // The fp32 path uses both halves and an error-free difference t^P - t^Q, so a
 // gradient that cancels to near zero keeps its accuracy; the bf16 path uses
@@ -218,92 +220,177 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
 }
 
 // --------------------------------------------------------------------------
-// KL(P||Q): dP and / or dQ
+// Paired inputs (KL, generalized JSD): dP and / or dQ. The per-row policy
+// Row gives the NaN state of the row and the element formula.
 // --------------------------------------------------------------------------
+// KL(P||Q). NaN row (NaN / +inf anywhere, or no finite P logit): both
+// gradients NaN; support mismatch (KL = +inf): dP is NaN, dQ = g (q - p)
+// stays finite.
+template <typename T>
+struct KLGradRow {
+    RowStat sp, sq;
+    float g;
+    bool all_nan, p_nan;
+    __device__ __forceinline__ KLGradRow(const RowStat *stats_p, const RowStat *stats_q, const float *g_in,
+                                         int64_t r) {
+        sp = load_rowstat(stats_p + r);
+        sq = load_rowstat(stats_q + r);
+        g = g_in[r];
+        all_nan = (sp.flags & (kRowNanInf | kRowEmpty)) || (sq.flags & kRowNanInf);
+        p_nan = all_nan || (sp.flags & kRowMismatch);
+    }
+    template <bool kDP, bool kDQ>
+    __device__ __forceinline__ void elem(float zp, float zq, float &dp, float &dq) const {
+        kl_grad_elem<T, kDP, kDQ>(zp, zq, sp, sq, g, p_nan, dp, dq);
+    }
+};
+
+// Generalized JSD with interior beta, (P, Q) = (A, B), mix = beta q + (1 - beta) p:
+//   dA_j = g (1 - beta) p_j ((log p_j - log mix_j) - KL(p || mix)),
+//   dB_j = g beta q_j ((log q_j - log mix_j) - KL(q || mix)),
+// exactly 0 where p_j = 0 (q_j = 0); the KL-to-mixture values are the c fields
+// of the forward's records. Rows with a NaN / +inf or no finite logit in A or
+// B give NaN rows.
+template <typename T>
+struct JSDGradRow {
+    float ma, mb, la_hi, la_lo, lb_hi, lb_lo, ka, kb, beta, omb, ga, gb;
+    bool all_nan;
+    static constexpr bool p_nan = false;
+    __device__ __forceinline__ JSDGradRow(const RowStat *stats_a, const RowStat *stats_b, const float *g_in,
+                                          int64_t r, float beta_) {
+        const RowStat sa = load_rowstat(stats_a + r), sb = load_rowstat(stats_b + r);
+        ma = sa.m; mb = sb.m;
+        la_hi = sa.logS_hi; la_lo = sa.logS_lo; lb_hi = sb.logS_hi; lb_lo = sb.logS_lo;
+        ka = sa.c_hi + sa.c_lo;
+        kb = sb.c_hi + sb.c_lo;
+        beta = beta_;
+        omb = 1.f - beta_;
+        const float g = g_in[r];
+        ga = g * omb;
+        gb = g * beta_;
+        all_nan = ((sa.flags | sb.flags) & (kRowNanInf | kRowEmpty)) != 0;
+    }
+    template <bool kDP, bool kDQ>
+    __device__ __forceinline__ void elem(float za, float zb, float &da, float &db) const {
+        if constexpr (Elem<T>::kPrecise) {
+            const float lp = ((za - ma) - la_hi) - la_lo, lq = ((zb - mb) - lb_hi) - lb_lo;   // z - m exact
+            const float p = expf(lp), q = expf(lq);
+            const float lmix = logf(fmaf(beta, q, omb * p));
+            if (kDP) da = (p > 0.f) ? ga * p * ((lp - lmix) - ka) : 0.f;
+            if (kDQ) db = (q > 0.f) ? gb * q * ((lq - lmix) - kb) : 0.f;
+        } else {
+            constexpr float kLn2f = 0.6931471805599453f;
+            const float xa = fmaf(za - ma, kLog2e, -(la_hi + la_lo) * kLog2e);   // log2 p
+            const float xb = fmaf(zb - mb, kLog2e, -(lb_hi + lb_lo) * kLog2e);
+            float p, q;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(xa));
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(q) : "f"(xb));
+            float lm;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lm) : "f"(fmaf(beta, q, omb * p)));
+            lm = fmaxf(lm, -250.f);
+            if (kDP) da = (p > 0.f) ? ga * p * fmaf(xa - lm, kLn2f, -ka) : 0.f;
+            if (kDQ) db = (q > 0.f) ? gb * q * fmaf(xb - lm, kLn2f, -kb) : 0.f;
+        }
+    }
+};
+
+template <typename T, bool kDP, bool kDQ, class Row>
+__device__ __forceinline__ void pair_grad_tile(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,
+                                               const Row &row, int64_t r, int seg, T *__restrict__ dP,
+                                               T *__restrict__ dQ) {
+    constexpr int kVec = Elem<T>::kVec;
+    const int tid = threadIdx.x;
+    const int64_t off = rows.off(r);
+    const T *prow = P + off, *qrow = Q + off;
+    T *dprow = kDP ? dP + r * (int64_t)V : nullptr;
+    T *dqrow = kDQ ? dQ + r * (int64_t)V : nullptr;
+    const bool all_nan = row.all_nan;
+    const bool p_nan = row.p_nan;
+
+    uintptr_t ph = (uintptr_t)prow & 15u;
+    bool vec = (((uintptr_t)qrow & 15u) == ph);
+    if (kDP) vec = vec && (((uintptr_t)dprow & 15u) == ph);
+    if (kDQ) vec = vec && (((uintptr_t)dqrow & 15u) == ph);
+
+    auto scalar_range = [&](int64_t j0, int64_t j1) {
+        for (int64_t j = j0 + tid; j < j1; j += kBwdThreads) {
+            float dp = qnan(), dq = qnan();
+            if (!all_nan) row.template elem<kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), dp, dq);
+            if (kDP) Elem<T>::store1(dprow + j, dp);
+            if (kDQ) Elem<T>::store1(dqrow + j, dq);
+        }
+    };
+
+    if (vec) {
+        const int head = head_count(prow, V);
+        const int nv = (V - head) / kVec;
+        const int tail0 = head + nv * kVec;
+        if (seg == 0) {
+            scalar_range(0, head);
+            scalar_range(tail0, V);
+        }
+        const int v0 = seg * kTileVec;
+        const int v1 = min(nv, v0 + kTileVec);
+        const uint4 *vp = reinterpret_cast<const uint4 *>(prow + head);
+        const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + head);
+        uint4 *vdp = kDP ? reinterpret_cast<uint4 *>(dprow + head) : nullptr;
+        uint4 *vdq = kDQ ? reinterpret_cast<uint4 *>(dqrow + head) : nullptr;
+        if (all_nan || (kDP && !kDQ && p_nan)) {
+            const uint4 c = splat<T>(qnan());
+            for (int i = v0 + tid; i < v1; i += kBwdThreads) {
+                if (kDP) stg_stream(vdp + i, c);
+                if (kDQ) stg_stream(vdq + i, c);
+            }
+            return;
+        }
+        uint4 up[kBwdVecPerThread], uq[kBwdVecPerThread];
+#pragma unroll
+        for (int k = 0; k < kBwdVecPerThread; ++k) {
+            const int i = v0 + tid + k * kBwdThreads;
+            if (i < v1) { up[k] = ldg_stream(vp + i); uq[k] = ldg_stream(vq + i); }
+        }
+#pragma unroll
+        for (int k = 0; k < kBwdVecPerThread; ++k) {
+            const int i = v0 + tid + k * kBwdThreads;
+            if (i < v1) {
+                float zp[kVec], zq[kVec], dp[kVec], dq[kVec];
+                Elem<T>::unpack(up[k], zp);
+                Elem<T>::unpack(uq[k], zq);
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) row.template elem<kDP, kDQ>(zp[e], zq[e], dp[e], dq[e]);
+                if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
+                if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
+            }
+        }
+    } else {
+        const int64_t e0 = (int64_t)seg * kTileVec * kVec;
+        scalar_range(e0, min((int64_t)V, e0 + (int64_t)kTileVec * kVec));
+    }
+}
+
 template <typename T, bool kDP, bool kDQ>
 __global__ void __launch_bounds__(kBwdThreads)
 kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,
                const RowStat *__restrict__ stats_p, const RowStat *__restrict__ stats_q,
                const float *__restrict__ g_in, T *__restrict__ dP, T *__restrict__ dQ, int tiles_per_row,
                int64_t total_tiles) {
-    constexpr int kVec = Elem<T>::kVec;
-    const int tid = threadIdx.x;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         const int64_t r = tile / tiles_per_row;
-        const int seg = (int)(tile - r * tiles_per_row);
-        const int64_t off = rows.off(r);
-        const T *prow = P + off, *qrow = Q + off;
-        T *dprow = kDP ? dP + r * (int64_t)V : nullptr;
-        T *dqrow = kDQ ? dQ + r * (int64_t)V : nullptr;
-        const RowStat sp = load_rowstat(stats_p + r), sq = load_rowstat(stats_q + r);
-        const float g = g_in[r];
-        // NaN row (NaN / +inf anywhere, or no finite P logit): both gradients NaN;
-        // support mismatch (KL = +inf): dP is NaN, dQ = g (q - p) stays finite
-        const bool all_nan = (sp.flags & (kRowNanInf | kRowEmpty)) || (sq.flags & kRowNanInf);
-        const bool p_nan = all_nan || (sp.flags & kRowMismatch);
+        const KLGradRow<T> row(stats_p, stats_q, g_in, r);
+        pair_grad_tile<T, kDP, kDQ>(P, Q, V, rows, row, r, (int)(tile - r * tiles_per_row), dP, dQ);
+    }
+}
 
-        uintptr_t ph = (uintptr_t)prow & 15u;
-        bool vec = (((uintptr_t)qrow & 15u) == ph);
-        if (kDP) vec = vec && (((uintptr_t)dprow & 15u) == ph);
-        if (kDQ) vec = vec && (((uintptr_t)dqrow & 15u) == ph);
-
-        auto scalar_range = [&](int64_t j0, int64_t j1) {
-            for (int64_t j = j0 + tid; j < j1; j += kBwdThreads) {
-                float dp = qnan(), dq = qnan();
-                if (!all_nan)
-                    kl_grad_elem<T, kDP, kDQ>(Elem<T>::load1(prow + j), Elem<T>::load1(qrow + j), sp, sq, g, p_nan,
-                                              dp, dq);
-                if (kDP) Elem<T>::store1(dprow + j, dp);
-                if (kDQ) Elem<T>::store1(dqrow + j, dq);
-            }
-        };
-
-        if (vec) {
-            const int head = head_count(prow, V);
-            const int nv = (V - head) / kVec;
-            const int tail0 = head + nv * kVec;
-            if (seg == 0) {
-                scalar_range(0, head);
-                scalar_range(tail0, V);
-            }
-            const int v0 = seg * kTileVec;
-            const int v1 = min(nv, v0 + kTileVec);
-            const uint4 *vp = reinterpret_cast<const uint4 *>(prow + head);
-            const uint4 *vq = reinterpret_cast<const uint4 *>(qrow + head);
-            uint4 *vdp = kDP ? reinterpret_cast<uint4 *>(dprow + head) : nullptr;
-            uint4 *vdq = kDQ ? reinterpret_cast<uint4 *>(dqrow + head) : nullptr;
-            if (all_nan || (kDP && !kDQ && p_nan)) {
-                const uint4 c = splat<T>(qnan());
-                for (int i = v0 + tid; i < v1; i += kBwdThreads) {
-                    if (kDP) stg_stream(vdp + i, c);
-                    if (kDQ) stg_stream(vdq + i, c);
-                }
-                continue;
-            }
-            uint4 up[kBwdVecPerThread], uq[kBwdVecPerThread];
-#pragma unroll
-            for (int k = 0; k < kBwdVecPerThread; ++k) {
-                const int i = v0 + tid + k * kBwdThreads;
-                if (i < v1) { up[k] = ldg_stream(vp + i); uq[k] = ldg_stream(vq + i); }
-            }
-#pragma unroll
-            for (int k = 0; k < kBwdVecPerThread; ++k) {
-                const int i = v0 + tid + k * kBwdThreads;
-                if (i < v1) {
-                    float zp[kVec], zq[kVec], dp[kVec], dq[kVec];
-                    Elem<T>::unpack(up[k], zp);
-                    Elem<T>::unpack(uq[k], zq);
-#pragma unroll
-                    for (int e = 0; e < kVec; ++e)
-                        kl_grad_elem<T, kDP, kDQ>(zp[e], zq[e], sp, sq, g, p_nan, dp[e], dq[e]);
-                    if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
-                    if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
-                }
-            }
-        } else {
-            const int64_t e0 = (int64_t)seg * kTileVec * kVec;
-            scalar_range(e0, min((int64_t)V, e0 + (int64_t)kTileVec * kVec));
-        }
+template <typename T, bool kDA, bool kDB>
+__global__ void __launch_bounds__(kBwdThreads)
+jsd_grad_kernel(const T *__restrict__ A, const T *__restrict__ B, int V, Rows rows, float beta,
+                const RowStat *__restrict__ stats_a, const RowStat *__restrict__ stats_b,
+                const float *__restrict__ g_in, T *__restrict__ dA, T *__restrict__ dB, int tiles_per_row,
+                int64_t total_tiles) {
+    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        const int64_t r = tile / tiles_per_row;
+        const JSDGradRow<T> row(stats_a, stats_b, g_in, r, beta);
+        pair_grad_tile<T, kDA, kDB>(A, B, V, rows, row, r, (int)(tile - r * tiles_per_row), dA, dB);
     }
 }
 
@@ -359,6 +446,30 @@ static cudaError_t launch_kl_grad_dt(const KLBwdArgs &a) {
 
 cudaError_t launch_kl_bwd(const KLBwdArgs &a) {
     return a.bf16 ? launch_kl_grad_dt<__nv_bfloat16>(a) : launch_kl_grad_dt<float>(a);
+}
+
+template <typename T, bool kDA, bool kDB>
+static cudaError_t launch_jsd_grad_t(const JsdBwdArgs &a) {
+    int tpr;
+    int64_t total;
+    unsigned grid;
+    tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
+    jsd_grad_kernel<T, kDA, kDB><<<grid, kBwdThreads, 0, a.stream>>>(
+        static_cast<const T *>(a.a), static_cast<const T *>(a.b), (int)a.V, Rows{a.R, a.s_o, a.s_i}, (float)a.beta,
+        static_cast<const RowStat *>(a.stats_a), static_cast<const RowStat *>(a.stats_b), a.g,
+        static_cast<T *>(a.da), static_cast<T *>(a.db), tpr, total);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_jsd_grad_dt(const JsdBwdArgs &a) {
+    if (a.da && a.db) return launch_jsd_grad_t<T, true, true>(a);
+    if (a.da) return launch_jsd_grad_t<T, true, false>(a);
+    return launch_jsd_grad_t<T, false, true>(a);
+}
+
+cudaError_t launch_jsd_bwd(const JsdBwdArgs &a) {
+    return a.bf16 ? launch_jsd_grad_dt<__nv_bfloat16>(a) : launch_jsd_grad_dt<float>(a);
 }
 
 }  // namespace vp

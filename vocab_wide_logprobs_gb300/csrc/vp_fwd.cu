@@ -116,6 +116,32 @@ kl_fwd_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows
 }
 
 // ---------------------------------------------------------------------------
+// Generalized JSD, second pass, when A and B do not share their address modulo
+// 16: one CTA per row, element by element (vp_stats.cuh, LaneJSD::push).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kFwdThreads)
+jsd_fwd_kernel(const T *__restrict__ A, const T *__restrict__ B, int V, Rows rows, float beta,
+               float *__restrict__ jsd, RowStat *__restrict__ stats_a, RowStat *__restrict__ stats_b) {
+    const int64_t r = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int64_t off = rows.off(r);
+    const T *arow = A + off, *brow = B + off;
+    const JsdRow c = jsd_row_constants(load_rowstat(stats_a + r), load_rowstat(stats_b + r), beta);
+    LaneJSD<T> acc;
+    acc.init();
+    for (int j = tid; j < V; j += kFwdThreads) {
+        float a[1] = {Elem<T>::load1(arow + j)}, b[1] = {Elem<T>::load1(brow + j)};
+        acc.push(a, b, c);
+    }
+    __shared__ PartJSD<AccT<T>> parts[kFwdWarps];
+    const PartJSD<AccT<T>> w = jsd_warp_merge(acc);
+    if ((tid & 31) == 0) parts[tid >> 5] = w;
+    __syncthreads();
+    if (tid == 0) finish_jsd(parts, kFwdWarps, r, (double)beta, jsd, stats_a, stats_b);
+}
+
+// ---------------------------------------------------------------------------
 // Launchers (called by the C ABI after argument checks).
 // ---------------------------------------------------------------------------
 template <typename T>
@@ -128,6 +154,18 @@ static cudaError_t launch_kl_t(const KLFwdArgs &a) {
 
 cudaError_t launch_kl_fwd_rowwise(const KLFwdArgs &a) {
     return a.bf16 ? launch_kl_t<__nv_bfloat16>(a) : launch_kl_t<float>(a);
+}
+
+template <typename T>
+static cudaError_t launch_jsd_rowwise_t(const JsdFwdArgs &a) {
+    jsd_fwd_kernel<T><<<(unsigned)a.N, kFwdThreads, 0, a.stream>>>(
+        static_cast<const T *>(a.a), static_cast<const T *>(a.b), (int)a.V, Rows{a.R, a.s_o, a.s_i}, (float)a.beta,
+        a.jsd, static_cast<RowStat *>(a.stats_a), static_cast<RowStat *>(a.stats_b));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_jsd_fwd_rowwise(const JsdFwdArgs &a) {
+    return a.bf16 ? launch_jsd_rowwise_t<__nv_bfloat16>(a) : launch_jsd_rowwise_t<float>(a);
 }
 
 }  // namespace vp

@@ -398,6 +398,132 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
 }
 
 // ---------------------------------------------------------------------------
+// Generalized JSD, second pass: KL(p || mix) and KL(q || mix) per row from a
+// second read of A and B, with the first pass's records (vp_stats.cuh). A and
+// B share their address modulo 16 (checked by the launcher).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kTmaThreads, kCtasPerSm)
+jsd_fwd_tma_kernel(const T *__restrict__ A, const T *__restrict__ B, int64_t N, int V, Rows rows, float beta,
+                   float *__restrict__ jsd, RowStat *__restrict__ stats_a, RowStat *__restrict__ stats_b) {
+    constexpr int kVec = Elem<T>::kVec;
+    constexpr int kHalf = kStageBytes / 2;                      // A and B halves of a stage
+    constexpr int kChunkVec = kHalf / 16;
+    constexpr int kPerThread = kChunkVec / kTmaConsumers;
+    extern __shared__ __align__(128) uint8_t ring_mem[];
+    __shared__ Ring ring;
+    __shared__ PartJSD<AccT<T>> parts[2][kTmaConsumerWarps];
+    ring_init(ring);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == kFinisherWarp) {
+        int rowi = 0;
+        for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
+            const int slot = rowi & 1;
+            if (!mbar_wait(&ring.parts_full[slot], (rowi >> 1) & 1)) {
+                atomicOr(&g_tma_fault, 2u);
+                return;
+            }
+            __syncwarp();
+            if (lane == 0) finish_jsd(parts[slot], kTmaConsumerWarps, r, (double)beta, jsd, stats_a, stats_b);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ring.parts_empty[slot]);
+        }
+        return;
+    }
+    if (warp == kProducerWarp) {
+        if (lane != 0) return;
+        const uint64_t pol = policy_evict_first();
+        uint32_t it = 0;
+        for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
+            const int64_t off = rows.off(r);
+            const T *arow = A + off, *brow = B + off;
+            const int head = head_count(arow, V);
+            const int nv = (V - head) / kVec;
+            const uint8_t *ab = reinterpret_cast<const uint8_t *>(arow + head);
+            const uint8_t *bb = reinterpret_cast<const uint8_t *>(brow + head);
+            for (int c0 = 0; c0 < nv; c0 += kChunkVec, ++it) {
+                uint32_t st;
+                if (!acquire_stage(ring, it, st)) { drain(ring, it); return; }
+                const uint32_t bytes = (uint32_t)min(kChunkVec, nv - c0) * 16u;
+                mbar_arrive_expect_tx(&ring.full[st], 2u * bytes);
+                uint8_t *dst = ring_mem + st * kStageBytes;
+                bulk_g2s(dst, ab + (int64_t)c0 * 16, bytes, &ring.full[st], pol);
+                bulk_g2s(dst + kHalf, bb + (int64_t)c0 * 16, bytes, &ring.full[st], pol);
+            }
+        }
+        return;
+    }
+
+    const int ct = threadIdx.x;
+    RingPos pos;
+    bool ok = true;
+    int rowi = 0;
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x, ++rowi) {
+        const int64_t off = rows.off(r);
+        const T *arow = A + off, *brow = B + off;
+        const int head = head_count(arow, V);
+        const int nv = (V - head) / kVec;
+        const int tail0 = head + nv * kVec;
+        const JsdRow c = jsd_row_constants(load_rowstat(stats_a + r), load_rowstat(stats_b + r), beta);
+        LaneJSD<T> acc;
+        acc.init();
+        for (int c0 = 0; c0 < nv; c0 += kChunkVec, pos.next()) {
+            const uint32_t st = pos.st;
+            if (ok && !mbar_wait(&ring.full[st], pos.ph)) {
+                ok = false;
+                atomicOr(&g_tma_fault, 2u);
+            }
+            const int cnt = min(kChunkVec, nv - c0);
+            const uint4 *sa = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes);
+            const uint4 *sb = reinterpret_cast<const uint4 *>(ring_mem + st * kStageBytes + kHalf);
+            const uint4 pad = splat_neg_inf<T>();
+            uint4 ua[kPerThread], ub[kPerThread];
+            if (cnt == kChunkVec) {
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    ua[k] = sa[ct + k * kTmaConsumers];
+                    ub[k] = sb[ct + k * kTmaConsumers];
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    const int i = ct + k * kTmaConsumers;
+                    ua[k] = i < cnt ? sa[i] : pad;
+                    ub[k] = i < cnt ? sb[i] : pad;
+                }
+            }
+            release_stage(ring, st, lane);
+            if constexpr (Elem<T>::kPrecise) {
+                float a[kPerThread * kVec], b[kPerThread * kVec];
+#pragma unroll
+                for (int k = 0; k < kPerThread; ++k) {
+                    Elem<T>::unpack(ua[k], a + k * kVec);
+                    Elem<T>::unpack(ub[k], b + k * kVec);
+                }
+                acc.push(a, b, c);
+            } else {
+                acc.push_bf16(ua, ub, c);
+            }
+        }
+        if (ct < head) {
+            float a[1] = {Elem<T>::load1(arow + ct)}, b[1] = {Elem<T>::load1(brow + ct)};
+            acc.push(a, b, c);
+        }
+        if (ct < V - tail0) {
+            float a[1] = {Elem<T>::load1(arow + tail0 + ct)}, b[1] = {Elem<T>::load1(brow + tail0 + ct)};
+            acc.push(a, b, c);
+        }
+        PartJSD<AccT<T>> w = jsd_warp_merge(acc);
+        if (!ok) w.ka = AccT<T>(__int_as_float(0x7fc00000));   // a timed-out row finishes as NaN
+        if (!hand_over(ring, parts, rowi, w, warp, lane)) {
+            atomicOr(&g_tma_fault, 2u);
+            return;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
 static int sm_count() {
@@ -467,6 +593,27 @@ cudaError_t launch_kl_fwd(const KLFwdArgs &a) {
     // element-wise CTA-per-row kernel reads them
     if ((((uintptr_t)a.p ^ (uintptr_t)a.q) & 15u) != 0) return launch_kl_fwd_rowwise(a);
     return a.bf16 ? launch_kl_tma<__nv_bfloat16>(a) : launch_kl_tma<float>(a);
+}
+
+template <typename T>
+static cudaError_t launch_jsd_pass2(const JsdFwdArgs &a) {
+    static std::atomic<uint64_t> done{0};
+    auto k = jsd_fwd_tma_kernel<T>;
+    cudaError_t e = allow_ring(k, done);
+    if (e != cudaSuccess) return e;
+    k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
+        static_cast<const T *>(a.a), static_cast<const T *>(a.b), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i},
+        (float)a.beta, a.jsd, static_cast<RowStat *>(a.stats_a), static_cast<RowStat *>(a.stats_b));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_jsd_fwd(const JsdFwdArgs &a) {
+    // first pass: each row's (m, logS) of A and of B, the KL scan without its output
+    KLFwdArgs k{a.a, a.b, a.bf16, a.N, a.V, a.R, a.s_o, a.s_i, nullptr, a.stats_a, a.stats_b, a.stream};
+    cudaError_t e = launch_kl_fwd(k);
+    if (e != cudaSuccess) return e;
+    if ((((uintptr_t)a.a ^ (uintptr_t)a.b) & 15u) != 0) return launch_jsd_fwd_rowwise(a);
+    return a.bf16 ? launch_jsd_pass2<__nv_bfloat16>(a) : launch_jsd_pass2<float>(a);
 }
 
 cudaError_t read_fault(uint32_t *value, bool clear) {

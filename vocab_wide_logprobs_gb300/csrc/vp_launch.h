@@ -41,6 +41,32 @@ struct MergeArgs {
     cudaStream_t stream;
 };
 
+// Generalized JSD with interior beta: A is the first argument (p), B the second (q).
+struct JsdFwdArgs {
+    const void *a, *b;
+    bool bf16;
+    int64_t N, V, R, s_o, s_i;
+    double beta;
+    float *jsd;
+    void *stats_a, *stats_b;  // vp_rowstat [N] each; c = KL(p || mix) / KL(q || mix)
+    cudaStream_t stream;
+};
+
+struct JsdBwdArgs {
+    const void *a, *b;
+    bool bf16;
+    int64_t N, V, R, s_o, s_i;
+    double beta;
+    const void *stats_a, *stats_b;
+    const float *g;
+    void *da, *db;  // either may be NULL
+    cudaStream_t stream;
+};
+
+cudaError_t launch_jsd_fwd(const JsdFwdArgs &a);
+cudaError_t launch_jsd_fwd_rowwise(const JsdFwdArgs &a);
+cudaError_t launch_jsd_bwd(const JsdBwdArgs &a);
+
 cudaError_t launch_logprobs_merge(const MergeArgs &a);
 cudaError_t launch_entropy_merge(const MergeArgs &a);
 cudaError_t launch_kl_merge(const MergeArgs &a);

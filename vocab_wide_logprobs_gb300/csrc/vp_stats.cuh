@@ -522,7 +522,162 @@ __device__ __forceinline__ void finish_kl(const PartKL<Acc> &s, int64_t r, float
     if ((fp & (kRowNanInf | kRowEmpty)) || (fq & kRowNanInf)) res = qnan();
     else if (fp & kRowMismatch) res = pinf();
     else res = (float)(c - logSp + logSq);
-    kl[r] = res;
+    if (kl) kl[r] = res;   // NULL: the records only (first pass of the JSD)
+}
+
+// ---------------------------------------------------------------------------
+// Generalized JSD, second pass ([P1] commit message adding vocab_parallel_jsd:
+// "reuse global normalization and reduce the two KL-to-mixture expectations
+// together"). With the rows' (m, logS) of A and B from the first pass, the two
+// expectations are plain sums, no centre needed:
+//   KL(p || mix) = sum p (log p - log mix),  KL(q || mix) = sum q (log q - log mix),
+//   mix = beta q + (1 - beta) p,
+// accumulated in base-2 units (log2 p, log2 mix) and scaled by ln 2 at the end.
+// ---------------------------------------------------------------------------
+struct JsdRow {
+    float ma, mb;                         // exact row maxima of A and B
+    float la_hi, la_lo, lb_hi, lb_lo;     // logS of A and B
+    float beta, omb;                      // beta, 1 - beta
+};
+
+__device__ __forceinline__ JsdRow jsd_row_constants(const RowStat &sa, const RowStat &sb, float beta) {
+    return JsdRow{sa.m, sb.m, sa.logS_hi, sa.logS_lo, sb.logS_hi, sb.logS_lo, beta, 1.f - beta};
+}
+
+__device__ __forceinline__ float lg2_fast(float a) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a));
+    return y;
+}
+
+template <typename T>
+struct LaneJSD {
+    DF ka, kb;   // base-2 units
+
+    __device__ __forceinline__ void init() { ka = kb = DF{0.f, 0.f}; }
+
+    // Scalar path. fp32 inputs: accurate exponentials and logarithms,
+    // double-float sums. bf16 (the unaligned head and tail of a row): the
+    // hardware base-2 forms of the fast path.
+    template <int n>
+    __device__ __forceinline__ void push(const float (&a)[n], const float (&b)[n], const JsdRow &c) {
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            if constexpr (Elem<T>::kPrecise) {
+                const float lp = ((a[i] - c.ma) - c.la_hi) - c.la_lo;   // a - m is exact
+                const float lq = ((b[i] - c.mb) - c.lb_hi) - c.lb_lo;
+                const float p = expf(lp), q = expf(lq);
+                const float lmix = logf(fmaf(c.beta, q, c.omb * p));
+                if (p > 0.f) df_add(ka, p * (lp - lmix) * kLog2e);
+                if (q > 0.f) df_add(kb, q * (lq - lmix) * kLog2e);
+            } else {
+                const float xa = fmaf(a[i] - c.ma, kLog2e, -(c.la_hi + c.la_lo) * kLog2e);   // log2 p
+                const float xb = fmaf(b[i] - c.mb, kLog2e, -(c.lb_hi + c.lb_lo) * kLog2e);
+                const float p = ex2_fast(xa), q = ex2_fast(xb);
+                const float lm = fmaxf(lg2_fast(fmaf(c.beta, q, c.omb * p)), -250.f);
+                if (p > 0.f) ka.hi = fmaf(p, xa - lm, ka.hi);
+                if (q > 0.f) kb.hi = fmaf(q, xb - lm, kb.hi);
+            }
+        }
+    }
+
+    // bf16 fast path on raw 16-byte words: packed f32x2 arithmetic, MUFU ex2 and
+    // lg2. Terms are taken unguarded; a chunk whose sums come out non-finite (a
+    // -inf logit gives 0 * inf) is redone with zero-weight terms skipped.
+    template <int K>
+    __device__ __forceinline__ void push_bf16(const uint4 (&ua)[K], const uint4 (&ub)[K], const JsdRow &c) {
+        const float2 nma = make_float2(-c.ma, -c.ma), nmb = make_float2(-c.mb, -c.mb);
+        const float la2 = -(c.la_hi + c.la_lo) * kLog2e, lb2 = -(c.lb_hi + c.lb_lo) * kLog2e;
+        const float2 nla = make_float2(la2, la2), nlb = make_float2(lb2, lb2);
+        const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
+        const float2 bt = make_float2(c.beta, c.beta), ob = make_float2(c.omb, c.omb);
+        float2 sa[2], sb[2];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 xa = __ffma2_rn(__fadd2_rn(bf16_pair(word(ua[k], q)), nma), l2e, nla);   // log2 p
+                const float2 xb = __ffma2_rn(__fadd2_rn(bf16_pair(word(ub[k], q)), nmb), l2e, nlb);   // log2 q
+                const float2 p = make_float2(ex2_fast(xa.x), ex2_fast(xa.y));
+                const float2 qv = make_float2(ex2_fast(xb.x), ex2_fast(xb.y));
+                const float2 mix = __ffma2_rn(bt, qv, __fmul2_rn(ob, p));
+                const float2 lm = make_float2(fmaxf(lg2_fast(mix.x), -250.f), fmaxf(lg2_fast(mix.y), -250.f));
+                const float2 da = __ffma2_rn(lm, m1, xa), db = __ffma2_rn(lm, m1, xb);
+                if (k == 0 && q < 2) {
+                    sa[q] = __fmul2_rn(p, da);
+                    sb[q] = __fmul2_rn(qv, db);
+                } else {
+                    sa[q & 1] = __ffma2_rn(p, da, sa[q & 1]);
+                    sb[q & 1] = __ffma2_rn(qv, db, sb[q & 1]);
+                }
+            }
+        }
+        float2 ra = __fadd2_rn(sa[0], sa[1]);
+        float2 rb = __fadd2_rn(sb[0], sb[1]);
+        float suma = ra.x + ra.y, sumb = rb.x + rb.y;
+        if (!(fabsf(suma) < INFINITY && fabsf(sumb) < INFINITY)) {
+            suma = sumb = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 xa = __ffma2_rn(__fadd2_rn(bf16_pair(word(ua[k], q)), nma), l2e, nla);
+                    const float2 xb = __ffma2_rn(__fadd2_rn(bf16_pair(word(ub[k], q)), nmb), l2e, nlb);
+                    const float xs[4] = {xa.x, xa.y, xb.x, xb.y};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float p = ex2_fast(xs[h]), qv = ex2_fast(xs[2 + h]);
+                        const float lm = fmaxf(lg2_fast(fmaf(c.beta, qv, c.omb * p)), -250.f);
+                        if (p > 0.f) suma = fmaf(p, xs[h] - lm, suma);       // zero-weight terms add nothing
+                        if (qv > 0.f) sumb = fmaf(qv, xs[2 + h] - lm, sumb);
+                    }
+                }
+            }
+        }
+        ka.hi += suma;   // plain fp32 lane sums on the bf16 path (about ten chunks per row)
+        kb.hi += sumb;
+    }
+};
+
+template <typename V>
+struct PartJSD {
+    V ka, kb;
+};
+
+template <typename T>
+__device__ __forceinline__ PartJSD<AccT<T>> jsd_warp_merge(const LaneJSD<T> &L) {
+    DF a = L.ka, b = L.kb;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        df_add(a, shfl_xor(a, m));
+        df_add(b, shfl_xor(b, m));
+    }
+    return PartJSD<AccT<T>>{df_to<AccT<T>>(a), df_to<AccT<T>>(b)};
+}
+
+// Finishes a row: JSD = ln 2 (beta KB + (1 - beta) KA) from the warps' partials
+// (summed in a fixed order in fp64), and KL(p || mix), KL(q || mix) into the c
+// fields of the two records (flags keep only the NaN / empty bits).
+template <typename V>
+__device__ __forceinline__ void finish_jsd(const PartJSD<V> *parts, int count, int64_t r, double beta, float *jsd,
+                                           RowStat *stats_a, RowStat *stats_b) {
+    double ka = 0.0, kb = 0.0;
+    for (int w = 0; w < count; ++w) {
+        ka += (double)parts[w].ka;
+        kb += (double)parts[w].kb;
+    }
+    constexpr double kLn2 = 0.69314718055994530942;
+    ka *= kLn2;
+    kb *= kLn2;
+    const uint32_t fa = stats_a[r].flags & (kRowNanInf | kRowEmpty), fb = stats_b[r].flags & (kRowNanInf | kRowEmpty);
+    const DF ca = df_from(ka), cb = df_from(kb);
+    stats_a[r].c_hi = ca.hi;
+    stats_a[r].c_lo = ca.lo;
+    stats_a[r].flags = fa;
+    stats_b[r].c_hi = cb.hi;
+    stats_b[r].c_lo = cb.lo;
+    stats_b[r].flags = fb;
+    jsd[r] = (fa | fb) ? qnan() : (float)(beta * kb + (1.0 - beta) * ka);
 }
 
 // Per-shard record of a row (vocabulary-sharded forms): the merged partial
