@@ -253,6 +253,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for(dom),
                 "algorithmic_bytes": nbytes[dom]}
 
+    jsd = jsd_bench(args, a, b, g, dev, peaks) if rank == 0 else None
+
     linear = None
     if not args.no_linear and rank == 0:
         linear = linear_bench(args, dev, N=args.linear_rows)
@@ -276,11 +278,48 @@ def run_ours(args, rank, world, local_rank):
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu, "linear_logp": linear,
+            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "linear_logp": linear,
         }
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
+
+
+def jsd_bench(args, a, b, g, dev, peaks, beta=0.5):
+    """Generalized JSD (interior beta) on the step's buffers: two-pass forward and both gradients."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    N, V = a.shape
+    E2 = 2 * N * V * a.element_size()           # one read of A and B
+    jsd, sa, sb = vp.vp_jsd_fwd(a, b, beta)
+    da, db = torch.empty_like(a), torch.empty_like(a)
+    fwd = lambda: vp.vp_jsd_fwd(a, b, beta, jsd=jsd, stats_a=sa, stats_b=sb)
+    bwd = lambda: vp.vp_jsd_bwd(a, b, beta, sa, sb, g, da=da, db=db)
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 10))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tf = tb = 0.0
+    for _ in range(reps):
+        ev[0].record()
+        fwd()
+        ev[1].record()
+        bwd()
+        ev[2].record()
+        torch.cuda.synchronize()
+        tf += ev[0].elapsed_time(ev[1])
+        tb += ev[1].elapsed_time(ev[2])
+    tf, tb = tf / reps, tb / reps
+    gbs = lambda nbytes, ms: round(nbytes / (ms * 1e-3) / 1e9, 1)
+    return {"workload": f"{N}x{V} bf16, beta={beta}, gradients to both inputs", "fwd_ms": round(tf, 4),
+            "bwd_ms": round(tb, 4), "fwd_gbs": gbs(2 * E2, tf), "bwd_gbs": gbs(2 * E2, tb),
+            "fwd_bytes": 2 * E2, "bwd_bytes": 2 * E2,
+            "note": "forward = two reads of A and B (statistics, then both KL-to-mixture sums); "
+                    "backward = one read of A and B and one write of dA and dB",
+            "frac_of_copy_peak": {"fwd": round(2 * E2 / (tf * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                  "bwd": round(2 * E2 / (tb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
 def linear_bench(args, dev, N=8192, V=75968, D=4096):
