@@ -53,6 +53,8 @@ _SIGS = {
     "vpo_num_threads": ([], ctypes.c_int),
     "vpo_logprobs_fwd": (["P", "I", "I", "I", "P", "P", "P", "P", "P"], None),
     "vpo_logprobs_bwd": (["P", "I", "I", "I", "P", "P", "P"], None),
+    "vpo_logprobs_topk_fwd": (["P", "I", "I", "I", "I", "P", "P", "P"], None),
+    "vpo_logprobs_topk_bwd": (["P", "I", "I", "I", "I", "P", "P", "P"], None),
     "vpo_entropy_fwd": (["P", "I", "I", "P", "P", "P"], None),
     "vpo_entropy_bwd": (["P", "I", "I", "P", "P"], None),
     "vpo_kl_fwd": (["P", "P", "I", "I", "i", "P", "P", "P", "P", "P"], None),
@@ -131,6 +133,27 @@ def logprobs_bwd(x, targets, g, vocab_start=0, lib=None):
     t, g = _i64(targets), _f64(g)
     dx = np.empty((N, V))
     (lib or _load()).vpo_logprobs_bwd(_p(x), N, V, vocab_start, _p(t), _p(g), _p(dx))
+    return dx
+
+
+def logprobs_topk_fwd(x, targets, vocab_start=0, lib=None):
+    """logp [N, K] of K target ids per row (targets [N, K]); returns (logp, err)."""
+    x, t = _f64(x), _i64(targets)
+    N, V = _shape(x)
+    K = t.shape[1]
+    logp = np.empty((N, K))
+    err = np.zeros(1, dtype=np.int32)
+    (lib or _load()).vpo_logprobs_topk_fwd(_p(x), N, V, K, vocab_start, _p(t), _p(logp), _p(err))
+    return logp, int(err[0])
+
+
+def logprobs_topk_bwd(x, targets, g, vocab_start=0, lib=None):
+    """Gradient of sum_k g[r, k] logp[r, k]; targets and g are [N, K]."""
+    x, t, g = _f64(x), _i64(targets), _f64(g)
+    N, V = _shape(x)
+    K = t.shape[1]
+    dx = np.empty((N, V))
+    (lib or _load()).vpo_logprobs_topk_bwd(_p(x), N, V, K, vocab_start, _p(t), _p(g), _p(dx))
     return dx
 
 

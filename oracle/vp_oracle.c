@@ -148,6 +148,61 @@ void vpo_logprobs_bwd(const double *x, int64_t N, int64_t V, int64_t vocab_start
 }
 
 /* ------------------------------------------------------------------------ */
+/* Several target ids per row (top-k) [P1 PR description, "Tests": duplicate */
+/* and ignored top-k ids and a fully ignored row]. targets and g are N x K,  */
+/* row-major. Per id, R5: a negative id is ignored (logp 0, no gradient     */
+/* term), an id >= 0 outside the shard is a data error (logp NaN, err bit,   */
+/* and the row's gradient is NaN). The gradient is that of                   */
+/* sum_k g_rk logp_rk: sum over the ids not ignored of g_rk (onehot - p),    */
+/* so duplicate ids add up.                                                  */
+/* ------------------------------------------------------------------------ */
+void vpo_logprobs_topk_fwd(const double *x, int64_t N, int64_t V, int64_t K, int64_t vocab_start,
+                           const int64_t *targets, double *logp, int32_t *err) {
+    int32_t e = 0;
+#pragma omp parallel for schedule(static) reduction(| : e)
+    for (int64_t r = 0; r < N; ++r) {
+        const double *z = x + r * V;
+        row_stats s = scan_row(z, V);
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t t = targets[r * K + k];
+            double *out = logp + r * K + k;
+            if (t < 0) { *out = 0.0; continue; }
+            int64_t loc = t - vocab_start;
+            if (loc < 0 || loc >= V) { *out = NAN; e |= VPO_ERR_TARGET; continue; }
+            *out = (s.bad || s.S == 0.0) ? NAN : log_prob(z[loc], &s);
+        }
+    }
+    if (err) *err |= e;
+}
+
+void vpo_logprobs_topk_bwd(const double *x, int64_t N, int64_t V, int64_t K, int64_t vocab_start,
+                           const int64_t *targets, const double *g, double *dx) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) {
+        const double *z = x + r * V;
+        double *d = dx + r * V;
+        row_stats s = scan_row(z, V);
+        double gsum = 0.0;
+        int used = 0, bad = 0;
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t t = targets[r * K + k];
+            if (t < 0) continue;
+            int64_t loc = t - vocab_start;
+            if (loc < 0 || loc >= V) bad = 1;
+            used = 1;
+            gsum += g[r * K + k];
+        }
+        if (!used) { for (int64_t j = 0; j < V; ++j) d[j] = 0.0; continue; }
+        if (bad || s.bad || s.S == 0.0) { for (int64_t j = 0; j < V; ++j) d[j] = NAN; continue; }
+        for (int64_t j = 0; j < V; ++j) d[j] = -gsum * exp(log_prob(z[j], &s));
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t t = targets[r * K + k];
+            if (t >= 0) d[t - vocab_start] += g[r * K + k];
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Entropy H = -sum_{p_j>0} p_j log p_j  [P1 first and second commit msgs]  */
 /* ------------------------------------------------------------------------ */
 static double entropy_row(const double *z, int64_t V, const row_stats *s) {

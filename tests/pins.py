@@ -21,6 +21,9 @@ build) and raises AssertionError when the oracle disagrees with:
 * the per-shard records (max, sum-exp, centred weighted sum, flags) against
   Decimal sums over each shard;
 * hand-built rows for every NaN / inf precedence rule and target rule;
+* several target ids per row: Decimal brute force with duplicate and ignored
+  ids and a fully ignored row, K = 1 against the single-id definition,
+  duplicated ids against one id carrying the summed gradient;
 * the generalized JSD: Decimal brute force of the value and of both gradients,
   JSD(A, A) = 0, disjoint supports giving the entropy of the mixing weights,
   symmetry at beta = 1/2, bounds, and the limits JSD_beta / beta -> KL(B||A)
@@ -163,6 +166,48 @@ def pin_brute_force_grads(lib=None):
                 _close(db_r[r], f(ref_db), 1e-13, 1e-12, f"dKL/dB V={V}")
                 _close(da_f[r], f(ref_da), 1e-13, 1e-12, f"dKL/dA (forward, swapped) V={V}")
                 _close(db_f[r], f(ref_db), 1e-13, 1e-12, f"dKL/dB (forward, swapped) V={V}")
+
+
+def pin_topk_targets(lib=None):
+    """Several ids per row: Decimal brute force, the single-id oracle at K = 1, duplicates add up."""
+    with localcontext() as ctx:
+        ctx.prec = 80
+        for V in (3, 5, 8):
+            x = _tiny_rows(500 + V, V, 4, mask_frac=0.2)
+            t = np.array([[0, 0, -1], [V - 1, 1 % V, 2 % V], [-1, -1, -1], [2 % V, -5, 0]])
+            x[np.arange(4)[:, None], np.maximum(t, 0)] = 0.25      # ids never sit on a masked logit
+            g = np.array([[0.5, -1.5, 9.0], [1.0, 2.0, -0.5], [3.0, 3.0, 3.0], [0.7, 4.0, -1.1]])
+            lp, err = oracle.logprobs_topk_fwd(x, t, lib=lib)
+            dx = oracle.logprobs_topk_bwd(x, t, g, lib=lib)
+            assert err == 0
+            for r in range(4):
+                row = list(x[r])
+                for k in range(3):
+                    ref = 0.0 if t[r, k] < 0 else float(_dlogp(row, t[r, k]))
+                    _close(lp[r, k], ref, 1e-14, 1e-14, f"top-k logp V={V}")
+                used = [(Decimal(g[r, k]), t[r, k]) for k in range(3) if t[r, k] >= 0]
+                f = lambda z: sum((gk * _dlogp(z, tk) for gk, tk in used), Decimal(0))
+                ref = [float(d) for d in _dgrad(f, row)] if used else [0.0] * V
+                _close(dx[r], ref, 1e-13, 1e-12, f"top-k gradient V={V} row {r}")
+    # K = 1 is the single-id oracle; a duplicated id carries the sum of its gradients
+    N, V = 6, 300
+    x = _rand(81, N, V)
+    t1 = np.random.default_rng(82).integers(0, V, N)
+    t1[2] = -1
+    g1 = np.linspace(-1, 2, N)
+    assert np.array_equal(oracle.logprobs_topk_fwd(x, t1[:, None], lib=lib)[0][:, 0],
+                          oracle.logprobs_fwd(x, t1, lib=lib)[0])
+    _close(oracle.logprobs_topk_bwd(x, t1[:, None], g1[:, None], lib=lib), oracle.logprobs_bwd(x, t1, g1, lib=lib),
+           1e-15, 0, "top-k K = 1")
+    g2 = np.stack([0.25 * g1, 0.75 * g1], 1)
+    _close(oracle.logprobs_topk_bwd(x, np.stack([t1, t1], 1), g2, lib=lib), oracle.logprobs_bwd(x, t1, g1, lib=lib),
+           1e-15, 1e-14, "duplicated ids")
+    # an id outside the shard: NaN for that id, the error bit, a NaN gradient row
+    t = np.stack([t1, t1], 1)
+    t[4, 1] = V + 7
+    lp, err = oracle.logprobs_topk_fwd(x, t, lib=lib)
+    assert err == 1 and np.isnan(lp[4, 1]) and np.isfinite(lp[4, 0])
+    assert np.isnan(oracle.logprobs_topk_bwd(x, t, g2, lib=lib)[4]).all()
 
 
 # ----------------------------------------------------------------------------
@@ -631,6 +676,7 @@ def pin_linear_logp_finite_differences(lib=None):
 ALL_PINS = [
     pin_brute_force_fwd,
     pin_brute_force_grads,
+    pin_topk_targets,
     pin_uniform_row,
     pin_two_token_closed_form,
     pin_one_hot_extremes,

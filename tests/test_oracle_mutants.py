@@ -60,6 +60,11 @@ MUTANTS = [
     ("JSD dB wrong weight", "g[r] * beta * q * ((lq - lmix) - kb)", "g[r] * (1.0 - beta) * q * ((lq - lmix) - kb)"),
     ("JSD endpoint directions swapped", "if (beta == 0.0) jsd[r] = kl_row(B, A, V, &sb, &sa);",
      "if (beta == 0.0) jsd[r] = kl_row(A, B, V, &sa, &sb);"),
+    ("top-k duplicates overwrite", "if (t >= 0) d[t - vocab_start] += g[r * K + k];",
+     "if (t >= 0) d[t - vocab_start] = g[r * K + k];"),
+    ("top-k ignored ids counted", "if (t < 0) continue;\n            int64_t loc = t - vocab_start;\n            if (loc < 0 || loc >= V) bad = 1;",
+     "if (t < 0) { gsum += g[r * K + k]; continue; }\n            int64_t loc = t - vocab_start;\n            if (loc < 0 || loc >= V) bad = 1;"),
+    ("top-k id stride", "int64_t t = targets[r * K + k];\n            double *out", "int64_t t = targets[r + k];\n            double *out"),
     ("linear logits transposed", "acc += h[r * D + k] * W[j * D + k];", "acc += h[r * D + k] * W[k * V + j];"),
     ("linear dW wrong row", "out[k] += c * h[r * D + k];", "out[k] += c * h[((r + 1) % N) * D + k];"),
     ("linear dh wrong vocab row", "out[k] += c * W[j * D + k];", "out[k] += c * W[((j + 1) % V) * D + k];"),
