@@ -167,6 +167,26 @@ VP_API vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V,
                                  const float *grad_out, void *dx, int32_t *err_word,
                                  vp_stream stream);
 
+/* Several target ids per row (top-k) [P1, PR description, "Tests": duplicate
+ * and ignored top-k ids and a fully ignored row]. targets: int64 [N, K]
+ * row-major (global ids, each following the rules of vp_logprobs_fwd: a
+ * negative id is ignored and gives 0, an id >= 0 outside the shard gives NaN
+ * and VP_ERRBIT_TARGET). Outputs: logp fp32 [N, K] and stats (vp_rowstat [N],
+ * the same record as vp_logprobs_fwd). K >= 1. */
+VP_API vp_status vp_logprobs_topk_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                                      int64_t s_i, int64_t vocab_start, const int64_t *targets, int64_t K,
+                                      float *logp, vp_rowstat *stats, int32_t *err_word, vp_stream stream);
+
+/* Gradient of sum_k g[r, k] logp[r, k]: dx[r, j] = G_j - p_j Gsum, with Gsum
+ * the sum of g over the row's ids that are not ignored and G_j the sum over
+ * the ids equal to j (duplicate ids add up). grad_out: fp32 [N, K]. A row with
+ * an id outside the shard (or without valid statistics) is NaN; a row whose
+ * ids are all ignored is 0. dx: contiguous [N, V], dtype of x. */
+VP_API vp_status vp_logprobs_topk_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                                      int64_t s_i, int64_t vocab_start, const int64_t *targets, int64_t K,
+                                      const vp_rowstat *stats, const float *grad_out, void *dx, int32_t *err_word,
+                                      vp_stream stream);
+
 /* ------------------------------------------------------------------------ */
 /* Entropy [P1, second commit message and reviewer's suggested change]      */
 /* ------------------------------------------------------------------------ */

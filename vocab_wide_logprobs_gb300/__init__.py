@@ -12,7 +12,7 @@ from .api import (KL_FORWARD, KL_REVERSE, PART_HAS_TARGET, PART_IGNORED, PART_MI
                   vp_entropy_merge, vp_entropy_partial, vp_fault_status, vp_jsd_bwd, vp_jsd_fwd, vp_kl_bwd, vp_kl_fwd, vp_kl_merge,
                   vp_kl_partial, vp_linear_logp_bwd, vp_linear_logp_bwd_workspace_size, vp_linear_logp_fwd,
                   vp_linear_logp_fwd_noalloc, vp_linear_logp_workspace_size, vp_logprobs_bwd, vp_logprobs_fwd,
-                  vp_logprobs_merge, vp_logprobs_partial)
+                  vp_logprobs_merge, vp_logprobs_partial, vp_logprobs_topk_bwd, vp_logprobs_topk_fwd)
 
 __all__ = ["KL_FORWARD", "KL_REVERSE", "PART_HAS_TARGET", "PART_IGNORED", "PART_MISMATCH", "PART_NANINF",
            "PART_NANINF_B", "ROW_BADTARGET", "ROW_EMPTY", "ROW_MISMATCH", "ROW_NANINF", "ROW_SHARDED", "VPError",
@@ -20,4 +20,5 @@ __all__ = ["KL_FORWARD", "KL_REVERSE", "PART_HAS_TARGET", "PART_IGNORED", "PART_
            "vp_entropy_fwd", "vp_entropy_merge", "vp_entropy_partial", "vp_fault_status", "vp_jsd_bwd", "vp_jsd_fwd", "vp_kl_bwd", "vp_kl_fwd",
            "vp_kl_merge", "vp_kl_partial", "vp_linear_logp_bwd", "vp_linear_logp_bwd_workspace_size",
            "vp_linear_logp_fwd", "vp_linear_logp_fwd_noalloc", "vp_linear_logp_workspace_size", "vp_logprobs_bwd",
-           "vp_logprobs_fwd", "vp_logprobs_merge", "vp_logprobs_partial"]
+           "vp_logprobs_fwd", "vp_logprobs_merge", "vp_logprobs_partial", "vp_logprobs_topk_bwd",
+           "vp_logprobs_topk_fwd"]

@@ -20,6 +20,8 @@ P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 SIGNATURES = {
     "vp_logprobs_fwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P],
     "vp_logprobs_bwd": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P, P, P, P],
+    "vp_logprobs_topk_fwd": [P, I32, I64, I64, I64, I64, I64, I64, P, I64, P, P, P, P],
+    "vp_logprobs_topk_bwd": [P, I32, I64, I64, I64, I64, I64, I64, P, I64, P, P, P, P, P],
     "vp_entropy_fwd": [P, I32, I64, I64, I64, I64, I64, P, P, P],
     "vp_entropy_bwd": [P, I32, I64, I64, I64, I64, I64, P, P, P, P],
     "vp_kl_fwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P],

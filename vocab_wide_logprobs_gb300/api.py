@@ -127,6 +127,34 @@ def vp_logprobs_bwd(x, targets, stats, grad, vocab_start: int = 0, err_word=None
     return dx
 
 
+def _topk_ids(targets):
+    if targets.dim() != 2 or targets.dtype != torch.int64 or not targets.is_contiguous():
+        raise VPError(2, "top-k ids must be a contiguous int64 [N, K] tensor")
+    return targets.shape[1]
+
+
+def vp_logprobs_topk_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=None, stats=None):
+    """logp of K ids per row; targets int64 [N, K]. Returns (logp fp32 [N, K], stats)."""
+    N, V, R, s_o, s_i = rows_of(x)
+    K = _topk_ids(targets)
+    logp = torch.empty((N, K), dtype=torch.float32, device=x.device) if logp is None else logp
+    stats = rowstats(N, x.device) if stats is None else stats
+    _check(_lib.lib().vp_logprobs_topk_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets), K,
+                                           _ptr(logp), _ptr(stats), _ptr(err_word), _stream()), "vp_logprobs_topk_fwd")
+    return logp, stats
+
+
+def vp_logprobs_topk_bwd(x, targets, stats, grad, vocab_start: int = 0, err_word=None, dx=None):
+    """Gradient of sum_k grad[r, k] logp[r, k] (grad fp32 [N, K]); returns dx [N, V] in the dtype of x."""
+    N, V, R, s_o, s_i = rows_of(x)
+    K = _topk_ids(targets)
+    dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
+    _check(_lib.lib().vp_logprobs_topk_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets), K,
+                                           _ptr(stats), _ptr(grad), _ptr(dx), _ptr(err_word), _stream()),
+           "vp_logprobs_topk_bwd")
+    return dx
+
+
 def vp_entropy_fwd(x, H=None, stats=None):
     """Returns (H fp32 [N], stats)."""
     N, V, R, s_o, s_i = rows_of(x)

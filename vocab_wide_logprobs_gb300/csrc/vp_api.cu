@@ -90,6 +90,44 @@ vp_status vp_logprobs_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_
     return launched(vp::launch_logprobs_bwd(a));
 }
 
+vp_status vp_logprobs_topk_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                               int64_t s_i, int64_t vocab_start, const int64_t *targets, int64_t K, float *logp,
+                               vp_rowstat *stats, int32_t *err_word, vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (K < 1 || K > kMaxRowsPerLaunch / (N > 0 ? N : 1)) return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!x || !targets || !logp || !stats) return VP_ERR_NULL;
+    if (!aligned(x, elem_size(dtype)) || !aligned(targets, 8) || !aligned(logp, 4) || !aligned(stats, 16) ||
+        !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::StatsArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, targets, logp, stats, err_word,
+                    (cudaStream_t)stream};
+    a.K = K;
+    return launched(vp::launch_logprobs_topk_fwd(a));
+}
+
+vp_status vp_logprobs_topk_bwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o,
+                               int64_t s_i, int64_t vocab_start, const int64_t *targets, int64_t K,
+                               const vp_rowstat *stats, const float *grad_out, void *dx, int32_t *err_word,
+                               vp_stream stream) {
+    vp_status st = check_rows(dtype, N, V, R, s_o, s_i);
+    if (st != VP_OK) return st;
+    if (K < 1 || K > kMaxRowsPerLaunch / (N > 0 ? N : 1)) return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!x || !targets || !stats || !grad_out || !dx) return VP_ERR_NULL;
+    const size_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(dx, es) || !aligned(targets, 8) || !aligned(stats, 16) ||
+        !aligned(grad_out, 4) || !aligned(err_word, 4))
+        return VP_ERR_ALIGN;
+    if ((st = check_device()) != VP_OK) return st;
+    vp::GradArgs a{x, dtype == VP_BF16, N, V, R, s_o, s_i, vocab_start, stats, grad_out, targets, dx, err_word,
+                   (cudaStream_t)stream};
+    a.K = K;
+    return launched(vp::launch_logprobs_topk_bwd(a));
+}
+
 vp_status vp_entropy_fwd(const void *x, int dtype, int64_t N, int64_t V, int64_t R, int64_t s_o, int64_t s_i,
                          float *H, vp_rowstat *stats, vp_stream stream) {
     vp_status st = check_rows(dtype, N, V, R, s_o, s_i);

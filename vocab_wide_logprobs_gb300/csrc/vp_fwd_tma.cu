@@ -149,14 +149,15 @@ __device__ __forceinline__ void drain(Ring &ring, uint32_t issued) {
 }
 
 // ---------------------------------------------------------------------------
-// logprobs (kOp = 0) and entropy (kOp = 1)
+// logprobs (kOp = 0), entropy (kOp = 1), logprobs of K ids per row (kOp = 2)
 // ---------------------------------------------------------------------------
 template <int kOp, typename T>
 __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm)
 stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const int64_t *__restrict__ targets,
                      int64_t vocab_start, float *__restrict__ out, RowStat *__restrict__ stats,
-                     int32_t *__restrict__ err, PartialRec *__restrict__ shard_parts) {
+                     int32_t *__restrict__ err, PartialRec *__restrict__ shard_parts, int64_t K) {
     constexpr bool kW = kOp == 1;
+    constexpr int kSt = kOp == 1 ? 1 : 0;                       // statistics of logprobs or entropy
     constexpr int kVec = Elem<T>::kVec;
     constexpr int kChunkVec = kStageBytes / 16;                 // 16-byte vectors per stage
     constexpr int kPerThread = kChunkVec / kTmaConsumers;       // 4
@@ -185,10 +186,13 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
             }
             const Part1<AccT<T>> p = merge_parts<kW>(parts[slot], kTmaConsumerWarps);
             __syncwarp();
-            if (lane == 0) {
+            if (kOp == 2) {
+                if (lane == 0) mbar_arrive(&ring.parts_empty[slot]);
+                finish_topk(p, r, V, K, targets, vocab_start, x + rows.off(r), out, stats, err, lane);
+            } else if (lane == 0) {
                 mbar_arrive(&ring.parts_empty[slot]);
-                if (shard_parts) finish_partial<kOp>(p, r, V, t, vocab_start, zt, shard_parts);
-                else finish_stats<kOp>(p, r, V, t, vocab_start, zt, out, stats, err);
+                if (shard_parts) finish_partial<kSt>(p, r, V, t, vocab_start, zt, shard_parts);
+                else finish_stats<kSt>(p, r, V, t, vocab_start, zt, out, stats, err);
             }
         }
         return;
@@ -564,7 +568,7 @@ static cudaError_t launch_stats_tma(const StatsArgs &a) {
     if (e != cudaSuccess) return e;
     k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
         static_cast<const T *>(a.x), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, a.targets, a.vocab_start, a.out,
-        static_cast<RowStat *>(a.stats), a.err, static_cast<PartialRec *>(a.parts));
+        static_cast<RowStat *>(a.stats), a.err, static_cast<PartialRec *>(a.parts), a.K);
     return cudaGetLastError();
 }
 
@@ -574,6 +578,10 @@ cudaError_t launch_logprobs_fwd(const StatsArgs &a) {
 
 cudaError_t launch_entropy_fwd(const StatsArgs &a) {
     return a.bf16 ? launch_stats_tma<1, __nv_bfloat16>(a) : launch_stats_tma<1, float>(a);
+}
+
+cudaError_t launch_logprobs_topk_fwd(const StatsArgs &a) {
+    return a.bf16 ? launch_stats_tma<2, __nv_bfloat16>(a) : launch_stats_tma<2, float>(a);
 }
 
 template <typename T>

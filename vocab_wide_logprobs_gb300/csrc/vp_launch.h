@@ -19,6 +19,7 @@ struct StatsArgs {
     int32_t *err;
     cudaStream_t stream;
     void *parts = nullptr;  // vp_partial [N]: per-shard records instead of out / stats
+    int64_t K = 1;          // ids per row (top-k logprobs: targets [N, K], out [N, K])
 };
 
 struct KLFwdArgs {
@@ -81,6 +82,7 @@ struct GradArgs {
     void *dx;
     int32_t *err;
     cudaStream_t stream;
+    int64_t K = 1;          // ids per row (top-k logprobs: targets and g are [N, K])
 };
 
 struct KLBwdArgs {
@@ -130,6 +132,8 @@ cudaError_t read_linear_fault(uint32_t *value, bool clear);
 
 cudaError_t launch_logprobs_fwd(const StatsArgs &a);
 cudaError_t launch_entropy_fwd(const StatsArgs &a);
+cudaError_t launch_logprobs_topk_fwd(const StatsArgs &a);
+cudaError_t launch_logprobs_topk_bwd(const GradArgs &a);
 cudaError_t launch_kl_fwd(const KLFwdArgs &a);
 cudaError_t launch_kl_fwd_rowwise(const KLFwdArgs &a);
 cudaError_t read_fault(uint32_t *value, bool clear);

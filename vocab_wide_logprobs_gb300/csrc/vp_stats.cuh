@@ -503,6 +503,43 @@ __device__ __forceinline__ void finish_stats(const Part1<Acc> &p, int64_t r, int
     out[r] = bad ? qnan() : (float)(((double)zt - (double)p.mx) - logS);
 }
 
+// Several target ids per row (top-k): the row's record as for logprobs, then
+// logp for each of the K ids, lanes of the finisher warp taking ids k = lane,
+// lane + 32, ... (per id: negative = ignored, 0; outside the shard = NaN and
+// the error bit). Called by a whole warp; `p` is valid in every lane.
+template <typename T, typename Acc>
+__device__ __forceinline__ void finish_topk(const Part1<Acc> &p, int64_t r, int V, int64_t K,
+                                            const int64_t *targets, int64_t vocab_start, const T *row, float *out,
+                                            RowStat *stats, int32_t *err, int lane) {
+    double logS = 0.0;
+    uint32_t flags = 0;
+    if (lane == 0) {
+        const double S = p.S;
+        if (S != S) flags |= kRowNanInf;
+        else if (S == 0.0) flags |= kRowEmpty;
+        logS = log(S) - ((double)p.mx - (double)p.ref);
+        store_rowstat(stats + r, p.mx, logS, 0.0, flags);
+    }
+    logS = __shfl_sync(0xffffffffu, logS, 0);
+    flags = __shfl_sync(0xffffffffu, flags, 0);
+    for (int64_t k = lane; k < K; k += 32) {
+        const int64_t t = targets[r * K + k];
+        float v;
+        if (t < 0) {
+            v = 0.f;
+        } else {
+            const int64_t loc = t - vocab_start;
+            if (loc < 0 || loc >= V) {
+                v = qnan();
+                if (err) atomicOr(err, VP_ERRBIT_TARGET_);
+            } else {
+                v = flags ? qnan() : (float)(((double)Elem<T>::load1(row + loc) - (double)p.mx) - logS);
+            }
+        }
+        out[r * K + k] = v;
+    }
+}
+
 template <typename Acc>
 __device__ __forceinline__ void finish_kl(const PartKL<Acc> &s, int64_t r, float *kl, RowStat *stats_p,
                                           RowStat *stats_q) {

@@ -91,3 +91,19 @@ def linear(seed: int = 4, N: int = ROWS, V: int = VOCAB, D: int = 4096, dtype=to
     h = _normal(gen, (N, D), 1.0).to(dtype)
     w = _normal(gen, (V, D), 0.02).to(dtype)
     return {"hidden": h, "weight": w, "targets": _targets(gen, N, V), "grad": _normal(gen, (N,), 1.0)}
+
+
+def topk_ids(seed: int, N: int, V: int, K: int, vocab_start: int = 0, ignore_frac: float = 0.1,
+             dup_frac: float = 0.1):
+    """K target ids per row ([N, K] int64) with upstream gradients [N, K] fp32 ~ N(0, 1).
+
+    Ids are uniform in [vocab_start, vocab_start + V); a share ``dup_frac`` of
+    the slots repeats the row's first id (duplicate ids) and a share
+    ``ignore_frac`` is -1 (ignored ids).
+    """
+    gen = _gen(seed)
+    t = torch.randint(0, V, (N, K), generator=gen, dtype=torch.int64).add_(vocab_start)
+    dup = torch.rand(N, K, generator=gen) < dup_frac
+    t = torch.where(dup, t[:, :1].expand(N, K), t)
+    t[torch.rand(N, K, generator=gen) < ignore_frac] = -1
+    return {"targets": t.contiguous(), "grad": _normal(gen, (N, K), 1.0)}
