@@ -70,6 +70,10 @@ _SIGS = {
     "vpo_linear_logits": (["P", "P", "I", "I", "I", "P"], None),
     "vpo_linear_logp_fwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P", "P"], None),
     "vpo_linear_logp_bwd": (["P", "P", "I", "I", "I", "I", "P", "P", "P", "P", "P"], None),
+    "vpo_linear_entropy_fwd": (["P", "P", "I", "I", "I", "P", "P", "P", "P"], None),
+    "vpo_linear_entropy_bwd": (["P", "P", "I", "I", "I", "P", "P", "P", "P"], None),
+    "vpo_linear_kl_fwd": (["P", "P", "P", "P", "I", "I", "I", "I", "i", "P", "P", "P", "P", "P", "P"], None),
+    "vpo_linear_kl_bwd": (["P", "P", "P", "P", "I", "I", "I", "I", "i", "P", "P", "P", "P", "P", "P"], None),
 }
 _CT = {"P": ctypes.c_void_p, "I": ctypes.c_int64, "i": ctypes.c_int, "d": ctypes.c_double}
 
@@ -320,3 +324,56 @@ def linear_logp_bwd(h, W, targets, g, vocab_start=0, want_dh=True, want_dW=True,
     (lib or _load()).vpo_linear_logp_bwd(_p(h), _p(W), N, V, D, vocab_start, _p(t), _p(g), _p(dh),
                                 _p(dW), _p(dz))
     return dh, dW
+
+
+def _linear_shapes(h, W):
+    h, W = _f64(h), _f64(W)
+    if h.ndim != 2 or W.ndim != 2 or W.shape[1] != h.shape[1]:
+        raise ValueError("hidden [N, D] and weight [V, D] disagree")
+    return h, W, h.shape[0], W.shape[0], h.shape[1]
+
+
+def linear_entropy_fwd(h, W, lib=None):
+    """Returns (H, m, logS) of the logits h . W^T (materialised in fp64; small cases only)."""
+    h, W, N, V, D = _linear_shapes(h, W)
+    H, m, logS = (np.empty(N) for _ in range(3))
+    logits = np.empty((N, V))
+    (lib or _load()).vpo_linear_entropy_fwd(_p(h), _p(W), N, V, D, _p(H), _p(m), _p(logS), _p(logits))
+    return H, m, logS
+
+
+def linear_entropy_bwd(h, W, g, want_dh=True, want_dW=True, lib=None):
+    """Returns (dhidden, dW) of sum_r g_r H_r; either is None when not wanted."""
+    h, W, N, V, D = _linear_shapes(h, W)
+    g = _f64(g)
+    dh = np.empty((N, D)) if want_dh else None
+    dW = np.empty((V, D)) if want_dW else None
+    scratch = np.empty((2, N, V))
+    (lib or _load()).vpo_linear_entropy_bwd(_p(h), _p(W), N, V, D, _p(g), _p(dh), _p(dW), _p(scratch))
+    return dh, dW
+
+
+def linear_kl_fwd(ha, Wa, hb, Wb, direction=REVERSE, lib=None):
+    """KL between model A (ha . Wa^T) and model B (hb . Wb^T); reverse = KL(A||B).
+    Returns (kl, ma, logSa, mb, logSb)."""
+    ha, Wa, N, V, Da = _linear_shapes(ha, Wa)
+    hb, Wb, Nb, Vb, Db = _linear_shapes(hb, Wb)
+    if (Nb, Vb) != (N, V):
+        raise ValueError("the two models disagree on N or V")
+    kl, ma, lsa, mb, lsb = (np.empty(N) for _ in range(5))
+    scratch = np.empty((2, N, V))
+    (lib or _load()).vpo_linear_kl_fwd(_p(ha), _p(Wa), _p(hb), _p(Wb), N, V, Da, Db, int(direction), _p(kl),
+                                       _p(ma), _p(lsa), _p(mb), _p(lsb), _p(scratch))
+    return kl, ma, lsa, mb, lsb
+
+
+def linear_kl_bwd(ha, Wa, hb, Wb, g, direction=REVERSE, want=(True, True, True, True), lib=None):
+    """Returns (dha, dWa, dhb, dWb) of sum_r g_r KL_r; entries not wanted are None."""
+    ha, Wa, N, V, Da = _linear_shapes(ha, Wa)
+    hb, Wb, _, _, Db = _linear_shapes(hb, Wb)
+    g = _f64(g)
+    outs = [np.empty(s) if w else None for s, w in zip(((N, Da), (V, Da), (N, Db), (V, Db)), want)]
+    scratch = np.empty((4, N, V))
+    (lib or _load()).vpo_linear_kl_bwd(_p(ha), _p(Wa), _p(hb), _p(Wb), N, V, Da, Db, int(direction), _p(g),
+                                       *[_p(o) for o in outs], _p(scratch))
+    return tuple(outs)

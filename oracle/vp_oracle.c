@@ -632,3 +632,83 @@ void vpo_linear_logp_bwd(const double *h, const double *W, int64_t N, int64_t V,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Fused linear entropy and KL: the entropy of softmax(h . W^T), and the KL   */
+/* between the next-token distributions of two models, each with its own      */
+/* hidden states and LM-head weight [P1, JSD pull request "Motivation": a     */
+/* teacher-student divergence computed from tiled LM-head projections         */
+/* without the full logits]. The definitions are those of vpo_entropy_* and  */
+/* vpo_kl_* applied to the fp64 logits rows h_r . W_j (materialised here);    */
+/* the chain rule is the one of vpo_linear_logp_bwd [P2, review nitpick]:     */
+/* dhidden = dz . W, dW = dz^T . h.                                           */
+/* ------------------------------------------------------------------------ */
+
+/* dh = dz . W ([N][D]) and dW = dz^T . h ([V][D]) for a materialised dz [N][V];
+ * either output may be NULL. */
+static void linear_chain_rule(const double *h, const double *W, int64_t N, int64_t V, int64_t D,
+                              const double *dz, double *dh, double *dW) {
+    if (dh) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < N; ++r) {
+            double *out = dh + r * D;
+            for (int64_t k = 0; k < D; ++k) out[k] = 0.0;
+            for (int64_t j = 0; j < V; ++j) {
+                double c = dz[r * V + j];
+                for (int64_t k = 0; k < D; ++k) out[k] += c * W[j * D + k];
+            }
+        }
+    }
+    if (dW) {
+#pragma omp parallel for schedule(static)
+        for (int64_t j = 0; j < V; ++j) {
+            double *out = dW + j * D;
+            for (int64_t k = 0; k < D; ++k) out[k] = 0.0;
+            for (int64_t r = 0; r < N; ++r) {
+                double c = dz[r * V + j];
+                for (int64_t k = 0; k < D; ++k) out[k] += c * h[r * D + k];
+            }
+        }
+    }
+}
+
+/* H_r, m_r, logS_r of the logits h_r . W^T. logits: caller-owned [N][V]. */
+void vpo_linear_entropy_fwd(const double *h, const double *W, int64_t N, int64_t V, int64_t D,
+                            double *H, double *m_out, double *logS_out, double *logits) {
+    vpo_linear_logits(h, W, N, V, D, logits);
+    vpo_entropy_fwd(logits, N, V, H, m_out, logS_out);
+}
+
+/* dhidden and dW of sum_r g_r H_r. scratch: caller-owned [2][N][V]. */
+void vpo_linear_entropy_bwd(const double *h, const double *W, int64_t N, int64_t V, int64_t D,
+                            const double *g, double *dh, double *dW, double *scratch) {
+    double *logits = scratch, *dz = scratch + N * V;
+    vpo_linear_logits(h, W, N, V, D, logits);
+    vpo_entropy_bwd(logits, N, V, g, dz);
+    linear_chain_rule(h, W, N, V, D, dz, dh, dW);
+}
+
+/* KL between model A (ha [N][Da], Wa [V][Da]) and model B (hb [N][Db], Wb [V][Db])
+ * in the direction of vpo_kl_fwd (R1), with both models' row max and log-sum.
+ * scratch: caller-owned [2][N][V]. */
+void vpo_linear_kl_fwd(const double *ha, const double *Wa, const double *hb, const double *Wb, int64_t N,
+                       int64_t V, int64_t Da, int64_t Db, int direction, double *kl, double *ma, double *lsa,
+                       double *mb, double *lsb, double *scratch) {
+    double *za = scratch, *zb = scratch + N * V;
+    vpo_linear_logits(ha, Wa, N, V, Da, za);
+    vpo_linear_logits(hb, Wb, N, V, Db, zb);
+    vpo_kl_fwd(za, zb, N, V, direction, kl, ma, lsa, mb, lsb);
+}
+
+/* dhidden and dW of both models for sum_r g_r KL_r; any output may be NULL.
+ * scratch: caller-owned [4][N][V]. */
+void vpo_linear_kl_bwd(const double *ha, const double *Wa, const double *hb, const double *Wb, int64_t N,
+                       int64_t V, int64_t Da, int64_t Db, int direction, const double *g, double *dha,
+                       double *dWa, double *dhb, double *dWb, double *scratch) {
+    double *za = scratch, *zb = scratch + N * V, *dza = scratch + 2 * N * V, *dzb = scratch + 3 * N * V;
+    vpo_linear_logits(ha, Wa, N, V, Da, za);
+    vpo_linear_logits(hb, Wb, N, V, Db, zb);
+    vpo_kl_bwd(za, zb, N, V, direction, g, dza, dzb);
+    linear_chain_rule(ha, Wa, N, V, Da, dza, dha, dWa);
+    linear_chain_rule(hb, Wb, N, V, Db, dzb, dhb, dWb);
+}

@@ -673,6 +673,80 @@ def pin_linear_logp_finite_differences(lib=None):
            1e-14, 1e-14, "linear logp = logprobs(logits)")
 
 
+# ----------------------------------------------------------------------------
+# Fused linear entropy and KL (two models with their own hidden size)
+# ----------------------------------------------------------------------------
+def _two_models(seed, N, V, Da, Db):
+    rng = np.random.default_rng(seed)
+    return (rng.normal(0, 1, (N, Da)), rng.normal(0, 0.6, (V, Da)), rng.normal(0, 1, (N, Db)),
+            rng.normal(0, 0.6, (V, Db)), rng.normal(size=N))
+
+
+def _dlogits(h, W):
+    return [[sum((Decimal(h[r, k]) * Decimal(W[j, k]) for k in range(h.shape[1])), Decimal(0))
+             for j in range(W.shape[0])] for r in range(h.shape[0])]
+
+
+def pin_linear_entropy_kl_brute_force(lib=None):
+    ha, Wa, hb, Wb, _ = _two_models(61, 3, 5, 4, 6)
+    H = oracle.linear_entropy_fwd(ha, Wa, lib=lib)[0]
+    rev = oracle.linear_kl_fwd(ha, Wa, hb, Wb, oracle.REVERSE, lib=lib)[0]
+    fwd = oracle.linear_kl_fwd(ha, Wa, hb, Wb, oracle.FORWARD, lib=lib)[0]
+    with localcontext() as ctx:
+        ctx.prec = 60
+        za, zb = _dlogits(ha, Wa), _dlogits(hb, Wb)
+        for r in range(3):
+            _close(H[r], float(_dentropy(za[r])), 1e-14, 1e-14, "linear entropy brute force")
+            _close(rev[r], float(_dkl(za[r], zb[r])), 1e-14, 1e-13, "linear KL(A||B) brute force")
+            _close(fwd[r], float(_dkl(zb[r], za[r])), 1e-14, 1e-13, "linear KL(B||A) brute force")
+
+
+def _fd(f, x, eps=1e-6):
+    out = np.empty_like(x)
+    for i in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[i] += eps
+        xm[i] -= eps
+        out[i] = (f(xp) - f(xm)) / (2 * eps)
+    return out
+
+
+def pin_linear_entropy_kl_finite_differences(lib=None):
+    ha, Wa, hb, Wb, g = _two_models(62, 3, 5, 3, 4)
+    dh, dW = oracle.linear_entropy_bwd(ha, Wa, g, lib=lib)
+    H = lambda h, W: float(np.dot(g, oracle.linear_entropy_fwd(h, W, lib=lib)[0]))
+    _close(dh, _fd(lambda x: H(x, Wa), ha), 1e-8, 1e-6, "linear entropy dhidden FD")
+    _close(dW, _fd(lambda x: H(ha, x), Wa), 1e-8, 1e-6, "linear entropy dW FD")
+    for d in (oracle.REVERSE, oracle.FORWARD):
+        dha, dWa, dhb, dWb = oracle.linear_kl_bwd(ha, Wa, hb, Wb, g, d, lib=lib)
+        K = lambda a, b, c, e: float(np.dot(g, oracle.linear_kl_fwd(a, b, c, e, d, lib=lib)[0]))
+        _close(dha, _fd(lambda x: K(x, Wa, hb, Wb), ha), 1e-8, 1e-6, f"linear KL dir {d} dha FD")
+        _close(dWa, _fd(lambda x: K(ha, x, hb, Wb), Wa), 1e-8, 1e-6, f"linear KL dir {d} dWa FD")
+        _close(dhb, _fd(lambda x: K(ha, Wa, x, Wb), hb), 1e-8, 1e-6, f"linear KL dir {d} dhb FD")
+        _close(dWb, _fd(lambda x: K(ha, Wa, hb, x), Wb), 1e-8, 1e-6, f"linear KL dir {d} dWb FD")
+
+
+def pin_linear_entropy_kl_closed_forms(lib=None):
+    N, V, D = 4, 7, 5
+    ha, Wa, hb, Wb, g = _two_models(63, N, V, D, D + 2)
+    # a zero LM head: uniform distribution, H = log V, zero gradients
+    H = oracle.linear_entropy_fwd(ha, np.zeros((V, D)), lib=lib)[0]
+    _close(H, np.full(N, math.log(V)), 1e-15, 1e-15, "linear entropy of a zero head")
+    dh, dW = oracle.linear_entropy_bwd(ha, np.zeros((V, D)), g, lib=lib)
+    _close(dh, np.zeros_like(dh), 1e-15, 0, "zero-head entropy dhidden")
+    _close(dW, np.zeros_like(dW), 1e-15, 0, "zero-head entropy dW")
+    # model B = model A with two extra hidden units that its head ignores: KL = 0, gradients 0
+    hpad = np.concatenate([ha, hb[:, :2]], 1)
+    Wpad = np.concatenate([Wa, np.zeros((V, 2))], 1)
+    for d in (oracle.REVERSE, oracle.FORWARD):
+        assert (oracle.linear_kl_fwd(ha, Wa, hpad, Wpad, d, lib=lib)[0] == 0).all(), "KL of a model with itself"
+        for o in oracle.linear_kl_bwd(ha, Wa, hpad, Wpad, g, d, lib=lib):
+            assert (o == 0).all(), "gradients of KL of a model with itself"
+    # forward KL of (A, B) is reverse KL of (B, A)
+    _close(oracle.linear_kl_fwd(ha, Wa, hb, Wb, oracle.FORWARD, lib=lib)[0],
+           oracle.linear_kl_fwd(hb, Wb, ha, Wa, oracle.REVERSE, lib=lib)[0], 1e-15, 1e-15, "KL direction swap")
+
+
 ALL_PINS = [
     pin_brute_force_fwd,
     pin_brute_force_grads,
@@ -692,4 +766,7 @@ ALL_PINS = [
     pin_jsd_special_rows,
     pin_linear_logp_brute_force,
     pin_linear_logp_finite_differences,
+    pin_linear_entropy_kl_brute_force,
+    pin_linear_entropy_kl_finite_differences,
+    pin_linear_entropy_kl_closed_forms,
 ]

@@ -69,6 +69,15 @@ MUTANTS = [
     ("linear dW wrong row", "out[k] += c * h[r * D + k];", "out[k] += c * h[((r + 1) % N) * D + k];"),
     ("linear dh wrong vocab row", "out[k] += c * W[j * D + k];", "out[k] += c * W[((j + 1) % V) * D + k];"),
     ("linear bwd onehot dropped", "z[j] = g[r] * (((j == loc) ? 1.0 : 0.0) - p);", "z[j] = g[r] * (0.0 - p);"),
+    ("linear chain rule dz transposed", "double c = dz[r * V + j];", "double c = dz[j * N + r];"),
+    ("linear chain rule dW from the wrong hidden column", "for (int64_t r = 0; r < N; ++r) {\n                double c = dz[r * V + j];\n                for (int64_t k = 0; k < D; ++k) out[k] += c * h[r * D + k];",
+     "for (int64_t r = 0; r < N; ++r) {\n                double c = dz[r * V + j];\n                for (int64_t k = 0; k < D; ++k) out[k] += c * h[r * D + (D - 1 - k)];"),
+    ("linear KL model B with model A's width", "vpo_linear_logits(hb, Wb, N, V, Db, zb);\n    vpo_kl_fwd",
+     "vpo_linear_logits(hb, Wb, N, V, Da, zb);\n    vpo_kl_fwd"),
+    ("linear KL bwd gradients of A and B swapped", "linear_chain_rule(ha, Wa, N, V, Da, dza, dha, dWa);",
+     "linear_chain_rule(ha, Wa, N, V, Da, dzb, dha, dWa);"),
+    ("linear entropy bwd reads logits as dz", "linear_chain_rule(h, W, N, V, D, dz, dh, dW);",
+     "linear_chain_rule(h, W, N, V, D, logits, dh, dW);"),
 ]
 
 
