@@ -192,20 +192,22 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
                     Elem<T>::unpack(u[k], z);
                     const int64_t j0 = head + (int64_t)i * kVec;
                     if (kOp == 0 && !Elem<T>::kPrecise) {
-                        // every element as a non-target; the vector holding the target fixes it up
+                        // every element as a non-target; the target is rewritten below
 #pragma unroll
                         for (int e = 0; e < kVec; ++e) d[e] = grad_elem<0, T>(z[e], 0, s, g, -1);
-                        if (loc >= j0 && loc < j0 + kVec) {
-#pragma unroll
-                            for (int e = 0; e < kVec; ++e)
-                                if (j0 + e == loc) d[e] = grad_elem<0, T>(z[e], loc, s, g, loc);
-                        }
                     } else {
 #pragma unroll
                         for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, s, g, loc);
                     }
                     stg_stream(vout + i, Elem<T>::pack(d));
                 }
+            }
+            if (kOp == 0 && !Elem<T>::kPrecise && loc >= head && loc < tail0) {
+                // the thread that stored the target's vector rewrites the target element
+                // (same thread, same address: the later store wins)
+                const int it = (int)((loc - head) / kVec);
+                if (it >= v0 && it < v1 && (it - v0) % kBwdThreads == tid)
+                    Elem<T>::store1(out + loc, grad_elem<0, T>(Elem<T>::load1(in + loc), loc, s, g, loc));
             }
         } else {
             const int64_t e0 = (int64_t)seg * kTileVec * kVec;
