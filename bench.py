@@ -322,42 +322,41 @@ def jsd_bench(args, a, b, g, dev, peaks, beta=0.5):
                                   "bwd": round(2 * E2 / (tb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
+def _time_ms(fn, reps):
+    """Mean ms of fn over reps calls, CUDA events on the current stream, after one untimed call."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def linear_bench(args, dev, N=8192, V=75968, D=4096):
-    """Fused linear logp forward on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16)."""
+    """Fused linear ops on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16): logp, entropy and
+    KL against a second model of the same shape, forward and backward."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     from vocab_wide_logprobs_gb300 import workloads
     w = workloads.linear(N=N, V=V, D=D)
     h, W, t = w["hidden"].to(dev), w["weight"].to(dev), w["targets"].to(dev)
+    g = w["grad"].to(dev)
     logp = torch.empty(N, dtype=torch.float32, device=dev)
     st = vp.rowstats(N, dev)
     ws = torch.empty(vp.vp_linear_logp_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
-    run = lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws)
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
+    for _ in range(2):
+        vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws)
     reps = max(3, min(args.steps, 10))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        run()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    g = w["grad"].to(dev)
+    ms = _time_ms(lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws), reps)
     dh = torch.empty_like(h)
     dW = torch.empty_like(W)
     wsb = torch.empty(vp.vp_linear_logp_bwd_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
-    runb = lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb)
-    runb()
-    torch.cuda.synchronize()
-    breps = 3
-    e0.record()
-    for _ in range(breps):
-        runb()
-    e1.record()
-    torch.cuda.synchronize()
-    ms_b = e0.elapsed_time(e1) / breps
+    ms_b = _time_ms(lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb), 3)
+    del wsb
     flops = 2.0 * N * V * D
     peak = None
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -366,14 +365,46 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
             peak = json.load(f).get("bf16_tflops")
     tf = flops / (ms * 1e-3) / 1e12
     tfb = 3 * flops / (ms_b * 1e-3) / 1e12
+    frac = lambda x: round(x / peak, 4) if peak else None
+
+    # entropy of the same model
+    H = torch.empty(N, dtype=torch.float32, device=dev)
+    wse = torch.empty(max(vp._lib.lib().vp_linear_entropy_bwd_workspace_size(N, V, D),
+                          vp._lib.lib().vp_linear_entropy_workspace_size(N, V, D)), dtype=torch.uint8, device=dev)
+    ms_ef = _time_ms(lambda: vp.vp_linear_entropy_fwd(h, W, H=H, stats=st, workspace=wse), reps)
+    ms_eb = _time_ms(lambda: vp.vp_linear_entropy_bwd(h, W, st, g, dhidden=dh, dW=dW, workspace=wse), 3)
+    del wse
+    # KL(A||B) against a second model (teacher) of the same shape, gradients to both models
+    tw = workloads.linear(seed=14, N=N, V=V, D=D)
+    hb, Wb = tw["hidden"].to(dev), tw["weight"].to(dev)
+    del tw
+    kl = torch.empty(N, dtype=torch.float32, device=dev)
+    sb = vp.rowstats(N, dev)
+    wsk = torch.empty(vp._lib.lib().vp_linear_kl_bwd_workspace_size(N, V, D, D), dtype=torch.uint8, device=dev)
+    outs = [dh, dW, torch.empty_like(hb), torch.empty_like(Wb)]
+    ms_kf = _time_ms(lambda: vp.vp_linear_kl_fwd(h, W, hb, Wb, vp.KL_REVERSE, kl=kl, stats_a=st, stats_b=sb,
+                                                 workspace=wsk), reps)
+    ms_kb = _time_ms(lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, vp.KL_REVERSE, st, sb, g, outs=outs, workspace=wsk), 3)
+    del wsk, outs, hb, Wb
+    torch.cuda.empty_cache()
+
+    def line(fwd_ms, bwd_ms, fwd_gemms, bwd_gemms, what):
+        a, b = fwd_gemms * flops / (fwd_ms * 1e-3) / 1e12, bwd_gemms * flops / (bwd_ms * 1e-3) / 1e12
+        return {"workload": what, "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+                "fwd_tflops": round(a, 1), "bwd_tflops": round(b, 1), "fwd_frac": frac(a), "bwd_frac": frac(b),
+                "flops": {"fwd": fwd_gemms * flops, "bwd": bwd_gemms * flops}}
+
     return {"workload": f"hidden [{N},{D}] x W [{V},{D}] bf16, logp of uniform targets", "fwd_ms": round(ms, 4),
             "bwd_ms": round(ms_b, 4),
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
                          "peak_src": "measured bf16 burst" if peak else None,
-                         "frac": round(tf / peak, 4) if peak else None, "flops": flops},
+                         "frac": frac(tf), "flops": flops},
             "bwd_roofline": {"bound": "tensor", "achieved": round(tfb, 1), "peak": peak, "unit": "TFLOP/s",
-                             "frac": round(tfb / peak, 4) if peak else None, "flops": 3 * flops,
-                             "note": "three GEMMs of 2NVD each (logits recomputed, dhidden, dW)"}}
+                             "frac": frac(tfb), "flops": 3 * flops,
+                             "note": "three GEMMs of 2NVD each (logits recomputed, dhidden, dW)"},
+            "entropy": line(ms_ef, ms_eb, 1, 3, "entropy of softmax(h W^T); backward: logits, dhidden, dW"),
+            "kl": line(ms_kf, ms_kb, 2, 6, "KL(A||B) of two models of this shape; forward: both logits tiles; "
+                       "backward: both logits tiles, dhidden and dW of both models")}
 
 
 def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev, chunks=8):

@@ -430,13 +430,90 @@ VP_API vp_status vp_linear_logp_fwd_noalloc(const void *hidden, const void *weig
                                             vp_rowstat *stats, int32_t *err_word, vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused linear entropy and KL [P1, the commit message adding               */
+/* vocab_parallel_jsd, "Motivation": teacher-student divergences computed    */
+/* from tiled LM-head projections without the full logits; P2,              */
+/* "Implementation" and the review nitpick on the chunked backward]          */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace vp_linear_entropy_fwd needs: a 16-byte record per
+ * row and 256-column vocabulary tile. 0 for invalid sizes. */
+VP_API size_t vp_linear_entropy_workspace_size(int64_t N, int64_t V, int64_t D);
+
+/* H[r] = entropy of softmax(h_r . W^T) over the V rows of W, without
+ * materialising the logits: tcgen05 tiles (bf16 inputs, fp32 accumulation in
+ * TMEM) whose epilogue takes, per row and tile, the max m, S = sum e^{z-m} and
+ * W = sum e^{z-m} (z-m); a merge per row re-centres the tiles on the row max
+ * and writes H = log S - W / S [P1, second commit message]. hidden: bf16
+ * [N, D]; weight: bf16 [V, D]; row-major, 16-byte aligned, D a multiple of 64.
+ * Outputs: H fp32 [N] and stats (vp_rowstat [N]: m = max logit, logS,
+ * c = W / S) for the backward. workspace: at least
+ * vp_linear_entropy_workspace_size(N, V, D) bytes, 256-byte aligned, caller
+ * owned, scratch. A row whose logits hold NaN or +inf gives NaN. */
+VP_API vp_status vp_linear_entropy_fwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                       float *H, vp_rowstat *stats, void *workspace, size_t workspace_bytes,
+                                       vp_stream stream);
+
+/* Bytes of device workspace vp_linear_entropy_bwd needs: dz of one vocabulary
+ * chunk (bf16 [N, vc], vc as for vp_linear_logp_bwd_workspace_size) and an fp32
+ * accumulator of dhidden ([N, D]). 0 for invalid sizes. */
+VP_API size_t vp_linear_entropy_bwd_workspace_size(int64_t N, int64_t V, int64_t D);
+
+/* Gradients of sum_r g[r] H[r]: per vocabulary chunk the logits tile is
+ * recomputed and dz = -g p (log p + H) = -g p ((z - m) - c) formed in the
+ * epilogue and rounded to bf16, then dhidden += dz . W_c and dW_c = dz^T . h
+ * (as vp_linear_logp_bwd). dhidden: bf16 [N, D]; dW: bf16 [V, D]; either may
+ * be NULL (not both). stats: the records of vp_linear_entropy_fwd. Rows
+ * without valid statistics make their dhidden row and all of dW NaN. */
+VP_API vp_status vp_linear_entropy_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                       const vp_rowstat *stats, const float *grad_out, void *dhidden, void *dW,
+                                       void *workspace, size_t workspace_bytes, vp_stream stream);
+
+/* Bytes of device workspace vp_linear_kl_fwd needs: a 32-byte record per row
+ * and 256-column vocabulary tile. 0 for invalid sizes. */
+VP_API size_t vp_linear_kl_workspace_size(int64_t N, int64_t V);
+
+/* KL between the next-token distributions of two models over the same V
+ * vocabulary rows: model A (hidden ha bf16 [N, Da], head wa bf16 [V, Da]) and
+ * model B (hb bf16 [N, Db], wb bf16 [V, Db]); each model has its own hidden
+ * size (Da, Db multiples of 64). direction VP_KL_REVERSE gives KL(A||B),
+ * VP_KL_FORWARD gives KL(B||A), as vp_kl_fwd. One dual tcgen05 GEMM puts the
+ * same logits tile of both models in TMEM; the epilogue takes each tile's
+ * maxima, sum-exps and W = sum e^{P-m_P} ((P - m_P) - (Q - m_Q)), and a merge
+ * per row re-centres the tiles and writes KL = W / S_P - log S_P + log S_Q.
+ * Outputs: kl fp32 [N]; stats_a, stats_b (vp_rowstat [N] each, the records of
+ * vp_kl_fwd). workspace: at least vp_linear_kl_workspace_size(N, V) bytes,
+ * 256-byte aligned. A row whose logits hold NaN or +inf gives NaN. */
+VP_API vp_status vp_linear_kl_fwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
+                                  int64_t V, int64_t Da, int64_t Db, int direction, float *kl, vp_rowstat *stats_a,
+                                  vp_rowstat *stats_b, void *workspace, size_t workspace_bytes, vp_stream stream);
+
+/* Bytes of device workspace vp_linear_kl_bwd needs: dz of one vocabulary chunk
+ * for each model (bf16 [N, vc] twice) and fp32 accumulators of both dhidden
+ * ([N, Da] and [N, Db]). 0 for invalid sizes. */
+VP_API size_t vp_linear_kl_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t Db);
+
+/* Gradients of sum_r g[r] KL[r] with respect to both models' hidden states
+ * and heads: per vocabulary chunk the dual GEMM recomputes both logits tiles,
+ * the epilogue forms dP = g p ((P - m_P) - (Q - m_Q) - c) and dQ = g (q - p)
+ * (rounded to bf16), and the gradient GEMMs of each model follow. dha bf16
+ * [N, Da], dwa bf16 [V, Da], dhb bf16 [N, Db], dwb bf16 [V, Db]: any may be
+ * NULL (not all); a model with neither output (a frozen teacher) costs no
+ * gradient GEMMs. stats_a, stats_b: the records of vp_linear_kl_fwd with the
+ * same direction. NaN rows give NaN dhidden rows and NaN heads' gradients. */
+VP_API vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
+                                  int64_t V, int64_t Da, int64_t Db, int direction, const vp_rowstat *stats_a,
+                                  const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
+                                  void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
 /* Misc                                                                      */
 /* ------------------------------------------------------------------------ */
 
 /* Reads the library's device fault word of the current device into *value
  * and, when `clear` is non-zero, resets it. The word is non-zero only if a
  * kernel's bounded wait on its copy pipeline gave up (bits 0-1: the forward
- * scans' producer / consumers; bits 2-4: the linear-logp producer / MMA /
+ * scans' producer / consumers; bits 2-4: the fused-linear GEMMs' producer / MMA /
  * epilogue); that kernel then skipped its outputs and returned instead of
  * spinning. Unlike every other call, this one synchronises with the device.
  * (No counterpart on the pages: a safety net of this implementation.) */

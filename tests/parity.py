@@ -234,3 +234,28 @@ def compare_all(got: dict, ref: dict, rows=None, tag=""):
         else:
             worst[k] = check_out(sel(gk), r, f"{tag}{k}")
     return worst
+
+
+# ---------------------------------------------------------------------------
+# Gradients of the fused linear ops: dz is rounded to bf16 for the two gradient
+# GEMMs, so each output is held to one bf16 ulp plus the forward error bound of
+# a dot product with bf16-rounded dz and fp32 accumulation: 2^-8 sum |dz| |operand|.
+# Where dz itself is a difference that can cancel (the entropy and KL
+# gradients), the fp32 evaluation error of dz enters as well: the elementwise
+# rule KAPPA_BF16 2^-24 M_j carried through the same dot product,
+# KAPPA_BF16 2^-24 sum M_j |operand| (eval_mag).
+# ---------------------------------------------------------------------------
+GEMM_KAPPA = 2.0 ** -8
+
+
+def check_gemm_grad(got, ref, mag, what, eval_mag=None):
+    g = to64(got)
+    r = rne_bf16(ref)
+    _placement(g, r, what)
+    fin = np.isfinite(r)
+    err = np.abs(g[fin] - r[fin])
+    tol = ulp_bf16(r[fin]) + GEMM_KAPPA * mag[fin]
+    if eval_mag is not None:
+        tol = tol + KAPPA_BF16 * 2.0 ** -24 * eval_mag[fin]
+    assert (err <= tol).all(), f"{what}: worst err/tol {(err / tol).max():.3f}, {(err > tol).sum()} bad of {err.size}"
+    return float((err / tol).max())

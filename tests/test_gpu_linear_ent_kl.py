@@ -1,0 +1,203 @@
+"""GPU parity of the fused linear entropy and the fused linear KL of two models (tcgen05 path)
+against the fp64 oracle.
+
+Forward outputs (H, KL) at 2e-5 + 2e-5 relative, the records' maxima and log-sums
+likewise (fp32 accumulations against fp64 logits); gradients (dhidden, dW of each
+model) at one bf16 ulp plus the forward error bound of a GEMM with bf16-rounded
+dz (parity.check_gemm_grad). Shapes span several 128-row and 256-column tiles
+with ragged edges, several backward vocabulary chunks, models of different
+hidden sizes, both KL directions, a frozen model, a model compared with itself
+(exactly 0) and batch invariance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import vocab_wide_logprobs_gb300 as vp
+from vocab_wide_logprobs_gb300 import workloads
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _model(seed, N, V, D, scale=25.0):
+    """hidden ~ N(0, 1), head ~ N(0, (0.02 scale)^2): logits with a spread of several units."""
+    w = workloads.linear(seed=seed, N=N, V=V, D=D)
+    return w["hidden"], (w["weight"].float() * scale).to(torch.bfloat16), w["grad"]
+
+
+# ---------------------------------------------------------------------------
+# Entropy
+# ---------------------------------------------------------------------------
+ENT_SHAPES = [(256, 1024, 256), (200, 777, 128), (130, 300, 64), (64, 4096, 1024), (72, 70000, 64)]
+
+
+@pytest.mark.parametrize("N,V,D", ENT_SHAPES)
+def test_linear_entropy_fwd_bwd(N, V, D):
+    h, W, g = _model(N + 3 * V + D, N, V, D)
+    hd, Wd, gd = h.to(DEV), W.to(DEV), g.to(DEV)
+    H, st = vp.vp_linear_entropy_fwd(hd, Wd)
+    dh, dW = vp.vp_linear_entropy_bwd(hd, Wd, st, gd)
+    torch.cuda.synchronize()
+    h64, W64, g64 = parity.to64(h), parity.to64(W), g.double().numpy()
+    rH, rm, rls = oracle.linear_entropy_fwd(h64, W64)
+    parity.check_out(H, rH, f"{N}x{V}x{D} H")
+    d = vp.decode_rowstats(st)
+    parity.check_out(d["m"], rm, f"{N}x{V}x{D} max logit")
+    parity.check_out(d["logS"], rls, f"{N}x{V}x{D} logS")
+    rdh, rdW = oracle.linear_entropy_bwd(h64, W64, g64)
+    z = oracle.linear_logits(h64, W64)
+    dz = np.abs(oracle.entropy_bwd(z, g64))
+    M = parity.oracle_all(z, z, np.zeros(N, np.int64), g64, ops=("entropy",))["_mag"]["dH"]
+    parity.check_gemm_grad(dh, rdh, dz @ np.abs(W64), f"{N}x{V}x{D} entropy dhidden", M @ np.abs(W64))
+    parity.check_gemm_grad(dW, rdW, dz.T @ np.abs(h64), f"{N}x{V}x{D} entropy dW", M.T @ np.abs(h64))
+
+
+def test_linear_entropy_single_outputs_and_batch_invariance():
+    N, V, D = 384, 2000, 256
+    h, W, g = (t.to(DEV) for t in _model(7, N, V, D))
+    H, st = vp.vp_linear_entropy_fwd(h, W)
+    dh, dW = vp.vp_linear_entropy_bwd(h, W, st, g)
+    dh_only, none_w = vp.vp_linear_entropy_bwd(h, W, st, g, want_dW=False)
+    none_h, dW_only = vp.vp_linear_entropy_bwd(h, W, st, g, want_dhidden=False)
+    part, _ = vp.vp_linear_entropy_fwd(h[128:256].contiguous(), W)
+    torch.cuda.synchronize()
+    assert none_w is None and none_h is None
+    assert torch.equal(dh_only, dh) and torch.equal(dW_only, dW)
+    assert torch.equal(H[128:256].view(torch.int32), part.view(torch.int32))
+
+
+def test_linear_entropy_zero_head_is_uniform():
+    N, V, D = 130, 1000, 128
+    h = _model(8, N, V, D)[0].to(DEV)
+    W = torch.zeros(V, D, dtype=torch.bfloat16, device=DEV)
+    g = torch.randn(N, generator=torch.Generator().manual_seed(8)).to(DEV)
+    H, st = vp.vp_linear_entropy_fwd(h, W)
+    dh, dW = vp.vp_linear_entropy_bwd(h, W, st, g)
+    torch.cuda.synchronize()
+    parity.check_out(H, np.full(N, np.log(V)), "zero head H")
+    assert (dh == 0).all() and (dW == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# KL of two models
+# ---------------------------------------------------------------------------
+KL_SHAPES = [(256, 1024, 256, 128), (200, 777, 128, 192), (130, 300, 64, 64), (72, 70000, 64, 128)]
+
+
+def _kl_case(N, V, Da, Db, seed):
+    ha, Wa, g = _model(seed, N, V, Da)
+    hb, Wb, _ = _model(seed + 1, N, V, Db, scale=20.0)
+    return ha, Wa, hb, Wb, g
+
+
+def _check_kl(ha, Wa, hb, Wb, g, direction, tag):
+    dev = [t.to(DEV) for t in (ha, Wa, hb, Wb, g)]
+    kl, sa, sb = vp.vp_linear_kl_fwd(*dev[:4], direction)
+    grads = vp.vp_linear_kl_bwd(*dev[:4], direction, sa, sb, dev[4])
+    torch.cuda.synchronize()
+    ha64, Wa64, hb64, Wb64 = (parity.to64(t) for t in (ha, Wa, hb, Wb))
+    g64 = g.double().numpy()
+    rkl, rma, rla, rmb, rlb = oracle.linear_kl_fwd(ha64, Wa64, hb64, Wb64, direction)
+    parity.check_out(kl, rkl, f"{tag} KL")
+    for st, rm, rl, name in ((sa, rma, rla, "A"), (sb, rmb, rlb, "B")):
+        d = vp.decode_rowstats(st)
+        parity.check_out(d["m"], rm, f"{tag} max logit of {name}")
+        parity.check_out(d["logS"], rl, f"{tag} logS of {name}")
+    ref = oracle.linear_kl_bwd(ha64, Wa64, hb64, Wb64, g64, direction)
+    za, zb = oracle.linear_logits(ha64, Wa64), oracle.linear_logits(hb64, Wb64)
+    dza, dzb = (np.abs(x) for x in oracle.kl_bwd(za, zb, g64, direction))
+    op = "kl_rev" if direction == vp.KL_REVERSE else "kl_fwd"
+    M = parity.oracle_all(za, zb, np.zeros(za.shape[0], np.int64), g64, ops=(op,))["_mag"]
+    Ma, Mb = M["d" + op + "_a"], M["d" + op + "_b"]
+    mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
+    evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
+    for got, r, mg, ev, name in zip(grads, ref, mags, evals, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, mg, f"{tag} {name}", ev)
+    return kl, grads
+
+
+@pytest.mark.parametrize("direction", [vp.KL_REVERSE, vp.KL_FORWARD], ids=["reverse", "forward"])
+@pytest.mark.parametrize("N,V,Da,Db", KL_SHAPES)
+def test_linear_kl_fwd_bwd(N, V, Da, Db, direction):
+    _check_kl(*_kl_case(N, V, Da, Db, seed=N + V + Da + Db), direction, f"{N}x{V} Da={Da} Db={Db} dir={direction}")
+
+
+def test_linear_kl_close_models():
+    """A student close to its teacher: small KL, cancellation in the W sums."""
+    N, V, D = 192, 3000, 128
+    ha, Wa, g = _model(31, N, V, D)
+    gen = torch.Generator().manual_seed(32)
+    Wb = (Wa.float() + 0.01 * torch.randn(V, D, generator=gen)).to(torch.bfloat16)
+    hb = (ha.float() + 0.01 * torch.randn(N, D, generator=gen)).to(torch.bfloat16)
+    for d in (vp.KL_REVERSE, vp.KL_FORWARD):
+        kl, _ = _check_kl(ha, Wa, hb, Wb, g, d, f"close models dir={d}")
+        assert float(kl.max()) < 0.05
+
+
+def test_linear_kl_model_with_itself_and_frozen_teacher():
+    N, V, Da, Db = 136, 1500, 128, 64
+    ha, Wa, hb, Wb, g = (t.to(DEV) for t in _kl_case(N, V, Da, Db, seed=41))
+    for d in (vp.KL_REVERSE, vp.KL_FORWARD):
+        kl, sa, sb = vp.vp_linear_kl_fwd(ha, Wa, ha, Wa, d)
+        zero = vp.vp_linear_kl_bwd(ha, Wa, ha, Wa, d, sa, sb, g)
+        torch.cuda.synchronize()
+        assert (kl == 0).all(), "KL of a model with itself"
+        assert all((z == 0).all() for z in zero)
+        kl, sa, sb = vp.vp_linear_kl_fwd(ha, Wa, hb, Wb, d)
+        full = vp.vp_linear_kl_bwd(ha, Wa, hb, Wb, d, sa, sb, g)
+        student = vp.vp_linear_kl_bwd(ha, Wa, hb, Wb, d, sa, sb, g, want=(True, True, False, False))
+        head_b = vp.vp_linear_kl_bwd(ha, Wa, hb, Wb, d, sa, sb, g, want=(False, False, False, True))
+        torch.cuda.synchronize()
+        assert student[2] is None and student[3] is None and head_b[0] is None
+        assert torch.equal(student[0], full[0]) and torch.equal(student[1], full[1])
+        assert torch.equal(head_b[3], full[3])
+
+
+def test_linear_kl_batch_invariance():
+    N, V, Da, Db = 384, 2000, 128, 256
+    ha, Wa, hb, Wb, _ = (t.to(DEV) for t in _kl_case(N, V, Da, Db, seed=51))
+    kl, _, _ = vp.vp_linear_kl_fwd(ha, Wa, hb, Wb)
+    part, _, _ = vp.vp_linear_kl_fwd(ha[128:256].contiguous(), Wa, hb[128:256].contiguous(), Wb)
+    torch.cuda.synchronize()
+    assert torch.equal(kl[128:256].view(torch.int32), part.view(torch.int32))
+
+
+def test_linear_ent_kl_argument_errors():
+    h = torch.zeros(4, 96, dtype=torch.bfloat16, device=DEV)     # D not a multiple of 64
+    W = torch.zeros(8, 96, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(vp.VPError):
+        vp.vp_linear_entropy_fwd(h, W)
+    h = torch.zeros(4, 64, dtype=torch.bfloat16, device=DEV)
+    W = torch.zeros(8, 64, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(vp.VPError):
+        vp.vp_linear_kl_fwd(h, W, h, W, direction=2)
+    H, st = vp.vp_linear_entropy_fwd(h[:0], W)
+    assert H.numel() == 0
+
+
+# ---------------------------------------------------------------------------
+# Full size: hidden [8192, 4096] x W [75968, 4096], sampled rows
+# ---------------------------------------------------------------------------
+@pytest.mark.slow
+def test_linear_entropy_kl_full_size_sampled():
+    w = workloads.linear()
+    t = workloads.linear(seed=14)
+    ha, Wa, hb, Wb, g = (x.to(DEV) for x in (w["hidden"], w["weight"], t["hidden"], t["weight"], w["grad"]))
+    H, st = vp.vp_linear_entropy_fwd(ha, Wa)
+    kl, sa, sb = vp.vp_linear_kl_fwd(ha, Wa, hb, Wb)
+    dha, dWa = vp.vp_linear_entropy_bwd(ha, Wa, st, g)
+    torch.cuda.synchronize()
+    rows = [0, 777, 8191]
+    h64, W64, hb64, Wb64 = (parity.to64(x) for x in (w["hidden"][rows], w["weight"], t["hidden"][rows], t["weight"]))
+    parity.check_out(H[rows], oracle.linear_entropy_fwd(h64, W64)[0], "full-size H")
+    parity.check_out(kl[rows], oracle.linear_kl_fwd(h64, W64, hb64, Wb64)[0], "full-size KL")
+    g64 = w["grad"][rows].double().numpy()
+    rdh, _ = oracle.linear_entropy_bwd(h64, W64, g64, want_dW=False)
+    z = oracle.linear_logits(h64, W64)
+    dz = np.abs(oracle.entropy_bwd(z, g64))
+    M = parity.oracle_all(z, z, np.zeros(len(rows), np.int64), g64, ops=("entropy",))["_mag"]["dH"]
+    parity.check_gemm_grad(dha[rows], rdh, dz @ np.abs(W64), "full-size entropy dhidden", M @ np.abs(W64))
+    assert torch.isfinite(dWa).all()

@@ -29,6 +29,10 @@ SIGNATURES = {
     "vp_linear_logp_fwd": [P, P, I64, I64, I64, I64, P, P, P, P, ctypes.c_size_t, P, P],
     "vp_linear_logp_fwd_noalloc": [P, P, I64, I64, I64, I64, P, P, P, P, P],
     "vp_linear_logp_bwd": [P, P, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_size_t, P, P],
+    "vp_linear_entropy_fwd": [P, P, I64, I64, I64, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_entropy_bwd": [P, P, I64, I64, I64, P, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_kl_fwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_kl_bwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
     "vp_jsd_fwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P],
     "vp_jsd_bwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P],
     "vp_logprobs_partial": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P],
@@ -61,6 +65,13 @@ def lib():
             h.vp_linear_logp_workspace_size.restype = ctypes.c_size_t
             h.vp_linear_logp_bwd_workspace_size.argtypes = [I64, I64, I64]
             h.vp_linear_logp_bwd_workspace_size.restype = ctypes.c_size_t
+            for name, args in (("vp_linear_entropy_workspace_size", [I64, I64, I64]),
+                               ("vp_linear_entropy_bwd_workspace_size", [I64, I64, I64]),
+                               ("vp_linear_kl_workspace_size", [I64, I64]),
+                               ("vp_linear_kl_bwd_workspace_size", [I64, I64, I64, I64])):
+                fn = getattr(h, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_size_t
             h.vp_fault_status.argtypes = [P, I32]
             h.vp_fault_status.restype = ctypes.c_int
             h.vp_version.argtypes = []

@@ -302,6 +302,89 @@ def vp_linear_logp_fwd_noalloc(hidden, weight, targets, vocab_start: int = 0, er
 
 
 # ---------------------------------------------------------------------------
+# Fused linear entropy and KL (logits never materialised)
+# ---------------------------------------------------------------------------
+def _linear_model(hidden, weight, what):
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise VPError(3, f"{what} takes bf16 hidden and weight")
+    if not (hidden.is_contiguous() and weight.is_contiguous()) or hidden.dim() != 2 or weight.dim() != 2:
+        raise VPError(4, "hidden and weight must be contiguous 2-D tensors")
+    if weight.shape[1] != hidden.shape[1]:
+        raise VPError(2, "hidden and weight disagree on D")
+    return hidden.shape[0], weight.shape[0], hidden.shape[1]
+
+
+def _workspace(nbytes, like):
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=like.device)
+
+
+def vp_linear_entropy_fwd(hidden, weight, H=None, stats=None, workspace=None):
+    """Entropy of softmax(hidden @ weight^T) per row; returns (H fp32 [N], stats)."""
+    N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_fwd")
+    H = _f32(N, hidden) if H is None else H
+    stats = rowstats(N, hidden.device) if stats is None else stats
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_entropy_workspace_size(N, V, D), hidden)
+    _check(_lib.lib().vp_linear_entropy_fwd(_ptr(hidden), _ptr(weight), N, V, D, _ptr(H), _ptr(stats),
+                                            _ptr(workspace), workspace.numel(), _stream()), "vp_linear_entropy_fwd")
+    return H, stats
+
+
+def vp_linear_entropy_bwd(hidden, weight, stats, grad, want_dhidden=True, want_dW=True, dhidden=None, dW=None,
+                          workspace=None):
+    """Gradients of sum_r grad[r] H[r]: (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None)."""
+    N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_bwd")
+    dhidden = (torch.empty((N, D), dtype=torch.bfloat16, device=hidden.device) if dhidden is None else dhidden) \
+        if want_dhidden else None
+    dW = (torch.empty((V, D), dtype=torch.bfloat16, device=hidden.device) if dW is None else dW) if want_dW else None
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_entropy_bwd_workspace_size(N, V, D), hidden)
+    _check(_lib.lib().vp_linear_entropy_bwd(_ptr(hidden), _ptr(weight), N, V, D, _ptr(stats), _ptr(grad),
+                                            _ptr(dhidden), _ptr(dW), _ptr(workspace), workspace.numel(), _stream()),
+           "vp_linear_entropy_bwd")
+    return dhidden, dW
+
+
+def _two_models(ha, wa, hb, wb, what):
+    N, V, Da = _linear_model(ha, wa, what)
+    Nb, Vb, Db = _linear_model(hb, wb, what)
+    if (Nb, Vb) != (N, V):
+        raise VPError(2, "the two models disagree on N or V")
+    return N, V, Da, Db
+
+
+def vp_linear_kl_fwd(ha, wa, hb, wb, direction: int = KL_REVERSE, kl=None, stats_a=None, stats_b=None,
+                     workspace=None):
+    """KL between softmax(ha @ wa^T) and softmax(hb @ wb^T); reverse = KL(A||B).
+    Returns (kl fp32 [N], stats_a, stats_b)."""
+    N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_fwd")
+    kl = _f32(N, ha) if kl is None else kl
+    stats_a = rowstats(N, ha.device) if stats_a is None else stats_a
+    stats_b = rowstats(N, ha.device) if stats_b is None else stats_b
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_kl_workspace_size(N, V), ha)
+    _check(_lib.lib().vp_linear_kl_fwd(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, int(direction), _ptr(kl),
+                                       _ptr(stats_a), _ptr(stats_b), _ptr(workspace), workspace.numel(), _stream()),
+           "vp_linear_kl_fwd")
+    return kl, stats_a, stats_b
+
+
+def vp_linear_kl_bwd(ha, wa, hb, wb, direction, stats_a, stats_b, grad, want=(True, True, True, True), outs=None,
+                     workspace=None):
+    """Gradients of sum_r grad[r] KL[r]: (dha, dwa, dhb, dwb), bf16, None where not wanted."""
+    N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_bwd")
+    shapes = ((N, Da), (V, Da), (N, Db), (V, Db))
+    if outs is None:
+        outs = [torch.empty(s, dtype=torch.bfloat16, device=ha.device) if w else None for s, w in zip(shapes, want)]
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_kl_bwd_workspace_size(N, V, Da, Db), ha)
+    _check(_lib.lib().vp_linear_kl_bwd(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, int(direction),
+                                       _ptr(stats_a), _ptr(stats_b), _ptr(grad), *[_ptr(o) for o in outs],
+                                       _ptr(workspace), workspace.numel(), _stream()), "vp_linear_kl_bwd")
+    return tuple(outs)
+
+
+# ---------------------------------------------------------------------------
 # Vocabulary-sharded forms: per-shard records, gathered by the caller, merged
 # ---------------------------------------------------------------------------
 def vp_logprobs_partial(x, targets, vocab_start: int = 0, parts=None):

@@ -400,14 +400,113 @@ vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int64_t N, 
     return launched(vp::launch_linear_logp_bwd(a));
 }
 
+static bool linear_dims_ok(int64_t N, int64_t V, int64_t D) {
+    return N >= 0 && N <= kMaxRowsPerLaunch && V >= 1 && V <= kMaxV && D >= 64 && D % 64 == 0 && D <= (1 << 20);
+}
+
+size_t vp_linear_entropy_workspace_size(int64_t N, int64_t V, int64_t D) {
+    if (!linear_dims_ok(N, V, D)) return 0;
+    return vp::linear_entropy_workspace_bytes(N, V);
+}
+
+vp_status vp_linear_entropy_fwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D, float *H,
+                                vp_rowstat *stats, void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, D)) return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !H || !stats || !workspace) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(H, 4) || !aligned(stats, 16) ||
+        !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_entropy_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearEntArgs a{hidden, weight, N, V, D, H, stats, nullptr, nullptr, nullptr, workspace,
+                        (cudaStream_t)stream};
+    return launched(vp::launch_linear_entropy_fwd(a));
+}
+
+size_t vp_linear_entropy_bwd_workspace_size(int64_t N, int64_t V, int64_t D) {
+    if (!linear_dims_ok(N, V, D)) return 0;
+    return vp::linear_entropy_bwd_workspace_bytes(N, V, D);
+}
+
+vp_status vp_linear_entropy_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                const vp_rowstat *stats, const float *grad_out, void *dhidden, void *dW,
+                                void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, D)) return VP_ERR_SHAPE;
+    if (!dhidden && !dW) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !stats || !grad_out || !workspace) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(stats, 16) || !aligned(grad_out, 4) ||
+        !aligned(dhidden, 16) || !aligned(dW, 16) || !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_entropy_bwd_workspace_bytes(N, V, D)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearEntArgs a{hidden, weight, N, V, D, nullptr, const_cast<vp_rowstat *>(stats), grad_out, dhidden, dW,
+                        workspace, (cudaStream_t)stream};
+    return launched(vp::launch_linear_entropy_bwd(a));
+}
+
+size_t vp_linear_kl_workspace_size(int64_t N, int64_t V) {
+    if (!linear_dims_ok(N, V, 64)) return 0;
+    return vp::linear_kl_workspace_bytes(N, V);
+}
+
+vp_status vp_linear_kl_fwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
+                           int64_t Da, int64_t Db, int direction, float *kl, vp_rowstat *stats_a,
+                           vp_rowstat *stats_b, void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!ha || !wa || !hb || !wb || !kl || !stats_a || !stats_b || !workspace) return VP_ERR_NULL;
+    if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(kl, 4) ||
+        !aligned(stats_a, 16) || !aligned(stats_b, 16) || !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_kl_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, direction, kl, stats_a, stats_b, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, workspace, (cudaStream_t)stream};
+    return launched(vp::launch_linear_kl_fwd(a));
+}
+
+size_t vp_linear_kl_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t Db) {
+    if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return 0;
+    return vp::linear_kl_bwd_workspace_bytes(N, V, Da, Db);
+}
+
+vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
+                           int64_t Da, int64_t Db, int direction, const vp_rowstat *stats_a,
+                           const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
+                           void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (!dha && !dwa && !dhb && !dwb) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!ha || !wa || !hb || !wb || !stats_a || !stats_b || !grad_out || !workspace) return VP_ERR_NULL;
+    if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(stats_a, 16) ||
+        !aligned(stats_b, 16) || !aligned(grad_out, 4) || !aligned(dha, 16) || !aligned(dwa, 16) ||
+        !aligned(dhb, 16) || !aligned(dwb, 16) || !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_kl_bwd_workspace_bytes(N, V, Da, Db)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, direction, nullptr,
+                       const_cast<vp_rowstat *>(stats_a), const_cast<vp_rowstat *>(stats_b), grad_out,
+                       dha, dwa, dhb, dwb, workspace, (cudaStream_t)stream};
+    return launched(vp::launch_linear_kl_bwd(a));
+}
+
 vp_status vp_fault_status(uint32_t *value, int clear) {
     if (!value) return VP_ERR_NULL;
     vp_status st = check_device();
     if (st != VP_OK) return st;
-    uint32_t a = 0, b = 0;
-    if (vp::read_fault(&a, clear != 0) != cudaSuccess || vp::read_linear_fault(&b, clear != 0) != cudaSuccess)
+    uint32_t a = 0, b = 0, c = 0;
+    if (vp::read_fault(&a, clear != 0) != cudaSuccess || vp::read_linear_logp_fault(&b, clear != 0) != cudaSuccess ||
+        vp::read_linear_ent_kl_fault(&c, clear != 0) != cudaSuccess)
         return VP_ERR_LAUNCH;
-    *value = a | (b << 2);
+    *value = a | ((b | c) << 2);
     return VP_OK;
 }
 

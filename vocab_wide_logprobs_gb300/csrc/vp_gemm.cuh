@@ -1,0 +1,390 @@
+// vp_gemm.cuh -- the persistent tcgen05 GEMM shared by the fused linear ops
+// (linear logp, linear entropy, linear KL), its operand tensor maps and the
+// gradient GEMMs of the chunked backward.
+//
+// Each translation unit that includes this header gets its own copy of the
+// kernels' fault word (g_linear_fault); read_linear_fault reads every copy.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "vp_device.cuh"
+#include "vp_launch.h"
+#include "vp_umma.cuh"
+
+namespace vp {
+
+constexpr int kLBM = 128, kLBN = 256, kLBK = 64;
+constexpr int kLStages = 4;
+constexpr int kLAStage = kLBM * kLBK * 2;          // 16 KB
+constexpr int kLBStage = kLBN * kLBK * 2;          // 32 KB
+constexpr int kLStageBytes = kLAStage + kLBStage;  // 48 KB
+constexpr int kLSmemBytes = kLStages * kLStageBytes + 1024;  // + alignment slack
+constexpr int kLThreads = 192;                     // TMA warp, MMA warp, 4 epilogue warps
+constexpr uint32_t kLTmemCols = 2 * kLBN;          // two accumulators
+
+// Set when a bounded wait of the linear kernels gave up.
+static __device__ uint32_t g_linear_fault;   // one per translation unit
+
+struct LinearBars {
+    uint64_t full[kLStages], empty[kLStages], acc_full[2], acc_empty[2];
+    uint32_t tmem_base;
+};
+
+// ---------------------------------------------------------------------------
+// Persistent tcgen05 GEMM C[M, Nn] = A[M, K] . B[Nn, K]^T (bf16 operands through
+// 2-D tensor maps, fp32 accumulation in TMEM) with a pluggable epilogue.
+// Operand layouts: K-major (kAMn / kBMn false: a row of the operand's tensor map
+// holds K-consecutive elements; one box of 64 x rows per stage) or MN-major
+// (true: the map's rows run along K and hold MN-consecutive elements; 64 x 64
+// boxes, 8 KB apart in shared memory), so that a transposed operand is read in
+// place. Tiles run N-major (consecutive CTAs share one B tile through L2).
+// Dual form (kDual, K-major operands only): each tile also computes a second
+// product C2 = A2 . B2^T (K2 deep) of the same shape into the other 256 TMEM
+// columns, so that an epilogue sees the same logits tile of two models at
+// once; the two accumulators fill TMEM, so there is one accumulator set and
+// the epilogue of a tile does not overlap the MMAs of the next (the producer
+// still fills the ring meanwhile).
+// The epilogue functor is called by each of the 128 epilogue threads for its
+// accumulator row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the
+// row's 256 columns; it reads them with tmem_ld32, which is warp-collective, so
+// every lane runs every load (rows past M included) and only the global
+// accesses are guarded.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kLMnAtomBytes = 64 * kLBK * 2;   // one 64 (MN) x 64 (K) box: 8 KB
+
+template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
+__global__ void __launch_bounds__(kLThreads, 1)
+umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                 const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M, int Nn,
+                 int K, int K2, const Epi epi) {
+    static_assert(!kDual || (!kAMn && !kBMn), "the dual form takes K-major operands");
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ LinearBars bars;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_mb = (M + kLBM - 1) / kLBM, n_nb = (Nn + kLBN - 1) / kLBN;
+    const int64_t n_tiles = (int64_t)n_mb * n_nb;
+    const int n_k = (K + kLBK - 1) / kLBK;
+    const int n_k2 = kDual ? (K2 + kLBK - 1) / kLBK : 0;   // k-blocks of the second product
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kLStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.acc_full[b], 1);
+            mbar_init(&bars.acc_empty[b], 4 * 32);
+        }
+        fence_mbar_init();
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
+        if (kDual) {
+            prefetch_tensormap(&tm_a2);
+            prefetch_tensormap(&tm_b2);
+        }
+    }
+    if (warp == 1) tmem_alloc(&bars.tmem_base, kLTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+                const int mb = (int)(tile % n_mb), nb = (int)(tile / n_mb);
+                for (int kb = 0; kb < n_k + n_k2; ++kb, ++it) {
+                    const uint32_t st = it % kLStages, use = it / kLStages;
+                    if (use > 0 && !mbar_wait(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
+                    uint8_t *a = smem + st * kLStageBytes;
+                    mbar_arrive_expect_tx(&bars.full[st], kLStageBytes);
+                    if (kDual && kb >= n_k) {                // second product
+                        tma_load_2d(a, &tm_a2, (kb - n_k) * kLBK, mb * kLBM, &bars.full[st]);
+                        tma_load_2d(a + kLAStage, &tm_b2, (kb - n_k) * kLBK, nb * kLBN, &bars.full[st]);
+                        continue;
+                    }
+                    if (kAMn) {
+#pragma unroll
+                        for (int i = 0; i < kLBM / 64; ++i)
+                            tma_load_2d(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK, &bars.full[st]);
+                    } else {
+                        tma_load_2d(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st]);
+                    }
+                    if (kBMn) {
+#pragma unroll
+                        for (int i = 0; i < kLBN / 64; ++i)
+                            tma_load_2d(a + kLAStage + i * kLMnAtomBytes, &tm_b, nb * kLBN + 64 * i, kb * kLBK,
+                                        &bars.full[st]);
+                    } else {
+                        tma_load_2d(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st]);
+                    }
+                }
+            }
+            if (!ok) atomicOr(&g_linear_fault, 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(kLBM, kLBN, kAMn, kBMn);
+            uint32_t it = 0, j = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++j) {
+                const uint32_t buf = kDual ? 0 : j & 1, use_b = kDual ? j : j >> 1;
+                if (use_b > 0 && !mbar_wait(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < n_k + n_k2; ++kb, ++it) {
+                    const uint32_t st = it % kLStages;
+                    if (!mbar_wait(&bars.full[st], (it / kLStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const bool second = kDual && kb >= n_k;
+                    const uint32_t d = tmem + buf * kLBN + (second ? kLBN : 0);
+                    const int kb0 = second ? kb - n_k : kb;     // k-block within its product
+                    const uint8_t *a = smem + st * kLStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kLBK / 16; ++kk) {
+                        // a 16-deep K step: 32 bytes along a K-major row, two 8-row groups MN-major
+                        const uint64_t da = kAMn ? umma_desc_sw128_mn(a + kk * 2048, kLMnAtomBytes)
+                                                 : umma_desc_sw128(a + kk * 32);
+                        const uint64_t db = kBMn ? umma_desc_sw128_mn(a + kLAStage + kk * 2048, kLMnAtomBytes)
+                                                 : umma_desc_sw128(a + kLAStage + kk * 32);
+                        umma_bf16(d, da, db, idesc, (kb0 | kk) != 0);
+                    }
+                    umma_commit(&bars.empty[st]);       // frees the stage once these MMAs are done
+                }
+                umma_commit(&bars.acc_full[buf]);       // the accumulator is complete
+            }
+            if (!ok) atomicOr(&g_linear_fault, 2u);
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;                          // TMEM lane quarter of this warp
+        const int r_in = q * 32 + lane;
+        uint32_t j = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
+            const int mb = (int)(tile % n_mb), nb = (int)(tile / n_mb);
+            const uint32_t buf = kDual ? 0 : j & 1;
+            if (ok && !mbar_wait(&bars.acc_full[buf], (kDual ? j : j >> 1) & 1)) {
+                ok = false;
+                atomicOr(&g_linear_fault, 4u);
+            }
+            tc_fence_after();
+            // tcgen05.ld is warp-collective: the whole warp calls the epilogue or
+            // none of it does, and epilogues guard only their global accesses
+            if (__all_sync(0xffffffffu, ok))
+                epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
+                    tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
+            tc_fence_before();
+            mbar_arrive(&bars.acc_empty[buf]);           // the MMA warp may reuse the accumulator
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kLTmemCols);
+}
+
+// Backward K2 epilogue: acc[row][col] (+)= tile, fp32 (pitch ld).
+struct AccEpi {
+    int M, ld;
+    bool first;
+    float *acc;
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        const bool valid = row < M;
+        float *dst = acc + (int64_t)(valid ? row : 0) * ld + col0;
+#pragma unroll 1
+        for (int c = 0; c < kLBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            if (!valid || c * 32 >= ncol) continue;
+            float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                if (!first) {
+                    const float4 a = d4[k];
+                    o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
+                }
+                d4[k] = o;
+            }
+        }
+    }
+};
+
+// Backward K3 epilogue: out[row0 + row][col] = bf16(tile) (pitch ld), rows < M.
+struct StoreBf16Epi {
+    int M, ld;
+    int64_t row0;
+    __nv_bfloat16 *out;
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        const bool valid = row < M;
+        __nv_bfloat16 *dst = out + (row0 + (valid ? row : 0)) * (int64_t)ld + col0;
+#pragma unroll 1
+        for (int c = 0; c < kLBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(taddr + c * 32, v);
+            if (!valid || c * 32 >= ncol) continue;
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                packed[i] = *reinterpret_cast<uint32_t *>(&b);
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+        }
+    }
+};
+
+// out[i] = bf16(acc[i]) for rows x cols (pitches in elements)
+static __global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ acc, int64_t n,
+                                                             __nv_bfloat16 *__restrict__ out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = __float2bfloat16_rn(acc[i]);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load();
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// Row-major bf16 matrix of `rows` rows of `cols` valid elements, `pitch`
+// elements apart; boxes of box_rows x 64 with the 128-byte swizzle. Boxes past
+// the extents read as zeros.
+static bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int64_t pitch, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kLBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MN-major operand map: `rows` along K, `cols` (the operand's M or N) consecutive,
+// boxes of 64 x 64.
+static bool make_map_mn(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int64_t pitch) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)pitch * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)kLBK};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
+static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
+                                    const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
+                                    cudaStream_t stream) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done.load() & (1ull << (dev & 63)))) {
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi, kAMn, kBMn, kDual>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(1ull << (dev & 63));
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t n_tiles = (int64_t)((M + kLBM - 1) / kLBM) * ((Nn + kLBN - 1) / kLBN);
+    const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
+    umma_gemm_kernel<Epi, kAMn, kBMn, kDual><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, ta2, tb2, M, Nn, K,
+                                                                                       K2, epi);
+    return cudaGetLastError();
+}
+
+template <class Epi, bool kAMn = false, bool kBMn = false>
+static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, const Epi &epi,
+                               cudaStream_t stream) {
+    return launch_gemm_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, epi, stream);
+}
+
+// Both products of the dual form: C = A . B^T (K deep) and C2 = A2 . B2^T (K2 deep).
+template <class Epi>
+static cudaError_t launch_gemm_dual(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
+                                    const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
+                                    cudaStream_t stream) {
+    return launch_gemm_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, epi, stream);
+}
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Backward vocabulary chunk: vc rows of W at a time (32768 for up to 8192
+// hidden rows, fewer for more rows, so that dz of a chunk stays near 0.5 GB;
+// larger chunks mean fewer launches and fewer read-modify-write passes over
+// dhidden).
+static int64_t chunk_cols(int64_t N, int64_t V) {
+    const int64_t vc = N <= 8192 ? 32768 : N <= 16384 ? 16384 : 8192;
+    return V < vc ? ((V + 255) / 256) * 256 : vc;
+}
+
+// The two gradient GEMMs of one vocabulary chunk [v0, v0 + nv) for one model
+// (hidden h [N, D], head W [V, D]) given the chunk's dz (bf16 [N, nv], pitch vc):
+//   K2  acc (+)= dz . W_c  (A = dz K-major, B = W_c MN-major, K = nv; first chunk stores)
+//   K3  dW_c = dz^T . h    (A = dz MN-major, B = h MN-major, K = N), written as bf16
+// acc and dW may each be null (that GEMM is skipped).
+static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_bfloat16 *W, int N, int D, int64_t v0,
+                                        int nv, int64_t vc, const __nv_bfloat16 *dz, float *acc,
+                                        __nv_bfloat16 *dW, cudaStream_t stream) {
+    cudaError_t e;
+    if (acc) {
+        CUtensorMap tm_dz, tm_wc_mn;
+        if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
+            return cudaErrorInvalidValue;
+        const AccEpi ae{N, D, v0 == 0, acc};
+        if ((e = launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream)) != cudaSuccess) return e;
+    }
+    if (dW) {
+        CUtensorMap tm_dz_mn;
+        if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc)) return cudaErrorInvalidValue;
+        const StoreBf16Epi se{nv, D, v0, dW};
+        if ((e = launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream)) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+// dhidden = bf16(acc) over N x D elements.
+static cudaError_t finish_dhidden(const float *acc, int64_t n, __nv_bfloat16 *dh, cudaStream_t stream) {
+    to_bf16_kernel<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256, 0, stream>>>(acc, n, dh);
+    return cudaGetLastError();
+}
+
+// Reads (and optionally clears) this translation unit's fault word.
+static cudaError_t read_tu_fault(uint32_t *value, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(value, g_linear_fault, sizeof(uint32_t));
+    if (e == cudaSuccess && clear && *value) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_linear_fault, &zero, sizeof(uint32_t));
+    }
+    return e;
+}
+
+}  // namespace vp

@@ -128,7 +128,45 @@ cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a);
 constexpr size_t kNoAllocScratchBytes = (size_t)24 << 20;
 cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a);
 cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a);
-cudaError_t read_linear_fault(uint32_t *value, bool clear);
+// fault words of the GEMM kernels, one per translation unit
+cudaError_t read_linear_logp_fault(uint32_t *value, bool clear);
+cudaError_t read_linear_ent_kl_fault(uint32_t *value, bool clear);
+
+// Fused linear entropy: model (hidden [N, D], weight [V, D]), bf16 row-major.
+struct LinearEntArgs {
+    const void *hidden, *weight;
+    int64_t N, V, D;
+    float *H;                     // forward output, fp32 [N]
+    void *stats;                  // vp_rowstat [N]: written by the forward, read by the backward
+    const float *g;               // backward: upstream gradient of H, fp32 [N]
+    void *dhidden, *dW;           // backward outputs, bf16; either may be NULL
+    void *workspace;
+    cudaStream_t stream;
+};
+
+size_t linear_entropy_workspace_bytes(int64_t N, int64_t V);
+size_t linear_entropy_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D);
+cudaError_t launch_linear_entropy_fwd(const LinearEntArgs &a);
+cudaError_t launch_linear_entropy_bwd(const LinearEntArgs &a);
+
+// Fused linear KL between model A (ha [N, Da], wa [V, Da]) and model B (hb [N, Db],
+// wb [V, Db]); reverse = KL(A||B), forward = KL(B||A).
+struct LinearKLArgs {
+    const void *ha, *wa, *hb, *wb;
+    int64_t N, V, Da, Db;
+    int direction;
+    float *kl;                    // forward output, fp32 [N]
+    void *stats_a, *stats_b;      // vp_rowstat [N] each
+    const float *g;               // backward: upstream gradient of KL, fp32 [N]
+    void *dha, *dwa, *dhb, *dwb;  // backward outputs, bf16; any may be NULL (not all)
+    void *workspace;
+    cudaStream_t stream;
+};
+
+size_t linear_kl_workspace_bytes(int64_t N, int64_t V);
+size_t linear_kl_bwd_workspace_bytes(int64_t N, int64_t V, int64_t Da, int64_t Db);
+cudaError_t launch_linear_kl_fwd(const LinearKLArgs &a);
+cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a);
 
 cudaError_t launch_logprobs_fwd(const StatsArgs &a);
 cudaError_t launch_entropy_fwd(const StatsArgs &a);
