@@ -254,6 +254,7 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_bytes": nbytes[dom]}
 
     jsd = jsd_bench(args, a, b, g, dev, peaks) if rank == 0 else None
+    topk = topk_bench(args, a, dev, peaks) if rank == 0 else None
 
     linear = None
     if not args.no_linear and rank == 0:
@@ -278,7 +279,7 @@ def run_ours(args, rank, world, local_rank):
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "linear_logp": linear,
+            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "linear_logp": linear,
         }
         print(json.dumps(line))
     if dist:
@@ -320,6 +321,28 @@ def jsd_bench(args, a, b, g, dev, peaks, beta=0.5):
                     "backward = one read of A and B and one write of dA and dB",
             "frac_of_copy_peak": {"fwd": round(2 * E2 / (tf * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                                   "bwd": round(2 * E2 / (tb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}
+
+
+def topk_bench(args, a, dev, peaks, K=20):
+    """Logprobs of K ids per row (top-k) on the step's logits A: one scan forward, one read + one write backward."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    from vocab_wide_logprobs_gb300 import workloads
+    N, V = a.shape
+    ids = workloads.topk_ids(seed=101, N=N, V=V, K=K)
+    t, g = ids["targets"].to(dev), ids["grad"].to(dev)
+    lp, st = vp.vp_logprobs_topk_fwd(a, t)
+    dx = torch.empty_like(a)
+    reps = max(3, min(args.steps, 10))
+    tf = _time_ms(lambda: vp.vp_logprobs_topk_fwd(a, t, logp=lp, stats=st), reps)
+    tb = _time_ms(lambda: vp.vp_logprobs_topk_bwd(a, t, st, g, dx=dx), reps)
+    E = N * V * a.element_size()
+    fb, bb = E + 16 * N * K, 2 * E + 12 * N * K
+    gbs = lambda nbytes, ms: round(nbytes / (ms * 1e-3) / 1e9, 1)
+    return {"workload": f"{N}x{V} bf16, K={K} ids per row (10% duplicates, 10% ignored)", "fwd_ms": round(tf, 4),
+            "bwd_ms": round(tb, 4), "fwd_gbs": gbs(fb, tf), "bwd_gbs": gbs(bb, tb), "fwd_bytes": fb,
+            "bwd_bytes": bb, "frac_of_copy_peak": {"fwd": round(fb / (tf * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                                   "bwd": round(bb / (tb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
 def _time_ms(fn, reps):

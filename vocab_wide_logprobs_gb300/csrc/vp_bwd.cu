@@ -131,6 +131,16 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
         const int seg = (int)(tile - r * tiles_per_row);
         const T *in = x + rows.off(r);
         T *out = dx + r * (int64_t)V;
+        // the tile's streaming loads go out first, ahead of the row header's loads
+        const int hin = head_count(in, V), hout = head_count(out, V);
+        const int v0 = seg * kTileVec;
+        const int v1 = hin == hout ? min((V - hin) / kVec, v0 + kTileVec) : 0;
+        uint4 u[kBwdVecPerThread];
+#pragma unroll
+        for (int k = 0; k < kBwdVecPerThread; ++k) {
+            const int i = v0 + tid + k * kBwdThreads;
+            if (i < v1) u[k] = ldg_stream(reinterpret_cast<const uint4 *>(in + hin) + i);
+        }
         const RowStat s = load_rowstat(stats + r);
         const float g = g_in[r];
         int64_t loc = -1;
@@ -152,7 +162,6 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
             }
         }
 
-        const int hin = head_count(in, V), hout = head_count(out, V);
         if (hin == hout) {
             const int head = hin;
             const int nv = (V - head) / kVec;
@@ -169,20 +178,11 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
                     Elem<T>::store1(out + j, d);
                 }
             }
-            const int v0 = seg * kTileVec;
-            const int v1 = min(nv, v0 + kTileVec);
-            const uint4 *vin = reinterpret_cast<const uint4 *>(in + head);
             uint4 *vout = reinterpret_cast<uint4 *>(out + head);
             if (mode != kNormal) {
                 const uint4 c = splat<T>(mode == kZero ? 0.f : qnan());
                 for (int i = v0 + tid; i < v1; i += kBwdThreads) stg_stream(vout + i, c);
                 continue;
-            }
-            uint4 u[kBwdVecPerThread];
-#pragma unroll
-            for (int k = 0; k < kBwdVecPerThread; ++k) {
-                const int i = v0 + tid + k * kBwdThreads;
-                if (i < v1) u[k] = ldg_stream(vin + i);
             }
 #pragma unroll
             for (int k = 0; k < kBwdVecPerThread; ++k) {
@@ -224,11 +224,14 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
 // --------------------------------------------------------------------------
 // Logprobs of K ids per row (top-k): dz_j = G_j - p_j Gsum, where Gsum sums the
 // upstream gradients of the ids that are not ignored and G_j those of the ids
-// equal to j (duplicates add up). Each tile first writes -Gsum p_j over its
-// span, then (after a CTA barrier) its threads rewrite the elements of the ids
-// that fall in the span as G_j (1 - p_j) - p_j (Gsum - G_j), 1 - p_j without
-// cancellation. A row holding an id outside the shard is NaN (error bit); a
-// row whose ids are all ignored is 0.
+// equal to j (duplicates add up). One CTA per row (grid-stride over rows):
+// every warp reads the row's K (id, g) pairs once and reduces them in a fixed
+// order (no CTA barrier; the same Gsum in every warp), the CTA writes
+// -Gsum p_j over the row tile by tile, then the warp that stored an id's
+// element rewrites it as G_j (1 - p_j) - p_j (Gsum - G_j), 1 - p_j without
+// cancellation (after a warp barrier, so the later store wins). Duplicate ids
+// rewrite the same value. A row holding an id outside the shard is NaN (error
+// bit); a row whose ids are all ignored is 0.
 // --------------------------------------------------------------------------
 template <typename T>
 __device__ __forceinline__ float topk_target_elem(float z, const RowStat &s, float G, float gsum) {
@@ -250,82 +253,78 @@ __device__ __forceinline__ float topk_target_elem(float z, const RowStat &s, flo
 
 template <typename T>
 __global__ void __launch_bounds__(kBwdThreads)
-topk_grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict__ stats,
+topk_grad_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const RowStat *__restrict__ stats,
                  const float *__restrict__ g_in, const int64_t *__restrict__ targets, int64_t K, int64_t vocab_start,
-                 T *__restrict__ dx, int32_t *__restrict__ err, int tiles_per_row, int64_t total_tiles) {
+                 T *__restrict__ dx, int32_t *__restrict__ err) {
     constexpr int kVec = Elem<T>::kVec;
-    const int tid = threadIdx.x, lane = tid & 31;
-    __shared__ float s_gsum;
-    __shared__ int s_mode;
-    for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        const int64_t r = tile / tiles_per_row;
-        const int seg = (int)(tile - r * tiles_per_row);
+    static_assert((kBwdThreads & (kBwdThreads - 1)) == 0 && kTileVec % kBwdThreads == 0, "tiles of whole blocks");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int64_t r = blockIdx.x; r < N; r += gridDim.x) {
         const T *in = x + rows.off(r);
         T *out = dx + r * (int64_t)V;
-        const RowStat s = load_rowstat(stats + r);
-        __syncthreads();                                   // the previous tile is done with the header
-        if (tid < 32) {                                    // row header: Gsum, any id used, any id out of the shard
-            float gs = 0.f;
-            int used = 0, bad = 0;
-            for (int64_t k = lane; k < K; k += 32) {
-                const int64_t t = targets[r * K + k];
-                if (t < 0) continue;
-                used = 1;
-                const int64_t loc = t - vocab_start;
-                if (loc < 0 || loc >= V) bad = 1;
-                gs += g_in[r * K + k];
-            }
-            for (int m = 16; m > 0; m >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);   // fixed order
-            used = __any_sync(0xffffffffu, used);
-            bad = __any_sync(0xffffffffu, bad);
-            if (lane == 0) {
-                s_gsum = gs;
-                s_mode = !used ? kZero : (bad || (s.flags & (kRowNanInf | kRowEmpty))) ? kNaN : kNormal;
-                if (bad && err && seg == 0) atomicOr(err, VP_ERRBIT_TARGET_);
-            }
-        }
-        __syncthreads();
-        const float gsum = s_gsum;
-        const int mode = s_mode;
-
-        // phase 1: -Gsum p over the tile's span (0 / NaN rows filled)
+        const int64_t *tr = targets + r * K;
+        const float *gr = g_in + r * K;
         const int hin = head_count(in, V), hout = head_count(out, V);
         const bool vec = hin == hout;
         const int head = vec ? hin : 0;
         const int nv = vec ? (V - head) / kVec : 0;
         const int tail0 = head + nv * kVec;
-        const int64_t e0 = vec ? head + (int64_t)seg * kTileVec * kVec : (int64_t)seg * kTileVec * kVec;
-        const int64_t e1 = vec ? head + (int64_t)min(nv, (seg + 1) * kTileVec) * kVec
-                               : min((int64_t)V, e0 + (int64_t)kTileVec * kVec);
-        auto scalar_range = [&](int64_t j0, int64_t j1) {
-            for (int64_t j = j0 + tid; j < j1; j += kBwdThreads) {
+        // the first tile's streaming loads go out ahead of the row header's loads
+        uint4 u[kBwdVecPerThread];
+#pragma unroll
+        for (int k = 0; k < kBwdVecPerThread; ++k) {
+            const int i = tid + k * kBwdThreads;
+            if (i < nv) u[k] = ldg_stream(reinterpret_cast<const uint4 *>(in + head) + i);
+        }
+        const RowStat s = load_rowstat(stats + r);
+        // row header, in every warp: Gsum, any id used, any id out of the shard
+        float gsum = 0.f;
+        int used = 0, bad = 0;
+        for (int64_t k = lane; k < K; k += 32) {
+            const int64_t t = tr[k];
+            if (t < 0) continue;
+            used = 1;
+            const int64_t loc = t - vocab_start;
+            if (loc < 0 || loc >= V) bad = 1;
+            gsum += gr[k];
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, m);   // fixed order
+        used = __any_sync(0xffffffffu, used);
+        bad = __any_sync(0xffffffffu, bad);
+        const int mode = !used ? kZero : (bad || (s.flags & (kRowNanInf | kRowEmpty))) ? kNaN : kNormal;
+        if (bad && err && tid == 0) atomicOr(err, VP_ERRBIT_TARGET_);
+
+        // phase 1: -Gsum p over the row (0 / NaN rows filled)
+        auto scalar_range = [&](int j0, int j1) {
+            for (int j = j0 + tid; j < j1; j += kBwdThreads) {
                 const float d = mode == kZero ? 0.f : mode == kNaN ? qnan()
                                 : grad_elem<0, T>(Elem<T>::load1(in + j), 0, s, gsum, -1);
                 Elem<T>::store1(out + j, d);
             }
         };
         if (vec) {
-            if (seg == 0) {
-                scalar_range(0, head);
-                scalar_range(tail0, V);
-            }
-            const int v0 = seg * kTileVec, v1 = min(nv, v0 + kTileVec);
+            scalar_range(0, head);
+            scalar_range(tail0, V);
             const uint4 *vin = reinterpret_cast<const uint4 *>(in + head);
             uint4 *vout = reinterpret_cast<uint4 *>(out + head);
-            if (mode != kNormal) {
-                const uint4 c = splat<T>(mode == kZero ? 0.f : qnan());
-                for (int i = v0 + tid; i < v1; i += kBwdThreads) stg_stream(vout + i, c);
-            } else {
-                uint4 u[kBwdVecPerThread];
+            const uint4 c = splat<T>(mode == kZero ? 0.f : qnan());
+            for (int v0 = 0; v0 < nv; v0 += kTileVec) {
+                if (v0 > 0) {
 #pragma unroll
-                for (int k = 0; k < kBwdVecPerThread; ++k) {
-                    const int i = v0 + tid + k * kBwdThreads;
-                    if (i < v1) u[k] = ldg_stream(vin + i);
+                    for (int k = 0; k < kBwdVecPerThread; ++k) {
+                        const int i = v0 + tid + k * kBwdThreads;
+                        if (i < nv) u[k] = ldg_stream(vin + i);
+                    }
                 }
 #pragma unroll
                 for (int k = 0; k < kBwdVecPerThread; ++k) {
                     const int i = v0 + tid + k * kBwdThreads;
-                    if (i < v1) {
+                    if (i < nv) {
+                        if (mode != kNormal) {
+                            stg_stream(vout + i, c);
+                            continue;
+                        }
                         float z[kVec], d[kVec];
                         Elem<T>::unpack(u[k], z);
 #pragma unroll
@@ -335,21 +334,29 @@ topk_grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__res
                 }
             }
         } else {
-            scalar_range(e0, e1);
+            scalar_range(0, V);
         }
         if (mode != kNormal) continue;
 
-        // phase 2: the ids' own elements in this tile's span
-        __syncthreads();                                   // phase-1 stores of this CTA come first
-        for (int64_t k = tid; k < K; k += kBwdThreads) {
-            const int64_t t = targets[r * K + k];
+        // phase 2: the ids' own elements. Element j was stored in phase 1 by
+        // thread owner(j) (the tiles start at multiples of kBwdThreads); the
+        // lanes of each warp share out the row's ids, and an id whose element
+        // this warp stored is rewritten by a lane of this warp after
+        // __syncwarp, which orders the warp's phase-1 stores before it.
+        auto owner = [&](int j) -> int {   // j in [0, V)
+            if (!vec || j < head) return j & (kBwdThreads - 1);
+            if (j >= tail0) return (j - tail0) & (kBwdThreads - 1);
+            return (int)((unsigned)(j - head) / (unsigned)kVec) & (kBwdThreads - 1);
+        };
+        __syncwarp();
+        for (int64_t k = lane; k < K; k += 32) {
+            const int64_t t = tr[k];
             if (t < 0) continue;
-            const int64_t j = t - vocab_start;
-            const bool mine = (j >= e0 && j < e1) || (vec && seg == 0 && (j < head || j >= tail0));
-            if (!mine) continue;
+            const int j = (int)(t - vocab_start);          // in [0, V): the row has no id outside the shard
+            if ((owner(j) >> 5) != warp) continue;
             float G = 0.f;                                 // every id equal to this one, in id order
             for (int64_t k2 = 0; k2 < K; ++k2)
-                if (targets[r * K + k2] == t) G += g_in[r * K + k2];
+                if (tr[k2] == t) G += gr[k2];
             Elem<T>::store1(out + j, topk_target_elem<T>(Elem<T>::load1(in + j), s, G, gsum));
         }
     }
@@ -562,13 +569,10 @@ cudaError_t launch_entropy_bwd(const GradArgs &a) {
 
 template <typename T>
 static cudaError_t launch_topk_grad(const GradArgs &a) {
-    int tpr;
-    int64_t total;
-    unsigned grid;
-    tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
+    const unsigned grid = (unsigned)(a.N < (int64_t)(1u << 30) ? a.N : (int64_t)(1u << 30));   // one CTA per row
     topk_grad_kernel<T><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i}, static_cast<const RowStat *>(a.stats), a.g,
-        a.targets, a.K, a.vocab_start, static_cast<T *>(a.dx), a.err, tpr, total);
+        static_cast<const T *>(a.x), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, static_cast<const RowStat *>(a.stats),
+        a.g, a.targets, a.K, a.vocab_start, static_cast<T *>(a.dx), a.err);
     return cudaGetLastError();
 }
 
