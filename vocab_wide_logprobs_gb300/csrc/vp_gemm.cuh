@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "vp_device.cuh"
@@ -56,11 +57,26 @@ struct LinearBars {
 // ---------------------------------------------------------------------------
 constexpr uint32_t kLMnAtomBytes = 64 * kLBK * 2;   // one 64 (MN) x 64 (K) box: 8 KB
 
+// Tile order: groups of group_m m-blocks; within a group, m-blocks vary fastest,
+// then n-blocks. group_m >= n_mb is plain N-major order (consecutive CTAs share
+// one B tile, and all of A stays in L2: right when A is small); a small group_m
+// keeps the concurrent tiles on a few A and B tiles each (right when both
+// operands are large and stream along a long K).
+__device__ __forceinline__ void tile_coords(int64_t tile, int n_mb, int n_nb, int group_m, int &mb, int &nb) {
+    const int64_t per_group = (int64_t)group_m * n_nb;
+    const int g = (int)(tile / per_group);
+    const int first = g * group_m;
+    const int gm = min(group_m, n_mb - first);
+    const int w = (int)(tile - (int64_t)g * per_group);
+    mb = first + w % gm;
+    nb = w / gm;
+}
+
 template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
 __global__ void __launch_bounds__(kLThreads, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M, int Nn,
-                 int K, int K2, const Epi epi) {
+                 int K, int K2, int group_m, int l2hints, const Epi epi) {
     static_assert(!kDual || (!kAMn && !kBMn), "the dual form takes K-major operands");
     extern __shared__ uint8_t smem_raw[];
     __shared__ LinearBars bars;
@@ -97,34 +113,38 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
+            // L2 eviction priority of the A and B tiles (bits 0-1 and 2-3 of l2hints)
+            const uint64_t pol_a = l2_policy(l2hints & 3), pol_b = l2_policy((l2hints >> 2) & 3);
             uint32_t it = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-                const int mb = (int)(tile % n_mb), nb = (int)(tile / n_mb);
+                int mb, nb;
+                tile_coords(tile, n_mb, n_nb, group_m, mb, nb);
                 for (int kb = 0; kb < n_k + n_k2; ++kb, ++it) {
                     const uint32_t st = it % kLStages, use = it / kLStages;
                     if (use > 0 && !mbar_wait(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
                     uint8_t *a = smem + st * kLStageBytes;
                     mbar_arrive_expect_tx(&bars.full[st], kLStageBytes);
                     if (kDual && kb >= n_k) {                // second product
-                        tma_load_2d(a, &tm_a2, (kb - n_k) * kLBK, mb * kLBM, &bars.full[st]);
-                        tma_load_2d(a + kLAStage, &tm_b2, (kb - n_k) * kLBK, nb * kLBN, &bars.full[st]);
+                        tma_load_2d_hint(a, &tm_a2, (kb - n_k) * kLBK, mb * kLBM, &bars.full[st], pol_a);
+                        tma_load_2d_hint(a + kLAStage, &tm_b2, (kb - n_k) * kLBK, nb * kLBN, &bars.full[st], pol_b);
                         continue;
                     }
                     if (kAMn) {
 #pragma unroll
                         for (int i = 0; i < kLBM / 64; ++i)
-                            tma_load_2d(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK, &bars.full[st]);
+                            tma_load_2d_hint(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK,
+                                             &bars.full[st], pol_a);
                     } else {
-                        tma_load_2d(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st]);
+                        tma_load_2d_hint(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st], pol_a);
                     }
                     if (kBMn) {
 #pragma unroll
                         for (int i = 0; i < kLBN / 64; ++i)
-                            tma_load_2d(a + kLAStage + i * kLMnAtomBytes, &tm_b, nb * kLBN + 64 * i, kb * kLBK,
-                                        &bars.full[st]);
+                            tma_load_2d_hint(a + kLAStage + i * kLMnAtomBytes, &tm_b, nb * kLBN + 64 * i, kb * kLBK,
+                                             &bars.full[st], pol_b);
                     } else {
-                        tma_load_2d(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st]);
+                        tma_load_2d_hint(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st], pol_b);
                     }
                 }
             }
@@ -170,7 +190,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         uint32_t j = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
-            const int mb = (int)(tile % n_mb), nb = (int)(tile / n_mb);
+            int mb, nb;
+            tile_coords(tile, n_mb, n_nb, group_m, mb, nb);
             const uint32_t buf = kDual ? 0 : j & 1;
             if (ok && !mbar_wait(&bars.acc_full[buf], (kDual ? j : j >> 1) & 1)) {
                 ok = false;
@@ -300,8 +321,8 @@ static bool make_map_mn(CUtensorMap *map, const void *ptr, int64_t rows, int64_t
 
 template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
 static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
-                                    const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
-                                    cudaStream_t stream) {
+                                    const CUtensorMap &tb2, int M, int Nn, int K, int K2, int group_m,
+                                    int l2hints, const Epi &epi, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -315,15 +336,37 @@ static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t n_tiles = (int64_t)((M + kLBM - 1) / kLBM) * ((Nn + kLBN - 1) / kLBN);
     const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
+    const int n_mb = (M + kLBM - 1) / kLBM;
+    if (group_m <= 0) {   // about 32 MB of A (both products' A tiles in the dual form) per m-group
+        const int64_t a_tile = (int64_t)kLBM * (K + (kDual ? K2 : 0)) * 2;
+        group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / a_tile);
+    }
+    if (group_m > n_mb) group_m = n_mb;
     umma_gemm_kernel<Epi, kAMn, kBMn, kDual><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, ta2, tb2, M, Nn, K,
-                                                                                       K2, epi);
+                                                                                       K2, group_m, l2hints, epi);
     return cudaGetLastError();
 }
 
+// L2 eviction priorities of the operand tiles (l2hints: A in bits 0-1, B in bits 2-3;
+// 1 = evict_first, 2 = evict_last, 0 = normal), measured on GB300 at hidden
+// [8192, 4096] x W [75968, 4096]:
+//  - logits GEMMs (forward, backward K1, dual): A = hidden rows, reused by every
+//    vocabulary tile of the group, evict_last; B = W, streamed, evict_first.
+//    With groups of about 32 MB of A this cut the forward's DRAM reads from
+//    6.3 GB (h re-fetched for every few W tiles) to near one read of W, and
+//    its time by 16%.
+//  - K2 (dz . W_c): both operands evict_last (each is re-read by the other's
+//    group).
+//  - K3 (dz^T . h): A = dz^T evict_last, B = h evict_first.
+constexpr int kHintLogits = 2 | (1 << 2);
+constexpr int kHintK2 = 2 | (2 << 2);
+constexpr int kHintK3 = 2 | (1 << 2);
+
+// group_m <= 0: about 32 MB of A per m-group (see tile_coords and launch_gemm_impl)
 template <class Epi, bool kAMn = false, bool kBMn = false>
 static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, const Epi &epi,
-                               cudaStream_t stream) {
-    return launch_gemm_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, epi, stream);
+                               cudaStream_t stream, int group_m = 0, int l2hints = kHintLogits) {
+    return launch_gemm_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, group_m, l2hints, epi, stream);
 }
 
 // Both products of the dual form: C = A . B^T (K deep) and C2 = A2 . B2^T (K2 deep).
@@ -331,7 +374,7 @@ template <class Epi>
 static cudaError_t launch_gemm_dual(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                                     const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
                                     cudaStream_t stream) {
-    return launch_gemm_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, epi, stream);
+    return launch_gemm_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, 0, kHintLogits, epi, stream);
 }
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -349,7 +392,12 @@ static int64_t chunk_cols(int64_t N, int64_t V) {
 // (hidden h [N, D], head W [V, D]) given the chunk's dz (bf16 [N, nv], pitch vc):
 //   K2  acc (+)= dz . W_c  (A = dz K-major, B = W_c MN-major, K = nv; first chunk stores)
 //   K3  dW_c = dz^T . h    (A = dz MN-major, B = h MN-major, K = N), written as bf16
-// acc and dW may each be null (that GEMM is skipped).
+// acc and dW may each be null (that GEMM is skipped). Both GEMMs stream two
+// operands far larger than L2 along a long K, so their tiles run in small
+// m-groups (tile_coords): the concurrent CTAs then share a few A and B tiles
+// instead of each A tile being fetched from DRAM once per n-block.
+constexpr int kGradGroupM = 16;   // K2: 16 m-blocks of dz (8 MB each at vc = 32768) x the 16 n-blocks of D = 4096
+constexpr int kWGroupM = 8;       // K3: 8 m-blocks of dz^T (2 MB each at N = 8192) x the n-blocks of D
 static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_bfloat16 *W, int N, int D, int64_t v0,
                                         int nv, int64_t vc, const __nv_bfloat16 *dz, float *acc,
                                         __nv_bfloat16 *dW, cudaStream_t stream) {
@@ -359,13 +407,16 @@ static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_b
         if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
             return cudaErrorInvalidValue;
         const AccEpi ae{N, D, v0 == 0, acc};
-        if ((e = launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream)) != cudaSuccess) return e;
+        if ((e = launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM, kHintK2)) !=
+            cudaSuccess)
+            return e;
     }
     if (dW) {
         CUtensorMap tm_dz_mn;
         if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc)) return cudaErrorInvalidValue;
         const StoreBf16Epi se{nv, D, v0, dW};
-        if ((e = launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream)) != cudaSuccess)
+        if ((e = launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream, kWGroupM, kHintK3)) !=
+            cudaSuccess)
             return e;
     }
     return cudaSuccess;
