@@ -123,3 +123,40 @@ def test_jsd_entry_points_check_beta_first():
     assert lib.vp_jsd_fwd(FAKE, FAKE, 7, 4, 16, 4, 0, 16, 0.5, FAKE, FAKE, FAKE, None) == ERR_DTYPE
     assert lib.vp_jsd_bwd(FAKE, FAKE, 1, 4, 16, 4, 0, 16, 0.5, FAKE, FAKE, FAKE, None, None, None) == ERR_ARG
     assert lib.vp_jsd_fwd(FAKE, FAKE, 1, 4, 16, 4, 0, 16, 0.5, FAKE_ODD, FAKE, FAKE, None) == ERR_ALIGN
+
+
+def test_topk_entry_points_check_arguments_on_the_host():
+    lib = _lib.lib()
+    row = (FAKE, 1, 4, 16, 4, 0, 16, 0)                  # x, dtype, N, V, R, s_o, s_i, vocab_start
+    assert lib.vp_logprobs_topk_fwd(*row, FAKE, 0, FAKE, FAKE, None, None) == ERR_SHAPE        # K = 0
+    assert lib.vp_logprobs_topk_fwd(*row, None, 3, FAKE, FAKE, None, None) == ERR_NULL
+    assert lib.vp_logprobs_topk_fwd(*row, FAKE_ODD, 3, FAKE, FAKE, None, None) == ERR_ALIGN
+    assert lib.vp_logprobs_topk_fwd(FAKE, 5, 4, 16, 4, 0, 16, 0, FAKE, 3, FAKE, FAKE, None, None) == ERR_DTYPE
+    assert lib.vp_logprobs_topk_bwd(*row, FAKE, 3, FAKE, None, FAKE, None, None) == ERR_NULL
+    assert lib.vp_logprobs_topk_bwd(*row, FAKE, 3, ctypes.c_void_p(0x100008), FAKE, FAKE, None, None) == ERR_ALIGN
+    assert lib.vp_logprobs_topk_fwd(None, 1, 0, 16, 1, 0, 16, 0, None, 3, None, None, None, None) == OK   # N = 0
+
+
+def test_linear_entropy_kl_entry_points_check_arguments_on_the_host():
+    lib = _lib.lib()
+    size_t = ctypes.c_size_t
+    ws = size_t(1 << 30)
+    # hidden sizes must be positive multiples of 64
+    assert lib.vp_linear_entropy_fwd(FAKE, FAKE, 4, 16, 96, FAKE, FAKE, FAKE, ws, None) == ERR_SHAPE
+    assert lib.vp_linear_entropy_workspace_size(4, 16, 96) == 0
+    assert lib.vp_linear_entropy_fwd(FAKE, None, 4, 16, 64, FAKE, FAKE, FAKE, ws, None) == ERR_NULL
+    assert lib.vp_linear_entropy_fwd(FAKE_ODD, FAKE, 4, 16, 64, FAKE, FAKE, FAKE, ws, None) == ERR_ALIGN
+    assert lib.vp_linear_entropy_fwd(FAKE, FAKE, 4, 16, 64, FAKE, FAKE, FAKE, size_t(16), None) == ERR_ARG
+    assert lib.vp_linear_entropy_bwd(FAKE, FAKE, 4, 16, 64, FAKE, FAKE, None, None, FAKE, ws, None) == ERR_ARG
+    assert lib.vp_linear_entropy_fwd(None, None, 0, 16, 64, None, None, None, size_t(0), None) == OK   # N = 0
+    two = (FAKE, FAKE, FAKE, FAKE, 4, 16)
+    assert lib.vp_linear_kl_fwd(*two, 64, 100, 0, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_SHAPE     # Db
+    assert lib.vp_linear_kl_fwd(*two, 64, 128, 2, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_ARG       # direction
+    assert lib.vp_linear_kl_fwd(*two, 64, 128, 0, FAKE, FAKE, FAKE, FAKE, size_t(64), None) == ERR_ARG
+    assert lib.vp_linear_kl_fwd(*two, 64, 128, 0, FAKE, FAKE_ODD, FAKE, FAKE, ws, None) == ERR_ALIGN
+    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, FAKE, None, None, None, None, FAKE, ws,
+                                None) == ERR_ARG                                                  # no output
+    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, None, FAKE, None, None, None, FAKE, ws,
+                                None) == ERR_NULL
+    assert lib.vp_linear_kl_bwd_workspace_size(4, 16, 64, 128) > 0
+    assert lib.vp_linear_kl_workspace_size(4, 0) == 0
