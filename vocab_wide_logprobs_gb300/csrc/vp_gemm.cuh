@@ -212,6 +212,161 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     if (warp == 1) tmem_dealloc(tmem, kLTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// The same GEMM on CTA pairs (clusters of two CTAs on two SMs, tcgen05
+// cta_group::2): each pair computes a 256 x 256 tile. CTA r of the pair holds
+// rows 128 r .. 128 r + 127 of the A tile and of the accumulator, and rows
+// 128 r .. 128 r + 127 of the B tile, so a stage is 32 KB per CTA instead of
+// 48 KB and six stages fit (twice the bytes in flight per FLOP of the
+// single-CTA form). The leader's (rank 0) TMA thread posts the stage's byte
+// count and both CTAs' TMA loads complete on the leader's "full" barrier; one
+// thread of the leader issues the pair MMAs and commits each stage to the
+// "empty" barriers and each tile to the "acc_full" barriers of both CTAs; the
+// epilogue warps of both CTAs read their own TMEM rows and arrive on the
+// leader's "acc_empty" barrier. Every wait is bounded; every thread of both
+// CTAs reaches the final cluster barrier.
+// ---------------------------------------------------------------------------
+constexpr int kPStages = 6;
+constexpr int kPBHalf = kLBN / 2;                       // rows of the B tile per CTA
+constexpr int kPAStage = kLBM * kLBK * 2;               // 16 KB
+constexpr int kPBStage = kPBHalf * kLBK * 2;            // 16 KB
+constexpr int kPStageBytes = kPAStage + kPBStage;       // 32 KB
+constexpr int kPSmemBytes = kPStages * kPStageBytes + 1024;
+
+struct PairBars {
+    uint64_t full[kPStages], empty[kPStages], acc_full[2], acc_empty[2];
+    uint32_t tmem_base;
+};
+
+template <class Epi, bool kAMn = false, bool kBMn = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLThreads, 1)
+umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M,
+                      int Nn, int K, int group_m, int l2hints, const Epi epi) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ PairBars bars;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int n_mp = (M + 2 * kLBM - 1) / (2 * kLBM), n_nb = (Nn + kLBN - 1) / kLBN;
+    const int64_t n_tiles = (int64_t)n_mp * n_nb;
+    const int n_k = (K + kLBK - 1) / kLBK;
+    const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.acc_full[b], 1);
+            mbar_init(&bars.acc_empty[b], 2 * 4 * 32);   // the epilogue threads of both CTAs
+        }
+        fence_mbar_init();
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
+    }
+    if (warp == 1) tmem_alloc_pair(&bars.tmem_base, kLTmemCols);
+    tc_fence_before();
+    cluster_sync();                                      // barriers and TMEM ready in both CTAs
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        if (lane == 0) {
+            const uint64_t pol_a = l2_policy(l2hints & 3), pol_b = l2_policy((l2hints >> 2) & 3);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t tile = pair; tile < n_tiles && ok; tile += n_pairs) {
+                int mp, nb;
+                tile_coords(tile, n_mp, n_nb, group_m, mp, nb);
+                const int mb = 2 * mp + (int)rank;
+                const int nrow = nb * kLBN + (int)rank * kPBHalf;
+                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                    const uint32_t st = it % kPStages, use = it / kPStages;
+                    if (use > 0 && !mbar_wait_cluster(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
+                    uint8_t *a = smem + st * kPStageBytes;
+                    const uint32_t fb = cluster_addr(&bars.full[st], 0);
+                    if (rank == 0) mbar_arrive_expect_tx(&bars.full[st], 2 * kPStageBytes);
+                    if (kAMn) {
+#pragma unroll
+                        for (int i = 0; i < kLBM / 64; ++i)
+                            tma_load_2d_pair(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK, fb, pol_a);
+                    } else {
+                        tma_load_2d_pair(a, &tm_a, kb * kLBK, mb * kLBM, fb, pol_a);
+                    }
+                    if (kBMn) {
+#pragma unroll
+                        for (int i = 0; i < kPBHalf / 64; ++i)
+                            tma_load_2d_pair(a + kPAStage + i * kLMnAtomBytes, &tm_b, nrow + 64 * i, kb * kLBK, fb,
+                                             pol_b);
+                    } else {
+                        tma_load_2d_pair(a + kPAStage, &tm_b, kb * kLBK, nrow, fb, pol_b);
+                    }
+                }
+            }
+            if (!ok) atomicOr(&g_linear_fault, 1u);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader only) ----------------
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(2 * kLBM, kLBN, kAMn, kBMn);
+            uint32_t it = 0, j = 0;
+            bool ok = true;
+            for (int64_t tile = pair; tile < n_tiles && ok; tile += n_pairs, ++j) {
+                const uint32_t buf = j & 1, use_b = j >> 1;
+                if (use_b > 0 && !mbar_wait_cluster(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * kLBN;
+                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                    const uint32_t st = it % kPStages;
+                    if (!mbar_wait(&bars.full[st], (it / kPStages) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint8_t *a = smem + st * kPStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kLBK / 16; ++kk) {
+                        const uint64_t da = kAMn ? umma_desc_sw128_mn(a + kk * 2048, kLMnAtomBytes)
+                                                 : umma_desc_sw128(a + kk * 32);
+                        const uint64_t db = kBMn ? umma_desc_sw128_mn(a + kPAStage + kk * 2048, kLMnAtomBytes)
+                                                 : umma_desc_sw128(a + kPAStage + kk * 32);
+                        umma_bf16_pair(d, da, db, idesc, (kb | kk) != 0);
+                    }
+                    umma_commit_pair(&bars.empty[st]);   // frees the stage in both CTAs
+                }
+                umma_commit_pair(&bars.acc_full[buf]);   // the tile's accumulators are complete
+            }
+            if (!ok) atomicOr(&g_linear_fault, 2u);
+        }
+    } else {
+        // ---------------- epilogue (both CTAs) ----------------
+        const int q = warp & 3;
+        const int r_in = q * 32 + lane;
+        uint32_t j = 0;
+        bool ok = true;
+        for (int64_t tile = pair; tile < n_tiles; tile += n_pairs, ++j) {
+            int mp, nb;
+            tile_coords(tile, n_mp, n_nb, group_m, mp, nb);
+            const int mb = 2 * mp + (int)rank;
+            const uint32_t buf = j & 1;
+            if (ok && !mbar_wait_cluster(&bars.acc_full[buf], (j >> 1) & 1)) {
+                ok = false;
+                atomicOr(&g_linear_fault, 4u);
+            }
+            tc_fence_after();
+            if (__all_sync(0xffffffffu, ok))
+                epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
+                    tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
+            tc_fence_before();
+            mbar_arrive_cluster(cluster_addr(&bars.acc_empty[buf], 0));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                      // no arrival or copy still targets either CTA
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, kLTmemCols);
+}
+
 // Backward K2 epilogue: acc[row][col] (+)= tile, fp32 (pitch ld).
 struct AccEpi {
     int M, ld;
@@ -369,6 +524,55 @@ static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int
     return launch_gemm_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, group_m, l2hints, epi, stream);
 }
 
+// CTA-pair form (umma_gemm_pair_kernel): K-major B maps need boxes of 128 rows
+// (kPBHalf); MN-major maps are the same 64 x 64 boxes as for one CTA. group_m
+// counts 256-row pair blocks; <= 0 picks about 32 MB of A per group.
+template <class Epi, bool kAMn = false, bool kBMn = false>
+static cudaError_t launch_gemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K,
+                                   const Epi &epi, cudaStream_t stream, int group_m, int l2hints) {
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!(attr_done.load() & (1ull << (dev & 63)))) {
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_pair_kernel<Epi, kAMn, kBMn>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done.fetch_or(1ull << (dev & 63));
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int n_mp = (M + 2 * kLBM - 1) / (2 * kLBM);
+    const int64_t n_tiles = (int64_t)n_mp * ((Nn + kLBN - 1) / kLBN);
+    const int64_t pairs = std::max(1, sms / 2);
+    const unsigned grid = (unsigned)(2 * (n_tiles < pairs ? n_tiles : pairs));
+    if (group_m <= 0) group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / ((int64_t)2 * kLBM * K * 2));
+    if (group_m > n_mp) group_m = n_mp;
+    umma_gemm_pair_kernel<Epi, kAMn, kBMn><<<grid, kLThreads, kPSmemBytes, stream>>>(ta, tb, M, Nn, K, group_m,
+                                                                                     l2hints, epi);
+    return cudaGetLastError();
+}
+
+#ifndef VP_GEMM_PAIRS
+#define VP_GEMM_PAIRS 1
+#endif
+#ifndef VP_GEMM_FWD_PAIRS
+#define VP_GEMM_FWD_PAIRS 1
+#endif
+constexpr bool kGemmPairs = VP_GEMM_PAIRS != 0;        // backward GEMMs on CTA pairs
+constexpr bool kFwdPairs = VP_GEMM_FWD_PAIRS != 0;     // forward logits GEMMs on CTA pairs
+
+// A logits GEMM: A = hidden rows [M, K], B = rows of W [Nn, K], both bf16
+// row-major (K-major), on CTA pairs or single CTAs; builds its tensor maps.
+template <class Epi>
+static cudaError_t launch_logits_gemm(const void *A, const void *B, int M, int Nn, int K, const Epi &epi,
+                                      cudaStream_t stream, bool pairs) {
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, A, M, K, K, kLBM) || !make_map(&tb, B, Nn, K, K, pairs ? kPBHalf : kLBN))
+        return cudaErrorInvalidValue;
+    return pairs ? launch_gemm_pair<Epi>(ta, tb, M, Nn, K, epi, stream, 0, kHintLogits)
+                 : launch_gemm(ta, tb, M, Nn, K, epi, stream);
+}
+
 // Both products of the dual form: C = A . B^T (K deep) and C2 = A2 . B2^T (K2 deep).
 template <class Epi>
 static cudaError_t launch_gemm_dual(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
@@ -407,16 +611,20 @@ static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_b
         if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
             return cudaErrorInvalidValue;
         const AccEpi ae{N, D, v0 == 0, acc};
-        if ((e = launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM, kHintK2)) !=
-            cudaSuccess)
-            return e;
+        e = kGemmPairs ? launch_gemm_pair<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM / 2,
+                                                                kHintK2)
+                       : launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM, kHintK2);
+        if (e != cudaSuccess) return e;
     }
     if (dW) {
         CUtensorMap tm_dz_mn;
         if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc)) return cudaErrorInvalidValue;
         const StoreBf16Epi se{nv, D, v0, dW};
-        if ((e = launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream, kWGroupM, kHintK3)) !=
-            cudaSuccess)
+        e = kGemmPairs ? launch_gemm_pair<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream,
+                                                                     kWGroupM / 2, kHintK3)
+                       : launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream, kWGroupM,
+                                                               kHintK3);
+        if (e != cudaSuccess)
             return e;
     }
     return cudaSuccess;

@@ -183,15 +183,12 @@ size_t linear_workspace_bytes(int64_t N, int64_t V) {
 }
 
 cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a) {
-    CUtensorMap tm_h, tm_w;
-    if (!make_map(&tm_h, a.hidden, a.N, a.D, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, a.D, kLBN))
-        return cudaErrorInvalidValue;
     const int64_t n_vt = (a.V + kLBN - 1) / kLBN;
     float2 *partials = static_cast<float2 *>(a.workspace);
     float *tgt = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) +
                                            (((size_t)a.N * n_vt * sizeof(float2) + 255) & ~(size_t)255));
     const LseEpi epi{(int)a.N, (int)a.V, (int)n_vt, a.vocab_start, a.targets, partials, tgt};
-    cudaError_t e = launch_gemm(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D, epi, a.stream);
+    cudaError_t e = launch_logits_gemm(a.hidden, a.weight, (int)a.N, (int)a.V, (int)a.D, epi, a.stream, kFwdPairs);
     if (e != cudaSuccess) return e;
     linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
         (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
@@ -227,9 +224,6 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
     void *scratch = nullptr;
     cudaError_t e = noalloc_scratch_address(&scratch);
     if (e != cudaSuccess) return e;
-    CUtensorMap tm_h, tm_w;
-    if (!make_map(&tm_h, a.hidden, a.N, a.D, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, a.D, kLBN))
-        return cudaErrorInvalidValue;
     const int64_t n_vt = (a.V + kLBN - 1) / kLBN;
     // Every partial and every in-shard target logit is written by the first
     // kernel before the merge reads it, so nothing in the array needs clearing.
@@ -237,7 +231,7 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
     float *tgt = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
                                            (((size_t)a.N * n_vt * sizeof(float2) + 255) & ~(size_t)255));
     const LseEpi epi{(int)a.N, (int)a.V, (int)n_vt, a.vocab_start, a.targets, partials, tgt};
-    e = launch_gemm(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D, epi, a.stream);
+    e = launch_logits_gemm(a.hidden, a.weight, (int)a.N, (int)a.V, (int)a.D, epi, a.stream, kFwdPairs);
     if (e != cudaSuccess) return e;
     linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
         (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
@@ -276,16 +270,14 @@ cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
     const int N = (int)a.N, V = (int)a.V, D = (int)a.D;
     cudaError_t e;
 
-    CUtensorMap tm_h, tm_h_mn;
-    if (!make_map(&tm_h, h, N, D, D, kLBM) || !make_map_mn(&tm_h_mn, h, N, D, D)) return cudaErrorInvalidValue;
+    CUtensorMap tm_h_mn;
+    if (!make_map_mn(&tm_h_mn, h, N, D, D)) return cudaErrorInvalidValue;
     for (int64_t v0 = 0; v0 < V; v0 += vc) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
-        // K1 over this chunk's rows of W (the map's rows start at v0)
-        CUtensorMap tm_wc;
-        if (!make_map(&tm_wc, W + v0 * D, nv, D, D, kLBN)) return cudaErrorInvalidValue;
+        // K1 over this chunk's rows of W
         const DzEpi de{N, V, (int)v0, (int)vc, a.vocab_start, a.targets, static_cast<const RowStat *>(a.stats), a.g,
                        dz, a.err};
-        if ((e = launch_gemm(tm_h, tm_wc, N, nv, D, de, a.stream)) != cudaSuccess) return e;
+        if ((e = launch_logits_gemm(h, W + v0 * D, N, nv, D, de, a.stream, kGemmPairs)) != cudaSuccess) return e;
         if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dW),
                                       a.stream)) != cudaSuccess)
             return e;

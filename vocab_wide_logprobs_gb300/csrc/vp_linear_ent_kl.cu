@@ -328,13 +328,10 @@ size_t linear_entropy_workspace_bytes(int64_t N, int64_t V) {
 }
 
 cudaError_t launch_linear_entropy_fwd(const LinearEntArgs &a) {
-    CUtensorMap tm_h, tm_w;
-    if (!make_map(&tm_h, a.hidden, a.N, a.D, a.D, kLBM) || !make_map(&tm_w, a.weight, a.V, a.D, a.D, kLBN))
-        return cudaErrorInvalidValue;
     const int n_vt = (int)n_vtiles(a.V);
     EntTile *parts = static_cast<EntTile *>(a.workspace);
     const EntEpi epi{(int)a.N, n_vt, parts};
-    cudaError_t e = launch_gemm(tm_h, tm_w, (int)a.N, (int)a.V, (int)a.D, epi, a.stream);
+    cudaError_t e = launch_logits_gemm(a.hidden, a.weight, (int)a.N, (int)a.V, (int)a.D, epi, a.stream, kFwdPairs);
     if (e != cudaSuccess) return e;
     linear_entropy_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>((int)a.N, n_vt, parts, a.H,
                                                                                    static_cast<RowStat *>(a.stats));
@@ -354,14 +351,12 @@ cudaError_t launch_linear_entropy_bwd(const LinearEntArgs &a) {
     const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(a.weight);
     const int N = (int)a.N, V = (int)a.V, D = (int)a.D;
     cudaError_t e;
-    CUtensorMap tm_h, tm_h_mn;
-    if (!make_map(&tm_h, h, N, D, D, kLBM) || !make_map_mn(&tm_h_mn, h, N, D, D)) return cudaErrorInvalidValue;
+    CUtensorMap tm_h_mn;
+    if (!make_map_mn(&tm_h_mn, h, N, D, D)) return cudaErrorInvalidValue;
     for (int64_t v0 = 0; v0 < V; v0 += vc) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
-        CUtensorMap tm_wc;
-        if (!make_map(&tm_wc, W + v0 * D, nv, D, D, kLBN)) return cudaErrorInvalidValue;
         const DzEntEpi de{N, (int)vc, static_cast<const RowStat *>(a.stats), a.g, dz};
-        if ((e = launch_gemm(tm_h, tm_wc, N, nv, D, de, a.stream)) != cudaSuccess) return e;
+        if ((e = launch_logits_gemm(h, W + v0 * D, N, nv, D, de, a.stream, kGemmPairs)) != cudaSuccess) return e;
         if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dW),
                                       a.stream)) != cudaSuccess)
             return e;
