@@ -600,8 +600,14 @@ static int64_t chunk_cols(int64_t N, int64_t V) {
 // operands far larger than L2 along a long K, so their tiles run in small
 // m-groups (tile_coords): the concurrent CTAs then share a few A and B tiles
 // instead of each A tile being fetched from DRAM once per n-block.
-constexpr int kGradGroupM = 16;   // K2: 16 m-blocks of dz (8 MB each at vc = 32768) x the 16 n-blocks of D = 4096
-constexpr int kWGroupM = 8;       // K3: 8 m-blocks of dz^T (2 MB each at N = 8192) x the n-blocks of D
+#ifndef VP_K2_GROUP
+#define VP_K2_GROUP 16
+#endif
+#ifndef VP_K3_GROUP
+#define VP_K3_GROUP 8
+#endif
+constexpr int kGradGroupM = VP_K2_GROUP;   // K2: m-blocks of dz (8 MB each at vc = 32768) x the 16 n-blocks of D = 4096
+constexpr int kWGroupM = VP_K3_GROUP;      // K3: m-blocks of dz^T (2 MB each at N = 8192) x the n-blocks of D
 static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_bfloat16 *W, int N, int D, int64_t v0,
                                         int nv, int64_t vc, const __nv_bfloat16 *dz, float *acc,
                                         __nv_bfloat16 *dW, cudaStream_t stream) {
@@ -611,7 +617,7 @@ static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_b
         if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
             return cudaErrorInvalidValue;
         const AccEpi ae{N, D, v0 == 0, acc};
-        e = kGemmPairs ? launch_gemm_pair<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM / 2,
+        e = kGemmPairs ? launch_gemm_pair<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, (kGradGroupM + 1) / 2,
                                                                 kHintK2)
                        : launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM, kHintK2);
         if (e != cudaSuccess) return e;
@@ -621,7 +627,7 @@ static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_b
         if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc)) return cudaErrorInvalidValue;
         const StoreBf16Epi se{nv, D, v0, dW};
         e = kGemmPairs ? launch_gemm_pair<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream,
-                                                                     kWGroupM / 2, kHintK3)
+                                                                     (kWGroupM + 1) / 2, kHintK3)
                        : launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream, kWGroupM,
                                                                kHintK3);
         if (e != cudaSuccess)
