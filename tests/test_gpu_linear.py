@@ -126,3 +126,21 @@ def test_linear_logp_bwd_full_size_sampled():
     col = dW.double().sum(0).abs()
     scale = dW.double().abs().sum(0)
     assert torch.isfinite(dW).all() and (col <= 2.0 ** -7 * scale + 1e-6).all()
+
+
+@pytest.mark.parametrize("N", [9000, 17000])   # vocabulary chunks of 16384 and 8192 columns
+def test_linear_logp_bwd_many_rows_sampled(N):
+    V, D = 20011, 128
+    w = _bwd_case(N, V, D, seed=N)
+    dh, dW, err = _run_bwd(w)
+    assert err == 0
+    rows = [0, 1, 4095, 8191, N // 2, N - 1]
+    h64, W64 = parity.to64(w["hidden"][rows]), parity.to64(w["weight"])
+    t, g = w["targets"][rows].numpy(), w["grad"][rows].double().numpy()
+    ref_dh, _ = oracle.linear_logp_bwd(h64, W64, t, g, want_dW=False)
+    dz = np.abs(oracle.logprobs_bwd(oracle.linear_logits(h64, W64), t, g))
+    _check_gemm_grad(dh[rows], ref_dh, dz @ np.abs(W64), f"{N} rows dhidden")
+    # every dz row sums to 0, so each column of dW sums to 0 over the vocabulary
+    col = dW.double().sum(0).abs()
+    scale = dW.double().abs().sum(0)
+    assert torch.isfinite(dW).all() and (col <= 2.0 ** -7 * scale + 1e-6).all()
