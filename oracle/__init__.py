@@ -74,6 +74,8 @@ _SIGS = {
     "vpo_linear_entropy_bwd": (["P", "P", "I", "I", "I", "P", "P", "P", "P"], None),
     "vpo_linear_kl_fwd": (["P", "P", "P", "P", "I", "I", "I", "I", "i", "P", "P", "P", "P", "P", "P"], None),
     "vpo_linear_kl_bwd": (["P", "P", "P", "P", "I", "I", "I", "I", "i", "P", "P", "P", "P", "P", "P"], None),
+    "vpo_linear_jsd_fwd": (["P", "P", "P", "P", "I", "I", "I", "I", "d", "P", "P"], None),
+    "vpo_linear_jsd_bwd": (["P", "P", "P", "P", "I", "I", "I", "I", "d", "P", "P", "P", "P", "P", "P"], None),
 }
 _CT = {"P": ctypes.c_void_p, "I": ctypes.c_int64, "i": ctypes.c_int, "d": ctypes.c_double}
 
@@ -376,4 +378,29 @@ def linear_kl_bwd(ha, Wa, hb, Wb, g, direction=REVERSE, want=(True, True, True, 
     scratch = np.empty((4, N, V))
     (lib or _load()).vpo_linear_kl_bwd(_p(ha), _p(Wa), _p(hb), _p(Wb), N, V, Da, Db, int(direction), _p(g),
                                        *[_p(o) for o in outs], _p(scratch))
+    return tuple(outs)
+
+
+def linear_jsd_fwd(ha, Wa, hb, Wb, beta, lib=None):
+    """Generalized JSD (jsd_fwd) between model A (ha . Wa^T, the student) and model B (hb . Wb^T)."""
+    ha, Wa, N, V, Da = _linear_shapes(ha, Wa)
+    hb, Wb, Nb, Vb, Db = _linear_shapes(hb, Wb)
+    if (Nb, Vb) != (N, V):
+        raise ValueError("the two models disagree on N or V")
+    out = np.empty(N)
+    scratch = np.empty((2, N, V))
+    (lib or _load()).vpo_linear_jsd_fwd(_p(ha), _p(Wa), _p(hb), _p(Wb), N, V, Da, Db, float(beta), _p(out),
+                                        _p(scratch))
+    return out
+
+
+def linear_jsd_bwd(ha, Wa, hb, Wb, beta, g, want=(True, True, True, True), lib=None):
+    """Returns (dha, dWa, dhb, dWb) of sum_r g_r JSD_r; entries not wanted are None."""
+    ha, Wa, N, V, Da = _linear_shapes(ha, Wa)
+    hb, Wb, _, _, Db = _linear_shapes(hb, Wb)
+    g = _f64(g)
+    outs = [np.empty(s) if w else None for s, w in zip(((N, Da), (V, Da), (N, Db), (V, Db)), want)]
+    scratch = np.empty((4, N, V))
+    (lib or _load()).vpo_linear_jsd_bwd(_p(ha), _p(Wa), _p(hb), _p(Wb), N, V, Da, Db, float(beta), _p(g),
+                                        *[_p(o) for o in outs], _p(scratch))
     return tuple(outs)

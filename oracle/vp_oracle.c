@@ -712,3 +712,30 @@ void vpo_linear_kl_bwd(const double *ha, const double *Wa, const double *hb, con
     linear_chain_rule(ha, Wa, N, V, Da, dza, dha, dWa);
     linear_chain_rule(hb, Wb, N, V, Db, dzb, dhb, dWb);
 }
+
+/* Fused linear generalized JSD of two models [P1, the commit message adding
+ * vocab_parallel_jsd: "Motivation" (TRL's trainer computes KL/JSD from tiled
+ * LM-head projections without the full logits) and "Changes"]: the JSD of
+ * vpo_jsd_fwd (R13, with its beta = 0 / 1 endpoints) applied to the fp64
+ * logits rows of model A (ha . Wa^T, the student) and model B (hb . Wb^T, the
+ * teacher). scratch: caller-owned [2][N][V]. */
+void vpo_linear_jsd_fwd(const double *ha, const double *Wa, const double *hb, const double *Wb, int64_t N,
+                        int64_t V, int64_t Da, int64_t Db, double beta, double *jsd, double *scratch) {
+    double *za = scratch, *zb = scratch + N * V;
+    vpo_linear_logits(ha, Wa, N, V, Da, za);
+    vpo_linear_logits(hb, Wb, N, V, Db, zb);
+    vpo_jsd_fwd(za, zb, N, V, beta, jsd);
+}
+
+/* dhidden and dW of both models for sum_r g_r JSD_r; any output may be NULL.
+ * scratch: caller-owned [4][N][V]. */
+void vpo_linear_jsd_bwd(const double *ha, const double *Wa, const double *hb, const double *Wb, int64_t N,
+                        int64_t V, int64_t Da, int64_t Db, double beta, const double *g, double *dha, double *dWa,
+                        double *dhb, double *dWb, double *scratch) {
+    double *za = scratch, *zb = scratch + N * V, *dza = scratch + 2 * N * V, *dzb = scratch + 3 * N * V;
+    vpo_linear_logits(ha, Wa, N, V, Da, za);
+    vpo_linear_logits(hb, Wb, N, V, Db, zb);
+    vpo_jsd_bwd(za, zb, N, V, beta, g, dza, dzb);
+    linear_chain_rule(ha, Wa, N, V, Da, dza, dha, dWa);
+    linear_chain_rule(hb, Wb, N, V, Db, dzb, dhb, dWb);
+}

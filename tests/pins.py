@@ -747,6 +747,36 @@ def pin_linear_entropy_kl_closed_forms(lib=None):
            oracle.linear_kl_fwd(hb, Wb, ha, Wa, oracle.REVERSE, lib=lib)[0], 1e-15, 1e-15, "KL direction swap")
 
 
+def pin_linear_jsd(lib=None):
+    """Fused linear JSD: Decimal brute force, finite differences of all four gradients, the
+    endpoints as the linear KL calls, and a model against itself."""
+    ha, Wa, hb, Wb, g = _two_models(64, 3, 5, 3, 4)
+    with localcontext() as ctx:
+        ctx.prec = 60
+        za, zb = _dlogits(ha, Wa), _dlogits(hb, Wb)
+        for beta in (0.25, 0.7):
+            got = oracle.linear_jsd_fwd(ha, Wa, hb, Wb, beta, lib=lib)
+            for r in range(3):
+                _close(got[r], float(_djsd(za[r], zb[r], beta)), 1e-14, 1e-12, f"linear JSD brute force beta={beta}")
+    beta = 0.4
+    grads = oracle.linear_jsd_bwd(ha, Wa, hb, Wb, beta, g, lib=lib)
+    J = lambda a, b, c, e: float(np.dot(g, oracle.linear_jsd_fwd(a, b, c, e, beta, lib=lib)))
+    refs = (_fd(lambda x: J(x, Wa, hb, Wb), ha), _fd(lambda x: J(ha, x, hb, Wb), Wa),
+            _fd(lambda x: J(ha, Wa, x, Wb), hb), _fd(lambda x: J(ha, Wa, hb, x), Wb))
+    for got, ref, name in zip(grads, refs, ("dha", "dWa", "dhb", "dWb")):
+        _close(got, ref, 1e-8, 1e-6, f"linear JSD {name} FD")
+    # the endpoints are the KL calls: beta = 0 is KL(B || A), beta = 1 is KL(A || B)
+    _close(oracle.linear_jsd_fwd(ha, Wa, hb, Wb, 0.0, lib=lib),
+           oracle.linear_kl_fwd(ha, Wa, hb, Wb, oracle.FORWARD, lib=lib)[0], 1e-15, 1e-15, "linear JSD beta = 0")
+    _close(oracle.linear_jsd_fwd(ha, Wa, hb, Wb, 1.0, lib=lib),
+           oracle.linear_kl_fwd(ha, Wa, hb, Wb, oracle.REVERSE, lib=lib)[0], 1e-15, 1e-15, "linear JSD beta = 1")
+    # a model against itself: JSD = 0 and zero gradients
+    _close(oracle.linear_jsd_fwd(ha, Wa, ha, Wa, 0.5, lib=lib), np.zeros(3), 1e-15, 0,
+           "linear JSD of a model with itself")   # mix = p up to one rounding
+    for o in oracle.linear_jsd_bwd(ha, Wa, ha, Wa, 0.5, g, lib=lib):
+        _close(o, np.zeros_like(o), 1e-15, 0, "linear JSD gradients of a model with itself")
+
+
 ALL_PINS = [
     pin_brute_force_fwd,
     pin_brute_force_grads,
@@ -769,4 +799,5 @@ ALL_PINS = [
     pin_linear_entropy_kl_brute_force,
     pin_linear_entropy_kl_finite_differences,
     pin_linear_entropy_kl_closed_forms,
+    pin_linear_jsd,
 ]

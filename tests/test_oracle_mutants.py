@@ -78,6 +78,9 @@ MUTANTS = [
      "linear_chain_rule(ha, Wa, N, V, Da, dzb, dha, dWa);"),
     ("linear entropy bwd reads logits as dz", "linear_chain_rule(h, W, N, V, D, dz, dh, dW);",
      "linear_chain_rule(h, W, N, V, D, logits, dh, dW);"),
+    ("linear JSD models swapped", "vpo_jsd_fwd(za, zb, N, V, beta, jsd);", "vpo_jsd_fwd(zb, za, N, V, beta, jsd);"),
+    ("linear JSD bwd gradients of B to A", "vpo_jsd_bwd(za, zb, N, V, beta, g, dza, dzb);\n    linear_chain_rule(ha, Wa, N, V, Da, dza, dha, dWa);",
+     "vpo_jsd_bwd(za, zb, N, V, beta, g, dza, dzb);\n    linear_chain_rule(ha, Wa, N, V, Da, dzb, dha, dWa);"),
 ]
 
 
