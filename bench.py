@@ -417,6 +417,10 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     ms_kf = _time_ms(lambda: vp.vp_linear_kl_fwd(h, W, hb, Wb, vp.KL_REVERSE, kl=kl, stats_a=st, stats_b=sb,
                                                  workspace=wsk), reps)
     ms_kb = _time_ms(lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, vp.KL_REVERSE, st, sb, g, outs=outs, workspace=wsk), 3)
+    # generalized JSD (beta = 0.5) of the same two models: two forward passes of the dual GEMM
+    ms_jf = _time_ms(lambda: vp.vp_linear_jsd_fwd(h, W, hb, Wb, 0.5, jsd=kl, stats_a=st, stats_b=sb, workspace=wsk),
+                     reps)
+    ms_jb = _time_ms(lambda: vp.vp_linear_jsd_bwd(h, W, hb, Wb, 0.5, st, sb, g, outs=outs, workspace=wsk), 3)
     del wsk, outs, hb, Wb
     torch.cuda.empty_cache()
 
@@ -436,7 +440,9 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
                              "note": "three GEMMs of 2NVD each (logits recomputed, dhidden, dW)"},
             "entropy": line(ms_ef, ms_eb, 1, 3, "entropy of softmax(h W^T); backward: logits, dhidden, dW"),
             "kl": line(ms_kf, ms_kb, 2, 6, "KL(A||B) of two models of this shape; forward: both logits tiles; "
-                       "backward: both logits tiles, dhidden and dW of both models")}
+                       "backward: both logits tiles, dhidden and dW of both models"),
+            "jsd": line(ms_jf, ms_jb, 4, 6, "generalized JSD (beta = 0.5) of the two models; forward: two passes "
+                        "of both logits tiles; backward: as for KL")}
 
 
 def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev, chunks=8):

@@ -470,7 +470,7 @@ VP_API vp_status vp_linear_entropy_bwd(const void *hidden, const void *weight, i
                                        void *workspace, size_t workspace_bytes, vp_stream stream);
 
 /* Bytes of device workspace vp_linear_kl_fwd needs: a 32-byte record per row
- * and 256-column vocabulary tile. 0 for invalid sizes. */
+ * and 128 columns of the vocabulary. 0 for invalid sizes. */
 VP_API size_t vp_linear_kl_workspace_size(int64_t N, int64_t V);
 
 /* KL between the next-token distributions of two models over the same V
@@ -505,6 +505,38 @@ VP_API vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb
                                   int64_t V, int64_t Da, int64_t Db, int direction, const vp_rowstat *stats_a,
                                   const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
                                   void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream);
+
+/* Generalized JSD between two models' next-token distributions [P1, the
+ * commit message adding vocab_parallel_jsd: "Motivation" (divergences over
+ * tiled LM-head projections without the full logits) and "Changes"], with the
+ * JSD of vp_jsd_fwd: p = softmax(ha . wa^T) (A, the student), q =
+ * softmax(hb . wb^T) (B, the teacher), mix = beta q + (1 - beta) p,
+ * JSD = beta KL(q || mix) + (1 - beta) KL(p || mix). Models and layouts as
+ * vp_linear_kl_fwd. beta = 0 and beta = 1 are vp_linear_kl_fwd with
+ * VP_KL_FORWARD and VP_KL_REVERSE; 0 < beta < 1 takes two passes of the dual
+ * GEMM: the rows' maxima and log-sums of A and B, then both KL-to-mixture
+ * expectations together. Outputs: jsd fp32 [N]; stats_a, stats_b
+ * (vp_rowstat [N], the c fields holding KL(p || mix) and KL(q || mix)).
+ * workspace: vp_linear_jsd_workspace_size(N, V) bytes. beta outside [0, 1]
+ * or NaN: VP_ERR_ARG. */
+VP_API size_t vp_linear_jsd_workspace_size(int64_t N, int64_t V);
+VP_API vp_status vp_linear_jsd_fwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
+                                   int64_t V, int64_t Da, int64_t Db, double beta, float *jsd,
+                                   vp_rowstat *stats_a, vp_rowstat *stats_b, void *workspace, size_t workspace_bytes,
+                                   vp_stream stream);
+
+/* Gradients of sum_r g[r] JSD[r] from the records of vp_linear_jsd_fwd with
+ * the same beta: dz_A = g (1 - beta) p ((log p - log mix) - KL(p || mix)),
+ * dz_B = g beta q ((log q - log mix) - KL(q || mix)) formed in the dual GEMM's
+ * epilogue, then dhidden = dz . W and dW = dz^T . h for each model asked for
+ * (outputs as vp_linear_kl_bwd; any may be NULL, not all). At beta = 0 and 1,
+ * vp_linear_kl_bwd with the matching direction. workspace:
+ * vp_linear_jsd_bwd_workspace_size(N, V, Da, Db) bytes. */
+VP_API size_t vp_linear_jsd_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t Db);
+VP_API vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
+                                   int64_t V, int64_t Da, int64_t Db, double beta, const vp_rowstat *stats_a,
+                                   const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
+                                   void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                      */

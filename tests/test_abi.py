@@ -160,3 +160,17 @@ def test_linear_entropy_kl_entry_points_check_arguments_on_the_host():
                                 None) == ERR_NULL
     assert lib.vp_linear_kl_bwd_workspace_size(4, 16, 64, 128) > 0
     assert lib.vp_linear_kl_workspace_size(4, 0) == 0
+
+
+def test_linear_jsd_entry_points_check_beta_first():
+    lib = _lib.lib()
+    ws = ctypes.c_size_t(1 << 30)
+    two = (FAKE, FAKE, FAKE, FAKE, 4, 16, 64, 128)
+    for beta in (-0.1, 1.5, float("nan")):
+        assert lib.vp_linear_jsd_fwd(*two, beta, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_ARG
+        assert lib.vp_linear_jsd_bwd(*two, beta, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, ws, None) == ERR_ARG
+    assert lib.vp_linear_jsd_fwd(FAKE, FAKE, FAKE, FAKE, 4, 16, 64, 96, 0.5, FAKE, FAKE, FAKE, FAKE, ws,
+                                 None) == ERR_SHAPE
+    assert lib.vp_linear_jsd_bwd(*two, 0.5, FAKE, FAKE, FAKE, None, None, None, None, FAKE, ws, None) == ERR_ARG
+    assert lib.vp_linear_jsd_fwd(*two, 0.5, FAKE_ODD, FAKE, FAKE, FAKE, ws, None) == ERR_ALIGN
+    assert lib.vp_linear_jsd_workspace_size(4, 16) == lib.vp_linear_kl_workspace_size(4, 16)

@@ -201,3 +201,63 @@ def test_linear_entropy_kl_full_size_sampled():
     M = parity.oracle_all(z, z, np.zeros(len(rows), np.int64), g64, ops=("entropy",))["_mag"]["dH"]
     parity.check_gemm_grad(dha[rows], rdh, dz @ np.abs(W64), "full-size entropy dhidden", M @ np.abs(W64))
     assert torch.isfinite(dWa).all()
+
+
+# ---------------------------------------------------------------------------
+# Generalized JSD of two models (interior beta; the endpoints are the KL calls)
+# ---------------------------------------------------------------------------
+def _jsd_mags(za, zb, beta, g):
+    """M_j of the fp32 evaluation of dA and dB (as for the logits-level JSD)."""
+    _, ma, la = oracle.entropy_fwd(za)
+    _, mb, lb = oracle.entropy_fwd(zb)
+    lp, lq = (za - ma[:, None]) - la[:, None], (zb - mb[:, None]) - lb[:, None]
+    p, q = np.exp(lp), np.exp(lq)
+    lmix = np.log(beta * q + (1 - beta) * p)
+    ka, kb = np.sum(p * (lp - lmix), 1), np.sum(q * (lq - lmix), 1)
+    ag = np.abs(g)[:, None]
+    Ma = ag * (1 - beta) * p * (np.abs(lp) + np.abs(lmix) + np.abs(ka)[:, None] + 1.0)
+    Mb = ag * beta * q * (np.abs(lq) + np.abs(lmix) + np.abs(kb)[:, None] + 1.0)
+    return Ma, Mb
+
+
+@pytest.mark.parametrize("beta", [0.3, 0.5, 0.9])
+@pytest.mark.parametrize("N,V,Da,Db", [(256, 1024, 256, 128), (130, 300, 64, 64), (72, 70000, 64, 128)])
+def test_linear_jsd_fwd_bwd(N, V, Da, Db, beta):
+    ha, Wa, hb, Wb, g = _kl_case(N, V, Da, Db, seed=N + V + Da + Db + 7)
+    dev = [t.to(DEV) for t in (ha, Wa, hb, Wb, g)]
+    jsd, sa, sb = vp.vp_linear_jsd_fwd(*dev[:4], beta)
+    grads = vp.vp_linear_jsd_bwd(*dev[:4], beta, sa, sb, dev[4])
+    torch.cuda.synchronize()
+    ha64, Wa64, hb64, Wb64 = (parity.to64(t) for t in (ha, Wa, hb, Wb))
+    g64 = g.double().numpy()
+    tag = f"{N}x{V} Da={Da} Db={Db} beta={beta}"
+    parity.check_out(jsd, oracle.linear_jsd_fwd(ha64, Wa64, hb64, Wb64, beta), f"{tag} JSD")
+    ref = oracle.linear_jsd_bwd(ha64, Wa64, hb64, Wb64, beta, g64)
+    za, zb = oracle.linear_logits(ha64, Wa64), oracle.linear_logits(hb64, Wb64)
+    dza, dzb = (np.abs(x) for x in oracle.jsd_bwd(za, zb, beta, g64))
+    Ma, Mb = _jsd_mags(za, zb, beta, g64)
+    mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
+    evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
+    for got, r, mg, ev, name in zip(grads, ref, mags, evals, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, mg, f"{tag} {name}", ev)
+
+
+def test_linear_jsd_endpoints_frozen_teacher_and_invariance():
+    N, V, Da, Db = 136, 1500, 128, 64
+    ha, Wa, hb, Wb, g = (t.to(DEV) for t in _kl_case(N, V, Da, Db, seed=43))
+    for beta, d in ((0.0, vp.KL_FORWARD), (1.0, vp.KL_REVERSE)):
+        jsd, _, _ = vp.vp_linear_jsd_fwd(ha, Wa, hb, Wb, beta)
+        kl, _, _ = vp.vp_linear_kl_fwd(ha, Wa, hb, Wb, d)
+        torch.cuda.synchronize()
+        assert torch.equal(jsd, kl), f"beta = {beta} is the KL call"
+    jsd, sa, sb = vp.vp_linear_jsd_fwd(ha, Wa, hb, Wb, 0.5)
+    full = vp.vp_linear_jsd_bwd(ha, Wa, hb, Wb, 0.5, sa, sb, g)
+    student = vp.vp_linear_jsd_bwd(ha, Wa, hb, Wb, 0.5, sa, sb, g, want=(True, True, False, False))
+    part, _, _ = vp.vp_linear_jsd_fwd(ha[64:128].contiguous(), Wa, hb[64:128].contiguous(), Wb, 0.5)
+    same, _, _ = vp.vp_linear_jsd_fwd(ha, Wa, ha, Wa, 0.5)
+    torch.cuda.synchronize()
+    assert student[2] is None and torch.equal(student[0], full[0]) and torch.equal(student[1], full[1])
+    assert torch.equal(jsd[64:128].view(torch.int32), part.view(torch.int32))
+    assert float(same.abs().max()) < 1e-5          # a model against itself: mix = p up to rounding
+    with pytest.raises(vp.VPError):
+        vp.vp_linear_jsd_fwd(ha, Wa, hb, Wb, 1.5)

@@ -33,6 +33,9 @@ SIGNATURES = {
     "vp_linear_entropy_bwd": [P, P, I64, I64, I64, P, P, P, P, P, ctypes.c_size_t, P],
     "vp_linear_kl_fwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, ctypes.c_size_t, P],
     "vp_linear_kl_bwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_jsd_fwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_jsd_bwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P, P, P, ctypes.c_size_t,
+                          P],
     "vp_jsd_fwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P],
     "vp_jsd_bwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P],
     "vp_logprobs_partial": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P],
@@ -68,7 +71,9 @@ def lib():
             for name, args in (("vp_linear_entropy_workspace_size", [I64, I64, I64]),
                                ("vp_linear_entropy_bwd_workspace_size", [I64, I64, I64]),
                                ("vp_linear_kl_workspace_size", [I64, I64]),
-                               ("vp_linear_kl_bwd_workspace_size", [I64, I64, I64, I64])):
+                               ("vp_linear_kl_bwd_workspace_size", [I64, I64, I64, I64]),
+                               ("vp_linear_jsd_workspace_size", [I64, I64]),
+                               ("vp_linear_jsd_bwd_workspace_size", [I64, I64, I64, I64])):
                 fn = getattr(h, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_size_t

@@ -384,6 +384,36 @@ def vp_linear_kl_bwd(ha, wa, hb, wb, direction, stats_a, stats_b, grad, want=(Tr
     return tuple(outs)
 
 
+def vp_linear_jsd_fwd(ha, wa, hb, wb, beta: float = 0.5, jsd=None, stats_a=None, stats_b=None, workspace=None):
+    """Generalized JSD of softmax(ha @ wa^T) (student) and softmax(hb @ wb^T) (teacher).
+    Returns (jsd fp32 [N], stats_a, stats_b)."""
+    N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_jsd_fwd")
+    jsd = _f32(N, ha) if jsd is None else jsd
+    stats_a = rowstats(N, ha.device) if stats_a is None else stats_a
+    stats_b = rowstats(N, ha.device) if stats_b is None else stats_b
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_jsd_workspace_size(N, V), ha)
+    _check(_lib.lib().vp_linear_jsd_fwd(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, float(beta),
+                                        _ptr(jsd), _ptr(stats_a), _ptr(stats_b), _ptr(workspace), workspace.numel(),
+                                        _stream()), "vp_linear_jsd_fwd")
+    return jsd, stats_a, stats_b
+
+
+def vp_linear_jsd_bwd(ha, wa, hb, wb, beta, stats_a, stats_b, grad, want=(True, True, True, True), outs=None,
+                      workspace=None):
+    """Gradients of sum_r grad[r] JSD[r]: (dha, dwa, dhb, dwb), bf16, None where not wanted."""
+    N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_jsd_bwd")
+    shapes = ((N, Da), (V, Da), (N, Db), (V, Db))
+    if outs is None:
+        outs = [torch.empty(s, dtype=torch.bfloat16, device=ha.device) if w else None for s, w in zip(shapes, want)]
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_jsd_bwd_workspace_size(N, V, Da, Db), ha)
+    _check(_lib.lib().vp_linear_jsd_bwd(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, float(beta),
+                                        _ptr(stats_a), _ptr(stats_b), _ptr(grad), *[_ptr(o) for o in outs],
+                                        _ptr(workspace), workspace.numel(), _stream()), "vp_linear_jsd_bwd")
+    return tuple(outs)
+
+
 # ---------------------------------------------------------------------------
 # Vocabulary-sharded forms: per-shard records, gathered by the caller, merged
 # ---------------------------------------------------------------------------

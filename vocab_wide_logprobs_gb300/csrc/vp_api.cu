@@ -498,6 +498,63 @@ vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb, const
     return launched(vp::launch_linear_kl_bwd(a));
 }
 
+static bool beta_ok(double beta) { return beta >= 0.0 && beta <= 1.0; }   // false for NaN
+
+size_t vp_linear_jsd_workspace_size(int64_t N, int64_t V) { return vp_linear_kl_workspace_size(N, V); }
+
+vp_status vp_linear_jsd_fwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
+                            int64_t Da, int64_t Db, double beta, float *jsd, vp_rowstat *stats_a,
+                            vp_rowstat *stats_b, void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!beta_ok(beta)) return VP_ERR_ARG;
+    if (beta == 0.0)
+        return vp_linear_kl_fwd(ha, wa, hb, wb, N, V, Da, Db, VP_KL_FORWARD, jsd, stats_a, stats_b, workspace,
+                                workspace_bytes, stream);
+    if (beta == 1.0)
+        return vp_linear_kl_fwd(ha, wa, hb, wb, N, V, Da, Db, VP_KL_REVERSE, jsd, stats_a, stats_b, workspace,
+                                workspace_bytes, stream);
+    if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!ha || !wa || !hb || !wb || !jsd || !stats_a || !stats_b || !workspace) return VP_ERR_NULL;
+    if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(jsd, 4) ||
+        !aligned(stats_a, 16) || !aligned(stats_b, 16) || !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_kl_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, 0, jsd, stats_a, stats_b, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, workspace, (cudaStream_t)stream, (float)beta};
+    return launched(vp::launch_linear_jsd_fwd(a));
+}
+
+size_t vp_linear_jsd_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t Db) {
+    return vp_linear_kl_bwd_workspace_size(N, V, Da, Db);
+}
+
+vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
+                            int64_t Da, int64_t Db, double beta, const vp_rowstat *stats_a,
+                            const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
+                            void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!beta_ok(beta)) return VP_ERR_ARG;
+    if (beta == 0.0 || beta == 1.0)
+        return vp_linear_kl_bwd(ha, wa, hb, wb, N, V, Da, Db, beta == 0.0 ? VP_KL_FORWARD : VP_KL_REVERSE, stats_a,
+                                stats_b, grad_out, dha, dwa, dhb, dwb, workspace, workspace_bytes, stream);
+    if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
+    if (!dha && !dwa && !dhb && !dwb) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!ha || !wa || !hb || !wb || !stats_a || !stats_b || !grad_out || !workspace) return VP_ERR_NULL;
+    if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(stats_a, 16) ||
+        !aligned(stats_b, 16) || !aligned(grad_out, 4) || !aligned(dha, 16) || !aligned(dwa, 16) ||
+        !aligned(dhb, 16) || !aligned(dwb, 16) || !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_kl_bwd_workspace_bytes(N, V, Da, Db)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, 0, nullptr,
+                       const_cast<vp_rowstat *>(stats_a), const_cast<vp_rowstat *>(stats_b), grad_out,
+                       dha, dwa, dhb, dwb, workspace, (cudaStream_t)stream, (float)beta};
+    return launched(vp::launch_linear_jsd_bwd(a));
+}
+
 vp_status vp_fault_status(uint32_t *value, int clear) {
     if (!value) return VP_ERR_NULL;
     vp_status st = check_device();

@@ -25,6 +25,12 @@ constexpr int kLBStage = kLBN * kLBK * 2;          // 32 KB
 constexpr int kLStageBytes = kLAStage + kLBStage;  // 48 KB
 constexpr int kLSmemBytes = kLStages * kLStageBytes + 1024;  // + alignment slack
 constexpr int kLThreads = 192;                     // TMA warp, MMA warp, 4 epilogue warps
+// The dual form has 8 epilogue warps: two per TMEM lane quarter, each taking
+// one 128-column half of the accumulators, so that the epilogue (which the
+// single accumulator set does not overlap with the next tile's MMAs) has half
+// the work per warp and twice the warps to hide its latencies.
+constexpr int kDualEpiCols = 128;
+__host__ __device__ constexpr int gemm_threads(bool dual) { return dual ? 64 + 8 * 32 : kLThreads; }
 constexpr uint32_t kLTmemCols = 2 * kLBN;          // two accumulators
 
 // Set when a bounded wait of the linear kernels gave up.
@@ -73,7 +79,7 @@ __device__ __forceinline__ void tile_coords(int64_t tile, int n_mb, int n_nb, in
 }
 
 template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
-__global__ void __launch_bounds__(kLThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(kDual), 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M, int Nn,
                  int K, int K2, int group_m, int l2hints, const Epi epi) {
@@ -94,7 +100,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars.acc_full[b], 1);
-            mbar_init(&bars.acc_empty[b], 4 * 32);
+            mbar_init(&bars.acc_empty[b], gemm_threads(kDual) - 64);   // every epilogue thread
         }
         fence_mbar_init();
         prefetch_tensormap(&tm_a);
@@ -187,6 +193,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         // ---------------- epilogue ----------------
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const int r_in = q * 32 + lane;
+        const int half = kDual ? (warp - 2) >> 2 : 0;   // dual form: the warp's 128-column half
         uint32_t j = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
@@ -200,9 +207,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             tc_fence_after();
             // tcgen05.ld is warp-collective: the whole warp calls the epilogue or
             // none of it does, and epilogues guard only their global accesses
-            if (__all_sync(0xffffffffu, ok))
-                epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
-                    tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
+            const int c0 = nb * kLBN + half * kDualEpiCols;
+            const int ncol = min(kDual ? kDualEpiCols : kLBN, Nn - c0);
+            if (__all_sync(0xffffffffu, ok) && ncol > 0)
+                epi(mb * kLBM + r_in, c0, ncol, tmem + buf * kLBN + half * kDualEpiCols + ((uint32_t)(q * 32) << 16));
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[buf]);           // the MMA warp may reuse the accumulator
         }
@@ -497,7 +505,7 @@ static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb
         group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / a_tile);
     }
     if (group_m > n_mb) group_m = n_mb;
-    umma_gemm_kernel<Epi, kAMn, kBMn, kDual><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, ta2, tb2, M, Nn, K,
+    umma_gemm_kernel<Epi, kAMn, kBMn, kDual><<<grid, gemm_threads(kDual), kLSmemBytes, stream>>>(ta, tb, ta2, tb2, M, Nn, K,
                                                                                        K2, group_m, l2hints, epi);
     return cudaGetLastError();
 }

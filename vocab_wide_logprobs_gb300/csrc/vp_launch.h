@@ -161,12 +161,16 @@ struct LinearKLArgs {
     void *dha, *dwa, *dhb, *dwb;  // backward outputs, bf16; any may be NULL (not all)
     void *workspace;
     cudaStream_t stream;
+    float beta = 0.f;             // generalized JSD: 0 < beta < 1 (the KL calls at 0 and 1)
 };
 
 size_t linear_kl_workspace_bytes(int64_t N, int64_t V);
 size_t linear_kl_bwd_workspace_bytes(int64_t N, int64_t V, int64_t Da, int64_t Db);
 cudaError_t launch_linear_kl_fwd(const LinearKLArgs &a);
 cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a);
+// Fused linear generalized JSD, interior beta (kl = the JSD output)
+cudaError_t launch_linear_jsd_fwd(const LinearKLArgs &a);
+cudaError_t launch_linear_jsd_bwd(const LinearKLArgs &a);
 
 cudaError_t launch_logprobs_fwd(const StatsArgs &a);
 cudaError_t launch_entropy_fwd(const StatsArgs &a);

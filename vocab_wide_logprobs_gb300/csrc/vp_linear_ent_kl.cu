@@ -96,7 +96,7 @@ struct KLEpi {
         const uint32_t tp = taddr + (p_is_a ? 0u : (uint32_t)kLBN), tq = taddr + (p_is_a ? (uint32_t)kLBN : 0u);
         float mp = -INFINITY, mq = -INFINITY;
 #pragma unroll 1
-        for (int c = 0; c < kLBN / 32; ++c) {
+        for (int c = 0; c < kDualEpiCols / 32; ++c) {
             float a[32], b[32];
             tmem_ld32(tp + c * 32, a);
             tmem_ld32(tq + c * 32, b);
@@ -109,7 +109,7 @@ struct KLEpi {
         }
         float sp = 0.f, sq = 0.f, w = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < kLBN / 32; ++c) {
+        for (int c = 0; c < kDualEpiCols / 32; ++c) {
             float a[32], b[32];
             tmem_ld32(tp + c * 32, a);
             tmem_ld32(tq + c * 32, b);
@@ -125,7 +125,7 @@ struct KLEpi {
             }
         }
         if (row >= N) return;
-        parts[(int64_t)row * n_vt + col0 / kLBN] = KLTile{mp, sp, mq, sq, w, 0.f, 0.f, 0.f};
+        parts[(int64_t)row * n_vt + col0 / kDualEpiCols] = KLTile{mp, sp, mq, sq, w, 0.f, 0.f, 0.f};
     }
 };
 
@@ -294,7 +294,7 @@ struct DzKLEpi {
         const uint32_t tp = taddr + (p_is_a ? 0u : (uint32_t)kLBN), tq = taddr + (p_is_a ? (uint32_t)kLBN : 0u);
         __nv_bfloat16 *dzp = p_is_a ? dza : dzb, *dzq = p_is_a ? dzb : dza;
 #pragma unroll 1
-        for (int c = 0; c < kLBN / 32; ++c) {
+        for (int c = 0; c < kDualEpiCols / 32; ++c) {
             float a[32], b[32];
             tmem_ld32(tp + c * 32, a);
             tmem_ld32(tq + c * 32, b);
@@ -365,14 +365,17 @@ cudaError_t launch_linear_entropy_bwd(const LinearEntArgs &a) {
     return cudaSuccess;
 }
 
-size_t linear_kl_workspace_bytes(int64_t N, int64_t V) { return up256((size_t)N * n_vtiles(V) * sizeof(KLTile)); }
+// records of the dual epilogues: one per 128-column half tile (kDualEpiCols)
+static int64_t n_dual_tiles(int64_t V) { return (V + kDualEpiCols - 1) / kDualEpiCols; }
+
+size_t linear_kl_workspace_bytes(int64_t N, int64_t V) { return up256((size_t)N * n_dual_tiles(V) * sizeof(KLTile)); }
 
 cudaError_t launch_linear_kl_fwd(const LinearKLArgs &a) {
     CUtensorMap tm_ha, tm_wa, tm_hb, tm_wb;
     if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kLBN) ||
         !make_map(&tm_hb, a.hb, a.N, a.Db, a.Db, kLBM) || !make_map(&tm_wb, a.wb, a.V, a.Db, a.Db, kLBN))
         return cudaErrorInvalidValue;
-    const int n_vt = (int)n_vtiles(a.V);
+    const int n_vt = (int)n_dual_tiles(a.V);
     const bool p_is_a = a.direction == 0;
     KLTile *parts = static_cast<KLTile *>(a.workspace);
     const KLEpi epi{(int)a.N, n_vt, p_is_a, parts};
@@ -391,7 +394,11 @@ size_t linear_kl_bwd_workspace_bytes(int64_t N, int64_t V, int64_t Da, int64_t D
     return 2 * dz + up256((size_t)N * Da * 4) + up256((size_t)N * Db * 4);
 }
 
-cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
+// Backward of a two-model op: per vocabulary chunk, the dual GEMM recomputes
+// both logits tiles and the epilogue made by make_epi(dza, dzb) writes dz of A
+// and / or B; then the gradient GEMMs of each model whose gradients are asked for.
+template <class MakeEpi>
+static cudaError_t two_model_bwd(const LinearKLArgs &a, MakeEpi make_epi) {
     const int64_t vc = chunk_cols(a.N, a.V);
     const size_t dz_bytes = up256((size_t)a.N * vc * 2);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
@@ -403,8 +410,6 @@ cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
     const __nv_bfloat16 *ha = static_cast<const __nv_bfloat16 *>(a.ha), *hb = static_cast<const __nv_bfloat16 *>(a.hb);
     const __nv_bfloat16 *Wa = static_cast<const __nv_bfloat16 *>(a.wa), *Wb = static_cast<const __nv_bfloat16 *>(a.wb);
     const int N = (int)a.N, V = (int)a.V, Da = (int)a.Da, Db = (int)a.Db;
-    const bool p_is_a = a.direction == 0;
-    const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
     cudaError_t e;
     CUtensorMap tm_ha, tm_hb, tm_ha_mn, tm_hb_mn;
     if (!make_map(&tm_ha, ha, N, Da, Da, kLBM) || !make_map(&tm_hb, hb, N, Db, Db, kLBM) ||
@@ -415,7 +420,7 @@ cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
         CUtensorMap tm_wac, tm_wbc;
         if (!make_map(&tm_wac, Wa + v0 * Da, nv, Da, Da, kLBN) || !make_map(&tm_wbc, Wb + v0 * Db, nv, Db, Db, kLBN))
             return cudaErrorInvalidValue;
-        const DzKLEpi de{N, (int)vc, p_is_a, p_is_a ? sa : sb, p_is_a ? sb : sa, a.g, dza, dzb};
+        const auto de = make_epi((int)vc, dza, dzb);
         if ((e = launch_gemm_dual(tm_ha, tm_wac, tm_hb, tm_wbc, N, nv, Da, Db, de, a.stream)) != cudaSuccess) return e;
         if (want_a && (e = chunk_gradient_gemms(tm_ha_mn, Wa, N, Da, v0, nv, vc, dza, acc_a,
                                                 static_cast<__nv_bfloat16 *>(a.dwa), a.stream)) != cudaSuccess)
@@ -429,6 +434,163 @@ cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
         return e;
     if (a.dhb) return finish_dhidden(acc_b, (int64_t)N * Db, static_cast<__nv_bfloat16 *>(a.dhb), a.stream);
     return cudaSuccess;
+}
+
+cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
+    const bool p_is_a = a.direction == 0;
+    const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
+    return two_model_bwd(a, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb) {
+        return DzKLEpi{(int)a.N, ldz, p_is_a, p_is_a ? sa : sb, p_is_a ? sb : sa, a.g, dza, dzb};
+    });
+}
+
+// ---------------------------------------------------------------------------
+// Generalized JSD of two models, interior beta ([P1], the commit message adding
+// vocab_parallel_jsd: "Motivation" names teacher-student divergences computed
+// from tiled LM-head projections, "Changes" the two passes: global
+// normalisation first, then both KL-to-mixture expectations together).
+//   pass 1  the KL forward's dual GEMM and merge: each row's exact maxima and
+//           log-sums of A and B in the two records;
+//   pass 2  the dual GEMM again; the epilogue (JsdEpi) forms log p, log q and
+//           log mix (mix = beta q + (1 - beta) p) in base-2 units and sums
+//           p (log p - log mix) and q (log q - log mix) per tile; a merge per
+//           row adds the tiles, writes JSD = beta KL(q||mix) + (1 - beta)
+//           KL(p||mix) and keeps the two expectations in the records' c fields;
+//   backward  the dual GEMM, dA = g (1 - beta) p ((log p - log mix) - KL(p||mix))
+//           and dB = g beta q ((log q - log mix) - KL(q||mix)) in the epilogue
+//           (DzJsdEpi), then the gradient GEMMs of each model asked for.
+// ---------------------------------------------------------------------------
+struct JsdTile {
+    float kp, kq;   // sum p (log2 p - log2 mix), sum q (log2 q - log2 mix) over the tile
+};
+
+struct JsdEpi {
+    int N, n_vt;
+    float beta;
+    const RowStat *sa, *sb;   // records of pass 1
+    JsdTile *parts;           // [N][n_vt]
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        const bool valid = row < N;
+        const int r = valid ? row : 0;
+        const RowStat A = load_rowstat(sa + r), B = load_rowstat(sb + r);
+        const float omb = 1.f - beta;
+        float kp = 0.f, kq = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kDualEpiCols / 32; ++c) {
+            float a[32], b[32];
+            tmem_ld32(taddr + c * 32, a);
+            tmem_ld32(taddr + kLBN + c * 32, b);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if (c * 32 + i >= ncol) continue;
+                const float xa = ((a[i] - A.m) - A.logS_hi) * kLog2e;   // log2 p
+                const float xb = ((b[i] - B.m) - B.logS_hi) * kLog2e;   // log2 q
+                const float p = ex2_fast(xa), q = ex2_fast(xb);
+                const float lm = fmaxf(lg2_fast(fmaf(beta, q, omb * p)), -250.f);
+                if (p > 0.f) kp = fmaf(p, xa - lm, kp);                  // zero-weight terms add nothing
+                if (q > 0.f) kq = fmaf(q, xb - lm, kq);
+            }
+        }
+        if (!valid) return;
+        parts[(int64_t)row * n_vt + col0 / kDualEpiCols] = JsdTile{kp, kq};
+    }
+};
+
+__global__ void __launch_bounds__(256)
+linear_jsd_merge_kernel(int N, int n_vt, float beta, const JsdTile *__restrict__ parts, float *__restrict__ jsd,
+                        RowStat *__restrict__ sa, RowStat *__restrict__ sb) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const JsdTile *p = parts + (int64_t)row * n_vt;
+    DF kp{0.f, 0.f}, kq{0.f, 0.f};
+    for (int i = lane; i < n_vt; i += 32) {
+        df_add(kp, p[i].kp);
+        df_add(kq, p[i].kq);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        df_add(kp, shfl_xor(kp, m));
+        df_add(kq, shfl_xor(kq, m));
+    }
+    if (lane != 0) return;
+    const double ln2 = 0.69314718055994530942;
+    const double KLp = df_value(kp) * ln2, KLq = df_value(kq) * ln2;
+    const bool bad = ((sa[row].flags | sb[row].flags) & (kRowNanInf | kRowEmpty)) != 0;
+    const DF cp = df_from(KLp), cq = df_from(KLq);
+    sa[row].c_hi = cp.hi;
+    sa[row].c_lo = cp.lo;
+    sb[row].c_hi = cq.hi;
+    sb[row].c_lo = cq.lo;
+    jsd[row] = bad ? qnan() : (float)((double)beta * KLq + (1.0 - (double)beta) * KLp);
+}
+
+struct DzJsdEpi {
+    int N, ldz;
+    float beta;
+    const RowStat *sa, *sb;
+    const float *g;
+    __nv_bfloat16 *dza, *dzb;   // either may be null
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+        const bool valid = row < N;
+        const int r = valid ? row : 0;
+        const RowStat A = load_rowstat(sa + r), B = load_rowstat(sb + r);
+        const bool nan = ((A.flags | B.flags) & (kRowNanInf | kRowEmpty)) != 0;
+        const float gr = valid ? g[row] : 0.f, omb = 1.f - beta;
+        const float ka = A.c_hi + A.c_lo, kb = B.c_hi + B.c_lo;   // KL(p||mix), KL(q||mix)
+        const float ln2 = 0.69314718055994530942f;
+#pragma unroll 1
+        for (int c = 0; c < kDualEpiCols / 32; ++c) {
+            float a[32], b[32];
+            tmem_ld32(taddr + c * 32, a);
+            tmem_ld32(taddr + kLBN + c * 32, b);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float la = (a[i] - A.m) - A.logS_hi, lb = (b[i] - B.m) - B.logS_hi;   // log p, log q
+                const float p = ex2_fast(la * kLog2e), q = ex2_fast(lb * kLog2e);
+                const float lmix = fmaxf(lg2_fast(fmaf(beta, q, omb * p)), -250.f) * ln2;
+                float dA = p == 0.f ? 0.f : gr * omb * p * ((la - lmix) - ka);
+                float dB = q == 0.f ? 0.f : gr * beta * q * ((lb - lmix) - kb);
+                if (c * 32 + i >= ncol) dA = dB = 0.f;
+                else if (nan) dA = dB = qnan();
+                a[i] = dA;
+                b[i] = dB;
+            }
+            if (!valid) continue;
+            const int64_t off = (int64_t)row * ldz + col0 + c * 32;
+            if (dza) store_dz32(dza + off, a);
+            if (dzb) store_dz32(dzb + off, b);
+        }
+    }
+};
+
+cudaError_t launch_linear_jsd_fwd(const LinearKLArgs &a) {
+    // pass 1: the records (the KL forward; its KL output is overwritten below)
+    LinearKLArgs k = a;
+    k.direction = 0;
+    cudaError_t e = launch_linear_kl_fwd(k);
+    if (e != cudaSuccess) return e;
+    // pass 2: both KL-to-mixture expectations (the workspace is free again)
+    CUtensorMap tm_ha, tm_wa, tm_hb, tm_wb;
+    if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kLBN) ||
+        !make_map(&tm_hb, a.hb, a.N, a.Db, a.Db, kLBM) || !make_map(&tm_wb, a.wb, a.V, a.Db, a.Db, kLBN))
+        return cudaErrorInvalidValue;
+    const int n_vt = (int)n_dual_tiles(a.V);
+    RowStat *sa = static_cast<RowStat *>(a.stats_a), *sb = static_cast<RowStat *>(a.stats_b);
+    JsdTile *parts = static_cast<JsdTile *>(a.workspace);
+    const JsdEpi epi{(int)a.N, n_vt, a.beta, sa, sb, parts};
+    e = launch_gemm_dual(tm_ha, tm_wa, tm_hb, tm_wb, (int)a.N, (int)a.V, (int)a.Da, (int)a.Db, epi, a.stream);
+    if (e != cudaSuccess) return e;
+    linear_jsd_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>((int)a.N, n_vt, a.beta, parts, a.kl, sa,
+                                                                               sb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_linear_jsd_bwd(const LinearKLArgs &a) {
+    const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
+    return two_model_bwd(a, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb) {
+        return DzJsdEpi{(int)a.N, ldz, a.beta, sa, sb, a.g, dza, dzb};
+    });
 }
 
 cudaError_t read_linear_ent_kl_fault(uint32_t *value, bool clear) { return read_tu_fault(value, clear); }
