@@ -261,3 +261,39 @@ def test_linear_jsd_endpoints_frozen_teacher_and_invariance():
     assert float(same.abs().max()) < 1e-5          # a model against itself: mix = p up to rounding
     with pytest.raises(vp.VPError):
         vp.vp_linear_jsd_fwd(ha, Wa, hb, Wb, 1.5)
+
+
+# ---------------------------------------------------------------------------
+# Edge cases: the smallest problem, and a NaN row of hidden states
+# ---------------------------------------------------------------------------
+def test_linear_ops_smallest_problem():
+    ha, Wa, hb, Wb, g = _kl_case(1, 1, 64, 64, seed=61)
+    dev = [t.to(DEV) for t in (ha, Wa, hb, Wb, g)]
+    t = torch.zeros(1, dtype=torch.int64, device=DEV)
+    lp, _ = vp.vp_linear_logp_fwd(dev[0], dev[1], t)
+    H, _ = vp.vp_linear_entropy_fwd(dev[0], dev[1])
+    kl, _, _ = vp.vp_linear_kl_fwd(*dev[:4])
+    jsd, sa, sb = vp.vp_linear_jsd_fwd(*dev[:4], 0.5)
+    grads = vp.vp_linear_jsd_bwd(*dev[:4], 0.5, sa, sb, dev[4])
+    torch.cuda.synchronize()
+    # one vocabulary row: p = q = 1, so logp = H = KL = JSD = 0 and every gradient is 0
+    for x in (lp, H, kl, jsd):
+        assert float(x.abs().max()) == 0.0
+    assert all(float(gr.abs().max()) == 0.0 for gr in grads)
+
+
+def test_linear_ops_nan_hidden_row():
+    N, V, D = 130, 1000, 128
+    ha, Wa, hb, Wb, g = _kl_case(N, V, D, D, seed=62)
+    ha = ha.clone()
+    ha[7, 5] = float("nan")
+    dev = [t.to(DEV) for t in (ha, Wa, hb, Wb, g)]
+    H, st = vp.vp_linear_entropy_fwd(dev[0], dev[1])
+    dh, dW = vp.vp_linear_entropy_bwd(dev[0], dev[1], st, dev[4])
+    kl, sa, sb = vp.vp_linear_kl_fwd(*dev[:4])
+    torch.cuda.synchronize()
+    ha64, Wa64, hb64, Wb64 = (parity.to64(t) for t in (ha, Wa, hb, Wb))
+    parity.check_out(H, oracle.linear_entropy_fwd(ha64, Wa64)[0], "NaN row: H")
+    parity.check_out(kl, oracle.linear_kl_fwd(ha64, Wa64, hb64, Wb64)[0], "NaN row: KL")
+    assert torch.isnan(H[7]) and torch.isnan(kl[7]) and torch.isfinite(H[:7]).all() and torch.isfinite(kl[8:]).all()
+    assert torch.isnan(dh[7]).all() and torch.isfinite(dh[8]).all() and torch.isnan(dW).all()
