@@ -48,7 +48,7 @@ struct LinearBars {
 // holds K-consecutive elements; one box of 64 x rows per stage) or MN-major
 // (true: the map's rows run along K and hold MN-consecutive elements; 64 x 64
 // boxes, 8 KB apart in shared memory), so that a transposed operand is read in
-// place. Tiles run N-major (consecutive CTAs share one B tile through L2).
+// place. Tiles run in m-groups (tile_coords) with L2 eviction hints per operand.
 // Dual form (kDual, K-major operands only): each tile also computes a second
 // product C2 = A2 . B2^T (K2 deep) of the same shape into the other 256 TMEM
 // columns, so that an epilogue sees the same logits tile of two models at

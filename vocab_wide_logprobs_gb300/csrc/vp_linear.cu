@@ -10,19 +10,20 @@
 //   [P1] page "Add Triton kernels for vocab-parallel logprobs, entropy and KL",
 //        second commit message (partials re-centred on the max).
 //
-// Kernel 1 (umma_gemm_kernel<LseEpi>), a persistent grid of one CTA per SM:
-//   tiles of 128 hidden rows x 256 vocabulary rows of W, K = D in steps of 64;
-//   warp 0 (one thread) streams the bf16 operand tiles with 2-D TMA into a
-//   4-stage ring (48 KB per stage, 128-byte swizzle); warp 1 (one thread)
-//   issues tcgen05.mma (M = 128, N = 256, K = 16 per instruction) into one of
-//   two 256-column fp32 accumulators in TMEM and commits each stage back to
-//   the producer; warps 2-5 read a finished accumulator with tcgen05.ld (one
-//   thread per row), take the tile's per-row max m and sum-exp S in fp32,
-//   pick out the target logit when the target falls in the tile, and hand the
-//   accumulator back. The logits exist only in TMEM and registers.
-//   Tiles run vocabulary-major, so the CTAs working at the same time share one
-//   2 MB slice of W through L2 while the hidden states (here 64 MB) stay
-//   resident in L2.
+// Kernel 1 (umma_gemm_pair_kernel<LseEpi>, vp_gemm.cuh), a persistent grid of
+//   CTA pairs: tiles of 256 hidden rows x 256 vocabulary rows of W, K = D in
+//   steps of 64. Each CTA of a pair holds 128 rows of the hidden tile, 128 rows
+//   of the W tile and its 128 rows of the accumulators; its TMA thread streams
+//   the bf16 operand tiles into a 6-stage ring (32 KB per stage, 128-byte
+//   swizzle); one thread of the leader issues tcgen05.mma.cta_group::2
+//   (M = 256, N = 256, K = 16) into one of two 256-column fp32 accumulators in
+//   TMEM. The epilogue warps read a finished accumulator with tcgen05.ld (one
+//   thread per row), take the tile's per-row max m and sum-exp S in fp32, pick
+//   out the target logit when the target falls in the tile, and hand the
+//   accumulator back. The logits exist only in TMEM and registers. Tiles run
+//   in groups of about 32 MB of hidden rows, with the hidden tiles marked
+//   evict_last and the W tiles evict_first in L2, so that W is read from DRAM
+//   about once per group while the group's hidden rows stay in L2.
 // Kernel 2 (linear_merge_kernel): one warp per row re-centres the row's
 //   per-tile (m, S) on their max (fp32 exponentials, double-float sums), in a
 //   fixed order, and writes logp and the vp_rowstat record (fp64 finish).
