@@ -55,9 +55,10 @@ struct LinearBars {
 // once; the two accumulators fill TMEM, so there is one accumulator set and
 // the epilogue of a tile does not overlap the MMAs of the next (the producer
 // still fills the ring meanwhile).
-// The epilogue functor is called by each of the 128 epilogue threads for its
-// accumulator row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the
-// row's 256 columns; it reads them with tmem_ld32, which is warp-collective, so
+// The epilogue functor is called by each epilogue thread for its accumulator
+// row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the row's 256
+// columns (in the dual form, of one 128-column half, the second product's at
+// taddr + 256); it reads them with tmem_ld32, which is warp-collective, so
 // every lane runs every load (rows past M included) and only the global
 // accesses are guarded.
 // ---------------------------------------------------------------------------
