@@ -174,3 +174,11 @@ def test_linear_jsd_entry_points_check_beta_first():
     assert lib.vp_linear_jsd_bwd(*two, 0.5, FAKE, FAKE, FAKE, None, None, None, None, FAKE, ws, None) == ERR_ARG
     assert lib.vp_linear_jsd_fwd(*two, 0.5, FAKE_ODD, FAKE, FAKE, FAKE, ws, None) == ERR_ALIGN
     assert lib.vp_linear_jsd_workspace_size(4, 16) == lib.vp_linear_kl_workspace_size(4, 16)
+
+
+def test_binding_wraps_every_entry_point():
+    import vocab_wide_logprobs_gb300 as vp
+    missing = [n for n in declared_functions() if not hasattr(vp, n)]
+    assert not missing, missing
+    assert vp.vp_version() >= 1 and vp.vp_status_string(ERR_ARG) == "invalid argument"
+    assert vp.vp_linear_kl_workspace_size(4, 16) == vp.vp_linear_jsd_workspace_size(4, 16) > 0

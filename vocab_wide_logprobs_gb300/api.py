@@ -318,6 +318,38 @@ def _workspace(nbytes, like):
     return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=like.device)
 
 
+def vp_linear_entropy_workspace_size(N: int, V: int, D: int) -> int:
+    return int(_lib.lib().vp_linear_entropy_workspace_size(N, V, D))
+
+
+def vp_linear_entropy_bwd_workspace_size(N: int, V: int, D: int) -> int:
+    return int(_lib.lib().vp_linear_entropy_bwd_workspace_size(N, V, D))
+
+
+def vp_linear_kl_workspace_size(N: int, V: int) -> int:
+    return int(_lib.lib().vp_linear_kl_workspace_size(N, V))
+
+
+def vp_linear_kl_bwd_workspace_size(N: int, V: int, Da: int, Db: int) -> int:
+    return int(_lib.lib().vp_linear_kl_bwd_workspace_size(N, V, Da, Db))
+
+
+def vp_linear_jsd_workspace_size(N: int, V: int) -> int:
+    return int(_lib.lib().vp_linear_jsd_workspace_size(N, V))
+
+
+def vp_linear_jsd_bwd_workspace_size(N: int, V: int, Da: int, Db: int) -> int:
+    return int(_lib.lib().vp_linear_jsd_bwd_workspace_size(N, V, Da, Db))
+
+
+def vp_status_string(status: int) -> str:
+    return _lib.status_string(status)
+
+
+def vp_version() -> int:
+    return int(_lib.lib().vp_version())
+
+
 def vp_linear_entropy_fwd(hidden, weight, H=None, stats=None, workspace=None):
     """Entropy of softmax(hidden @ weight^T) per row; returns (H fp32 [N], stats)."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_fwd")
