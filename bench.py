@@ -453,6 +453,7 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
     is cut into `chunks` row blocks: block k's host-to-device copy runs on a copy
     stream while the calls of block k - 1 run on the compute stream."""
     import torch
+    import vocab_wide_logprobs_gb300 as vp
     N = a.shape[0]
     # pinned host buffers on the GPU's own NUMA node (first touch under a CPU
     # affinity local to the GPU); a buffer on the far node halves the copy rate
@@ -482,14 +483,14 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
             with torch.cuda.stream(copy):
                 copy.wait_event(read[k])            # the previous step is done with these rows
                 for dst, src in ((a, h_a), (b, h_b), (t, h_t), (g, h_g)):
-                    dst[sl].copy_(src[sl], non_blocking=True)
+                    vp.vp_upload(dst[sl], src[sl])
                 landed[k].record(copy)
             stream.wait_event(landed[k])
             for name in ops:
                 calls[k][name]()
             read[k].record(stream)
             for i, key in enumerate(("lp", "H", "kl", "kl2")):
-                h_out[i, sl].copy_(st[key][sl], non_blocking=True)
+                vp.vp_download(h_out[i, sl], st[key][sl])
 
     e2e_step()
     torch.cuda.synchronize()
@@ -513,7 +514,7 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
         e2e_ms = float(tt.item())
     return {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": f"{chunks} row blocks; host-to-device copies on a copy stream overlap the calls",
+            "pipeline": f"{chunks} row blocks; host-to-device copies (vp_upload) on a copy stream overlap the calls",
             "h2d_link_gbs": round(h2d_gbs, 1), "host_buffers_numa_local": bool(numa)}
 
 

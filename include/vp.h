@@ -542,6 +542,15 @@ VP_API vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *h
 /* Misc                                                                      */
 /* ------------------------------------------------------------------------ */
 
+/* Host-buffer transfers (no counterpart on the pages: they let a caller whose
+ * data starts in host memory run a whole step through this library). One
+ * cudaMemcpyAsync of `bytes` bytes on `stream`, host to device (vp_upload) or
+ * device to host (vp_download). The host buffer should be page-locked, or the
+ * copy is not asynchronous. bytes = 0 queues nothing; NULL pointers otherwise:
+ * VP_ERR_NULL; a failed enqueue: VP_ERR_LAUNCH. */
+VP_API vp_status vp_upload(void *dst_device, const void *src_host, size_t bytes, vp_stream stream);
+VP_API vp_status vp_download(void *dst_host, const void *src_device, size_t bytes, vp_stream stream);
+
 /* Reads the library's device fault word of the current device into *value
  * and, when `clear` is non-zero, resets it. The word is non-zero only if a
  * kernel's bounded wait on its copy pipeline gave up (bits 0-1: the forward

@@ -182,3 +182,10 @@ def test_binding_wraps_every_entry_point():
     assert not missing, missing
     assert vp.vp_version() >= 1 and vp.vp_status_string(ERR_ARG) == "invalid argument"
     assert vp.vp_linear_kl_workspace_size(4, 16) == vp.vp_linear_jsd_workspace_size(4, 16) > 0
+
+
+def test_host_transfers_check_arguments_on_the_host():
+    lib = _lib.lib()
+    assert lib.vp_upload(None, FAKE, ctypes.c_size_t(16), None) == ERR_NULL
+    assert lib.vp_download(FAKE, None, ctypes.c_size_t(16), None) == ERR_NULL
+    assert lib.vp_upload(None, None, ctypes.c_size_t(0), None) == OK        # nothing to copy

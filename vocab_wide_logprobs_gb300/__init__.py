@@ -16,7 +16,7 @@ from .api import (KL_FORWARD, KL_REVERSE, PART_HAS_TARGET, PART_IGNORED, PART_MI
                  vp_linear_kl_fwd, vp_linear_kl_workspace_size, vp_linear_logp_bwd, vp_linear_logp_bwd_workspace_size,
                  vp_linear_logp_fwd, vp_linear_logp_fwd_noalloc, vp_linear_logp_workspace_size, vp_logprobs_bwd,
                  vp_logprobs_fwd, vp_logprobs_merge, vp_logprobs_partial, vp_logprobs_topk_bwd, vp_logprobs_topk_fwd,
-                 vp_status_string, vp_version)
+                 vp_status_string, vp_upload, vp_download, vp_version)
 
 __all__ = ["KL_FORWARD", "KL_REVERSE", "PART_HAS_TARGET", "PART_IGNORED", "PART_MISMATCH", "PART_NANINF",
            "PART_NANINF_B", "ROW_BADTARGET", "ROW_EMPTY", "ROW_MISMATCH", "ROW_NANINF", "ROW_SHARDED", "VPError",
@@ -29,4 +29,4 @@ __all__ = ["KL_FORWARD", "KL_REVERSE", "PART_HAS_TARGET", "PART_IGNORED", "PART_
            "vp_linear_kl_workspace_size", "vp_linear_logp_bwd", "vp_linear_logp_bwd_workspace_size",
            "vp_linear_logp_fwd", "vp_linear_logp_fwd_noalloc", "vp_linear_logp_workspace_size", "vp_logprobs_bwd",
            "vp_logprobs_fwd", "vp_logprobs_merge", "vp_logprobs_partial", "vp_logprobs_topk_bwd",
-           "vp_logprobs_topk_fwd", "vp_status_string", "vp_version"]
+           "vp_logprobs_topk_fwd", "vp_status_string", "vp_upload", "vp_download", "vp_version"]

@@ -36,6 +36,8 @@ SIGNATURES = {
     "vp_linear_jsd_fwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, ctypes.c_size_t, P],
     "vp_linear_jsd_bwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P, P, P, ctypes.c_size_t,
                           P],
+    "vp_upload": [P, P, ctypes.c_size_t, P],
+    "vp_download": [P, P, ctypes.c_size_t, P],
     "vp_jsd_fwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P],
     "vp_jsd_bwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P],
     "vp_logprobs_partial": [P, I32, I64, I64, I64, I64, I64, I64, P, P, P],

@@ -342,6 +342,27 @@ def vp_linear_jsd_bwd_workspace_size(N: int, V: int, Da: int, Db: int) -> int:
     return int(_lib.lib().vp_linear_jsd_bwd_workspace_size(N, V, Da, Db))
 
 
+def _same_bytes(dst, src):
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise VPError(4, "host-buffer transfers take contiguous tensors")
+    n = dst.numel() * dst.element_size()
+    if n != src.numel() * src.element_size():
+        raise VPError(2, "source and destination sizes differ")
+    return n
+
+
+def vp_upload(dst, src):
+    """Copy a (page-locked) host tensor into a device tensor of the same size, on the current stream."""
+    _check(_lib.lib().vp_upload(_ptr(dst), _ptr(src), _same_bytes(dst, src), _stream()), "vp_upload")
+    return dst
+
+
+def vp_download(dst, src):
+    """Copy a device tensor into a (page-locked) host tensor of the same size, on the current stream."""
+    _check(_lib.lib().vp_download(_ptr(dst), _ptr(src), _same_bytes(dst, src), _stream()), "vp_download")
+    return dst
+
+
 def vp_status_string(status: int) -> str:
     return _lib.status_string(status)
 

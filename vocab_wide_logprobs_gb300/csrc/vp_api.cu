@@ -555,6 +555,22 @@ vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *hb, cons
     return launched(vp::launch_linear_jsd_bwd(a));
 }
 
+static vp_status copy_async(void *dst, const void *src, size_t bytes, cudaMemcpyKind kind, vp_stream stream) {
+    if (bytes == 0) return VP_OK;
+    if (!dst || !src) return VP_ERR_NULL;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    return cudaMemcpyAsync(dst, src, bytes, kind, (cudaStream_t)stream) == cudaSuccess ? VP_OK : VP_ERR_LAUNCH;
+}
+
+vp_status vp_upload(void *dst_device, const void *src_host, size_t bytes, vp_stream stream) {
+    return copy_async(dst_device, src_host, bytes, cudaMemcpyHostToDevice, stream);
+}
+
+vp_status vp_download(void *dst_host, const void *src_device, size_t bytes, vp_stream stream) {
+    return copy_async(dst_host, src_device, bytes, cudaMemcpyDeviceToHost, stream);
+}
+
 vp_status vp_fault_status(uint32_t *value, int clear) {
     if (!value) return VP_ERR_NULL;
     vp_status st = check_device();
