@@ -25,12 +25,8 @@ constexpr int kLBStage = kLBN * kLBK * 2;          // 32 KB
 constexpr int kLStageBytes = kLAStage + kLBStage;  // 48 KB
 constexpr int kLSmemBytes = kLStages * kLStageBytes + 1024;  // + alignment slack
 constexpr int kLThreads = 192;                     // TMA warp, MMA warp, 4 epilogue warps
-// The dual form has 8 epilogue warps: two per TMEM lane quarter, each taking
-// one 128-column half of the accumulators, so that the epilogue (which the
-// single accumulator set does not overlap with the next tile's MMAs) has half
-// the work per warp and twice the warps to hide its latencies.
+// Columns per epilogue thread in the dual form (one half of a 256-column tile).
 constexpr int kDualEpiCols = 128;
-__host__ __device__ constexpr int gemm_threads(bool dual) { return dual ? 64 + 8 * 32 : kLThreads; }
 constexpr uint32_t kLTmemCols = 2 * kLBN;          // two accumulators
 
 // Set when a bounded wait of the linear kernels gave up.
@@ -49,18 +45,10 @@ struct LinearBars {
 // (true: the map's rows run along K and hold MN-consecutive elements; 64 x 64
 // boxes, 8 KB apart in shared memory), so that a transposed operand is read in
 // place. Tiles run in m-groups (tile_coords) with L2 eviction hints per operand.
-// Dual form (kDual, K-major operands only): each tile also computes a second
-// product C2 = A2 . B2^T (K2 deep) of the same shape into the other 256 TMEM
-// columns, so that an epilogue sees the same logits tile of two models at
-// once; the two accumulators fill TMEM, so there is one accumulator set and
-// the epilogue of a tile does not overlap the MMAs of the next (the producer
-// still fills the ring meanwhile).
 // The epilogue functor is called by each epilogue thread for its accumulator
 // row: epi(row, col0, ncol, taddr), taddr = the TMEM address of the row's 256
-// columns (in the dual form, of one 128-column half, the second product's at
-// taddr + 256); it reads them with tmem_ld32, which is warp-collective, so
-// every lane runs every load (rows past M included) and only the global
-// accesses are guarded.
+// columns. TMEM loads (tmem_ld32) are warp-collective, so every lane runs every
+// load (rows past M included) and only the global accesses are guarded.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kLMnAtomBytes = 64 * kLBK * 2;   // one 64 (MN) x 64 (K) box: 8 KB
 
@@ -79,12 +67,10 @@ __device__ __forceinline__ void tile_coords(int64_t tile, int n_mb, int n_nb, in
     nb = w / gm;
 }
 
-template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
-__global__ void __launch_bounds__(gemm_threads(kDual), 1)
-umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                 const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M, int Nn,
-                 int K, int K2, int group_m, int l2hints, const Epi epi) {
-    static_assert(!kDual || (!kAMn && !kBMn), "the dual form takes K-major operands");
+template <class Epi, bool kAMn = false, bool kBMn = false>
+__global__ void __launch_bounds__(kLThreads, 1)
+umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M, int Nn,
+                 int K, int group_m, int l2hints, const Epi epi) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ LinearBars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -92,7 +78,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     const int n_mb = (M + kLBM - 1) / kLBM, n_nb = (Nn + kLBN - 1) / kLBN;
     const int64_t n_tiles = (int64_t)n_mb * n_nb;
     const int n_k = (K + kLBK - 1) / kLBK;
-    const int n_k2 = kDual ? (K2 + kLBK - 1) / kLBK : 0;   // k-blocks of the second product
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLStages; ++s) {
@@ -101,15 +86,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars.acc_full[b], 1);
-            mbar_init(&bars.acc_empty[b], gemm_threads(kDual) - 64);   // every epilogue thread
+            mbar_init(&bars.acc_empty[b], kLThreads - 64);   // every epilogue thread
         }
         fence_mbar_init();
         prefetch_tensormap(&tm_a);
         prefetch_tensormap(&tm_b);
-        if (kDual) {
-            prefetch_tensormap(&tm_a2);
-            prefetch_tensormap(&tm_b2);
-        }
     }
     if (warp == 1) tmem_alloc(&bars.tmem_base, kLTmemCols);
     tc_fence_before();
@@ -127,16 +108,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 int mb, nb;
                 tile_coords(tile, n_mb, n_nb, group_m, mb, nb);
-                for (int kb = 0; kb < n_k + n_k2; ++kb, ++it) {
+                for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t st = it % kLStages, use = it / kLStages;
                     if (use > 0 && !mbar_wait(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
                     uint8_t *a = smem + st * kLStageBytes;
                     mbar_arrive_expect_tx(&bars.full[st], kLStageBytes);
-                    if (kDual && kb >= n_k) {                // second product
-                        tma_load_2d_hint(a, &tm_a2, (kb - n_k) * kLBK, mb * kLBM, &bars.full[st], pol_a);
-                        tma_load_2d_hint(a + kLAStage, &tm_b2, (kb - n_k) * kLBK, nb * kLBN, &bars.full[st], pol_b);
-                        continue;
-                    }
                     if (kAMn) {
 #pragma unroll
                         for (int i = 0; i < kLBM / 64; ++i)
@@ -164,16 +140,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             uint32_t it = 0, j = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++j) {
-                const uint32_t buf = kDual ? 0 : j & 1, use_b = kDual ? j : j >> 1;
+                const uint32_t buf = j & 1, use_b = j >> 1;
                 if (use_b > 0 && !mbar_wait(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                for (int kb = 0; kb < n_k + n_k2; ++kb, ++it) {
+                const uint32_t d = tmem + buf * kLBN;
+                for (int kb = 0; kb < n_k; ++kb, ++it) {
                     const uint32_t st = it % kLStages;
                     if (!mbar_wait(&bars.full[st], (it / kLStages) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const bool second = kDual && kb >= n_k;
-                    const uint32_t d = tmem + buf * kLBN + (second ? kLBN : 0);
-                    const int kb0 = second ? kb - n_k : kb;     // k-block within its product
                     const uint8_t *a = smem + st * kLStageBytes;
 #pragma unroll
                     for (int kk = 0; kk < kLBK / 16; ++kk) {
@@ -182,7 +156,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                                                  : umma_desc_sw128(a + kk * 32);
                         const uint64_t db = kBMn ? umma_desc_sw128_mn(a + kLAStage + kk * 2048, kLMnAtomBytes)
                                                  : umma_desc_sw128(a + kLAStage + kk * 32);
-                        umma_bf16(d, da, db, idesc, (kb0 | kk) != 0);
+                        umma_bf16(d, da, db, idesc, (kb | kk) != 0);
                     }
                     umma_commit(&bars.empty[st]);       // frees the stage once these MMAs are done
                 }
@@ -194,24 +168,22 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         // ---------------- epilogue ----------------
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const int r_in = q * 32 + lane;
-        const int half = kDual ? (warp - 2) >> 2 : 0;   // dual form: the warp's 128-column half
         uint32_t j = 0;
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
             int mb, nb;
             tile_coords(tile, n_mb, n_nb, group_m, mb, nb);
-            const uint32_t buf = kDual ? 0 : j & 1;
-            if (ok && !mbar_wait(&bars.acc_full[buf], (kDual ? j : j >> 1) & 1)) {
+            const uint32_t buf = j & 1;
+            if (ok && !mbar_wait(&bars.acc_full[buf], (j >> 1) & 1)) {
                 ok = false;
                 atomicOr(&g_linear_fault, 4u);
             }
             tc_fence_after();
             // tcgen05.ld is warp-collective: the whole warp calls the epilogue or
             // none of it does, and epilogues guard only their global accesses
-            const int c0 = nb * kLBN + half * kDualEpiCols;
-            const int ncol = min(kDual ? kDualEpiCols : kLBN, Nn - c0);
-            if (__all_sync(0xffffffffu, ok) && ncol > 0)
-                epi(mb * kLBM + r_in, c0, ncol, tmem + buf * kLBN + half * kDualEpiCols + ((uint32_t)(q * 32) << 16));
+            if (__all_sync(0xffffffffu, ok))
+                epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
+                    tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
             tc_fence_before();
             mbar_arrive(&bars.acc_empty[buf]);           // the MMA warp may reuse the accumulator
         }
@@ -234,6 +206,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 // epilogue warps of both CTAs read their own TMEM rows and arrive on the
 // leader's "acc_empty" barrier. Every wait is bounded; every thread of both
 // CTAs reaches the final cluster barrier.
+// The dual form (kDual) runs here too, with the dual protocol of the
+// single-CTA kernel (per-product barriers; the first product copied to
+// registers and freed at once). It has 12 warps: warp 0 TMA, warp 1 MMA, warps
+// 2-3 idle, warps 4-11 the epilogue (two per TMEM lane quarter, one 128-column
+// half each). An epilogue thread holds 128 fp32 values, so the epilogue
+// warpgroups take registers from the first: of the 168 a thread is launched
+// with, setmaxnreg leaves 56 to warpgroup 0 and gives 224 to warpgroups 1-2
+// (4 x 56 + 8 x 224 = 12 x 168).
 // ---------------------------------------------------------------------------
 constexpr int kPStages = 6;
 constexpr int kPBHalf = kLBN / 2;                       // rows of the B tile per CTA
@@ -247,10 +227,18 @@ struct PairBars {
     uint32_t tmem_base;
 };
 
-template <class Epi, bool kAMn = false, bool kBMn = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kLThreads, 1)
-umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M,
-                      int Nn, int K, int group_m, int l2hints, const Epi epi) {
+constexpr int kPairDualRegsLaunch = 168, kPairDualRegsLow = 56, kPairDualRegsHigh = 224;
+static_assert(4 * kPairDualRegsLow + 8 * kPairDualRegsHigh == 12 * kPairDualRegsLaunch,
+              "the epilogue warpgroups take exactly what warpgroup 0 gives up");
+__host__ __device__ constexpr int pair_threads(bool dual) { return dual ? 12 * 32 : kLThreads; }
+__host__ __device__ constexpr int pair_epi_first_warp(bool dual) { return dual ? 4 : 2; }
+
+template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(kDual), 1)
+umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M,
+                      int Nn, int K, int K2, int group_m, int l2hints, const Epi epi) {
+    static_assert(!kDual || (!kAMn && !kBMn), "the dual form takes K-major operands");
     extern __shared__ uint8_t smem_raw[];
     __shared__ PairBars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -259,7 +247,9 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
     const int n_mp = (M + 2 * kLBM - 1) / (2 * kLBM), n_nb = (Nn + kLBN - 1) / kLBN;
     const int64_t n_tiles = (int64_t)n_mp * n_nb;
     const int n_k = (K + kLBK - 1) / kLBK;
+    const int n_k2 = kDual ? (K2 + kLBK - 1) / kLBK : 0;   // k-blocks of the second product
     const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    constexpr int kEpiThreads = pair_threads(kDual) - 32 * pair_epi_first_warp(kDual);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
@@ -268,11 +258,15 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars.acc_full[b], 1);
-            mbar_init(&bars.acc_empty[b], 2 * 4 * 32);   // the epilogue threads of both CTAs
+            mbar_init(&bars.acc_empty[b], 2 * kEpiThreads);   // the epilogue threads of both CTAs
         }
         fence_mbar_init();
         prefetch_tensormap(&tm_a);
         prefetch_tensormap(&tm_b);
+        if (kDual) {
+            prefetch_tensormap(&tm_a2);
+            prefetch_tensormap(&tm_b2);
+        }
     }
     if (warp == 1) tmem_alloc_pair(&bars.tmem_base, kLTmemCols);
     tc_fence_before();
@@ -280,6 +274,9 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
+    if (warp < pair_epi_first_warp(kDual)) {
+    // warpgroup 0 in the dual form (TMA, MMA and two idle warps)
+    if constexpr (kDual) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPairDualRegsLow));
     if (warp == 0) {
         // ---------------- TMA producer (both CTAs) ----------------
         if (lane == 0) {
@@ -291,12 +288,17 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                 tile_coords(tile, n_mp, n_nb, group_m, mp, nb);
                 const int mb = 2 * mp + (int)rank;
                 const int nrow = nb * kLBN + (int)rank * kPBHalf;
-                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                for (int kb = 0; kb < n_k + n_k2; ++kb, ++it) {
                     const uint32_t st = it % kPStages, use = it / kPStages;
                     if (use > 0 && !mbar_wait_cluster(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
                     uint8_t *a = smem + st * kPStageBytes;
                     const uint32_t fb = cluster_addr(&bars.full[st], 0);
                     if (rank == 0) mbar_arrive_expect_tx(&bars.full[st], 2 * kPStageBytes);
+                    if (kDual && kb >= n_k) {                // second product
+                        tma_load_2d_pair(a, &tm_a2, (kb - n_k) * kLBK, mb * kLBM, fb, pol_a);
+                        tma_load_2d_pair(a + kPAStage, &tm_b2, (kb - n_k) * kLBK, nrow, fb, pol_b);
+                        continue;
+                    }
                     if (kAMn) {
 #pragma unroll
                         for (int i = 0; i < kLBM / 64; ++i)
@@ -323,50 +325,81 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
             uint32_t it = 0, j = 0;
             bool ok = true;
             for (int64_t tile = pair; tile < n_tiles && ok; tile += n_pairs, ++j) {
-                const uint32_t buf = j & 1, use_b = j >> 1;
-                if (use_b > 0 && !mbar_wait_cluster(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t d = tmem + buf * kLBN;
-                for (int kb = 0; kb < n_k; ++kb, ++it) {
-                    const uint32_t st = it % kPStages;
-                    if (!mbar_wait(&bars.full[st], (it / kPStages) & 1)) { ok = false; break; }
+                // product p of the dual form: accumulator columns p * 256 and
+                // barriers acc_full[p] / acc_empty[p]; otherwise buffer j & 1
+                for (int p = 0; p < (kDual ? 2 : 1) && ok; ++p) {
+                    const uint32_t buf = kDual ? p : j & 1, use_b = kDual ? j : j >> 1;
+                    if (use_b > 0 && !mbar_wait_cluster(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint8_t *a = smem + st * kPStageBytes;
+                    const uint32_t d = tmem + buf * kLBN;
+                    const int nkb = p ? n_k2 : n_k;
+                    for (int kb = 0; kb < nkb; ++kb, ++it) {
+                        const uint32_t st = it % kPStages;
+                        if (!mbar_wait(&bars.full[st], (it / kPStages) & 1)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint8_t *a = smem + st * kPStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kLBK / 16; ++kk) {
-                        const uint64_t da = kAMn ? umma_desc_sw128_mn(a + kk * 2048, kLMnAtomBytes)
-                                                 : umma_desc_sw128(a + kk * 32);
-                        const uint64_t db = kBMn ? umma_desc_sw128_mn(a + kPAStage + kk * 2048, kLMnAtomBytes)
-                                                 : umma_desc_sw128(a + kPAStage + kk * 32);
-                        umma_bf16_pair(d, da, db, idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < kLBK / 16; ++kk) {
+                            const uint64_t da = kAMn ? umma_desc_sw128_mn(a + kk * 2048, kLMnAtomBytes)
+                                                     : umma_desc_sw128(a + kk * 32);
+                            const uint64_t db = kBMn ? umma_desc_sw128_mn(a + kPAStage + kk * 2048, kLMnAtomBytes)
+                                                     : umma_desc_sw128(a + kPAStage + kk * 32);
+                            umma_bf16_pair(d, da, db, idesc, (kb | kk) != 0);
+                        }
+                        umma_commit_pair(&bars.empty[st]);   // frees the stage in both CTAs
                     }
-                    umma_commit_pair(&bars.empty[st]);   // frees the stage in both CTAs
+                    umma_commit_pair(&bars.acc_full[buf]);   // the accumulator (product) is complete
                 }
-                umma_commit_pair(&bars.acc_full[buf]);   // the tile's accumulators are complete
             }
             if (!ok) atomicOr(&g_linear_fault, 2u);
         }
+    }
     } else {
         // ---------------- epilogue (both CTAs) ----------------
+        if constexpr (kDual) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kPairDualRegsHigh));
         const int q = warp & 3;
         const int r_in = q * 32 + lane;
+        const int half = kDual ? (warp - 4) >> 2 : 0;   // dual form: the warp's 128-column half
+        const uint32_t lanes = (uint32_t)(q * 32) << 16;
         uint32_t j = 0;
         bool ok = true;
         for (int64_t tile = pair; tile < n_tiles; tile += n_pairs, ++j) {
             int mp, nb;
             tile_coords(tile, n_mp, n_nb, group_m, mp, nb);
             const int mb = 2 * mp + (int)rank;
-            const uint32_t buf = j & 1;
-            if (ok && !mbar_wait_cluster(&bars.acc_full[buf], (j >> 1) & 1)) {
-                ok = false;
-                atomicOr(&g_linear_fault, 4u);
+            if constexpr (kDual) {
+                const int c0 = nb * kLBN + half * kDualEpiCols;
+                const int ncol = min(kDualEpiCols, Nn - c0);
+                if (ok && !mbar_wait_cluster(&bars.acc_full[0], j & 1)) {
+                    ok = false;
+                    atomicOr(&g_linear_fault, 4u);
+                }
+                tc_fence_after();
+                const uint32_t ta = tmem + half * kDualEpiCols + lanes;
+                float x[kDualEpiCols];                   // the first product, out of TMEM
+                if (__all_sync(0xffffffffu, ok) && ncol > 0) tmem_ld128(ta, x);
+                tc_fence_before();
+                mbar_arrive_cluster(cluster_addr(&bars.acc_empty[0], 0));   // the next first product may start
+                if (ok && !mbar_wait_cluster(&bars.acc_full[1], j & 1)) {
+                    ok = false;
+                    atomicOr(&g_linear_fault, 4u);
+                }
+                tc_fence_after();
+                if (__all_sync(0xffffffffu, ok) && ncol > 0) epi(mb * kLBM + r_in, c0, ncol, x, ta + kLBN);
+                tc_fence_before();
+                mbar_arrive_cluster(cluster_addr(&bars.acc_empty[1], 0));
+            } else {
+                const uint32_t buf = j & 1;
+                if (ok && !mbar_wait_cluster(&bars.acc_full[buf], (j >> 1) & 1)) {
+                    ok = false;
+                    atomicOr(&g_linear_fault, 4u);
+                }
+                tc_fence_after();
+                if (__all_sync(0xffffffffu, ok))
+                    epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN), tmem + buf * kLBN + lanes);
+                tc_fence_before();
+                mbar_arrive_cluster(cluster_addr(&bars.acc_empty[buf], 0));
             }
-            tc_fence_after();
-            if (__all_sync(0xffffffffu, ok))
-                epi(mb * kLBM + r_in, nb * kLBN, min(kLBN, Nn - nb * kLBN),
-                    tmem + buf * kLBN + ((uint32_t)(q * 32) << 16));
-            tc_fence_before();
-            mbar_arrive_cluster(cluster_addr(&bars.acc_empty[buf], 0));
         }
     }
     tc_fence_before();
@@ -483,15 +516,14 @@ static bool make_map_mn(CUtensorMap *map, const void *ptr, int64_t rows, int64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
-static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
-                                    const CUtensorMap &tb2, int M, int Nn, int K, int K2, int group_m,
+template <class Epi, bool kAMn = false, bool kBMn = false>
+static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, int group_m,
                                     int l2hints, const Epi &epi, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi, kAMn, kBMn, kDual>,
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi, kAMn, kBMn>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(1ull << (dev & 63));
@@ -501,28 +533,30 @@ static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb
     const int64_t n_tiles = (int64_t)((M + kLBM - 1) / kLBM) * ((Nn + kLBN - 1) / kLBN);
     const unsigned grid = (unsigned)(n_tiles < sms ? n_tiles : sms);
     const int n_mb = (M + kLBM - 1) / kLBM;
-    if (group_m <= 0) {   // about 32 MB of A (both products' A tiles in the dual form) per m-group
-        const int64_t a_tile = (int64_t)kLBM * (K + (kDual ? K2 : 0)) * 2;
-        group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / a_tile);
-    }
+    if (group_m <= 0)   // about 32 MB of A per m-group
+        group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / ((int64_t)kLBM * K * 2));
     if (group_m > n_mb) group_m = n_mb;
-    umma_gemm_kernel<Epi, kAMn, kBMn, kDual><<<grid, gemm_threads(kDual), kLSmemBytes, stream>>>(ta, tb, ta2, tb2, M, Nn, K,
-                                                                                       K2, group_m, l2hints, epi);
+    umma_gemm_kernel<Epi, kAMn, kBMn><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, M, Nn, K, group_m, l2hints,
+                                                                                epi);
     return cudaGetLastError();
 }
 
 // L2 eviction priorities of the operand tiles (l2hints: A in bits 0-1, B in bits 2-3;
 // 1 = evict_first, 2 = evict_last, 0 = normal), measured on GB300 at hidden
 // [8192, 4096] x W [75968, 4096]:
-//  - logits GEMMs (forward, backward K1, dual): A = hidden rows, reused by every
+//  - logits GEMMs (forward, backward K1): A = hidden rows, reused by every
 //    vocabulary tile of the group, evict_last; B = W, streamed, evict_first.
 //    With groups of about 32 MB of A this cut the forward's DRAM reads from
 //    6.3 GB (h re-fetched for every few W tiles) to near one read of W, and
 //    its time by 16%.
+//  - the dual form: both evict_last. Two heads stream at once, and with W
+//    evict_first the pairs of a group that share a W tile missed it in L2
+//    (the KL forward took 5.79 ms with evict_first W, 5.65 ms with evict_last).
 //  - K2 (dz . W_c): both operands evict_last (each is re-read by the other's
 //    group).
 //  - K3 (dz^T . h): A = dz^T evict_last, B = h evict_first.
 constexpr int kHintLogits = 2 | (1 << 2);
+constexpr int kHintDual = 2 | (2 << 2);
 constexpr int kHintK2 = 2 | (2 << 2);
 constexpr int kHintK3 = 2 | (1 << 2);
 
@@ -530,20 +564,21 @@ constexpr int kHintK3 = 2 | (1 << 2);
 template <class Epi, bool kAMn = false, bool kBMn = false>
 static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, const Epi &epi,
                                cudaStream_t stream, int group_m = 0, int l2hints = kHintLogits) {
-    return launch_gemm_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, group_m, l2hints, epi, stream);
+    return launch_gemm_impl<Epi, kAMn, kBMn>(ta, tb, M, Nn, K, group_m, l2hints, epi, stream);
 }
 
 // CTA-pair form (umma_gemm_pair_kernel): K-major B maps need boxes of 128 rows
 // (kPBHalf); MN-major maps are the same 64 x 64 boxes as for one CTA. group_m
 // counts 256-row pair blocks; <= 0 picks about 32 MB of A per group.
-template <class Epi, bool kAMn = false, bool kBMn = false>
-static cudaError_t launch_gemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K,
-                                   const Epi &epi, cudaStream_t stream, int group_m, int l2hints) {
+template <class Epi, bool kAMn, bool kBMn, bool kDual>
+static cudaError_t launch_gemm_pair_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
+                                        const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
+                                        cudaStream_t stream, int group_m, int l2hints) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        cudaError_t e = cudaFuncSetAttribute(umma_gemm_pair_kernel<Epi, kAMn, kBMn>,
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(1ull << (dev & 63));
@@ -554,11 +589,17 @@ static cudaError_t launch_gemm_pair(const CUtensorMap &ta, const CUtensorMap &tb
     const int64_t n_tiles = (int64_t)n_mp * ((Nn + kLBN - 1) / kLBN);
     const int64_t pairs = std::max(1, sms / 2);
     const unsigned grid = (unsigned)(2 * (n_tiles < pairs ? n_tiles : pairs));
-    if (group_m <= 0) group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / ((int64_t)2 * kLBM * K * 2));
+    if (group_m <= 0)   // about 32 MB of A (both products' A tiles in the dual form) per m-group
+        group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / ((int64_t)2 * kLBM * (K + (kDual ? K2 : 0)) * 2));
     if (group_m > n_mp) group_m = n_mp;
-    umma_gemm_pair_kernel<Epi, kAMn, kBMn><<<grid, kLThreads, kPSmemBytes, stream>>>(ta, tb, M, Nn, K, group_m,
-                                                                                     l2hints, epi);
+    umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual><<<grid, pair_threads(kDual), kPSmemBytes, stream>>>(
+        ta, tb, ta2, tb2, M, Nn, K, K2, group_m, l2hints, epi);
     return cudaGetLastError();
+}
+template <class Epi, bool kAMn = false, bool kBMn = false>
+static cudaError_t launch_gemm_pair(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K,
+                                   const Epi &epi, cudaStream_t stream, int group_m, int l2hints) {
+    return launch_gemm_pair_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, epi, stream, group_m, l2hints);
 }
 
 #ifndef VP_GEMM_PAIRS
@@ -582,12 +623,13 @@ static cudaError_t launch_logits_gemm(const void *A, const void *B, int M, int N
                  : launch_gemm(ta, tb, M, Nn, K, epi, stream);
 }
 
-// Both products of the dual form: C = A . B^T (K deep) and C2 = A2 . B2^T (K2 deep).
+// Both products of the dual form, on CTA pairs: C = A . B^T (K deep) and
+// C2 = A2 . B2^T (K2 deep); the B maps have kPBHalf-row boxes.
 template <class Epi>
 static cudaError_t launch_gemm_dual(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                                     const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
                                     cudaStream_t stream) {
-    return launch_gemm_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, 0, kHintLogits, epi, stream);
+    return launch_gemm_pair_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, epi, stream, 0, kHintDual);
 }
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -26,11 +26,12 @@
 //             gradient GEMMs.
 // KL between model A (h_a . W_a^T) and model B (h_b . W_b^T), each model with
 // its own hidden size; reverse = KL(A||B), forward = KL(B||A):
-//   forward   the dual GEMM puts the same tile of both models' logits in TMEM
-//             (A in columns 0-255, B in 256-511); the epilogue (KLEpi) takes the
-//             tile's maxima of P and Q, S_P, S_Q and W = sum e^{P - m_P}
-//             ((P - m_P) - (Q - m_Q)); the merge re-centres the tiles
-//             (W_i -> alpha_i (W_i - (dP_i - dQ_i) S_P,i)) and writes
+//   forward   the dual GEMM (on CTA pairs) puts the same tile of both models'
+//             logits in TMEM, P's model first; the epilogue (KLEpi) takes P's
+//             columns into registers at once (freeing them for the next tile)
+//             and, with Q's columns, the tile's maxima of P and Q, S_P, S_Q and
+//             W = sum e^{P - m_P} ((P - m_P) - (Q - m_Q)); the merge re-centres
+//             the tiles (W_i -> alpha_i (W_i - (dP_i - dQ_i) S_P,i)) and writes
 //             KL = W / S_P - log S_P + log S_Q with both records;
 //   backward  the dual GEMM again, dP = g p ((P - m_P) - (Q - m_Q) - c) and
 //             dQ = g (q - p) in the epilogue (DzKLEpi), then the gradient GEMMs
@@ -88,35 +89,64 @@ struct KLTile {
     float mp, Sp, mq, Sq, W, pad0, pad1, pad2;
 };
 
+// Packed helpers of the dual-form full-tile paths: two columns per fp32
+// instruction (f32x2), a three-input max for the tile maxima.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float max32(float m, const float (&v)[32]) {
+    float m0 = m, m1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        m0 = max3f(m0, v[i], v[i + 1]);
+        m1 = max3f(m1, v[i + 2], v[i + 3]);
+    }
+    return fmaxf(m0, m1);
+}
+__device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 pair_at(const float (&v)[32], int i) { return make_float2(v[i], v[i + 1]); }
+__device__ __forceinline__ float2 ex2_pair(float2 x) { return make_float2(ex2_fast(x.x), ex2_fast(x.y)); }
+__device__ __forceinline__ float2 lg2_pair(float2 x) { return make_float2(lg2_fast(x.x), lg2_fast(x.y)); }
+__device__ __forceinline__ bool finite(float x) { return fabsf(x) < INFINITY; }
+
+__device__ __forceinline__ float2 pair128(const float (&v)[128], int i) { return make_float2(v[i], v[i + 1]); }
+
+// Dual-form epilogues: x holds the thread's 128 columns (one half of the
+// tile) of the first product, model A, already out of TMEM; tb is the TMEM
+// address of the same columns of the second product, model B, read here in
+// 32-column chunks.
+// KL(P||Q) with P the first product (the launcher puts the P model first).
 struct KLEpi {
     int N, n_vt;
-    bool p_is_a;      // reverse: P = A (accumulator columns 0-255), Q = B (256-511)
     KLTile *parts;    // [N][n_vt]
-    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
-        const uint32_t tp = taddr + (p_is_a ? 0u : (uint32_t)kLBN), tq = taddr + (p_is_a ? (uint32_t)kLBN : 0u);
-        float mp = -INFINITY, mq = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < kDualEpiCols / 32; ++c) {
-            float a[32], b[32];
-            tmem_ld32(tp + c * 32, a);
-            tmem_ld32(tq + c * 32, b);
+
+    // any tile: columns past ncol left out, zero-weight terms skipped
+    __device__ __forceinline__ KLTile checked(int ncol, const float (&x)[128], uint32_t tb) const {
+        float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 if (c * 32 + i < ncol) {
-                    mp = fmaxf(mp, a[i]);
-                    mq = fmaxf(mq, b[i]);
+                    ma = fmaxf(ma, x[c * 32 + i]);
+                    mb = fmaxf(mb, b[i]);
                 }
         }
+        const float mp = ma, mq = mb;
         float sp = 0.f, sq = 0.f, w = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < kDualEpiCols / 32; ++c) {
-            float a[32], b[32];
-            tmem_ld32(tp + c * 32, a);
-            tmem_ld32(tq + c * 32, b);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const bool in = c * 32 + i < ncol;
-                const float tP = a[i] - mp, tQ = b[i] - mq;
+                const float vp = x[c * 32 + i], vq = b[i];
+                const float tP = vp - mp, tQ = vq - mq;
                 const float ep = in ? ex2_fast(tP * kLog2e) : 0.f;
                 const float eq = in ? ex2_fast(tQ * kLog2e) : 0.f;
                 sp += ep;
@@ -124,8 +154,62 @@ struct KLEpi {
                 w = ep == 0.f ? w : fmaf(ep, tP - tQ, w);
             }
         }
+        return KLTile{mp, sp, mq, sq, w, 0.f, 0.f, 0.f};
+    }
+
+    // a full tile, two columns per instruction and no per-column tests: a zero
+    // weight times an infinite (tP - tQ) makes W NaN, and such a tile is redone
+    // by checked()
+    __device__ __forceinline__ KLTile full(const float (&x)[128], uint32_t tb) const {
+        float ma0 = -INFINITY, ma1 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; i += 4) {
+            ma0 = max3f(ma0, x[i], x[i + 1]);
+            ma1 = max3f(ma1, x[i + 2], x[i + 3]);
+        }
+        const float ma = fmaxf(ma0, ma1);
+        float mb = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
+            mb = max32(mb, b);
+        }
+        const float2 nma = splat(-ma), nmb = splat(-mb), l2e = splat(kLog2e), m1 = splat(-1.f);
+        float2 sa[2] = {splat(0.f), splat(0.f)}, sb[2] = {splat(0.f), splat(0.f)}, w[2] = {splat(0.f), splat(0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int k = (i >> 1) & 1;
+                const float2 tA = __fadd2_rn(pair128(x, c * 32 + i), nma), tB = __fadd2_rn(pair_at(b, i), nmb);
+                const float2 eA = ex2_pair(__fmul2_rn(tA, l2e)), eB = ex2_pair(__fmul2_rn(tB, l2e));
+                sa[k] = __fadd2_rn(sa[k], eA);
+                sb[k] = __fadd2_rn(sb[k], eB);
+                w[k] = __ffma2_rn(eA, __ffma2_rn(tB, m1, tA), w[k]);   // e_P (tP - tQ)
+            }
+        }
+        const float2 a2 = __fadd2_rn(sa[0], sa[1]), b2 = __fadd2_rn(sb[0], sb[1]), w2 = __fadd2_rn(w[0], w[1]);
+        const float SA = a2.x + a2.y, SB = b2.x + b2.y, W = w2.x + w2.y;
+        return KLTile{ma, SA, mb, SB, W, 0.f, 0.f, 0.f};
+    }
+
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, const float (&x)[128], uint32_t tb) const {
+        KLTile t;
+        if (ncol == kDualEpiCols) {                 // warp-uniform: the tile's columns
+            t = full(x, tb);
+            const bool redo = !finite(t.W);
+            if (__any_sync(0xffffffffu, redo)) {    // TMEM loads are warp-collective
+                const KLTile u = checked(ncol, x, tb);
+                if (redo) t = u;
+            }
+        } else {
+            t = checked(ncol, x, tb);
+        }
         if (row >= N) return;
-        parts[(int64_t)row * n_vt + col0 / kDualEpiCols] = KLTile{mp, sp, mq, sq, w, 0.f, 0.f, 0.f};
+        parts[(int64_t)row * n_vt + col0 / kDualEpiCols] = t;
     }
 };
 
@@ -279,41 +363,86 @@ struct DzEntEpi {
 
 // KL(P||Q): dP = g p ((tP - tQ) - c), dQ = g (q - p), tX = X - m_X, c from P's
 // record; written to the dz of A and / or B (either may be null) by direction.
+// 8 consecutive gradient values as bf16 (round to nearest even), one 16-byte store.
+__device__ __forceinline__ void store_dz8(__nv_bfloat16 *dst, const float (&d)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(d[2 * k], d[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// KL(P||Q) with P the first product (the launcher puts the P model first);
+// dzp, dzq: the dz of P and of Q, either may be null.
 struct DzKLEpi {
     int N, ldz;
-    bool p_is_a;
     const RowStat *sp, *sq;
     const float *g;
-    __nv_bfloat16 *dza, *dzb;
-    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+    __nv_bfloat16 *dzp, *dzq;
+
+    // columns j0 .. j0 + 7 of the half tile (x[j0 + u], b[i0 + u]) with the
+    // per-column tests: columns past ncol give 0, zero-weight terms give 0,
+    // NaN rows give NaN
+    __device__ __forceinline__ void checked(int j0, int i0, int ncol, bool nan, float gr, const RowStat &P,
+                                            const RowStat &Q, const float (&x)[128], const float (&b)[32],
+                                            float (&oa)[8], float (&ob)[8]) const {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float vp = x[j0 + u], vq = b[i0 + u];
+            const float tP = vp - P.m, tQ = vq - Q.m;
+            const float p = ex2_fast((tP - P.logS_hi) * kLog2e);
+            const float q = ex2_fast((tQ - Q.logS_hi) * kLog2e);
+            float dP = p == 0.f ? 0.f : gr * p * (((tP - tQ) - P.c_hi) - P.c_lo);
+            float dQ = gr * (q - p);
+            if (j0 + u >= ncol) dP = dQ = 0.f;
+            else if (nan) dP = dQ = qnan();
+            oa[u] = dP;
+            ob[u] = dQ;
+        }
+    }
+
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, const float (&x)[128], uint32_t tb) const {
         const bool valid = row < N;
         const int r = valid ? row : 0;
         const RowStat P = load_rowstat(sp + r), Q = load_rowstat(sq + r);
         const bool nan = ((P.flags & (kRowNanInf | kRowEmpty)) | (Q.flags & kRowNanInf)) != 0;
         const float gr = valid ? g[row] : 0.f;
-        const uint32_t tp = taddr + (p_is_a ? 0u : (uint32_t)kLBN), tq = taddr + (p_is_a ? (uint32_t)kLBN : 0u);
-        __nv_bfloat16 *dzp = p_is_a ? dza : dzb, *dzq = p_is_a ? dzb : dza;
-#pragma unroll 1
-        for (int c = 0; c < kDualEpiCols / 32; ++c) {
-            float a[32], b[32];
-            tmem_ld32(tp + c * 32, a);
-            tmem_ld32(tq + c * 32, b);
+        const bool full = ncol == kDualEpiCols;
+        const float2 nPm = splat(-P.m), nQm = splat(-Q.m), l2e = splat(kLog2e), m1 = splat(-1.f);
+        const float2 nCp = splat(-P.logS_hi * kLog2e), nCq = splat(-Q.logS_hi * kLog2e);
+        const float2 nch = splat(-P.c_hi), ncl = splat(-P.c_lo), g2 = splat(gr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float tP = a[i] - P.m, tQ = b[i] - Q.m;
-                const float p = ex2_fast((tP - P.logS_hi) * kLog2e);
-                const float q = ex2_fast((tQ - Q.logS_hi) * kLog2e);
-                float dP = p == 0.f ? 0.f : gr * p * (((tP - tQ) - P.c_hi) - P.c_lo);
-                float dQ = gr * (q - p);
-                if (c * 32 + i >= ncol) dP = dQ = 0.f;
-                else if (nan) dP = dQ = qnan();
-                a[i] = dP;
-                b[i] = dQ;
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+                const int i0 = gq * 8, j0 = c * 32 + i0;
+                // two columns per instruction, no per-column tests; a zero p
+                // times an infinite (tP - tQ - c) leaves the group's sum
+                // non-finite, and such a group is redone with the tests
+                float oa[8], ob[8];
+                float2 chk = splat(0.f);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    const float2 tP = __fadd2_rn(pair128(x, j0 + u), nPm), tQ = __fadd2_rn(pair_at(b, i0 + u), nQm);
+                    const float2 p = ex2_pair(__ffma2_rn(tP, l2e, nCp)), q = ex2_pair(__ffma2_rn(tQ, l2e, nCq));
+                    const float2 d = __fadd2_rn(__fadd2_rn(__ffma2_rn(tQ, m1, tP), nch), ncl);
+                    chk = __fadd2_rn(chk, d);
+                    const float2 dP = __fmul2_rn(__fmul2_rn(g2, p), d), dQ = __fmul2_rn(g2, __ffma2_rn(p, m1, q));
+                    oa[u] = dP.x;
+                    oa[u + 1] = dP.y;
+                    ob[u] = dQ.x;
+                    ob[u + 1] = dQ.y;
+                }
+                if (!full || nan || !finite(chk.x + chk.y)) checked(j0, i0, ncol, nan, gr, P, Q, x, b, oa, ob);
+                if (!valid) continue;
+                const int64_t off = (int64_t)row * ldz + col0 + j0;
+                if (dzp) store_dz8(dzp + off, oa);
+                if (dzq) store_dz8(dzq + off, ob);
             }
-            if (!valid) continue;
-            const int64_t off = (int64_t)row * ldz + col0 + c * 32;
-            if (dzp) store_dz32(dzp + off, a);
-            if (dzq) store_dz32(dzq + off, b);
         }
     }
 };
@@ -372,15 +501,16 @@ size_t linear_kl_workspace_bytes(int64_t N, int64_t V) { return up256((size_t)N 
 
 cudaError_t launch_linear_kl_fwd(const LinearKLArgs &a) {
     CUtensorMap tm_ha, tm_wa, tm_hb, tm_wb;
-    if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kLBN) ||
-        !make_map(&tm_hb, a.hb, a.N, a.Db, a.Db, kLBM) || !make_map(&tm_wb, a.wb, a.V, a.Db, a.Db, kLBN))
+    if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kPBHalf) ||
+        !make_map(&tm_hb, a.hb, a.N, a.Db, a.Db, kLBM) || !make_map(&tm_wb, a.wb, a.V, a.Db, a.Db, kPBHalf))
         return cudaErrorInvalidValue;
     const int n_vt = (int)n_dual_tiles(a.V);
     const bool p_is_a = a.direction == 0;
     KLTile *parts = static_cast<KLTile *>(a.workspace);
-    const KLEpi epi{(int)a.N, n_vt, p_is_a, parts};
-    cudaError_t e = launch_gemm_dual(tm_ha, tm_wa, tm_hb, tm_wb, (int)a.N, (int)a.V, (int)a.Da, (int)a.Db, epi,
-                                     a.stream);
+    // P first: the forward direction, KL(B||A), runs the dual GEMM with model B first
+    const int N = (int)a.N, V = (int)a.V, Da = (int)a.Da, Db = (int)a.Db;
+    cudaError_t e = p_is_a ? launch_gemm_dual(tm_ha, tm_wa, tm_hb, tm_wb, N, V, Da, Db, KLEpi{N, n_vt, parts}, a.stream)
+                           : launch_gemm_dual(tm_hb, tm_wb, tm_ha, tm_wa, N, V, Db, Da, KLEpi{N, n_vt, parts}, a.stream);
     if (e != cudaSuccess) return e;
     RowStat *sa = static_cast<RowStat *>(a.stats_a), *sb = static_cast<RowStat *>(a.stats_b);
     linear_kl_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>((int)a.N, n_vt, parts, a.kl,
@@ -397,8 +527,10 @@ size_t linear_kl_bwd_workspace_bytes(int64_t N, int64_t V, int64_t Da, int64_t D
 // Backward of a two-model op: per vocabulary chunk, the dual GEMM recomputes
 // both logits tiles and the epilogue made by make_epi(dza, dzb) writes dz of A
 // and / or B; then the gradient GEMMs of each model whose gradients are asked for.
+// b_first: the dual GEMM takes model B as its first product; make_epi(ldz,
+// dz of the first product, dz of the second) builds the epilogue.
 template <class MakeEpi>
-static cudaError_t two_model_bwd(const LinearKLArgs &a, MakeEpi make_epi) {
+static cudaError_t two_model_bwd(const LinearKLArgs &a, bool b_first, MakeEpi make_epi) {
     const int64_t vc = chunk_cols(a.N, a.V);
     const size_t dz_bytes = up256((size_t)a.N * vc * 2);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
@@ -418,10 +550,12 @@ static cudaError_t two_model_bwd(const LinearKLArgs &a, MakeEpi make_epi) {
     for (int64_t v0 = 0; v0 < V; v0 += vc) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
         CUtensorMap tm_wac, tm_wbc;
-        if (!make_map(&tm_wac, Wa + v0 * Da, nv, Da, Da, kLBN) || !make_map(&tm_wbc, Wb + v0 * Db, nv, Db, Db, kLBN))
+        if (!make_map(&tm_wac, Wa + v0 * Da, nv, Da, Da, kPBHalf) ||
+            !make_map(&tm_wbc, Wb + v0 * Db, nv, Db, Db, kPBHalf))
             return cudaErrorInvalidValue;
-        const auto de = make_epi((int)vc, dza, dzb);
-        if ((e = launch_gemm_dual(tm_ha, tm_wac, tm_hb, tm_wbc, N, nv, Da, Db, de, a.stream)) != cudaSuccess) return e;
+        e = b_first ? launch_gemm_dual(tm_hb, tm_wbc, tm_ha, tm_wac, N, nv, Db, Da, make_epi((int)vc, dzb, dza), a.stream)
+                    : launch_gemm_dual(tm_ha, tm_wac, tm_hb, tm_wbc, N, nv, Da, Db, make_epi((int)vc, dza, dzb), a.stream);
+        if (e != cudaSuccess) return e;
         if (want_a && (e = chunk_gradient_gemms(tm_ha_mn, Wa, N, Da, v0, nv, vc, dza, acc_a,
                                                 static_cast<__nv_bfloat16 *>(a.dwa), a.stream)) != cudaSuccess)
             return e;
@@ -439,8 +573,9 @@ static cudaError_t two_model_bwd(const LinearKLArgs &a, MakeEpi make_epi) {
 cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
     const bool p_is_a = a.direction == 0;
     const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
-    return two_model_bwd(a, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb) {
-        return DzKLEpi{(int)a.N, ldz, p_is_a, p_is_a ? sa : sb, p_is_a ? sb : sa, a.g, dza, dzb};
+    // P first: the forward direction, KL(B||A), runs the dual GEMM with model B first
+    return two_model_bwd(a, !p_is_a, [&](int ldz, __nv_bfloat16 *dzp, __nv_bfloat16 *dzq) {
+        return DzKLEpi{(int)a.N, ldz, p_is_a ? sa : sb, p_is_a ? sb : sa, a.g, dzp, dzq};
     });
 }
 
@@ -469,30 +604,77 @@ struct JsdEpi {
     float beta;
     const RowStat *sa, *sb;   // records of pass 1
     JsdTile *parts;           // [N][n_vt]
-    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
-        const bool valid = row < N;
-        const int r = valid ? row : 0;
-        const RowStat A = load_rowstat(sa + r), B = load_rowstat(sb + r);
+
+    // any tile: columns past ncol left out, zero-weight terms skipped, log2 mix
+    // kept above -250
+    __device__ __forceinline__ JsdTile checked(int ncol, const RowStat &A, const RowStat &B, const float (&x)[128],
+                                               uint32_t tb) const {
         const float omb = 1.f - beta;
         float kp = 0.f, kq = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < kDualEpiCols / 32; ++c) {
-            float a[32], b[32];
-            tmem_ld32(taddr + c * 32, a);
-            tmem_ld32(taddr + kLBN + c * 32, b);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 if (c * 32 + i >= ncol) continue;
-                const float xa = ((a[i] - A.m) - A.logS_hi) * kLog2e;   // log2 p
-                const float xb = ((b[i] - B.m) - B.logS_hi) * kLog2e;   // log2 q
+                const float xa = ((x[c * 32 + i] - A.m) - A.logS_hi) * kLog2e;   // log2 p
+                const float xb = ((b[i] - B.m) - B.logS_hi) * kLog2e;            // log2 q
                 const float p = ex2_fast(xa), q = ex2_fast(xb);
                 const float lm = fmaxf(lg2_fast(fmaf(beta, q, omb * p)), -250.f);
                 if (p > 0.f) kp = fmaf(p, xa - lm, kp);                  // zero-weight terms add nothing
                 if (q > 0.f) kq = fmaf(q, xb - lm, kq);
             }
         }
+        return JsdTile{kp, kq};
+    }
+
+    // a full tile, two columns per instruction: log2 p = z log2(e) - C with
+    // C = (m + log S) log2(e) rounded once; a mixture that underflows to 0 makes
+    // log2 mix = -inf and the sums non-finite, and such a tile is redone by
+    // checked()
+    __device__ __forceinline__ JsdTile full(const RowStat &A, const RowStat &B, const float (&x)[128],
+                                            uint32_t tb) const {
+        const double l2e = 1.4426950408889634074;
+        const float2 nCa = splat((float)(-((double)A.m + A.logS_hi + A.logS_lo) * l2e));
+        const float2 nCb = splat((float)(-((double)B.m + B.logS_hi + B.logS_lo) * l2e));
+        const float2 L = splat(kLog2e), bet = splat(beta), omb = splat(1.f - beta), m1 = splat(-1.f);
+        float2 kp[2] = {splat(0.f), splat(0.f)}, kq[2] = {splat(0.f), splat(0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int k = (i >> 1) & 1;
+                const float2 xa = __ffma2_rn(pair128(x, c * 32 + i), L, nCa), xb = __ffma2_rn(pair_at(b, i), L, nCb);
+                const float2 p = ex2_pair(xa), q = ex2_pair(xb);
+                const float2 lm = lg2_pair(__ffma2_rn(bet, q, __fmul2_rn(omb, p)));
+                kp[k] = __ffma2_rn(p, __ffma2_rn(lm, m1, xa), kp[k]);
+                kq[k] = __ffma2_rn(q, __ffma2_rn(lm, m1, xb), kq[k]);
+            }
+        }
+        const float2 p2 = __fadd2_rn(kp[0], kp[1]), q2 = __fadd2_rn(kq[0], kq[1]);
+        return JsdTile{p2.x + p2.y, q2.x + q2.y};
+    }
+
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, const float (&x)[128], uint32_t tb) const {
+        const bool valid = row < N;
+        const int r = valid ? row : 0;
+        const RowStat A = load_rowstat(sa + r), B = load_rowstat(sb + r);
+        JsdTile t;
+        if (ncol == kDualEpiCols) {                 // warp-uniform
+            t = full(A, B, x, tb);
+            const bool redo = !finite(t.kp) || !finite(t.kq);
+            if (__any_sync(0xffffffffu, redo)) {    // TMEM loads are warp-collective
+                const JsdTile u = checked(ncol, A, B, x, tb);
+                if (redo) t = u;
+            }
+        } else {
+            t = checked(ncol, A, B, x, tb);
+        }
         if (!valid) return;
-        parts[(int64_t)row * n_vt + col0 / kDualEpiCols] = JsdTile{kp, kq};
+        parts[(int64_t)row * n_vt + col0 / kDualEpiCols] = t;
     }
 };
 
@@ -531,35 +713,76 @@ struct DzJsdEpi {
     const RowStat *sa, *sb;
     const float *g;
     __nv_bfloat16 *dza, *dzb;   // either may be null
-    __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
+
+    // columns j0 .. j0 + 7 of the half tile with the per-column tests: columns
+    // past ncol give 0, zero-weight terms give 0, log2 mix kept above -250, NaN
+    // rows give NaN
+    __device__ __forceinline__ void checked(int j0, int i0, int ncol, bool nan, float gr, const RowStat &A,
+                                            const RowStat &B, const float (&x)[128], const float (&b)[32],
+                                            float (&oa)[8], float (&ob)[8]) const {
+        const float omb = 1.f - beta;
+        const float ka = A.c_hi + A.c_lo, kb = B.c_hi + B.c_lo;   // KL(p||mix), KL(q||mix)
+        const float ln2 = 0.69314718055994530942f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float la = (x[j0 + u] - A.m) - A.logS_hi, lb = (b[i0 + u] - B.m) - B.logS_hi;   // log p, log q
+            const float p = ex2_fast(la * kLog2e), q = ex2_fast(lb * kLog2e);
+            const float lmix = fmaxf(lg2_fast(fmaf(beta, q, omb * p)), -250.f) * ln2;
+            float dA = p == 0.f ? 0.f : gr * omb * p * ((la - lmix) - ka);
+            float dB = q == 0.f ? 0.f : gr * beta * q * ((lb - lmix) - kb);
+            if (j0 + u >= ncol) dA = dB = 0.f;
+            else if (nan) dA = dB = qnan();
+            oa[u] = dA;
+            ob[u] = dB;
+        }
+    }
+
+    __device__ __forceinline__ void operator()(int row, int col0, int ncol, const float (&x)[128], uint32_t tb) const {
         const bool valid = row < N;
         const int r = valid ? row : 0;
         const RowStat A = load_rowstat(sa + r), B = load_rowstat(sb + r);
         const bool nan = ((A.flags | B.flags) & (kRowNanInf | kRowEmpty)) != 0;
-        const float gr = valid ? g[row] : 0.f, omb = 1.f - beta;
-        const float ka = A.c_hi + A.c_lo, kb = B.c_hi + B.c_lo;   // KL(p||mix), KL(q||mix)
-        const float ln2 = 0.69314718055994530942f;
-#pragma unroll 1
-        for (int c = 0; c < kDualEpiCols / 32; ++c) {
-            float a[32], b[32];
-            tmem_ld32(taddr + c * 32, a);
-            tmem_ld32(taddr + kLBN + c * 32, b);
+        const float gr = valid ? g[row] : 0.f;
+        const bool full = ncol == kDualEpiCols;
+        // log p = z - C with C = m + log S rounded once
+        const float2 nCa = splat((float)(-((double)A.m + A.logS_hi + A.logS_lo)));
+        const float2 nCb = splat((float)(-((double)B.m + B.logS_hi + B.logS_lo)));
+        const float2 L = splat(kLog2e), bet = splat(beta), omb = splat(1.f - beta), m1 = splat(-1.f);
+        const float2 ln2 = splat(0.69314718055994530942f);
+        const float2 nka = splat(-(A.c_hi + A.c_lo)), nkb = splat(-(B.c_hi + B.c_lo));
+        const float2 ga = splat(gr * (1.f - beta)), gb = splat(gr * beta);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float la = (a[i] - A.m) - A.logS_hi, lb = (b[i] - B.m) - B.logS_hi;   // log p, log q
-                const float p = ex2_fast(la * kLog2e), q = ex2_fast(lb * kLog2e);
-                const float lmix = fmaxf(lg2_fast(fmaf(beta, q, omb * p)), -250.f) * ln2;
-                float dA = p == 0.f ? 0.f : gr * omb * p * ((la - lmix) - ka);
-                float dB = q == 0.f ? 0.f : gr * beta * q * ((lb - lmix) - kb);
-                if (c * 32 + i >= ncol) dA = dB = 0.f;
-                else if (nan) dA = dB = qnan();
-                a[i] = dA;
-                b[i] = dB;
+        for (int c = 0; c < 4; ++c) {
+            float b[32];
+            tmem_ld32(tb + c * 32, b);
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+                const int i0 = gq * 8, j0 = c * 32 + i0;
+                // two columns per instruction, no per-column tests; an
+                // underflowed mixture (log mix = -inf) leaves the group's sum
+                // non-finite, and such a group is redone with the tests
+                float oa[8], ob[8];
+                float2 chk = splat(0.f);
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    const float2 la = __fadd2_rn(pair128(x, j0 + u), nCa), lb = __fadd2_rn(pair_at(b, i0 + u), nCb);
+                    const float2 p = ex2_pair(__fmul2_rn(la, L)), q = ex2_pair(__fmul2_rn(lb, L));
+                    const float2 lmix = __fmul2_rn(lg2_pair(__ffma2_rn(bet, q, __fmul2_rn(omb, p))), ln2);
+                    const float2 ua = __fadd2_rn(__ffma2_rn(lmix, m1, la), nka);
+                    const float2 ub = __fadd2_rn(__ffma2_rn(lmix, m1, lb), nkb);
+                    chk = __fadd2_rn(chk, __fadd2_rn(ua, ub));
+                    const float2 dA = __fmul2_rn(__fmul2_rn(ga, p), ua), dB = __fmul2_rn(__fmul2_rn(gb, q), ub);
+                    oa[u] = dA.x;
+                    oa[u + 1] = dA.y;
+                    ob[u] = dB.x;
+                    ob[u + 1] = dB.y;
+                }
+                if (!full || nan || !finite(chk.x + chk.y)) checked(j0, i0, ncol, nan, gr, A, B, x, b, oa, ob);
+                if (!valid) continue;
+                const int64_t off = (int64_t)row * ldz + col0 + j0;
+                if (dza) store_dz8(dza + off, oa);
+                if (dzb) store_dz8(dzb + off, ob);
             }
-            if (!valid) continue;
-            const int64_t off = (int64_t)row * ldz + col0 + c * 32;
-            if (dza) store_dz32(dza + off, a);
-            if (dzb) store_dz32(dzb + off, b);
         }
     }
 };
@@ -572,8 +795,8 @@ cudaError_t launch_linear_jsd_fwd(const LinearKLArgs &a) {
     if (e != cudaSuccess) return e;
     // pass 2: both KL-to-mixture expectations (the workspace is free again)
     CUtensorMap tm_ha, tm_wa, tm_hb, tm_wb;
-    if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kLBN) ||
-        !make_map(&tm_hb, a.hb, a.N, a.Db, a.Db, kLBM) || !make_map(&tm_wb, a.wb, a.V, a.Db, a.Db, kLBN))
+    if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kPBHalf) ||
+        !make_map(&tm_hb, a.hb, a.N, a.Db, a.Db, kLBM) || !make_map(&tm_wb, a.wb, a.V, a.Db, a.Db, kPBHalf))
         return cudaErrorInvalidValue;
     const int n_vt = (int)n_dual_tiles(a.V);
     RowStat *sa = static_cast<RowStat *>(a.stats_a), *sb = static_cast<RowStat *>(a.stats_b);
@@ -588,7 +811,7 @@ cudaError_t launch_linear_jsd_fwd(const LinearKLArgs &a) {
 
 cudaError_t launch_linear_jsd_bwd(const LinearKLArgs &a) {
     const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
-    return two_model_bwd(a, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb) {
+    return two_model_bwd(a, false, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb) {
         return DzJsdEpi{(int)a.N, ldz, a.beta, sa, sb, a.g, dza, dzb};
     });
 }

@@ -89,10 +89,10 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes
-// 32 (w % 4) .. 32 (w % 4) + 31).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
+// Issue a load of 32 consecutive fp32 columns of this thread's TMEM lane (warp
+// w reads lanes 32 (w % 4) .. 32 (w % 4) + 31); the registers hold the values
+// only after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -103,9 +103,42 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    tmem_ld32_issue(taddr, r);
+    tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 128 consecutive fp32 columns of this thread's TMEM lane, four loads behind one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+    uint32_t r[4][32];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) tmem_ld32_issue(taddr + 32 * k, r[k]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[32 * k + i] = __uint_as_float(r[k][i]);
+}
+
+// Two 32-column loads (columns ta.. of a, tb.. of b) behind one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
+    uint32_t ra[32], rb[32];
+    tmem_ld32_issue(ta, ra);
+    tmem_ld32_issue(tb, rb);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        a[i] = __uint_as_float(ra[i]);
+        b[i] = __uint_as_float(rb[i]);
+    }
 }
 
 // --- 2-D tiled TMA --------------------------------------------------------
