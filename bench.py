@@ -270,7 +270,9 @@ def run_ours(args, rank, world, local_rank):
 
     linear = None
     if not args.no_linear and rank == 0:
-        linear = linear_bench(args, dev, N=args.linear_rows)
+        with ClockSampler(local_rank) as lin_clocks:
+            linear = linear_bench(args, dev, N=args.linear_rows)
+        linear["clocks"] = lin_clocks.summary()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -354,11 +356,14 @@ def topk_bench(args, a, dev, peaks, K=20):
                                                    "bwd": round(bb / (tb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
-def _time_ms(fn, reps):
-    """Mean ms of fn over reps calls, CUDA events on the current stream, after one untimed call."""
+def _time_ms(fn, reps, idle_s=0.0):
+    """Mean ms of fn over reps calls, CUDA events on the current stream, after one untimed call
+    (and idle_s seconds of idle GPU, so that a burst is timed from the same power state)."""
     import torch
     fn()
     torch.cuda.synchronize()
+    if idle_s > 0:
+        time.sleep(idle_s)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(reps):
@@ -368,9 +373,14 @@ def _time_ms(fn, reps):
     return e0.elapsed_time(e1) / reps
 
 
+IDLE_S = 1.0   # idle seconds before each timed burst of the linear ops
+
+
 def linear_bench(args, dev, N=8192, V=75968, D=4096):
     """Fused linear ops on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16): logp, entropy and
-    KL against a second model of the same shape, forward and backward."""
+    KL against a second model of the same shape, forward and backward. Each op is timed as a burst, after
+    IDLE_S seconds of idle GPU, against the measured burst bf16 peak: a long GEMM heats the part and the
+    power cap then lowers the clock of whatever runs next."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     from vocab_wide_logprobs_gb300 import workloads
@@ -383,11 +393,11 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     for _ in range(2):
         vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws)
     reps = max(3, min(args.steps, 10))
-    ms = _time_ms(lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws), reps)
+    ms = _time_ms(lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws), reps, IDLE_S)
     dh = torch.empty_like(h)
     dW = torch.empty_like(W)
     wsb = torch.empty(vp.vp_linear_logp_bwd_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
-    ms_b = _time_ms(lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb), 3)
+    ms_b = _time_ms(lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb), 3, IDLE_S)
     del wsb
     flops = 2.0 * N * V * D
     peak = None
@@ -403,8 +413,8 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     H = torch.empty(N, dtype=torch.float32, device=dev)
     wse = torch.empty(max(vp._lib.lib().vp_linear_entropy_bwd_workspace_size(N, V, D),
                           vp._lib.lib().vp_linear_entropy_workspace_size(N, V, D)), dtype=torch.uint8, device=dev)
-    ms_ef = _time_ms(lambda: vp.vp_linear_entropy_fwd(h, W, H=H, stats=st, workspace=wse), reps)
-    ms_eb = _time_ms(lambda: vp.vp_linear_entropy_bwd(h, W, st, g, dhidden=dh, dW=dW, workspace=wse), 3)
+    ms_ef = _time_ms(lambda: vp.vp_linear_entropy_fwd(h, W, H=H, stats=st, workspace=wse), reps, IDLE_S)
+    ms_eb = _time_ms(lambda: vp.vp_linear_entropy_bwd(h, W, st, g, dhidden=dh, dW=dW, workspace=wse), 3, IDLE_S)
     del wse
     # KL(A||B) against a second model (teacher) of the same shape, gradients to both models
     tw = workloads.linear(seed=14, N=N, V=V, D=D)
@@ -415,12 +425,13 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     wsk = torch.empty(vp._lib.lib().vp_linear_kl_bwd_workspace_size(N, V, D, D), dtype=torch.uint8, device=dev)
     outs = [dh, dW, torch.empty_like(hb), torch.empty_like(Wb)]
     ms_kf = _time_ms(lambda: vp.vp_linear_kl_fwd(h, W, hb, Wb, vp.KL_REVERSE, kl=kl, stats_a=st, stats_b=sb,
-                                                 workspace=wsk), reps)
-    ms_kb = _time_ms(lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, vp.KL_REVERSE, st, sb, g, outs=outs, workspace=wsk), 3)
+                                                 workspace=wsk), reps, IDLE_S)
+    ms_kb = _time_ms(lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, vp.KL_REVERSE, st, sb, g, outs=outs, workspace=wsk), 3,
+                     IDLE_S)
     # generalized JSD (beta = 0.5) of the same two models: two forward passes of the dual GEMM
     ms_jf = _time_ms(lambda: vp.vp_linear_jsd_fwd(h, W, hb, Wb, 0.5, jsd=kl, stats_a=st, stats_b=sb, workspace=wsk),
-                     reps)
-    ms_jb = _time_ms(lambda: vp.vp_linear_jsd_bwd(h, W, hb, Wb, 0.5, st, sb, g, outs=outs, workspace=wsk), 3)
+                     reps, IDLE_S)
+    ms_jb = _time_ms(lambda: vp.vp_linear_jsd_bwd(h, W, hb, Wb, 0.5, st, sb, g, outs=outs, workspace=wsk), 3, IDLE_S)
     del wsk, outs, hb, Wb
     torch.cuda.empty_cache()
 
