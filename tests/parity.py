@@ -244,11 +244,24 @@ def compare_all(got: dict, ref: dict, rows=None, tag=""):
 # gradients), the fp32 evaluation error of dz enters as well: the elementwise
 # rule KAPPA_BF16 2^-24 M_j carried through the same dot product,
 # KAPPA_BF16 2^-24 sum M_j |operand| (eval_mag).
+# The exponentials flush a probability below the fp32 normal range (2^-126) to
+# 0, as the subnormal rule above says, so an element of dz whose p (or q) is
+# that small may be lost whole: its share M_j of the tolerance, carried through
+# the same dot product, enters unscaled (flush_mag; flushed() selects it).
 # ---------------------------------------------------------------------------
 GEMM_KAPPA = 2.0 ** -8
 
 
-def check_gemm_grad(got, ref, mag, what, eval_mag=None):
+def flushed(M, *probs, below=TINY):
+    """M_j at the elements where one of the formula's probabilities is below `below`, else 0."""
+    mask = np.zeros(np.shape(M), bool)
+    for p in probs:
+        with np.errstate(invalid="ignore"):
+            mask |= np.asarray(p) < below
+    return np.where(mask, M, 0.0)
+
+
+def check_gemm_grad(got, ref, mag, what, eval_mag=None, flush_mag=None):
     g = to64(got)
     r = rne_bf16(ref)
     _placement(g, r, what)
@@ -257,5 +270,7 @@ def check_gemm_grad(got, ref, mag, what, eval_mag=None):
     tol = ulp_bf16(r[fin]) + GEMM_KAPPA * mag[fin]
     if eval_mag is not None:
         tol = tol + KAPPA_BF16 * 2.0 ** -24 * eval_mag[fin]
+    if flush_mag is not None:
+        tol = tol + flush_mag[fin]
     assert (err <= tol).all(), f"{what}: worst err/tol {(err / tol).max():.3f}, {(err > tol).sum()} bad of {err.size}"
     return float((err / tol).max())

@@ -112,11 +112,21 @@ def _check_kl(ha, Wa, hb, Wb, g, direction, tag):
     op = "kl_rev" if direction == vp.KL_REVERSE else "kl_fwd"
     M = parity.oracle_all(za, zb, np.zeros(za.shape[0], np.int64), g64, ops=(op,))["_mag"]
     Ma, Mb = M["d" + op + "_a"], M["d" + op + "_b"]
+    pa, pb = _probs(za), _probs(zb)
+    pP = pa if direction == vp.KL_REVERSE else pb
+    Fa, Fb = parity.flushed(Ma, pP, pa, pb), parity.flushed(Mb, pP, pa, pb)
     mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
     evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
-    for got, r, mg, ev, name in zip(grads, ref, mags, evals, ("dhidden A", "dW A", "dhidden B", "dW B")):
-        parity.check_gemm_grad(got, r, mg, f"{tag} {name}", ev)
+    flush = (Fa @ np.abs(Wa64), Fa.T @ np.abs(ha64), Fb @ np.abs(Wb64), Fb.T @ np.abs(hb64))
+    for got, r, mg, ev, fl, name in zip(grads, ref, mags, evals, flush, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, mg, f"{tag} {name}", ev, fl)
     return kl, grads
+
+
+def _probs(z):
+    """softmax of fp64 logits, row by row."""
+    e = np.exp(z - z.max(1, keepdims=True))
+    return e / e.sum(1, keepdims=True)
 
 
 @pytest.mark.parametrize("direction", [vp.KL_REVERSE, vp.KL_FORWARD], ids=["reverse", "forward"])
@@ -297,3 +307,61 @@ def test_linear_ops_nan_hidden_row():
     parity.check_out(kl, oracle.linear_kl_fwd(ha64, Wa64, hb64, Wb64)[0], "NaN row: KL")
     assert torch.isnan(H[7]) and torch.isnan(kl[7]) and torch.isfinite(H[:7]).all() and torch.isfinite(kl[8:]).all()
     assert torch.isnan(dh[7]).all() and torch.isfinite(dh[8]).all() and torch.isnan(dW).all()
+
+
+def test_linear_two_model_nan_row_backward():
+    """A NaN row of model A's hidden states: NaN KL / JSD and NaN gradient rows for both models (the
+    dual epilogues' column-checked path), every other row finite."""
+    N, V, D = 130, 1000, 128
+    ha, Wa, hb, Wb, g = _kl_case(N, V, D, D, seed=63)
+    ha = ha.clone()
+    ha[9, 3] = float("nan")
+    dev = [t.to(DEV) for t in (ha, Wa, hb, Wb, g)]
+    for direction in (vp.KL_REVERSE, vp.KL_FORWARD):
+        kl, sa, sb = vp.vp_linear_kl_fwd(*dev[:4], direction)
+        dha, dwa, dhb, dwb = vp.vp_linear_kl_bwd(*dev[:4], direction, sa, sb, dev[4])
+        torch.cuda.synchronize()
+        assert torch.isnan(kl[9]) and torch.isfinite(kl[:9]).all() and torch.isfinite(kl[10:]).all()
+        for dh in (dha, dhb):
+            assert torch.isnan(dh[9]).all() and torch.isfinite(dh[:9]).all() and torch.isfinite(dh[10:]).all()
+        assert torch.isnan(dwa).all() and torch.isnan(dwb).all()
+    jsd, sa, sb = vp.vp_linear_jsd_fwd(*dev[:4], 0.5)
+    dha, dwa, dhb, dwb = vp.vp_linear_jsd_bwd(*dev[:4], 0.5, sa, sb, dev[4])
+    torch.cuda.synchronize()
+    assert torch.isnan(jsd[9]) and torch.isfinite(jsd[:9]).all() and torch.isfinite(jsd[10:]).all()
+    for dh in (dha, dhb):
+        assert torch.isnan(dh[9]).all() and torch.isfinite(dh[:9]).all() and torch.isfinite(dh[10:]).all()
+
+
+def test_linear_two_model_wide_logit_spread():
+    """Heads scaled so that the logits of a row spread over several hundred units: most p and q
+    underflow to 0, the JSD's mixture underflows where both do (log mix = -inf), and the dual
+    epilogues redo those tiles and groups with the column checks. KL and JSD, forward and
+    backward, against the oracle."""
+    N, V, Da, Db = 136, 1300, 64, 128
+    ha, Wa, g = _model(71, N, V, Da, scale=400.0)
+    hb, Wb, _ = _model(72, N, V, Db, scale=300.0)
+    ha64, Wa64, hb64, Wb64 = (parity.to64(t) for t in (ha, Wa, hb, Wb))
+    za, zb = oracle.linear_logits(ha64, Wa64), oracle.linear_logits(hb64, Wb64)
+    spread = np.minimum(za.max(1) - za.min(1), zb.max(1) - zb.min(1))
+    assert spread.min() > 200.0, "the case must push exp(z - m) below the fp32 range"
+    _check_kl(ha, Wa, hb, Wb, g, vp.KL_REVERSE, "wide spread")
+    _check_kl(ha, Wa, hb, Wb, g, vp.KL_FORWARD, "wide spread")
+    beta = 0.4
+    dev = [t.to(DEV) for t in (ha, Wa, hb, Wb, g)]
+    jsd, sa, sb = vp.vp_linear_jsd_fwd(*dev[:4], beta)
+    grads = vp.vp_linear_jsd_bwd(*dev[:4], beta, sa, sb, dev[4])
+    torch.cuda.synchronize()
+    g64 = g.double().numpy()
+    parity.check_out(jsd, oracle.linear_jsd_fwd(ha64, Wa64, hb64, Wb64, beta), "wide spread JSD")
+    ref = oracle.linear_jsd_bwd(ha64, Wa64, hb64, Wb64, beta, g64)
+    dza, dzb = (np.abs(x) for x in oracle.jsd_bwd(za, zb, beta, g64))
+    Ma, Mb = _jsd_mags(za, zb, beta, g64)
+    # p, q and the mixture (>= min(beta, 1 - beta) max(p, q)) flush below 2^-126
+    below = parity.TINY / min(beta, 1.0 - beta)
+    Fa, Fb = parity.flushed(Ma, _probs(za), below=below), parity.flushed(Mb, _probs(zb), below=below)
+    mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
+    evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
+    flush = (Fa @ np.abs(Wa64), Fa.T @ np.abs(ha64), Fb @ np.abs(Wb64), Fb.T @ np.abs(hb64))
+    for got, r, mg, ev, fl, name in zip(grads, ref, mags, evals, flush, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, mg, f"wide spread JSD {name}", ev, fl)
