@@ -570,10 +570,8 @@ def _oracle_rows(w, rows):
     return run, np
 
 
-def cpu_baseline(w, seconds=12.0, batch_rows=64):
-    """The oracle as it stands, all four ops fwd+bwd, on batches of rows until `seconds` pass."""
-    import oracle
-    run, _ = _oracle_rows(w, slice(0, batch_rows))
+def _oracle_rate(run, batch_rows, seconds):
+    """GB/s of the oracle running `run` (batch_rows rows per call) until `seconds` pass; (rate, rows, s)."""
     t0 = time.perf_counter()
     reps = 0
     while True:
@@ -583,11 +581,28 @@ def cpu_baseline(w, seconds=12.0, batch_rows=64):
             break
     dt = time.perf_counter() - t0
     rows = reps * batch_rows
-    step_bytes = sum(algorithmic_bytes(rows, VOCAB).values())
-    return {"value": round(step_bytes / dt / 1e9, 4), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": f"{rows} rows ({reps} x {batch_rows}) of the 8192x75968 bf16 workload, all four ops fwd+bwd, "
-                      f"fp64 C oracle with OpenMP over rows; GB/s = the same algorithmic bytes per row as the GPU"}
+    return sum(algorithmic_bytes(rows, VOCAB).values()) / dt / 1e9, rows, dt
+
+
+def cpu_baseline(w, seconds=12.0, batch_rows=64, single_seconds=4.0):
+    """The oracle as it stands, all four ops fwd+bwd, on batches of rows until `seconds` pass, with
+    OpenMP over rows on all host cores; then on one thread for `single_seconds` (8 rows per call)."""
+    import oracle
+    run, _ = _oracle_rows(w, slice(0, batch_rows))
+    cores = oracle.num_threads()
+    rate, rows, dt = _oracle_rate(run, batch_rows, seconds)
+    run1, _ = _oracle_rows(w, slice(0, 8))
+    oracle.set_num_threads(1)
+    try:
+        rate1, rows1, dt1 = _oracle_rate(run1, 8, single_seconds)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{rows} rows ({rows // batch_rows} x {batch_rows}) of the 8192x75968 bf16 workload, all four "
+                      f"ops fwd+bwd, fp64 C oracle with OpenMP over rows; GB/s = the same algorithmic bytes per row "
+                      f"as the GPU",
+            "single_thread": {"value": round(rate1, 4), "unit": UNIT, "cores": 1, "seconds": round(dt1, 2),
+                              "sample": f"{rows1} rows ({rows1 // 8} x 8), the same ops, one OpenMP thread"}}
 
 
 def run_reference(args, rank, world):

@@ -51,6 +51,7 @@ def build(force: bool = False) -> str:
 
 _SIGS = {
     "vpo_num_threads": ([], ctypes.c_int),
+    "vpo_set_num_threads": (["i"], None),
     "vpo_logprobs_fwd": (["P", "I", "I", "I", "P", "P", "P", "P", "P"], None),
     "vpo_logprobs_bwd": (["P", "I", "I", "I", "P", "P", "P"], None),
     "vpo_logprobs_topk_fwd": (["P", "I", "I", "I", "I", "P", "P", "P"], None),
@@ -101,6 +102,11 @@ def _load():
 def num_threads(lib=None) -> int:
     """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all host cores)."""
     return (lib or _load()).vpo_num_threads()
+
+
+def set_num_threads(n: int, lib=None) -> None:
+    """OpenMP threads for the following oracle calls (timing only; results do not depend on it)."""
+    (lib or _load()).vpo_set_num_threads(int(n))
 
 
 def _f64(a) -> np.ndarray:

@@ -63,6 +63,15 @@ int vpo_num_threads(void) {
 #endif
 }
 
+/* Threads for the following calls (n >= 1); timing only, the results do not depend on it. */
+void vpo_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 int vpo_version(void) { return 1; }
 
 /* ------------------------------------------------------------------------ */
