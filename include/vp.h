@@ -513,9 +513,9 @@ VP_API vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb
  * softmax(hb . wb^T) (B, the teacher), mix = beta q + (1 - beta) p,
  * JSD = beta KL(q || mix) + (1 - beta) KL(p || mix). Models and layouts as
  * vp_linear_kl_fwd. beta = 0 and beta = 1 are vp_linear_kl_fwd with
- * VP_KL_FORWARD and VP_KL_REVERSE; 0 < beta < 1 takes two passes of the dual
- * GEMM: the rows' maxima and log-sums of A and B, then both KL-to-mixture
- * expectations together. Outputs: jsd fp32 [N]; stats_a, stats_b
+ * VP_KL_FORWARD and VP_KL_REVERSE; 0 < beta < 1 takes two passes: one GEMM
+ * per model for the rows' maxima and log-sums of A and B, then the dual GEMM
+ * for both KL-to-mixture expectations together. Outputs: jsd fp32 [N]; stats_a, stats_b
  * (vp_rowstat [N], the c fields holding KL(p || mix) and KL(q || mix)).
  * workspace: vp_linear_jsd_workspace_size(N, V) bytes. beta outside [0, 1]
  * or NaN: VP_ERR_ARG. */

@@ -584,8 +584,9 @@ cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
 // vocab_parallel_jsd: "Motivation" names teacher-student divergences computed
 // from tiled LM-head projections, "Changes" the two passes: global
 // normalisation first, then both KL-to-mixture expectations together).
-//   pass 1  the KL forward's dual GEMM and merge: each row's exact maxima and
-//           log-sums of A and B in the two records;
+//   pass 1  each model's single-product GEMM and merge (the entropy
+//           forward's): each row's exact maxima and log-sums of A and B in
+//           the two records;
 //   pass 2  the dual GEMM again; the epilogue (JsdEpi) forms log p, log q and
 //           log mix (mix = beta q + (1 - beta) p) in base-2 units and sums
 //           p (log p - log mix) and q (log q - log mix) per tile; a merge per
@@ -788,11 +789,14 @@ struct DzJsdEpi {
 };
 
 cudaError_t launch_linear_jsd_fwd(const LinearKLArgs &a) {
-    // pass 1: the records (the KL forward; its KL output is overwritten below)
-    LinearKLArgs k = a;
-    k.direction = 0;
-    cudaError_t e = launch_linear_kl_fwd(k);
+    // pass 1: each model's records (row max, log-sum, flags) from its own
+    // single-product forward, the entropy's (its H output, written to jsd, is
+    // overwritten below): two single GEMMs cost less than one dual KL pass
+    LinearEntArgs ea{a.ha, a.wa, a.N, a.V, a.Da, a.kl, a.stats_a, nullptr, nullptr, nullptr, a.workspace, a.stream};
+    cudaError_t e = launch_linear_entropy_fwd(ea);
     if (e != cudaSuccess) return e;
+    LinearEntArgs eb{a.hb, a.wb, a.N, a.V, a.Db, a.kl, a.stats_b, nullptr, nullptr, nullptr, a.workspace, a.stream};
+    if ((e = launch_linear_entropy_fwd(eb)) != cudaSuccess) return e;
     // pass 2: both KL-to-mixture expectations (the workspace is free again)
     CUtensorMap tm_ha, tm_wa, tm_hb, tm_wb;
     if (!make_map(&tm_ha, a.ha, a.N, a.Da, a.Da, kLBM) || !make_map(&tm_wa, a.wa, a.V, a.Da, a.Da, kPBHalf) ||
