@@ -581,6 +581,15 @@ static cudaError_t launch_gemm_pair_impl(const CUtensorMap &ta, const CUtensorMa
         cudaError_t e = cudaFuncSetAttribute(umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
+        if (kDual) {
+            // the register split assumes the kernel is launched with exactly
+            // kPairDualRegsLaunch registers a thread; with fewer, setmaxnreg.inc
+            // would wait for registers that do not exist, so refuse instead
+            cudaFuncAttributes fa;
+            if ((e = cudaFuncGetAttributes(&fa, umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual>)) != cudaSuccess)
+                return e;
+            if (fa.numRegs != kPairDualRegsLaunch) return cudaErrorInvalidConfiguration;
+        }
         attr_done.fetch_or(1ull << (dev & 63));
     }
     int sms = 0;

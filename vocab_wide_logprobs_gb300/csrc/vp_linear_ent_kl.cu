@@ -225,19 +225,34 @@ linear_entropy_merge_kernel(int N, int n_vt, const EntTile *__restrict__ parts, 
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
     const EntTile *p = parts + (int64_t)row * n_vt;
+    // tiles lane, lane + 32, ... in that order, four loads issued together
+    constexpr int kB = 4;
+    const EntTile empty{-INFINITY, 0.f, 0.f, 0.f};
     float M = -INFINITY;
-    for (int i = lane; i < n_vt; i += 32) M = fmaxf(M, p[i].m);
+    for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
+        float m[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) m[u] = i0 + 32 * u < n_vt ? p[i0 + 32 * u].m : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kB; ++u) M = fmaxf(M, m[u]);
+    }
     M = warp_max(M);
     DF S{0.f, 0.f}, W{0.f, 0.f};
     bool nan = false;
-    for (int i = lane; i < n_vt; i += 32) {
-        const EntTile t = p[i];
-        if (t.S != t.S || t.W != t.W || t.m == INFINITY) { nan = true; continue; }
-        if (!(t.S > 0.f)) continue;                       // zero-weight tile
-        const float a = expf(t.m - M);
-        if (a == 0.f) continue;
-        df_add(S, a * t.S);
-        df_add(W, a * fmaf(-(M - t.m), t.S, t.W));        // both terms <= 0
+    for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
+        EntTile tt[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) tt[u] = i0 + 32 * u < n_vt ? p[i0 + 32 * u] : empty;
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const EntTile &t = tt[u];
+            if (t.S != t.S || t.W != t.W || t.m == INFINITY) { nan = true; continue; }
+            if (!(t.S > 0.f)) continue;                       // zero-weight tile
+            const float a = expf(t.m - M);
+            if (a == 0.f) continue;
+            df_add(S, a * t.S);
+            df_add(W, a * fmaf(-(M - t.m), t.S, t.W));        // both terms <= 0
+        }
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) {
@@ -262,34 +277,53 @@ linear_kl_merge_kernel(int N, int n_vt, const KLTile *__restrict__ parts, float 
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
     const KLTile *p = parts + (int64_t)row * n_vt;
+    // each lane takes tiles lane, lane + 32, ... in that order; the loads of four
+    // of them are issued together (an absent tile reads as an empty one)
+    constexpr int kB = 4;
+    const KLTile empty{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, 0.f, 0.f};
     float Mp = -INFINITY, Mq = -INFINITY;
-    for (int i = lane; i < n_vt; i += 32) {
-        Mp = fmaxf(Mp, p[i].mp);
-        Mq = fmaxf(Mq, p[i].mq);
+    for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
+        float2 m[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int i = i0 + 32 * u;
+            m[u] = i < n_vt ? make_float2(p[i].mp, p[i].mq) : make_float2(-INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            Mp = fmaxf(Mp, m[u].x);
+            Mq = fmaxf(Mq, m[u].y);
+        }
     }
     Mp = warp_max(Mp);
     Mq = warp_max(Mq);
     DF Sp{0.f, 0.f}, Sq{0.f, 0.f}, W{0.f, 0.f};
     bool nanp = false, nanq = false;
-    for (int i = lane; i < n_vt; i += 32) {
-        const KLTile t = p[i];
-        const bool bp = t.Sp != t.Sp || t.W != t.W || t.mp == INFINITY;
-        const bool bq = t.Sq != t.Sq || t.mq == INFINITY;
-        nanp |= bp;
-        nanq |= bq;
-        if (bp || bq) continue;
-        if (t.Sq > 0.f) {
-            const float aq = expf(t.mq - Mq);
-            if (aq != 0.f) df_add(Sq, aq * t.Sq);
-        }
-        if (t.Sp > 0.f) {
-            const float ap = expf(t.mp - Mp);
-            if (ap != 0.f) {
-                df_add(Sp, ap * t.Sp);
-                // W_i about the row centres: W_i - ((Mp - mp_i) - (Mq - mq_i)) S_P,i
-                const float shift = (Mp - t.mp) - (Mq - t.mq);
-                df_add(W, ap * t.W);
-                df_add(W, -(ap * shift) * t.Sp);
+    for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
+        KLTile tt[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) tt[u] = i0 + 32 * u < n_vt ? p[i0 + 32 * u] : empty;
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const KLTile &t = tt[u];
+            const bool bp = t.Sp != t.Sp || t.W != t.W || t.mp == INFINITY;
+            const bool bq = t.Sq != t.Sq || t.mq == INFINITY;
+            nanp |= bp;
+            nanq |= bq;
+            if (bp || bq) continue;
+            if (t.Sq > 0.f) {
+                const float aq = expf(t.mq - Mq);
+                if (aq != 0.f) df_add(Sq, aq * t.Sq);
+            }
+            if (t.Sp > 0.f) {
+                const float ap = expf(t.mp - Mp);
+                if (ap != 0.f) {
+                    df_add(Sp, ap * t.Sp);
+                    // W_i about the row centres: W_i - ((Mp - mp_i) - (Mq - mq_i)) S_P,i
+                    const float shift = (Mp - t.mp) - (Mq - t.mq);
+                    df_add(W, ap * t.W);
+                    df_add(W, -(ap * shift) * t.Sp);
+                }
             }
         }
     }
@@ -686,10 +720,18 @@ linear_jsd_merge_kernel(int N, int n_vt, float beta, const JsdTile *__restrict__
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
     const JsdTile *p = parts + (int64_t)row * n_vt;
+    // tiles lane, lane + 32, ... in that order, four loads issued together
+    constexpr int kB = 4;
     DF kp{0.f, 0.f}, kq{0.f, 0.f};
-    for (int i = lane; i < n_vt; i += 32) {
-        df_add(kp, p[i].kp);
-        df_add(kq, p[i].kq);
+    for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
+        JsdTile tt[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) tt[u] = i0 + 32 * u < n_vt ? p[i0 + 32 * u] : JsdTile{0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            df_add(kp, tt[u].kp);
+            df_add(kq, tt[u].kq);
+        }
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) {
