@@ -380,7 +380,7 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     """Fused linear ops on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16): logp, entropy and
     KL against a second model of the same shape, forward and backward. Each op is timed as a burst, after
     IDLE_S seconds of idle GPU, against the measured burst bf16 peak: a long GEMM heats the part and the
-    power cap then lowers the clock of whatever runs next."""
+    power cap then lowers the clock of whatever runs next, or of its own later calls."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     from vocab_wide_logprobs_gb300 import workloads
@@ -392,7 +392,7 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     ws = torch.empty(vp.vp_linear_logp_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
     for _ in range(2):
         vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws)
-    reps = max(3, min(args.steps, 10))
+    reps = 3   # a burst of three calls (the longest burst, three KL backwards, is about 50 ms)
     ms = _time_ms(lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws), reps, IDLE_S)
     dh = torch.empty_like(h)
     dW = torch.empty_like(W)

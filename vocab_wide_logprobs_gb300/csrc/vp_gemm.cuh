@@ -544,22 +544,21 @@ static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb
 // L2 eviction priorities of the operand tiles (l2hints: A in bits 0-1, B in bits 2-3;
 // 1 = evict_first, 2 = evict_last, 0 = normal), measured on GB300 at hidden
 // [8192, 4096] x W [75968, 4096]:
-//  - logits GEMMs (forward, backward K1): A = hidden rows, reused by every
-//    vocabulary tile of the group, evict_last; B = W, streamed, evict_first.
-//    With groups of about 32 MB of A this cut the forward's DRAM reads from
-//    6.3 GB (h re-fetched for every few W tiles) to near one read of W, and
-//    its time by 16%.
-//  - the dual form: both evict_last. Two heads stream at once, and with W
-//    evict_first the pairs of a group that share a W tile missed it in L2
-//    (the KL forward took 5.79 ms with evict_first W, 5.65 ms with evict_last).
+//  - logits GEMMs (forward, backward K1, the dual form): A = hidden rows,
+//    reused by every vocabulary tile of the group, evict_last; with groups of
+//    about 32 MB of A this cut the forward's DRAM reads from 6.3 GB (h
+//    re-fetched for every few W tiles) to near one read of W, and its time by
+//    16%. B = W evict_last as well: with W evict_first, the CTA pairs of a
+//    group that share a W tile missed it in L2 (on one box the logp forward
+//    took 2.76 ms against 2.66 ms, its backward 8.52 against 8.31 ms, and the
+//    KL forward 5.79 against 5.65 ms).
 //  - K2 (dz . W_c): both operands evict_last (each is re-read by the other's
 //    group).
 //  - K3 (dz^T . h): both evict_last, in groups of 4 m-blocks (2 on CTA pairs):
 //    h (64 MB) then stays in L2 while dz streams past it; with h evict_first
 //    it was re-read from DRAM for every group, and the backward took 8.5 ms
 //    instead of 8.1-8.2 ms.
-constexpr int kHintLogits = 2 | (1 << 2);
-constexpr int kHintDual = 2 | (2 << 2);
+constexpr int kHintLogits = 2 | (2 << 2);
 constexpr int kHintK2 = 2 | (2 << 2);
 constexpr int kHintK3 = 2 | (2 << 2);
 
@@ -641,7 +640,7 @@ template <class Epi>
 static cudaError_t launch_gemm_dual(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                                     const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
                                     cudaStream_t stream) {
-    return launch_gemm_pair_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, epi, stream, 0, kHintDual);
+    return launch_gemm_pair_impl<Epi, false, false, true>(ta, tb, ta2, tb2, M, Nn, K, K2, epi, stream, 0, kHintLogits);
 }
 
 static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
