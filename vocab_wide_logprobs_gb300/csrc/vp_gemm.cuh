@@ -410,19 +410,24 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
 }
 
 // Backward K2 epilogue: acc[row][col] (+)= tile, fp32 (pitch ld).
+// On the last chunk (out non-null) the sum is rounded to bf16 and written to
+// out (same pitch) instead of acc: the dhidden output, with no separate pass.
 struct AccEpi {
     int M, ld;
     bool first;
     float *acc;
+    __nv_bfloat16 *out;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
         const bool valid = row < M;
-        float *dst = acc + (int64_t)(valid ? row : 0) * ld + col0;
+        const int64_t off = (int64_t)(valid ? row : 0) * ld + col0;
+        float *dst = acc + off;
 #pragma unroll 1
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
             if (!valid || c * 32 >= ncol) continue;
             float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+            uint32_t packed[16];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
@@ -430,7 +435,19 @@ struct AccEpi {
                     const float4 a = d4[k];
                     o.x += a.x; o.y += a.y; o.z += a.z; o.w += a.w;
                 }
-                d4[k] = o;
+                if (out) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+                    packed[2 * k] = *reinterpret_cast<uint32_t *>(&lo);
+                    packed[2 * k + 1] = *reinterpret_cast<uint32_t *>(&hi);
+                } else {
+                    d4[k] = o;
+                }
+            }
+            if (out) {
+                uint4 *o4 = reinterpret_cast<uint4 *>(out + off + c * 32);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    o4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
             }
         }
     }
@@ -462,13 +479,6 @@ struct StoreBf16Epi {
         }
     }
 };
-
-// out[i] = bf16(acc[i]) for rows x cols (pitches in elements)
-static __global__ void __launch_bounds__(256) to_bf16_kernel(const float *__restrict__ acc, int64_t n,
-                                                             __nv_bfloat16 *__restrict__ out) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        out[i] = __float2bfloat16_rn(acc[i]);
-}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -656,9 +666,12 @@ static int64_t chunk_cols(int64_t N, int64_t V) {
 
 // The two gradient GEMMs of one vocabulary chunk [v0, v0 + nv) for one model
 // (hidden h [N, D], head W [V, D]) given the chunk's dz (bf16 [N, nv], pitch vc):
-//   K2  acc (+)= dz . W_c  (A = dz K-major, B = W_c MN-major, K = nv; first chunk stores)
+//   K2  acc (+)= dz . W_c  (A = dz K-major, B = W_c MN-major, K = nv; the first
+//       chunk stores; the last one (last = true) writes bf16(acc + tile) to
+//       dhidden instead)
 //   K3  dW_c = dz^T . h    (A = dz MN-major, B = h MN-major, K = N), written as bf16
-// acc and dW may each be null (that GEMM is skipped). Both GEMMs stream two
+// acc and dW may each be null (that GEMM is skipped); dhidden is non-null when
+// acc is. Both GEMMs stream two
 // operands far larger than L2 along a long K, so their tiles run in small
 // m-groups (tile_coords): the concurrent CTAs then share a few A and B tiles
 // instead of each A tile being fetched from DRAM once per n-block.
@@ -672,13 +685,13 @@ constexpr int kGradGroupM = VP_K2_GROUP;   // K2: m-blocks of dz (8 MB each at v
 constexpr int kWGroupM = VP_K3_GROUP;      // K3: m-blocks of dz^T (2 MB each at N = 8192) x the n-blocks of D
 static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_bfloat16 *W, int N, int D, int64_t v0,
                                         int nv, int64_t vc, const __nv_bfloat16 *dz, float *acc,
-                                        __nv_bfloat16 *dW, cudaStream_t stream) {
+                                        __nv_bfloat16 *dhidden, __nv_bfloat16 *dW, bool last, cudaStream_t stream) {
     cudaError_t e;
     if (acc) {
         CUtensorMap tm_dz, tm_wc_mn;
         if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
             return cudaErrorInvalidValue;
-        const AccEpi ae{N, D, v0 == 0, acc};
+        const AccEpi ae{N, D, v0 == 0, acc, last ? dhidden : nullptr};
         e = kGemmPairs ? launch_gemm_pair<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, (kGradGroupM + 1) / 2,
                                                                 kHintK2)
                        : launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM, kHintK2);
@@ -696,12 +709,6 @@ static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_b
             return e;
     }
     return cudaSuccess;
-}
-
-// dhidden = bf16(acc) over N x D elements.
-static cudaError_t finish_dhidden(const float *acc, int64_t n, __nv_bfloat16 *dh, cudaStream_t stream) {
-    to_bf16_kernel<<<(unsigned)((n + 255) / 256 < 65535 ? (n + 255) / 256 : 65535), 256, 0, stream>>>(acc, n, dh);
-    return cudaGetLastError();
 }
 
 // Reads (and optionally clears) this translation unit's fault word.

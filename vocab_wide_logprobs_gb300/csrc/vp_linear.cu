@@ -279,11 +279,10 @@ cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
         const DzEpi de{N, V, (int)v0, (int)vc, a.vocab_start, a.targets, static_cast<const RowStat *>(a.stats), a.g,
                        dz, a.err};
         if ((e = launch_logits_gemm(h, W + v0 * D, N, nv, D, de, a.stream, kGemmPairs)) != cudaSuccess) return e;
-        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dW),
-                                      a.stream)) != cudaSuccess)
+        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dhidden),
+                                      static_cast<__nv_bfloat16 *>(a.dW), v0 + vc >= V, a.stream)) != cudaSuccess)
             return e;
     }
-    if (a.dhidden) return finish_dhidden(acc, (int64_t)N * D, static_cast<__nv_bfloat16 *>(a.dhidden), a.stream);
     return cudaSuccess;
 }
 

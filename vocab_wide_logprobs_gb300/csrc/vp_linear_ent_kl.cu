@@ -520,11 +520,10 @@ cudaError_t launch_linear_entropy_bwd(const LinearEntArgs &a) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
         const DzEntEpi de{N, (int)vc, static_cast<const RowStat *>(a.stats), a.g, dz};
         if ((e = launch_logits_gemm(h, W + v0 * D, N, nv, D, de, a.stream, kGemmPairs)) != cudaSuccess) return e;
-        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dW),
-                                      a.stream)) != cudaSuccess)
+        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dhidden),
+                                      static_cast<__nv_bfloat16 *>(a.dW), v0 + vc >= V, a.stream)) != cudaSuccess)
             return e;
     }
-    if (a.dhidden) return finish_dhidden(acc, (int64_t)N * D, static_cast<__nv_bfloat16 *>(a.dhidden), a.stream);
     return cudaSuccess;
 }
 
@@ -590,17 +589,16 @@ static cudaError_t two_model_bwd(const LinearKLArgs &a, bool b_first, MakeEpi ma
         e = b_first ? launch_gemm_dual(tm_hb, tm_wbc, tm_ha, tm_wac, N, nv, Db, Da, make_epi((int)vc, dzb, dza), a.stream)
                     : launch_gemm_dual(tm_ha, tm_wac, tm_hb, tm_wbc, N, nv, Da, Db, make_epi((int)vc, dza, dzb), a.stream);
         if (e != cudaSuccess) return e;
+        const bool last = v0 + vc >= V;
         if (want_a && (e = chunk_gradient_gemms(tm_ha_mn, Wa, N, Da, v0, nv, vc, dza, acc_a,
-                                                static_cast<__nv_bfloat16 *>(a.dwa), a.stream)) != cudaSuccess)
+                                                static_cast<__nv_bfloat16 *>(a.dha),
+                                                static_cast<__nv_bfloat16 *>(a.dwa), last, a.stream)) != cudaSuccess)
             return e;
         if (want_b && (e = chunk_gradient_gemms(tm_hb_mn, Wb, N, Db, v0, nv, vc, dzb, acc_b,
-                                                static_cast<__nv_bfloat16 *>(a.dwb), a.stream)) != cudaSuccess)
+                                                static_cast<__nv_bfloat16 *>(a.dhb),
+                                                static_cast<__nv_bfloat16 *>(a.dwb), last, a.stream)) != cudaSuccess)
             return e;
     }
-    if (a.dha && (e = finish_dhidden(acc_a, (int64_t)N * Da, static_cast<__nv_bfloat16 *>(a.dha), a.stream)) !=
-                     cudaSuccess)
-        return e;
-    if (a.dhb) return finish_dhidden(acc_b, (int64_t)N * Db, static_cast<__nv_bfloat16 *>(a.dhb), a.stream);
     return cudaSuccess;
 }
 
