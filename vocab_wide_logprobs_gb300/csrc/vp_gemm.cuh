@@ -1,6 +1,7 @@
 // vp_gemm.cuh -- the persistent tcgen05 GEMM shared by the fused linear ops
-// (linear logp, linear entropy, linear KL), its operand tensor maps and the
-// gradient GEMMs of the chunked backward.
+// (linear logp, entropy, KL and JSD): single-CTA and CTA-pair kernels, the
+// two-model dual form, their operand tensor maps, tile order and L2 hints, and
+// the gradient GEMMs of the chunked backward.
 //
 // Each translation unit that includes this header gets its own copy of the
 // kernels' fault word (g_linear_fault); read_linear_fault reads every copy.
@@ -206,14 +207,24 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
 // epilogue warps of both CTAs read their own TMEM rows and arrive on the
 // leader's "acc_empty" barrier. Every wait is bounded; every thread of both
 // CTAs reaches the final cluster barrier.
-// The dual form (kDual) runs here too, with the dual protocol of the
-// single-CTA kernel (per-product barriers; the first product copied to
-// registers and freed at once). It has 12 warps: warp 0 TMA, warp 1 MMA, warps
-// 2-3 idle, warps 4-11 the epilogue (two per TMEM lane quarter, one 128-column
-// half each). An epilogue thread holds 128 fp32 values, so the epilogue
-// warpgroups take registers from the first: of the 168 a thread is launched
-// with, setmaxnreg leaves 56 to warpgroup 0 and gives 224 to warpgroups 1-2
-// (4 x 56 + 8 x 224 = 12 x 168).
+// Dual form (kDual, K-major operands only): each tile also computes a second
+// product C2 = A2 . B2^T (K2 deep) of the same shape into the other 256 TMEM
+// columns, so that an epilogue sees the same logits tile of two models at
+// once. The two products fill TMEM, so instead of two accumulator sets each
+// product has its own barriers (acc_full[p], acc_empty[p]): the epilogue
+// copies its columns of the first product into registers as soon as that
+// product is done and frees them, so the next tile's first product queues
+// behind this tile's second and the tensor pipe does not drain between tiles;
+// the epilogue then works through the second product while the next first
+// product runs. The epilogue functor is called as epi(row, col0, ncol, x, tb),
+// x the row's 128 columns (one half of the tile) of the first product and tb
+// the TMEM address of the same columns of the second. The dual kernel has 12
+// warps: warp 0 TMA, warp 1 MMA, warps 2-3 idle, warps 4-11 the epilogue (two
+// per TMEM lane quarter, one 128-column half each). An epilogue thread holds
+// 128 fp32 values, so the epilogue warpgroups take registers from the first:
+// of the 168 a thread is launched with, setmaxnreg leaves 56 to warpgroup 0
+// and gives 224 to warpgroups 1-2 (4 x 56 + 8 x 224 = 12 x 168); the launcher
+// checks the 168 before the first launch.
 // ---------------------------------------------------------------------------
 constexpr int kPStages = 6;
 constexpr int kPBHalf = kLBN / 2;                       // rows of the B tile per CTA
