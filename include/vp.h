@@ -390,7 +390,9 @@ VP_API size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D)
  * W and h in place (transposed operands as MN-major tiles); dhidden
  * accumulates across chunks in fp32 and is rounded to bf16 at the end; dW is
  * written chunk by chunk. dhidden: bf16 [N, D]; dW: bf16 [V, D]; either may
- * be NULL (not both). stats: the records written by vp_linear_logp_fwd.
+ * be NULL (not both). stats: the records written by vp_linear_logp_fwd, or by
+ * vp_logprobs_merge for a vocabulary shard (see the sharded fused linear ops
+ * below: a target outside the shard is then held by another shard).
  * Rows with an ignored target contribute nothing; rows with a data error or
  * without valid statistics make their dhidden row and all of dW NaN. */
 VP_API vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
@@ -537,6 +539,49 @@ VP_API vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *h
                                    int64_t V, int64_t Da, int64_t Db, double beta, const vp_rowstat *stats_a,
                                    const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
                                    void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream);
+
+/* ------------------------------------------------------------------------ */
+/* Vocabulary-sharded fused linear ops [P2, "Implementation": tensor-parallel */
+/* shards of the head's rows, each reducing its own logit tiles; P1, second   */
+/* commit message: per-shard max, sum-exp and centred sum combined on the     */
+/* row max]. The flow of the sharded forms above, with W's rows as the shard: */
+/*  1. shard k (rows [vocab_start_k, vocab_start_k + V_k) of W, passed as    */
+/*     weight + vocab_start_k * D with V = V_k) calls vp_linear_*_partial;   */
+/*  2. the caller gathers the K arrays shard-major;                          */
+/*  3. vp_logprobs_merge / vp_entropy_merge / vp_kl_merge write the outputs  */
+/*     and records that the unsharded vp_linear_*_fwd would write;           */
+/*  4. each shard calls vp_linear_*_bwd on its rows of W with the merged     */
+/*     records: its dW rows are complete, and its dhidden is that shard's    */
+/*     term of the sum over shards (dz_k . W_k, rounded to bf16); the caller */
+/*     adds the K terms (e.g. an all-reduce). vp_linear_logp_bwd takes a     */
+/*     target outside its shard as held elsewhere when the records come from */
+/*     vp_logprobs_merge (VP_ROW_SHARDED), and gives VP_ROW_BADTARGET rows   */
+/*     NaN gradient rows.                                                    */
+/* parts: vp_partial [N], 8-byte aligned; workspace as the unsharded forward */
+/* (vp_linear_logp_workspace_size / vp_linear_entropy_workspace_size /       */
+/* vp_linear_kl_workspace_size with the shard's V). Argument errors as the   */
+/* unsharded forwards.                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* The shard's logprobs records: m and S over the shard's logits, z_t and
+ * VP_PART_HAS_TARGET when the target (a global id) lies in the shard,
+ * VP_PART_IGNORED for a negative target, VP_PART_NANINF for a NaN or +inf
+ * logit. A target in another shard sets neither and is not an error here. */
+VP_API vp_status vp_linear_logp_partial(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                        int64_t vocab_start, const int64_t *targets, vp_partial *parts,
+                                        void *workspace, size_t workspace_bytes, vp_stream stream);
+
+/* The shard's entropy records: m, S and W = sum exp(z - m) (z - m). */
+VP_API vp_status vp_linear_entropy_partial(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                           vp_partial *parts, void *workspace, size_t workspace_bytes,
+                                           vp_stream stream);
+
+/* The shard's KL(P||Q) records of two models ((P, Q) = (A, B) for
+ * VP_KL_REVERSE, (B, A) for VP_KL_FORWARD; wa and wb hold the same shard of
+ * the vocabulary): m, S of P, m_b, S_b of Q and W as vp_kl_partial. */
+VP_API vp_status vp_linear_kl_partial(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
+                                      int64_t V, int64_t Da, int64_t Db, int direction, vp_partial *parts,
+                                      void *workspace, size_t workspace_bytes, vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                      */

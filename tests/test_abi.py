@@ -176,6 +176,23 @@ def test_linear_jsd_entry_points_check_beta_first():
     assert lib.vp_linear_jsd_workspace_size(4, 16) == lib.vp_linear_kl_workspace_size(4, 16)
 
 
+def test_linear_partial_entry_points_check_arguments_on_the_host():
+    lib = _lib.lib()
+    ws = ctypes.c_size_t(1 << 30)
+    assert lib.vp_linear_logp_partial(FAKE, FAKE, 4, 16, 96, 0, FAKE, FAKE, FAKE, ws, None) == ERR_SHAPE   # D
+    assert lib.vp_linear_logp_partial(FAKE, FAKE, 4, 16, 64, 0, FAKE, None, FAKE, ws, None) == ERR_NULL   # parts
+    assert lib.vp_linear_logp_partial(FAKE, FAKE, 4, 16, 64, 0, FAKE_ODD, FAKE, FAKE, ws, None) == ERR_ALIGN
+    assert lib.vp_linear_logp_partial(FAKE, FAKE, 4, 16, 64, 0, FAKE, FAKE, FAKE, ctypes.c_size_t(8),
+                                      None) == ERR_ARG                                             # workspace
+    assert lib.vp_linear_logp_partial(None, None, 0, 16, 64, 0, None, None, None, ctypes.c_size_t(0), None) == OK
+    assert lib.vp_linear_entropy_partial(FAKE, FAKE, 4, 0, 64, FAKE, FAKE, ws, None) == ERR_SHAPE        # V
+    assert lib.vp_linear_entropy_partial(FAKE, FAKE, 4, 16, 64, FAKE_ODD, FAKE, ws, None) == ERR_ALIGN
+    two = (FAKE, FAKE, FAKE, FAKE, 4, 16, 64, 128)
+    assert lib.vp_linear_kl_partial(*two, 2, FAKE, FAKE, ws, None) == ERR_ARG                           # direction
+    assert lib.vp_linear_kl_partial(*two, 0, None, FAKE, ws, None) == ERR_NULL
+    assert lib.vp_linear_kl_partial(FAKE, FAKE, FAKE, FAKE, 4, 16, 64, 32, 1, FAKE, FAKE, ws, None) == ERR_SHAPE
+
+
 def test_binding_wraps_every_entry_point():
     import vocab_wide_logprobs_gb300 as vp
     missing = [n for n in declared_functions() if not hasattr(vp, n)]

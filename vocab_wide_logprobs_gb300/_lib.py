@@ -34,6 +34,9 @@ SIGNATURES = {
     "vp_linear_kl_fwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, ctypes.c_size_t, P],
     "vp_linear_kl_bwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
     "vp_linear_jsd_fwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_logp_partial": [P, P, I64, I64, I64, I64, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_entropy_partial": [P, P, I64, I64, I64, P, P, ctypes.c_size_t, P],
+    "vp_linear_kl_partial": [P, P, P, P, I64, I64, I64, I64, I32, P, P, ctypes.c_size_t, P],
     "vp_linear_jsd_bwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P, P, P, ctypes.c_size_t,
                           P],
     "vp_upload": [P, P, ctypes.c_size_t, P],

@@ -540,3 +540,38 @@ def vp_fault_status(clear: bool = False) -> int:
     v = ctypes.c_uint32(0)
     _check(_lib.lib().vp_fault_status(ctypes.byref(v), int(clear)), "vp_fault_status")
     return int(v.value)
+
+
+def vp_linear_logp_partial(hidden, weight, targets, vocab_start: int = 0, parts=None, workspace=None):
+    """Per-row logprobs records over the vocabulary shard held by weight (rows vocab_start .. + V of the head)."""
+    N, V, D = _linear_model(hidden, weight, "vp_linear_logp_partial")
+    parts = partials(N, hidden.device) if parts is None else parts
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_logp_workspace_size(N, V, D), hidden)
+    _check(_lib.lib().vp_linear_logp_partial(_ptr(hidden), _ptr(weight), N, V, D, vocab_start, _ptr(targets),
+                                             _ptr(parts), _ptr(workspace), workspace.numel(), _stream()),
+           "vp_linear_logp_partial")
+    return parts
+
+
+def vp_linear_entropy_partial(hidden, weight, parts=None, workspace=None):
+    """Per-row entropy records over the vocabulary shard held by weight."""
+    N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_partial")
+    parts = partials(N, hidden.device) if parts is None else parts
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_entropy_workspace_size(N, V, D), hidden)
+    _check(_lib.lib().vp_linear_entropy_partial(_ptr(hidden), _ptr(weight), N, V, D, _ptr(parts), _ptr(workspace),
+                                                workspace.numel(), _stream()), "vp_linear_entropy_partial")
+    return parts
+
+
+def vp_linear_kl_partial(ha, wa, hb, wb, direction: int = KL_REVERSE, parts=None, workspace=None):
+    """Per-row KL records of two models over the vocabulary shard held by wa and wb."""
+    N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_partial")
+    parts = partials(N, ha.device) if parts is None else parts
+    if workspace is None:
+        workspace = _workspace(_lib.lib().vp_linear_kl_workspace_size(N, V), ha)
+    _check(_lib.lib().vp_linear_kl_partial(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, int(direction),
+                                           _ptr(parts), _ptr(workspace), workspace.numel(), _stream()),
+           "vp_linear_kl_partial")
+    return parts

@@ -602,3 +602,56 @@ const char *vp_status_string(int status) {
 int vp_version(void) { return 1; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Vocabulary-sharded fused linear ops: the shard's vp_partial records
+// ---------------------------------------------------------------------------
+vp_status vp_linear_logp_partial(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                 int64_t vocab_start, const int64_t *targets, vp_partial *parts, void *workspace,
+                                 size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, D)) return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !targets || !parts || !workspace) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8) || !aligned(parts, 8) ||
+        !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearFwdArgs a{hidden, weight, N, V, D, vocab_start, targets, nullptr, nullptr, workspace, nullptr,
+                        (cudaStream_t)stream, parts};
+    return launched(vp::launch_linear_logp_fwd(a));
+}
+
+vp_status vp_linear_entropy_partial(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
+                                    vp_partial *parts, void *workspace, size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, D)) return VP_ERR_SHAPE;
+    if (N == 0) return VP_OK;
+    if (!hidden || !weight || !parts || !workspace) return VP_ERR_NULL;
+    if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(parts, 8) || !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_entropy_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearEntArgs a{hidden, weight, N, V, D, nullptr, nullptr, nullptr, nullptr, nullptr, workspace,
+                        (cudaStream_t)stream, parts};
+    return launched(vp::launch_linear_entropy_fwd(a));
+}
+
+vp_status vp_linear_kl_partial(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
+                               int64_t Da, int64_t Db, int direction, vp_partial *parts, void *workspace,
+                               size_t workspace_bytes, vp_stream stream) {
+    if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
+    if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
+    if (N == 0) return VP_OK;
+    if (!ha || !wa || !hb || !wb || !parts || !workspace) return VP_ERR_NULL;
+    if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(parts, 8) ||
+        !aligned(workspace, 256))
+        return VP_ERR_ALIGN;
+    if (workspace_bytes < vp::linear_kl_workspace_bytes(N, V)) return VP_ERR_ARG;
+    vp_status st = check_device();
+    if (st != VP_OK) return st;
+    vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, direction, nullptr, nullptr, nullptr, nullptr,
+                       nullptr, nullptr, nullptr, nullptr, workspace, (cudaStream_t)stream, 0.f, parts};
+    return launched(vp::launch_linear_kl_fwd(a));
+}

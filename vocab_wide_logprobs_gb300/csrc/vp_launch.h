@@ -104,6 +104,7 @@ struct LinearFwdArgs {
     void *workspace;  // linear_workspace_bytes(N, V)
     int32_t *err;
     cudaStream_t stream;
+    void *parts = nullptr;   // vp_partial [N]: the shard's records instead of logp and stats
 };
 
 size_t linear_workspace_bytes(int64_t N, int64_t V);
@@ -142,6 +143,7 @@ struct LinearEntArgs {
     void *dhidden, *dW;           // backward outputs, bf16; either may be NULL
     void *workspace;
     cudaStream_t stream;
+    void *parts = nullptr;        // forward: vp_partial [N], the shard's records instead of H and stats
 };
 
 size_t linear_entropy_workspace_bytes(int64_t N, int64_t V);
@@ -162,6 +164,7 @@ struct LinearKLArgs {
     void *workspace;
     cudaStream_t stream;
     float beta = 0.f;             // generalized JSD: 0 < beta < 1 (the KL calls at 0 and 1)
+    void *parts = nullptr;        // KL forward: vp_partial [N], the shard's records instead of KL and stats
 };
 
 size_t linear_kl_workspace_bytes(int64_t N, int64_t V);

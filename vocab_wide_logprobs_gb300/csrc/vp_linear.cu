@@ -97,10 +97,15 @@ struct DzEpi {
         const int64_t tg = valid ? targets[row] : -1;
         const int64_t tl = tg - vocab_start;                // target column in the shard
         int mode = 0;                                      // 0 normal, 1 zero row, 2 NaN row
+        // records merged from vocabulary shards (kRowSharded): a target outside
+        // this shard has its onehot term in another shard; the merge flagged
+        // the rows whose target no shard holds (kRowBadTarget)
+        const bool sharded = (s.flags & kRowSharded) != 0;
         if (tg < 0) mode = 1;
-        else if (tl < 0 || tl >= V) mode = 2;
+        else if ((tl < 0 || tl >= V) && !sharded) mode = 2;
         if (s.flags & (kRowNanInf | kRowEmpty)) mode = mode == 1 ? 1 : 2;
-        if (valid && mode == 2 && err && col0 == 0 && v0 == 0 && tg >= 0 && (tl < 0 || tl >= V))
+        if (tg >= 0 && (s.flags & kRowBadTarget)) mode = 2;
+        if (valid && mode == 2 && err && col0 == 0 && v0 == 0 && tg >= 0 && (tl < 0 || tl >= V) && !sharded)
             atomicOr(err, VP_ERRBIT_TARGET_);
         const int64_t tcol = tl - v0 - col0;               // target column within this tile
         const float gr = valid ? g[row] : 0.f;
@@ -134,10 +139,14 @@ struct DzEpi {
 };
 
 // One warp per row: merge of the row's per-tile (m, S) in a fixed order.
+// kPart: the row's record over this vocabulary shard (vp_partial) instead of
+// logp and the row statistics; a target in another shard is not an error.
+template <bool kPart>
 __global__ void __launch_bounds__(256)
 linear_merge_kernel(int N, int V, int64_t vocab_start, const int64_t *__restrict__ targets,
                     const float2 *__restrict__ partials, const float *__restrict__ tgt_logit,
-                    float *__restrict__ logp, RowStat *__restrict__ stats, int32_t *__restrict__ err) {
+                    float *__restrict__ logp, RowStat *__restrict__ stats, int32_t *__restrict__ err,
+                    PartialRec *__restrict__ shard_parts) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
@@ -161,6 +170,19 @@ linear_merge_kernel(int N, int V, int64_t vocab_start, const int64_t *__restrict
     nan = __any_sync(0xffffffffu, nan);
     if (lane != 0) return;
     const double S = df_value(Sdf);
+    if constexpr (kPart) {
+        uint32_t pf = (nan || S != S) ? kPartNanInf : 0u;
+        const int64_t t = targets[row];
+        float zt = 0.f;
+        if (t < 0) {
+            pf |= kPartIgnored;
+        } else if (t - vocab_start >= 0 && t - vocab_start < V) {
+            pf |= kPartHasTarget;
+            zt = tgt_logit[row];
+        }
+        shard_parts[row] = PartialRec{S > 0.0 ? M : kNegBig, 0.f, S, 0.0, 0.0, zt, pf};
+        return;
+    }
     uint32_t flags = 0;
     if (nan || S != S) flags |= kRowNanInf;
     else if (S == 0.0) flags |= kRowEmpty;
@@ -191,8 +213,14 @@ cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a) {
     const LseEpi epi{(int)a.N, (int)a.V, (int)n_vt, a.vocab_start, a.targets, partials, tgt};
     cudaError_t e = launch_logits_gemm(a.hidden, a.weight, (int)a.N, (int)a.V, (int)a.D, epi, a.stream, kFwdPairs);
     if (e != cudaSuccess) return e;
-    linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
-        (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
+    PartialRec *parts = static_cast<PartialRec *>(a.parts);
+    if (parts)
+        linear_merge_kernel<true><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+            (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, nullptr, nullptr, nullptr, parts);
+    else
+        linear_merge_kernel<false><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+            (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats),
+            a.err, nullptr);
     return cudaGetLastError();
 }
 
@@ -234,8 +262,9 @@ cudaError_t launch_linear_logp_fwd_noalloc(const LinearFwdArgs &a) {
     const LseEpi epi{(int)a.N, (int)a.V, (int)n_vt, a.vocab_start, a.targets, partials, tgt};
     e = launch_logits_gemm(a.hidden, a.weight, (int)a.N, (int)a.V, (int)a.D, epi, a.stream, kFwdPairs);
     if (e != cudaSuccess) return e;
-    linear_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
-        (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err);
+    linear_merge_kernel<false><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+        (int)a.N, (int)a.V, a.vocab_start, a.targets, partials, tgt, a.logp, static_cast<RowStat *>(a.stats), a.err,
+        nullptr);
     return cudaGetLastError();
 }
 

@@ -218,9 +218,12 @@ struct KLEpi {
 // then a fixed shuffle tree), fp32 exponentials summed as double-floats, fp64
 // finish; the result depends on V only, not on N (batch invariance).
 // ---------------------------------------------------------------------------
+// kPart: the row's record over this vocabulary shard (vp_partial: m, S, W
+// about m, flags) instead of H and the row statistics.
+template <bool kPart>
 __global__ void __launch_bounds__(256)
 linear_entropy_merge_kernel(int N, int n_vt, const EntTile *__restrict__ parts, float *__restrict__ H,
-                            RowStat *__restrict__ stats) {
+                            RowStat *__restrict__ stats, PartialRec *__restrict__ shard_parts) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
@@ -262,6 +265,10 @@ linear_entropy_merge_kernel(int N, int n_vt, const EntTile *__restrict__ parts, 
     nan = __any_sync(0xffffffffu, nan);
     if (lane != 0) return;
     const double s = df_value(S), w = df_value(W);
+    if constexpr (kPart) {
+        shard_parts[row] = PartialRec{s > 0.0 ? M : kNegBig, 0.f, s, 0.0, w, 0.f, (nan || s != s) ? kPartNanInf : 0u};
+        return;
+    }
     uint32_t flags = 0;
     if (nan || s != s || M != M) flags |= kRowNanInf;
     else if (!(s > 0.0)) flags |= kRowEmpty;
@@ -270,9 +277,13 @@ linear_entropy_merge_kernel(int N, int n_vt, const EntTile *__restrict__ parts, 
     H[row] = flags ? qnan() : (float)(logS - c);
 }
 
+// kPart: the row's record over this vocabulary shard (vp_partial: both
+// maxima and sum-exps, W about the maxima, flags) instead of KL and the records.
+template <bool kPart>
 __global__ void __launch_bounds__(256)
 linear_kl_merge_kernel(int N, int n_vt, const KLTile *__restrict__ parts, float *__restrict__ kl,
-                       RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q) {
+                       RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q,
+                       PartialRec *__restrict__ shard_parts) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
@@ -337,6 +348,11 @@ linear_kl_merge_kernel(int N, int n_vt, const KLTile *__restrict__ parts, float 
     nanq = __any_sync(0xffffffffu, nanq);
     if (lane != 0) return;
     const double sp = df_value(Sp), sq = df_value(Sq), w = df_value(W);
+    if constexpr (kPart) {
+        const uint32_t pf = ((nanp || sp != sp) ? kPartNanInf : 0u) | ((nanq || sq != sq) ? kPartNanInfB : 0u);
+        shard_parts[row] = PartialRec{sp > 0.0 ? Mp : kNegBig, sq > 0.0 ? Mq : kNegBig, sp, sq, w, 0.f, pf};
+        return;
+    }
     uint32_t fp = 0, fq = 0;
     if (nanp || sp != sp || Mp != Mp) fp |= kRowNanInf;
     else if (!(sp > 0.0)) fp |= kRowEmpty;
@@ -496,8 +512,12 @@ cudaError_t launch_linear_entropy_fwd(const LinearEntArgs &a) {
     const EntEpi epi{(int)a.N, n_vt, parts};
     cudaError_t e = launch_logits_gemm(a.hidden, a.weight, (int)a.N, (int)a.V, (int)a.D, epi, a.stream, kFwdPairs);
     if (e != cudaSuccess) return e;
-    linear_entropy_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>((int)a.N, n_vt, parts, a.H,
-                                                                                   static_cast<RowStat *>(a.stats));
+    if (a.parts)
+        linear_entropy_merge_kernel<true><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+            (int)a.N, n_vt, parts, nullptr, nullptr, static_cast<PartialRec *>(a.parts));
+    else
+        linear_entropy_merge_kernel<false><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+            (int)a.N, n_vt, parts, a.H, static_cast<RowStat *>(a.stats), nullptr);
     return cudaGetLastError();
 }
 
@@ -546,8 +566,12 @@ cudaError_t launch_linear_kl_fwd(const LinearKLArgs &a) {
                            : launch_gemm_dual(tm_hb, tm_wb, tm_ha, tm_wa, N, V, Db, Da, KLEpi{N, n_vt, parts}, a.stream);
     if (e != cudaSuccess) return e;
     RowStat *sa = static_cast<RowStat *>(a.stats_a), *sb = static_cast<RowStat *>(a.stats_b);
-    linear_kl_merge_kernel<<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>((int)a.N, n_vt, parts, a.kl,
-                                                                              p_is_a ? sa : sb, p_is_a ? sb : sa);
+    if (a.parts)
+        linear_kl_merge_kernel<true><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+            (int)a.N, n_vt, parts, nullptr, nullptr, nullptr, static_cast<PartialRec *>(a.parts));
+    else
+        linear_kl_merge_kernel<false><<<(unsigned)((a.N + 7) / 8), 256, 0, a.stream>>>(
+            (int)a.N, n_vt, parts, a.kl, p_is_a ? sa : sb, p_is_a ? sb : sa, nullptr);
     return cudaGetLastError();
 }
 
