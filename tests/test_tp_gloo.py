@@ -103,3 +103,37 @@ def test_gather_partials_two_ranks_merge_to_the_unsharded_entropy():
         assert np.array_equal(np.isnan(H), np.isnan(ref))
         fin = ~np.isnan(ref)
         assert np.allclose(H[fin], ref[fin], rtol=1e-13, atol=1e-13)
+
+
+def _reduce_rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from vocab_wide_logprobs_gb300.tp import reduce_dhidden
+        g = torch.Generator().manual_seed(100 + rank)
+        term = torch.randn(16, 64, generator=g).to(torch.bfloat16)   # this rank's dz_k . W_k
+        q.put((rank, term.float().numpy(), reduce_dhidden(term).float().numpy()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(180)
+def test_reduce_dhidden_two_ranks_sums_the_terms_in_fp32():
+    """The backward's exchange step of the sharded fused linear ops: every rank gets
+    bf16(fp32 term_0 + fp32 term_1)."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_reduce_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in procs:
+        r, term, total = q.get(timeout=150)
+        res[r] = (term, total)
+    for p in procs:
+        p.join(timeout=30)
+        assert p.exitcode == 0
+    ref = torch.from_numpy(res[0][0] + res[1][0]).to(torch.bfloat16).float().numpy()
+    for r in range(2):
+        assert np.array_equal(res[r][1], ref)

@@ -42,3 +42,33 @@ def tp_logprobs_fwd(x_shard, targets, vocab_start: int, group=None, err_word=Non
 def tp_kl_fwd(a_shard, b_shard, direction: int = api.KL_REVERSE, group=None):
     """KL over rows split across ranks: (kl, stats_a, stats_b) on every rank."""
     return api.vp_kl_merge(gather_partials(api.vp_kl_partial(a_shard, b_shard, direction), group), direction)
+
+
+# ---------------------------------------------------------------------------
+# The fused linear ops with the head's rows split across ranks ([P2] page "[Feat]
+# [Kernel] Add TP Fused linear logp Triton", "Implementation"): each rank holds
+# hidden in full and its shard of W's rows; the forward is one record gather,
+# and the backward's dhidden is the sum of every rank's term (reduce_dhidden).
+# ---------------------------------------------------------------------------
+def tp_linear_logp_fwd(hidden, w_shard, targets, vocab_start: int, group=None, err_word=None):
+    """logp of global target ids with the head's rows split across ranks: (logp, stats) on every rank."""
+    parts = api.vp_linear_logp_partial(hidden, w_shard, targets, vocab_start)
+    return api.vp_logprobs_merge(gather_partials(parts, group), err_word=err_word)
+
+
+def tp_linear_entropy_fwd(hidden, w_shard, group=None):
+    """Entropy of softmax(hidden @ W^T) with W's rows split across ranks: (H, stats) on every rank."""
+    return api.vp_entropy_merge(gather_partials(api.vp_linear_entropy_partial(hidden, w_shard), group))
+
+
+def tp_linear_kl_fwd(ha, wa_shard, hb, wb_shard, direction: int = api.KL_REVERSE, group=None):
+    """KL of two models whose heads' rows are split the same way across ranks: (kl, stats_a, stats_b)."""
+    parts = api.vp_linear_kl_partial(ha, wa_shard, hb, wb_shard, direction)
+    return api.vp_kl_merge(gather_partials(parts, group), direction)
+
+
+def reduce_dhidden(dh_term: torch.Tensor, group=None) -> torch.Tensor:
+    """dhidden from every rank's bf16 term dz_k . W_k: summed in fp32 across the ranks, rounded to bf16."""
+    total = dh_term.float()
+    dist.all_reduce(total, op=dist.ReduceOp.SUM, group=group)
+    return total.to(torch.bfloat16)
