@@ -267,6 +267,7 @@ def run_ours(args, rank, world, local_rank):
 
     jsd = jsd_bench(args, a, b, g, dev, peaks) if rank == 0 else None
     topk = topk_bench(args, a, dev, peaks) if rank == 0 else None
+    strided = strided_bench(args, dev, peaks, st, err, dx, da, db) if rank == 0 and not args.no_strided else None
 
     linear = None
     if not args.no_linear and rank == 0:
@@ -290,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "linear_logp": linear,
+            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "strided": strided, "linear_logp": linear,
         }
         print(json.dumps(line))
     if dist:
@@ -332,6 +333,55 @@ def jsd_bench(args, a, b, g, dev, peaks, beta=0.5):
                     "backward = one read of A and B and one write of dA and dB",
             "frac_of_copy_peak": {"fwd": round(2 * E2 / (tf * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                                   "bwd": round(2 * E2 / (tb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}
+
+
+def strided_bench(args, dev, peaks, st, err, dx, da, db):
+    """The step's eight calls on the strided workload: x[:, :-1] of [16, 513, 75968] bf16 tensors (8192
+    rows addressed with two strides, read in place), into the step's contiguous outputs."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    from vocab_wide_logprobs_gb300 import workloads
+    w = workloads.strided()
+    af, bf = w["a_full"].to(dev), w["b_full"].to(dev)
+    t, g = w["targets"].reshape(-1).to(dev), w["grad"].reshape(-1).to(dev)
+    del w
+    a, b = af[:, :-1], bf[:, :-1]
+    N, V = a.shape[0] * a.shape[1], a.shape[2]
+    R, F = vp.KL_REVERSE, vp.KL_FORWARD
+    calls = {
+        "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a, t, 0, err, st["lp"], st["lp_s"]),
+        "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a, t, st["lp_s"], g, 0, err, dx),
+        "entropy_fwd": lambda: vp.vp_entropy_fwd(a, st["H"], st["H_s"]),
+        "entropy_bwd": lambda: vp.vp_entropy_bwd(a, st["H_s"], g, dx),
+        "kl_rev_fwd": lambda: vp.vp_kl_fwd(a, b, R, st["kl"], st["sa"], st["sb"]),
+        "kl_rev_bwd": lambda: vp.vp_kl_bwd(a, b, R, st["sa"], st["sb"], g, da=da, db=db),
+        "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a, b, F, st["kl2"], st["sa2"], st["sb2"]),
+        "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a, b, F, st["sa2"], st["sb2"], g, da=da, db=db),
+    }
+    nbytes = algorithmic_bytes(N, V)
+    for _ in range(3):
+        for name in STEP_ORDER:
+            calls[name]()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 10))
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in STEP_ORDER}
+    per_op = {k: 0.0 for k in STEP_ORDER}
+    for _ in range(reps):
+        for name in STEP_ORDER:
+            ev[name][0].record()
+            calls[name]()
+            ev[name][1].record()
+        torch.cuda.synchronize()
+        for name in STEP_ORDER:
+            per_op[name] += ev[name][0].elapsed_time(ev[name][1]) / reps
+    ms = sum(per_op.values())
+    total = sum(nbytes.values())
+    del af, bf
+    return {"workload": "x[:, :-1] of [16, 513, 75968] bf16 tensors A and B: 8192 rows, 512 per outer index, "
+                        "read in place with two row strides; gradients written contiguous",
+            "ms_per_step": round(ms, 4), "value_gbs": round(total / (ms * 1e-3) / 1e9, 1),
+            "frac_of_copy_peak": round(total / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op.items()}}
 
 
 def topk_bench(args, a, dev, peaks, K=20):
@@ -642,6 +692,7 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-strided", action="store_true", help="skip the strided-view line")
     p.add_argument("--reference-rows", type=int, default=64)
     p.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (8192 is the benchmarked workload)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
