@@ -268,6 +268,7 @@ def run_ours(args, rank, world, local_rank):
     jsd = jsd_bench(args, a, b, g, dev, peaks) if rank == 0 else None
     topk = topk_bench(args, a, dev, peaks) if rank == 0 else None
     strided = strided_bench(args, dev, peaks, st, err, dx, da, db) if rank == 0 and not args.no_strided else None
+    stress = stress_bench(args, dev, peaks) if rank == 0 and not args.no_strided else None
 
     linear = None
     if not args.no_linear and rank == 0:
@@ -291,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "strided": strided, "linear_logp": linear,
+            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "strided": strided, "fp32_stress": stress, "linear_logp": linear,
         }
         print(json.dumps(line))
     if dist:
@@ -358,30 +359,67 @@ def strided_bench(args, dev, peaks, st, err, dx, da, db):
         "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a, b, F, st["kl2"], st["sa2"], st["sb2"]),
         "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a, b, F, st["sa2"], st["sb2"], g, da=da, db=db),
     }
-    nbytes = algorithmic_bytes(N, V)
+    line = _time_calls(args, calls, STEP_ORDER, algorithmic_bytes(N, V), peaks)
+    del af, bf
+    return {"workload": "x[:, :-1] of [16, 513, 75968] bf16 tensors A and B: 8192 rows, 512 per outer index, "
+                        "read in place with two row strides; gradients written contiguous", **line}
+
+
+def _time_calls(args, calls, order, nbytes, peaks):
+    """Per-call CUDA-event times of `calls` run in `order` (3 untimed rounds, then the mean of several), as
+    the step's ms, GB/s over the algorithmic bytes `nbytes` and per-call GB/s."""
+    import torch
     for _ in range(3):
-        for name in STEP_ORDER:
+        for name in order:
             calls[name]()
     torch.cuda.synchronize()
     reps = max(3, min(args.steps, 10))
-    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in STEP_ORDER}
-    per_op = {k: 0.0 for k in STEP_ORDER}
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in order}
+    per_op = {k: 0.0 for k in order}
     for _ in range(reps):
-        for name in STEP_ORDER:
+        for name in order:
             ev[name][0].record()
             calls[name]()
             ev[name][1].record()
         torch.cuda.synchronize()
-        for name in STEP_ORDER:
+        for name in order:
             per_op[name] += ev[name][0].elapsed_time(ev[name][1]) / reps
     ms = sum(per_op.values())
-    total = sum(nbytes.values())
-    del af, bf
-    return {"workload": "x[:, :-1] of [16, 513, 75968] bf16 tensors A and B: 8192 rows, 512 per outer index, "
-                        "read in place with two row strides; gradients written contiguous",
-            "ms_per_step": round(ms, 4), "value_gbs": round(total / (ms * 1e-3) / 1e9, 1),
+    total = sum(nbytes[k] for k in order)
+    return {"ms_per_step": round(ms, 4), "value_gbs": round(total / (ms * 1e-3) / 1e9, 1),
             "frac_of_copy_peak": round(total / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op.items()}}
+
+
+def stress_bench(args, dev, peaks):
+    """The fp32 numerics-stress workload: entropy and KL in both directions, fwd and bwd (gradients to
+    both inputs), on [8192, 75968] fp32 rows offset by 1e4 with 1% of B masked to -inf, so that KL(A||B) is
+    +inf on essentially every row and KL(B||A) runs the zero-weight path at a large offset."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    from vocab_wide_logprobs_gb300 import workloads
+    w = workloads.numerics_stress()
+    a, b, g = w["a"].to(dev), w["b"].to(dev), w["grad"].to(dev)
+    del w
+    N, V = a.shape
+    f32 = lambda: torch.empty(N, dtype=torch.float32, device=dev)
+    o = {k: f32() for k in ("H", "kl", "kl2")}
+    o.update({k: vp.rowstats(N, dev) for k in ("H_s", "sa", "sb", "sa2", "sb2")})
+    dx, da, db = torch.empty_like(a), torch.empty_like(a), torch.empty_like(a)
+    R, F = vp.KL_REVERSE, vp.KL_FORWARD
+    calls = {
+        "entropy_fwd": lambda: vp.vp_entropy_fwd(a, o["H"], o["H_s"]),
+        "entropy_bwd": lambda: vp.vp_entropy_bwd(a, o["H_s"], g, dx),
+        "kl_rev_fwd": lambda: vp.vp_kl_fwd(a, b, R, o["kl"], o["sa"], o["sb"]),
+        "kl_rev_bwd": lambda: vp.vp_kl_bwd(a, b, R, o["sa"], o["sb"], g, da=da, db=db),
+        "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a, b, F, o["kl2"], o["sa2"], o["sb2"]),
+        "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a, b, F, o["sa2"], o["sb2"], g, da=da, db=db),
+    }
+    order = [k for k in STEP_ORDER if k in calls]
+    line = _time_calls(args, calls, order, algorithmic_bytes(N, V, s=4), peaks)
+    del a, b, dx, da, db
+    return {"workload": "8192x75968 fp32, N(0, 9) + 1e4 on every row of A and B, 1% of B set to -inf; entropy "
+                        "and KL both directions, fwd+bwd", **line}
 
 
 def topk_bench(args, a, dev, peaks, K=20):
@@ -692,7 +730,7 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-strided", action="store_true", help="skip the strided-view line")
+    p.add_argument("--no-strided", action="store_true", help="skip the strided and fp32-stress lines")
     p.add_argument("--reference-rows", type=int, default=64)
     p.add_argument("--rows", type=int, default=N_ROWS, help="rows per GPU (8192 is the benchmarked workload)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
