@@ -277,6 +277,31 @@ linear_entropy_merge_kernel(int N, int n_vt, const EntTile *__restrict__ parts, 
     H[row] = flags ? qnan() : (float)(logS - c);
 }
 
+// s *= a for a double-float and a float a in [0, 1] (the product's rounding
+// error kept in lo).
+__device__ __forceinline__ void df_scale(DF &s, float a) {
+    const float hi = s.hi * a;
+    s.lo = fmaf(s.lo, a, fmaf(s.hi, a, -hi));
+    s.hi = hi;
+}
+
+// Moves KL sums (S_P, S_Q and W about the centres (cp, cq)) to the centres
+// (np, nq) >= (cp, cq): S_P *= e^{cp - np}, S_Q *= e^{cq - nq} and
+// W -> e^{cp - np} (W - ((np - cp) - (nq - cq)) S_P) (the merge rule of the
+// KL records). Sums about -inf centres are empty and only take the new centres.
+__device__ __forceinline__ void kl_recentre(DF &Sp, DF &Sq, DF &W, float &cp, float &cq, float np, float nq) {
+    if (cp != -INFINITY) {
+        const float dp = np - cp, dq = cq != -INFINITY ? nq - cq : 0.f;
+        df_add(W, -((dp - dq) * Sp.hi));
+        const float a = expf(-dp);
+        df_scale(W, a);
+        df_scale(Sp, a);
+    }
+    if (cq != -INFINITY) df_scale(Sq, expf(cq - nq));
+    cp = np;
+    cq = nq;
+}
+
 // kPart: the row's record over this vocabulary shard (vp_partial: both
 // maxima and sum-exps, W about the maxima, flags) instead of KL and the records.
 template <bool kPart>
@@ -288,26 +313,15 @@ linear_kl_merge_kernel(int N, int n_vt, const KLTile *__restrict__ parts, float 
     const int lane = threadIdx.x & 31;
     if (row >= N) return;
     const KLTile *p = parts + (int64_t)row * n_vt;
-    // each lane takes tiles lane, lane + 32, ... in that order; the loads of four
-    // of them are issued together (an absent tile reads as an empty one)
+    // One pass: each lane takes tiles lane, lane + 32, ... in that order (four
+    // loads in flight; an absent tile reads as an empty one) and keeps its sums
+    // about its own centres (cp, cq), the maxima of the tiles it has added so
+    // far, moving them up when a tile brings a larger maximum; the lanes' sums
+    // are then moved to the warp's centres and added in a fixed shuffle tree.
     constexpr int kB = 4;
     const KLTile empty{-INFINITY, 0.f, -INFINITY, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float Mp = -INFINITY, Mq = -INFINITY;
-    for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
-        float2 m[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const int i = i0 + 32 * u;
-            m[u] = i < n_vt ? make_float2(p[i].mp, p[i].mq) : make_float2(-INFINITY, -INFINITY);
-        }
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            Mp = fmaxf(Mp, m[u].x);
-            Mq = fmaxf(Mq, m[u].y);
-        }
-    }
-    Mp = warp_max(Mp);
-    Mq = warp_max(Mq);
+    float Mp = -INFINITY, Mq = -INFINITY;   // maxima over every tile: the records' m
+    float cp = -INFINITY, cq = -INFINITY;   // this lane's centres
     DF Sp{0.f, 0.f}, Sq{0.f, 0.f}, W{0.f, 0.f};
     bool nanp = false, nanq = false;
     for (int i0 = lane; i0 < n_vt; i0 += 32 * kB) {
@@ -317,27 +331,34 @@ linear_kl_merge_kernel(int N, int n_vt, const KLTile *__restrict__ parts, float 
 #pragma unroll
         for (int u = 0; u < kB; ++u) {
             const KLTile &t = tt[u];
+            Mp = fmaxf(Mp, t.mp);
+            Mq = fmaxf(Mq, t.mq);
             const bool bp = t.Sp != t.Sp || t.W != t.W || t.mp == INFINITY;
             const bool bq = t.Sq != t.Sq || t.mq == INFINITY;
             nanp |= bp;
             nanq |= bq;
-            if (bp || bq) continue;
+            if (bp || bq || !(t.Sp > 0.f || t.Sq > 0.f)) continue;
+            if (t.mp > cp || t.mq > cq) kl_recentre(Sp, Sq, W, cp, cq, fmaxf(cp, t.mp), fmaxf(cq, t.mq));
             if (t.Sq > 0.f) {
-                const float aq = expf(t.mq - Mq);
+                const float aq = expf(t.mq - cq);
                 if (aq != 0.f) df_add(Sq, aq * t.Sq);
             }
             if (t.Sp > 0.f) {
-                const float ap = expf(t.mp - Mp);
+                const float ap = expf(t.mp - cp);
                 if (ap != 0.f) {
                     df_add(Sp, ap * t.Sp);
-                    // W_i about the row centres: W_i - ((Mp - mp_i) - (Mq - mq_i)) S_P,i
-                    const float shift = (Mp - t.mp) - (Mq - t.mq);
+                    // W_i about the centres: W_i - ((cp - mp_i) - (cq - mq_i)) S_P,i
+                    const float shift = (cp - t.mp) - (cq - t.mq);
                     df_add(W, ap * t.W);
                     df_add(W, -(ap * shift) * t.Sp);
                 }
             }
         }
     }
+    Mp = warp_max(Mp);
+    Mq = warp_max(Mq);
+    const float wp = warp_max(cp), wq = warp_max(cq);   // the warp's centres
+    if (cp < wp || cq < wq) kl_recentre(Sp, Sq, W, cp, cq, wp, wq);
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) {
         df_add(Sp, shfl_xor(Sp, m));
