@@ -577,19 +577,23 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
     landed = [torch.cuda.Event() for _ in blocks]   # block k's inputs are on the device
     read = [torch.cuda.Event() for _ in blocks]     # block k's calls have read its inputs
 
+    # each block's host and device views, made once (the step then only issues calls)
+    ups = [[(dst[sl], src[sl]) for dst, src in ((a, h_a), (b, h_b), (t, h_t), (g, h_g))] for sl in blocks]
+    downs = [[(h_out[i, sl], st[key][sl]) for i, key in enumerate(("lp", "H", "kl", "kl2"))] for sl in blocks]
+
     def e2e_step():
-        for k, sl in enumerate(blocks):
+        for k in range(len(blocks)):
             with torch.cuda.stream(copy):
                 copy.wait_event(read[k])            # the previous step is done with these rows
-                for dst, src in ((a, h_a), (b, h_b), (t, h_t), (g, h_g)):
-                    vp.vp_upload(dst[sl], src[sl])
+                for dst, src in ups[k]:
+                    vp.vp_upload(dst, src)
                 landed[k].record(copy)
             stream.wait_event(landed[k])
             for name in ops:
                 calls[k][name]()
             read[k].record(stream)
-            for i, key in enumerate(("lp", "H", "kl", "kl2")):
-                vp.vp_download(h_out[i, sl], st[key][sl])
+            for dst, src in downs[k]:
+                vp.vp_download(dst, src)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -602,8 +606,10 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
     e2e_steps = max(3, min(args.steps, 10))
     e0.record(stream)
     copy.wait_event(e0)
+    h0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
+    enqueue_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps   # host time to issue one step's calls
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -614,7 +620,8 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
     return {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipeline": f"{chunks} row blocks; host-to-device copies (vp_upload) on a copy stream overlap the calls",
-            "h2d_link_gbs": round(h2d_gbs, 1), "host_buffers_numa_local": bool(numa)}
+            "h2d_link_gbs": round(h2d_gbs, 1), "host_buffers_numa_local": bool(numa),
+            "host_enqueue_ms_per_step": round(enqueue_ms, 3)}
 
 
 def _gpu_local_cpus(dev):
