@@ -128,17 +128,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
         for (int i = 0; i < 32; ++i) v[32 * k + i] = __uint_as_float(r[k][i]);
 }
 
-// Two 32-column loads (columns ta.. of a, tb.. of b) behind one wait.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
-    uint32_t ra[32], rb[32];
-    tmem_ld32_issue(ta, ra);
-    tmem_ld32_issue(tb, rb);
-    tmem_wait_ld();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        a[i] = __uint_as_float(ra[i]);
-        b[i] = __uint_as_float(rb[i]);
-    }
 }
 
 // --- 2-D tiled TMA --------------------------------------------------------
