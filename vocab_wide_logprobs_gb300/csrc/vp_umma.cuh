@@ -128,8 +128,6 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
         for (int i = 0; i < 32; ++i) v[32 * k + i] = __uint_as_float(r[k][i]);
 }
 
-}
-
 // --- 2-D tiled TMA --------------------------------------------------------
 // Box at element coordinates (x = inner, y = row) into shared memory; the inner
 // coordinate times the element size must be a multiple of 16 bytes.
