@@ -1,0 +1,59 @@
+"""Host logic of bench.py (no GPU): the algorithmic bytes behind its GB/s, the
+clock summary that accepts or rejects a run, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_algorithmic_bytes_of_the_step():
+    N, V = 8192, 75968
+    E = N * V * 2
+    b = bench.algorithmic_bytes(N, V)
+    assert sum(b.values()) == 18 * E                     # 22.40 GB per step at bf16
+    assert b["logprobs_fwd"] == E and b["logprobs_bwd"] == 2 * E
+    assert b["kl_rev_fwd"] == 2 * E and b["kl_fwd_bwd"] == 4 * E   # read A and B; write dA and dB too
+    assert sum(bench.algorithmic_bytes(N, V, s=4).values()) == 2 * sum(b.values())
+
+
+def test_clock_summary_takes_loaded_samples_and_throttle_reasons():
+    c = bench.ClockSampler(0)
+    c.proc = object()                                   # as if nvidia-smi had run
+    rows = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 2070, 2070, 910.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 345, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active",   # idle: left out
+            "0, 1980, 2070, 1200.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "garbled line"]
+    c.tmp.write("\n".join(rows) + "\n")
+    c.tmp.flush()
+    s = c.summary()
+    os.unlink(c.tmp.name)
+    assert s["sm_max_mhz"] == 2070.0 and s["sm_mhz"] == 2070.0 and s["samples"] == 4
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_summary_reports_a_thermal_slowdown():
+    c = bench.ClockSampler(0)
+    c.proc = object()
+    c.tmp.write("0, 1500, 2070, 1300.0, 0x40, Not Active, Active, Not Active, Not Active\n")
+    c.tmp.flush()
+    s = c.summary()
+    os.unlink(c.tmp.name)
+    assert s["reasons"] == ["hw_thermal_slowdown"] and s["sm_mhz"] == 1500.0
+
+
+def test_reference_arm_prints_the_contract_line():
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3",
+                          "--reference-rows", "2"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["n_gpus"] == 1 and line["steps"] == 1 and line["warmup"] == 3 and line["higher_is_better"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"] == line["cpu_baseline"]["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["metric"] == bench.METRIC
