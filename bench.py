@@ -97,6 +97,21 @@ def traffic_for(kernel_key: str):
     return e.get("bytes_per_launch")
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (a job's time is its slowest rank's); x itself on one rank."""
+    if not dist:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate_gbs(step_bytes: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every rank's step bytes over the slowest rank's step time (weak scaling)."""
+    return step_bytes * world / (ms_per_step * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
@@ -241,15 +256,11 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    if dist:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
     per_op_ms = {name: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                  for i, name in enumerate(ops)}
     ms_per_step = elapsed_ms / args.steps
-    value = step_bytes * world / (ms_per_step * 1e-3) / 1e9
+    value = job_rate_gbs(step_bytes, world, ms_per_step)
 
     # dominant kernel (largest share of the step) and its roofline
     dom = max(per_op_ms, key=per_op_ms.get)
@@ -612,12 +623,8 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
     enqueue_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps   # host time to issue one step's calls
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    return {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    return {"value": round(job_rate_gbs(step_bytes, world, e2e_ms), 1), "unit": UNIT,
             "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipeline": f"{chunks} row blocks; host-to-device copies (vp_upload) on a copy stream overlap the calls",
             "h2d_link_gbs": round(h2d_gbs, 1), "host_buffers_numa_local": bool(numa),

@@ -57,3 +57,38 @@ def test_reference_arm_prints_the_contract_line():
     assert line["e2e"]["value"] == line["value"] == line["cpu_baseline"]["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["metric"] == bench.METRIC
+
+
+def _max_rank(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 3.0 + rank * 0.5                           # rank 1 is the slower one
+        worst = bench.max_over_ranks(ms, dist, "cpu")
+        q.put((rank, worst, bench.job_rate_gbs(22.4e9, world, worst)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_agree_on_the_slowest_time_and_the_job_rate():
+    """The N > 1 timing path of bench.py over gloo: every rank takes the max of the ranks'
+    times, and the whole-job rate counts both ranks' bytes over that time."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_max_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict((r, (w, g)) for r, w, g in (q.get(timeout=150) for _ in procs))
+    for p in procs:
+        p.join(timeout=30)
+        assert p.exitcode == 0
+    for r in range(2):
+        assert res[r][0] == 3.5
+        assert abs(res[r][1] - 2 * 22.4e9 / 3.5e-3 / 1e9) < 1e-9
+    assert bench.max_over_ranks(1.25, None, "cpu") == 1.25
