@@ -159,3 +159,35 @@ def test_linear_sharded_single_shard_equals_unsharded():
     parity.check_out(H, rH.double().cpu().numpy(), "K = 1 H")
     d, rd = vp.decode_rowstats(st), vp.decode_rowstats(rst)
     assert torch.equal(d["m"], rd["m"])
+
+
+def test_linear_partial_records_match_the_oracle_shard_sums():
+    """Each shard's records field by field against the oracle's sums over the same columns of the
+    fp64 logits: maxima and target logits at the output tolerance, S and W to 5e-5 (the GEMM's
+    logits are fp32 accumulations, so the records are not bitwise the fp64 ones)."""
+    D = 128
+    h, W, _ = _model(91, N, V, D)
+    t = _targets(92)
+    hd, Wd, td = h.to(DEV), W.to(DEV), t.to(DEV)
+    z = oracle.linear_logits(parity.to64(h), parity.to64(W))
+    tt = t.numpy()
+    for v0, v1 in CUTS:
+        lrec = vp.decode_partials(vp.vp_linear_logp_partial(hd, Wd[v0:v1], td, vocab_start=v0))
+        erec = vp.decode_partials(vp.vp_linear_entropy_partial(hd, Wd[v0:v1]))
+        torch.cuda.synchronize()
+        ref = oracle.shard_stats(z, v0, v1)                       # m, S, W, bad
+        assert not ref[:, 3].any()
+        for rec, name in ((lrec, "logp"), (erec, "entropy")):
+            tag = f"{name} shard [{v0}, {v1})"
+            parity.check_out(rec["m"], ref[:, 0], f"{tag} max")
+            assert np.allclose(rec["S"].cpu().numpy(), ref[:, 1], rtol=5e-5, atol=0), f"{tag} S"
+            assert (rec["flags"].cpu().numpy() & vp.PART_NANINF == 0).all()
+        Wg = erec["W"].cpu().numpy()
+        assert (np.abs(Wg - ref[:, 2]) <= 5e-5 * (np.abs(ref[:, 2]) + ref[:, 1])).all(), "shard W"
+        assert (lrec["W"].cpu().numpy() == 0).all()
+        has = (tt >= v0) & (tt < v1)
+        lfl = lrec["flags"].cpu().numpy()
+        assert (((lfl & vp.PART_HAS_TARGET) != 0) == has).all()
+        assert (((lfl & vp.PART_IGNORED) != 0) == (tt < 0)).all()
+        rows = np.nonzero(has)[0]
+        parity.check_out(lrec["z_t"][torch.from_numpy(rows).to(DEV)], z[rows, tt[rows]], "target logit")
