@@ -137,3 +137,13 @@ def test_reduce_dhidden_two_ranks_sums_the_terms_in_fp32():
     ref = torch.from_numpy(res[0][0] + res[1][0]).to(torch.bfloat16).float().numpy()
     for r in range(2):
         assert np.array_equal(res[r][1], ref)
+
+
+def test_gather_partials_rejects_records_of_the_wrong_layout():
+    """The record layout is checked before any collective (no process group needed)."""
+    from vocab_wide_logprobs_gb300.api import VPError
+    from vocab_wide_logprobs_gb300.tp import gather_partials
+    for bad in (torch.zeros(4, 4, dtype=torch.float64), torch.zeros(4, 5, dtype=torch.float32),
+                torch.zeros(2, 4, 5, dtype=torch.float64)):
+        with pytest.raises(VPError):
+            gather_partials(bad)
