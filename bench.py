@@ -65,12 +65,15 @@ KERNEL_OF = {  # op -> kernel name prefix in profiles (mangled names contain the
 
 
 def measured_peaks() -> dict:
+    """Copy bandwidth and bf16 tensor rates (burst and sustained) measured on this machine's GPUs, else the
+    fallback figures of one earlier GB300 measurement."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": d["hbm_gbs"], "src": "measured"}
-    return {"hbm_gbs": 6800.0, "src": "fallback"}
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
 
 
 def source_hash(files=None) -> str:
@@ -206,19 +209,22 @@ def run_ours(args, rank, world, local_rank):
 
     R, F = vp.KL_REVERSE, vp.KL_FORWARD
 
-    def make_calls(sl):
-        """The step's eight calls on the rows `sl` of every buffer."""
-        a_, b_, t_, g_, dx_, da_, db_ = a[sl], b[sl], t[sl], g[sl], dx[sl], da[sl], db[sl]
+    def make_calls(sl, grads=None):
+        """The step's eight calls on the rows `sl` of every buffer. `grads` gives each backward its own
+        gradient buffers (keys of GRAD_OUTPUTS); by default the backwards share dx, da and db."""
+        gr = grads or {"lp": dx, "H": dx, "ra": da, "rb": db, "fa": da, "fb": db}
+        a_, b_, t_, g_ = a[sl], b[sl], t[sl], g[sl]
+        d_ = {k: v[sl] for k, v in gr.items()}
         s_ = {k: v[sl] for k, v in st.items()}
         return {
             "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a_, t_, 0, err, s_["lp"], s_["lp_s"]),
-            "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a_, t_, s_["lp_s"], g_, 0, err, dx_),
+            "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a_, t_, s_["lp_s"], g_, 0, err, d_["lp"]),
             "entropy_fwd": lambda: vp.vp_entropy_fwd(a_, s_["H"], s_["H_s"]),
-            "entropy_bwd": lambda: vp.vp_entropy_bwd(a_, s_["H_s"], g_, dx_),
+            "entropy_bwd": lambda: vp.vp_entropy_bwd(a_, s_["H_s"], g_, d_["H"]),
             "kl_rev_fwd": lambda: vp.vp_kl_fwd(a_, b_, R, s_["kl"], s_["sa"], s_["sb"]),
-            "kl_rev_bwd": lambda: vp.vp_kl_bwd(a_, b_, R, s_["sa"], s_["sb"], g_, da=da_, db=db_),
+            "kl_rev_bwd": lambda: vp.vp_kl_bwd(a_, b_, R, s_["sa"], s_["sb"], g_, da=d_["ra"], db=d_["rb"]),
             "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a_, b_, F, s_["kl2"], s_["sa2"], s_["sb2"]),
-            "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a_, b_, F, s_["sa2"], s_["sb2"], g_, da=da_, db=db_),
+            "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a_, b_, F, s_["sa2"], s_["sb2"], g_, da=d_["fa"], db=d_["fb"]),
         }
 
     calls = make_calls(slice(None))
@@ -274,7 +280,11 @@ def run_ours(args, rank, world, local_rank):
     # the end-to-end step right after the device-timed one, before the other workloads
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev)
+        per_row = end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev,
+                             with_grads=False)
+        e2e = end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev,
+                         with_grads=True)
+        e2e["per_row_outputs_only"] = per_row
 
     jsd = jsd_bench(args, a, b, g, dev, peaks) if rank == 0 else None
     topk = topk_bench(args, a, dev, peaks) if rank == 0 else None
@@ -473,13 +483,16 @@ def _time_ms(fn, reps, idle_s=0.0):
 
 
 IDLE_S = 1.0   # idle seconds before each timed burst of the linear ops
+SUSTAINED_CALLS = 20   # back-to-back calls of each linear op in the sustained figures
 
 
-def linear_bench(args, dev, N=8192, V=75968, D=4096):
-    """Fused linear ops on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16): logp, entropy and
-    KL against a second model of the same shape, forward and backward. Each op is timed as a burst, after
-    IDLE_S seconds of idle GPU, against the measured burst bf16 peak: a long GEMM heats the part and the
-    power cap then lowers the clock of whatever runs next, or of its own later calls."""
+def linear_bench(args, dev, N=8192, V=75968, D=4096, sustained=True):
+    """Fused linear ops on the linear workload (hidden [8192, 4096], W [75968, 4096] bf16): logp, entropy,
+    KL against a second model of the same shape and the generalized JSD, forward and backward, the
+    backwards at both precisions (exact: dz as a bf16 pair, the default; fast: dz rounded to bf16).
+    Each op is timed as a burst of three calls after IDLE_S seconds of idle GPU, against the measured
+    burst bf16 peak; with `sustained`, also as SUSTAINED_CALLS back-to-back calls, against the measured
+    sustained peak (a training step runs these GEMMs back to back under the power cap)."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     from vocab_wide_logprobs_gb300 import workloads
@@ -488,34 +501,18 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     g = w["grad"].to(dev)
     logp = torch.empty(N, dtype=torch.float32, device=dev)
     st = vp.rowstats(N, dev)
-    ws = torch.empty(vp.vp_linear_logp_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
-    for _ in range(2):
-        vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws)
-    reps = 3   # a burst of three calls (the longest burst, three KL backwards, is about 50 ms)
-    ms = _time_ms(lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws), reps, IDLE_S)
-    dh = torch.empty_like(h)
-    dW = torch.empty_like(W)
-    wsb = torch.empty(vp.vp_linear_logp_bwd_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
-    ms_b = _time_ms(lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb), 3, IDLE_S)
-    del wsb
-    flops = 2.0 * N * V * D
-    peak = None
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        with open(p) as f:
-            peak = json.load(f).get("bf16_tflops")
-    tf = flops / (ms * 1e-3) / 1e12
-    tfb = 3 * flops / (ms_b * 1e-3) / 1e12
-    frac = lambda x: round(x / peak, 4) if peak else None
+    peaks = measured_peaks()
+    burst_peak, sus_peak = peaks.get("bf16_tflops"), peaks.get("bf16_tflops_sustained")
+    unit = 2.0 * N * V * D          # one GEMM of the logits' shape
+    EXACT, FAST = vp.GRAD_EXACT, vp.GRAD_FAST
+    reps = 3   # a burst of three calls
 
-    # entropy of the same model
+    ws = torch.empty(vp.vp_linear_logp_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
+    dh, dW = torch.empty_like(h), torch.empty_like(W)
+    wsb = torch.empty(vp.vp_linear_logp_bwd_workspace_size(N, V, D), dtype=torch.uint8, device=dev)
     H = torch.empty(N, dtype=torch.float32, device=dev)
     wse = torch.empty(max(vp._lib.lib().vp_linear_entropy_bwd_workspace_size(N, V, D),
                           vp._lib.lib().vp_linear_entropy_workspace_size(N, V, D)), dtype=torch.uint8, device=dev)
-    ms_ef = _time_ms(lambda: vp.vp_linear_entropy_fwd(h, W, H=H, stats=st, workspace=wse), reps, IDLE_S)
-    ms_eb = _time_ms(lambda: vp.vp_linear_entropy_bwd(h, W, st, g, dhidden=dh, dW=dW, workspace=wse), 3, IDLE_S)
-    del wse
-    # KL(A||B) against a second model (teacher) of the same shape, gradients to both models
     tw = workloads.linear(seed=14, N=N, V=V, D=D)
     hb, Wb = tw["hidden"].to(dev), tw["weight"].to(dev)
     del tw
@@ -523,45 +520,97 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096):
     sb = vp.rowstats(N, dev)
     wsk = torch.empty(vp._lib.lib().vp_linear_kl_bwd_workspace_size(N, V, D, D), dtype=torch.uint8, device=dev)
     outs = [dh, dW, torch.empty_like(hb), torch.empty_like(Wb)]
-    ms_kf = _time_ms(lambda: vp.vp_linear_kl_fwd(h, W, hb, Wb, vp.KL_REVERSE, kl=kl, stats_a=st, stats_b=sb,
-                                                 workspace=wsk), reps, IDLE_S)
-    ms_kb = _time_ms(lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, vp.KL_REVERSE, st, sb, g, outs=outs, workspace=wsk), 3,
-                     IDLE_S)
-    # generalized JSD (beta = 0.5) of the same two models: two forward passes of the dual GEMM
-    ms_jf = _time_ms(lambda: vp.vp_linear_jsd_fwd(h, W, hb, Wb, 0.5, jsd=kl, stats_a=st, stats_b=sb, workspace=wsk),
-                     reps, IDLE_S)
-    ms_jb = _time_ms(lambda: vp.vp_linear_jsd_bwd(h, W, hb, Wb, 0.5, st, sb, g, outs=outs, workspace=wsk), 3, IDLE_S)
-    del wsk, outs, hb, Wb
+    R = vp.KL_REVERSE
+    # (name, call, GEMM units of 2 N V D flops)
+    ops = [
+        ("logp_fwd", lambda: vp.vp_linear_logp_fwd(h, W, t, logp=logp, stats=st, workspace=ws), 1),
+        ("logp_bwd", lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb), 5),
+        ("logp_bwd_fast", lambda: vp.vp_linear_logp_bwd(h, W, t, st, g, dhidden=dh, dW=dW, workspace=wsb,
+                                                        precision=FAST), 3),
+        ("entropy_fwd", lambda: vp.vp_linear_entropy_fwd(h, W, H=H, stats=st, workspace=wse), 1),
+        ("entropy_bwd", lambda: vp.vp_linear_entropy_bwd(h, W, st, g, dhidden=dh, dW=dW, workspace=wse), 5),
+        ("entropy_bwd_fast", lambda: vp.vp_linear_entropy_bwd(h, W, st, g, dhidden=dh, dW=dW, workspace=wse,
+                                                              precision=FAST), 3),
+        ("kl_fwd", lambda: vp.vp_linear_kl_fwd(h, W, hb, Wb, R, kl=kl, stats_a=st, stats_b=sb, workspace=wsk), 2),
+        ("kl_bwd", lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, R, st, sb, g, outs=outs, workspace=wsk), 10),
+        ("kl_bwd_fast", lambda: vp.vp_linear_kl_bwd(h, W, hb, Wb, R, st, sb, g, outs=outs, workspace=wsk,
+                                                    precision=FAST), 6),
+        ("jsd_fwd", lambda: vp.vp_linear_jsd_fwd(h, W, hb, Wb, 0.5, jsd=kl, stats_a=st, stats_b=sb, workspace=wsk),
+         4),
+        ("jsd_bwd", lambda: vp.vp_linear_jsd_bwd(h, W, hb, Wb, 0.5, st, sb, g, outs=outs, workspace=wsk), 10),
+        ("jsd_bwd_fast", lambda: vp.vp_linear_jsd_bwd(h, W, hb, Wb, 0.5, st, sb, g, outs=outs, workspace=wsk,
+                                                      precision=FAST), 6),
+    ]
+    # the records each backward reads: the matching forward runs right before it
+    fwd_of = {"logp": 0, "entropy": 3, "kl": 6, "jsd": 9}
+    burst, sus = {}, {}
+    for k, (name, fn, units) in enumerate(ops):
+        if not name.endswith("_fwd"):
+            ops[fwd_of[name.split("_")[0]]][1]()
+        ms = _time_ms(fn, reps, IDLE_S)
+        burst[name] = (ms, units * unit / (ms * 1e-3) / 1e12)
+    clocks = None
+    if sustained:
+        with ClockSampler(dev.index or 0) as ck:
+            for name, fn, units in ops:
+                if name.endswith("_fast"):
+                    continue
+                if not name.endswith("_fwd"):
+                    ops[fwd_of[name.split("_")[0]]][1]()
+                ms = _time_ms(fn, SUSTAINED_CALLS)
+                sus[name] = (ms, units * unit / (ms * 1e-3) / 1e12)
+        clocks = ck.summary()
+    del ws, wsb, wse, wsk, outs, hb, Wb
     torch.cuda.empty_cache()
 
-    def line(fwd_ms, bwd_ms, fwd_gemms, bwd_gemms, what):
-        a, b = fwd_gemms * flops / (fwd_ms * 1e-3) / 1e12, bwd_gemms * flops / (bwd_ms * 1e-3) / 1e12
-        return {"workload": what, "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
-                "fwd_tflops": round(a, 1), "bwd_tflops": round(b, 1), "fwd_frac": frac(a), "bwd_frac": frac(b),
-                "flops": {"fwd": fwd_gemms * flops, "bwd": bwd_gemms * flops}}
+    frac = lambda x, pk: round(x / pk, 4) if pk else None
 
-    return {"workload": f"hidden [{N},{D}] x W [{V},{D}] bf16, logp of uniform targets", "fwd_ms": round(ms, 4),
-            "bwd_ms": round(ms_b, 4),
-            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak, "unit": "TFLOP/s",
-                         "peak_src": "measured bf16 burst" if peak else None,
-                         "frac": frac(tf), "flops": flops},
-            "bwd_roofline": {"bound": "tensor", "achieved": round(tfb, 1), "peak": peak, "unit": "TFLOP/s",
-                             "frac": frac(tfb), "flops": 3 * flops,
-                             "note": "three GEMMs of 2NVD each (logits recomputed, dhidden, dW)"},
-            "entropy": line(ms_ef, ms_eb, 1, 3, "entropy of softmax(h W^T); backward: logits, dhidden, dW"),
-            "kl": line(ms_kf, ms_kb, 2, 6, "KL(A||B) of two models of this shape; forward: both logits tiles; "
-                       "backward: both logits tiles, dhidden and dW of both models"),
-            "jsd": line(ms_jf, ms_jb, 4, 6, "generalized JSD (beta = 0.5) of the two models; forward: two passes "
-                        "of both logits tiles; backward: as for KL")}
+    def entry(op, fwd_units, bwd_units, fast_units, what):
+        f, b, bf = burst[op + "_fwd"], burst[op + "_bwd"], burst[op + "_bwd_fast"]
+        e = {"workload": what, "fwd_ms": round(f[0], 4), "bwd_ms": round(b[0], 4), "bwd_fast_ms": round(bf[0], 4),
+             "fwd_tflops": round(f[1], 1), "bwd_tflops": round(b[1], 1), "bwd_fast_tflops": round(bf[1], 1),
+             "fwd_frac": frac(f[1], burst_peak), "bwd_frac": frac(b[1], burst_peak),
+             "bwd_fast_frac": frac(bf[1], burst_peak),
+             "flops": {"fwd": fwd_units * unit, "bwd": bwd_units * unit, "bwd_fast": fast_units * unit}}
+        if sus:
+            sf, sbw = sus[op + "_fwd"], sus[op + "_bwd"]
+            e["sustained"] = {"calls": SUSTAINED_CALLS, "fwd_ms": round(sf[0], 4), "bwd_ms": round(sbw[0], 4),
+                              "fwd_tflops": round(sf[1], 1), "bwd_tflops": round(sbw[1], 1),
+                              "fwd_frac": frac(sf[1], sus_peak), "bwd_frac": frac(sbw[1], sus_peak),
+                              "peak": sus_peak, "peak_src": "measured bf16 sustained"}
+        return e
+
+    out = entry("logp", 1, 5, 3, f"hidden [{N},{D}] x W [{V},{D}] bf16, logp of uniform targets")
+    out["roofline"] = {"bound": "tensor", "achieved": out["fwd_tflops"], "peak": burst_peak, "unit": "TFLOP/s",
+                       "peak_src": "measured bf16 burst" if burst_peak else None, "frac": out["fwd_frac"],
+                       "flops": unit}
+    out["bwd_roofline"] = {"bound": "tensor", "achieved": out["bwd_tflops"], "peak": burst_peak, "unit": "TFLOP/s",
+                           "frac": out["bwd_frac"], "flops": 5 * unit,
+                           "note": "exact precision: logits recomputed (2NVD), dhidden and dW with dz_hi and dz_lo "
+                                   "(4NVD each); fast precision: 3 GEMMs of 2NVD"}
+    out["entropy"] = entry("entropy", 1, 5, 3, "entropy of softmax(h W^T); backward: logits, dhidden, dW")
+    out["kl"] = entry("kl", 2, 10, 6, "KL(A||B) of two models of this shape; forward: both logits tiles; "
+                      "backward: both logits tiles, dhidden and dW of both models")
+    out["jsd"] = entry("jsd", 4, 10, 6, "generalized JSD (beta = 0.5) of the two models; forward: two passes of "
+                       "both logits tiles; backward: as for KL")
+    out["sustained_clocks"] = clocks
+    return out
 
 
-def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev, chunks=8):
+GRAD_OUTPUTS = ("lp", "H", "ra", "rb", "fa", "fb")   # dlogits of logprobs, entropy; dA, dB of both KLs
+
+
+def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist, stream, dev, chunks=8,
+               with_grads=True):
     """The step end to end through the public API with host buffers.
 
     Every step copies the step's inputs from pinned host memory, runs the eight
-    calls and reads the per-row results back. Rows are independent, so the step
-    is cut into `chunks` row blocks: block k's host-to-device copy runs on a copy
-    stream while the calls of block k - 1 run on the compute stream."""
+    calls and copies the step's results back to pinned host memory: the four
+    per-row outputs and, with `with_grads`, all six gradients the step produces
+    (each backward then writes its own gradient buffer). Rows are independent,
+    so the step is cut into `chunks` row blocks: block k's host-to-device copy
+    runs on an upload stream and block k - 1's results go back on a download
+    stream while the calls of the blocks between run on the compute stream."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     N = a.shape[0]
@@ -575,36 +624,45 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
         h_a, h_b = w["a"].pin_memory(), w["b"].pin_memory()
         h_t, h_g = w["targets"].pin_memory(), w["grad"].pin_memory()
         h_out = torch.empty(4, N, dtype=torch.float32).pin_memory()
+        h_grads = ({k: torch.empty(a.shape, dtype=a.dtype, pin_memory=True) for k in GRAD_OUTPUTS}
+                   if with_grads else {})
     finally:
         if saved:
             os.sched_setaffinity(0, saved)
+    grads = {k: torch.empty_like(a) for k in GRAD_OUTPUTS} if with_grads else None
     h2d = sum(x.numel() * x.element_size() for x in (h_a, h_b, h_t, h_g))
-    d2h = h_out.numel() * 4
+    d2h = h_out.numel() * 4 + sum(x.numel() * x.element_size() for x in h_grads.values())
     chunks = max(1, min(chunks, N))
     bounds = [N * k // chunks for k in range(chunks + 1)]
     blocks = [slice(bounds[k], bounds[k + 1]) for k in range(chunks)]
-    calls = [make_calls(sl) for sl in blocks]
-    copy = torch.cuda.Stream(dev)
+    calls = [make_calls(sl, grads) for sl in blocks]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     landed = [torch.cuda.Event() for _ in blocks]   # block k's inputs are on the device
-    read = [torch.cuda.Event() for _ in blocks]     # block k's calls have read its inputs
+    read = [torch.cuda.Event() for _ in blocks]     # block k's calls are done (inputs read, results written)
+    fetched = [torch.cuda.Event() for _ in blocks]  # block k's results are in host memory
 
     # each block's host and device views, made once (the step then only issues calls)
     ups = [[(dst[sl], src[sl]) for dst, src in ((a, h_a), (b, h_b), (t, h_t), (g, h_g))] for sl in blocks]
-    downs = [[(h_out[i, sl], st[key][sl]) for i, key in enumerate(("lp", "H", "kl", "kl2"))] for sl in blocks]
+    downs = [[(h_out[i, sl], st[key][sl]) for i, key in enumerate(("lp", "H", "kl", "kl2"))]
+             + [(h_grads[k][sl], grads[k][sl]) for k in h_grads] for sl in blocks]
 
     def e2e_step():
         for k in range(len(blocks)):
-            with torch.cuda.stream(copy):
-                copy.wait_event(read[k])            # the previous step is done with these rows
+            with torch.cuda.stream(up):
+                up.wait_event(read[k])              # the previous step is done with these rows
                 for dst, src in ups[k]:
                     vp.vp_upload(dst, src)
-                landed[k].record(copy)
+                landed[k].record(up)
             stream.wait_event(landed[k])
+            stream.wait_event(fetched[k])           # the previous step's results of these rows are out
             for name in ops:
                 calls[k][name]()
             read[k].record(stream)
-            for dst, src in downs[k]:
-                vp.vp_download(dst, src)
+            with torch.cuda.stream(down):
+                down.wait_event(read[k])
+                for dst, src in downs[k]:
+                    vp.vp_download(dst, src)
+                fetched[k].record(down)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -616,19 +674,26 @@ def end_to_end(args, w, a, b, t, g, st, ops, make_calls, step_bytes, world, dist
     h2d_gbs = a.numel() * a.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9
     e2e_steps = max(3, min(args.steps, 10))
     e0.record(stream)
-    copy.wait_event(e0)
+    up.wait_event(e0)
     h0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
     enqueue_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps   # host time to issue one step's calls
+    for ev in fetched:
+        stream.wait_event(ev)                       # the timed region ends when the last results are out
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
-    return {"value": round(job_rate_gbs(step_bytes, world, e2e_ms), 1), "unit": UNIT,
-            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": f"{chunks} row blocks; host-to-device copies (vp_upload) on a copy stream overlap the calls",
-            "h2d_link_gbs": round(h2d_gbs, 1), "host_buffers_numa_local": bool(numa),
-            "host_enqueue_ms_per_step": round(enqueue_ms, 3)}
+    out = {"value": round(job_rate_gbs(step_bytes, world, e2e_ms), 1), "unit": UNIT,
+           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "results_copied_back": ("per-row outputs and all six gradients (dlogits of logprobs and entropy, "
+                                   "dA and dB of both KL directions)") if with_grads else "per-row outputs only",
+           "pipeline": f"{chunks} row blocks; uploads (vp_upload) and downloads (vp_download) on their own "
+                       "streams overlap the calls",
+           "h2d_link_gbs": round(h2d_gbs, 1), "host_buffers_numa_local": bool(numa),
+           "host_enqueue_ms_per_step": round(enqueue_ms, 3)}
+    del grads, h_grads
+    return out
 
 
 def _gpu_local_cpus(dev):
@@ -736,6 +801,59 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+def _free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def rank_command(n: int, argv, port: int) -> list:
+    """torchrun command that starts n ranks of this script on one node (rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + list(argv)
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """`--gpus n` without a launcher: start n ranks of this script, one per GPU, and return their
+    exit status. Each rank times its own batch (rows are independent: replicas with no data-path
+    collective); NCCL's initialisation log goes to stderr so that the rank count can be checked."""
+    env = dict(os.environ)
+    env.setdefault("NCCL_DEBUG", "INFO")
+    env.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
+    env.setdefault("NCCL_DEBUG_FILE", "/dev/stderr")
+    env.setdefault("OMP_NUM_THREADS", "1")
+    return subprocess.call(rank_command(n, argv, _free_port()), env=env, cwd=ROOT)
+
+
+def launch_check(rank: int, world: int, local_rank: int):
+    """Rank plumbing without GPU work: every rank joins the process group (NCCL on GPUs, gloo
+    otherwise), the max over ranks is taken as for a timing, and rank 0 prints who took part."""
+    import torch
+    import torch.distributed as dist
+    cuda = torch.cuda.is_available()
+    dev = torch.device("cuda", local_rank) if cuda else torch.device("cpu")
+    if world > 1:
+        if cuda:
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=dev)
+        else:
+            dist.init_process_group("gloo")
+    ranks = torch.zeros(world, dtype=torch.float64, device=dev)
+    ranks[rank] = 1.0
+    if world > 1:
+        dist.all_reduce(ranks)
+    slowest = max_over_ranks(float(rank + 1), dist if world > 1 else None, dev)
+    if rank == 0:
+        print(json.dumps({"launch_check": True, "n_gpus": world, "ranks_seen": int(ranks.sum().item()),
+                          "max_over_ranks": slowest, "backend": (dist.get_backend() if world > 1 else None)}))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -752,11 +870,20 @@ def main():
     p.add_argument("--linear-only", action="store_true",
                    help="only the fused linear-logp measurement (profiling of the GEMM kernels)")
     p.add_argument("--linear-rows", type=int, default=8192, help="hidden rows of the linear-logp workload")
+    p.add_argument("--launch-check", action="store_true",
+                   help="only start the ranks, take the max over them and print who took part (no GPU work)")
     args = p.parse_args()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
-    if args.impl == "reference":
+    if args.gpus != world:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one rank per GPU", file=sys.stderr)
+        sys.exit(2)
+    if args.launch_check:
+        launch_check(rank, world, local_rank)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)

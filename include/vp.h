@@ -376,20 +376,39 @@ VP_API vp_status vp_linear_logp_fwd(const void *hidden, const void *weight, int6
                                     int64_t vocab_start, const int64_t *targets, float *logp, vp_rowstat *stats,
                                     void *workspace, size_t workspace_bytes, int32_t *err_word, vp_stream stream);
 
-/* Bytes of device workspace vp_linear_logp_bwd needs: dz of one vocabulary
- * chunk (bf16 [N, vc], vc = 32768 columns for N <= 8192, 16384 for N <= 16384,
- * else 8192, at most V rounded up to 256) and an fp32 accumulator of dhidden
- * ([N, D]). 0 for invalid sizes. */
+/* Precision of the fused linear backwards (the `precision` argument of
+ * vp_linear_logp_bwd, vp_linear_entropy_bwd, vp_linear_kl_bwd and
+ * vp_linear_jsd_bwd). dz = dL/dlogits is formed in fp32 in the epilogue of
+ * the recomputed logits tile, and the two gradient GEMMs (dhidden = dz . W,
+ * dW = dz^T . h) run on bf16 tensor cores:
+ *   VP_GRAD_EXACT  dz is carried as the pair dz_hi = bf16(dz), dz_lo =
+ *                  bf16(dz - dz_hi) (about 16 significant bits), and each
+ *                  gradient GEMM adds the dz_lo product into the same fp32
+ *                  accumulator: the gradients then carry only the fp32
+ *                  accumulation error, and the two gradient GEMMs cost twice
+ *                  the work (10 N V D flops for the whole backward instead of
+ *                  6 N V D);
+ *   VP_GRAD_FAST   dz is rounded to bf16 once (relative error up to 2^-9 per
+ *                  term of the dot products). */
+#define VP_GRAD_EXACT 0
+#define VP_GRAD_FAST  1
+
+/* Bytes of device workspace vp_linear_logp_bwd needs (for either precision):
+ * dz of one vocabulary chunk twice over (bf16 [N, vc] for dz_hi and for dz_lo;
+ * vc = 32768 columns for N <= 8192, 16384 for N <= 16384, else 8192, at most V
+ * rounded up to 256) and an fp32 accumulator of dhidden ([N, D]). 0 for
+ * invalid sizes. */
 VP_API size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D);
 
 /* Gradients of sum_r g[r] logp[r] for the forward above [P2, review nitpick on
  * the chunked backward: dz = g (onehot - exp(logits - lse)), dhidden = dz . W,
  * dW = dz^T . h]. The logits are recomputed chunk by chunk (vc vocabulary
- * rows of W at a time, see above) on tcgen05 tensor cores; dz of a chunk is rounded to
- * bf16 for the two gradient GEMMs (fp32 accumulation in TMEM), which read dz,
- * W and h in place (transposed operands as MN-major tiles); dhidden
- * accumulates across chunks in fp32 and is rounded to bf16 at the end; dW is
- * written chunk by chunk. dhidden: bf16 [N, D]; dW: bf16 [V, D]; either may
+ * rows of W at a time, see above) on tcgen05 tensor cores; dz of a chunk goes
+ * to the two gradient GEMMs (fp32 accumulation in TMEM) as a bf16 pair or
+ * rounded once, by `precision` (VP_GRAD_EXACT or VP_GRAD_FAST, above; any other
+ * value is VP_ERR_ARG); the GEMMs read dz, W and h in place (transposed
+ * operands as MN-major tiles); dhidden accumulates across chunks in fp32 and
+ * is rounded to bf16 at the end; dW is written chunk by chunk. dhidden: bf16 [N, D]; dW: bf16 [V, D]; either may
  * be NULL (not both). stats: the records written by vp_linear_logp_fwd, or by
  * vp_logprobs_merge for a vocabulary shard (see the sharded fused linear ops
  * below: a target outside the shard is then held by another shard).
@@ -397,7 +416,7 @@ VP_API size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D)
  * without valid statistics make their dhidden row and all of dW NaN. */
 VP_API vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
                                     int64_t vocab_start, const int64_t *targets, const vp_rowstat *stats,
-                                    const float *grad_out, void *dhidden, void *dW, void *workspace,
+                                    const float *grad_out, void *dhidden, void *dW, int precision, void *workspace,
                                     size_t workspace_bytes, int32_t *err_word, vp_stream stream);
 
 /* The paper has no counterpart of this entry point; it exists for callers that
@@ -421,8 +440,10 @@ VP_API vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int6
  *    problems needing more than 24 MiB return VP_ERR_SCRATCH before any work
  *    is queued (e.g. V = 75968 allows up to about 10,500 rows);
  *  - the first call on each device looks up the array's device address once
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture;
+ *    (cudaGetSymbolAddress, with that device current) and caches it with the
+ *    context it belongs to; a call from another context on that device (for
+ *    instance after cudaDeviceReset) looks it up again. Make the first call
+ *    on each device, and in each new context, before any stream capture;
  *  - all calls share the one array and it keeps the last call's contents;
  *    nothing in it needs clearing (every entry is written before it is read
  *    within a call), but calls that overlap on the GPU (concurrent streams)
@@ -456,20 +477,21 @@ VP_API vp_status vp_linear_entropy_fwd(const void *hidden, const void *weight, i
                                        float *H, vp_rowstat *stats, void *workspace, size_t workspace_bytes,
                                        vp_stream stream);
 
-/* Bytes of device workspace vp_linear_entropy_bwd needs: dz of one vocabulary
- * chunk (bf16 [N, vc], vc as for vp_linear_logp_bwd_workspace_size) and an fp32
- * accumulator of dhidden ([N, D]). 0 for invalid sizes. */
+/* Bytes of device workspace vp_linear_entropy_bwd needs (for either
+ * precision): dz of one vocabulary chunk twice over (bf16 [N, vc] each, vc as
+ * for vp_linear_logp_bwd_workspace_size) and an fp32 accumulator of dhidden
+ * ([N, D]). 0 for invalid sizes. */
 VP_API size_t vp_linear_entropy_bwd_workspace_size(int64_t N, int64_t V, int64_t D);
 
 /* Gradients of sum_r g[r] H[r]: per vocabulary chunk the logits tile is
  * recomputed and dz = -g p (log p + H) = -g p ((z - m) - c) formed in the
- * epilogue and rounded to bf16, then dhidden += dz . W_c and dW_c = dz^T . h
- * (as vp_linear_logp_bwd). dhidden: bf16 [N, D]; dW: bf16 [V, D]; either may
+ * epilogue, then dhidden += dz . W_c and dW_c = dz^T . h (as
+ * vp_linear_logp_bwd, with the same `precision`). dhidden: bf16 [N, D]; dW: bf16 [V, D]; either may
  * be NULL (not both). stats: the records of vp_linear_entropy_fwd. Rows
  * without valid statistics make their dhidden row and all of dW NaN. */
 VP_API vp_status vp_linear_entropy_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
                                        const vp_rowstat *stats, const float *grad_out, void *dhidden, void *dW,
-                                       void *workspace, size_t workspace_bytes, vp_stream stream);
+                                       int precision, void *workspace, size_t workspace_bytes, vp_stream stream);
 
 /* Bytes of device workspace vp_linear_kl_fwd needs: a 32-byte record per row
  * and 128 columns of the vocabulary. 0 for invalid sizes. */
@@ -490,15 +512,17 @@ VP_API vp_status vp_linear_kl_fwd(const void *ha, const void *wa, const void *hb
                                   int64_t V, int64_t Da, int64_t Db, int direction, float *kl, vp_rowstat *stats_a,
                                   vp_rowstat *stats_b, void *workspace, size_t workspace_bytes, vp_stream stream);
 
-/* Bytes of device workspace vp_linear_kl_bwd needs: dz of one vocabulary chunk
- * for each model (bf16 [N, vc] twice) and fp32 accumulators of both dhidden
- * ([N, Da] and [N, Db]). 0 for invalid sizes. */
+/* Bytes of device workspace vp_linear_kl_bwd needs (for either precision): dz
+ * of one vocabulary chunk for each model (dz_hi and dz_lo, bf16 [N, vc] each)
+ * and fp32 accumulators of both dhidden ([N, Da] and [N, Db]). 0 for invalid
+ * sizes. */
 VP_API size_t vp_linear_kl_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t Db);
 
 /* Gradients of sum_r g[r] KL[r] with respect to both models' hidden states
  * and heads: per vocabulary chunk the dual GEMM recomputes both logits tiles,
- * the epilogue forms dP = g p ((P - m_P) - (Q - m_Q) - c) and dQ = g (q - p)
- * (rounded to bf16), and the gradient GEMMs of each model follow. dha bf16
+ * the epilogue forms dP = g p ((P - m_P) - (Q - m_Q) - c) and dQ = g (q - p),
+ * and the gradient GEMMs of each model follow (`precision` as for
+ * vp_linear_logp_bwd). dha bf16
  * [N, Da], dwa bf16 [V, Da], dhb bf16 [N, Db], dwb bf16 [V, Db]: any may be
  * NULL (not all); a model with neither output (a frozen teacher) costs no
  * gradient GEMMs. stats_a, stats_b: the records of vp_linear_kl_fwd with the
@@ -506,7 +530,8 @@ VP_API size_t vp_linear_kl_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, 
 VP_API vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
                                   int64_t V, int64_t Da, int64_t Db, int direction, const vp_rowstat *stats_a,
                                   const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
-                                  void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream);
+                                  void *dwb, int precision, void *workspace, size_t workspace_bytes,
+                                  vp_stream stream);
 
 /* Generalized JSD between two models' next-token distributions [P1, the
  * commit message adding vocab_parallel_jsd: "Motivation" (divergences over
@@ -531,14 +556,15 @@ VP_API vp_status vp_linear_jsd_fwd(const void *ha, const void *wa, const void *h
  * the same beta: dz_A = g (1 - beta) p ((log p - log mix) - KL(p || mix)),
  * dz_B = g beta q ((log q - log mix) - KL(q || mix)) formed in the dual GEMM's
  * epilogue, then dhidden = dz . W and dW = dz^T . h for each model asked for
- * (outputs as vp_linear_kl_bwd; any may be NULL, not all). At beta = 0 and 1,
- * vp_linear_kl_bwd with the matching direction. workspace:
+ * (outputs and `precision` as vp_linear_kl_bwd; any output may be NULL, not
+ * all). At beta = 0 and 1, vp_linear_kl_bwd with the matching direction. workspace:
  * vp_linear_jsd_bwd_workspace_size(N, V, Da, Db) bytes. */
 VP_API size_t vp_linear_jsd_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t Db);
 VP_API vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N,
                                    int64_t V, int64_t Da, int64_t Db, double beta, const vp_rowstat *stats_a,
                                    const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
-                                   void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream);
+                                   void *dwb, int precision, void *workspace, size_t workspace_bytes,
+                                   vp_stream stream);
 
 /* ------------------------------------------------------------------------ */
 /* Vocabulary-sharded fused linear ops [P2, "Implementation": tensor-parallel */

@@ -304,6 +304,41 @@ def linear_logits(h, W, lib=None):
     return out
 
 
+def linear_row_stats(h, W, rows_per_block=512):
+    """Exact row max m and log S = log sum_j exp(z_j - m) of the logits z = h . W^T for every row,
+    in fp64: one fp64 matrix product per block of rows (numpy), then the max and the sum of
+    exponentials of each row written out. For the full-size linear workload, where every row's
+    normaliser is needed and the per-row loop of linear_logp_fwd would take minutes; the two agree
+    (tests/test_oracle_pins.py)."""
+    h, W = _f64(h), _f64(W)
+    if h.ndim != 2 or W.ndim != 2 or W.shape[1] != h.shape[1]:
+        raise ValueError("hidden [N, D] and weight [V, D] disagree")
+    N = h.shape[0]
+    m, logS = np.empty(N), np.empty(N)
+    for r0 in range(0, N, rows_per_block):
+        z = h[r0:r0 + rows_per_block] @ W.T
+        mb = z.max(axis=1)
+        m[r0:r0 + len(mb)] = mb
+        logS[r0:r0 + len(mb)] = np.log(np.exp(z - mb[:, None]).sum(axis=1))
+    return m, logS
+
+
+def linear_logp_dW_rows(h, W, targets, g, ids, vocab_start=0):
+    """Rows `ids` (shard columns) of dW for sum_r g_r logp_r, in fp64: every row's normaliser
+    (linear_row_stats), then dz[:, ids] = g (onehot - p) and dW[ids] = dz[:, ids]^T . h.
+    Returns (dW rows [len(ids), D], dz[:, ids] [N, len(ids)]). Rows with a negative target
+    contribute nothing; targets outside the shard are not expected here."""
+    h, W = _f64(h), _f64(W)
+    t, g = _i64(targets), _f64(g)
+    ids = np.asarray(ids, np.int64)
+    m, logS = linear_row_stats(h, W)
+    z = h @ W[ids].T
+    p = np.exp((z - m[:, None]) - logS[:, None])
+    onehot = ((t - vocab_start)[:, None] == ids[None, :]).astype(np.float64)
+    dz = np.where((t >= 0)[:, None], g[:, None] * (onehot - p), 0.0)
+    return dz.T @ h, dz
+
+
 def linear_logp_fwd(h, W, targets, vocab_start=0, lib=None):
     """Returns (logp, m, logS, err) of logits h . W^T, one fp64 logits row at a time."""
     h, W = _f64(h), _f64(W)

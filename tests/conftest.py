@@ -25,3 +25,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With VP_PARITY_REPORT set, writes the parity checks' error statistics there as JSON."""
+    path = os.environ.get("VP_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from tests import parity
+    except Exception:  # pragma: no cover
+        return
+    import json
+    with open(path, "w") as f:
+        json.dump(parity.STATS, f, indent=1, sort_keys=True)

@@ -673,6 +673,34 @@ def pin_linear_logp_finite_differences(lib=None):
            1e-14, 1e-14, "linear logp = logprobs(logits)")
 
 
+def pin_linear_row_stats(lib=None):
+    """The block-wise normalisers (row max and log-sum-exp of h . W^T) against Decimal sums, with
+    blocks of 2 rows over 5 rows (a ragged last block), and against the per-row oracle."""
+    N, V, D = 5, 7, 4
+    h, W, _, _ = _linear_case(53, N, V, D)
+    h[3] += 40.0                                     # one row with a large spread
+    m, ls = oracle.linear_row_stats(h, W, rows_per_block=2)
+    with localcontext() as ctx:
+        ctx.prec = 60
+        for r in range(N):
+            z = [sum((Decimal(h[r, k]) * Decimal(W[j, k]) for k in range(D)), Decimal(0)) for j in range(V)]
+            zm = max(z)
+            _close(m[r], float(zm), 1e-14, 1e-14, "linear row max")
+            _close(ls[r], float(sum(_dexp(x - zm) for x in z).ln()), 1e-14, 1e-14, "linear row log S")
+    tg = np.arange(N) % V
+    _, m2, ls2, _ = oracle.linear_logp_fwd(h, W, tg, lib=lib)
+    _close(m, m2, 1e-13, 1e-13, "row stats vs per-row oracle (max)")
+    _close(ls, ls2, 1e-13, 1e-13, "row stats vs per-row oracle (log S)")
+    # selected rows of dW equal those of the full backward (finite-difference pinned), an
+    # ignored target included; the shard starts at vocab_start
+    tg[2] = -1
+    g = np.linspace(-1.0, 2.0, N)
+    _, dW = oracle.linear_logp_bwd(h, W, tg + 100 * (tg >= 0), g, vocab_start=100, lib=lib)
+    ids = [0, 3, 6]
+    rows, _ = oracle.linear_logp_dW_rows(h, W, tg + 100 * (tg >= 0), g, ids, vocab_start=100)
+    _close(rows, dW[ids], 1e-13, 1e-12, "selected dW rows")
+
+
 # ----------------------------------------------------------------------------
 # Fused linear entropy and KL (two models with their own hidden size)
 # ----------------------------------------------------------------------------
@@ -796,6 +824,7 @@ ALL_PINS = [
     pin_jsd_special_rows,
     pin_linear_logp_brute_force,
     pin_linear_logp_finite_differences,
+    pin_linear_row_stats,
     pin_linear_entropy_kl_brute_force,
     pin_linear_entropy_kl_finite_differences,
     pin_linear_entropy_kl_closed_forms,

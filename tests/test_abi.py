@@ -147,17 +147,21 @@ def test_linear_entropy_kl_entry_points_check_arguments_on_the_host():
     assert lib.vp_linear_entropy_fwd(FAKE, None, 4, 16, 64, FAKE, FAKE, FAKE, ws, None) == ERR_NULL
     assert lib.vp_linear_entropy_fwd(FAKE_ODD, FAKE, 4, 16, 64, FAKE, FAKE, FAKE, ws, None) == ERR_ALIGN
     assert lib.vp_linear_entropy_fwd(FAKE, FAKE, 4, 16, 64, FAKE, FAKE, FAKE, size_t(16), None) == ERR_ARG
-    assert lib.vp_linear_entropy_bwd(FAKE, FAKE, 4, 16, 64, FAKE, FAKE, None, None, FAKE, ws, None) == ERR_ARG
+    assert lib.vp_linear_entropy_bwd(FAKE, FAKE, 4, 16, 64, FAKE, FAKE, None, None, 0, FAKE, ws, None) == ERR_ARG
+    # precision: VP_GRAD_EXACT (0) or VP_GRAD_FAST (1) only
+    assert lib.vp_linear_entropy_bwd(FAKE, FAKE, 4, 16, 64, FAKE, FAKE, FAKE, None, 2, FAKE, ws, None) == ERR_ARG
     assert lib.vp_linear_entropy_fwd(None, None, 0, 16, 64, None, None, None, size_t(0), None) == OK   # N = 0
     two = (FAKE, FAKE, FAKE, FAKE, 4, 16)
     assert lib.vp_linear_kl_fwd(*two, 64, 100, 0, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_SHAPE     # Db
     assert lib.vp_linear_kl_fwd(*two, 64, 128, 2, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_ARG       # direction
     assert lib.vp_linear_kl_fwd(*two, 64, 128, 0, FAKE, FAKE, FAKE, FAKE, size_t(64), None) == ERR_ARG
     assert lib.vp_linear_kl_fwd(*two, 64, 128, 0, FAKE, FAKE_ODD, FAKE, FAKE, ws, None) == ERR_ALIGN
-    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, FAKE, None, None, None, None, FAKE, ws,
+    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, FAKE, None, None, None, None, 0, FAKE, ws,
                                 None) == ERR_ARG                                                  # no output
-    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, None, FAKE, None, None, None, FAKE, ws,
+    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, None, FAKE, None, None, None, 0, FAKE, ws,
                                 None) == ERR_NULL
+    assert lib.vp_linear_kl_bwd(*two, 64, 128, 1, FAKE, FAKE, FAKE, FAKE, None, None, None, -1, FAKE, ws,
+                                None) == ERR_ARG                                                  # precision
     assert lib.vp_linear_kl_bwd_workspace_size(4, 16, 64, 128) > 0
     assert lib.vp_linear_kl_workspace_size(4, 0) == 0
 
@@ -168,10 +172,12 @@ def test_linear_jsd_entry_points_check_beta_first():
     two = (FAKE, FAKE, FAKE, FAKE, 4, 16, 64, 128)
     for beta in (-0.1, 1.5, float("nan")):
         assert lib.vp_linear_jsd_fwd(*two, beta, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_ARG
-        assert lib.vp_linear_jsd_bwd(*two, beta, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, ws, None) == ERR_ARG
+        assert lib.vp_linear_jsd_bwd(*two, beta, FAKE, FAKE, FAKE, FAKE, None, None, None, 0, FAKE, ws,
+                                     None) == ERR_ARG
     assert lib.vp_linear_jsd_fwd(FAKE, FAKE, FAKE, FAKE, 4, 16, 64, 96, 0.5, FAKE, FAKE, FAKE, FAKE, ws,
                                  None) == ERR_SHAPE
-    assert lib.vp_linear_jsd_bwd(*two, 0.5, FAKE, FAKE, FAKE, None, None, None, None, FAKE, ws, None) == ERR_ARG
+    assert lib.vp_linear_jsd_bwd(*two, 0.5, FAKE, FAKE, FAKE, None, None, None, None, 0, FAKE, ws, None) == ERR_ARG
+    assert lib.vp_linear_jsd_bwd(*two, 0.5, FAKE, FAKE, FAKE, FAKE, None, None, None, 5, FAKE, ws, None) == ERR_ARG
     assert lib.vp_linear_jsd_fwd(*two, 0.5, FAKE_ODD, FAKE, FAKE, FAKE, ws, None) == ERR_ALIGN
     assert lib.vp_linear_jsd_workspace_size(4, 16) == lib.vp_linear_kl_workspace_size(4, 16)
 

@@ -92,3 +92,27 @@ def test_two_ranks_agree_on_the_slowest_time_and_the_job_rate():
         assert res[r][0] == 3.5
         assert abs(res[r][1] - 2 * 22.4e9 / 3.5e-3 / 1e9) < 1e-9
     assert bench.max_over_ranks(1.25, None, "cpu") == 1.25
+
+
+def test_gpus_two_starts_two_ranks_by_itself():
+    """`bench.py --gpus 2` with no launcher starts two ranks (gloo without a GPU) and prints one line."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--launch-check"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.strip().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    line = json.loads(lines[0])
+    assert line["n_gpus"] == 2 and line["ranks_seen"] == 2 and line["max_over_ranks"] == 2.0
+
+
+def test_rank_command_uses_the_loopback_rendezvous():
+    cmd = bench.rank_command(4, ["--steps", "3"], 29500)
+    assert "--nproc-per-node=4" in cmd and "127.0.0.1" in cmd and cmd[-2:] == ["--steps", "3"]
+
+
+def test_gpus_must_match_the_launcher():
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    out = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--launch-check"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert out.returncode == 2 and "WORLD_SIZE" in out.stderr

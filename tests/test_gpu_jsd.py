@@ -55,11 +55,11 @@ def _check(a, b, g, beta, tag, want=(True, True)):
         assert (m64[fin] == m[fin]).all(), f"{tag} row max of {name}"
         parity.check_out(parity.to64(d["logS"])[ok], ls[ok], f"{tag} logS of {name}")
     if want[0]:
-        worst["da"] = parity.check_grad(da, rda, f"{tag} dA", Ma)
+        worst["da"] = parity.check_grad(da, rda, f"{tag} dA", Ma, kappa=parity.KAPPA_JSD)
     else:
         assert da is None
     if want[1]:
-        worst["db"] = parity.check_grad(db, rdb, f"{tag} dB", Mb)
+        worst["db"] = parity.check_grad(db, rdb, f"{tag} dB", Mb, kappa=parity.KAPPA_JSD)
     else:
         assert db is None
     return worst, (jsd, sa, sb, da, db)

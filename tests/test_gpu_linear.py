@@ -91,8 +91,8 @@ def test_linear_logp_bwd_small(N, V, D):
     t, g = w["targets"].numpy(), w["grad"].double().numpy()
     ref_dh, ref_dW = oracle.linear_logp_bwd(h64, W64, t, g)
     dz = np.abs(oracle.logprobs_bwd(oracle.linear_logits(h64, W64), t, g))
-    _check_gemm_grad(dh, ref_dh, dz @ np.abs(W64), f"{N}x{V}x{D} dhidden")
-    _check_gemm_grad(dW, ref_dW, dz.T @ np.abs(h64), f"{N}x{V}x{D} dW")
+    _check_gemm_grad(dh, ref_dh, parity.gemm_norms(dz, W64), f"{N}x{V}x{D} dhidden")
+    _check_gemm_grad(dW, ref_dW, parity.gemm_norms(dz.T, h64), f"{N}x{V}x{D} dW")
 
 
 def test_linear_logp_bwd_single_outputs_and_special_targets():
@@ -121,11 +121,29 @@ def test_linear_logp_bwd_full_size_sampled():
     tt, gg = w["targets"][rows].numpy(), w["grad"][rows].double().numpy()
     ref_dh, _ = oracle.linear_logp_bwd(h64, W64, tt, gg, want_dW=False)
     dz = np.abs(oracle.logprobs_bwd(oracle.linear_logits(h64, W64), tt, gg))
-    _check_gemm_grad(dh[rows], ref_dh, dz @ np.abs(W64), "config 5 dhidden")
+    _check_gemm_grad(dh[rows], ref_dh, parity.gemm_norms(dz, W64), "config 5 dhidden")
     # dW on every row: each column of dW sums to 0 over the vocabulary (every dz row sums to 0)
     col = dW.double().sum(0).abs()
     scale = dW.double().abs().sum(0)
     assert torch.isfinite(dW).all() and (col <= 2.0 ** -7 * scale + 1e-6).all()
+
+
+@pytest.mark.slow
+def test_linear_logp_bwd_full_size_dW_rows():
+    """Whole rows of dW (all D columns) at the full linear workload: dW_j = sum_n dz[n, j] h_n needs
+    every row's normaliser, which the oracle takes block by block in fp64 (linear_row_stats)."""
+    w = workloads.linear()
+    h, W, t, g = (w[k].to(DEV) for k in ("hidden", "weight", "targets", "grad"))
+    lp, st = vp.vp_linear_logp_fwd(h, W, t)
+    dh, dW = vp.vp_linear_logp_bwd(h, W, t, st, g)
+    torch.cuda.synchronize()
+    h64, W64 = parity.to64(w["hidden"]), parity.to64(w["weight"])
+    tt, gg = w["targets"].numpy(), w["grad"].double().numpy()
+    V = W64.shape[0]
+    # chunk edges (32768 columns) and the targets of a few rows
+    ids = np.unique(np.concatenate([[0, 1, 32767, 32768, 65535, 65536, V - 1], tt[[0, 5, 4096]]]))
+    ref, dz = oracle.linear_logp_dW_rows(h64, W64, tt, gg, ids)
+    _check_gemm_grad(dW[torch.as_tensor(ids, device=DEV)], ref, parity.gemm_norms(dz.T, h64), "config 5 dW rows")
 
 
 @pytest.mark.parametrize("N", [9000, 17000])   # vocabulary chunks of 16384 and 8192 columns
@@ -139,7 +157,7 @@ def test_linear_logp_bwd_many_rows_sampled(N):
     t, g = w["targets"][rows].numpy(), w["grad"][rows].double().numpy()
     ref_dh, _ = oracle.linear_logp_bwd(h64, W64, t, g, want_dW=False)
     dz = np.abs(oracle.logprobs_bwd(oracle.linear_logits(h64, W64), t, g))
-    _check_gemm_grad(dh[rows], ref_dh, dz @ np.abs(W64), f"{N} rows dhidden")
+    _check_gemm_grad(dh[rows], ref_dh, parity.gemm_norms(dz, W64), f"{N} rows dhidden")
     # every dz row sums to 0, so each column of dW sums to 0 over the vocabulary
     col = dW.double().sum(0).abs()
     scale = dW.double().abs().sum(0)

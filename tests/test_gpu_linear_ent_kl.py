@@ -51,8 +51,9 @@ def test_linear_entropy_fwd_bwd(N, V, D):
     z = oracle.linear_logits(h64, W64)
     dz = np.abs(oracle.entropy_bwd(z, g64))
     M = parity.oracle_all(z, z, np.zeros(N, np.int64), g64, ops=("entropy",))["_mag"]["dH"]
-    parity.check_gemm_grad(dh, rdh, dz @ np.abs(W64), f"{N}x{V}x{D} entropy dhidden", M @ np.abs(W64))
-    parity.check_gemm_grad(dW, rdW, dz.T @ np.abs(h64), f"{N}x{V}x{D} entropy dW", M.T @ np.abs(h64))
+    M = M * (1.0 + parity.logit_scale((h64, W64)))[:, None]
+    parity.check_gemm_grad(dh, rdh, parity.gemm_norms(dz, W64), f"{N}x{V}x{D} entropy dhidden", M @ np.abs(W64))
+    parity.check_gemm_grad(dW, rdW, parity.gemm_norms(dz.T, h64), f"{N}x{V}x{D} entropy dW", M.T @ np.abs(h64))
 
 
 def test_linear_entropy_single_outputs_and_batch_invariance():
@@ -115,11 +116,14 @@ def _check_kl(ha, Wa, hb, Wb, g, direction, tag):
     pa, pb = _probs(za), _probs(zb)
     pP = pa if direction == vp.KL_REVERSE else pb
     Fa, Fb = parity.flushed(Ma, pP, pa, pb), parity.flushed(Mb, pP, pa, pb)
-    mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
+    lam = (1.0 + parity.logit_scale((ha64, Wa64), (hb64, Wb64)))[:, None]
+    Ma, Mb = Ma * lam, Mb * lam
+    norms = (parity.gemm_norms(dza, Wa64), parity.gemm_norms(dza.T, ha64), parity.gemm_norms(dzb, Wb64),
+             parity.gemm_norms(dzb.T, hb64))
     evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
     flush = (Fa @ np.abs(Wa64), Fa.T @ np.abs(ha64), Fb @ np.abs(Wb64), Fb.T @ np.abs(hb64))
-    for got, r, mg, ev, fl, name in zip(grads, ref, mags, evals, flush, ("dhidden A", "dW A", "dhidden B", "dW B")):
-        parity.check_gemm_grad(got, r, mg, f"{tag} {name}", ev, fl)
+    for got, r, nm, ev, fl, name in zip(grads, ref, norms, evals, flush, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, nm, f"{tag} {name}", ev, fl)
     return kl, grads
 
 
@@ -209,7 +213,8 @@ def test_linear_entropy_kl_full_size_sampled():
     z = oracle.linear_logits(h64, W64)
     dz = np.abs(oracle.entropy_bwd(z, g64))
     M = parity.oracle_all(z, z, np.zeros(len(rows), np.int64), g64, ops=("entropy",))["_mag"]["dH"]
-    parity.check_gemm_grad(dha[rows], rdh, dz @ np.abs(W64), "full-size entropy dhidden", M @ np.abs(W64))
+    M = M * (1.0 + parity.logit_scale((h64, W64)))[:, None]
+    parity.check_gemm_grad(dha[rows], rdh, parity.gemm_norms(dz, W64), "full-size entropy dhidden", M @ np.abs(W64))
     assert torch.isfinite(dWa).all()
 
 
@@ -246,10 +251,13 @@ def test_linear_jsd_fwd_bwd(N, V, Da, Db, beta):
     za, zb = oracle.linear_logits(ha64, Wa64), oracle.linear_logits(hb64, Wb64)
     dza, dzb = (np.abs(x) for x in oracle.jsd_bwd(za, zb, beta, g64))
     Ma, Mb = _jsd_mags(za, zb, beta, g64)
-    mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
+    lam = (1.0 + parity.logit_scale((ha64, Wa64), (hb64, Wb64)))[:, None]
+    Ma, Mb = Ma * lam, Mb * lam
+    norms = (parity.gemm_norms(dza, Wa64), parity.gemm_norms(dza.T, ha64), parity.gemm_norms(dzb, Wb64),
+             parity.gemm_norms(dzb.T, hb64))
     evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
-    for got, r, mg, ev, name in zip(grads, ref, mags, evals, ("dhidden A", "dW A", "dhidden B", "dW B")):
-        parity.check_gemm_grad(got, r, mg, f"{tag} {name}", ev)
+    for got, r, nm, ev, name in zip(grads, ref, norms, evals, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, nm, f"{tag} {name}", ev, kappa=parity.KAPPA_JSD)
 
 
 def test_linear_jsd_endpoints_frozen_teacher_and_invariance():
@@ -360,8 +368,11 @@ def test_linear_two_model_wide_logit_spread():
     # p, q and the mixture (>= min(beta, 1 - beta) max(p, q)) flush below 2^-126
     below = parity.TINY / min(beta, 1.0 - beta)
     Fa, Fb = parity.flushed(Ma, _probs(za), below=below), parity.flushed(Mb, _probs(zb), below=below)
-    mags = (dza @ np.abs(Wa64), dza.T @ np.abs(ha64), dzb @ np.abs(Wb64), dzb.T @ np.abs(hb64))
+    lam = (1.0 + parity.logit_scale((ha64, Wa64), (hb64, Wb64)))[:, None]
+    Ma, Mb = Ma * lam, Mb * lam
+    norms = (parity.gemm_norms(dza, Wa64), parity.gemm_norms(dza.T, ha64), parity.gemm_norms(dzb, Wb64),
+             parity.gemm_norms(dzb.T, hb64))
     evals = (Ma @ np.abs(Wa64), Ma.T @ np.abs(ha64), Mb @ np.abs(Wb64), Mb.T @ np.abs(hb64))
     flush = (Fa @ np.abs(Wa64), Fa.T @ np.abs(ha64), Fb @ np.abs(Wb64), Fb.T @ np.abs(hb64))
-    for got, r, mg, ev, fl, name in zip(grads, ref, mags, evals, flush, ("dhidden A", "dW A", "dhidden B", "dW B")):
-        parity.check_gemm_grad(got, r, mg, f"wide spread JSD {name}", ev, fl)
+    for got, r, nm, ev, fl, name in zip(grads, ref, norms, evals, flush, ("dhidden A", "dW A", "dhidden B", "dW B")):
+        parity.check_gemm_grad(got, r, nm, f"wide spread JSD {name}", ev, fl, kappa=parity.KAPPA_JSD)

@@ -35,8 +35,8 @@ def _check_terms(dh_k, dW_k, dz, Mz, h64, W64, v0, v1, tag):
     """dW rows [v0, v1) and the shard's dhidden term dz[:, v0:v1] . W[v0:v1]."""
     dzk, Mk, Wk = dz[:, v0:v1], Mz[:, v0:v1], W64[v0:v1]
     adz = np.abs(dzk)
-    parity.check_gemm_grad(dh_k, dzk @ Wk, adz @ np.abs(Wk), f"{tag} dhidden term", Mk @ np.abs(Wk))
-    parity.check_gemm_grad(dW_k, dzk.T @ h64, adz.T @ np.abs(h64), f"{tag} dW rows", Mk.T @ np.abs(h64))
+    parity.check_gemm_grad(dh_k, dzk @ Wk, parity.gemm_norms(adz, Wk), f"{tag} dhidden term", Mk @ np.abs(Wk))
+    parity.check_gemm_grad(dW_k, dzk.T @ h64, parity.gemm_norms(adz.T, h64), f"{tag} dW rows", Mk.T @ np.abs(h64))
 
 
 def test_linear_logp_sharded():
@@ -105,6 +105,7 @@ def test_linear_entropy_sharded():
     z = oracle.linear_logits(h64, W64)
     dz = oracle.entropy_bwd(z, g64)
     Mz = parity.oracle_all(z, z, np.zeros(N, np.int64), g64, ops=("entropy",))["_mag"]["dH"]
+    Mz = Mz * (1.0 + parity.logit_scale((h64, W64)))[:, None]
     for (dh_k, dW_k), (v0, v1) in zip(grads, CUTS):
         _check_terms(dh_k, dW_k, dz, Mz, h64, W64, v0, v1, f"entropy shard [{v0}, {v1})")
 
@@ -134,6 +135,8 @@ def test_linear_kl_sharded(direction):
     dza, dzb = oracle.kl_bwd(za, zb, g64, direction)
     op = "kl_rev" if direction == vp.KL_REVERSE else "kl_fwd"
     M = parity.oracle_all(za, zb, np.zeros(N, np.int64), g64, ops=(op,))["_mag"]
+    lam = (1.0 + parity.logit_scale((ha64, Wa64), (hb64, Wb64)))[:, None]
+    M = {k: v * lam for k, v in M.items()}
     pa, pb = _probs(za), _probs(zb)
     assert min(pa.min(), pb.min()) > parity.TINY, "no probability of this case is flushed"
     for (dha, dwa, dhb, dwb), (v0, v1) in zip(grads, CUTS):

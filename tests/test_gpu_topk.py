@@ -22,7 +22,8 @@ DEV = "cuda"
 
 
 def _mag(x64, t, g):
-    """M_j: |g| summed over the row's used ids times p_j, plus |g| summed over the ids equal to j."""
+    """M_j: |g| summed over the row's used ids times p_j, plus |g| summed over the ids equal to j
+    (the operands of the element's formula, for parity.KAPPA_BF16 and parity.ORACLE_EPS)."""
     N, V = x64.shape
     _, m, ls = oracle.entropy_fwd(x64)
     with np.errstate(all="ignore"):
@@ -55,7 +56,8 @@ def _check(x, t, g, tag, vocab_start=0):
     ok = np.isfinite(m) & np.isfinite(ls) & ~(np.isnan(x64) | np.isposinf(x64)).any(1)   # rows with a record
     assert (parity.to64(d["m"])[ok] == m[ok]).all(), f"{tag} row max"
     parity.check_out(parity.to64(d["logS"])[ok], ls[ok], f"{tag} logS")
-    worst["dx"] = parity.check_grad(dx, rdx, f"{tag} dx", _mag(x64, t64 - vocab_start * (t64 >= 0), g64))
+    M = _mag(x64, t64 - vocab_start * (t64 >= 0), g64)
+    worst["dx"] = parity.check_grad(dx, rdx, f"{tag} dx", M, oracle_mag=M)
     return worst, (lp, st, dx)
 
 
@@ -185,7 +187,8 @@ def test_topk_full_pages_shape_sampled():
     rlp, _ = oracle.logprobs_topk_fwd(x64, t64)
     parity.check_out(lp[rows], rlp, "full topk logp")
     rdx = oracle.logprobs_topk_bwd(x64, t64, g64)
-    parity.check_grad(dx[rows], rdx, "full topk dx", _mag(x64, t64, g64))
+    M = _mag(x64, t64, g64)
+    parity.check_grad(dx[rows], rdx, "full topk dx", M, oracle_mag=M)
     # every row: the gradient sums to ~0 (shift invariance), logp <= 0
     s = dx.float().sum(1).abs()
     assert float(s.max()) < 1e-2 * float(g.abs().sum(1).max())

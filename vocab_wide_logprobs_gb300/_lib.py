@@ -28,17 +28,17 @@ SIGNATURES = {
     "vp_kl_bwd": [P, P, I32, I64, I64, I64, I64, I64, I32, P, P, P, P, P, P],
     "vp_linear_logp_fwd": [P, P, I64, I64, I64, I64, P, P, P, P, ctypes.c_size_t, P, P],
     "vp_linear_logp_fwd_noalloc": [P, P, I64, I64, I64, I64, P, P, P, P, P],
-    "vp_linear_logp_bwd": [P, P, I64, I64, I64, I64, P, P, P, P, P, P, ctypes.c_size_t, P, P],
+    "vp_linear_logp_bwd": [P, P, I64, I64, I64, I64, P, P, P, P, P, I32, P, ctypes.c_size_t, P, P],
     "vp_linear_entropy_fwd": [P, P, I64, I64, I64, P, P, P, ctypes.c_size_t, P],
-    "vp_linear_entropy_bwd": [P, P, I64, I64, I64, P, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_entropy_bwd": [P, P, I64, I64, I64, P, P, P, P, I32, P, ctypes.c_size_t, P],
     "vp_linear_kl_fwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, ctypes.c_size_t, P],
-    "vp_linear_kl_bwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
+    "vp_linear_kl_bwd": [P, P, P, P, I64, I64, I64, I64, I32, P, P, P, P, P, P, P, I32, P, ctypes.c_size_t, P],
     "vp_linear_jsd_fwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, ctypes.c_size_t, P],
     "vp_linear_logp_partial": [P, P, I64, I64, I64, I64, P, P, P, ctypes.c_size_t, P],
     "vp_linear_entropy_partial": [P, P, I64, I64, I64, P, P, ctypes.c_size_t, P],
     "vp_linear_kl_partial": [P, P, P, P, I64, I64, I64, I64, I32, P, P, ctypes.c_size_t, P],
-    "vp_linear_jsd_bwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P, P, P, ctypes.c_size_t,
-                          P],
+    "vp_linear_jsd_bwd": [P, P, P, P, I64, I64, I64, I64, ctypes.c_double, P, P, P, P, P, P, P, I32, P,
+                          ctypes.c_size_t, P],
     "vp_upload": [P, P, ctypes.c_size_t, P],
     "vp_download": [P, P, ctypes.c_size_t, P],
     "vp_jsd_fwd": [P, P, I32, I64, I64, I64, I64, I64, ctypes.c_double, P, P, P, P],

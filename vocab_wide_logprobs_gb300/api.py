@@ -23,6 +23,7 @@ from . import _lib
 
 F32, BF16 = 0, 1
 KL_REVERSE, KL_FORWARD = 0, 1
+GRAD_EXACT, GRAD_FAST = 0, 1   # precision of the fused linear backwards (VP_GRAD_EXACT / VP_GRAD_FAST)
 ERRBIT_TARGET = 1
 ROW_NANINF, ROW_EMPTY, ROW_MISMATCH, ROW_SHARDED, ROW_BADTARGET = 1, 2, 4, 8, 16
 ROWSTAT_FLOATS = 8  # sizeof(vp_rowstat) / 4
@@ -91,6 +92,10 @@ def _ptr(t):
 
 def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _precision(p):
+    return GRAD_EXACT if p is None else int(p)
 
 
 def _check(status: int, where: str):
@@ -264,8 +269,9 @@ def vp_linear_logp_bwd_workspace_size(N: int, V: int, D: int) -> int:
 
 
 def vp_linear_logp_bwd(hidden, weight, targets, stats, grad, vocab_start: int = 0, want_dhidden=True, want_dW=True,
-                       err_word=None, dhidden=None, dW=None, workspace=None):
-    """Returns (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None)."""
+                       err_word=None, dhidden=None, dW=None, workspace=None, precision: int = None):
+    """Returns (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None). precision: GRAD_EXACT (default:
+    dz as a bf16 pair hi + lo in the gradient GEMMs) or GRAD_FAST (dz rounded to bf16)."""
     N, D = hidden.shape
     V = weight.shape[0]
     if want_dhidden and dhidden is None:
@@ -278,8 +284,9 @@ def vp_linear_logp_bwd(hidden, weight, targets, stats, grad, vocab_start: int = 
         need = vp_linear_logp_bwd_workspace_size(N, V, D)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=hidden.device)
     _check(_lib.lib().vp_linear_logp_bwd(_ptr(hidden), _ptr(weight), N, V, D, vocab_start, _ptr(targets),
-                                         _ptr(stats), _ptr(grad), _ptr(dhidden), _ptr(dW), _ptr(workspace),
-                                         workspace.numel() * workspace.element_size(), _ptr(err_word), _stream()),
+                                         _ptr(stats), _ptr(grad), _ptr(dhidden), _ptr(dW), _precision(precision),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _ptr(err_word), _stream()),
            "vp_linear_logp_bwd")
     return dhidden, dW
 
@@ -384,7 +391,7 @@ def vp_linear_entropy_fwd(hidden, weight, H=None, stats=None, workspace=None):
 
 
 def vp_linear_entropy_bwd(hidden, weight, stats, grad, want_dhidden=True, want_dW=True, dhidden=None, dW=None,
-                          workspace=None):
+                          workspace=None, precision: int = None):
     """Gradients of sum_r grad[r] H[r]: (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None)."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_bwd")
     dhidden = (torch.empty((N, D), dtype=torch.bfloat16, device=hidden.device) if dhidden is None else dhidden) \
@@ -393,7 +400,8 @@ def vp_linear_entropy_bwd(hidden, weight, stats, grad, want_dhidden=True, want_d
     if workspace is None:
         workspace = _workspace(_lib.lib().vp_linear_entropy_bwd_workspace_size(N, V, D), hidden)
     _check(_lib.lib().vp_linear_entropy_bwd(_ptr(hidden), _ptr(weight), N, V, D, _ptr(stats), _ptr(grad),
-                                            _ptr(dhidden), _ptr(dW), _ptr(workspace), workspace.numel(), _stream()),
+                                            _ptr(dhidden), _ptr(dW), _precision(precision), _ptr(workspace),
+                                            workspace.numel(), _stream()),
            "vp_linear_entropy_bwd")
     return dhidden, dW
 
@@ -423,7 +431,7 @@ def vp_linear_kl_fwd(ha, wa, hb, wb, direction: int = KL_REVERSE, kl=None, stats
 
 
 def vp_linear_kl_bwd(ha, wa, hb, wb, direction, stats_a, stats_b, grad, want=(True, True, True, True), outs=None,
-                     workspace=None):
+                     workspace=None, precision: int = None):
     """Gradients of sum_r grad[r] KL[r]: (dha, dwa, dhb, dwb), bf16, None where not wanted."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_bwd")
     shapes = ((N, Da), (V, Da), (N, Db), (V, Db))
@@ -433,7 +441,8 @@ def vp_linear_kl_bwd(ha, wa, hb, wb, direction, stats_a, stats_b, grad, want=(Tr
         workspace = _workspace(_lib.lib().vp_linear_kl_bwd_workspace_size(N, V, Da, Db), ha)
     _check(_lib.lib().vp_linear_kl_bwd(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, int(direction),
                                        _ptr(stats_a), _ptr(stats_b), _ptr(grad), *[_ptr(o) for o in outs],
-                                       _ptr(workspace), workspace.numel(), _stream()), "vp_linear_kl_bwd")
+                                       _precision(precision), _ptr(workspace), workspace.numel(), _stream()),
+           "vp_linear_kl_bwd")
     return tuple(outs)
 
 
@@ -453,7 +462,7 @@ def vp_linear_jsd_fwd(ha, wa, hb, wb, beta: float = 0.5, jsd=None, stats_a=None,
 
 
 def vp_linear_jsd_bwd(ha, wa, hb, wb, beta, stats_a, stats_b, grad, want=(True, True, True, True), outs=None,
-                      workspace=None):
+                      workspace=None, precision: int = None):
     """Gradients of sum_r grad[r] JSD[r]: (dha, dwa, dhb, dwb), bf16, None where not wanted."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_jsd_bwd")
     shapes = ((N, Da), (V, Da), (N, Db), (V, Db))
@@ -463,7 +472,8 @@ def vp_linear_jsd_bwd(ha, wa, hb, wb, beta, stats_a, stats_b, grad, want=(True, 
         workspace = _workspace(_lib.lib().vp_linear_jsd_bwd_workspace_size(N, V, Da, Db), ha)
     _check(_lib.lib().vp_linear_jsd_bwd(_ptr(ha), _ptr(wa), _ptr(hb), _ptr(wb), N, V, Da, Db, float(beta),
                                         _ptr(stats_a), _ptr(stats_b), _ptr(grad), *[_ptr(o) for o in outs],
-                                        _ptr(workspace), workspace.numel(), _stream()), "vp_linear_jsd_bwd")
+                                        _precision(precision), _ptr(workspace), workspace.numel(), _stream()),
+           "vp_linear_jsd_bwd")
     return tuple(outs)
 
 

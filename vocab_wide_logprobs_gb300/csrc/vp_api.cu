@@ -374,6 +374,8 @@ vp_status vp_linear_logp_fwd_noalloc(const void *hidden, const void *weight, int
     return launched(vp::launch_linear_logp_fwd_noalloc(a));
 }
 
+static bool precision_ok(int precision) { return precision == VP_GRAD_EXACT || precision == VP_GRAD_FAST; }
+
 size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D) {
     if (N < 0 || V < 1 || D < 64) return 0;
     return vp::linear_bwd_workspace_bytes(N, V, D);
@@ -381,11 +383,12 @@ size_t vp_linear_logp_bwd_workspace_size(int64_t N, int64_t V, int64_t D) {
 
 vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
                              int64_t vocab_start, const int64_t *targets, const vp_rowstat *stats,
-                             const float *grad_out, void *dhidden, void *dW, void *workspace, size_t workspace_bytes,
-                             int32_t *err_word, vp_stream stream) {
+                             const float *grad_out, void *dhidden, void *dW, int precision, void *workspace,
+                             size_t workspace_bytes, int32_t *err_word, vp_stream stream) {
     if (N < 0 || N > kMaxRowsPerLaunch || V < 1 || V > kMaxV || D < 64 || D % 64 != 0 || D > (1 << 20))
         return VP_ERR_SHAPE;
     if (!dhidden && !dW) return VP_ERR_ARG;
+    if (!precision_ok(precision)) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
     if (!hidden || !weight || !targets || !stats || !grad_out || !workspace) return VP_ERR_NULL;
     if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(targets, 8) || !aligned(stats, 16) ||
@@ -396,7 +399,7 @@ vp_status vp_linear_logp_bwd(const void *hidden, const void *weight, int64_t N, 
     vp_status st = check_device();
     if (st != VP_OK) return st;
     vp::LinearBwdArgs a{hidden, weight, N, V, D, vocab_start, targets, stats, grad_out, dhidden, dW, workspace,
-                        err_word, (cudaStream_t)stream};
+                        err_word, (cudaStream_t)stream, precision};
     return launched(vp::launch_linear_logp_bwd(a));
 }
 
@@ -432,9 +435,10 @@ size_t vp_linear_entropy_bwd_workspace_size(int64_t N, int64_t V, int64_t D) {
 
 vp_status vp_linear_entropy_bwd(const void *hidden, const void *weight, int64_t N, int64_t V, int64_t D,
                                 const vp_rowstat *stats, const float *grad_out, void *dhidden, void *dW,
-                                void *workspace, size_t workspace_bytes, vp_stream stream) {
+                                int precision, void *workspace, size_t workspace_bytes, vp_stream stream) {
     if (!linear_dims_ok(N, V, D)) return VP_ERR_SHAPE;
     if (!dhidden && !dW) return VP_ERR_ARG;
+    if (!precision_ok(precision)) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
     if (!hidden || !weight || !stats || !grad_out || !workspace) return VP_ERR_NULL;
     if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(stats, 16) || !aligned(grad_out, 4) ||
@@ -445,6 +449,7 @@ vp_status vp_linear_entropy_bwd(const void *hidden, const void *weight, int64_t 
     if (st != VP_OK) return st;
     vp::LinearEntArgs a{hidden, weight, N, V, D, nullptr, const_cast<vp_rowstat *>(stats), grad_out, dhidden, dW,
                         workspace, (cudaStream_t)stream};
+    a.precision = precision;
     return launched(vp::launch_linear_entropy_bwd(a));
 }
 
@@ -479,10 +484,11 @@ size_t vp_linear_kl_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_t
 vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
                            int64_t Da, int64_t Db, int direction, const vp_rowstat *stats_a,
                            const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
-                           void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream) {
+                           void *dwb, int precision, void *workspace, size_t workspace_bytes, vp_stream stream) {
     if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
     if (direction != VP_KL_REVERSE && direction != VP_KL_FORWARD) return VP_ERR_ARG;
     if (!dha && !dwa && !dhb && !dwb) return VP_ERR_ARG;
+    if (!precision_ok(precision)) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
     if (!ha || !wa || !hb || !wb || !stats_a || !stats_b || !grad_out || !workspace) return VP_ERR_NULL;
     if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(stats_a, 16) ||
@@ -495,6 +501,7 @@ vp_status vp_linear_kl_bwd(const void *ha, const void *wa, const void *hb, const
     vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, direction, nullptr,
                        const_cast<vp_rowstat *>(stats_a), const_cast<vp_rowstat *>(stats_b), grad_out,
                        dha, dwa, dhb, dwb, workspace, (cudaStream_t)stream};
+    a.precision = precision;
     return launched(vp::launch_linear_kl_bwd(a));
 }
 
@@ -533,13 +540,14 @@ size_t vp_linear_jsd_bwd_workspace_size(int64_t N, int64_t V, int64_t Da, int64_
 vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *hb, const void *wb, int64_t N, int64_t V,
                             int64_t Da, int64_t Db, double beta, const vp_rowstat *stats_a,
                             const vp_rowstat *stats_b, const float *grad_out, void *dha, void *dwa, void *dhb,
-                            void *dwb, void *workspace, size_t workspace_bytes, vp_stream stream) {
+                            void *dwb, int precision, void *workspace, size_t workspace_bytes, vp_stream stream) {
     if (!beta_ok(beta)) return VP_ERR_ARG;
     if (beta == 0.0 || beta == 1.0)
         return vp_linear_kl_bwd(ha, wa, hb, wb, N, V, Da, Db, beta == 0.0 ? VP_KL_FORWARD : VP_KL_REVERSE, stats_a,
-                                stats_b, grad_out, dha, dwa, dhb, dwb, workspace, workspace_bytes, stream);
+                                stats_b, grad_out, dha, dwa, dhb, dwb, precision, workspace, workspace_bytes, stream);
     if (!linear_dims_ok(N, V, Da) || !linear_dims_ok(N, V, Db)) return VP_ERR_SHAPE;
     if (!dha && !dwa && !dhb && !dwb) return VP_ERR_ARG;
+    if (!precision_ok(precision)) return VP_ERR_ARG;
     if (N == 0) return VP_OK;
     if (!ha || !wa || !hb || !wb || !stats_a || !stats_b || !grad_out || !workspace) return VP_ERR_NULL;
     if (!aligned(ha, 16) || !aligned(wa, 16) || !aligned(hb, 16) || !aligned(wb, 16) || !aligned(stats_a, 16) ||
@@ -552,6 +560,7 @@ vp_status vp_linear_jsd_bwd(const void *ha, const void *wa, const void *hb, cons
     vp::LinearKLArgs a{ha, wa, hb, wb, N, V, Da, Db, 0, nullptr,
                        const_cast<vp_rowstat *>(stats_a), const_cast<vp_rowstat *>(stats_b), grad_out,
                        dha, dwa, dhb, dwb, workspace, (cudaStream_t)stream, (float)beta};
+    a.precision = precision;
     return launched(vp::launch_linear_jsd_bwd(a));
 }
 

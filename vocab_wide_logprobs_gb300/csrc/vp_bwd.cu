@@ -21,8 +21,9 @@
 //             dB_j = g beta q_j ((log q_j - log mix_j) - KL(q || mix)), mix = beta q + (1 - beta) p
 // m is the exact row max, so t_j is exact; logS and c arrive as hi + lo pairs.
 // The fp32 path uses both halves and an error-free difference t^P - t^Q, so a
-// gradient that cancels to near zero keeps its accuracy; the bf16 path uses
-// the hi halves (its gradients are rounded to bf16).
+// gradient that cancels to near zero keeps its accuracy. The bf16 path
+// subtracts both halves of c, and of log S where 1 - p of a target cancels;
+// where q ~ p it forms q - p as p (e^d - 1) from d = log q - log p.
 //
 // Shape: each CTA (256 threads) handles one tile of one row: up to 1024
 // 16-byte vectors of the input (8192 bf16 / 4096 fp32 logits), four loads in
@@ -51,19 +52,6 @@ __device__ __forceinline__ uint4 splat(float v) {
 // double-floats, takes an accurate exponential and rounds each gradient once;
 // the bf16 path uses fp32 arithmetic and the hardware exponential.
 // --------------------------------------------------------------------------
-// e^x - 1 for |x| < 1/2 by its Taylor series to x^8/8! (relative error < 1e-8 there):
-// used where e^x - 1 would cancel.
-__device__ __forceinline__ float expm1_small(float x) {
-    float t = 2.4801587301587302e-05f;      // 1/8!
-    t = fmaf(t, x, 1.9841269841269841e-04f);  // 1/7!
-    t = fmaf(t, x, 1.3888888888888889e-03f);  // 1/6!
-    t = fmaf(t, x, 8.3333333333333333e-03f);  // 1/5!
-    t = fmaf(t, x, 4.1666666666666667e-02f);  // 1/4!
-    t = fmaf(t, x, 1.6666666666666667e-01f);  // 1/3!
-    t = fmaf(t, x, 0.5f);                     // 1/2!
-    return fmaf(t * x, x, x);                 // x + x^2 (1/2 + x/6 + ...)
-}
-
 template <int kOp, typename T>
 __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s, float g, int64_t loc) {
     if constexpr (Elem<T>::kPrecise) {
@@ -85,15 +73,19 @@ __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s,
         const float p = Elem<T>::exp(lp);
         if (kOp == 0) {
             if (j != loc) return -g * p;
-            return g * (lp > -0.5f ? -expm1_small(lp) : 1.f - p);   // 1 - p without cancellation
+            const float lpt = lp - s.logS_lo;                          // log p of the target, both halves
+            return g * (lpt > -0.5f ? -expm1_small(lpt) : 1.f - p);   // 1 - p without cancellation
         }
         return (p == 0.f) ? 0.f : -g * p * ((t - s.c_hi) - s.c_lo);
     }
 }
 
+// k_pq = log S_P - log S_Q of the row (double-float): log q_j - log p_j =
+// (t^Q_j - t^P_j) + k_pq. Where that difference d is small, q - p cancels, and
+// the bf16 path evaluates it as p (e^d - 1) with a series for e^d - 1.
 template <typename T, bool kDP, bool kDQ>
-__device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, float g,
-                                             bool p_nan, float &dp, float &dq) {
+__device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, const DF &k_pq,
+                                             float g, bool p_nan, float &dp, float &dq) {
     if constexpr (Elem<T>::kPrecise) {
         const DF tp = df_diff(zp, sp.m), tq = df_diff(zq, sq.m);
         const DF lp = df_sub(tp, sp.logS_hi, sp.logS_lo), lq = df_sub(tq, sq.logS_hi, sq.logS_lo);
@@ -111,7 +103,10 @@ __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &
     } else {
         const float tp = zp - sp.m, tq = zq - sq.m;          // exact for bf16 values
         const float p = Elem<T>::exp(tp - sp.logS_hi), q = Elem<T>::exp(tq - sq.logS_hi);
-        if (kDQ) dq = g * (q - p);
+        if (kDQ) {
+            const float d = ((tq - tp) + k_pq.hi) + k_pq.lo;  // log q - log p
+            dq = g * (fabsf(d) < 0.5f ? p * expm1_small(d) : q - p);
+        }
         if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * (((tp - tq) - sp.c_hi) - sp.c_lo);
     }
 }
@@ -228,27 +223,19 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
 // every warp reads the row's K (id, g) pairs once and reduces them in a fixed
 // order (no CTA barrier; the same Gsum in every warp), the CTA writes
 // -Gsum p_j over the row tile by tile, then the warp that stored an id's
-// element rewrites it as G_j (1 - p_j) - p_j (Gsum - G_j), 1 - p_j without
-// cancellation (after a warp barrier, so the later store wins). Duplicate ids
+// element rewrites it as G_j (1 - p_j) - p_j Gother_j in fp64 (topk_target_elem;
+// after a warp barrier, so the later store wins). Duplicate ids
 // rewrite the same value. A row holding an id outside the shard is NaN (error
 // bit); a row whose ids are all ignored is 0.
 // --------------------------------------------------------------------------
-template <typename T>
-__device__ __forceinline__ float topk_target_elem(float z, const RowStat &s, float G, float gsum) {
-    if constexpr (Elem<T>::kPrecise) {
-        const DF t = df_diff(z, s.m);
-        const DF lp = df_sub(t, s.logS_hi, s.logS_lo);
-        const DF p = exp_df(lp.hi, lp.lo);
-        const float ph = p.hi * gsum;
-        const DF pg{ph, fmaf(p.hi, gsum, -ph) + p.lo * gsum};   // gsum p, error-free to fp32 rounding of lo
-        const DF d = df_sub(DF{G, 0.f}, pg.hi, pg.lo);
-        return d.hi + d.lo;
-    } else {
-        const float lp = (z - s.m) - s.logS_hi;
-        const float p = Elem<T>::exp(lp);
-        const float omp = lp > -0.5f ? -expm1_small(lp) : 1.f - p;
-        return G * omp - p * (gsum - G);
-    }
+// An id's own element: G (1 - p) - p Gother, where G sums the upstream
+// gradients of the ids equal to this one and Gother those of the row's other
+// (not ignored) ids, in fp64 (a row has only K such elements): 1 - p is taken
+// as -(e^{log p} - 1), so neither it nor the difference of the two terms
+// loses accuracy when p ~ 1 or when the terms nearly cancel.
+__device__ __forceinline__ float topk_target_elem(float z, const RowStat &s, double G, double Gother) {
+    const double lp = (((double)z - (double)s.m) - (double)s.logS_hi) - (double)s.logS_lo;
+    return (float)(G * -expm1(lp) - exp(lp) * Gother);
 }
 
 template <typename T>
@@ -354,10 +341,13 @@ topk_grad_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const Row
             if (t < 0) continue;
             const int j = (int)(t - vocab_start);          // in [0, V): the row has no id outside the shard
             if ((owner(j) >> 5) != warp) continue;
-            float G = 0.f;                                 // every id equal to this one, in id order
-            for (int64_t k2 = 0; k2 < K; ++k2)
-                if (tr[k2] == t) G += gr[k2];
-            Elem<T>::store1(out + j, topk_target_elem<T>(Elem<T>::load1(in + j), s, G, gsum));
+            double G = 0.0, Gother = 0.0;                  // ids equal to this one / the other ids, in id order
+            for (int64_t k2 = 0; k2 < K; ++k2) {
+                const int64_t t2 = tr[k2];
+                if (t2 == t) G += gr[k2];
+                else if (t2 >= 0) Gother += gr[k2];
+            }
+            Elem<T>::store1(out + j, topk_target_elem(Elem<T>::load1(in + j), s, G, Gother));
         }
     }
 }
@@ -372,19 +362,22 @@ topk_grad_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const Row
 template <typename T>
 struct KLGradRow {
     RowStat sp, sq;
+    DF k_pq;   // log S_P - log S_Q
     float g;
     bool all_nan, p_nan;
     __device__ __forceinline__ KLGradRow(const RowStat *stats_p, const RowStat *stats_q, const float *g_in,
                                          int64_t r) {
         sp = load_rowstat(stats_p + r);
         sq = load_rowstat(stats_q + r);
+        k_pq = two_sum(sp.logS_hi, -sq.logS_hi);
+        k_pq.lo = __fadd_rn(k_pq.lo, __fsub_rn(sp.logS_lo, sq.logS_lo));
         g = g_in[r];
         all_nan = (sp.flags & (kRowNanInf | kRowEmpty)) || (sq.flags & kRowNanInf);
         p_nan = all_nan || (sp.flags & kRowMismatch);
     }
     template <bool kDP, bool kDQ>
     __device__ __forceinline__ void elem(float zp, float zq, float &dp, float &dq) const {
-        kl_grad_elem<T, kDP, kDQ>(zp, zq, sp, sq, g, p_nan, dp, dq);
+        kl_grad_elem<T, kDP, kDQ>(zp, zq, sp, sq, k_pq, g, p_nan, dp, dq);
     }
 };
 

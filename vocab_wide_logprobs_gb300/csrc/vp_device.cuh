@@ -235,6 +235,19 @@ __device__ __forceinline__ DF exp_df(float a_hi, float a_lo) {
     return e;
 }
 
+// e^x - 1 for |x| < 1/2 by its Taylor series to x^8/8! (relative error < 1e-8 there):
+// used where e^x - 1 would cancel.
+__device__ __forceinline__ float expm1_small(float x) {
+    float t = 2.4801587301587302e-05f;      // 1/8!
+    t = fmaf(t, x, 1.9841269841269841e-04f);  // 1/7!
+    t = fmaf(t, x, 1.3888888888888889e-03f);  // 1/6!
+    t = fmaf(t, x, 8.3333333333333333e-03f);  // 1/5!
+    t = fmaf(t, x, 4.1666666666666667e-02f);  // 1/4!
+    t = fmaf(t, x, 1.6666666666666667e-01f);  // 1/3!
+    t = fmaf(t, x, 0.5f);                     // 1/2!
+    return fmaf(t * x, x, x);                 // x + x^2 (1/2 + x/6 + ...)
+}
+
 // Product (x_hi + x_lo) * (y_hi + y_lo) rounded once to fp32.
 __device__ __forceinline__ float df_mul_round(const DF &x, const DF &y) {
     const float p = x.hi * y.hi;

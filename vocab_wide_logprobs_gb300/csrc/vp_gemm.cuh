@@ -68,9 +68,10 @@ __device__ __forceinline__ void tile_coords(int64_t tile, int n_mb, int n_nb, in
     nb = w / gm;
 }
 
-template <class Epi, bool kAMn = false, bool kBMn = false>
+template <class Epi, bool kAMn = false, bool kBMn = false, bool kChain = false>
 __global__ void __launch_bounds__(kLThreads, 1)
-umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, int M, int Nn,
+umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                 const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M, int Nn,
                  int K, int group_m, int l2hints, const Epi epi) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ LinearBars bars;
@@ -79,6 +80,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     const int n_mb = (M + kLBM - 1) / kLBM, n_nb = (Nn + kLBN - 1) / kLBN;
     const int64_t n_tiles = (int64_t)n_mb * n_nb;
     const int n_k = (K + kLBK - 1) / kLBK;
+    const int n_kt = kChain ? 2 * n_k : n_k;   // a chained second product (A2 . B2^T, K deep) follows
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kLStages; ++s) {
@@ -109,26 +111,29 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
             for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
                 int mb, nb;
                 tile_coords(tile, n_mb, n_nb, group_m, mb, nb);
-                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                for (int kb = 0; kb < n_kt; ++kb, ++it) {
                     const uint32_t st = it % kLStages, use = it / kLStages;
                     if (use > 0 && !mbar_wait(&bars.empty[st], (use - 1) & 1)) { ok = false; break; }
                     uint8_t *a = smem + st * kLStageBytes;
                     mbar_arrive_expect_tx(&bars.full[st], kLStageBytes);
+                    const bool second = kChain && kb >= n_k;
+                    const CUtensorMap *ma = second ? &tm_a2 : &tm_a, *mbm = second ? &tm_b2 : &tm_b;
+                    const int kc = (second ? kb - n_k : kb) * kLBK;
                     if (kAMn) {
 #pragma unroll
                         for (int i = 0; i < kLBM / 64; ++i)
-                            tma_load_2d_hint(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK,
-                                             &bars.full[st], pol_a);
+                            tma_load_2d_hint(a + i * kLMnAtomBytes, ma, mb * kLBM + 64 * i, kc, &bars.full[st],
+                                             pol_a);
                     } else {
-                        tma_load_2d_hint(a, &tm_a, kb * kLBK, mb * kLBM, &bars.full[st], pol_a);
+                        tma_load_2d_hint(a, ma, kc, mb * kLBM, &bars.full[st], pol_a);
                     }
                     if (kBMn) {
 #pragma unroll
                         for (int i = 0; i < kLBN / 64; ++i)
-                            tma_load_2d_hint(a + kLAStage + i * kLMnAtomBytes, &tm_b, nb * kLBN + 64 * i, kb * kLBK,
+                            tma_load_2d_hint(a + kLAStage + i * kLMnAtomBytes, mbm, nb * kLBN + 64 * i, kc,
                                              &bars.full[st], pol_b);
                     } else {
-                        tma_load_2d_hint(a + kLAStage, &tm_b, kb * kLBK, nb * kLBN, &bars.full[st], pol_b);
+                        tma_load_2d_hint(a + kLAStage, mbm, kc, nb * kLBN, &bars.full[st], pol_b);
                     }
                 }
             }
@@ -145,7 +150,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                 if (use_b > 0 && !mbar_wait(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + buf * kLBN;
-                for (int kb = 0; kb < n_k; ++kb, ++it) {
+                for (int kb = 0; kb < n_kt; ++kb, ++it) {
                     const uint32_t st = it % kLStages;
                     if (!mbar_wait(&bars.full[st], (it / kLStages) & 1)) { ok = false; break; }
                     tc_fence_after();
@@ -244,12 +249,13 @@ static_assert(4 * kPairDualRegsLow + 8 * kPairDualRegsHigh == 12 * kPairDualRegs
 __host__ __device__ constexpr int pair_threads(bool dual) { return dual ? 12 * 32 : kLThreads; }
 __host__ __device__ constexpr int pair_epi_first_warp(bool dual) { return dual ? 4 : 2; }
 
-template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false>
+template <class Epi, bool kAMn = false, bool kBMn = false, bool kDual = false, bool kChain = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(kDual), 1)
 umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2, int M,
                       int Nn, int K, int K2, int group_m, int l2hints, const Epi epi) {
     static_assert(!kDual || (!kAMn && !kBMn), "the dual form takes K-major operands");
+    static_assert(!(kDual && kChain), "one second product at a time");
     extern __shared__ uint8_t smem_raw[];
     __shared__ PairBars bars;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -258,7 +264,7 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
     const int n_mp = (M + 2 * kLBM - 1) / (2 * kLBM), n_nb = (Nn + kLBN - 1) / kLBN;
     const int64_t n_tiles = (int64_t)n_mp * n_nb;
     const int n_k = (K + kLBK - 1) / kLBK;
-    const int n_k2 = kDual ? (K2 + kLBK - 1) / kLBK : 0;   // k-blocks of the second product
+    const int n_k2 = (kDual || kChain) ? (K2 + kLBK - 1) / kLBK : 0;   // k-blocks of the second product
     const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
     constexpr int kEpiThreads = pair_threads(kDual) - 32 * pair_epi_first_warp(kDual);
 
@@ -305,25 +311,23 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     uint8_t *a = smem + st * kPStageBytes;
                     const uint32_t fb = cluster_addr(&bars.full[st], 0);
                     if (rank == 0) mbar_arrive_expect_tx(&bars.full[st], 2 * kPStageBytes);
-                    if (kDual && kb >= n_k) {                // second product
-                        tma_load_2d_pair(a, &tm_a2, (kb - n_k) * kLBK, mb * kLBM, fb, pol_a);
-                        tma_load_2d_pair(a + kPAStage, &tm_b2, (kb - n_k) * kLBK, nrow, fb, pol_b);
-                        continue;
-                    }
+                    // k-blocks past n_k belong to the second product (its own maps)
+                    const bool second = (kDual || kChain) && kb >= n_k;
+                    const CUtensorMap *ma = second ? &tm_a2 : &tm_a, *mbm = second ? &tm_b2 : &tm_b;
+                    const int kc = (second ? kb - n_k : kb) * kLBK;
                     if (kAMn) {
 #pragma unroll
                         for (int i = 0; i < kLBM / 64; ++i)
-                            tma_load_2d_pair(a + i * kLMnAtomBytes, &tm_a, mb * kLBM + 64 * i, kb * kLBK, fb, pol_a);
+                            tma_load_2d_pair(a + i * kLMnAtomBytes, ma, mb * kLBM + 64 * i, kc, fb, pol_a);
                     } else {
-                        tma_load_2d_pair(a, &tm_a, kb * kLBK, mb * kLBM, fb, pol_a);
+                        tma_load_2d_pair(a, ma, kc, mb * kLBM, fb, pol_a);
                     }
                     if (kBMn) {
 #pragma unroll
                         for (int i = 0; i < kPBHalf / 64; ++i)
-                            tma_load_2d_pair(a + kPAStage + i * kLMnAtomBytes, &tm_b, nrow + 64 * i, kb * kLBK, fb,
-                                             pol_b);
+                            tma_load_2d_pair(a + kPAStage + i * kLMnAtomBytes, mbm, nrow + 64 * i, kc, fb, pol_b);
                     } else {
-                        tma_load_2d_pair(a + kPAStage, &tm_b, kb * kLBK, nrow, fb, pol_b);
+                        tma_load_2d_pair(a + kPAStage, mbm, kc, nrow, fb, pol_b);
                     }
                 }
             }
@@ -343,7 +347,8 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
                     if (use_b > 0 && !mbar_wait_cluster(&bars.acc_empty[buf], (use_b - 1) & 1)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d = tmem + buf * kLBN;
-                    const int nkb = p ? n_k2 : n_k;
+                    // a chained second product accumulates into the same accumulator
+                    const int nkb = kChain ? n_k + n_k2 : p ? n_k2 : n_k;
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const uint32_t st = it % kPStages;
                         if (!mbar_wait(&bars.full[st], (it / kPStages) & 1)) { ok = false; break; }
@@ -418,6 +423,29 @@ umma_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_con
     cluster_sync();                                      // no arrival or copy still targets either CTA
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(tmem, kLTmemCols);
+}
+
+// dz of the backward K1 epilogues: n (a multiple of 8) consecutive values as
+// bf16, rounded to nearest even, at dst (16-byte stores). With lo_off != 0 the
+// remainders x - bf16(x) (exact in fp32), rounded to bf16, go to dst + lo_off,
+// the dz_lo buffer of the chained gradient GEMMs.
+template <int n>
+__device__ __forceinline__ void store_dz(__nv_bfloat16 *dst, const float (&d)[n], int64_t lo_off) {
+    static_assert(n % 8 == 0, "whole 16-byte vectors");
+#pragma unroll
+    for (int k = 0; k < n / 8; ++k) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float x0 = d[8 * k + 2 * i], x1 = d[8 * k + 2 * i + 1];
+            const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+            hi[i] = *reinterpret_cast<const uint32_t *>(&h);
+            const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+            lo[i] = *reinterpret_cast<const uint32_t *>(&l);
+        }
+        reinterpret_cast<uint4 *>(dst)[k] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        if (lo_off) reinterpret_cast<uint4 *>(dst + lo_off)[k] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
 }
 
 // Backward K2 epilogue: acc[row][col] (+)= tile, fp32 (pitch ld).
@@ -537,14 +565,15 @@ static bool make_map_mn(CUtensorMap *map, const void *ptr, int64_t rows, int64_t
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <class Epi, bool kAMn = false, bool kBMn = false>
-static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, int group_m,
-                                    int l2hints, const Epi &epi, cudaStream_t stream) {
+template <class Epi, bool kAMn = false, bool kBMn = false, bool kChain = false>
+static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
+                                    const CUtensorMap &tb2, int M, int Nn, int K, int group_m, int l2hints,
+                                    const Epi &epi, cudaStream_t stream) {
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi, kAMn, kBMn>,
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_kernel<Epi, kAMn, kBMn, kChain>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
         if (e != cudaSuccess) return e;
         attr_done.fetch_or(1ull << (dev & 63));
@@ -557,8 +586,8 @@ static cudaError_t launch_gemm_impl(const CUtensorMap &ta, const CUtensorMap &tb
     if (group_m <= 0)   // about 32 MB of A per m-group
         group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / ((int64_t)kLBM * K * 2));
     if (group_m > n_mb) group_m = n_mb;
-    umma_gemm_kernel<Epi, kAMn, kBMn><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, M, Nn, K, group_m, l2hints,
-                                                                                epi);
+    umma_gemm_kernel<Epi, kAMn, kBMn, kChain><<<grid, kLThreads, kLSmemBytes, stream>>>(ta, tb, ta2, tb2, M, Nn, K,
+                                                                                        group_m, l2hints, epi);
     return cudaGetLastError();
 }
 
@@ -587,13 +616,13 @@ constexpr int kHintK3 = 2 | (2 << 2);
 template <class Epi, bool kAMn = false, bool kBMn = false>
 static cudaError_t launch_gemm(const CUtensorMap &ta, const CUtensorMap &tb, int M, int Nn, int K, const Epi &epi,
                                cudaStream_t stream, int group_m = 0, int l2hints = kHintLogits) {
-    return launch_gemm_impl<Epi, kAMn, kBMn>(ta, tb, M, Nn, K, group_m, l2hints, epi, stream);
+    return launch_gemm_impl<Epi, kAMn, kBMn>(ta, tb, ta, tb, M, Nn, K, group_m, l2hints, epi, stream);
 }
 
 // CTA-pair form (umma_gemm_pair_kernel): K-major B maps need boxes of 128 rows
 // (kPBHalf); MN-major maps are the same 64 x 64 boxes as for one CTA. group_m
 // counts 256-row pair blocks; <= 0 picks about 32 MB of A per group.
-template <class Epi, bool kAMn, bool kBMn, bool kDual>
+template <class Epi, bool kAMn, bool kBMn, bool kDual, bool kChain = false>
 static cudaError_t launch_gemm_pair_impl(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                                         const CUtensorMap &tb2, int M, int Nn, int K, int K2, const Epi &epi,
                                         cudaStream_t stream, int group_m, int l2hints) {
@@ -601,7 +630,7 @@ static cudaError_t launch_gemm_pair_impl(const CUtensorMap &ta, const CUtensorMa
     int dev = 0;
     cudaGetDevice(&dev);
     if (!(attr_done.load() & (1ull << (dev & 63)))) {
-        cudaError_t e = cudaFuncSetAttribute(umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual>,
+        cudaError_t e = cudaFuncSetAttribute(umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual, kChain>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
         if (kDual) {
@@ -609,7 +638,7 @@ static cudaError_t launch_gemm_pair_impl(const CUtensorMap &ta, const CUtensorMa
             // kPairDualRegsLaunch registers a thread; with fewer, setmaxnreg.inc
             // would wait for registers that do not exist, so refuse instead
             cudaFuncAttributes fa;
-            if ((e = cudaFuncGetAttributes(&fa, umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual>)) != cudaSuccess)
+            if ((e = cudaFuncGetAttributes(&fa, umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual, kChain>)) != cudaSuccess)
                 return e;
             if (fa.numRegs != kPairDualRegsLaunch) return cudaErrorInvalidConfiguration;
         }
@@ -624,7 +653,7 @@ static cudaError_t launch_gemm_pair_impl(const CUtensorMap &ta, const CUtensorMa
     if (group_m <= 0)   // about 32 MB of A (both products' A tiles in the dual form) per m-group
         group_m = (int)std::max<int64_t>(1, ((int64_t)32 << 20) / ((int64_t)2 * kLBM * (K + (kDual ? K2 : 0)) * 2));
     if (group_m > n_mp) group_m = n_mp;
-    umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual><<<grid, pair_threads(kDual), kPSmemBytes, stream>>>(
+    umma_gemm_pair_kernel<Epi, kAMn, kBMn, kDual, kChain><<<grid, pair_threads(kDual), kPSmemBytes, stream>>>(
         ta, tb, ta2, tb2, M, Nn, K, K2, group_m, l2hints, epi);
     return cudaGetLastError();
 }
@@ -681,6 +710,10 @@ static int64_t chunk_cols(int64_t N, int64_t V) {
 //       chunk stores; the last one (last = true) writes bf16(acc + tile) to
 //       dhidden instead)
 //   K3  dW_c = dz^T . h    (A = dz MN-major, B = h MN-major, K = N), written as bf16
+// With dz_lo (the same layout) dz is the pair dz_hi + dz_lo of bf16 values
+// (dz_hi = dz rounded to bf16, dz_lo = the remainder rounded to bf16, about 16
+// significant bits together), and each GEMM chains a second product with
+// dz_lo in place of dz into the same fp32 accumulator, at twice the work.
 // acc and dW may each be null (that GEMM is skipped); dhidden is non-null when
 // acc is. Both GEMMs stream two
 // operands far larger than L2 along a long K, so their tiles run in small
@@ -694,30 +727,44 @@ static int64_t chunk_cols(int64_t N, int64_t V) {
 #endif
 constexpr int kGradGroupM = VP_K2_GROUP;   // K2: m-blocks of dz (8 MB each at vc = 32768) x the 16 n-blocks of D = 4096
 constexpr int kWGroupM = VP_K3_GROUP;      // K3: m-blocks of dz^T (2 MB each at N = 8192) x the n-blocks of D
+
+template <class Epi, bool kAMn, bool kBMn>
+static cudaError_t launch_grad_gemm(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
+                                    bool chain, int M, int Nn, int K, const Epi &epi, cudaStream_t stream,
+                                    int group_m, int l2hints) {
+    if (kGemmPairs)
+        return chain ? launch_gemm_pair_impl<Epi, kAMn, kBMn, false, true>(ta, tb, ta2, tb, M, Nn, K, K, epi, stream,
+                                                                          (group_m + 1) / 2, l2hints)
+                     : launch_gemm_pair_impl<Epi, kAMn, kBMn, false>(ta, tb, ta, tb, M, Nn, K, 0, epi, stream,
+                                                                    (group_m + 1) / 2, l2hints);
+    return chain ? launch_gemm_impl<Epi, kAMn, kBMn, true>(ta, tb, ta2, tb, M, Nn, K, group_m, l2hints, epi, stream)
+                 : launch_gemm_impl<Epi, kAMn, kBMn>(ta, tb, ta, tb, M, Nn, K, group_m, l2hints, epi, stream);
+}
+
 static cudaError_t chunk_gradient_gemms(const CUtensorMap &tm_h_mn, const __nv_bfloat16 *W, int N, int D, int64_t v0,
-                                        int nv, int64_t vc, const __nv_bfloat16 *dz, float *acc,
-                                        __nv_bfloat16 *dhidden, __nv_bfloat16 *dW, bool last, cudaStream_t stream) {
+                                        int nv, int64_t vc, const __nv_bfloat16 *dz, const __nv_bfloat16 *dz_lo,
+                                        float *acc, __nv_bfloat16 *dhidden, __nv_bfloat16 *dW, bool last,
+                                        cudaStream_t stream) {
     cudaError_t e;
+    const bool chain = dz_lo != nullptr;
     if (acc) {
-        CUtensorMap tm_dz, tm_wc_mn;
-        if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D))
+        CUtensorMap tm_dz, tm_dz_lo, tm_wc_mn;
+        if (!make_map(&tm_dz, dz, N, nv, vc, kLBM) || !make_map_mn(&tm_wc_mn, W + v0 * D, nv, D, D) ||
+            (chain && !make_map(&tm_dz_lo, dz_lo, N, nv, vc, kLBM)))
             return cudaErrorInvalidValue;
         const AccEpi ae{N, D, v0 == 0, acc, last ? dhidden : nullptr};
-        e = kGemmPairs ? launch_gemm_pair<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, (kGradGroupM + 1) / 2,
-                                                                kHintK2)
-                       : launch_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, N, D, nv, ae, stream, kGradGroupM, kHintK2);
+        e = launch_grad_gemm<AccEpi, false, true>(tm_dz, tm_wc_mn, chain ? tm_dz_lo : tm_dz, chain, N, D, nv, ae,
+                                                  stream, kGradGroupM, kHintK2);
         if (e != cudaSuccess) return e;
     }
     if (dW) {
-        CUtensorMap tm_dz_mn;
-        if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc)) return cudaErrorInvalidValue;
+        CUtensorMap tm_dz_mn, tm_dz_lo_mn;
+        if (!make_map_mn(&tm_dz_mn, dz, N, nv, vc) || (chain && !make_map_mn(&tm_dz_lo_mn, dz_lo, N, nv, vc)))
+            return cudaErrorInvalidValue;
         const StoreBf16Epi se{nv, D, v0, dW};
-        e = kGemmPairs ? launch_gemm_pair<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream,
-                                                                     (kWGroupM + 1) / 2, kHintK3)
-                       : launch_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, nv, D, N, se, stream, kWGroupM,
-                                                               kHintK3);
-        if (e != cudaSuccess)
-            return e;
+        e = launch_grad_gemm<StoreBf16Epi, true, true>(tm_dz_mn, tm_h_mn, chain ? tm_dz_lo_mn : tm_dz_mn, chain, nv, D,
+                                                       N, se, stream, kWGroupM, kHintK3);
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

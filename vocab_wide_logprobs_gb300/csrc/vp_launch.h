@@ -8,6 +8,8 @@
 namespace vp {
 
 constexpr int VP_ERRBIT_TARGET_ = 1;  // same value as VP_ERRBIT_TARGET in include/vp.h
+constexpr int VP_GRAD_EXACT_ = 0;     // same values as VP_GRAD_EXACT / VP_GRAD_FAST in include/vp.h
+constexpr int VP_GRAD_FAST_ = 1;
 
 struct StatsArgs {
     const void *x;
@@ -119,6 +121,7 @@ struct LinearBwdArgs {
     void *workspace;              // linear_bwd_workspace_bytes(N, V, D)
     int32_t *err;
     cudaStream_t stream;
+    int precision = 0;            // VP_GRAD_EXACT: dz as a bf16 pair hi + lo; VP_GRAD_FAST: dz in bf16
 };
 
 size_t linear_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D);
@@ -144,6 +147,7 @@ struct LinearEntArgs {
     void *workspace;
     cudaStream_t stream;
     void *parts = nullptr;        // forward: vp_partial [N], the shard's records instead of H and stats
+    int precision = 0;            // backward: VP_GRAD_EXACT or VP_GRAD_FAST (as LinearBwdArgs)
 };
 
 size_t linear_entropy_workspace_bytes(int64_t N, int64_t V);
@@ -165,6 +169,7 @@ struct LinearKLArgs {
     cudaStream_t stream;
     float beta = 0.f;             // generalized JSD: 0 < beta < 1 (the KL calls at 0 and 1)
     void *parts = nullptr;        // KL forward: vp_partial [N], the shard's records instead of KL and stats
+    int precision = 0;            // backward: VP_GRAD_EXACT or VP_GRAD_FAST (as LinearBwdArgs)
 };
 
 size_t linear_kl_workspace_bytes(int64_t N, int64_t V);

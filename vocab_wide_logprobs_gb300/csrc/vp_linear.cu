@@ -29,6 +29,8 @@
 //   fixed order, and writes logp and the vp_rowstat record (fp64 finish).
 // Scratch: float2 partials [N][ceil(V/256)] and the target logits [N] fp32,
 //   in a caller-provided workspace (see vp_linear_logp_workspace_size).
+#include <mutex>
+
 #include "vp_gemm.cuh"
 #include "vp_stats.cuh"
 
@@ -79,10 +81,12 @@ struct LseEpi {
 
 // Backward K1 epilogue: dz = g (onehot - p), p = exp((z - m) - logS), for a
 // 256-column tile of a vocabulary chunk starting at shard column v0, written
-// as bf16 (round to nearest even) row-major dz[row][col] (pitch ldz); the two
-// gradient GEMMs read it in place, dz^T through an MN-major tensor map. Rows
-// with an ignored target get 0, rows with a data error or without valid
-// statistics get NaN.
+// as bf16 (round to nearest even) row-major dz[row][col] (pitch ldz), and with
+// lo_off != 0 the remainder as a second bf16 array at dz + lo_off (store_dz);
+// the gradient GEMMs read both in place, dz^T through an MN-major tensor map.
+// At the target 1 - p is formed as -(e^{log p} - 1) where p > e^{-1/2}, so it
+// keeps its relative accuracy as p -> 1. Rows with an ignored target get 0,
+// rows with a data error or without valid statistics get NaN.
 struct DzEpi {
     int N, V, v0, ldz;
     int64_t vocab_start;
@@ -91,6 +95,7 @@ struct DzEpi {
     const float *g;
     __nv_bfloat16 *dz;
     int32_t *err;
+    int64_t lo_off;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
         const bool valid = row < N;
         const RowStat s = load_rowstat(stats + (valid ? row : 0));
@@ -113,27 +118,21 @@ struct DzEpi {
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
-            uint32_t packed[16];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                float d[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = c * 32 + i + e;
-                    const float p = ex2_fast(((v[i + e] - s.m) - s.logS_hi) * kLog2e);
-                    float x = (col == tcol) ? gr * (1.f - p) : -gr * p;
-                    if (mode == 1 || col >= ncol) x = 0.f;
-                    else if (mode == 2) x = __int_as_float(0x7fc00000);
-                    d[e] = x;
+            for (int i = 0; i < 32; ++i) {
+                const int col = c * 32 + i;
+                const float lp = (v[i] - s.m) - s.logS_hi;
+                const float p = ex2_fast(lp * kLog2e);
+                float x = -gr * p;
+                if (col == tcol) {
+                    const float lpt = lp - s.logS_lo;
+                    x = gr * (lpt > -0.5f ? -expm1_small(lpt) : 1.f - p);
                 }
-                __nv_bfloat162 b = __floats2bfloat162_rn(d[0], d[1]);
-                packed[i / 2] = *reinterpret_cast<uint32_t *>(&b);
+                if (mode == 1 || col >= ncol) x = 0.f;
+                else if (mode == 2) x = __int_as_float(0x7fc00000);
+                v[i] = x;
             }
-            if (!valid) continue;
-            uint4 *dst = reinterpret_cast<uint4 *>(dz + (int64_t)row * ldz + col0 + c * 32);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+            if (valid) store_dz(dz + (int64_t)row * ldz + col0 + c * 32, v, lo_off);
         }
     }
 };
@@ -230,22 +229,48 @@ cudaError_t launch_linear_logp_fwd(const LinearFwdArgs &a) {
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device. In host code the
-// symbol's name is only a host-side stand-in, so the address is looked up once
-// per device with that device current, and cached.
+// Device address of g_noalloc_scratch in the current context. In host code the
+// symbol's name is only a host-side stand-in, so the address is looked up with
+// the device current (cudaGetSymbolAddress) at the first call on each device,
+// and cached together with the context it belongs to: a call from another
+// context on that device (after cudaDeviceReset, or a context the caller made
+// current) looks the address up again instead of reusing a stale one.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+static CUcontext current_context() {
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load();
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f);
+    }
+    CUcontext ctx = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f)(&ctx) == CUDA_SUCCESS ? ctx : nullptr;
+}
+
 static cudaError_t noalloc_scratch_address(void **out) {
-    static std::atomic<void *> cached[64];
+    struct Entry {
+        CUcontext ctx;
+        void *addr;
+    };
+    static Entry cached[64];
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    void *p = cached[dev].load();
-    if (!p) {
+    std::lock_guard<std::mutex> lock(mu);
+    CUcontext ctx = current_context();
+    if (!cached[dev].addr || !ctx || cached[dev].ctx != ctx) {
+        void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        cached[dev].store(p);
+        cached[dev] = Entry{current_context(), p};   // the lookup makes the primary context current if none was
     }
-    *out = p;
+    *out = cached[dev].addr;
     return cudaSuccess;
 }
 
@@ -278,11 +303,13 @@ struct BwdLayout {
     size_t dz, acc, total;
 };
 
+// dz of one chunk twice over (hi and lo halves of the exact form; the fast
+// form uses the first), then the fp32 dhidden accumulator
 static BwdLayout bwd_layout(int64_t N, int64_t V, int64_t D) {
     const int64_t vc = chunk_cols(N, V);
     BwdLayout L;
     L.dz = 0;
-    L.acc = L.dz + up256((size_t)N * vc * 2);
+    L.acc = L.dz + up256((size_t)2 * N * vc * 2);
     L.total = L.acc + up256((size_t)N * D * 4);
     return L;
 }
@@ -294,6 +321,7 @@ cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
     const int64_t vc = chunk_cols(a.N, a.V);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     __nv_bfloat16 *dz = reinterpret_cast<__nv_bfloat16 *>(ws + L.dz);
+    const int64_t lo_off = a.precision == VP_GRAD_EXACT_ ? a.N * vc : 0;   // dz_lo follows dz_hi
     float *acc = a.dhidden ? reinterpret_cast<float *>(ws + L.acc) : nullptr;
     const __nv_bfloat16 *h = static_cast<const __nv_bfloat16 *>(a.hidden);
     const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(a.weight);
@@ -306,10 +334,11 @@ cudaError_t launch_linear_logp_bwd(const LinearBwdArgs &a) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
         // K1 over this chunk's rows of W
         const DzEpi de{N, V, (int)v0, (int)vc, a.vocab_start, a.targets, static_cast<const RowStat *>(a.stats), a.g,
-                       dz, a.err};
+                       dz, a.err, lo_off};
         if ((e = launch_logits_gemm(h, W + v0 * D, N, nv, D, de, a.stream, kGemmPairs)) != cudaSuccess) return e;
-        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dhidden),
-                                      static_cast<__nv_bfloat16 *>(a.dW), v0 + vc >= V, a.stream)) != cudaSuccess)
+        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, lo_off ? dz + lo_off : nullptr, acc,
+                                      static_cast<__nv_bfloat16 *>(a.dhidden), static_cast<__nv_bfloat16 *>(a.dW),
+                                      v0 + vc >= V, a.stream)) != cudaSuccess)
             return e;
     }
     return cudaSuccess;

@@ -64,24 +64,28 @@ struct EntEpi {
             for (int i = 0; i < 32; ++i)
                 if (c * 32 + i < ncol) m = fmaxf(m, v[i]);
         }
-        float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
+        // each 32-column chunk summed in fp32, the chunks folded into double-floats
+        DF S{0.f, 0.f}, W{0.f, 0.f};
 #pragma unroll 1
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
             tmem_ld32(taddr + c * 32, v);
+            float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
                 const float t0 = v[i] - m, t1 = v[i + 1] - m;
-                const float e0 = c * 32 + i < ncol ? ex2_fast(t0 * kLog2e) : 0.f;
-                const float e1 = c * 32 + i + 1 < ncol ? ex2_fast(t1 * kLog2e) : 0.f;
+                const float e0 = c * 32 + i < ncol ? exp_fwd(t0) : 0.f;
+                const float e1 = c * 32 + i + 1 < ncol ? exp_fwd(t1) : 0.f;
                 s0 += e0;
                 s1 += e1;
                 w0 = e0 == 0.f ? w0 : fmaf(e0, t0, w0);   // zero-weight terms add nothing
                 w1 = e1 == 0.f ? w1 : fmaf(e1, t1, w1);
             }
+            df_add(S, s0 + s1);
+            df_add(W, w0 + w1);
         }
         if (row >= N) return;
-        parts[(int64_t)row * n_vt + col0 / kLBN] = EntTile{m, s0 + s1, w0 + w1, 0.f};
+        parts[(int64_t)row * n_vt + col0 / kLBN] = EntTile{m, S.hi + S.lo, W.hi + W.lo, 0.f};
     }
 };
 
@@ -113,6 +117,24 @@ __device__ __forceinline__ bool finite(float x) { return fabsf(x) < INFINITY; }
 
 __device__ __forceinline__ float2 pair128(const float (&v)[128], int i) { return make_float2(v[i], v[i + 1]); }
 
+// expm1_small (vp_device.cuh) on two values at once
+__device__ __forceinline__ float2 expm1_small2(float2 x) {
+    float2 t = splat(2.4801587301587302e-05f);                    // 1/8!
+    t = __ffma2_rn(t, x, splat(1.9841269841269841e-04f));          // 1/7!
+    t = __ffma2_rn(t, x, splat(1.3888888888888889e-03f));          // 1/6!
+    t = __ffma2_rn(t, x, splat(8.3333333333333333e-03f));          // 1/5!
+    t = __ffma2_rn(t, x, splat(4.1666666666666667e-02f));          // 1/4!
+    t = __ffma2_rn(t, x, splat(1.6666666666666667e-01f));          // 1/3!
+    t = __ffma2_rn(t, x, splat(0.5f));                             // 1/2!
+    return __ffma2_rn(__fmul2_rn(t, x), x, x);
+}
+
+// q - p from p and d = log q - log p: p (e^d - 1) where |d| < 1/2 (q ~ p, where
+// the difference of the two exponentials would cancel), else q - p
+__device__ __forceinline__ float q_minus_p(float q, float p, float d) {
+    return fabsf(d) < 0.5f ? p * expm1_small(d) : q - p;
+}
+
 // Dual-form epilogues: x holds the thread's 128 columns (one half of the
 // tile) of the first product, model A, already out of TMEM; tb is the TMEM
 // address of the same columns of the second product, model B, read here in
@@ -137,24 +159,28 @@ struct KLEpi {
                 }
         }
         const float mp = ma, mq = mb;
-        float sp = 0.f, sq = 0.f, w = 0.f;
+        DF SP{0.f, 0.f}, SQ{0.f, 0.f}, WW{0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float b[32];
             tmem_ld32(tb + c * 32, b);
+            float sp = 0.f, sq = 0.f, w = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const bool in = c * 32 + i < ncol;
                 const float vp = x[c * 32 + i], vq = b[i];
                 const float tP = vp - mp, tQ = vq - mq;
-                const float ep = in ? ex2_fast(tP * kLog2e) : 0.f;
-                const float eq = in ? ex2_fast(tQ * kLog2e) : 0.f;
+                const float ep = in ? exp_fwd(tP) : 0.f;
+                const float eq = in ? exp_fwd(tQ) : 0.f;
                 sp += ep;
                 sq += eq;
                 w = ep == 0.f ? w : fmaf(ep, tP - tQ, w);
             }
+            df_add(SP, sp);
+            df_add(SQ, sq);
+            df_add(WW, w);
         }
-        return KLTile{mp, sp, mq, sq, w, 0.f, 0.f, 0.f};
+        return KLTile{mp, SP.hi + SP.lo, mq, SQ.hi + SQ.lo, WW.hi + WW.lo, 0.f, 0.f, 0.f};
     }
 
     // a full tile, two columns per instruction and no per-column tests: a zero
@@ -175,25 +201,29 @@ struct KLEpi {
             tmem_ld32(tb + c * 32, b);
             mb = max32(mb, b);
         }
-        const float2 nma = splat(-ma), nmb = splat(-mb), l2e = splat(kLog2e), m1 = splat(-1.f);
-        float2 sa[2] = {splat(0.f), splat(0.f)}, sb[2] = {splat(0.f), splat(0.f)}, w[2] = {splat(0.f), splat(0.f)};
+        const float2 nma = splat(-ma), nmb = splat(-mb), m1 = splat(-1.f);
+        // each 32-column chunk summed in fp32 (f32x2), the chunks folded into double-floats
+        DF SA{0.f, 0.f}, SB{0.f, 0.f}, WW{0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float b[32];
             tmem_ld32(tb + c * 32, b);
+            float2 sa[2] = {splat(0.f), splat(0.f)}, sb[2] = {splat(0.f), splat(0.f)}, w[2] = {splat(0.f), splat(0.f)};
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
                 const int k = (i >> 1) & 1;
                 const float2 tA = __fadd2_rn(pair128(x, c * 32 + i), nma), tB = __fadd2_rn(pair_at(b, i), nmb);
-                const float2 eA = ex2_pair(__fmul2_rn(tA, l2e)), eB = ex2_pair(__fmul2_rn(tB, l2e));
+                const float2 eA = exp_fwd2(tA), eB = exp_fwd2(tB);
                 sa[k] = __fadd2_rn(sa[k], eA);
                 sb[k] = __fadd2_rn(sb[k], eB);
                 w[k] = __ffma2_rn(eA, __ffma2_rn(tB, m1, tA), w[k]);   // e_P (tP - tQ)
             }
+            const float2 a2 = __fadd2_rn(sa[0], sa[1]), b2 = __fadd2_rn(sb[0], sb[1]), w2 = __fadd2_rn(w[0], w[1]);
+            df_add(SA, a2.x + a2.y);
+            df_add(SB, b2.x + b2.y);
+            df_add(WW, w2.x + w2.y);
         }
-        const float2 a2 = __fadd2_rn(sa[0], sa[1]), b2 = __fadd2_rn(sb[0], sb[1]), w2 = __fadd2_rn(w[0], w[1]);
-        const float SA = a2.x + a2.y, SB = b2.x + b2.y, W = w2.x + w2.y;
-        return KLTile{ma, SA, mb, SB, W, 0.f, 0.f, 0.f};
+        return KLTile{ma, SA.hi + SA.lo, mb, SB.hi + SB.lo, WW.hi + WW.lo, 0.f, 0.f, 0.f};
     }
 
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, const float (&x)[128], uint32_t tb) const {
@@ -387,33 +417,27 @@ linear_kl_merge_kernel(int N, int n_vt, const KLTile *__restrict__ parts, float 
 
 // ---------------------------------------------------------------------------
 // Backward K1 epilogues: dz of a 256-column tile of a vocabulary chunk, bf16
-// (round to nearest even), row-major [row][col] with pitch ldz; the gradient
-// GEMMs read it in place. Rows without valid statistics get NaN.
+// (round to nearest even), row-major [row][col] with pitch ldz, and with
+// lo_off != 0 the remainder at dz + lo_off (store_dz); the gradient GEMMs read
+// both in place. Rows without valid statistics get NaN.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void store_dz32(__nv_bfloat16 *dst, const float (&d)[32]) {
-    uint32_t packed[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(d[2 * i], d[2 * i + 1]);
-        packed[i] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) d4[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-}
 
 // Entropy: dz = -g p ((z - m) - c), c = W / S from the record (so that
-// (z - m) - c = log p + H).
+// (z - m) - c = log p + H), taken as (z - K_hi) - K_lo with K = m + c as a
+// double-float: where z ~ K the first difference is exact, so dz keeps its
+// relative accuracy where it cancels.
 struct DzEntEpi {
     int N, ldz;
     const RowStat *stats;
     const float *g;
     __nv_bfloat16 *dz;
+    int64_t lo_off;
     __device__ __forceinline__ void operator()(int row, int col0, int ncol, uint32_t taddr) const {
         const bool valid = row < N;
         const RowStat s = load_rowstat(stats + (valid ? row : 0));
         const bool nan = (s.flags & (kRowNanInf | kRowEmpty)) != 0;
         const float gr = valid ? g[row] : 0.f;
+        const DF K = df_from((double)s.m + ((double)s.c_hi + (double)s.c_lo));
 #pragma unroll 1
         for (int c = 0; c < kLBN / 32; ++c) {
             float v[32];
@@ -422,28 +446,18 @@ struct DzEntEpi {
             for (int i = 0; i < 32; ++i) {
                 const float t = v[i] - s.m;
                 const float p = ex2_fast((t - s.logS_hi) * kLog2e);
-                float x = p == 0.f ? 0.f : -gr * p * ((t - s.c_hi) - s.c_lo);
+                float x = p == 0.f ? 0.f : -gr * p * ((v[i] - K.hi) - K.lo);
                 if (c * 32 + i >= ncol) x = 0.f;
                 else if (nan) x = qnan();
                 v[i] = x;
             }
-            if (valid) store_dz32(dz + (int64_t)row * ldz + col0 + c * 32, v);
+            if (valid) store_dz(dz + (int64_t)row * ldz + col0 + c * 32, v, lo_off);
         }
     }
 };
 
 // KL(P||Q): dP = g p ((tP - tQ) - c), dQ = g (q - p), tX = X - m_X, c from P's
 // record; written to the dz of A and / or B (either may be null) by direction.
-// 8 consecutive gradient values as bf16 (round to nearest even), one 16-byte store.
-__device__ __forceinline__ void store_dz8(__nv_bfloat16 *dst, const float (&d)[8]) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        __nv_bfloat162 b = __floats2bfloat162_rn(d[2 * k], d[2 * k + 1]);
-        w[k] = *reinterpret_cast<uint32_t *>(&b);
-    }
-    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-}
 
 // KL(P||Q) with P the first product (the launcher puts the P model first);
 // dzp, dzq: the dz of P and of Q, either may be null.
@@ -452,21 +466,23 @@ struct DzKLEpi {
     const RowStat *sp, *sq;
     const float *g;
     __nv_bfloat16 *dzp, *dzq;
+    int64_t lo_off;
 
     // columns j0 .. j0 + 7 of the half tile (x[j0 + u], b[i0 + u]) with the
     // per-column tests: columns past ncol give 0, zero-weight terms give 0,
     // NaN rows give NaN
     __device__ __forceinline__ void checked(int j0, int i0, int ncol, bool nan, float gr, const RowStat &P,
-                                            const RowStat &Q, const float (&x)[128], const float (&b)[32],
-                                            float (&oa)[8], float (&ob)[8]) const {
+                                            const RowStat &Q, const DF &KP, const DF &KQ, const float (&x)[128],
+                                            const float (&b)[32], float (&oa)[8], float (&ob)[8]) const {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const float vp = x[j0 + u], vq = b[i0 + u];
             const float tP = vp - P.m, tQ = vq - Q.m;
             const float p = ex2_fast((tP - P.logS_hi) * kLog2e);
             const float q = ex2_fast((tQ - Q.logS_hi) * kLog2e);
-            float dP = p == 0.f ? 0.f : gr * p * (((tP - tQ) - P.c_hi) - P.c_lo);
-            float dQ = gr * (q - p);
+            const DF s = two_sum(vp, -vq);                           // vp - vq exactly
+            float dP = p == 0.f ? 0.f : gr * p * (((s.hi - KP.hi) - KP.lo) + s.lo);
+            float dQ = gr * q_minus_p(q, p, ((KQ.hi - s.hi) + KQ.lo) - s.lo);
             if (j0 + u >= ncol) dP = dQ = 0.f;
             else if (nan) dP = dQ = qnan();
             oa[u] = dP;
@@ -483,7 +499,14 @@ struct DzKLEpi {
         const bool full = ncol == kDualEpiCols;
         const float2 nPm = splat(-P.m), nQm = splat(-Q.m), l2e = splat(kLog2e), m1 = splat(-1.f);
         const float2 nCp = splat(-P.logS_hi * kLog2e), nCq = splat(-Q.logS_hi * kLog2e);
-        const float2 nch = splat(-P.c_hi), ncl = splat(-P.c_lo), g2 = splat(gr);
+        const float2 g2 = splat(gr);
+        // with s = vp - vq (exactly, as a double-float): (tP - tQ) - c = s - KP and
+        // log q - log p = KQ - s, KP = (m_P - m_Q) + c, KQ = (m_P - m_Q) + (log S_P - log S_Q);
+        // where either cancels, s and the constant are close and their difference is exact
+        const double dm = (double)P.m - (double)Q.m;
+        const DF KP = df_from(dm + ((double)P.c_hi + (double)P.c_lo));
+        const DF KQ = df_from(dm + (((double)P.logS_hi + (double)P.logS_lo) - ((double)Q.logS_hi + (double)Q.logS_lo)));
+        const float2 nkph = splat(-KP.hi), nkpl = splat(-KP.lo), kqh = splat(KQ.hi), kql = splat(KQ.lo);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             float b[32];
@@ -498,21 +521,32 @@ struct DzKLEpi {
                 float2 chk = splat(0.f);
 #pragma unroll
                 for (int u = 0; u < 8; u += 2) {
-                    const float2 tP = __fadd2_rn(pair128(x, j0 + u), nPm), tQ = __fadd2_rn(pair_at(b, i0 + u), nQm);
+                    const float2 vp = pair128(x, j0 + u), vq = pair_at(b, i0 + u);
+                    const float2 tP = __fadd2_rn(vp, nPm), tQ = __fadd2_rn(vq, nQm);
                     const float2 p = ex2_pair(__ffma2_rn(tP, l2e, nCp)), q = ex2_pair(__ffma2_rn(tQ, l2e, nCq));
-                    const float2 d = __fadd2_rn(__fadd2_rn(__ffma2_rn(tQ, m1, tP), nch), ncl);
+                    // s + e = vp - vq exactly (two-sum)
+                    const float2 s = __ffma2_rn(vq, m1, vp);
+                    const float2 bb = __ffma2_rn(vp, m1, s);
+                    const float2 e = __ffma2_rn(__fadd2_rn(vq, bb), m1, __ffma2_rn(__ffma2_rn(bb, m1, s), m1, vp));
+                    const float2 d = __fadd2_rn(__fadd2_rn(__fadd2_rn(s, nkph), nkpl), e);         // (tP - tQ) - c
                     chk = __fadd2_rn(chk, d);
-                    const float2 dP = __fmul2_rn(__fmul2_rn(g2, p), d), dQ = __fmul2_rn(g2, __ffma2_rn(p, m1, q));
+                    // q - p, as p (e^dd - 1) where q ~ p (q_minus_p)
+                    const float2 dd = __ffma2_rn(e, m1, __fadd2_rn(__ffma2_rn(s, m1, kqh), kql));    // log q - log p
+                    const float2 em = __fmul2_rn(p, expm1_small2(dd));
+                    float2 qp = __ffma2_rn(p, m1, q);
+                    qp.x = fabsf(dd.x) < 0.5f ? em.x : qp.x;
+                    qp.y = fabsf(dd.y) < 0.5f ? em.y : qp.y;
+                    const float2 dP = __fmul2_rn(__fmul2_rn(g2, p), d), dQ = __fmul2_rn(g2, qp);
                     oa[u] = dP.x;
                     oa[u + 1] = dP.y;
                     ob[u] = dQ.x;
                     ob[u + 1] = dQ.y;
                 }
-                if (!full || nan || !finite(chk.x + chk.y)) checked(j0, i0, ncol, nan, gr, P, Q, x, b, oa, ob);
+                if (!full || nan || !finite(chk.x + chk.y)) checked(j0, i0, ncol, nan, gr, P, Q, KP, KQ, x, b, oa, ob);
                 if (!valid) continue;
                 const int64_t off = (int64_t)row * ldz + col0 + j0;
-                if (dzp) store_dz8(dzp + off, oa);
-                if (dzq) store_dz8(dzq + off, ob);
+                if (dzp) store_dz(dzp + off, oa, lo_off);
+                if (dzq) store_dz(dzq + off, ob, lo_off);
             }
         }
     }
@@ -542,15 +576,18 @@ cudaError_t launch_linear_entropy_fwd(const LinearEntArgs &a) {
     return cudaGetLastError();
 }
 
+// dz of one chunk twice over (hi and lo halves of the exact form), then the
+// fp32 dhidden accumulator
 size_t linear_entropy_bwd_workspace_bytes(int64_t N, int64_t V, int64_t D) {
-    return up256((size_t)N * chunk_cols(N, V) * 2) + up256((size_t)N * D * 4);
+    return up256((size_t)2 * N * chunk_cols(N, V) * 2) + up256((size_t)N * D * 4);
 }
 
 cudaError_t launch_linear_entropy_bwd(const LinearEntArgs &a) {
     const int64_t vc = chunk_cols(a.N, a.V);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     __nv_bfloat16 *dz = reinterpret_cast<__nv_bfloat16 *>(ws);
-    float *acc = a.dhidden ? reinterpret_cast<float *>(ws + up256((size_t)a.N * vc * 2)) : nullptr;
+    const int64_t lo_off = a.precision == VP_GRAD_EXACT_ ? a.N * vc : 0;   // dz_lo follows dz_hi
+    float *acc = a.dhidden ? reinterpret_cast<float *>(ws + up256((size_t)2 * a.N * vc * 2)) : nullptr;
     const __nv_bfloat16 *h = static_cast<const __nv_bfloat16 *>(a.hidden);
     const __nv_bfloat16 *W = static_cast<const __nv_bfloat16 *>(a.weight);
     const int N = (int)a.N, V = (int)a.V, D = (int)a.D;
@@ -559,10 +596,11 @@ cudaError_t launch_linear_entropy_bwd(const LinearEntArgs &a) {
     if (!make_map_mn(&tm_h_mn, h, N, D, D)) return cudaErrorInvalidValue;
     for (int64_t v0 = 0; v0 < V; v0 += vc) {
         const int nv = (int)(V - v0 < vc ? V - v0 : vc);
-        const DzEntEpi de{N, (int)vc, static_cast<const RowStat *>(a.stats), a.g, dz};
+        const DzEntEpi de{N, (int)vc, static_cast<const RowStat *>(a.stats), a.g, dz, lo_off};
         if ((e = launch_logits_gemm(h, W + v0 * D, N, nv, D, de, a.stream, kGemmPairs)) != cudaSuccess) return e;
-        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, acc, static_cast<__nv_bfloat16 *>(a.dhidden),
-                                      static_cast<__nv_bfloat16 *>(a.dW), v0 + vc >= V, a.stream)) != cudaSuccess)
+        if ((e = chunk_gradient_gemms(tm_h_mn, W, N, D, v0, nv, vc, dz, lo_off ? dz + lo_off : nullptr, acc,
+                                      static_cast<__nv_bfloat16 *>(a.dhidden), static_cast<__nv_bfloat16 *>(a.dW),
+                                      v0 + vc >= V, a.stream)) != cudaSuccess)
             return e;
     }
     return cudaSuccess;
@@ -596,9 +634,10 @@ cudaError_t launch_linear_kl_fwd(const LinearKLArgs &a) {
     return cudaGetLastError();
 }
 
-// dz of A and of B for one chunk, then the fp32 dhidden accumulators of A and B.
+// dz of A and of B for one chunk (each twice over: the hi and lo halves of the
+// exact form), then the fp32 dhidden accumulators of A and B.
 size_t linear_kl_bwd_workspace_bytes(int64_t N, int64_t V, int64_t Da, int64_t Db) {
-    const size_t dz = up256((size_t)N * chunk_cols(N, V) * 2);
+    const size_t dz = up256((size_t)2 * N * chunk_cols(N, V) * 2);
     return 2 * dz + up256((size_t)N * Da * 4) + up256((size_t)N * Db * 4);
 }
 
@@ -606,11 +645,12 @@ size_t linear_kl_bwd_workspace_bytes(int64_t N, int64_t V, int64_t Da, int64_t D
 // both logits tiles and the epilogue made by make_epi(dza, dzb) writes dz of A
 // and / or B; then the gradient GEMMs of each model whose gradients are asked for.
 // b_first: the dual GEMM takes model B as its first product; make_epi(ldz,
-// dz of the first product, dz of the second) builds the epilogue.
+// dz of the first product, dz of the second, lo_off) builds the epilogue.
 template <class MakeEpi>
 static cudaError_t two_model_bwd(const LinearKLArgs &a, bool b_first, MakeEpi make_epi) {
     const int64_t vc = chunk_cols(a.N, a.V);
-    const size_t dz_bytes = up256((size_t)a.N * vc * 2);
+    const size_t dz_bytes = up256((size_t)2 * a.N * vc * 2);
+    const int64_t lo_off = a.precision == VP_GRAD_EXACT_ ? a.N * vc : 0;   // each dz_lo follows its dz_hi
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
     const bool want_a = a.dha || a.dwa, want_b = a.dhb || a.dwb;
     __nv_bfloat16 *dza = want_a ? reinterpret_cast<__nv_bfloat16 *>(ws) : nullptr;
@@ -631,16 +671,18 @@ static cudaError_t two_model_bwd(const LinearKLArgs &a, bool b_first, MakeEpi ma
         if (!make_map(&tm_wac, Wa + v0 * Da, nv, Da, Da, kPBHalf) ||
             !make_map(&tm_wbc, Wb + v0 * Db, nv, Db, Db, kPBHalf))
             return cudaErrorInvalidValue;
-        e = b_first ? launch_gemm_dual(tm_hb, tm_wbc, tm_ha, tm_wac, N, nv, Db, Da, make_epi((int)vc, dzb, dza), a.stream)
-                    : launch_gemm_dual(tm_ha, tm_wac, tm_hb, tm_wbc, N, nv, Da, Db, make_epi((int)vc, dza, dzb), a.stream);
+        e = b_first ? launch_gemm_dual(tm_hb, tm_wbc, tm_ha, tm_wac, N, nv, Db, Da, make_epi((int)vc, dzb, dza, lo_off),
+                                       a.stream)
+                    : launch_gemm_dual(tm_ha, tm_wac, tm_hb, tm_wbc, N, nv, Da, Db, make_epi((int)vc, dza, dzb, lo_off),
+                                       a.stream);
         if (e != cudaSuccess) return e;
         const bool last = v0 + vc >= V;
-        if (want_a && (e = chunk_gradient_gemms(tm_ha_mn, Wa, N, Da, v0, nv, vc, dza, acc_a,
-                                                static_cast<__nv_bfloat16 *>(a.dha),
+        if (want_a && (e = chunk_gradient_gemms(tm_ha_mn, Wa, N, Da, v0, nv, vc, dza, lo_off ? dza + lo_off : nullptr,
+                                                acc_a, static_cast<__nv_bfloat16 *>(a.dha),
                                                 static_cast<__nv_bfloat16 *>(a.dwa), last, a.stream)) != cudaSuccess)
             return e;
-        if (want_b && (e = chunk_gradient_gemms(tm_hb_mn, Wb, N, Db, v0, nv, vc, dzb, acc_b,
-                                                static_cast<__nv_bfloat16 *>(a.dhb),
+        if (want_b && (e = chunk_gradient_gemms(tm_hb_mn, Wb, N, Db, v0, nv, vc, dzb, lo_off ? dzb + lo_off : nullptr,
+                                                acc_b, static_cast<__nv_bfloat16 *>(a.dhb),
                                                 static_cast<__nv_bfloat16 *>(a.dwb), last, a.stream)) != cudaSuccess)
             return e;
     }
@@ -651,8 +693,8 @@ cudaError_t launch_linear_kl_bwd(const LinearKLArgs &a) {
     const bool p_is_a = a.direction == 0;
     const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
     // P first: the forward direction, KL(B||A), runs the dual GEMM with model B first
-    return two_model_bwd(a, !p_is_a, [&](int ldz, __nv_bfloat16 *dzp, __nv_bfloat16 *dzq) {
-        return DzKLEpi{(int)a.N, ldz, p_is_a ? sa : sb, p_is_a ? sb : sa, a.g, dzp, dzq};
+    return two_model_bwd(a, !p_is_a, [&](int ldz, __nv_bfloat16 *dzp, __nv_bfloat16 *dzq, int64_t lo_off) {
+        return DzKLEpi{(int)a.N, ldz, p_is_a ? sa : sb, p_is_a ? sb : sa, a.g, dzp, dzq, lo_off};
     });
 }
 
@@ -799,6 +841,7 @@ struct DzJsdEpi {
     const RowStat *sa, *sb;
     const float *g;
     __nv_bfloat16 *dza, *dzb;   // either may be null
+    int64_t lo_off;
 
     // columns j0 .. j0 + 7 of the half tile with the per-column tests: columns
     // past ncol give 0, zero-weight terms give 0, log2 mix kept above -250, NaN
@@ -866,8 +909,8 @@ struct DzJsdEpi {
                 if (!full || nan || !finite(chk.x + chk.y)) checked(j0, i0, ncol, nan, gr, A, B, x, b, oa, ob);
                 if (!valid) continue;
                 const int64_t off = (int64_t)row * ldz + col0 + j0;
-                if (dza) store_dz8(dza + off, oa);
-                if (dzb) store_dz8(dzb + off, ob);
+                if (dza) store_dz(dza + off, oa, lo_off);
+                if (dzb) store_dz(dzb + off, ob, lo_off);
             }
         }
     }
@@ -900,8 +943,8 @@ cudaError_t launch_linear_jsd_fwd(const LinearKLArgs &a) {
 
 cudaError_t launch_linear_jsd_bwd(const LinearKLArgs &a) {
     const RowStat *sa = static_cast<const RowStat *>(a.stats_a), *sb = static_cast<const RowStat *>(a.stats_b);
-    return two_model_bwd(a, false, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb) {
-        return DzJsdEpi{(int)a.N, ldz, a.beta, sa, sb, a.g, dza, dzb};
+    return two_model_bwd(a, false, [&](int ldz, __nv_bfloat16 *dza, __nv_bfloat16 *dzb, int64_t lo_off) {
+        return DzJsdEpi{(int)a.N, ldz, a.beta, sa, sb, a.g, dza, dzb, lo_off};
     });
 }
 

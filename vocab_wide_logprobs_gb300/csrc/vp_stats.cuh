@@ -15,8 +15,6 @@
 
 #include <string.h>
 
-#include <type_traits>
-
 #include "vp_device.cuh"
 #include "vp_launch.h"
 
@@ -75,6 +73,19 @@ __device__ __forceinline__ float ex2_fast(float a) {
     return y;
 }
 
+// e^t for the forward sums: the base-2 argument t log2(e) with log2(e) split
+// into fp32 hi + lo parts (the product with the hi part exact inside the FMA),
+// so that the sums are those of e^t and not of e^{t (1 - 1.3e-8)}: with the
+// fp32 constant alone, every weight is off by a factor e^{-1.3e-8 t}, which
+// moves the centred mean c = W / S by about 1.3e-8 Var_p(t) (~1e-7 for the
+// pages' logits), a bias the cancelling gradients (t ~ c) resolve.
+constexpr float kLog2eLo = 1.925963033500011e-08f;   // log2(e) - kLog2e
+__device__ __forceinline__ float exp_fwd(float t) { return ex2_fast(fmaf(t, kLog2e, t * kLog2eLo)); }
+__device__ __forceinline__ float2 exp_fwd2(float2 t) {
+    const float2 a = __ffma2_rn(t, make_float2(kLog2e, kLog2e), __fmul2_rn(t, make_float2(kLog2eLo, kLog2eLo)));
+    return make_float2(ex2_fast(a.x), ex2_fast(a.y));
+}
+
 __device__ __forceinline__ uint32_t word(const uint4 &u, int q) {
     return q == 0 ? u.x : q == 1 ? u.y : q == 2 ? u.z : u.w;
 }
@@ -130,7 +141,7 @@ struct Lane1 {
 #pragma unroll
             for (int i = 0; i < n; ++i) {
                 const float t = v[i] - ref;   // exact for bf16 values
-                const float e = Elem<T>::exp(t);
+                const float e = exp_fwd(t);
                 // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
                 if (i & 1) { s1 += e; if (kW) w1 = fmaf(e, fmaxf(t, -128.f), w1); }
                 else       { s0 += e; if (kW) w0 = fmaf(e, fmaxf(t, -128.f), w0); }
@@ -142,22 +153,23 @@ struct Lane1 {
 
     // bf16 fast path on raw 16-byte words (8 values each): packed max, packed
     // f32x2 arithmetic and four independent accumulator pairs. The chunk sums
-    // are added to the lane's running sums in plain fp32 (S.hi, W.hi; a lane
-    // takes about ten chunks per row); only the fp32 path carries double-floats.
+    // are folded into the lane's double-float sums with an error-free two-sum,
+    // so the only roundings left are those inside a chunk; the centred mean
+    // c = W / S of the row then carries ~2^-27 relative error, which the
+    // entropy gradient -p (t - c) needs where t ~ c.
     template <int K>
     __device__ __forceinline__ void push_bf16(const uint4 (&u)[K]) {
         const float c = max_bf16(u);
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
-        const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
+        const float2 nref = make_float2(-ref, -ref);
         float2 s[4], w[4];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
-                const float2 a = __fmul2_rn(t, l2e);
-                const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                const float2 e = exp_fwd2(t);
                 if (k == 0) {
                     s[q] = e;
                     if (kW) w[q] = __fmul2_rn(e, t);
@@ -168,7 +180,7 @@ struct Lane1 {
             }
         }
         const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
-        S.hi += ss.x + ss.y;
+        df_add(S, ss.x + ss.y);
         if (kW) {
             float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
             float wsum = ww.x + ww.y;
@@ -182,24 +194,24 @@ struct Lane1 {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);
-                        const float2 a = __fmul2_rn(t, l2e);
-                        const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
+                        const float2 e = exp_fwd2(t);
                         w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
                     }
                 }
                 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
                 wsum = ww.x + ww.y;
             }
-            W.hi += wsum;
+            df_add(W, wsum);
         }
     }
 };
 
-// Merged partials carry their sums in fp64 on the fp32 path and in fp32 on the
-// bf16 path (whose results are held to bf16 and 2e-5 accuracy); GB300's fp64
-// pipe is narrow, so the bf16 path keeps it for the one-thread row finish only.
+// Merged partials (a warp's, then the row's) carry their sums in fp64 on both
+// paths: a warp merges its lanes' double-floats, and the finisher warp
+// re-centres and adds the 8 warp partials of a row once per row, off the
+// consumers' critical path.
 template <typename T>
-using AccT = typename std::conditional<Elem<T>::kPrecise, double, float>::type;
+using AccT = double;
 
 __device__ __forceinline__ double exp_acc(double x) { return exp(x); }
 __device__ __forceinline__ float exp_acc(float x) { return expf(x); }
@@ -325,7 +337,7 @@ struct LaneKL {
 #pragma unroll
             for (int i = 0; i < n; ++i) {
                 const float tp = p[i] - rp, tq = q[i] - rq;
-                const float ep = Elem<T>::exp(tp), eq = Elem<T>::exp(tq);
+                const float ep = exp_fwd(tp), eq = exp_fwd(tq);
                 const float dl = (ep > 0.f) ? (tp - tq) : 0.f;  // zero-weight terms add nothing
                 if (i & 1) { sp1 += ep; sq1 += eq; w1 = fmaf(ep, dl, w1); }
                 else       { sp0 += ep; sq0 += eq; w0 = fmaf(ep, dl, w0); }
@@ -348,7 +360,7 @@ struct LaneKL {
         const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
         if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
         const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
-        const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
+        const float2 m1 = make_float2(-1.f, -1.f);
         float2 sp[4], sq[4], w[4];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -356,9 +368,7 @@ struct LaneKL {
             for (int q = 0; q < 4; ++q) {
                 const float2 tp = __fadd2_rn(bf16_pair(word(up[k], q)), nrp);
                 const float2 tq = __fadd2_rn(bf16_pair(word(uq[k], q)), nrq);
-                const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
-                const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
-                const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
+                const float2 ep = exp_fwd2(tp), eq = exp_fwd2(tq);
                 const float2 d = __ffma2_rn(tq, m1, tp);                             // tp - tq
                 if (k == 0) {
                     sp[q] = ep;
@@ -387,8 +397,7 @@ struct LaneKL {
                     const uint32_t pw = word(up[k], q), qw = word(uq[k], q);
                     fl |= __vcmpeq2(qw, kBf16NegInf2) & ~__vcmpeq2(pw, kBf16NegInf2);
                     const float2 tp = __fadd2_rn(bf16_pair(pw), nrp), tq = __fadd2_rn(bf16_pair(qw), nrq);
-                    const float2 ap = __fmul2_rn(tp, l2e);
-                    const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
+                    const float2 ep = exp_fwd2(tp);
                     float2 d = __ffma2_rn(tq, m1, tp);                            // tp - tq
                     d.x = ep.x > 0.f ? d.x : 0.f;                                 // zero-weight terms add nothing
                     d.y = ep.y > 0.f ? d.y : 0.f;
@@ -401,9 +410,9 @@ struct LaneKL {
         }
         const float2 a = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
         const float2 b = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
-        Sp.hi += a.x + a.y;   // plain fp32 lane sums on the bf16 path (see Lane1::push_bf16)
-        Sq.hi += b.x + b.y;
-        W.hi += wsum;
+        df_add(Sp, a.x + a.y);   // double-float lane sums (see Lane1::push_bf16)
+        df_add(Sq, b.x + b.y);
+        df_add(W, wsum);
     }
 };
 
@@ -612,8 +621,8 @@ struct LaneJSD {
                 const float xb = fmaf(b[i] - c.mb, kLog2e, -(c.lb_hi + c.lb_lo) * kLog2e);
                 const float p = ex2_fast(xa), q = ex2_fast(xb);
                 const float lm = fmaxf(lg2_fast(fmaf(c.beta, q, c.omb * p)), -250.f);
-                if (p > 0.f) ka.hi = fmaf(p, xa - lm, ka.hi);
-                if (q > 0.f) kb.hi = fmaf(q, xb - lm, kb.hi);
+                if (p > 0.f) df_add(ka, p * (xa - lm));
+                if (q > 0.f) df_add(kb, q * (xb - lm));
             }
         }
     }
@@ -671,8 +680,8 @@ struct LaneJSD {
                 }
             }
         }
-        ka.hi += suma;   // plain fp32 lane sums on the bf16 path (about ten chunks per row)
-        kb.hi += sumb;
+        df_add(ka, suma);   // double-float lane sums (see Lane1::push_bf16)
+        df_add(kb, sumb);
     }
 };
 
