@@ -55,18 +55,20 @@ __device__ __forceinline__ uint4 splat(float v) {
 template <int kOp, typename T>
 __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s, float g, int64_t loc) {
     if constexpr (Elem<T>::kPrecise) {
+        // exact t and log p (double-float), p from the split-argument exponential
+        // (relative error below 1.5e-7), each gradient rounded once: within 1e-6
+        // of the exact gradient for |g| up to ~6
         const DF t = df_diff(z, s.m);
         const DF lp = df_sub(t, s.logS_hi, s.logS_lo);
-        const DF p = exp_df(lp.hi, lp.lo);
+        const float p = exp_split(lp.hi, lp.lo);
         if (kOp == 0) {                                   // g (onehot - p)
-            const DF d = df_sub(DF{j == loc ? 1.f : 0.f, 0.f}, p.hi, p.lo);
-            return df_mul_round(DF{g, 0.f}, d);
+            if (j != loc) return -g * p;
+            const float lpf = lp.hi + lp.lo;
+            return g * (lpf > -0.5f ? -expm1_small(lpf) : 1.f - p);   // 1 - p without cancellation
         }
-        if (p.hi == 0.f) return 0.f;                      // -g p (t - c)
+        if (p == 0.f) return 0.f;                         // -g p (t - c)
         const DF r = df_sub(t, s.c_hi, s.c_lo);
-        const float gp = -g * p.hi;
-        const DF gpd{gp, fmaf(-g, p.hi, -gp) - g * p.lo};
-        return df_mul_round(gpd, r);
+        return -g * p * (r.hi + r.lo);
     } else {
         const float t = z - s.m;
         const float lp = t - s.logS_hi;
@@ -87,25 +89,35 @@ template <typename T, bool kDP, bool kDQ>
 __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &sp, const RowStat &sq, const DF &k_pq,
                                              float g, bool p_nan, float &dp, float &dq) {
     if constexpr (Elem<T>::kPrecise) {
+        // as grad_elem: exact centred values and log-probabilities, split-argument
+        // exponentials, q - p as p (e^d - 1) where |d| < 1/2, each gradient rounded once
         const DF tp = df_diff(zp, sp.m), tq = df_diff(zq, sq.m);
         const DF lp = df_sub(tp, sp.logS_hi, sp.logS_lo), lq = df_sub(tq, sq.logS_hi, sq.logS_lo);
-        const DF p = exp_df(lp.hi, lp.lo), q = exp_df(lq.hi, lq.lo);
-        if (kDQ) dq = df_mul_round(DF{g, 0.f}, df_sub(q, p.hi, p.lo));   // g (q - p)
+        const float p = exp_split(lp.hi, lp.lo), q = exp_split(lq.hi, lq.lo);
+        if (kDQ) {
+            const DF dd = df_sub(lq, lp.hi, lp.lo);
+            const float d = dd.hi + dd.lo;
+            dq = g * (fabsf(d) < 0.5f ? p * expm1_small(d) : q - p);
+        }
         if (kDP) {                                                     // g p ((tP - tQ) - c)
             if (p_nan) dp = qnan();
-            else if (p.hi == 0.f) dp = 0.f;
+            else if (p == 0.f) dp = 0.f;
             else {
                 const DF r = df_sub(df_sub(tp, tq.hi, tq.lo), sp.c_hi, sp.c_lo);
-                const float gp = g * p.hi;
-                dp = df_mul_round(DF{gp, fmaf(g, p.hi, -gp) + g * p.lo}, r);
+                dp = g * p * (r.hi + r.lo);
             }
         }
     } else {
         const float tp = zp - sp.m, tq = zq - sq.m;          // exact for bf16 values
         const float p = Elem<T>::exp(tp - sp.logS_hi), q = Elem<T>::exp(tq - sq.logS_hi);
         if (kDQ) {
-            const float d = ((tq - tp) + k_pq.hi) + k_pq.lo;  // log q - log p
-            dq = g * (fabsf(d) < 0.5f ? p * expm1_small(d) : q - p);
+            // q - p = p (e^d - 1), d = log q - log p. Below |d| = 1/64 the difference
+            // of the two exponentials would lose more than 2^-9 of itself (each carries
+            // up to ~2^-18 relative error from its rounded argument), so it is taken from
+            // the series d + d^2/2 (truncation below d^2/6 < 2^-14 of the result).
+            const float d = ((tq - tp) + k_pq.hi) + k_pq.lo;
+            const float em1 = fmaf(0.5f * d, d, d);
+            dq = g * (fabsf(d) < 0.015625f ? p * em1 : q - p);
         }
         if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * (((tp - tq) - sp.c_hi) - sp.c_lo);
     }
@@ -230,12 +242,19 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
 // --------------------------------------------------------------------------
 // An id's own element: G (1 - p) - p Gother, where G sums the upstream
 // gradients of the ids equal to this one and Gother those of the row's other
-// (not ignored) ids, in fp64 (a row has only K such elements): 1 - p is taken
-// as -(e^{log p} - 1), so neither it nor the difference of the two terms
-// loses accuracy when p ~ 1 or when the terms nearly cancel.
+// (not ignored) ids (a row has only K such elements). p comes from the
+// double-float exponential (relative error ~1e-8), 1 - p as -(e^{log p} - 1)
+// where p > e^{-1/2} (no cancellation as p -> 1), and the two terms are
+// combined in fp64, so that their difference keeps its accuracy where they
+// nearly cancel.
 __device__ __forceinline__ float topk_target_elem(float z, const RowStat &s, double G, double Gother) {
-    const double lp = (((double)z - (double)s.m) - (double)s.logS_hi) - (double)s.logS_lo;
-    return (float)(G * -expm1(lp) - exp(lp) * Gother);
+    const DF t = df_diff(z, s.m);
+    const DF lp = df_sub(t, s.logS_hi, s.logS_lo);
+    const DF e = exp_df(lp.hi, lp.lo);
+    const double p = (double)e.hi + (double)e.lo;
+    const float lpf = lp.hi + lp.lo;
+    const double omp = lpf > -0.5f ? (double)-expm1_small(lpf) : 1.0 - p;
+    return (float)(G * omp - p * Gother);
 }
 
 template <typename T>
@@ -379,6 +398,64 @@ struct KLGradRow {
     __device__ __forceinline__ void elem(float zp, float zq, float &dp, float &dq) const {
         kl_grad_elem<T, kDP, kDQ>(zp, zq, sp, sq, k_pq, g, p_nan, dp, dq);
     }
+    // One 16-byte vector of P and of Q. bf16: the formulas of kl_grad_elem two
+    // columns per instruction (f32x2); the base-2 arguments are formed as
+    // t log2(e) - log S log2(e) with one FMA.
+    template <bool kDP, bool kDQ>
+    __device__ __forceinline__ void vec(const uint4 &up, const uint4 &uq, uint4 &op, uint4 &oq) const {
+        if constexpr (Elem<T>::kPrecise) {
+            float zp[4], zq[4], dp[4], dq[4];
+            Elem<T>::unpack(up, zp);
+            Elem<T>::unpack(uq, zq);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) elem<kDP, kDQ>(zp[e], zq[e], dp[e], dq[e]);
+            if (kDP) op = Elem<T>::pack(dp);
+            if (kDQ) oq = Elem<T>::pack(dq);
+        } else {
+            const float2 nmp = make_float2(-sp.m, -sp.m), nmq = make_float2(-sq.m, -sq.m);
+            const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
+            const float lp0 = -sp.logS_hi * kLog2e, lq0 = -sq.logS_hi * kLog2e;
+            const float2 nlp = make_float2(lp0, lp0), nlq = make_float2(lq0, lq0);
+            const float2 kh = make_float2(k_pq.hi, k_pq.hi), kl = make_float2(k_pq.lo, k_pq.lo);
+            const float2 nch = make_float2(-sp.c_hi, -sp.c_hi), ncl = make_float2(-sp.c_lo, -sp.c_lo);
+            const float2 g2 = make_float2(g, g), half = make_float2(0.5f, 0.5f);
+            uint32_t wp[4], wq[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t a = w == 0 ? up.x : w == 1 ? up.y : w == 2 ? up.z : up.w;
+                const uint32_t b = w == 0 ? uq.x : w == 1 ? uq.y : w == 2 ? uq.z : uq.w;
+                const float2 tp = __fadd2_rn(make_float2(__uint_as_float(a << 16), __uint_as_float(a & 0xffff0000u)), nmp);
+                const float2 tq = __fadd2_rn(make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u)), nmq);
+                const float2 ap = __ffma2_rn(tp, l2e, nlp), aq = __ffma2_rn(tq, l2e, nlq);
+                float2 p, q;
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p.x) : "f"(ap.x));
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p.y) : "f"(ap.y));
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(q.x) : "f"(aq.x));
+                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(q.y) : "f"(aq.y));
+                if (kDQ) {   // g (q - p), the series where |log q - log p| < 1/64 (kl_grad_elem)
+                    const float2 d = __fadd2_rn(__fadd2_rn(__ffma2_rn(tp, m1, tq), kh), kl);
+                    const float2 em1 = __ffma2_rn(__fmul2_rn(d, half), d, d);
+                    const float2 pe = __fmul2_rn(p, em1);
+                    float2 x = __ffma2_rn(p, m1, q);
+                    x.x = fabsf(d.x) < 0.015625f ? pe.x : x.x;
+                    x.y = fabsf(d.y) < 0.015625f ? pe.y : x.y;
+                    const float2 r = __fmul2_rn(g2, x);
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(r.x, r.y);
+                    wq[w] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+                if (kDP) {   // g p ((tP - tQ) - c), 0 where p = 0
+                    const float2 c = __fadd2_rn(__fadd2_rn(__ffma2_rn(tq, m1, tp), nch), ncl);
+                    float2 r = __fmul2_rn(__fmul2_rn(g2, p), c);
+                    r.x = p_nan ? qnan() : p.x == 0.f ? 0.f : r.x;
+                    r.y = p_nan ? qnan() : p.y == 0.f ? 0.f : r.y;
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(r.x, r.y);
+                    wp[w] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+            }
+            if (kDP) op = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+            if (kDQ) oq = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+    }
 };
 
 // Generalized JSD with interior beta, (P, Q) = (A, B), mix = beta q + (1 - beta) p:
@@ -427,6 +504,17 @@ struct JSDGradRow {
             if (kDP) da = (p > 0.f) ? ga * p * fmaf(xa - lm, kLn2f, -ka) : 0.f;
             if (kDQ) db = (q > 0.f) ? gb * q * fmaf(xb - lm, kLn2f, -kb) : 0.f;
         }
+    }
+    template <bool kDP, bool kDQ>
+    __device__ __forceinline__ void vec(const uint4 &up, const uint4 &uq, uint4 &op, uint4 &oq) const {
+        constexpr int kVec = Elem<T>::kVec;
+        float zp[kVec], zq[kVec], dp[kVec], dq[kVec];
+        Elem<T>::unpack(up, zp);
+        Elem<T>::unpack(uq, zq);
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) elem<kDP, kDQ>(zp[e], zq[e], dp[e], dq[e]);
+        if (kDP) op = Elem<T>::pack(dp);
+        if (kDQ) oq = Elem<T>::pack(dq);
     }
 };
 
@@ -489,13 +577,10 @@ __device__ __forceinline__ void pair_grad_tile(const T *__restrict__ P, const T 
         for (int k = 0; k < kBwdVecPerThread; ++k) {
             const int i = v0 + tid + k * kBwdThreads;
             if (i < v1) {
-                float zp[kVec], zq[kVec], dp[kVec], dq[kVec];
-                Elem<T>::unpack(up[k], zp);
-                Elem<T>::unpack(uq[k], zq);
-#pragma unroll
-                for (int e = 0; e < kVec; ++e) row.template elem<kDP, kDQ>(zp[e], zq[e], dp[e], dq[e]);
-                if (kDP) stg_stream(vdp + i, Elem<T>::pack(dp));
-                if (kDQ) stg_stream(vdq + i, Elem<T>::pack(dq));
+                uint4 op, oq;
+                row.template vec<kDP, kDQ>(up[k], uq[k], op, oq);
+                if (kDP) stg_stream(vdp + i, op);
+                if (kDQ) stg_stream(vdq + i, oq);
             }
         }
     } else {
@@ -504,8 +589,10 @@ __device__ __forceinline__ void pair_grad_tile(const T *__restrict__ P, const T 
     }
 }
 
+// Four CTAs (32 warps) per SM: 64 registers a thread, the occupancy that keeps
+// the HBM streams of both inputs and both gradients in flight.
 template <typename T, bool kDP, bool kDQ>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, 4)
 kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,
                const RowStat *__restrict__ stats_p, const RowStat *__restrict__ stats_q,
                const float *__restrict__ g_in, T *__restrict__ dP, T *__restrict__ dQ, int tiles_per_row,

@@ -15,6 +15,8 @@
 
 #include <string.h>
 
+#include <type_traits>
+
 #include "vp_device.cuh"
 #include "vp_launch.h"
 
@@ -73,12 +75,14 @@ __device__ __forceinline__ float ex2_fast(float a) {
     return y;
 }
 
-// e^t for the forward sums: the base-2 argument t log2(e) with log2(e) split
-// into fp32 hi + lo parts (the product with the hi part exact inside the FMA),
-// so that the sums are those of e^t and not of e^{t (1 - 1.3e-8)}: with the
-// fp32 constant alone, every weight is off by a factor e^{-1.3e-8 t}, which
-// moves the centred mean c = W / S by about 1.3e-8 Var_p(t) (~1e-7 for the
-// pages' logits), a bias the cancelling gradients (t ~ c) resolve.
+// e^t for the fused-linear forward tiles: the base-2 argument t log2(e) with
+// log2(e) split into fp32 hi + lo parts (the product with the hi part exact
+// inside the FMA), so that the sums are those of e^t and not of
+// e^{t (1 - 1.3e-8)}: with the fp32 constant alone, every weight is off by a
+// factor e^{-1.3e-8 t}, which moves the centred mean c = W / S by about
+// 1.3e-8 Var_p(t). (The GEMM epilogues have the issue slots to spare; the
+// HBM-bound logits scans do not, and there the hardware exponential's own
+// error pattern is of the same size.)
 constexpr float kLog2eLo = 1.925963033500011e-08f;   // log2(e) - kLog2e
 __device__ __forceinline__ float exp_fwd(float t) { return ex2_fast(fmaf(t, kLog2e, t * kLog2eLo)); }
 __device__ __forceinline__ float2 exp_fwd2(float2 t) {
@@ -124,24 +128,29 @@ struct Lane1 {
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
         if constexpr (Elem<T>::kPrecise) {
-            // fp32 inputs: exact centred value, accurate exponential, double-float sums
+            // fp32 inputs: exact centred value (double-float), exponential with an exact
+            // argument (exp_split), the chunk summed in fp32 and folded into double-floats
+            float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
             for (int i = 0; i < n; ++i) {
                 const DF t = df_diff(v[i], ref);
-                const DF e = exp_df(t.hi, t.lo);
-                df_add(S, e);
-                if (kW && e.hi != 0.f) {
-                    const float p = e.hi * t.hi;
-                    const float pe = fmaf(e.hi, t.lo, fmaf(e.lo, t.hi, fmaf(e.hi, t.hi, -p)));
-                    df_add(W, DF{p, pe});
+                const float e = exp_split(t.hi, t.lo);
+                if (i & 1) {
+                    s1 += e;
+                    if (kW && e != 0.f) w1 = fmaf(e, t.hi, fmaf(e, t.lo, w1));
+                } else {
+                    s0 += e;
+                    if (kW && e != 0.f) w0 = fmaf(e, t.hi, fmaf(e, t.lo, w0));
                 }
             }
+            df_add(S, s0 + s1);
+            if (kW) df_add(W, w0 + w1);
         } else {
             float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
             for (int i = 0; i < n; ++i) {
                 const float t = v[i] - ref;   // exact for bf16 values
-                const float e = exp_fwd(t);
+                const float e = Elem<T>::exp(t);
                 // e is exactly 0 below t = -104, so clamping t keeps 0 * (-inf) out of W
                 if (i & 1) { s1 += e; if (kW) w1 = fmaf(e, fmaxf(t, -128.f), w1); }
                 else       { s0 += e; if (kW) w0 = fmaf(e, fmaxf(t, -128.f), w0); }
@@ -153,23 +162,26 @@ struct Lane1 {
 
     // bf16 fast path on raw 16-byte words (8 values each): packed max, packed
     // f32x2 arithmetic and four independent accumulator pairs. The chunk sums
-    // are folded into the lane's double-float sums with an error-free two-sum,
-    // so the only roundings left are those inside a chunk; the centred mean
-    // c = W / S of the row then carries ~2^-27 relative error, which the
-    // entropy gradient -p (t - c) needs where t ~ c.
+    // are added to the lane's running sums in plain fp32 (S.hi, W.hi; a lane
+    // takes about ten chunks per row, and every term of W has the sign of t,
+    // so W does not cancel); the warp merges the lanes as double-floats and
+    // the warp partials are merged in fp64. The hardware exponential's error
+    // pattern (bias -5e-8 below -1, +3.3e-8 above +1, spread 3e-8, measured on
+    // GB300) bounds c = W / S at ~2^-23 relative; finer sums would not move it.
     template <int K>
     __device__ __forceinline__ void push_bf16(const uint4 (&u)[K]) {
         const float c = max_bf16(u);
         mx = fmaxf(mx, c);
         if (c > ref + kSpan) move_centre(c);
-        const float2 nref = make_float2(-ref, -ref);
+        const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
         float2 s[4], w[4];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);   // exact
-                const float2 e = exp_fwd2(t);
+                const float2 a = __fmul2_rn(t, l2e);
+                const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
                 if (k == 0) {
                     s[q] = e;
                     if (kW) w[q] = __fmul2_rn(e, t);
@@ -180,7 +192,7 @@ struct Lane1 {
             }
         }
         const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
-        df_add(S, ss.x + ss.y);
+        S.hi += ss.x + ss.y;
         if (kW) {
             float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
             float wsum = ww.x + ww.y;
@@ -194,24 +206,26 @@ struct Lane1 {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float2 t = __fadd2_rn(bf16_pair(word(u[k], q)), nref);
-                        const float2 e = exp_fwd2(t);
+                        const float2 a = __fmul2_rn(t, l2e);
+                        const float2 e = make_float2(ex2_fast(a.x), ex2_fast(a.y));
                         w[q] = __ffma2_rn(e, make_float2(fmaxf(t.x, -128.f), fmaxf(t.y, -128.f)), w[q]);
                     }
                 }
                 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
                 wsum = ww.x + ww.y;
             }
-            df_add(W, wsum);
+            W.hi += wsum;
         }
     }
 };
 
-// Merged partials (a warp's, then the row's) carry their sums in fp64 on both
-// paths: a warp merges its lanes' double-floats, and the finisher warp
-// re-centres and adds the 8 warp partials of a row once per row, off the
-// consumers' critical path.
+// Merged partials carry their sums in fp64 on the fp32 path and in fp32 on the
+// bf16 path: a warp partial's rounding (2^-24 of the warp's share) is far below
+// the hardware exponential's error floor on c (~2^-23, see Lane1::push_bf16),
+// and GB300's fp64 pipe is narrow, so the bf16 path keeps fp64 for the
+// one-thread row finish only.
 template <typename T>
-using AccT = double;
+using AccT = typename std::conditional<Elem<T>::kPrecise, double, float>::type;
 
 __device__ __forceinline__ double exp_acc(double x) { return exp(x); }
 __device__ __forceinline__ float exp_acc(float x) { return expf(x); }
@@ -318,26 +332,30 @@ struct LaneKL {
         if (up || uq) move_centres(up ? cp : rp, uq ? cq : rq);
         int fl = 0;
         if constexpr (Elem<T>::kPrecise) {
+            // fp32 inputs: as Lane1::push (exact centred values, exp_split, chunk sums
+            // folded into double-floats)
+            float sp0 = 0.f, sq0 = 0.f, w0 = 0.f;
 #pragma unroll
             for (int i = 0; i < n; ++i) {
                 const DF tp = df_diff(p[i], rp), tq = df_diff(q[i], rq);
-                const DF ep = exp_df(tp.hi, tp.lo), eq = exp_df(tq.hi, tq.lo);
-                df_add(Sp, ep);
-                df_add(Sq, eq);
-                if (ep.hi != 0.f) {              // zero-weight terms add nothing
+                const float ep = exp_split(tp.hi, tp.lo), eq = exp_split(tq.hi, tq.lo);
+                sp0 += ep;
+                sq0 += eq;
+                if (ep != 0.f) {                 // zero-weight terms add nothing
                     const DF d = df_sub(tp, tq.hi, tq.lo);
-                    const float pr = ep.hi * d.hi;
-                    const float pe = fmaf(ep.hi, d.lo, fmaf(ep.lo, d.hi, fmaf(ep.hi, d.hi, -pr)));
-                    df_add(W, DF{pr, pe});
+                    w0 = fmaf(ep, d.hi, fmaf(ep, d.lo, w0));
                 }
                 fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
             }
+            df_add(Sp, sp0);
+            df_add(Sq, sq0);
+            df_add(W, w0);
         } else {
             float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
             for (int i = 0; i < n; ++i) {
                 const float tp = p[i] - rp, tq = q[i] - rq;
-                const float ep = exp_fwd(tp), eq = exp_fwd(tq);
+                const float ep = Elem<T>::exp(tp), eq = Elem<T>::exp(tq);
                 const float dl = (ep > 0.f) ? (tp - tq) : 0.f;  // zero-weight terms add nothing
                 if (i & 1) { sp1 += ep; sq1 += eq; w1 = fmaf(ep, dl, w1); }
                 else       { sp0 += ep; sq0 += eq; w0 = fmaf(ep, dl, w0); }
@@ -360,7 +378,7 @@ struct LaneKL {
         const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
         if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
         const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
-        const float2 m1 = make_float2(-1.f, -1.f);
+        const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
         float2 sp[4], sq[4], w[4];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -368,7 +386,9 @@ struct LaneKL {
             for (int q = 0; q < 4; ++q) {
                 const float2 tp = __fadd2_rn(bf16_pair(word(up[k], q)), nrp);
                 const float2 tq = __fadd2_rn(bf16_pair(word(uq[k], q)), nrq);
-                const float2 ep = exp_fwd2(tp), eq = exp_fwd2(tq);
+                const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
+                const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
+                const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
                 const float2 d = __ffma2_rn(tq, m1, tp);                             // tp - tq
                 if (k == 0) {
                     sp[q] = ep;
@@ -397,7 +417,8 @@ struct LaneKL {
                     const uint32_t pw = word(up[k], q), qw = word(uq[k], q);
                     fl |= __vcmpeq2(qw, kBf16NegInf2) & ~__vcmpeq2(pw, kBf16NegInf2);
                     const float2 tp = __fadd2_rn(bf16_pair(pw), nrp), tq = __fadd2_rn(bf16_pair(qw), nrq);
-                    const float2 ep = exp_fwd2(tp);
+                    const float2 ap = __fmul2_rn(tp, l2e);
+                    const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
                     float2 d = __ffma2_rn(tq, m1, tp);                            // tp - tq
                     d.x = ep.x > 0.f ? d.x : 0.f;                                 // zero-weight terms add nothing
                     d.y = ep.y > 0.f ? d.y : 0.f;
@@ -410,7 +431,9 @@ struct LaneKL {
         }
         const float2 a = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
         const float2 b = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
-        df_add(Sp, a.x + a.y);   // double-float lane sums (see Lane1::push_bf16)
+        // double-float lane sums: the terms of W take both signs (tp - tq), so its
+        // fp32 running sum would lose the digits of c = W / S_P that cancel
+        df_add(Sp, a.x + a.y);
         df_add(Sq, b.x + b.y);
         df_add(W, wsum);
     }
