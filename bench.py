@@ -290,6 +290,7 @@ def run_ours(args, rank, world, local_rank):
     topk = topk_bench(args, a, dev, peaks) if rank == 0 else None
     strided = strided_bench(args, dev, peaks, st, err, dx, da, db) if rank == 0 and not args.no_strided else None
     stress = stress_bench(args, dev, peaks) if rank == 0 and not args.no_strided else None
+    short = short_batch_bench(args, dev, peaks) if rank == 0 and not args.no_strided else None
 
     linear = None
     if not args.no_linear and rank == 0:
@@ -313,7 +314,8 @@ def run_ours(args, rank, world, local_rank):
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "strided": strided, "fp32_stress": stress, "linear_logp": linear,
+            "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "strided": strided, "fp32_stress": stress,
+            "short_batch": short, "linear_logp": linear,
         }
         print(json.dumps(line))
     if dist:
@@ -410,6 +412,78 @@ def _time_calls(args, calls, order, nbytes, peaks):
     return {"ms_per_step": round(ms, 4), "value_gbs": round(total / (ms * 1e-3) / 1e9, 1),
             "frac_of_copy_peak": round(total / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op.items()}}
+
+
+def short_batch_bench(args, dev, peaks, rows=1024, reps=10):
+    """The step's eight calls on a short batch (1024 rows of the pages' shape, 155.6 MB per logits tensor,
+    near the 129 MB L2), under both row-split settings of the forward scans. Before every timed call the
+    L2 is flushed: a 256 MiB buffer is written, then another 256 MiB buffer is read, so that the call
+    neither finds its inputs in L2 nor pays for the write-back of the flush's dirty lines. Calls are
+    queued back to back (no host synchronisation until the end), so the host's launch latency is not
+    counted either; each call is bracketed by CUDA events on the launching stream."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    from vocab_wide_logprobs_gb300 import workloads
+    w = workloads.pages_shape(seed=7, N=rows)
+    a, b, t, g = (w[k].to(dev) for k in ("a", "b", "targets", "grad"))
+    N, V = a.shape
+    nbytes = algorithmic_bytes(N, V)
+    R, F = vp.KL_REVERSE, vp.KL_FORWARD
+    f32 = lambda: torch.empty(N, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = {k: f32() for k in ("lp", "H", "kl", "kl2")}
+    s = {k: vp.rowstats(N, dev) for k in ("lp", "H", "a", "b", "a2", "b2")}
+    dx, da, db = torch.empty_like(a), torch.empty_like(a), torch.empty_like(a)
+    calls = {
+        "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a, t, 0, err, o["lp"], s["lp"]),
+        "logprobs_bwd": lambda: vp.vp_logprobs_bwd(a, t, s["lp"], g, 0, err, dx),
+        "entropy_fwd": lambda: vp.vp_entropy_fwd(a, o["H"], s["H"]),
+        "entropy_bwd": lambda: vp.vp_entropy_bwd(a, s["H"], g, dx),
+        "kl_rev_fwd": lambda: vp.vp_kl_fwd(a, b, R, o["kl"], s["a"], s["b"]),
+        "kl_rev_bwd": lambda: vp.vp_kl_bwd(a, b, R, s["a"], s["b"], g, da=da, db=db),
+        "kl_fwd_fwd": lambda: vp.vp_kl_fwd(a, b, F, o["kl2"], s["a2"], s["b2"]),
+        "kl_fwd_bwd": lambda: vp.vp_kl_bwd(a, b, F, s["a2"], s["b2"], g, da=da, db=db),
+    }
+    dirty = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        dirty.fill_(1)
+        clean.sum()
+
+    out = {"workload": f"pages shape, N={N}, V={V}, bf16", "reps": reps,
+           "l2": "flushed before every call: 256 MiB written, then 256 MiB read", "launch": "queued back to back"}
+    old = vp.vp_get_row_split()
+    try:
+        for split in (1, 2):
+            vp.vp_set_row_split(split)
+            for _ in range(3):
+                for name in STEP_ORDER:
+                    flush()
+                    calls[name]()
+            torch.cuda.synchronize()
+            ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in STEP_ORDER]
+                  for _ in range(reps)]
+            for k in range(reps):
+                for i, name in enumerate(STEP_ORDER):
+                    flush()
+                    ev[k][i][0].record()
+                    calls[name]()
+                    ev[k][i][1].record()
+            torch.cuda.synchronize()
+            per_op = {name: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(reps))
+                      for i, name in enumerate(STEP_ORDER)}
+            ms = sum(per_op.values())
+            total = sum(nbytes.values())
+            out[f"row_split_{split}"] = {
+                "ms_per_step": round(ms, 4), "value_gbs": round(total / (ms * 1e-3) / 1e9, 1),
+                "frac_of_copy_peak": round(total / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "per_op_us": {k: round(v * 1e3, 1) for k, v in per_op.items()},
+                "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op.items()}}
+    finally:
+        vp.vp_set_row_split(old)
+    out["default"] = f"row_split_{old}"
+    return out
 
 
 def stress_bench(args, dev, peaks):

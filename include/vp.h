@@ -630,6 +630,23 @@ VP_API vp_status vp_download(void *dst_host, const void *src_device, size_t byte
  * spinning. Unlike every other call, this one synchronises with the device.
  * (No counterpart on the pages: a safety net of this implementation.) */
 VP_API vp_status vp_fault_status(uint32_t *value, int clear);
+
+/* How many CTAs share one row's vocabulary in the forward scans (logprobs,
+ * top-k logprobs, entropy, KL, the generalized JSD's first pass and the
+ * vocabulary-shard partials of the first three); process-wide, every device.
+ * 1 (the default) streams each row through one CTA. 2 splits the aligned body
+ * of every row of 64 KB or more between the two CTAs of a thread-block
+ * cluster; the second CTA's partial statistics travel to the first CTA's
+ * shared memory, which merges the two in a fixed order and finishes the row.
+ * A row's arithmetic depends on this setting, V, the element size and the
+ * row's address modulo 16, never on N, so results do not depend on the batch
+ * size under either setting (they may differ by rounding between settings).
+ * On GB300, 1 measured faster at every batch size tried; 2 is kept as an
+ * option. Set it while no forward call is in flight. Other values:
+ * VP_ERR_ARG, setting unchanged. (No counterpart on the pages: a scheduling
+ * choice of this implementation.) */
+VP_API vp_status vp_set_row_split(int ctas);
+VP_API int vp_get_row_split(void);
 VP_API const char *vp_status_string(int status);
 VP_API int vp_version(void);
 

@@ -212,3 +212,18 @@ def test_host_transfers_check_arguments_on_the_host():
     assert lib.vp_upload(None, FAKE, ctypes.c_size_t(16), None) == ERR_NULL
     assert lib.vp_download(FAKE, None, ctypes.c_size_t(16), None) == ERR_NULL
     assert lib.vp_upload(None, None, ctypes.c_size_t(0), None) == OK        # nothing to copy
+
+
+def test_row_split_setting_checks_its_value():
+    # host-side setting: 1 or 2 CTAs per row in the forward scans, anything else refused and ignored
+    L = _lib.lib()
+    old = L.vp_get_row_split()
+    assert old in (1, 2)
+    try:
+        for bad in (0, 3, -1, 64):
+            assert L.vp_set_row_split(bad) == ERR_ARG
+            assert L.vp_get_row_split() == old
+        assert L.vp_set_row_split(2) == OK and L.vp_get_row_split() == 2
+        assert L.vp_set_row_split(1) == OK and L.vp_get_row_split() == 1
+    finally:
+        L.vp_set_row_split(old)

@@ -86,6 +86,10 @@ def lib():
             h.vp_fault_status.restype = ctypes.c_int
             h.vp_version.argtypes = []
             h.vp_version.restype = ctypes.c_int
+            h.vp_set_row_split.argtypes = [I32]
+            h.vp_set_row_split.restype = ctypes.c_int
+            h.vp_get_row_split.argtypes = []
+            h.vp_get_row_split.restype = ctypes.c_int
             _handle = h
     return _handle
 

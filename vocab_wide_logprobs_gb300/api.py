@@ -552,6 +552,15 @@ def vp_fault_status(clear: bool = False) -> int:
     return int(v.value)
 
 
+def vp_set_row_split(ctas: int) -> None:
+    """CTAs sharing one row's vocabulary in the forward scans (1, the default, or 2; process-wide)."""
+    _check(_lib.lib().vp_set_row_split(int(ctas)), "vp_set_row_split")
+
+
+def vp_get_row_split() -> int:
+    return int(_lib.lib().vp_get_row_split())
+
+
 def vp_linear_logp_partial(hidden, weight, targets, vocab_start: int = 0, parts=None, workspace=None):
     """Per-row logprobs records over the vocabulary shard held by weight (rows vocab_start .. + V of the head)."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_logp_partial")

@@ -592,6 +592,10 @@ vp_status vp_fault_status(uint32_t *value, int clear) {
     return VP_OK;
 }
 
+vp_status vp_set_row_split(int ctas) { return vp::set_row_split(ctas) ? VP_OK : VP_ERR_ARG; }
+
+int vp_get_row_split(void) { return vp::row_split(); }
+
 const char *vp_status_string(int status) {
     switch (status) {
         case VP_OK: return "ok";

@@ -109,7 +109,12 @@ __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &
         }
     } else {
         const float tp = zp - sp.m, tq = zq - sq.m;          // exact for bf16 values
-        const float p = Elem<T>::exp(tp - sp.logS_hi), q = Elem<T>::exp(tq - sq.logS_hi);
+        // base-2 arguments t log2(e) - log S log2(e) with one FMA, the operations
+        // of KLGradRow::vec, so that an element's gradient does not depend on
+        // which of the two paths (set by the rows' and outputs' alignment) takes it
+        float p, q;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(fmaf(tp, kLog2e, -sp.logS_hi * kLog2e)));
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(q) : "f"(fmaf(tq, kLog2e, -sq.logS_hi * kLog2e)));
         if (kDQ) {
             // q - p = p (e^d - 1), d = log q - log p. Below |d| = 1/64 the difference
             // of the two exponentials would lose more than 2^-9 of itself (each carries

@@ -187,6 +187,8 @@ cudaError_t launch_logprobs_topk_bwd(const GradArgs &a);
 cudaError_t launch_kl_fwd(const KLFwdArgs &a);
 cudaError_t launch_kl_fwd_rowwise(const KLFwdArgs &a);
 cudaError_t read_fault(uint32_t *value, bool clear);
+bool set_row_split(int ctas);   // 1 or 2 CTAs per row in the forward scans; false for other values
+int row_split();
 cudaError_t launch_logprobs_bwd(const GradArgs &a);
 cudaError_t launch_entropy_bwd(const GradArgs &a);
 cudaError_t launch_kl_bwd(const KLBwdArgs &a);

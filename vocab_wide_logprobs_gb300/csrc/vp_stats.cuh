@@ -275,12 +275,11 @@ __device__ __forceinline__ Part1<AccT<T>> warp_merge(const Lane1<T, kW> &L) {
     return o;
 }
 
-// Merge `count` (<= 32) warp partials, re-centred on the largest centre and in
-// a fixed order; called by one whole warp, the result is valid in all lanes.
+// Merge the partials held by the lanes of one warp (lane i holds partial i; an
+// empty partial where there is none), re-centred on the largest centre and
+// added in a fixed shuffle order; the result is valid in all lanes.
 template <bool kW, typename V>
-__device__ __forceinline__ Part1<V> merge_parts(const Part1<V> *parts, int count) {
-    const int lane = threadIdx.x & 31;
-    const Part1<V> q = lane < count ? parts[lane] : Part1<V>{kNegBig, kNegBig, V(0), V(0)};
+__device__ __forceinline__ Part1<V> merge_lane_parts(const Part1<V> &q) {
     const float M = warp_max(q.ref);
     const V a = (q.ref == M) ? V(1) : exp_acc((V)q.ref - (V)M);
     V sc = a * q.S, wc = V(0);
@@ -292,6 +291,17 @@ __device__ __forceinline__ Part1<V> merge_parts(const Part1<V> *parts, int count
     o.S = warp_sum_t(sc);
     o.W = kW ? warp_sum_t(wc) : V(0);
     return o;
+}
+
+template <typename V>
+__device__ __forceinline__ Part1<V> empty_part() { return Part1<V>{kNegBig, kNegBig, V(0), V(0)}; }
+
+// Merge `count` (<= 32) warp partials in a fixed order; called by one whole
+// warp, the result is valid in all lanes.
+template <bool kW, typename V>
+__device__ __forceinline__ Part1<V> merge_parts(const Part1<V> *parts, int count) {
+    const int lane = threadIdx.x & 31;
+    return merge_lane_parts<kW>(lane < count ? parts[lane] : empty_part<V>());
 }
 
 // ---------------------------------------------------------------------------
@@ -487,12 +497,14 @@ __device__ __forceinline__ PartKL<AccT<T>> kl_warp_merge(const LaneKL<T> &L) {
     return o;
 }
 
-// KL counterpart of merge_parts.
 template <typename V>
-__device__ __forceinline__ PartKL<V> kl_merge_parts(const PartKL<V> *parts, int count) {
-    const int lane = threadIdx.x & 31;
-    const PartKL<V> e{kNegBig, kNegBig, kNegBig, kNegBig, V(0), V(0), V(0), 0};
-    const PartKL<V> q = lane < count ? parts[lane] : e;
+__device__ __forceinline__ PartKL<V> empty_kl_part() {
+    return PartKL<V>{kNegBig, kNegBig, kNegBig, kNegBig, V(0), V(0), V(0), 0};
+}
+
+// KL counterpart of merge_lane_parts.
+template <typename V>
+__device__ __forceinline__ PartKL<V> kl_merge_lane_parts(const PartKL<V> &q) {
     const float Mp = warp_max(q.rp), Mq = warp_max(q.rq);
     V sp, sq, w;
     kl_recentred<V>(q.rp, q.rq, q.Sp, q.Sq, q.W, Mp, Mq, sp, sq, w);
@@ -503,6 +515,13 @@ __device__ __forceinline__ PartKL<V> kl_merge_parts(const PartKL<V> *parts, int 
     o.Sp = warp_sum_t(sp); o.Sq = warp_sum_t(sq); o.W = warp_sum_t(w);
     o.flag = __any_sync(0xffffffffu, q.flag);
     return o;
+}
+
+// KL counterpart of merge_parts.
+template <typename V>
+__device__ __forceinline__ PartKL<V> kl_merge_parts(const PartKL<V> *parts, int count) {
+    const int lane = threadIdx.x & 31;
+    return kl_merge_lane_parts(lane < count ? parts[lane] : empty_kl_part<V>());
 }
 
 // ---------------------------------------------------------------------------

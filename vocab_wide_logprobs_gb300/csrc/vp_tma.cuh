@@ -102,6 +102,22 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
+// Arrival on an mbarrier of another CTA of the cluster, without a release
+// fence: for a "slot free" signal whose only prior accesses are shared-memory
+// reads whose values the caller has already consumed.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Asynchronous 8-byte store into another CTA's shared memory that completes
+// 8 bytes of transaction on that CTA's mbarrier (both shared::cluster addresses
+// of the same CTA); no fence, the mbarrier phase carries the data.
+__device__ __forceinline__ void st_async_u64(uint32_t cluster_dst, uint64_t v, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(cluster_dst),
+                 "l"(v), "r"(cluster_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
     uint32_t ok;
     asm volatile(
