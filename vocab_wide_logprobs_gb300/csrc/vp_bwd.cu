@@ -82,6 +82,20 @@ __device__ __forceinline__ float grad_elem(float z, int64_t j, const RowStat &s,
     }
 }
 
+// fp32 inputs: grad_elem of two columns at once (f32x2, each lane rounded as
+// grad_elem rounds it), both taken as non-targets (logprobs: -g p; the caller
+// rewrites a target column with grad_elem).
+template <int kOp>
+__device__ __forceinline__ float2 grad_pair_f32(float2 z, const RowStat &s, float g) {
+    const DF2 t = two_sum2(z, f2(-s.m));
+    const DF2 lp = df_sub2(t, DF2{f2(s.logS_hi), f2(s.logS_lo)});
+    const float2 p = exp_split2(lp);
+    if (kOp == 0) return __fmul2_rn(f2(-g), p);
+    const DF2 r = df_sub2(t, DF2{f2(s.c_hi), f2(s.c_lo)});
+    const float2 d = __fmul2_rn(__fmul2_rn(f2(-g), p), __fadd2_rn(r.hi, r.lo));
+    return make_float2(p.x == 0.f ? 0.f : d.x, p.y == 0.f ? 0.f : d.y);
+}
+
 // k_pq = log S_P - log S_Q of the row (double-float): log q_j - log p_j =
 // (t^Q_j - t^P_j) + k_pq. Where that difference d is small, q - p cancels, and
 // the bf16 path evaluates it as p (e^d - 1) with a series for e^d - 1.
@@ -125,6 +139,33 @@ __device__ __forceinline__ void kl_grad_elem(float zp, float zq, const RowStat &
             dq = g * (fabsf(d) < 0.015625f ? p * em1 : q - p);
         }
         if (kDP) dp = p_nan ? qnan() : (p == 0.f) ? 0.f : g * p * (((tp - tq) - sp.c_hi) - sp.c_lo);
+    }
+}
+
+// fp32 inputs: kl_grad_elem of two columns at once (f32x2, each lane rounded
+// as kl_grad_elem rounds it).
+template <bool kDP, bool kDQ>
+__device__ __forceinline__ void kl_grad_pair_f32(float2 zp, float2 zq, const RowStat &sp, const RowStat &sq, float g,
+                                                 bool p_nan, float2 &dp, float2 &dq) {
+    const DF2 tp = two_sum2(zp, f2(-sp.m)), tq = two_sum2(zq, f2(-sq.m));
+    const DF2 lp = df_sub2(tp, DF2{f2(sp.logS_hi), f2(sp.logS_lo)});
+    const DF2 lq = df_sub2(tq, DF2{f2(sq.logS_hi), f2(sq.logS_lo)});
+    const float2 p = exp_split2(lp), q = exp_split2(lq);
+    if (kDQ) {
+        const DF2 dd = df_sub2(lq, lp);
+        const float2 d = __fadd2_rn(dd.hi, dd.lo);
+        const float2 pe = __fmul2_rn(p, expm1_small2(d));
+        const float2 qp = __ffma2_rn(p, f2(-1.f), q);                      // q - p
+        dq = __fmul2_rn(f2(g), make_float2(fabsf(d.x) < 0.5f ? pe.x : qp.x, fabsf(d.y) < 0.5f ? pe.y : qp.y));
+    }
+    if (kDP) {                                                           // g p ((tP - tQ) - c)
+        if (p_nan) {                                                     // the whole row (a flagged P)
+            dp = f2(qnan());
+        } else {
+            const DF2 r = df_sub2(df_sub2(tp, tq), DF2{f2(sp.c_hi), f2(sp.c_lo)});
+            const float2 v = __fmul2_rn(__fmul2_rn(f2(g), p), __fadd2_rn(r.hi, r.lo));
+            dp = make_float2(p.x == 0.f ? 0.f : v.x, p.y == 0.f ? 0.f : v.y);
+        }
     }
 }
 
@@ -207,6 +248,19 @@ grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict
                         // every element as a non-target; the target is rewritten below
 #pragma unroll
                         for (int e = 0; e < kVec; ++e) d[e] = grad_elem<0, T>(z[e], 0, s, g, -1);
+                    } else if constexpr (Elem<T>::kPrecise) {
+                        // pairs of columns (f32x2), then the target column, if here, alone
+#pragma unroll
+                        for (int e = 0; e < kVec; e += 2) {
+                            const float2 dd = grad_pair_f32<kOp>(make_float2(z[e], z[e + 1]), s, g);
+                            d[e] = dd.x;
+                            d[e + 1] = dd.y;
+                        }
+                        if (kOp == 0 && loc >= j0 && loc < j0 + kVec) {
+#pragma unroll
+                            for (int e = 0; e < kVec; ++e)
+                                if (j0 + e == loc) d[e] = grad_elem<0, T>(z[e], loc, s, g, loc);
+                        }
                     } else {
 #pragma unroll
                         for (int e = 0; e < kVec; ++e) d[e] = grad_elem<kOp, T>(z[e], j0 + e, s, g, loc);
@@ -413,7 +467,12 @@ struct KLGradRow {
             Elem<T>::unpack(up, zp);
             Elem<T>::unpack(uq, zq);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) elem<kDP, kDQ>(zp[e], zq[e], dp[e], dq[e]);
+            for (int e = 0; e < 4; e += 2) {   // kl_grad_elem's operations, two columns at once
+                float2 a, b;
+                kl_grad_pair_f32<kDP, kDQ>(make_float2(zp[e], zp[e + 1]), make_float2(zq[e], zq[e + 1]), sp, sq, g,
+                                           p_nan, a, b);
+                dp[e] = a.x; dp[e + 1] = a.y; dq[e] = b.x; dq[e + 1] = b.y;
+            }
             if (kDP) op = Elem<T>::pack(dp);
             if (kDQ) oq = Elem<T>::pack(dq);
         } else {
@@ -595,7 +654,8 @@ __device__ __forceinline__ void pair_grad_tile(const T *__restrict__ P, const T 
 }
 
 // Four CTAs (32 warps) per SM: 64 registers a thread, the occupancy that keeps
-// the HBM streams of both inputs and both gradients in flight.
+// the HBM streams of both inputs and both gradients in flight (for fp32 too:
+// three CTAs with the 85 registers that avoid a few spills measured slower).
 template <typename T, bool kDP, bool kDQ>
 __global__ void __launch_bounds__(kBwdThreads, 4)
 kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows rows,

@@ -248,6 +248,18 @@ __device__ __forceinline__ float expm1_small(float x) {
     return fmaf(t * x, x, x);                 // x + x^2 (1/2 + x/6 + ...)
 }
 
+// expm1_small of each lane (f32x2, the same operations)
+__device__ __forceinline__ float2 expm1_small2(float2 x) {
+    float2 t = make_float2(2.4801587301587302e-05f, 2.4801587301587302e-05f);
+    t = __ffma2_rn(t, x, make_float2(1.9841269841269841e-04f, 1.9841269841269841e-04f));
+    t = __ffma2_rn(t, x, make_float2(1.3888888888888889e-03f, 1.3888888888888889e-03f));
+    t = __ffma2_rn(t, x, make_float2(8.3333333333333333e-03f, 8.3333333333333333e-03f));
+    t = __ffma2_rn(t, x, make_float2(4.1666666666666667e-02f, 4.1666666666666667e-02f));
+    t = __ffma2_rn(t, x, make_float2(1.6666666666666667e-01f, 1.6666666666666667e-01f));
+    t = __ffma2_rn(t, x, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(__fmul2_rn(t, x), x, x);
+}
+
 // e^(t_hi + t_lo) as one fp32 value, from the hardware base-2 exponential
 // with its argument a = (t_hi + t_lo) log2(e) carried as a_hi + a_lo (the
 // product with the fp32 part of log2(e) exact inside an FMA, the low part of
@@ -265,6 +277,56 @@ __device__ __forceinline__ float exp_split(float t_hi, float t_lo) {
     float e;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(a_hi));
     return e == 0.f ? 0.f : fmaf(e, a_lo * kLn2, e);   // a_lo is NaN where t_hi is infinite
+}
+
+// ---------------------------------------------------------------------------
+// Packed (f32x2) forms of two_sum, df_sub and exp_split: two independent
+// values per instruction, each lane rounded exactly as the scalar form rounds
+// it (negations are folded into FMAs with -1 or with negated constants, which
+// round symmetrically), so the results are bitwise those of the scalar forms.
+// ---------------------------------------------------------------------------
+struct DF2 {
+    float2 hi, lo;
+};
+
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+// two_sum of each lane
+__device__ __forceinline__ DF2 two_sum2(float2 a, float2 b) {
+    const float2 m1 = f2(-1.f);
+    const float2 s = __fadd2_rn(a, b);
+    const float2 bb = __ffma2_rn(a, m1, s);                            // s - a
+    const float2 r = __ffma2_rn(__ffma2_rn(bb, m1, s), m1, a);         // a - (s - bb)
+    return {s, __fadd2_rn(r, __ffma2_rn(bb, m1, b))};                  // + (b - bb)
+}
+
+// two_sum(a, -y) of each lane
+__device__ __forceinline__ DF2 two_diff2(float2 a, float2 y) {
+    const float2 m1 = f2(-1.f);
+    const float2 s = __ffma2_rn(y, m1, a);                             // a - y
+    const float2 bb = __ffma2_rn(a, m1, s);                            // s - a
+    const float2 r = __ffma2_rn(__ffma2_rn(bb, m1, s), m1, a);         // a - (s - bb)
+    return {s, __ffma2_rn(__fadd2_rn(y, bb), m1, r)};                  // + (-y - bb)
+}
+
+// df_sub(x, y.hi, y.lo) of each lane
+__device__ __forceinline__ DF2 df_sub2(const DF2 &x, const DF2 &y) {
+    const DF2 d = two_diff2(x.hi, y.hi);
+    return {d.hi, __fadd2_rn(d.lo, __ffma2_rn(y.lo, f2(-1.f), x.lo))};
+}
+
+// exp_split of each lane, its zero test included (bitwise exp_split's)
+__device__ __forceinline__ float2 exp_split2(const DF2 &t) {
+    constexpr float kL = 1.4426950408889634f, kLlo = 1.925963033500011e-08f, kLn2 = 0.6931471805599453f;
+    const float2 a_hi = __fmul2_rn(t.hi, f2(kL));
+    float2 na = __ffma2_rn(t.hi, f2(-kL), a_hi);                       // -(t_hi kL - a_hi)
+    na = __ffma2_rn(t.hi, f2(-kLlo), na);
+    na = __ffma2_rn(t.lo, f2(-kL), na);                                // -a_lo
+    float2 e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(a_hi.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(a_hi.y));
+    const float2 r = __ffma2_rn(e, __fmul2_rn(na, f2(-kLn2)), e);      // e (1 + a_lo ln 2)
+    return make_float2(e.x == 0.f ? 0.f : r.x, e.y == 0.f ? 0.f : r.y);   // a_lo is NaN where t_hi is infinite
 }
 
 // Product (x_hi + x_lo) * (y_hi + y_lo) rounded once to fp32.

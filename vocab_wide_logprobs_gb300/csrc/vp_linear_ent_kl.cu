@@ -117,18 +117,6 @@ __device__ __forceinline__ bool finite(float x) { return fabsf(x) < INFINITY; }
 
 __device__ __forceinline__ float2 pair128(const float (&v)[128], int i) { return make_float2(v[i], v[i + 1]); }
 
-// expm1_small (vp_device.cuh) on two values at once
-__device__ __forceinline__ float2 expm1_small2(float2 x) {
-    float2 t = splat(2.4801587301587302e-05f);                    // 1/8!
-    t = __ffma2_rn(t, x, splat(1.9841269841269841e-04f));          // 1/7!
-    t = __ffma2_rn(t, x, splat(1.3888888888888889e-03f));          // 1/6!
-    t = __ffma2_rn(t, x, splat(8.3333333333333333e-03f));          // 1/5!
-    t = __ffma2_rn(t, x, splat(4.1666666666666667e-02f));          // 1/4!
-    t = __ffma2_rn(t, x, splat(1.6666666666666667e-01f));          // 1/3!
-    t = __ffma2_rn(t, x, splat(0.5f));                             // 1/2!
-    return __ffma2_rn(__fmul2_rn(t, x), x, x);
-}
-
 // q - p from p and d = log q - log p: p (e^d - 1) where |d| < 1/2 (q ~ p, where
 // the difference of the two exponentials would cancel), else q - p
 __device__ __forceinline__ float q_minus_p(float q, float p, float d) {

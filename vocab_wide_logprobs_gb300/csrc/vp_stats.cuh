@@ -129,18 +129,36 @@ struct Lane1 {
         if (c > ref + kSpan) move_centre(c);
         if constexpr (Elem<T>::kPrecise) {
             // fp32 inputs: exact centred value (double-float), exponential with an exact
-            // argument (exp_split), the chunk summed in fp32 and folded into double-floats
+            // argument (exp_split), the chunk summed in fp32 (even and odd values apart)
+            // and folded into double-floats; on pairs of values (f32x2) where n is even,
+            // each lane rounding exactly as the scalar form
             float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
+            if constexpr (n % 2 == 0) {
+                const float2 nref = f2(-ref);
+                float2 s2 = f2(0.f), w2 = f2(0.f);
 #pragma unroll
-            for (int i = 0; i < n; ++i) {
-                const DF t = df_diff(v[i], ref);
-                const float e = exp_split(t.hi, t.lo);
-                if (i & 1) {
-                    s1 += e;
-                    if (kW && e != 0.f) w1 = fmaf(e, t.hi, fmaf(e, t.lo, w1));
-                } else {
-                    s0 += e;
-                    if (kW && e != 0.f) w0 = fmaf(e, t.hi, fmaf(e, t.lo, w0));
+                for (int i = 0; i < n; i += 2) {
+                    const DF2 t = two_sum2(make_float2(v[i], v[i + 1]), nref);
+                    const float2 e = exp_split2(t);
+                    s2 = __fadd2_rn(s2, e);
+                    if (kW) {   // zero-weight terms add nothing (t may be -inf there)
+                        const float2 wn = __ffma2_rn(e, t.hi, __ffma2_rn(e, t.lo, w2));
+                        w2 = make_float2(e.x != 0.f ? wn.x : w2.x, e.y != 0.f ? wn.y : w2.y);
+                    }
+                }
+                s0 = s2.x; s1 = s2.y; w0 = w2.x; w1 = w2.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+                    const DF t = df_diff(v[i], ref);
+                    const float e = exp_split(t.hi, t.lo);
+                    if (i & 1) {
+                        s1 += e;
+                        if (kW && e != 0.f) w1 = fmaf(e, t.hi, fmaf(e, t.lo, w1));
+                    } else {
+                        s0 += e;
+                        if (kW && e != 0.f) w0 = fmaf(e, t.hi, fmaf(e, t.lo, w0));
+                    }
                 }
             }
             df_add(S, s0 + s1);
@@ -343,23 +361,48 @@ struct LaneKL {
         int fl = 0;
         if constexpr (Elem<T>::kPrecise) {
             // fp32 inputs: as Lane1::push (exact centred values, exp_split, chunk sums
-            // folded into double-floats)
-            float sp0 = 0.f, sq0 = 0.f, w0 = 0.f;
+            // of the even and the odd values folded into double-floats, pairs of values
+            // in f32x2 where n is even)
+            float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
+            if constexpr (n % 2 == 0) {
+                const float2 nrp = f2(-rp), nrq = f2(-rq);
+                float2 sp = f2(0.f), sq = f2(0.f), w = f2(0.f);
+                float qmin = q[0];
 #pragma unroll
-            for (int i = 0; i < n; ++i) {
-                const DF tp = df_diff(p[i], rp), tq = df_diff(q[i], rq);
-                const float ep = exp_split(tp.hi, tp.lo), eq = exp_split(tq.hi, tq.lo);
-                sp0 += ep;
-                sq0 += eq;
-                if (ep != 0.f) {                 // zero-weight terms add nothing
-                    const DF d = df_sub(tp, tq.hi, tq.lo);
-                    w0 = fmaf(ep, d.hi, fmaf(ep, d.lo, w0));
+                for (int i = 0; i < n; i += 2) {
+                    const DF2 tp = two_sum2(make_float2(p[i], p[i + 1]), nrp);
+                    const DF2 tq = two_sum2(make_float2(q[i], q[i + 1]), nrq);
+                    const float2 ep = exp_split2(tp), eq = exp_split2(tq);
+                    sp = __fadd2_rn(sp, ep);
+                    sq = __fadd2_rn(sq, eq);
+                    const DF2 d = df_sub2(tp, tq);
+                    const float2 wn = __ffma2_rn(ep, d.hi, __ffma2_rn(ep, d.lo, w));
+                    w = make_float2(ep.x != 0.f ? wn.x : w.x, ep.y != 0.f ? wn.y : w.y);   // zero weights add nothing
+                    qmin = fminf(qmin, fminf(q[i], q[i + 1]));
                 }
-                fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+                if (qmin == -INFINITY) {   // the support-mismatch flag, decided on the logits
+#pragma unroll
+                    for (int i = 0; i < n; ++i) fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+                }
+                sp0 = sp.x; sp1 = sp.y; sq0 = sq.x; sq1 = sq.y; w0 = w.x; w1 = w.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+                    const DF tp = df_diff(p[i], rp), tq = df_diff(q[i], rq);
+                    const float ep = exp_split(tp.hi, tp.lo), eq = exp_split(tq.hi, tq.lo);
+                    if (ep != 0.f) {                 // zero-weight terms add nothing
+                        const DF d = df_sub(tp, tq.hi, tq.lo);
+                        float &wi = (i & 1) ? w1 : w0;
+                        wi = fmaf(ep, d.hi, fmaf(ep, d.lo, wi));
+                    }
+                    if (i & 1) { sp1 += ep; sq1 += eq; }
+                    else       { sp0 += ep; sq0 += eq; }
+                    fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+                }
             }
-            df_add(Sp, sp0);
-            df_add(Sq, sq0);
-            df_add(W, w0);
+            df_add(Sp, sp0 + sp1);
+            df_add(Sq, sq0 + sq1);
+            df_add(W, w0 + w1);
         } else {
             float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
