@@ -263,7 +263,7 @@ def run_ours(args, rank, world, local_rank):
         if dist:
             dist.barrier()
     elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
-    per_op_ms = {name: statistics.mean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+    per_op_ms = {name: statistics.median(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                  for i, name in enumerate(ops)}
     ms_per_step = elapsed_ms / args.steps
     value = job_rate_gbs(step_bytes, world, ms_per_step)
@@ -286,6 +286,7 @@ def run_ours(args, rank, world, local_rank):
                          with_grads=True)
         e2e["per_row_outputs_only"] = per_row
 
+    table = ops_table(per_op_ms, nbytes, peaks, kl_da_only_ms(a, b, g, dev)) if rank == 0 else None
     jsd = jsd_bench(args, a, b, g, dev, peaks) if rank == 0 else None
     topk = topk_bench(args, a, dev, peaks) if rank == 0 else None
     strided = strided_bench(args, dev, peaks, st, err, dx, da, db) if rank == 0 and not args.no_strided else None
@@ -313,6 +314,7 @@ def run_ours(args, rank, world, local_rank):
                        "algorithmic_bytes_per_step": step_bytes},
             "per_op_ms": {k: round(v, 4) for k, v in per_op_ms.items()},
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op_ms.items()},
+            "ops_table": table,
             "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks.summary(), "cpu_baseline": cpu, "jsd": jsd, "topk": topk, "strided": strided, "fp32_stress": stress,
             "short_batch": short, "linear_logp": linear,
@@ -412,6 +414,56 @@ def _time_calls(args, calls, order, nbytes, peaks):
     return {"ms_per_step": round(ms, 4), "value_gbs": round(total / (ms * 1e-3) / 1e9, 1),
             "frac_of_copy_peak": round(total / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "per_op_gbs": {k: round(nbytes[k] / (v * 1e-3) / 1e9, 1) for k, v in per_op.items()}}
+
+
+NOMINAL_HBM_GBS = 8000.0   # the pages' "about 8 TB/s"
+
+
+def ops_table(per_op_ms, nbytes, peaks, kl_da_only_ms):
+    """Each op's fwd + bwd (in-step medians) against the nominal 8 TB/s and the measured copy peak, with
+    the 85%-of-8-TB/s mark; KL with dA only (the pages' timing model) from its own timed calls."""
+    rows = {"logprobs": ("logprobs_fwd", "logprobs_bwd"), "entropy": ("entropy_fwd", "entropy_bwd"),
+            "kl_da_db": ("kl_rev_fwd", "kl_rev_bwd")}
+    out = {}
+    for name, (f, b) in rows.items():
+        ms = per_op_ms[f] + per_op_ms[b]
+        out[name] = (ms, nbytes[f] + nbytes[b])
+    E2 = nbytes["logprobs_fwd"]                      # E * s
+    out["kl_da_only"] = (kl_da_only_ms, 5 * E2)      # read A, B twice, write dA
+    table = {}
+    for name, (ms, by) in out.items():
+        gbs = by / (ms * 1e-3) / 1e9
+        table[name] = {"ms": round(ms, 4), "bytes": by, "gbs": round(gbs, 1),
+                       "frac_of_8tbps": round(gbs / NOMINAL_HBM_GBS, 4),
+                       "frac_of_measured_copy": round(gbs / peaks["hbm_gbs"], 4),
+                       "mark_85pct_of_8tbps_ms": round(by / (0.85 * NOMINAL_HBM_GBS * 1e9) * 1e3, 4)}
+    return table
+
+
+def kl_da_only_ms(a, b, g, dev, reps=20):
+    """KL(A||B) forward plus the backward with dA only (a detached teacher), median of `reps` back-to-back
+    pairs after 5 warm-ups, CUDA events on the launching stream."""
+    import torch
+    import vocab_wide_logprobs_gb300 as vp
+    N = a.shape[0]
+    kl = torch.empty(N, dtype=torch.float32, device=dev)
+    sa, sb = vp.rowstats(N, dev), vp.rowstats(N, dev)
+    da = torch.empty_like(a)
+
+    def pair():
+        vp.vp_kl_fwd(a, b, vp.KL_REVERSE, kl, sa, sb)
+        vp.vp_kl_bwd(a, b, vp.KL_REVERSE, sa, sb, g, want_db=False, da=da)
+
+    for _ in range(5):
+        pair()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record()
+        pair()
+        e1.record()
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
 
 
 def short_batch_bench(args, dev, peaks, rows=1024, reps=10):

@@ -116,3 +116,17 @@ def test_gpus_must_match_the_launcher():
     out = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--launch-check"], cwd=ROOT, env=env,
                          capture_output=True, text=True, timeout=300)
     assert out.returncode == 2 and "WORLD_SIZE" in out.stderr
+
+
+def test_ops_table_against_the_nominal_and_measured_peaks():
+    # SURVEY-style table: fwd + bwd of each op, its bytes, the fraction of 8 TB/s and the 85% mark
+    nbytes = bench.algorithmic_bytes(8192, 75968)
+    per_op = {"logprobs_fwd": 0.2, "logprobs_bwd": 0.35, "entropy_fwd": 0.21, "entropy_bwd": 0.35,
+              "kl_rev_fwd": 0.41, "kl_rev_bwd": 0.71, "kl_fwd_fwd": 0.41, "kl_fwd_bwd": 0.71}
+    t = bench.ops_table(per_op, nbytes, {"hbm_gbs": 6775.6}, kl_da_only_ms=0.93)
+    E2 = 8192 * 75968 * 2
+    assert t["logprobs"]["bytes"] == 3 * E2 and t["kl_da_db"]["bytes"] == 6 * E2 and t["kl_da_only"]["bytes"] == 5 * E2
+    assert abs(t["logprobs"]["ms"] - 0.55) < 1e-9
+    assert abs(t["logprobs"]["mark_85pct_of_8tbps_ms"] - 3 * E2 / (0.85 * 8e12) * 1e3) < 1e-4   # 0.549 ms
+    assert abs(t["kl_da_only"]["mark_85pct_of_8tbps_ms"] - 0.915) < 1e-3
+    assert abs(t["kl_da_db"]["frac_of_8tbps"] - 6 * E2 / 1.12e-3 / 8e12) < 1e-4
