@@ -247,9 +247,11 @@ def run_ours(args, rank, world, local_rank):
         step()
     torch.cuda.synchronize()
 
+    # The timed region holds the steps' kernels back to back, with no event between them (an event
+    # between two kernels would also stop the next one from being scheduled while the previous one
+    # finishes); the per-op breakdown comes from a second pass of the same steps with an event pair
+    # around every call.
     stream = torch.cuda.current_stream()
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
-          for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
         if dist:
@@ -257,12 +259,17 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         start.record(stream)
         for k in range(args.steps):
-            step(ev[k])
+            step()
         stop.record(stream)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
     elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in ops]
+          for _ in range(args.steps)]
+    for k in range(args.steps):
+        step(ev[k])
+    torch.cuda.synchronize()
     per_op_ms = {name: statistics.median(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                  for i, name in enumerate(ops)}
     ms_per_step = elapsed_ms / args.steps

@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kBwdThreads)
 grad_kernel(const T *__restrict__ x, int V, Rows rows, const RowStat *__restrict__ stats,
             const float *__restrict__ g_in, const int64_t *__restrict__ targets, int64_t vocab_start,
             T *__restrict__ dx, int32_t *__restrict__ err, int tiles_per_row, int64_t total_tiles) {
+    pdl_enter<true>();   // no global access before this
     constexpr int kVec = Elem<T>::kVec;
     const int tid = threadIdx.x;
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__(kBwdThreads)
 topk_grad_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const RowStat *__restrict__ stats,
                  const float *__restrict__ g_in, const int64_t *__restrict__ targets, int64_t K, int64_t vocab_start,
                  T *__restrict__ dx, int32_t *__restrict__ err) {
+    pdl_enter<true>();   // no global access before this
     constexpr int kVec = Elem<T>::kVec;
     static_assert((kBwdThreads & (kBwdThreads - 1)) == 0 && kTileVec % kBwdThreads == 0, "tiles of whole blocks");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -662,6 +664,7 @@ kl_grad_kernel(const T *__restrict__ P, const T *__restrict__ Q, int V, Rows row
                const RowStat *__restrict__ stats_p, const RowStat *__restrict__ stats_q,
                const float *__restrict__ g_in, T *__restrict__ dP, T *__restrict__ dQ, int tiles_per_row,
                int64_t total_tiles) {
+    pdl_enter<true>();   // no global access before this
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         const int64_t r = tile / tiles_per_row;
         const KLGradRow<T> row(stats_p, stats_q, g_in, r);
@@ -675,6 +678,7 @@ jsd_grad_kernel(const T *__restrict__ A, const T *__restrict__ B, int V, Rows ro
                 const RowStat *__restrict__ stats_a, const RowStat *__restrict__ stats_b,
                 const float *__restrict__ g_in, T *__restrict__ dA, T *__restrict__ dB, int tiles_per_row,
                 int64_t total_tiles) {
+    pdl_enter<true>();   // no global access before this
     for (int64_t tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         const int64_t r = tile / tiles_per_row;
         const JSDGradRow<T> row(stats_a, stats_b, g_in, r, beta);
@@ -698,10 +702,11 @@ static cudaError_t launch_grad(const GradArgs &a) {
     int64_t total;
     unsigned grid;
     tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
-    grad_kernel<kOp, T><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i}, static_cast<const RowStat *>(a.stats),
-        a.g, a.targets, a.vocab_start, static_cast<T *>(a.dx), a.err, tpr, total);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(grad_kernel<kOp, T>, dim3(grid), dim3(kBwdThreads), 0, a.stream,
+                               static_cast<const T *>(a.x), (int)a.V, Rows{a.R, a.s_o, a.s_i},
+                               static_cast<const RowStat *>(a.stats), a.g, a.targets, a.vocab_start,
+                               static_cast<T *>(a.dx), a.err, tpr, total);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_logprobs_bwd(const GradArgs &a) {
@@ -715,10 +720,11 @@ cudaError_t launch_entropy_bwd(const GradArgs &a) {
 template <typename T>
 static cudaError_t launch_topk_grad(const GradArgs &a) {
     const unsigned grid = (unsigned)(a.N < (int64_t)(1u << 30) ? a.N : (int64_t)(1u << 30));   // one CTA per row
-    topk_grad_kernel<T><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.x), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i}, static_cast<const RowStat *>(a.stats),
-        a.g, a.targets, a.K, a.vocab_start, static_cast<T *>(a.dx), a.err);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(topk_grad_kernel<T>, dim3(grid), dim3(kBwdThreads), 0, a.stream,
+                               static_cast<const T *>(a.x), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i},
+                               static_cast<const RowStat *>(a.stats), a.g, a.targets, a.K, a.vocab_start,
+                               static_cast<T *>(a.dx), a.err);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_logprobs_topk_bwd(const GradArgs &a) {
@@ -731,11 +737,12 @@ static cudaError_t launch_kl_grad_t(const KLBwdArgs &a) {
     int64_t total;
     unsigned grid;
     tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
-    kl_grad_kernel<T, kDP, kDQ><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.p), static_cast<const T *>(a.q), (int)a.V, Rows{a.R, a.s_o, a.s_i},
-        static_cast<const RowStat *>(a.stats_p), static_cast<const RowStat *>(a.stats_q), a.g,
-        static_cast<T *>(a.dp), static_cast<T *>(a.dq), tpr, total);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(kl_grad_kernel<T, kDP, kDQ>, dim3(grid), dim3(kBwdThreads), 0, a.stream,
+                               static_cast<const T *>(a.p), static_cast<const T *>(a.q), (int)a.V,
+                               Rows{a.R, a.s_o, a.s_i}, static_cast<const RowStat *>(a.stats_p),
+                               static_cast<const RowStat *>(a.stats_q), a.g, static_cast<T *>(a.dp),
+                               static_cast<T *>(a.dq), tpr, total);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>
@@ -755,11 +762,12 @@ static cudaError_t launch_jsd_grad_t(const JsdBwdArgs &a) {
     int64_t total;
     unsigned grid;
     tile_grid(a.N, a.V, Elem<T>::kVec, tpr, total, grid);
-    jsd_grad_kernel<T, kDA, kDB><<<grid, kBwdThreads, 0, a.stream>>>(
-        static_cast<const T *>(a.a), static_cast<const T *>(a.b), (int)a.V, Rows{a.R, a.s_o, a.s_i}, (float)a.beta,
-        static_cast<const RowStat *>(a.stats_a), static_cast<const RowStat *>(a.stats_b), a.g,
-        static_cast<T *>(a.da), static_cast<T *>(a.db), tpr, total);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(jsd_grad_kernel<T, kDA, kDB>, dim3(grid), dim3(kBwdThreads), 0, a.stream,
+                               static_cast<const T *>(a.a), static_cast<const T *>(a.b), (int)a.V,
+                               Rows{a.R, a.s_o, a.s_i}, (float)a.beta, static_cast<const RowStat *>(a.stats_a),
+                               static_cast<const RowStat *>(a.stats_b), a.g, static_cast<T *>(a.da),
+                               static_cast<T *>(a.db), tpr, total);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T>

@@ -361,6 +361,49 @@ __device__ __forceinline__ void store_rowstat(RowStat *dst, float m, double logS
     d[1] = src[1];
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization (launch_pdl) may be scheduled while the stream's previous grid
+// is still finishing: it calls pdl_enter() before its first global-memory
+// access, and the wait returns once every grid it depends on has completed and
+// that grid's memory operations are visible.
+// kTrigger also lets the stream's next grid be scheduled once every CTA of this
+// grid has done so or exited, so that every CTA of this grid is resident by
+// then and a waiting dependent never holds a slot one of them needs. The
+// elementwise backward grids (many short CTAs) trigger: their dependents then
+// arrive as the last wave drains. The persistent forward grids do not: they
+// would trigger at once, and a dependent CTA would sit waiting beside them for
+// the whole scan (measured on GB300: the step took 3.47-3.51 ms with every
+// kernel triggering, 3.34 ms with the backwards only, 3.37 ms without PDL).
+// Without the launch attribute both instructions are no-ops.
+// ---------------------------------------------------------------------------
+template <bool kTrigger>
+__device__ __forceinline__ void pdl_enter() {
+    if (kTrigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+#ifndef VP_PDL
+#define VP_PDL 1
+#endif
+
+// kernel<<<grid, block, smem, stream>>>(args...) with programmatic stream
+// serialization (VP_PDL = 0 launches without it)
+template <typename K, typename... Args>
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = VP_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ __forceinline__ RowStat load_rowstat(const RowStat *p) {
     RowStat s;
     uint4 *d = reinterpret_cast<uint4 *>(&s);

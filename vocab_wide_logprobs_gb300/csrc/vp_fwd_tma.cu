@@ -250,6 +250,7 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
         cluster_slots_init(cs, rank);
         cluster_sync();                                         // every CTA's barriers are initialised
     }
+    pdl_enter<false>();                                                // no global access before this
     const int64_t unit0 = blockIdx.x / kC, n_units = gridDim.x / kC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -432,6 +433,7 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
         cluster_slots_init(cs, rank);
         cluster_sync();
     }
+    pdl_enter<false>();
     const int64_t unit0 = blockIdx.x / kC, n_units = gridDim.x / kC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -591,6 +593,7 @@ jsd_fwd_tma_kernel(const T *__restrict__ A, const T *__restrict__ B, int64_t N, 
     __shared__ Ring ring;
     __shared__ PartJSD<AccT<T>> parts[2][kTmaConsumerWarps];
     ring_init(ring);
+    pdl_enter<false>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == kFinisherWarp) {
@@ -758,21 +761,21 @@ static int fwd_split(int64_t V, int elem_bytes) {
 template <int kC, typename K, typename... Args>
 static cudaError_t launch_rows(K kernel, std::atomic<int> (&resident)[64], int64_t N, cudaStream_t stream,
                                Args... args) {
-    if constexpr (kC == 1) {   // no cluster: an ordinary launch
-        kernel<<<persistent_grid(N), kTmaThreads, kRingBytes, stream>>>(args...);
-        return cudaSuccess;
-    }
+    if constexpr (kC == 1)   // no cluster
+        return launch_pdl(kernel, dim3(persistent_grid(N)), dim3(kTmaThreads), kRingBytes, stream, args...);
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kTmaThreads);
     cfg.dynamicSmemBytes = kRingBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = VP_PDL;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     int dev = 0;
     cudaGetDevice(&dev);
     int max_units = (dev >= 0 && dev < 64) ? resident[dev].load() : 0;
@@ -850,10 +853,10 @@ static cudaError_t launch_jsd_pass2(const JsdFwdArgs &a) {
     auto k = jsd_fwd_tma_kernel<T>;
     cudaError_t e = allow_ring(k, done);
     if (e != cudaSuccess) return e;
-    k<<<persistent_grid(a.N), kTmaThreads, kRingBytes, a.stream>>>(
-        static_cast<const T *>(a.a), static_cast<const T *>(a.b), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i},
-        (float)a.beta, a.jsd, static_cast<RowStat *>(a.stats_a), static_cast<RowStat *>(a.stats_b));
-    return cudaGetLastError();
+    e = launch_pdl(k, dim3(persistent_grid(a.N)), dim3(kTmaThreads), kRingBytes, a.stream,
+                   static_cast<const T *>(a.a), static_cast<const T *>(a.b), a.N, (int)a.V, Rows{a.R, a.s_o, a.s_i},
+                   (float)a.beta, a.jsd, static_cast<RowStat *>(a.stats_a), static_cast<RowStat *>(a.stats_b));
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_jsd_fwd(const JsdFwdArgs &a) {
