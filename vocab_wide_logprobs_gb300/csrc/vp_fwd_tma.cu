@@ -413,7 +413,7 @@ stats_fwd_tma_kernel(const T *__restrict__ x, int64_t N, int V, Rows rows, const
 // KL(P||Q); P and Q share their address modulo 16 (checked by the launcher).
 // The vocabulary split across a cluster is that of stats_fwd_tma_kernel.
 // ---------------------------------------------------------------------------
-template <typename T, int kC>
+template <typename T, int kC, bool kW = true>
 __global__ void __launch_bounds__(kTmaThreads, kCtasPerSm)
 kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, int V, Rows rows,
                   float *__restrict__ kl, RowStat *__restrict__ stats_p, RowStat *__restrict__ stats_q,
@@ -514,7 +514,7 @@ kl_fwd_tma_kernel(const T *__restrict__ P, const T *__restrict__ Q, int64_t N, i
             const int tail0 = head + nv * kVec;
             int lo, hi;
             seg_range<kC>(nv, (int)rank, lo, hi);
-            LaneKL<T> acc;
+            LaneKL<T, kW> acc;
             acc.init(kNegBig, kNegBig);
             for (int c0 = lo; c0 < hi; c0 += kChunkVec, pos.next()) {
                 const uint32_t st = pos.st;
@@ -822,11 +822,11 @@ cudaError_t launch_logprobs_topk_fwd(const StatsArgs &a) {
     return a.bf16 ? launch_stats_tma<2, __nv_bfloat16>(a) : launch_stats_tma<2, float>(a);
 }
 
-template <typename T, int kC>
+template <typename T, int kC, bool kW = true>
 static cudaError_t launch_kl_tma_c(const KLFwdArgs &a) {
     static std::atomic<uint64_t> done{0};
     static std::atomic<int> resident[64];
-    auto k = kl_fwd_tma_kernel<T, kC>;
+    auto k = kl_fwd_tma_kernel<T, kC, kW>;
     cudaError_t e = allow_ring(k, done);
     if (e != cudaSuccess) return e;
     e = launch_rows<kC>(k, resident, a.N, a.stream, static_cast<const T *>(a.p), static_cast<const T *>(a.q), a.N, (int)a.V,
@@ -859,12 +859,22 @@ static cudaError_t launch_jsd_pass2(const JsdFwdArgs &a) {
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The JSD's first pass on the ring: each row's (m, logS) of A and of B, the
+// KL scan without its cross term and mismatch flag (the second pass rewrites
+// the records' c fields and keeps only their NaN and empty flags).
+template <typename T>
+static cudaError_t launch_pair_stats_tma(const KLFwdArgs &a) {
+    return fwd_split(a.V, sizeof(T)) == 2 ? launch_kl_tma_c<T, 2, false>(a) : launch_kl_tma_c<T, 1, false>(a);
+}
+
 cudaError_t launch_jsd_fwd(const JsdFwdArgs &a) {
-    // first pass: each row's (m, logS) of A and of B, the KL scan without its output
     KLFwdArgs k{a.a, a.b, a.bf16, a.N, a.V, a.R, a.s_o, a.s_i, nullptr, a.stats_a, a.stats_b, a.stream};
-    cudaError_t e = launch_kl_fwd(k);
+    if ((((uintptr_t)a.a ^ (uintptr_t)a.b) & 15u) != 0) {   // element-wise kernels for both passes
+        cudaError_t e = launch_kl_fwd_rowwise(k);
+        return e != cudaSuccess ? e : launch_jsd_fwd_rowwise(a);
+    }
+    cudaError_t e = a.bf16 ? launch_pair_stats_tma<__nv_bfloat16>(k) : launch_pair_stats_tma<float>(k);
     if (e != cudaSuccess) return e;
-    if ((((uintptr_t)a.a ^ (uintptr_t)a.b) & 15u) != 0) return launch_jsd_fwd_rowwise(a);
     return a.bf16 ? launch_jsd_pass2<__nv_bfloat16>(a) : launch_jsd_pass2<float>(a);
 }
 

@@ -325,7 +325,9 @@ __device__ __forceinline__ Part1<V> merge_parts(const Part1<V> *parts, int count
 // ---------------------------------------------------------------------------
 // KL(P||Q): paired statistics from one read of P and Q
 // ---------------------------------------------------------------------------
-template <typename T>
+// kW = false keeps the two distributions' sums only (no cross term W and no
+// mismatch flag): the JSD's first pass, which needs each row's maxima and sums.
+template <typename T, bool kW = true>
 struct LaneKL {
     float rp, rq, mxp, mxq;
     DF Sp, Sq, W;
@@ -375,12 +377,14 @@ struct LaneKL {
                     const float2 ep = exp_split2(tp), eq = exp_split2(tq);
                     sp = __fadd2_rn(sp, ep);
                     sq = __fadd2_rn(sq, eq);
-                    const DF2 d = df_sub2(tp, tq);
-                    const float2 wn = __ffma2_rn(ep, d.hi, __ffma2_rn(ep, d.lo, w));
-                    w = make_float2(ep.x != 0.f ? wn.x : w.x, ep.y != 0.f ? wn.y : w.y);   // zero weights add nothing
-                    qmin = fminf(qmin, fminf(q[i], q[i + 1]));
+                    if constexpr (kW) {
+                        const DF2 d = df_sub2(tp, tq);
+                        const float2 wn = __ffma2_rn(ep, d.hi, __ffma2_rn(ep, d.lo, w));
+                        w = make_float2(ep.x != 0.f ? wn.x : w.x, ep.y != 0.f ? wn.y : w.y);   // zero weights add nothing
+                        qmin = fminf(qmin, fminf(q[i], q[i + 1]));
+                    }
                 }
-                if (qmin == -INFINITY) {   // the support-mismatch flag, decided on the logits
+                if (kW && qmin == -INFINITY) {   // the support-mismatch flag, decided on the logits
 #pragma unroll
                     for (int i = 0; i < n; ++i) fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
                 }
@@ -390,14 +394,14 @@ struct LaneKL {
                 for (int i = 0; i < n; ++i) {
                     const DF tp = df_diff(p[i], rp), tq = df_diff(q[i], rq);
                     const float ep = exp_split(tp.hi, tp.lo), eq = exp_split(tq.hi, tq.lo);
-                    if (ep != 0.f) {                 // zero-weight terms add nothing
+                    if (kW && ep != 0.f) {           // zero-weight terms add nothing
                         const DF d = df_sub(tp, tq.hi, tq.lo);
                         float &wi = (i & 1) ? w1 : w0;
                         wi = fmaf(ep, d.hi, fmaf(ep, d.lo, wi));
                     }
                     if (i & 1) { sp1 += ep; sq1 += eq; }
                     else       { sp0 += ep; sq0 += eq; }
-                    fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+                    if (kW) fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
                 }
             }
             df_add(Sp, sp0 + sp1);
@@ -412,7 +416,7 @@ struct LaneKL {
                 const float dl = (ep > 0.f) ? (tp - tq) : 0.f;  // zero-weight terms add nothing
                 if (i & 1) { sp1 += ep; sq1 += eq; w1 = fmaf(ep, dl, w1); }
                 else       { sp0 += ep; sq0 += eq; w0 = fmaf(ep, dl, w0); }
-                fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
+                if (kW) fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
             }
             df_add(Sp, sp0 + sp1);
             df_add(Sq, sq0 + sq1);
@@ -442,24 +446,27 @@ struct LaneKL {
                 const float2 ap = __fmul2_rn(tp, l2e), aq = __fmul2_rn(tq, l2e);
                 const float2 ep = make_float2(ex2_fast(ap.x), ex2_fast(ap.y));
                 const float2 eq = make_float2(ex2_fast(aq.x), ex2_fast(aq.y));
-                const float2 d = __ffma2_rn(tq, m1, tp);                             // tp - tq
                 if (k == 0) {
                     sp[q] = ep;
                     sq[q] = eq;
-                    w[q] = __fmul2_rn(ep, d);
+                    if (kW) w[q] = __fmul2_rn(ep, __ffma2_rn(tq, m1, tp));       // ep (tp - tq)
                 } else {
                     sp[q] = __fadd2_rn(sp[q], ep);
                     sq[q] = __fadd2_rn(sq[q], eq);
-                    w[q] = __ffma2_rn(ep, d, w[q]);
+                    if (kW) w[q] = __ffma2_rn(ep, __ffma2_rn(tq, m1, tp), w[q]);
                 }
             }
         }
-        float2 c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
-        float wsum = c.x + c.y;
+        float2 c = f2(0.f);
+        float wsum = 0.f;
+        if (kW) {
+            c = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
+            wsum = c.x + c.y;
+        }
         // A -inf logit in P or Q (or a spread beyond FLT_MAX) makes some tp - tq
         // infinite or NaN and so W non-finite: redo W with zero-weight terms
         // skipped and take the support-mismatch flag (Q = -inf where P is not).
-        if (!(fabsf(wsum) < INFINITY)) {
+        if (kW && !(fabsf(wsum) < INFINITY)) {
             uint32_t fl = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) w[q] = make_float2(0.f, 0.f);
@@ -513,8 +520,8 @@ __device__ __forceinline__ void kl_recentred(float rp, float rq, V sp, V sq, V w
     else osp = V(0);
 }
 
-template <typename T>
-__device__ __forceinline__ PartKL<AccT<T>> kl_warp_merge(const LaneKL<T> &L) {
+template <typename T, bool kW>
+__device__ __forceinline__ PartKL<AccT<T>> kl_warp_merge(const LaneKL<T, kW> &L) {
     using V = AccT<T>;
     PartKL<V> o;
     o.mxp = warp_max(L.mxp);
