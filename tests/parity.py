@@ -77,6 +77,15 @@ def _record_ulp(what, err, ulp, rows=None):
         STATS[what]["rows_beyond"] = sorted({int(x) for x in np.asarray(rows)[err > ulp]})[:8]
 
 
+def _record_kappa(what, err, base, mag, kappa):
+    """The smallest conditioning factor the check would have passed with: max over the elements of
+    (err - base) / (2^-24 M), base being every other term of the tolerance; 0 where all are within base."""
+    with np.errstate(invalid="ignore", divide="ignore"):
+        need = np.where(err > base, (err - base) / (2.0 ** -24 * mag), 0.0)
+    STATS[what]["kappa_needed"] = float(np.nanmax(need)) if need.size else 0.0
+    STATS[what]["kappa"] = float(kappa)
+
+
 def _placement(got, ref, what):
     gn, rn = np.isnan(got), np.isnan(ref)
     if not (gn == rn).all():
@@ -128,6 +137,9 @@ def check_grad(got: torch.Tensor, ref: np.ndarray, what: str, mag=None, oracle_m
         if oracle_mag is not None:
             tol = tol + ORACLE_EPS * np.asarray(oracle_mag)[fin]
         _record_ulp(what, err, ulp, np.nonzero(fin)[0] if fin.ndim == 2 else None)
+        if mag is not None:
+            base = ulp + (ORACLE_EPS * np.asarray(oracle_mag)[fin] if oracle_mag is not None else 0.0)
+            _record_kappa(what, err, base, np.asarray(mag)[fin], kappa)
     else:
         _placement(g, ref, what)
         fin = np.isfinite(ref)
@@ -352,6 +364,9 @@ def check_gemm_grad(got, ref, norms, what, eval_mag=None, flush_mag=None, fast=F
     if flush_mag is not None:
         tol = tol + flush_mag[fin]
     _record_ulp(what, err, ulp)
+    if eval_mag is not None:
+        base = ulp + (GEMM_KAPPA * l1[fin] if fast else GEMM_RSS * l2[fin]) + (flush_mag[fin] if flush_mag is not None else 0.0)
+        _record_kappa(what, err, base, eval_mag[fin], kappa)
     with np.errstate(invalid="ignore", divide="ignore"):
         over = np.where(l2[fin] > 0, np.maximum(err - ulp, 0.0) / l2[fin], 0.0)
     STATS[what]["worst_beyond_ulp_over_rss"] = float(over.max()) if err.size else 0.0

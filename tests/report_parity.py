@@ -50,23 +50,31 @@ def table(stats: dict) -> str:
     for k, v in grad.items():
         fams.setdefault(_family(k), []).append((k, v))
     lines += ["## Summary by family", "",
-              "| family | checks | elements | beyond 1 ulp | share | worst err / tol |",
-              "|---|---:|---:|---:|---:|---:|"]
+              "| family | checks | elements | beyond 1 ulp | share | worst err / tol | κ needed (κ) |",
+              "|---|---:|---:|---:|---:|---:|---:|"]
     for fam in sorted(fams):
         rows = fams[fam]
         n = sum(v["n"] for _, v in rows)
         b = sum(v["beyond_1ulp"] for _, v in rows)
         w = max(v.get("worst_over_tol", 0.0) for _, v in rows)
-        lines.append(f"| {fam} | {len(rows)} | {n} | {b} | {b / n if n else 0:.2e} | {w:.3f} |")
+        kn = [v["kappa_needed"] for _, v in rows if "kappa_needed" in v]
+        kk = {v["kappa"] for _, v in rows if "kappa" in v}
+        ks = f"{max(kn):.2f} ({'/'.join(f'{x:g}' for x in sorted(kk))})" if kn else ""
+        lines.append(f"| {fam} | {len(rows)} | {n} | {b} | {b / n if n else 0:.2e} | {w:.3f} | {ks} |")
+    lines += ["", "κ needed: the smallest conditioning factor κ in the tolerance term κ·2⁻²⁴·M (tests/parity.py) with "
+              "which every element of the family's checks would still pass, every other term of the tolerance "
+              "(one ulp, the oracle's rounding, the GEMM's root-sum-square and flush terms) kept; κ: the factor "
+              "the checks use."]
     lines += ["", "## Every gradient check", "",
-              "| check | elements | beyond 1 ulp | worst err (ulp) | worst err / tol | GEMM: worst excess / RSS |",
-              "|---|---:|---:|---:|---:|---:|"]
+              "| check | elements | beyond 1 ulp | worst err (ulp) | worst err / tol | κ needed | GEMM: worst excess / RSS |",
+              "|---|---:|---:|---:|---:|---:|---:|"]
     for k in sorted(grad):
         v = grad[k]
         r = v.get("worst_beyond_ulp_over_rss")
         rs = "" if r is None else ("0" if r <= 0 else f"2^{math.log2(r):.1f}")
+        kn = f"{v['kappa_needed']:.2f}" if "kappa_needed" in v else ""
         lines.append(f"| {k} | {v['n']} | {v['beyond_1ulp']} | {v['worst_err_over_ulp']:.3g} | "
-                     f"{v.get('worst_over_tol', 0.0):.3f} | {rs} |")
+                     f"{v.get('worst_over_tol', 0.0):.3f} | {kn} | {rs} |")
     if cvals:
         lines += ["", "## Forward centred mean c of the saved records", "",
                   "| check | rows | max abs error | max rel error |", "|---|---:|---:|---:|"]
