@@ -187,7 +187,8 @@ def run_ours(args, rank, world, local_rank):
 
     if args.linear_only:
         if rank == 0:
-            print(json.dumps({"linear_logp": linear_bench(args, dev, N=args.linear_rows)}))
+            print(json.dumps({"linear_logp": linear_bench(args, dev, N=args.linear_rows,
+                                                          sustained=not args.no_sustained)}))
         if dist:
             dist.destroy_process_group()
         return
@@ -303,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
     linear = None
     if not args.no_linear and rank == 0:
         with ClockSampler(local_rank) as lin_clocks:
-            linear = linear_bench(args, dev, N=args.linear_rows)
+            linear = linear_bench(args, dev, N=args.linear_rows, sustained=not args.no_sustained)
         linear["clocks"] = lin_clocks.summary()
 
     cpu = None
@@ -676,6 +677,11 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096, sustained=True):
     ]
     # the records each backward reads: the matching forward runs right before it
     fwd_of = {"logp": 0, "entropy": 3, "kl": 6, "jsd": 9}
+    families = getattr(args, "linear_ops", None)
+    if families:   # a subset of the op families (a small profiling run)
+        keep = set(families.split(",")) & set(fwd_of)
+        ops = [o for o in ops if o[0].split("_")[0] in keep]
+        fwd_of = {f: next(j for j, o in enumerate(ops) if o[0] == f + "_fwd") for f in keep}
     burst, sus = {}, {}
     for k, (name, fn, units) in enumerate(ops):
         if not name.endswith("_fwd"):
@@ -713,19 +719,25 @@ def linear_bench(args, dev, N=8192, V=75968, D=4096, sustained=True):
                               "peak": sus_peak, "peak_src": "measured bf16 sustained"}
         return e
 
-    out = entry("logp", 1, 5, 3, f"hidden [{N},{D}] x W [{V},{D}] bf16, logp of uniform targets")
-    out["roofline"] = {"bound": "tensor", "achieved": out["fwd_tflops"], "peak": burst_peak, "unit": "TFLOP/s",
-                       "peak_src": "measured bf16 burst" if burst_peak else None, "frac": out["fwd_frac"],
-                       "flops": unit}
-    out["bwd_roofline"] = {"bound": "tensor", "achieved": out["bwd_tflops"], "peak": burst_peak, "unit": "TFLOP/s",
-                           "frac": out["bwd_frac"], "flops": 5 * unit,
-                           "note": "exact precision: logits recomputed (2NVD), dhidden and dW with dz_hi and dz_lo "
-                                   "(4NVD each); fast precision: 3 GEMMs of 2NVD"}
-    out["entropy"] = entry("entropy", 1, 5, 3, "entropy of softmax(h W^T); backward: logits, dhidden, dW")
-    out["kl"] = entry("kl", 2, 10, 6, "KL(A||B) of two models of this shape; forward: both logits tiles; "
-                      "backward: both logits tiles, dhidden and dW of both models")
-    out["jsd"] = entry("jsd", 4, 10, 6, "generalized JSD (beta = 0.5) of the two models; forward: two passes of "
-                       "both logits tiles; backward: as for KL")
+    have = {name.split("_")[0] for name, _, _ in ops}
+    out = {}
+    if "logp" in have:
+        out = entry("logp", 1, 5, 3, f"hidden [{N},{D}] x W [{V},{D}] bf16, logp of uniform targets")
+        out["roofline"] = {"bound": "tensor", "achieved": out["fwd_tflops"], "peak": burst_peak, "unit": "TFLOP/s",
+                           "peak_src": "measured bf16 burst" if burst_peak else None, "frac": out["fwd_frac"],
+                           "flops": unit}
+        out["bwd_roofline"] = {"bound": "tensor", "achieved": out["bwd_tflops"], "peak": burst_peak,
+                               "unit": "TFLOP/s", "frac": out["bwd_frac"], "flops": 5 * unit,
+                               "note": "exact precision: logits recomputed (2NVD), dhidden and dW with dz_hi and "
+                                       "dz_lo (4NVD each); fast precision: 3 GEMMs of 2NVD"}
+    if "entropy" in have:
+        out["entropy"] = entry("entropy", 1, 5, 3, "entropy of softmax(h W^T); backward: logits, dhidden, dW")
+    if "kl" in have:
+        out["kl"] = entry("kl", 2, 10, 6, "KL(A||B) of two models of this shape; forward: both logits tiles; "
+                          "backward: both logits tiles, dhidden and dW of both models")
+    if "jsd" in have:
+        out["jsd"] = entry("jsd", 4, 10, 6, "generalized JSD (beta = 0.5) of the two models; forward: two passes "
+                           "of both logits tiles; backward: as for KL")
     out["sustained_clocks"] = clocks
     return out
 
@@ -1003,6 +1015,9 @@ def main():
     p.add_argument("--linear-only", action="store_true",
                    help="only the fused linear-logp measurement (profiling of the GEMM kernels)")
     p.add_argument("--linear-rows", type=int, default=8192, help="hidden rows of the linear-logp workload")
+    p.add_argument("--linear-ops", default=None,
+                   help="comma-separated op families of the linear line (logp, entropy, kl, jsd); default all")
+    p.add_argument("--no-sustained", action="store_true", help="skip the linear line's sustained figures")
     p.add_argument("--launch-check", action="store_true",
                    help="only start the ranks, take the max over them and print who took part (no GPU work)")
     args = p.parse_args()
