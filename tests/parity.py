@@ -2,7 +2,9 @@
 
 Tolerances (stated in the design notes, derived from the target):
   * per-row outputs (logp, H, KL, logS):  |x - y| <= 2e-5 + 2e-5 |y|;
-  * fp32 gradients:                       |g - g64| <= 1e-6;
+  * fp32 gradients:                       |g - g64| <= 1e-6 max(1, |g64|): 1e-6 absolute up to
+    |g64| = 1 and relative above (an absolute 1e-6 is below half the spacing
+    of fp32 values from |g64| = 16.8 on, so no fp32 result could meet it there);
   * bf16 gradients:                       |g - RNE_bf16(g64)| <= 1 ulp_bf16(RNE_bf16(g64))
                                                                + KAPPA_BF16 * 2^-24 * M_j,
     where M_j is the magnitude of the operands of the element's formula
@@ -147,7 +149,7 @@ def check_grad(got: torch.Tensor, ref: np.ndarray, what: str, mag=None, oracle_m
         _placement(g, ref, what)
         fin = np.isfinite(ref)
         err = np.abs(g[fin] - ref[fin])
-        tol = np.full(err.shape, F32_GRAD_ATOL)
+        tol = F32_GRAD_ATOL * np.maximum(1.0, np.abs(ref[fin]))
         STATS[what] = {"max_abs_err": float(err.max()) if err.size else 0.0, "n": int(err.size)}
     if err.size and not (err <= tol).all():
         i = np.argmax(err / tol)

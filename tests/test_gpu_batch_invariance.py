@@ -205,3 +205,23 @@ def test_split_against_one_cta_per_row_within_tolerance():
         assert np.allclose(x, y, rtol=2e-6, atol=2e-6), k
     ref = oracle.entropy_fwd(parity.to64(w["a"]))[0]
     assert np.allclose(parity.to64(two["H"]), ref, rtol=2e-5, atol=2e-5)
+
+
+def test_split_many_rows_per_cluster_against_oracle():
+    # two CTAs per row and more than 32 rows per cluster (4999 rows over at most 152 clusters): the
+    # finisher's batches roll over under the split too; sampled rows include every cluster's later rows
+    old = vp.vp_get_row_split()
+    vp.vp_set_row_split(2)
+    try:
+        N, V = 4999, 32768
+        w = workloads.pages_shape(seed=72, N=N, V=V)
+        t = w["targets"].clone()
+        t[4900] = -1
+        a, b, g = w["a"].to(DEV), w["b"].to(DEV), w["grad"].to(DEV)
+        got = parity.gpu_all(a, b, t.to(DEV), g)
+        rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(4860, N), [1000, 2500, 4000]]))
+        ref = parity.oracle_all(parity.to64(w["a"][rows]), parity.to64(w["b"][rows]), t[rows].numpy(),
+                                w["grad"][rows].numpy())
+        parity.compare_all(got, ref, rows=torch.as_tensor(rows, device=DEV), tag="split 4999 rows ")
+    finally:
+        vp.vp_set_row_split(old)

@@ -77,6 +77,21 @@ def test_jsd_pages_recipe(N, V, dtype, beta):
     print("jsd worst/tol:", {k: round(v, 3) for k, v in worst.items()})
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_jsd_peaked_rows_late_chunks(dtype):
+    # one logit 18 to 24 above N(0, 1) rows past the first 8192 columns, at different columns in A and B
+    # (each distribution's mode lies in the other's far tail, the mixture's log there near log(1 - beta))
+    gen = torch.Generator().manual_seed(75)
+    N, V = 48, 75968
+    a = torch.randn(N, V, generator=gen)
+    b = torch.randn(N, V, generator=gen)
+    a[torch.arange(N), torch.randint(8192, V, (N,), generator=gen)] += 18.0 + 6.0 * torch.rand(N, generator=gen)
+    b[torch.arange(N), torch.randint(8192, V, (N,), generator=gen)] += 18.0 + 6.0 * torch.rand(N, generator=gen)
+    g = torch.randn(N, generator=gen) * 2.0
+    for beta in (0.3, 0.9):
+        _check(a.to(dtype).to(DEV), b.to(dtype).to(DEV), g.to(DEV), beta, f"late peaks {dtype} beta={beta}")
+
+
 def test_jsd_special_rows():
     N, V = 10, 3001
     for dtype in (torch.bfloat16, torch.float32):

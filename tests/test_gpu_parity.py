@@ -277,3 +277,70 @@ def test_zz_report_error_stats():
     """Prints the worst error / tolerance seen by the parity tests above (informational)."""
     for k, v in sorted(parity.STATS.items()):
         print(k, v)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_many_rows_per_cta(dtype):
+    # more rows than 32 per persistent CTA (20011 rows, at most 304 CTAs): the forward finisher's batches
+    # of 32 rows roll over, with the next batch's target ids and target logits read a batch ahead
+    N, V = 20011, 1537
+    w = workloads.pages_shape(seed=71, N=N, V=V, dtype=dtype)
+    t = w["targets"].clone()
+    t[::97] = -1                     # ignored
+    t[5::1301] = V + 3               # outside the shard: NaN rows and the error bit
+    a, b = w["a"].to(DEV), w["b"].to(DEV)
+    _run_and_compare(a, b, t.to(DEV), w["grad"].to(DEV), tag=f"{N} rows {dtype} ")
+    if dtype != torch.bfloat16:
+        return
+    a64, b64 = parity.rows2d(a), parity.rows2d(b)
+    # the JSD's statistics-only first pass and the shard records take the same batched finisher
+    j, _, _ = vp.vp_jsd_fwd(a, b, 0.3)
+    parity.check_out(j, oracle.jsd_fwd(a64, b64, 0.3), f"{N} rows jsd")
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lp, _ = vp.vp_logprobs_merge(vp.vp_logprobs_partial(a, t.to(DEV))[None], err_word=err)
+    ref_lp, _, _, ref_err = oracle.logprobs_fwd(a64, t.numpy())
+    parity.check_out(lp, ref_lp, f"{N} rows logprobs via shard records")
+    torch.cuda.synchronize()
+    assert int(err.item()) == ref_err
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_peaked_rows(dtype):
+    # one logit 12 above the rest in every row (p near 1), at different columns in A and B, so that P's
+    # mode lies far down in Q (a large KL and a large centred mean c); targets at the peak or elsewhere,
+    # upstream gradients of a few units: the fp32 sums of such rows are dominated by one term
+    N, V = 512, 3001
+    gen = torch.Generator().manual_seed(73)
+    a = torch.randn(N, V, generator=gen) * 3
+    b = torch.randn(N, V, generator=gen) * 3
+    pa = torch.randint(0, V, (N,), generator=gen)
+    pb = torch.randint(0, V, (N,), generator=gen)
+    a[torch.arange(N), pa] += 12.0 + 4.0 * torch.rand(N, generator=gen)
+    b[torch.arange(N), pb] += 12.0 + 4.0 * torch.rand(N, generator=gen)
+    t = torch.where(torch.rand(N, generator=gen) < 0.5, pa, torch.randint(0, V, (N,), generator=gen))
+    g = torch.randn(N, generator=gen) * 2.0
+    _run_and_compare(a.to(dtype).to(DEV), b.to(dtype).to(DEV), t.to(DEV), g.to(DEV), tag=f"peaked {dtype} ")
+
+
+def _late_peaks(seed, N, V):
+    # N(0, 1) rows with one logit 18 to 24 higher past the first 8192 columns, at different columns in A
+    # and B; half the targets at A's peak; upstream gradients of a few units
+    gen = torch.Generator().manual_seed(seed)
+    a = torch.randn(N, V, generator=gen)
+    b = torch.randn(N, V, generator=gen)
+    pa = torch.randint(8192, V, (N,), generator=gen)
+    pb = torch.randint(8192, V, (N,), generator=gen)
+    a[torch.arange(N), pa] += 18.0 + 6.0 * torch.rand(N, generator=gen)
+    b[torch.arange(N), pb] += 18.0 + 6.0 * torch.rand(N, generator=gen)
+    t = torch.where(torch.rand(N, generator=gen) < 0.5, pa, torch.randint(0, V, (N,), generator=gen))
+    return a, b, t, torch.randn(N, generator=gen) * 2.0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_peaked_rows_late_chunks(dtype):
+    # rows of many ring stages: each warp centres its sums on its own largest value of the first stage, so
+    # a peak that arrives in a later stage sits ~20 above the centre, and the sums' terms near it (e and
+    # e t) are 20 units' worth of exponent and distance large: a plain fp32 running sum of them would
+    # leave W/S about 2^-24 times that distance off, which the gradients at the peak (p near 1) resolve
+    a, b, t, g = _late_peaks(74, 96, 75968)
+    _run_and_compare(a.to(dtype).to(DEV), b.to(dtype).to(DEV), t.to(DEV), g.to(DEV), tag=f"late peaks {dtype} ")

@@ -20,7 +20,11 @@
 //   A lane moves its own centre only when a value exceeds it by more than
 //   kSpan (so e^{z - ref} cannot overflow); this happens only in rows whose
 //   values span more than kSpan natural-log units, and the warp then merges
-//   in fp64 with explicit re-centring.
+//   in fp64 with explicit re-centring. bf16 inputs move sooner, beyond
+//   kSpanFast: their exponential takes the rounded product (z - ref) log2(e),
+//   whose error is (z - ref) 2^-24 relative in e^{z - ref}, so a large value
+//   far above the centre (a peak that arrives after the centre was chosen)
+//   would carry that error into S whole.
 //   The empty state has ref = -FLT_MAX and S = W = 0: an all -inf slice leaves
 //   it unchanged and needs no special case.
 #pragma once
@@ -34,6 +38,7 @@ namespace vp {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kNegBig = -3.4028234663852886e38f;  // -FLT_MAX
 constexpr float kSpan = 64.0f;                       // largest exponent a lane accumulates
+constexpr float kSpanFast = 4.0f;                    // the same on the bf16 path
 constexpr int kFwdThreads = 512;
 constexpr int kFwdWarps = kFwdThreads / 32;
 constexpr int kBwdThreads = 256;
@@ -78,7 +83,7 @@ template <typename T> struct Elem;
 
 template <> struct Elem<float> {
     static constexpr int kVec = 4;
-    static constexpr bool kPrecise = true;   // fp32 gradients are held to 1e-6 absolute
+    static constexpr bool kPrecise = true;   // fp32 gradients are held to 1e-6 (absolute up to 1, relative above)
     static __device__ __forceinline__ float load1(const float *p) { return __ldg(p); }
     static __device__ __forceinline__ void unpack(const uint4 &u, float *v) {
         v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
@@ -327,6 +332,34 @@ __device__ __forceinline__ float2 exp_split2(const DF2 &t) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(a_hi.y));
     const float2 r = __ffma2_rn(e, __fmul2_rn(na, f2(-kLn2)), e);      // e (1 + a_lo ln 2)
     return make_float2(e.x == 0.f ? 0.f : r.x, e.y == 0.f ? 0.f : r.y);   // a_lo is NaN where t_hi is infinite
+}
+
+// ---------------------------------------------------------------------------
+// Offset fast two-sum. A running sum started at a power of two K that exceeds
+// every addend keeps an exponent at least that of each addend, so Dekker's fast
+// two-sum (h = s + e; error = e - (h - s)) gives each addition's rounding error
+// exactly in three operations, against the six of two_sum; at the end s - K is
+// exact too (K is a multiple of the final sum's ulp).
+// ---------------------------------------------------------------------------
+// k of K = 2^k above e^{c - ref} for a chunk whose largest value is c: the 2^-8
+// margin covers the rounding of (c - ref) log2(e) and of exp_split (both below
+// 2e-5 in log2 units), so every exponential of the chunk is below 2^k. Clamped
+// to [-100, 100]: a chunk below 2^-100 of its centre is negligible in the row's
+// sum however it is added, and a non-finite c belongs to a row whose sums are
+// NaN already.
+__device__ __forceinline__ int offset_log2(float c, float ref) {
+    const float x = fmaf(c - ref, 1.4426950408889634f, 0.00390625f);
+    return min(max(__float2int_rd(x), -101), 99) + 1;
+}
+
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((k + 127) << 23); }   // k in [-126, 127]
+
+// s += e in each lane, its rounding error added to lo (requires |s| >= 2^j > |e| for some j)
+__device__ __forceinline__ void fast_acc2(float2 &s, float2 &lo, float2 e) {
+    const float2 m1 = f2(-1.f);
+    const float2 h = __fadd2_rn(s, e);
+    lo = __fadd2_rn(lo, __ffma2_rn(__ffma2_rn(s, m1, h), m1, e));   // e - (h - s)
+    s = h;
 }
 
 // Product (x_hi + x_lo) * (y_hi + y_lo) rounded once to fp32.

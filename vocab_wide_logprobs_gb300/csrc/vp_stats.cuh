@@ -97,6 +97,14 @@ __device__ __forceinline__ uint32_t word(const uint4 &u, int q) {
 // ---------------------------------------------------------------------------
 // One distribution, one lane
 // ---------------------------------------------------------------------------
+// How far a value may exceed a lane's centre before the centre moves to it. The
+// fp32 path's exponential takes an exact argument, so only overflow bounds it;
+// the bf16 path's takes the rounded (t log2 e), t 2^-24 relative error in e^t,
+// and a move at t > 4 keeps that within the hardware exponential's own error
+// scale (at most 2.4 2^-24) for the terms that carry S.
+template <typename T>
+__device__ __forceinline__ constexpr float centre_span() { return Elem<T>::kPrecise ? kSpan : kSpanFast; }
+
 template <typename T, bool kW>
 struct Lane1 {
     float ref, mx;
@@ -107,15 +115,25 @@ struct Lane1 {
         ref = r; mx = kNegBig; S = {0.f, 0.f}; W = {0.f, 0.f}; moved = 0;
     }
 
-    // Rare: a value exceeds the centre by more than kSpan.
+    // Rare: a value exceeds the centre by more than centre_span<T>(). The sums are
+    // re-centred in fp64 on the fp32 path; on the bf16 path, whose lane sums are
+    // plain fp32, in fp32 (c - ref is exact for bf16 values, expf is within 2 ulp).
     __device__ __forceinline__ void move_centre(float c) {
-        const double d = (double)c - (double)ref;
-        const double a = exp(-d);
-        double s = df_value(S), w = df_value(W);
-        if (kW) w = (a == 0.0) ? 0.0 : a * (w - d * s);
-        s *= a;
-        S = df_from(s);
-        W = df_from(w);
+        if constexpr (Elem<T>::kPrecise) {
+            const double d = (double)c - (double)ref;
+            const double a = exp(-d);
+            double s = df_value(S), w = df_value(W);
+            if (kW) w = (a == 0.0) ? 0.0 : a * (w - d * s);
+            s *= a;
+            S = df_from(s);
+            W = df_from(w);
+        } else {
+            const float d = c - ref;
+            const float a = expf(-d);
+            const float s = S.hi + S.lo;
+            if (kW) W = DF{(a == 0.f) ? 0.f : a * (W.hi + W.lo - d * s), 0.f};
+            S = DF{s * a, 0.f};
+        }
         ref = c;
         moved = 1;
     }
@@ -126,43 +144,69 @@ struct Lane1 {
 #pragma unroll
         for (int i = 1; i < n; ++i) c = fmaxf(c, v[i]);
         mx = fmaxf(mx, c);
-        if (c > ref + kSpan) move_centre(c);
+        if (c > ref + centre_span<T>()) move_centre(c);
         if constexpr (Elem<T>::kPrecise) {
             // fp32 inputs: exact centred value (double-float), exponential with an exact
             // argument (exp_split), the chunk summed in fp32 (even and odd values apart)
             // and folded into double-floats; on pairs of values (f32x2) where n is even,
-            // each lane rounding exactly as the scalar form
-            float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
+            // each lane rounding exactly as the scalar form.
+            // S and W are summed compensated: each addition's rounding error, and each
+            // product e t's, goes to a low part. In a peaked row one term carries most
+            // of S and W, and a plain fp32 running sum would leave W/S with a few 2^-24
+            // of that term's distance from the centre (up to kSpan), which the gradient
+            // at a mode with p near 1 resolves. The pairs use the offset fast two-sum:
+            // S from K = 2^k above the chunk's exponentials, W from 2^(k+11), above
+            // eight of its terms (|e t| < 2^(k+7): t >= -88 wherever e is not 0).
+            float s0 = 0.f, s1 = 0.f, sl0 = 0.f, sl1 = 0.f, w0 = 0.f, w1 = 0.f, wl0 = 0.f, wl1 = 0.f;
             if constexpr (n % 2 == 0) {
+                const int k = offset_log2(c, ref);
+                const float K = pow2f(k), KW = pow2f(k + 11);
                 const float2 nref = f2(-ref);
-                float2 s2 = f2(0.f), w2 = f2(0.f);
+                float2 s2 = f2(K), sl2 = f2(0.f), w2 = f2(KW), wl2 = f2(0.f);
 #pragma unroll
                 for (int i = 0; i < n; i += 2) {
                     const DF2 t = two_sum2(make_float2(v[i], v[i + 1]), nref);
                     const float2 e = exp_split2(t);
-                    s2 = __fadd2_rn(s2, e);
-                    if (kW) {   // zero-weight terms add nothing (t may be -inf there)
-                        const float2 wn = __ffma2_rn(e, t.hi, __ffma2_rn(e, t.lo, w2));
-                        w2 = make_float2(e.x != 0.f ? wn.x : w2.x, e.y != 0.f ? wn.y : w2.y);
+                    fast_acc2(s2, sl2, e);
+                    if (kW) {   // zero-weight terms add nothing (t may be -inf or NaN there)
+                        const float2 th = make_float2(e.x != 0.f ? t.hi.x : 0.f, e.y != 0.f ? t.hi.y : 0.f);
+                        const float2 tl = make_float2(e.x != 0.f ? t.lo.x : 0.f, e.y != 0.f ? t.lo.y : 0.f);
+                        const float2 ph = __fmul2_rn(e, th);
+                        const float2 pe = __ffma2_rn(e, th, make_float2(-ph.x, -ph.y));   // e th - ph, exact
+                        fast_acc2(w2, wl2, ph);
+                        wl2 = __fadd2_rn(wl2, __ffma2_rn(e, tl, pe));
                     }
                 }
-                s0 = s2.x; s1 = s2.y; w0 = w2.x; w1 = w2.y;
+                s0 = s2.x - K; s1 = s2.y - K; sl0 = sl2.x; sl1 = sl2.y;   // exact differences
+                w0 = w2.x - KW; w1 = w2.y - KW; wl0 = wl2.x; wl1 = wl2.y;
             } else {
 #pragma unroll
                 for (int i = 0; i < n; ++i) {
                     const DF t = df_diff(v[i], ref);
                     const float e = exp_split(t.hi, t.lo);
-                    if (i & 1) {
-                        s1 += e;
-                        if (kW && e != 0.f) w1 = fmaf(e, t.hi, fmaf(e, t.lo, w1));
-                    } else {
-                        s0 += e;
-                        if (kW && e != 0.f) w0 = fmaf(e, t.hi, fmaf(e, t.lo, w0));
+                    float &si = (i & 1) ? s1 : s0;
+                    float &sli = (i & 1) ? sl1 : sl0;
+                    const DF ss = two_sum(si, e);
+                    si = ss.hi;
+                    sli += ss.lo;
+                    if (kW && e != 0.f) {
+                        const float ph = e * t.hi, pe = fmaf(e, t.hi, -ph);
+                        float &wi = (i & 1) ? w1 : w0;
+                        float &wli = (i & 1) ? wl1 : wl0;
+                        const DF sw = two_sum(wi, ph);
+                        wi = sw.hi;
+                        wli = wli + (sw.lo + fmaf(e, t.lo, pe));
                     }
                 }
             }
-            df_add(S, s0 + s1);
-            if (kW) df_add(W, w0 + w1);
+            df_add(S, s0);
+            df_add(S, s1);
+            S.lo = __fadd_rn(S.lo, sl0 + sl1);
+            if (kW) {
+                df_add(W, w0);
+                df_add(W, w1);
+                W.lo = __fadd_rn(W.lo, wl0 + wl1);
+            }
         } else {
             float s0 = 0.f, s1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
@@ -190,7 +234,7 @@ struct Lane1 {
     __device__ __forceinline__ void push_bf16(const uint4 (&u)[K]) {
         const float c = max_bf16(u);
         mx = fmaxf(mx, c);
-        if (c > ref + kSpan) move_centre(c);
+        if (c > ref + centre_span<T>()) move_centre(c);
         const float2 nref = make_float2(-ref, -ref), l2e = make_float2(kLog2e, kLog2e);
         float2 s[4], w[4];
 #pragma unroll
@@ -339,13 +383,23 @@ struct LaneKL {
         flag = 0; moved = 0;
     }
 
+    // as Lane1::move_centre, for both centres
     __device__ __forceinline__ void move_centres(float np, float nq) {
-        const double dp = (double)np - (double)rp, dq = (double)nq - (double)rq;
-        const double ap = exp(-dp), aq = exp(-dq);
-        const double sp = df_value(Sp), sq = df_value(Sq), w = df_value(W);
-        W = df_from(ap == 0.0 ? 0.0 : ap * (w - (dp - dq) * sp));
-        Sp = df_from(sp * ap);
-        Sq = df_from(sq * aq);
+        if constexpr (Elem<T>::kPrecise) {
+            const double dp = (double)np - (double)rp, dq = (double)nq - (double)rq;
+            const double ap = exp(-dp), aq = exp(-dq);
+            const double sp = df_value(Sp), sq = df_value(Sq), w = df_value(W);
+            W = df_from(ap == 0.0 ? 0.0 : ap * (w - (dp - dq) * sp));
+            Sp = df_from(sp * ap);
+            Sq = df_from(sq * aq);
+        } else {
+            const float dp = np - rp, dq = nq - rq;
+            const float ap = expf(-dp), aq = expf(-dq);
+            const float sp = Sp.hi + Sp.lo, sq = Sq.hi + Sq.lo;
+            W = DF{ap == 0.f ? 0.f : ap * (W.hi + W.lo - (dp - dq) * sp), 0.f};
+            Sp = DF{sp * ap, 0.f};
+            Sq = DF{sq * aq, 0.f};
+        }
         rp = np;
         rq = nq;
         moved = 1;
@@ -358,7 +412,7 @@ struct LaneKL {
         for (int i = 1; i < n; ++i) { cp = fmaxf(cp, p[i]); cq = fmaxf(cq, q[i]); }
         mxp = fmaxf(mxp, cp);
         mxq = fmaxf(mxq, cq);
-        const bool up = cp > rp + kSpan, uq = cq > rq + kSpan;
+        const bool up = cp > rp + centre_span<T>(), uq = cq > rq + centre_span<T>();
         if (up || uq) move_centres(up ? cp : rp, uq ? cq : rq);
         int fl = 0;
         if constexpr (Elem<T>::kPrecise) {
@@ -366,21 +420,34 @@ struct LaneKL {
             // of the even and the odd values folded into double-floats, pairs of values
             // in f32x2 where n is even)
             float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
+            // All three sums are compensated (see Lane1::push). Sp and Sq take the offset
+            // fast two-sum from 2^k above each chunk's exponentials; W's terms (the
+            // product's rounding error from an FMA, the sum's from a two-sum, both into
+            // wl) have no such bound, d = tp - tq growing without limit where Q is far
+            // below its centre. Where one term carries most of W (a peaked P whose mode Q
+            // puts far below its own), a plain fp32 sum would leave c = W / S_P with
+            // 2^-24 of that term's size
+            float wl0 = 0.f, wl1 = 0.f, spl0 = 0.f, sql0 = 0.f;   // low parts of the compensated sums
             if constexpr (n % 2 == 0) {
                 const float2 nrp = f2(-rp), nrq = f2(-rq);
-                float2 sp = f2(0.f), sq = f2(0.f), w = f2(0.f);
+                const float Kp = pow2f(offset_log2(cp, rp)), Kq = pow2f(offset_log2(cq, rq));
+                float2 sp = f2(Kp), sq = f2(Kq), spl = f2(0.f), sql = f2(0.f), w = f2(0.f), wl = f2(0.f);
                 float qmin = q[0];
 #pragma unroll
                 for (int i = 0; i < n; i += 2) {
                     const DF2 tp = two_sum2(make_float2(p[i], p[i + 1]), nrp);
                     const DF2 tq = two_sum2(make_float2(q[i], q[i + 1]), nrq);
                     const float2 ep = exp_split2(tp), eq = exp_split2(tq);
-                    sp = __fadd2_rn(sp, ep);
-                    sq = __fadd2_rn(sq, eq);
+                    fast_acc2(sp, spl, ep);
+                    fast_acc2(sq, sql, eq);
                     if constexpr (kW) {
                         const DF2 d = df_sub2(tp, tq);
-                        const float2 wn = __ffma2_rn(ep, d.hi, __ffma2_rn(ep, d.lo, w));
-                        w = make_float2(ep.x != 0.f ? wn.x : w.x, ep.y != 0.f ? wn.y : w.y);   // zero weights add nothing
+                        const float2 ph = __fmul2_rn(ep, d.hi);
+                        const float2 pe = __ffma2_rn(ep, d.hi, make_float2(-ph.x, -ph.y));   // ep d.hi - ph, exact
+                        const DF2 sw = two_sum2(w, ph);
+                        const float2 wln = __fadd2_rn(wl, __fadd2_rn(sw.lo, __ffma2_rn(ep, d.lo, pe)));
+                        w = make_float2(ep.x != 0.f ? sw.hi.x : w.x, ep.y != 0.f ? sw.hi.y : w.y);   // zero weights add nothing
+                        wl = make_float2(ep.x != 0.f ? wln.x : wl.x, ep.y != 0.f ? wln.y : wl.y);
                         qmin = fminf(qmin, fminf(q[i], q[i + 1]));
                     }
                 }
@@ -388,7 +455,10 @@ struct LaneKL {
 #pragma unroll
                     for (int i = 0; i < n; ++i) fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
                 }
-                sp0 = sp.x; sp1 = sp.y; sq0 = sq.x; sq1 = sq.y; w0 = w.x; w1 = w.y;
+                sp0 = sp.x - Kp; sp1 = sp.y - Kp; sq0 = sq.x - Kq; sq1 = sq.y - Kq;   // exact differences
+                w0 = w.x; w1 = w.y; wl0 = wl.x; wl1 = wl.y;
+                spl0 = spl.x + spl.y;
+                sql0 = sql.x + sql.y;
             } else {
 #pragma unroll
                 for (int i = 0; i < n; ++i) {
@@ -396,17 +466,32 @@ struct LaneKL {
                     const float ep = exp_split(tp.hi, tp.lo), eq = exp_split(tq.hi, tq.lo);
                     if (kW && ep != 0.f) {           // zero-weight terms add nothing
                         const DF d = df_sub(tp, tq.hi, tq.lo);
+                        const float ph = ep * d.hi, pe = fmaf(ep, d.hi, -ph);
                         float &wi = (i & 1) ? w1 : w0;
-                        wi = fmaf(ep, d.hi, fmaf(ep, d.lo, wi));
+                        float &wli = (i & 1) ? wl1 : wl0;
+                        const DF sw = two_sum(wi, ph);
+                        wi = sw.hi;
+                        wli = wli + (sw.lo + fmaf(ep, d.lo, pe));
                     }
-                    if (i & 1) { sp1 += ep; sq1 += eq; }
-                    else       { sp0 += ep; sq0 += eq; }
+                    float &spi = (i & 1) ? sp1 : sp0;
+                    float &sqi = (i & 1) ? sq1 : sq0;
+                    const DF ssp = two_sum(spi, ep), ssq = two_sum(sqi, eq);
+                    spi = ssp.hi;
+                    sqi = ssq.hi;
+                    spl0 += ssp.lo;
+                    sql0 += ssq.lo;
                     if (kW) fl |= (q[i] == -INFINITY) & (p[i] > -INFINITY);
                 }
             }
-            df_add(Sp, sp0 + sp1);
-            df_add(Sq, sq0 + sq1);
-            df_add(W, w0 + w1);
+            df_add(Sp, sp0);
+            df_add(Sp, sp1);
+            Sp.lo = __fadd_rn(Sp.lo, spl0);
+            df_add(Sq, sq0);
+            df_add(Sq, sq1);
+            Sq.lo = __fadd_rn(Sq.lo, sql0);
+            df_add(W, w0);
+            df_add(W, w1);
+            W.lo = __fadd_rn(W.lo, wl0 + wl1);
         } else {
             float sp0 = 0.f, sp1 = 0.f, sq0 = 0.f, sq1 = 0.f, w0 = 0.f, w1 = 0.f;
 #pragma unroll
@@ -432,7 +517,7 @@ struct LaneKL {
         const float cp = max_bf16(up), cq = max_bf16(uq);
         mxp = fmaxf(mxp, cp);
         mxq = fmaxf(mxq, cq);
-        const bool mp = cp > rp + kSpan, mq = cq > rq + kSpan;
+        const bool mp = cp > rp + centre_span<T>(), mq = cq > rq + centre_span<T>();
         if (mp || mq) move_centres(mp ? cp : rp, mq ? cq : rq);
         const float2 nrp = make_float2(-rp, -rp), nrq = make_float2(-rq, -rq);
         const float2 l2e = make_float2(kLog2e, kLog2e), m1 = make_float2(-1.f, -1.f);
