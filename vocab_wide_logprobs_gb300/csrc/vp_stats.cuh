@@ -223,13 +223,14 @@ struct Lane1 {
     }
 
     // bf16 fast path on raw 16-byte words (8 values each): packed max, packed
-    // f32x2 arithmetic and four independent accumulator pairs. The chunk sums
-    // are added to the lane's running sums in plain fp32 (S.hi, W.hi; a lane
-    // takes about ten chunks per row, and every term of W has the sign of t,
-    // so W does not cancel); the warp merges the lanes as double-floats and
-    // the warp partials are merged in fp64. The hardware exponential's error
-    // pattern (bias -5e-8 below -1, +3.3e-8 above +1, spread 3e-8, measured on
-    // GB300) bounds c = W / S at ~2^-23 relative; finer sums would not move it.
+    // f32x2 arithmetic and four independent accumulator pairs. The chunk sums are
+    // folded into the lane's double-float sums: after a lane's centre has moved to
+    // a peak (S near 1), the later chunks each add far less than an ulp of S, and
+    // a plain fp32 running sum would drop them whole (up to the lane's whole
+    // off-peak mass, some 2^-24 of S). The warp merges the lanes as double-floats
+    // and the partials likewise (warp_sum_acc). What remains is the hardware
+    // exponential's error pattern (bias -5e-8 below -1, +3.3e-8 above +1, spread
+    // 3e-8, measured on GB300), ~2^-23 relative on c = W / S.
     template <int K>
     __device__ __forceinline__ void push_bf16(const uint4 (&u)[K]) {
         const float c = max_bf16(u);
@@ -254,7 +255,7 @@ struct Lane1 {
             }
         }
         const float2 ss = __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
-        S.hi += ss.x + ss.y;
+        df_add(S, ss.x + ss.y);
         if (kW) {
             float2 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
             float wsum = ww.x + ww.y;
@@ -276,7 +277,7 @@ struct Lane1 {
                 ww = __fadd2_rn(__fadd2_rn(w[0], w[1]), __fadd2_rn(w[2], w[3]));
                 wsum = ww.x + ww.y;
             }
-            W.hi += wsum;
+            df_add(W, wsum);
         }
     }
 };
@@ -300,6 +301,22 @@ __device__ __forceinline__ V warp_sum_t(V v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
     return v;
+}
+
+// Sum over the warp's lanes for the merges of partials: fp64 values as they are;
+// fp32 values (the bf16 path) as double-floats, rounded once at the end. A plain
+// fp32 butterfly rounds at each of its five levels, and where one lane carries the
+// sum (the partial that holds a peaked row's mode) each rounding can take half an
+// ulp of it: up to 5 2^-24 of S in log S, which gradients at p near 1, and q - p
+// where q ~ p, resolve. The double-float add is symmetric, so all lanes agree;
+// a non-finite sum keeps the fp32 butterfly's value (W = +inf in a row whose
+// support mismatches stays +inf rather than turning NaN through its low part).
+__device__ __forceinline__ double warp_sum_acc(double v) { return warp_sum_t(v); }
+__device__ __forceinline__ float warp_sum_acc(float v) {
+    DF s{v, 0.f};
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) df_add(s, shfl_xor(s, m));
+    return isfinite(s.hi) ? s.hi + s.lo : s.hi;
 }
 
 template <typename V>
@@ -331,8 +348,8 @@ __device__ __forceinline__ Part1<AccT<T>> warp_merge(const Lane1<T, kW> &L) {
         if (sc != V(0)) { if (kW) wc = a * (w - ((V)M - (V)L.ref) * s); }
         else sc = V(0);
         o.ref = M;
-        o.S = warp_sum_t(sc);
-        o.W = kW ? warp_sum_t(wc) : V(0);
+        o.S = warp_sum_acc(sc);
+        o.W = kW ? warp_sum_acc(wc) : V(0);
     }
     return o;
 }
@@ -350,8 +367,8 @@ __device__ __forceinline__ Part1<V> merge_lane_parts(const Part1<V> &q) {
     Part1<V> o;
     o.ref = M;
     o.mx = warp_max(q.mx);
-    o.S = warp_sum_t(sc);
-    o.W = kW ? warp_sum_t(wc) : V(0);
+    o.S = warp_sum_acc(sc);
+    o.W = kW ? warp_sum_acc(wc) : V(0);
     return o;
 }
 
@@ -627,7 +644,7 @@ __device__ __forceinline__ PartKL<AccT<T>> kl_warp_merge(const LaneKL<T, kW> &L)
         V sp, sq, w;
         kl_recentred<V>(L.rp, L.rq, df_to<V>(L.Sp), df_to<V>(L.Sq), df_to<V>(L.W), Mp, Mq, sp, sq, w);
         o.rp = Mp; o.rq = Mq;
-        o.Sp = warp_sum_t(sp); o.Sq = warp_sum_t(sq); o.W = warp_sum_t(w);
+        o.Sp = warp_sum_acc(sp); o.Sq = warp_sum_acc(sq); o.W = warp_sum_acc(w);
     }
     return o;
 }
@@ -647,7 +664,7 @@ __device__ __forceinline__ PartKL<V> kl_merge_lane_parts(const PartKL<V> &q) {
     o.rp = Mp; o.rq = Mq;
     o.mxp = warp_max(q.mxp);
     o.mxq = warp_max(q.mxq);
-    o.Sp = warp_sum_t(sp); o.Sq = warp_sum_t(sq); o.W = warp_sum_t(w);
+    o.Sp = warp_sum_acc(sp); o.Sq = warp_sum_acc(sq); o.W = warp_sum_acc(w);
     o.flag = __any_sync(0xffffffffu, q.flag);
     return o;
 }
