@@ -370,17 +370,23 @@ def jsd_bench(args, a, b, g, dev, peaks, beta=0.5):
 
 
 def strided_bench(args, dev, peaks, st, err, dx, da, db):
-    """The step's eight calls on the strided workload: x[:, :-1] of [16, 513, 75968] bf16 tensors (8192
-    rows addressed with two strides, read in place), into the step's contiguous outputs."""
+    """The step's eight calls on the strided workload: x[:, :-1] of [B, 513, 75968] bf16 tensors (512 rows
+    per outer index addressed with two strides, read in place; B = ceil(rows / 512), 16 at the default 8192
+    rows), into the step's contiguous outputs, or into its own where its row count differs from the step's."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     from vocab_wide_logprobs_gb300 import workloads
-    w = workloads.strided()
+    w = workloads.strided(B=max(1, -(-args.rows // 512)))
     af, bf = w["a_full"].to(dev), w["b_full"].to(dev)
     t, g = w["targets"].reshape(-1).to(dev), w["grad"].reshape(-1).to(dev)
     del w
     a, b = af[:, :-1], bf[:, :-1]
     N, V = a.shape[0] * a.shape[1], a.shape[2]
+    if dx.shape != (N, V):   # the step's outputs hold another number of rows
+        f32 = lambda: torch.empty(N, dtype=torch.float32, device=dev)
+        st = {k: f32() for k in ("lp", "H", "kl", "kl2")}
+        st.update({k: vp.rowstats(N, dev) for k in ("lp_s", "H_s", "sa", "sb", "sa2", "sb2")})
+        dx, da, db = (torch.empty((N, V), dtype=a.dtype, device=dev) for _ in range(3))
     R, F = vp.KL_REVERSE, vp.KL_FORWARD
     calls = {
         "logprobs_fwd": lambda: vp.vp_logprobs_fwd(a, t, 0, err, st["lp"], st["lp_s"]),
@@ -394,8 +400,8 @@ def strided_bench(args, dev, peaks, st, err, dx, da, db):
     }
     line = _time_calls(args, calls, STEP_ORDER, algorithmic_bytes(N, V), peaks)
     del af, bf
-    return {"workload": "x[:, :-1] of [16, 513, 75968] bf16 tensors A and B: 8192 rows, 512 per outer index, "
-                        "read in place with two row strides; gradients written contiguous", **line}
+    return {"workload": f"x[:, :-1] of [{a.shape[0]}, 513, {V}] bf16 tensors A and B: {N} rows, 512 per outer "
+                        "index, read in place with two row strides; gradients written contiguous", **line}
 
 
 def _time_calls(args, calls, order, nbytes, peaks):
@@ -548,12 +554,13 @@ def short_batch_bench(args, dev, peaks, rows=1024, reps=10):
 
 def stress_bench(args, dev, peaks):
     """The fp32 numerics-stress workload: entropy and KL in both directions, fwd and bwd (gradients to
-    both inputs), on [8192, 75968] fp32 rows offset by 1e4 with 1% of B masked to -inf, so that KL(A||B) is
-    +inf on essentially every row and KL(B||A) runs the zero-weight path at a large offset."""
+    both inputs), on [N, 75968] fp32 rows (N = --rows, 8192 by default) offset by 1e4 with 1% of B masked
+    to -inf, so that KL(A||B) is +inf on essentially every row and KL(B||A) runs the zero-weight path at a
+    large offset."""
     import torch
     import vocab_wide_logprobs_gb300 as vp
     from vocab_wide_logprobs_gb300 import workloads
-    w = workloads.numerics_stress()
+    w = workloads.numerics_stress(N=args.rows)
     a, b, g = w["a"].to(dev), w["b"].to(dev), w["grad"].to(dev)
     del w
     N, V = a.shape
@@ -573,7 +580,7 @@ def stress_bench(args, dev, peaks):
     order = [k for k in STEP_ORDER if k in calls]
     line = _time_calls(args, calls, order, algorithmic_bytes(N, V, s=4), peaks)
     del a, b, dx, da, db
-    return {"workload": "8192x75968 fp32, N(0, 9) + 1e4 on every row of A and B, 1% of B set to -inf; entropy "
+    return {"workload": f"{N}x{V} fp32, N(0, 9) + 1e4 on every row of A and B, 1% of B set to -inf; entropy "
                         "and KL both directions, fwd+bwd", **line}
 
 

@@ -107,6 +107,36 @@ def _f32(n, like):
     return torch.empty(n, dtype=torch.float32, device=like.device)
 
 
+def _arg(t, n: int, dtype, like, what: str):
+    """A caller's tensor behind one of the C ABI's pointers. The library reads or writes exactly n elements
+    of dtype there, so another size, dtype or device, or a strided view, is refused here, before a kernel
+    could run past its end. None passes (an output to allocate, or an optional pointer)."""
+    if t is None:
+        return None
+    bad = (2 if t.numel() != n else 3 if t.dtype != dtype else 4 if (t.device != like.device or not t.is_contiguous())
+           else 0)
+    if bad:
+        raise VPError(bad, f"{what}: needs {n} contiguous {dtype} elements on {like.device}, got "
+                           f"{tuple(t.shape)} {t.dtype} on {t.device}{'' if t.is_contiguous() else ', strided'}")
+    return t
+
+
+def _row_args(like, N, targets=None, stats=(), grad=None, err_word=None, outs=(), K=1):
+    """The per-row arguments of a logits call: targets int64 [N] ([N, K] for top-k), vp_rowstat records,
+    the upstream gradient fp32 [N] ([N, K]), the error word int32 [1] and fp32 [N] ([N, K]) outputs."""
+    _arg(targets, N * K, torch.int64, like, "targets")
+    for i, st in enumerate(stats):
+        _arg(st, N * ROWSTAT_FLOATS, torch.float32, like, f"stats{'' if len(stats) == 1 else ' ' + 'ab'[i]}")
+    _arg(grad, N * K, torch.float32, like, "grad")
+    _arg(err_word, 1, torch.int32, like, "err_word")
+    for o in outs:
+        _arg(o, N * K, torch.float32, like, "per-row output")
+
+
+def _parts_arg(parts, n_records: int, like):
+    _arg(parts, n_records * PARTIAL_DOUBLES, torch.float64, like, "parts")
+
+
 def _same_layout(a: torch.Tensor, b: torch.Tensor):
     if a.shape != b.shape or a.stride() != b.stride() or a.dtype != b.dtype:
         raise VPError(4, "A and B must share shape, strides and dtype")
@@ -115,6 +145,7 @@ def _same_layout(a: torch.Tensor, b: torch.Tensor):
 def vp_logprobs_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=None, stats=None):
     """Returns (logp fp32 [N], stats vp_rowstat [N] as float32 [N, 8])."""
     N, V, R, s_o, s_i = rows_of(x)
+    _row_args(x, N, targets=targets, stats=(stats,), err_word=err_word, outs=(logp,))
     logp = _f32(N, x) if logp is None else logp
     stats = rowstats(N, x.device) if stats is None else stats
     _check(_lib.lib().vp_logprobs_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
@@ -125,6 +156,8 @@ def vp_logprobs_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=None, 
 def vp_logprobs_bwd(x, targets, stats, grad, vocab_start: int = 0, err_word=None, dx=None):
     """Returns dx, contiguous [N, V] in the dtype of x."""
     N, V, R, s_o, s_i = rows_of(x)
+    _row_args(x, N, targets=targets, stats=(stats,), grad=grad, err_word=err_word)
+    _arg(dx, N * V, x.dtype, x, "dx")
     dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
     _check(_lib.lib().vp_logprobs_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
                                       _ptr(stats), _ptr(grad), _ptr(dx), _ptr(err_word), _stream()),
@@ -142,6 +175,8 @@ def vp_logprobs_topk_fwd(x, targets, vocab_start: int = 0, err_word=None, logp=N
     """logp of K ids per row; targets int64 [N, K]. Returns (logp fp32 [N, K], stats)."""
     N, V, R, s_o, s_i = rows_of(x)
     K = _topk_ids(targets)
+    _row_args(x, N, targets=targets, err_word=err_word, outs=(logp,), K=K)
+    _row_args(x, N, stats=(stats,))
     logp = torch.empty((N, K), dtype=torch.float32, device=x.device) if logp is None else logp
     stats = rowstats(N, x.device) if stats is None else stats
     _check(_lib.lib().vp_logprobs_topk_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets), K,
@@ -153,6 +188,9 @@ def vp_logprobs_topk_bwd(x, targets, stats, grad, vocab_start: int = 0, err_word
     """Gradient of sum_k grad[r, k] logp[r, k] (grad fp32 [N, K]); returns dx [N, V] in the dtype of x."""
     N, V, R, s_o, s_i = rows_of(x)
     K = _topk_ids(targets)
+    _row_args(x, N, targets=targets, grad=grad, err_word=err_word, K=K)
+    _row_args(x, N, stats=(stats,))
+    _arg(dx, N * V, x.dtype, x, "dx")
     dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
     _check(_lib.lib().vp_logprobs_topk_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets), K,
                                            _ptr(stats), _ptr(grad), _ptr(dx), _ptr(err_word), _stream()),
@@ -163,6 +201,7 @@ def vp_logprobs_topk_bwd(x, targets, stats, grad, vocab_start: int = 0, err_word
 def vp_entropy_fwd(x, H=None, stats=None):
     """Returns (H fp32 [N], stats)."""
     N, V, R, s_o, s_i = rows_of(x)
+    _row_args(x, N, stats=(stats,), outs=(H,))
     H = _f32(N, x) if H is None else H
     stats = rowstats(N, x.device) if stats is None else stats
     _check(_lib.lib().vp_entropy_fwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(H), _ptr(stats), _stream()),
@@ -172,6 +211,8 @@ def vp_entropy_fwd(x, H=None, stats=None):
 
 def vp_entropy_bwd(x, stats, grad, dx=None):
     N, V, R, s_o, s_i = rows_of(x)
+    _row_args(x, N, stats=(stats,), grad=grad)
+    _arg(dx, N * V, x.dtype, x, "dx")
     dx = torch.empty((N, V), dtype=x.dtype, device=x.device) if dx is None else dx
     _check(_lib.lib().vp_entropy_bwd(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(stats), _ptr(grad),
                                      _ptr(dx), _stream()), "vp_entropy_bwd")
@@ -182,6 +223,7 @@ def vp_kl_fwd(a, b, direction: int = KL_REVERSE, kl=None, stats_a=None, stats_b=
     """Returns (kl, stats_a, stats_b); reverse = KL(A||B), forward = KL(B||A)."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
+    _row_args(a, N, stats=(stats_a, stats_b), outs=(kl,))
     kl = _f32(N, a) if kl is None else kl
     stats_a = rowstats(N, a.device) if stats_a is None else stats_a
     stats_b = rowstats(N, a.device) if stats_b is None else stats_b
@@ -194,6 +236,9 @@ def vp_kl_bwd(a, b, direction, stats_a, stats_b, grad, want_da=True, want_db=Tru
     """Returns (da, db); an unwanted gradient is None and is not computed."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
+    _row_args(a, N, stats=(stats_a, stats_b), grad=grad)
+    _arg(da if want_da else None, N * V, a.dtype, a, "da")
+    _arg(db if want_db else None, N * V, a.dtype, a, "db")
     if want_da and da is None:
         da = torch.empty((N, V), dtype=a.dtype, device=a.device)
     if want_db and db is None:
@@ -212,6 +257,7 @@ def vp_jsd_fwd(a, b, beta: float = 0.5, jsd=None, stats_a=None, stats_b=None):
     Returns (jsd fp32 [N], stats of a, stats of b)."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
+    _row_args(a, N, stats=(stats_a, stats_b), outs=(jsd,))
     jsd = _f32(N, a) if jsd is None else jsd
     stats_a = rowstats(N, a.device) if stats_a is None else stats_a
     stats_b = rowstats(N, a.device) if stats_b is None else stats_b
@@ -224,6 +270,9 @@ def vp_jsd_bwd(a, b, beta, stats_a, stats_b, grad, want_da=True, want_db=True, d
     """Returns (da, db); an unwanted gradient (a frozen input) is None and is not computed."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
+    _row_args(a, N, stats=(stats_a, stats_b), grad=grad)
+    _arg(da if want_da else None, N * V, a.dtype, a, "da")
+    _arg(db if want_db else None, N * V, a.dtype, a, "db")
     if want_da and da is None:
         da = torch.empty((N, V), dtype=a.dtype, device=a.device)
     if want_db and db is None:
@@ -252,6 +301,7 @@ def vp_linear_logp_fwd(hidden, weight, targets, vocab_start: int = 0, err_word=N
     V = weight.shape[0]
     if weight.shape[1] != D:
         raise VPError(2, "hidden and weight disagree on D")
+    _row_args(hidden, N, targets=targets, stats=(stats,), err_word=err_word, outs=(logp,))
     logp = _f32(N, hidden) if logp is None else logp
     stats = rowstats(N, hidden.device) if stats is None else stats
     need = vp_linear_logp_workspace_size(N, V, D)
@@ -272,8 +322,10 @@ def vp_linear_logp_bwd(hidden, weight, targets, stats, grad, vocab_start: int = 
                        err_word=None, dhidden=None, dW=None, workspace=None, precision: int = None):
     """Returns (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None). precision: GRAD_EXACT (default:
     dz as a bf16 pair hi + lo in the gradient GEMMs) or GRAD_FAST (dz rounded to bf16)."""
-    N, D = hidden.shape
-    V = weight.shape[0]
+    N, V, D = _linear_model(hidden, weight, "vp_linear_logp_bwd")
+    _row_args(hidden, N, targets=targets, stats=(stats,), grad=grad, err_word=err_word)
+    _arg(dhidden if want_dhidden else None, N * D, torch.bfloat16, hidden, "dhidden")
+    _arg(dW if want_dW else None, V * D, torch.bfloat16, hidden, "dW")
     if want_dhidden and dhidden is None:
         dhidden = torch.empty((N, D), dtype=torch.bfloat16, device=hidden.device)
     if want_dW and dW is None:
@@ -298,8 +350,8 @@ def vp_linear_logp_fwd_noalloc(hidden, weight, targets, vocab_start: int = 0, er
         raise VPError(3, "vp_linear_logp_fwd_noalloc takes bf16 hidden and weight")
     if not (hidden.is_contiguous() and weight.is_contiguous()) or hidden.dim() != 2 or weight.dim() != 2:
         raise VPError(4, "hidden and weight must be contiguous 2-D tensors")
-    N, D = hidden.shape
-    V = weight.shape[0]
+    N, V, D = _linear_model(hidden, weight, "vp_linear_logp_fwd_noalloc")
+    _row_args(hidden, N, targets=targets, stats=(stats,), err_word=err_word, outs=(logp,))
     logp = _f32(N, hidden) if logp is None else logp
     stats = rowstats(N, hidden.device) if stats is None else stats
     _check(_lib.lib().vp_linear_logp_fwd_noalloc(_ptr(hidden), _ptr(weight), N, V, D, vocab_start, _ptr(targets),
@@ -381,6 +433,7 @@ def vp_version() -> int:
 def vp_linear_entropy_fwd(hidden, weight, H=None, stats=None, workspace=None):
     """Entropy of softmax(hidden @ weight^T) per row; returns (H fp32 [N], stats)."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_fwd")
+    _row_args(hidden, N, stats=(stats,), outs=(H,))
     H = _f32(N, hidden) if H is None else H
     stats = rowstats(N, hidden.device) if stats is None else stats
     if workspace is None:
@@ -394,6 +447,9 @@ def vp_linear_entropy_bwd(hidden, weight, stats, grad, want_dhidden=True, want_d
                           workspace=None, precision: int = None):
     """Gradients of sum_r grad[r] H[r]: (dhidden bf16 [N, D] or None, dW bf16 [V, D] or None)."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_bwd")
+    _row_args(hidden, N, stats=(stats,), grad=grad)
+    _arg(dhidden if want_dhidden else None, N * D, torch.bfloat16, hidden, "dhidden")
+    _arg(dW if want_dW else None, V * D, torch.bfloat16, hidden, "dW")
     dhidden = (torch.empty((N, D), dtype=torch.bfloat16, device=hidden.device) if dhidden is None else dhidden) \
         if want_dhidden else None
     dW = (torch.empty((V, D), dtype=torch.bfloat16, device=hidden.device) if dW is None else dW) if want_dW else None
@@ -419,6 +475,7 @@ def vp_linear_kl_fwd(ha, wa, hb, wb, direction: int = KL_REVERSE, kl=None, stats
     """KL between softmax(ha @ wa^T) and softmax(hb @ wb^T); reverse = KL(A||B).
     Returns (kl fp32 [N], stats_a, stats_b)."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_fwd")
+    _row_args(ha, N, stats=(stats_a, stats_b), outs=(kl,))
     kl = _f32(N, ha) if kl is None else kl
     stats_a = rowstats(N, ha.device) if stats_a is None else stats_a
     stats_b = rowstats(N, ha.device) if stats_b is None else stats_b
@@ -435,6 +492,13 @@ def vp_linear_kl_bwd(ha, wa, hb, wb, direction, stats_a, stats_b, grad, want=(Tr
     """Gradients of sum_r grad[r] KL[r]: (dha, dwa, dhb, dwb), bf16, None where not wanted."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_bwd")
     shapes = ((N, Da), (V, Da), (N, Db), (V, Db))
+    _row_args(ha, N, stats=(stats_a, stats_b), grad=grad)
+    if outs is not None:
+        if len(outs) != 4:
+            raise VPError(7, "outs: four gradients (dha, dwa, dhb, dwb), None where not wanted")
+        for o, sh, w, nm in zip(outs, shapes, want, ("dha", "dwa", "dhb", "dwb")):
+            _arg(o if w else None, sh[0] * sh[1], torch.bfloat16, ha, nm)
+        outs = [o if w else None for o, w in zip(outs, want)]
     if outs is None:
         outs = [torch.empty(s, dtype=torch.bfloat16, device=ha.device) if w else None for s, w in zip(shapes, want)]
     if workspace is None:
@@ -450,6 +514,7 @@ def vp_linear_jsd_fwd(ha, wa, hb, wb, beta: float = 0.5, jsd=None, stats_a=None,
     """Generalized JSD of softmax(ha @ wa^T) (student) and softmax(hb @ wb^T) (teacher).
     Returns (jsd fp32 [N], stats_a, stats_b)."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_jsd_fwd")
+    _row_args(ha, N, stats=(stats_a, stats_b), outs=(jsd,))
     jsd = _f32(N, ha) if jsd is None else jsd
     stats_a = rowstats(N, ha.device) if stats_a is None else stats_a
     stats_b = rowstats(N, ha.device) if stats_b is None else stats_b
@@ -466,6 +531,13 @@ def vp_linear_jsd_bwd(ha, wa, hb, wb, beta, stats_a, stats_b, grad, want=(True, 
     """Gradients of sum_r grad[r] JSD[r]: (dha, dwa, dhb, dwb), bf16, None where not wanted."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_jsd_bwd")
     shapes = ((N, Da), (V, Da), (N, Db), (V, Db))
+    _row_args(ha, N, stats=(stats_a, stats_b), grad=grad)
+    if outs is not None:
+        if len(outs) != 4:
+            raise VPError(7, "outs: four gradients (dha, dwa, dhb, dwb), None where not wanted")
+        for o, sh, w, nm in zip(outs, shapes, want, ("dha", "dwa", "dhb", "dwb")):
+            _arg(o if w else None, sh[0] * sh[1], torch.bfloat16, ha, nm)
+        outs = [o if w else None for o, w in zip(outs, want)]
     if outs is None:
         outs = [torch.empty(s, dtype=torch.bfloat16, device=ha.device) if w else None for s, w in zip(shapes, want)]
     if workspace is None:
@@ -483,6 +555,8 @@ def vp_linear_jsd_bwd(ha, wa, hb, wb, beta, stats_a, stats_b, grad, want=(True, 
 def vp_logprobs_partial(x, targets, vocab_start: int = 0, parts=None):
     """Per-row records of logprobs over the shard x (columns vocab_start .. vocab_start + V)."""
     N, V, R, s_o, s_i = rows_of(x)
+    _row_args(x, N, targets=targets)
+    _parts_arg(parts, N, x)
     parts = partials(N, x.device) if parts is None else parts
     _check(_lib.lib().vp_logprobs_partial(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, vocab_start, _ptr(targets),
                                           _ptr(parts), _stream()), "vp_logprobs_partial")
@@ -492,6 +566,7 @@ def vp_logprobs_partial(x, targets, vocab_start: int = 0, parts=None):
 def vp_entropy_partial(x, parts=None):
     """Per-row records of entropy over the shard x."""
     N, V, R, s_o, s_i = rows_of(x)
+    _parts_arg(parts, N, x)
     parts = partials(N, x.device) if parts is None else parts
     _check(_lib.lib().vp_entropy_partial(_ptr(x), _dtype_code(x), N, V, R, s_o, s_i, _ptr(parts), _stream()),
            "vp_entropy_partial")
@@ -502,6 +577,7 @@ def vp_kl_partial(a, b, direction: int = KL_REVERSE, parts=None):
     """Per-row records of KL over the shard held by a and b."""
     _same_layout(a, b)
     N, V, R, s_o, s_i = rows_of(a)
+    _parts_arg(parts, N, a)
     parts = partials(N, a.device) if parts is None else parts
     _check(_lib.lib().vp_kl_partial(_ptr(a), _ptr(b), _dtype_code(a), N, V, R, s_o, s_i, int(direction),
                                     _ptr(parts), _stream()), "vp_kl_partial")
@@ -518,6 +594,7 @@ def _gathered(parts):
 def vp_logprobs_merge(parts, err_word=None, logp=None, stats=None):
     """Merges [K, N] shard records (shard-major) into (logp fp32 [N], stats) for the whole rows."""
     K, N = _gathered(parts)
+    _row_args(parts, N, stats=(stats,), err_word=err_word, outs=(logp,))
     logp = _f32(N, parts) if logp is None else logp
     stats = rowstats(N, parts.device) if stats is None else stats
     _check(_lib.lib().vp_logprobs_merge(_ptr(parts), K, N, _ptr(logp), _ptr(stats), _ptr(err_word), _stream()),
@@ -528,6 +605,7 @@ def vp_logprobs_merge(parts, err_word=None, logp=None, stats=None):
 def vp_entropy_merge(parts, H=None, stats=None):
     """Merges [K, N] shard records into (H fp32 [N], stats)."""
     K, N = _gathered(parts)
+    _row_args(parts, N, stats=(stats,), outs=(H,))
     H = _f32(N, parts) if H is None else H
     stats = rowstats(N, parts.device) if stats is None else stats
     _check(_lib.lib().vp_entropy_merge(_ptr(parts), K, N, _ptr(H), _ptr(stats), _stream()), "vp_entropy_merge")
@@ -537,6 +615,7 @@ def vp_entropy_merge(parts, H=None, stats=None):
 def vp_kl_merge(parts, direction: int = KL_REVERSE, kl=None, stats_a=None, stats_b=None):
     """Merges [K, N] shard records into (kl fp32 [N], stats of A, stats of B)."""
     K, N = _gathered(parts)
+    _row_args(parts, N, stats=(stats_a, stats_b), outs=(kl,))
     kl = _f32(N, parts) if kl is None else kl
     stats_a = rowstats(N, parts.device) if stats_a is None else stats_a
     stats_b = rowstats(N, parts.device) if stats_b is None else stats_b
@@ -564,6 +643,8 @@ def vp_get_row_split() -> int:
 def vp_linear_logp_partial(hidden, weight, targets, vocab_start: int = 0, parts=None, workspace=None):
     """Per-row logprobs records over the vocabulary shard held by weight (rows vocab_start .. + V of the head)."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_logp_partial")
+    _row_args(hidden, N, targets=targets)
+    _parts_arg(parts, N, hidden)
     parts = partials(N, hidden.device) if parts is None else parts
     if workspace is None:
         workspace = _workspace(_lib.lib().vp_linear_logp_workspace_size(N, V, D), hidden)
@@ -576,6 +657,7 @@ def vp_linear_logp_partial(hidden, weight, targets, vocab_start: int = 0, parts=
 def vp_linear_entropy_partial(hidden, weight, parts=None, workspace=None):
     """Per-row entropy records over the vocabulary shard held by weight."""
     N, V, D = _linear_model(hidden, weight, "vp_linear_entropy_partial")
+    _parts_arg(parts, N, hidden)
     parts = partials(N, hidden.device) if parts is None else parts
     if workspace is None:
         workspace = _workspace(_lib.lib().vp_linear_entropy_workspace_size(N, V, D), hidden)
@@ -587,6 +669,7 @@ def vp_linear_entropy_partial(hidden, weight, parts=None, workspace=None):
 def vp_linear_kl_partial(ha, wa, hb, wb, direction: int = KL_REVERSE, parts=None, workspace=None):
     """Per-row KL records of two models over the vocabulary shard held by wa and wb."""
     N, V, Da, Db = _two_models(ha, wa, hb, wb, "vp_linear_kl_partial")
+    _parts_arg(parts, N, ha)
     parts = partials(N, ha.device) if parts is None else parts
     if workspace is None:
         workspace = _workspace(_lib.lib().vp_linear_kl_workspace_size(N, V), ha)
