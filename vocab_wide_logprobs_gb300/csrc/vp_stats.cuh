@@ -97,6 +97,38 @@ __device__ __forceinline__ uint32_t word(const uint4 &u, int q) {
 // ---------------------------------------------------------------------------
 // One distribution, one lane
 // ---------------------------------------------------------------------------
+// max(a, b) that keeps a NaN operand (fmaxf would drop it).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// A centred value of each lane with a -inf made finite: t.hi at least -200, where
+// the exponential is already 0 (NaN kept), and t.lo at least -1 (below an ulp of
+// t.hi wherever the exponential is not 0; NaN only where t.hi is not finite).
+// Every term e, e t.hi and e t.lo is then finite, and exactly 0 for a -inf value,
+// so neither the exponential nor W needs a zero-weight test; where e is not 0 the
+// value is unchanged.
+__device__ __forceinline__ DF2 finite_centred2(const DF2 &t) {
+    return {make_float2(fmax_nan(t.hi.x, -200.f), fmax_nan(t.hi.y, -200.f)),
+            make_float2(fmaxf(t.lo.x, -1.f), fmaxf(t.lo.y, -1.f))};
+}
+
+// exp_split2 of a finite centred value (finite_centred2): the same operations
+// without the zero test, which only guards a_lo = NaN at an infinite t.hi.
+__device__ __forceinline__ float2 exp_split2_finite(const DF2 &t) {
+    constexpr float kL = 1.4426950408889634f, kLlo = 1.925963033500011e-08f, kLn2 = 0.6931471805599453f;
+    const float2 a_hi = __fmul2_rn(t.hi, f2(kL));
+    float2 na = __ffma2_rn(t.hi, f2(-kL), a_hi);                       // -(t_hi kL - a_hi)
+    na = __ffma2_rn(t.hi, f2(-kLlo), na);
+    na = __ffma2_rn(t.lo, f2(-kL), na);                                // -a_lo
+    float2 e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(a_hi.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(a_hi.y));
+    return __ffma2_rn(e, __fmul2_rn(na, f2(-kLn2)), e);                // e (1 + a_lo ln 2)
+}
+
 // How far a value may exceed a lane's centre before the centre moves to it. The
 // fp32 path's exponential takes an exact argument, so only overflow bounds it;
 // the bf16 path's takes the rounded (t log2 e), t 2^-24 relative error in e^t,
@@ -165,16 +197,14 @@ struct Lane1 {
                 float2 s2 = f2(K), sl2 = f2(0.f), w2 = f2(KW), wl2 = f2(0.f);
 #pragma unroll
                 for (int i = 0; i < n; i += 2) {
-                    const DF2 t = two_sum2(make_float2(v[i], v[i + 1]), nref);
-                    const float2 e = exp_split2(t);
+                    const DF2 t = finite_centred2(two_sum2(make_float2(v[i], v[i + 1]), nref));
+                    const float2 e = exp_split2_finite(t);
                     fast_acc2(s2, sl2, e);
-                    if (kW) {   // zero-weight terms add nothing (t may be -inf or NaN there)
-                        const float2 th = make_float2(e.x != 0.f ? t.hi.x : 0.f, e.y != 0.f ? t.hi.y : 0.f);
-                        const float2 tl = make_float2(e.x != 0.f ? t.lo.x : 0.f, e.y != 0.f ? t.lo.y : 0.f);
-                        const float2 ph = __fmul2_rn(e, th);
-                        const float2 pe = __ffma2_rn(e, th, make_float2(-ph.x, -ph.y));   // e th - ph, exact
+                    if (kW) {   // a zero-weight term is exactly 0 here (t is finite)
+                        const float2 ph = __fmul2_rn(e, t.hi);
+                        const float2 pe = __ffma2_rn(e, t.hi, make_float2(-ph.x, -ph.y));   // e t.hi - ph, exact
                         fast_acc2(w2, wl2, ph);
-                        wl2 = __fadd2_rn(wl2, __ffma2_rn(e, tl, pe));
+                        wl2 = __fadd2_rn(wl2, __ffma2_rn(e, t.lo, pe));
                     }
                 }
                 s0 = s2.x - K; s1 = s2.y - K; sl0 = sl2.x; sl1 = sl2.y;   // exact differences
