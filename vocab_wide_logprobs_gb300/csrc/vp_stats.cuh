@@ -181,7 +181,8 @@ struct Lane1 {
             // fp32 inputs: exact centred value (double-float), exponential with an exact
             // argument (exp_split), the chunk summed in fp32 (even and odd values apart)
             // and folded into double-floats; on pairs of values (f32x2) where n is even,
-            // each lane rounding exactly as the scalar form.
+            // whose centred values and exponentials round exactly as the scalar forms
+            // (the scalar form takes a row's unaligned head and tail).
             // S and W are summed compensated: each addition's rounding error, and each
             // product e t's, goes to a low part. In a peaked row one term carries most
             // of S and W, and a plain fp32 running sum would leave W/S with a few 2^-24
