@@ -12,11 +12,14 @@
 //   against a centre `ref` that all 32 lanes of a warp share: the max of the
 //   warp's first round of loads. Terms are summed in fp32 over one round of
 //   loads and folded into double-float (hi + lo) accumulators with an
-//   error-free two-sum, so the row sums keep ~2^-40 relative accuracy beyond
-//   the per-term exponentials. Because a warp shares one centre, the warp merge
-//   is a plain double-float sum; the 16 warp partials are re-centred on the
-//   largest centre in fp64 (S <- a S, W <- a (W - d S), a = e^{-d}), terms of
-//   zero weight skipped [P1], and the row is finished in fp64.
+//   error-free two-sum; on the fp32 path every addition inside the round is
+//   compensated as well (the offset fast two-sum below, FMA product errors), so
+//   the row sums keep ~2^-40 relative accuracy beyond the per-term
+//   exponentials. Because a warp shares one centre, the warp merge is a plain
+//   double-float sum; the warp partials are re-centred on the largest centre
+//   (S <- a S, W <- a (W - d S), a = e^{-d}; in fp64 on the fp32 path, and with
+//   fp32 factors and double-float sums on the bf16 path), terms of zero weight
+//   skipped [P1], and the row is finished in fp64.
 //   A lane moves its own centre only when a value exceeds it by more than
 //   kSpan (so e^{z - ref} cannot overflow); this happens only in rows whose
 //   values span more than kSpan natural-log units, and the warp then merges
