@@ -313,11 +313,13 @@ struct Lane1 {
     }
 };
 
-// Merged partials carry their sums in fp64 on the fp32 path and in fp32 on the
-// bf16 path: a warp partial's rounding (2^-24 of the warp's share) is far below
-// the hardware exponential's error floor on c (~2^-23, see Lane1::push_bf16),
-// and GB300's fp64 pipe is narrow, so the bf16 path keeps fp64 for the
-// one-thread row finish only.
+// Merged partials carry their sums in fp64 on the fp32 path and as fp32 values on
+// the bf16 path: one rounding of a partial (2^-24 of its share) is below the
+// hardware exponential's error floor on c (~2^-23, see Lane1::push_bf16), and
+// GB300's fp64 pipe is narrow, so the bf16 path keeps fp64 for the one-thread row
+// finish only. Sums over several partials are taken as double-floats and rounded
+// once (warp_sum_acc): repeated fp32 roundings would add up where one partial
+// carries the row.
 template <typename T>
 using AccT = typename std::conditional<Elem<T>::kPrecise, double, float>::type;
 
